@@ -1,0 +1,368 @@
+#!/usr/bin/env python
+"""Benchmark of the MSA hot path on GB300.
+
+One step = one pass of the whole hot path on the 128K training workload
+(B=1, N=131072, Hq=64, Hkv=8, d=d_idx=128, k=16, 128-token blocks): index
+selection (token scores + block max-pool + top-k), block-sparse GQA
+attention forward, KL alignment loss, and the fused backward.  Inputs are
+seeded synthetic bf16 tensors (block_sparse_gqa_causal_gb300.inputs) that are
+resident in HBM before the timed region; the per-step working set is far
+larger than L2, so no flush is needed between steps.
+
+value   = useful TFLOP/s of the whole step (closed-form FLOP counts of the
+          selected work, the same for every implementation), all ranks.
+e2e     = the same step through the same C-ABI calls with the inputs copied
+          from pinned host memory each step and the loss read back.
+roofline= the dominant kernel against MEASURED_PEAKS.json.
+cpu_baseline = the CPU oracle (test infrastructure) on a bounded row sample.
+
+`--impl reference` times the CPU oracle as the reference arm.  Multi-GPU
+(torchrun): every rank runs an independent replica (the path has no
+collective); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MSA fwd/bwd TFLOP/s and tokens/s at N=128K on 1 GB300; % of bf16 tensor peak"
+
+
+# ----------------------------------------------------------------- counts
+def tokens_per_row(w, pos):
+    """T_i: visible tokens of the selected blocks (independent of which
+    blocks are chosen: every non-local selected block is fully visible)."""
+    c0 = pos // w.block
+    return w.block * np.minimum(w.topk - 1, c0) + pos % w.block + 1
+
+
+def useful_flops(w, positions=None):
+    """Closed-form useful FLOPs per phase for one pass (all batch entries)."""
+    pos = np.arange(w.N, dtype=np.float64) if positions is None else np.asarray(positions, dtype=np.float64)
+    T = tokens_per_row(w, pos.astype(np.int64)).astype(np.float64)
+    B = w.B
+    f = {
+        "index": B * float(np.sum(2.0 * w.d_idx * (pos + 1) * w.Hkv)),
+        "fwd": B * float(np.sum(4.0 * w.d * T * w.Hq)),
+        "kl": B * float(np.sum(2.0 * w.d * T * w.Hq + 2.0 * w.d_idx * T * w.Hkv)),
+        "bwd": B * float(np.sum(10.0 * w.d * T * w.Hq + 6.0 * w.d_idx * T * w.Hkv)),
+    }
+    if not w.train:
+        f["kl"] = f["bwd"] = 0.0
+    return f
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------- dist
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity when world == 1)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------- oracle leg
+def oracle_sample(w, x, n_rows: int, seed: int = 0):
+    """Run the CPU oracle's whole hot path on n_rows sampled query rows of
+    the workload; returns (seconds, useful FLOPs of that sample, threads)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    rows = np.unique(np.concatenate([[w.N - 1], rng.choice(w.N, size=max(0, n_rows - 1), replace=False)]))
+    osh = oracle.Shape(B=w.B, Nq=w.N, Nk=w.N, Hq=w.Hq, Hkv=w.Hkv, d=w.d, d_idx=w.d_idx, topk=w.topk)
+    t0 = time.perf_counter()
+    bs = oracle.block_scores(osh, x["q_idx"], x["k_idx"], rows)
+    sel_rows = oracle.select(osh, bs, rows)
+    oracle.sparse_fwd(osh, x["q"], x["k"], x["v"], sel_rows, rows)
+    if w.train:
+        oracle.kl(osh, x["q"], x["k"], x["q_idx"], x["k_idx"], sel_rows, rows)
+        sel_full = np.full((w.B, w.Hkv, w.N, w.topk), -1, dtype=np.int32)
+        sel_full[0, :, rows, :] = sel_rows
+        oracle.bwd_rows(osh, x["q"], x["k"], x["v"], x["d_o"], x["q_idx"], x["k_idx"], sel_full, 1.0, rows)
+    dt = time.perf_counter() - t0
+    fl = useful_flops(w.scaled(B=1), positions=rows)
+    return dt, sum(fl.values()), oracle.num_threads(), len(rows)
+
+
+def calibrated_rows(w, x, target_s: float) -> tuple[int, float]:
+    dt, _, _, n = oracle_sample(w, x, 8, seed=99)
+    per = dt / n
+    return max(8, min(4096, int(target_s / max(per, 1e-6)))), per
+
+
+# ----------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="train_n128k")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+
+    from block_sparse_gqa_causal_gb300.workloads import BY_NAME
+    from block_sparse_gqa_causal_gb300.inputs import make_inputs
+    w = BY_NAME[args.workload]
+    world, rank, local = dist_env()
+
+    if args.impl == "reference":
+        return run_reference(args, w, world, rank)
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    from block_sparse_gqa_causal_gb300 import api
+
+    x = make_inputs(w, with_grad=w.train)
+    names = ["q", "k", "v", "q_idx", "k_idx"] + (["d_o"] if w.train else [])
+    host = {n: torch.from_numpy(x[n].view(np.int16)).view(torch.bfloat16) for n in names}
+    d = {n: host[n].to(dev) for n in names}
+    sh = api.Shape(B=w.B, Nq=w.N, Nk=w.N, Hq=w.Hq, Hkv=w.Hkv, d=w.d, d_idx=w.d_idx, topk=w.topk)
+    sel = torch.empty((w.B, w.Hkv, w.N, w.topk), dtype=torch.int32, device=dev)
+    o = torch.empty_like(d["q"])
+    lse = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device=dev)
+    lse_idx = torch.empty((w.B, w.Hkv, w.N), dtype=torch.float32, device=dev)
+    kl_rows = torch.empty((w.B, w.Hkv, w.N), dtype=torch.float32, device=dev)
+    kl_loss = torch.empty((), dtype=torch.float32, device=dev)
+    ws = {op: api.new_workspace(sh, op, dev) for op in range(4 if w.train else 2)}
+    grads = tuple(torch.empty_like(d[n]) for n in ("q", "k", "v", "q_idx", "k_idx")) if w.train else None
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev: ev[0].record(stream)
+        api.index_select(sh, d["q_idx"], d["k_idx"], sel_idx=sel, workspace=ws[0])
+        if ev: ev[1].record(stream)
+        api.sparse_attn_fwd(sh, d["q"], d["k"], d["v"], sel, o=o, lse=lse, workspace=ws[1])
+        if ev: ev[2].record(stream)
+        if w.train:
+            api.kl_fwd(sh, d["q"], d["k"], d["q_idx"], d["k_idx"], sel, lse, 1.0, lse_idx=lse_idx,
+                       kl_rows=kl_rows, kl_loss=kl_loss, workspace=ws[2])
+            if ev: ev[3].record(stream)
+            api.fused_bwd(sh, d["q"], d["k"], d["v"], o, d["d_o"], lse, d["q_idx"], d["k_idx"], sel, lse_idx, 1.0,
+                          grads=grads, workspace=ws[3])
+            if ev: ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    for op in ws:
+        api.check_device_status(ws[op])
+
+    # ---- device-resident timed region
+    nph = 5 if w.train else 3
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nph)] for _ in range(args.steps)]
+    clocks = ClockSampler(dev.index if world == 1 else local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    launches0 = api.launch_count()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(args.steps):
+        step(evs[s])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    launches = api.launch_count() - launches0
+    barrier(world)
+    clk = clocks.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
+    phase_names = ["index_select", "sparse_attn_fwd", "kl_fwd", "fused_bwd"][: nph - 1]
+    phase_ms = {n: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j, n in enumerate(phase_names)}
+
+    fl = useful_flops(w)
+    step_flops = sum(fl.values())
+    ms_per_step = elapsed_ms / args.steps
+    value = world * step_flops / (ms_per_step * 1e-3) / 1e12
+    tokens_s = world * w.B * w.N / (ms_per_step * 1e-3)
+
+    # ---- end to end through the same calls, inputs from pinned host memory
+    e2e = None
+    if not args.no_e2e:
+        pinned = {n: host[n].pin_memory() for n in names}
+        loss_host = torch.empty((), dtype=torch.float32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+
+        def e2e_step():
+            for n in names:
+                d[n].copy_(pinned[n], non_blocking=True)
+            step()
+            loss_host.copy_(kl_loss if w.train else lse[0, 0, 0], non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(a.elapsed_time(b), world, dev) / args.steps
+        e2e = {"value": round(world * step_flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+               "ms_per_step": round(e2e_ms, 3), "tokens_per_s": round(world * w.B * w.N / (e2e_ms * 1e-3), 1),
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": 4}
+
+    # ---- roofline of the dominant kernel (the phase that takes longest)
+    peaks = load_peaks()
+    phase_flops = {"index_select": fl["index"], "sparse_attn_fwd": fl["fwd"], "kl_fwd": fl["kl"], "fused_bwd": fl["bwd"]}
+    kernel_of = {"index_select": "index_scores_kernel (+ block_topk_kernel)", "sparse_attn_fwd": "sparse_attn_fwd_kernel",
+                 "kl_fwd": "kl_fwd_kernel (+ kl_reduce_kernel)", "fused_bwd": "fused_bwd_kernel (+ prep/finalize kernels)"}
+    dom = max(phase_ms, key=phase_ms.get)
+    ach = phase_flops[dom] / (phase_ms[dom] * 1e-3) / 1e12
+    roofline = {"kernel": kernel_of[dom], "bound": "tensor", "achieved": round(ach, 2),
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4),
+                "frac_of_sustained": round(ach / peaks["bf16_tflops_sustained"], 4),
+                "peak_source": peaks["source"] + " burst bf16", "traffic": None}
+
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        n_rows, _ = calibrated_rows(w, x, args.cpu_seconds)
+        dt, cfl, thr, n = oracle_sample(w, x, n_rows)
+        cpu = {"value": round(cfl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+               "sample": f"{n} query rows of {w.name} (index scores, selection, forward, KL, query-side backward "
+                         f"of each), {dt:.1f} s; FLOPs counted with the same closed form"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "N": w.N, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
+                       "d_idx": w.d_idx, "block": w.block, "topk": w.topk, "seed": w.seed,
+                       "global_batch": w.B * world, "seq_len": w.N, "parallelism": f"replicas x{world}",
+                       "l2": "no flush: per-step working set (>5 GB) exceeds the 129 MB L2"},
+            "tokens_per_s": round(tokens_s, 1),
+            "phases_ms": {k: round(v, 3) for k, v in phase_ms.items()},
+            "phases_tflops": {k: round(phase_flops[k] / (phase_ms[k] * 1e-3) / 1e12, 2) for k in phase_ms},
+            "useful_tflop_per_step": round(step_flops / 1e12, 4),
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
+            "clocks": clk, "impl": "ours",
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args, w, world, rank):
+    """Reference arm: the CPU oracle timed on the host cores."""
+    if rank != 0:
+        return
+    from block_sparse_gqa_causal_gb300.inputs import make_inputs
+    x = make_inputs(w, with_grad=w.train)
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    n_rows, _ = calibrated_rows(w, x, min(20.0, budget))
+    for s in range(args.warmup):
+        oracle_sample(w, x, n_rows, seed=1000 + s)
+    times, flops = [], []
+    thr = 1
+    for s in range(args.steps):
+        dt, fl, thr, n = oracle_sample(w, x, n_rows, seed=s)
+        times.append(dt)
+        flops.append(fl)
+    value = sum(flops) / sum(times) / 1e12
+    full = sum(useful_flops(w).values())
+    ms_per_step = full / (value * 1e12) * 1e3
+    line = {"metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "N": w.N, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
+                       "d_idx": w.d_idx, "block": w.block, "topk": w.topk, "seed": w.seed},
+            "impl": "reference",
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+                             "sample": f"{n_rows} query rows per step (whole hot path of each row; ms_per_step "
+                                       f"extrapolated to all rows by the closed-form FLOP count)"},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,241 @@
+"""Thin Python binding of libmsa.so (C-ABI in include/msa.h).
+
+Argument marshalling only: it checks dtypes and layouts, allocates outputs
+and workspaces with torch (device memory), and passes raw pointers and the
+current CUDA stream to the library.  Every step of the computation runs in
+the library's kernels; there is no fallback.  If libmsa.so has not been
+built, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmsa.so")
+
+OP_INDEX_SELECT, OP_SPARSE_ATTN_FWD, OP_KL_FWD, OP_FUSED_BWD = 0, 1, 2, 3
+STATUS = {0: "MSA_OK", 1: "MSA_ERR_INVALID_ARGUMENT", 2: "MSA_ERR_UNSUPPORTED", 3: "MSA_ERR_WORKSPACE",
+          4: "MSA_ERR_CUDA", 5: "MSA_ERR_TIMEOUT", 6: "MSA_ERR_DEVICE"}
+EXPORTS = ("msa_workspace_size", "msa_index_select", "msa_sparse_attn_fwd", "msa_kl_fwd", "msa_fused_bwd",
+           "msa_last_error", "msa_check_device_status", "msa_version", "msa_launch_count")
+
+
+class MsaError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{STATUS.get(code, code)}: {msg}")
+        self.code = code
+
+
+class _CShape(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("B", "Nq", "Nk", "q_offset", "Hq", "Hkv", "d", "d_idx", "block", "topk")] + [
+        ("kv_rows", ctypes.c_longlong), ("scale", ctypes.c_float), ("scale_idx", ctypes.c_float)]
+
+
+@dataclass
+class Shape:
+    """msa_shape: see include/msa.h for the meaning of each field."""
+    B: int
+    Nq: int
+    Nk: int
+    Hq: int
+    Hkv: int
+    d: int
+    d_idx: int
+    topk: int
+    block: int = 128
+    q_offset: int = 0
+    kv_rows: int = 0
+    scale: float = 0.0
+    scale_idx: float = 0.0
+
+    @property
+    def nb(self) -> int:
+        return (self.Nk + self.block - 1) // self.block
+
+    @property
+    def G(self) -> int:
+        return self.Hq // self.Hkv
+
+    @property
+    def rows_kv(self) -> int:
+        return self.kv_rows or self.Nk
+
+    def c(self) -> _CShape:
+        return _CShape(self.B, self.Nq, self.Nk, self.q_offset, self.Hq, self.Hkv, self.d, self.d_idx, self.block,
+                       self.topk, self.kv_rows, self.scale, self.scale_idx)
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmsa.so (fails loudly if it is missing: there is no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                                   "`python -c 'import __graft_entry__ as g; g.build()'`")
+            L = ctypes.CDLL(LIB_PATH)
+            P, S = ctypes.c_void_p, ctypes.POINTER(_CShape)
+            sz, f = ctypes.c_size_t, ctypes.c_float
+            L.msa_workspace_size.argtypes = [S, ctypes.c_int]
+            L.msa_workspace_size.restype = sz
+            L.msa_index_select.argtypes = [S, P, P, P, P, P, sz, P]
+            L.msa_sparse_attn_fwd.argtypes = [S, P, P, P, P, P, P, P, sz, P]
+            L.msa_kl_fwd.argtypes = [S, P, P, P, P, P, P, f, P, P, P, P, sz, P]
+            L.msa_fused_bwd.argtypes = [S, P, P, P, P, P, P, P, P, P, P, f, P, P, P, P, P, P, sz, P]
+            L.msa_check_device_status.argtypes = [P, P]
+            for fn in ("msa_index_select", "msa_sparse_attn_fwd", "msa_kl_fwd", "msa_fused_bwd",
+                       "msa_check_device_status"):
+                getattr(L, fn).restype = ctypes.c_int
+            L.msa_last_error.restype = ctypes.c_char_p
+            L.msa_version.restype = ctypes.c_char_p
+            L.msa_launch_count.restype = ctypes.c_ulonglong
+            _lib = L
+        return _lib
+
+
+def _check(code: int) -> None:
+    if code != 0:
+        raise MsaError(code, lib().msa_last_error().decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, shape, dtype) -> None:
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous() or not t.is_cuda:
+        raise ValueError(f"{name}: need a contiguous CUDA {dtype} tensor of shape {tuple(shape)}, "
+                         f"got {t.dtype} {tuple(t.shape)} contiguous={t.is_contiguous()} cuda={t.is_cuda}")
+
+
+def workspace_size(shape: Shape, op: int) -> int:
+    n = lib().msa_workspace_size(ctypes.byref(shape.c()), op)
+    if n == 0:
+        _check(1)
+    return int(n)
+
+
+def new_workspace(shape: Shape, op: int, device=None) -> torch.Tensor:
+    """A workspace with its 256-byte status word zeroed."""
+    n = workspace_size(shape, op)
+    ws = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+    ws[:256].zero_()
+    return ws
+
+
+def _ws(ws, shape, op, device):
+    if ws is None:
+        ws = new_workspace(shape, op, device)
+    return ws
+
+
+def index_select(shape: Shape, q_idx, k_idx, *, sel_idx=None, block_scores=None, return_scores=False,
+                 workspace=None, stream=None):
+    """msa_index_select.  Returns sel_idx [B,Hkv,Nq,topk] int32 (and the block
+    scores [B,Nq,Hkv,nb] fp32 when asked for)."""
+    s = shape
+    _need(q_idx, "q_idx", (s.B, s.Nq, s.Hkv, s.d_idx), torch.bfloat16)
+    _need(k_idx, "k_idx", (s.B, s.rows_kv, s.d_idx), torch.bfloat16)
+    dev = q_idx.device
+    if sel_idx is None:
+        sel_idx = torch.empty((s.B, s.Hkv, s.Nq, s.topk), dtype=torch.int32, device=dev)
+    if return_scores and block_scores is None:
+        block_scores = torch.empty((s.B, s.Nq, s.Hkv, s.nb), dtype=torch.float32, device=dev)
+    ws = _ws(workspace, s, OP_INDEX_SELECT, dev)
+    _check(lib().msa_index_select(ctypes.byref(s.c()), _ptr(q_idx), _ptr(k_idx), _ptr(sel_idx), _ptr(block_scores),
+                                  _ptr(ws), ws.numel(), _stream(stream)))
+    return (sel_idx, block_scores) if return_scores else sel_idx
+
+
+def sparse_attn_fwd(shape: Shape, q, k, v, sel_idx, *, o=None, lse=None, workspace=None, stream=None):
+    """msa_sparse_attn_fwd.  Returns (o [B,Nq,Hq,d] bf16, lse [B,Hq,Nq] fp32)."""
+    s = shape
+    _need(q, "q", (s.B, s.Nq, s.Hq, s.d), torch.bfloat16)
+    _need(k, "k", (s.B, s.rows_kv, s.Hkv, s.d), torch.bfloat16)
+    _need(v, "v", (s.B, s.rows_kv, s.Hkv, s.d), torch.bfloat16)
+    _need(sel_idx, "sel_idx", (s.B, s.Hkv, s.Nq, s.topk), torch.int32)
+    dev = q.device
+    o = torch.empty((s.B, s.Nq, s.Hq, s.d), dtype=torch.bfloat16, device=dev) if o is None else o
+    lse = torch.empty((s.B, s.Hq, s.Nq), dtype=torch.float32, device=dev) if lse is None else lse
+    ws = _ws(workspace, s, OP_SPARSE_ATTN_FWD, dev)
+    _check(lib().msa_sparse_attn_fwd(ctypes.byref(s.c()), _ptr(q), _ptr(k), _ptr(v), _ptr(sel_idx), _ptr(o),
+                                     _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)))
+    return o, lse
+
+
+def kl_fwd(shape: Shape, q, k, q_idx, k_idx, sel_idx, lse, kl_coef: float = 1.0, *, lse_idx=None, kl_rows=None,
+           kl_loss=None, want_rows=True, workspace=None, stream=None):
+    """msa_kl_fwd.  Returns (kl_loss scalar tensor, lse_idx [B,Hkv,Nq], kl_rows [B,Hkv,Nq] or None)."""
+    s = shape
+    _need(q, "q", (s.B, s.Nq, s.Hq, s.d), torch.bfloat16)
+    _need(k, "k", (s.B, s.rows_kv, s.Hkv, s.d), torch.bfloat16)
+    _need(q_idx, "q_idx", (s.B, s.Nq, s.Hkv, s.d_idx), torch.bfloat16)
+    _need(k_idx, "k_idx", (s.B, s.rows_kv, s.d_idx), torch.bfloat16)
+    _need(sel_idx, "sel_idx", (s.B, s.Hkv, s.Nq, s.topk), torch.int32)
+    _need(lse, "lse", (s.B, s.Hq, s.Nq), torch.float32)
+    dev = q.device
+    lse_idx = torch.empty((s.B, s.Hkv, s.Nq), dtype=torch.float32, device=dev) if lse_idx is None else lse_idx
+    if want_rows and kl_rows is None:
+        kl_rows = torch.empty((s.B, s.Hkv, s.Nq), dtype=torch.float32, device=dev)
+    kl_loss = torch.empty((), dtype=torch.float32, device=dev) if kl_loss is None else kl_loss
+    ws = _ws(workspace, s, OP_KL_FWD, dev)
+    _check(lib().msa_kl_fwd(ctypes.byref(s.c()), _ptr(q), _ptr(k), _ptr(q_idx), _ptr(k_idx), _ptr(sel_idx),
+                            _ptr(lse), ctypes.c_float(kl_coef), _ptr(lse_idx), _ptr(kl_rows), _ptr(kl_loss),
+                            _ptr(ws), ws.numel(), _stream(stream)))
+    return kl_loss, lse_idx, kl_rows
+
+
+def fused_bwd(shape: Shape, q, k, v, o, d_o, lse, q_idx, k_idx, sel_idx, lse_idx, kl_coef: float = 1.0, *,
+              grads=None, workspace=None, stream=None):
+    """msa_fused_bwd.  Returns (dq, dk, dv, dq_idx, dk_idx) bf16."""
+    s = shape
+    for t, n, shp in ((q, "q", (s.B, s.Nq, s.Hq, s.d)), (o, "o", (s.B, s.Nq, s.Hq, s.d)),
+                      (d_o, "d_o", (s.B, s.Nq, s.Hq, s.d)), (k, "k", (s.B, s.Nk, s.Hkv, s.d)),
+                      (v, "v", (s.B, s.Nk, s.Hkv, s.d)), (q_idx, "q_idx", (s.B, s.Nq, s.Hkv, s.d_idx)),
+                      (k_idx, "k_idx", (s.B, s.Nk, s.d_idx))):
+        _need(t, n, shp, torch.bfloat16)
+    _need(lse, "lse", (s.B, s.Hq, s.Nq), torch.float32)
+    _need(lse_idx, "lse_idx", (s.B, s.Hkv, s.Nq), torch.float32)
+    _need(sel_idx, "sel_idx", (s.B, s.Hkv, s.Nq, s.topk), torch.int32)
+    if grads is None:
+        grads = tuple(torch.empty_like(t) for t in (q, k, v, q_idx, k_idx))
+    dq, dk, dv, dqi, dki = grads
+    ws = _ws(workspace, s, OP_FUSED_BWD, q.device)
+    _check(lib().msa_fused_bwd(ctypes.byref(s.c()), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(d_o), _ptr(lse),
+                               _ptr(q_idx), _ptr(k_idx), _ptr(sel_idx), _ptr(lse_idx), ctypes.c_float(kl_coef),
+                               _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dqi), _ptr(dki), _ptr(ws), ws.numel(),
+                               _stream(stream)))
+    return dq, dk, dv, dqi, dki
+
+
+def check_device_status(workspace, stream=None) -> None:
+    """msa_check_device_status: raises MsaError on a recorded device-side error."""
+    _check(lib().msa_check_device_status(_ptr(workspace), _stream(stream)))
+
+
+def launch_count() -> int:
+    """Kernels launched through the library by this process so far."""
+    return int(lib().msa_launch_count())
+
+
+def version() -> str:
+    return lib().msa_version().decode()
+
+
+def default_scale(d: int) -> float:
+    return 1.0 / math.sqrt(d)

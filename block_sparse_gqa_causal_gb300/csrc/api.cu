@@ -1,0 +1,285 @@
+// api.cu -- the C-ABI of libmsa.so (declared in include/msa.h): argument
+// validation, workspace carve-up and kernel launches on the caller's stream.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <atomic>
+#include <string>
+
+#include "msa.h"
+#include "msa_internal.h"
+
+using namespace msa;
+
+namespace {
+
+thread_local std::string g_err;
+std::atomic<unsigned long long> g_launches{0};
+
+msa_status fail(msa_status st, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return st;
+}
+
+msa_status cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(MSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+bool aligned16(const void *ptr) { return ((uintptr_t)ptr & 15u) == 0; }
+
+int sm_count()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+    return n;
+}
+
+// Validates the shape and fills the internal problem description.
+msa_status make_problem(const msa_shape *s, Problem &p)
+{
+    if (!s) return fail(MSA_ERR_INVALID_ARGUMENT, "shape is NULL");
+    if (s->B < 1 || s->Nq < 1 || s->Nk < 1 || s->Hq < 1 || s->Hkv < 1 || s->d < 1 || s->d_idx < 1 ||
+        s->block < 1 || s->topk < 1 || s->q_offset < 0)
+        return fail(MSA_ERR_INVALID_ARGUMENT, "shape has a non-positive size (B=%d Nq=%d Nk=%d Hq=%d Hkv=%d d=%d "
+                    "d_idx=%d block=%d topk=%d q_offset=%d)", s->B, s->Nq, s->Nk, s->Hq, s->Hkv, s->d, s->d_idx,
+                    s->block, s->topk, s->q_offset);
+    if ((long long)s->q_offset + s->Nq > s->Nk)
+        return fail(MSA_ERR_INVALID_ARGUMENT, "q_offset + Nq (%lld) exceeds Nk (%d): a visible key is missing",
+                    (long long)s->q_offset + s->Nq, s->Nk);
+    if (s->Hq % s->Hkv != 0) return fail(MSA_ERR_INVALID_ARGUMENT, "Hq (%d) is not a multiple of Hkv (%d)", s->Hq, s->Hkv);
+    const long long kv_rows = s->kv_rows ? s->kv_rows : s->Nk;
+    if (kv_rows < s->Nk) return fail(MSA_ERR_INVALID_ARGUMENT, "kv_rows (%lld) < Nk (%d)", kv_rows, s->Nk);
+    if (s->block != 128) return fail(MSA_ERR_UNSUPPORTED, "block must be 128 (got %d)", s->block);
+    if (s->d != 64 && s->d != 128) return fail(MSA_ERR_UNSUPPORTED, "d must be 64 or 128 (got %d)", s->d);
+    if (s->d_idx != 64 && s->d_idx != 128) return fail(MSA_ERR_UNSUPPORTED, "d_idx must be 64 or 128 (got %d)", s->d_idx);
+    if (s->topk > 32) return fail(MSA_ERR_UNSUPPORTED, "topk must be <= 32 (got %d)", s->topk);
+    const int G = s->Hq / s->Hkv;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return fail(MSA_ERR_UNSUPPORTED, "Hq/Hkv must be 1, 2, 4 or 8 (got %d)", G);
+    if (!(s->scale >= 0.f) || !(s->scale_idx >= 0.f) || isinf(s->scale) || isinf(s->scale_idx))
+        return fail(MSA_ERR_INVALID_ARGUMENT, "scales must be finite and >= 0 (0 selects the default)");
+    if ((long long)s->B * s->Nq * s->Hq >= (1LL << 31) / 128 || kv_rows * s->B >= (1LL << 31))
+        return fail(MSA_ERR_UNSUPPORTED, "problem too large for 32-bit row indices");
+    p.B = s->B; p.Nq = s->Nq; p.Nk = s->Nk; p.q_offset = s->q_offset; p.Hq = s->Hq; p.Hkv = s->Hkv;
+    p.G = G; p.d = s->d; p.d_idx = s->d_idx; p.block = s->block; p.topk = s->topk;
+    p.nb = (s->Nk + s->block - 1) / s->block;
+    p.kv_rows = kv_rows;
+    p.scale = s->scale > 0.f ? s->scale : 1.0f / sqrtf((float)s->d);
+    p.scale_idx = s->scale_idx > 0.f ? s->scale_idx : 1.0f / sqrtf((float)s->d_idx);
+    p.num_sms = sm_count();
+    return MSA_OK;
+}
+
+struct Carve {
+    char *base;
+    size_t off = kStatusBytes;
+    template <class T>
+    T *take(size_t count)
+    {
+        T *ptr = reinterpret_cast<T *>(base + off);
+        off = align256(off + count * sizeof(T));
+        return ptr;
+    }
+};
+
+size_t bs_bytes(const Problem &p) { return align256((size_t)p.B * p.Nq * p.Hkv * p.nb * sizeof(float)); }
+size_t klrows_bytes(const Problem &p) { return align256((size_t)p.B * p.Hkv * p.Nq * sizeof(float)); }
+
+size_t bwd_bytes(const Problem &p)
+{
+    const size_t nbk = (size_t)p.B * p.Hkv * p.nb;
+    return align256((size_t)p.B * p.Hq * p.Nq * 4) + align256((size_t)p.B * p.Nq * p.Hq * p.d * 4) +
+           align256((size_t)p.B * p.Nq * p.Hkv * p.d_idx * 4) + align256((size_t)p.B * p.Nk * p.d_idx * 4) +
+           3 * align256((nbk + 1) * 4) + align256((size_t)p.B * p.Hkv * p.Nq * p.topk * 4);
+}
+
+#define REQUIRE_PTR(ptr, name)                                                                         \
+    do {                                                                                               \
+        if (!(ptr)) return fail(MSA_ERR_INVALID_ARGUMENT, "%s is NULL", name);                         \
+        if (!aligned16(ptr)) return fail(MSA_ERR_INVALID_ARGUMENT, "%s is not 16-byte aligned", name); \
+    } while (0)
+
+msa_status check_ws(void *ws, size_t ws_bytes, size_t need)
+{
+    if (!ws) return fail(MSA_ERR_INVALID_ARGUMENT, "workspace is NULL");
+    if (((uintptr_t)ws & 255u) != 0) return fail(MSA_ERR_INVALID_ARGUMENT, "workspace is not 256-byte aligned");
+    if (ws_bytes < need) return fail(MSA_ERR_WORKSPACE, "workspace too small: %zu < %zu bytes", ws_bytes, need);
+    return MSA_OK;
+}
+
+}  // namespace
+
+namespace msa {
+void note_launch(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+}  // namespace msa
+
+extern "C" {
+
+const char *msa_version(void) { return "msa-gb300 0.1 (sm_103a)"; }
+
+const char *msa_last_error(void) { return g_err.c_str(); }
+
+unsigned long long msa_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+size_t msa_workspace_size(const msa_shape *shape, int op)
+{
+    Problem p;
+    if (make_problem(shape, p) != MSA_OK) return 0;
+    switch (op) {
+    case MSA_OP_INDEX_SELECT: return kStatusBytes + bs_bytes(p);
+    case MSA_OP_SPARSE_ATTN_FWD: return kStatusBytes;
+    case MSA_OP_KL_FWD: return kStatusBytes + klrows_bytes(p);
+    case MSA_OP_FUSED_BWD: return kStatusBytes + bwd_bytes(p);
+    default: fail(MSA_ERR_INVALID_ARGUMENT, "unknown op %d", op); return 0;
+    }
+}
+
+msa_status msa_index_select(const msa_shape *shape, const void *q_idx, const void *k_idx, int32_t *sel_idx,
+                            float *block_scores, void *workspace, size_t workspace_bytes, void *stream)
+{
+    Problem p;
+    msa_status st = make_problem(shape, p);
+    if (st != MSA_OK) return st;
+    REQUIRE_PTR(q_idx, "q_idx");
+    REQUIRE_PTR(k_idx, "k_idx");
+    if (!sel_idx) return fail(MSA_ERR_INVALID_ARGUMENT, "sel_idx is NULL");
+    if (block_scores && !aligned16(block_scores)) return fail(MSA_ERR_INVALID_ARGUMENT, "block_scores is not 16-byte aligned");
+    st = check_ws(workspace, workspace_bytes, kStatusBytes + (block_scores ? 0 : bs_bytes(p)));
+    if (st != MSA_OK) return st;
+    Carve cv{static_cast<char *>(workspace)};
+    float *bs = block_scores ? block_scores : cv.take<float>((size_t)p.B * p.Nq * p.Hkv * p.nb);
+    DeviceStatus *ds = static_cast<DeviceStatus *>(workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_index_scores(p, static_cast<const bf16 *>(q_idx), static_cast<const bf16 *>(k_idx), bs, ds, s);
+    if (e != cudaSuccess) return cuda_fail(e, "index_scores launch");
+    e = launch_block_topk(p, bs, sel_idx, ds, s);
+    if (e != cudaSuccess) return cuda_fail(e, "block_topk launch");
+    return MSA_OK;
+}
+
+msa_status msa_sparse_attn_fwd(const msa_shape *shape, const void *q, const void *k, const void *v,
+                               const int32_t *sel_idx, void *o, float *lse, void *workspace,
+                               size_t workspace_bytes, void *stream)
+{
+    Problem p;
+    msa_status st = make_problem(shape, p);
+    if (st != MSA_OK) return st;
+    REQUIRE_PTR(q, "q");
+    REQUIRE_PTR(k, "k");
+    REQUIRE_PTR(v, "v");
+    REQUIRE_PTR(o, "o");
+    if (!sel_idx) return fail(MSA_ERR_INVALID_ARGUMENT, "sel_idx is NULL");
+    if (!lse) return fail(MSA_ERR_INVALID_ARGUMENT, "lse is NULL");
+    st = check_ws(workspace, workspace_bytes, kStatusBytes);
+    if (st != MSA_OK) return st;
+    cudaError_t e = launch_sparse_attn_fwd(p, static_cast<const bf16 *>(q), static_cast<const bf16 *>(k),
+                                           static_cast<const bf16 *>(v), sel_idx, static_cast<bf16 *>(o), lse,
+                                           static_cast<DeviceStatus *>(workspace), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "sparse_attn_fwd launch");
+    return MSA_OK;
+}
+
+msa_status msa_kl_fwd(const msa_shape *shape, const void *q, const void *k, const void *q_idx, const void *k_idx,
+                      const int32_t *sel_idx, const float *lse, float kl_coef, float *lse_idx, float *kl_rows,
+                      float *kl_loss, void *workspace, size_t workspace_bytes, void *stream)
+{
+    Problem p;
+    msa_status st = make_problem(shape, p);
+    if (st != MSA_OK) return st;
+    REQUIRE_PTR(q, "q");
+    REQUIRE_PTR(k, "k");
+    REQUIRE_PTR(q_idx, "q_idx");
+    REQUIRE_PTR(k_idx, "k_idx");
+    if (!sel_idx || !lse || !lse_idx || !kl_loss)
+        return fail(MSA_ERR_INVALID_ARGUMENT, "sel_idx, lse, lse_idx and kl_loss must be non-NULL");
+    if (!isfinite(kl_coef)) return fail(MSA_ERR_INVALID_ARGUMENT, "kl_coef must be finite");
+    st = check_ws(workspace, workspace_bytes, kStatusBytes + (kl_rows ? 0 : klrows_bytes(p)));
+    if (st != MSA_OK) return st;
+    Carve cv{static_cast<char *>(workspace)};
+    float *rows = kl_rows ? kl_rows : cv.take<float>((size_t)p.B * p.Hkv * p.Nq);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_kl_fwd(p, static_cast<const bf16 *>(q), static_cast<const bf16 *>(k),
+                                  static_cast<const bf16 *>(q_idx), static_cast<const bf16 *>(k_idx), sel_idx, lse,
+                                  lse_idx, rows, static_cast<DeviceStatus *>(workspace), s);
+    if (e != cudaSuccess) return cuda_fail(e, "kl_fwd launch");
+    e = launch_kl_reduce(p, rows, kl_coef, kl_loss, s);
+    if (e != cudaSuccess) return cuda_fail(e, "kl_reduce launch");
+    return MSA_OK;
+}
+
+msa_status msa_fused_bwd(const msa_shape *shape, const void *q, const void *k, const void *v, const void *o,
+                         const void *d_o, const float *lse, const void *q_idx, const void *k_idx,
+                         const int32_t *sel_idx, const float *lse_idx, float kl_coef, void *dq, void *dk, void *dv,
+                         void *dq_idx, void *dk_idx, void *workspace, size_t workspace_bytes, void *stream)
+{
+    Problem p;
+    msa_status st = make_problem(shape, p);
+    if (st != MSA_OK) return st;
+    if (p.q_offset != 0 || p.Nq != p.Nk || p.kv_rows != p.Nk)
+        return fail(MSA_ERR_UNSUPPORTED, "fused_bwd needs q_offset == 0, Nq == Nk and kv_rows == Nk");
+    REQUIRE_PTR(q, "q");
+    REQUIRE_PTR(k, "k");
+    REQUIRE_PTR(v, "v");
+    REQUIRE_PTR(o, "o");
+    REQUIRE_PTR(d_o, "d_o");
+    REQUIRE_PTR(q_idx, "q_idx");
+    REQUIRE_PTR(k_idx, "k_idx");
+    REQUIRE_PTR(dq, "dq");
+    REQUIRE_PTR(dk, "dk");
+    REQUIRE_PTR(dv, "dv");
+    REQUIRE_PTR(dq_idx, "dq_idx");
+    REQUIRE_PTR(dk_idx, "dk_idx");
+    if (!sel_idx || !lse || !lse_idx) return fail(MSA_ERR_INVALID_ARGUMENT, "sel_idx, lse and lse_idx must be non-NULL");
+    if (!isfinite(kl_coef)) return fail(MSA_ERR_INVALID_ARGUMENT, "kl_coef must be finite");
+    st = check_ws(workspace, workspace_bytes, kStatusBytes + bwd_bytes(p));
+    if (st != MSA_OK) return st;
+    Carve cv{static_cast<char *>(workspace)};
+    const size_t nbk = (size_t)p.B * p.Hkv * p.nb;
+    BwdWork w;
+    w.D = cv.take<float>((size_t)p.B * p.Hq * p.Nq);
+    w.dq_acc = cv.take<float>((size_t)p.B * p.Nq * p.Hq * p.d);
+    w.dqi_acc = cv.take<float>((size_t)p.B * p.Nq * p.Hkv * p.d_idx);
+    w.dki_acc = cv.take<float>((size_t)p.B * p.Nk * p.d_idx);
+    w.bucket_cnt = cv.take<int32_t>(nbk + 1);
+    w.bucket_off = cv.take<int32_t>(nbk + 1);
+    w.bucket_cur = cv.take<int32_t>(nbk + 1);
+    w.bucket_q = cv.take<int32_t>((size_t)p.B * p.Hkv * p.Nq * p.topk);
+    cudaError_t e = launch_fused_bwd(p, static_cast<const bf16 *>(q), static_cast<const bf16 *>(k),
+                                     static_cast<const bf16 *>(v), static_cast<const bf16 *>(o),
+                                     static_cast<const bf16 *>(d_o), lse, static_cast<const bf16 *>(q_idx),
+                                     static_cast<const bf16 *>(k_idx), sel_idx, lse_idx, kl_coef,
+                                     static_cast<bf16 *>(dq), static_cast<bf16 *>(dk), static_cast<bf16 *>(dv),
+                                     static_cast<bf16 *>(dq_idx), static_cast<bf16 *>(dk_idx), w,
+                                     static_cast<DeviceStatus *>(workspace), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "fused_bwd launch");
+    return MSA_OK;
+}
+
+msa_status msa_check_device_status(void *workspace, void *stream)
+{
+    if (!workspace) return fail(MSA_ERR_INVALID_ARGUMENT, "workspace is NULL");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    DeviceStatus h{};
+    cudaError_t e = cudaMemcpyAsync(&h, workspace, sizeof h, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+    if (h.code == 0) return MSA_OK;
+    e = cudaMemsetAsync(workspace, 0, sizeof h, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the device status word");
+    if (h.code == kDevTimeout)
+        return fail(MSA_ERR_TIMEOUT, "a device-side wait ran out (site %d, info %d)", h.where, h.info);
+    return fail(MSA_ERR_DEVICE, "device-side check failed (code %d, site %d, info %d)", h.code, h.where, h.info);
+}
+
+}  // extern "C"

@@ -1,0 +1,129 @@
+// common.cuh -- device helpers shared by the MSA kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#define MSA_DEV __device__ __forceinline__
+
+namespace msa {
+
+// ------------------------------------------------------------------ status
+// The first 256 bytes of every workspace hold this word.  Kernels record the
+// first device-side failure here instead of trapping, so the context stays
+// usable and the host can report it.
+struct DeviceStatus {
+    int code;   // 0 ok, 5 wait ran out, 6 other device check
+    int where;  // kernel-specific site id
+    int info;   // e.g. the offending index
+    int pad;
+};
+constexpr int kStatusBytes = 256;
+constexpr int kDevTimeout = 5;
+constexpr int kDevCheck = 6;
+
+MSA_DEV void report(DeviceStatus *st, int code, int where, int info)
+{
+    if (st && atomicCAS(&st->code, 0, code) == 0) {
+        st->where = where;
+        st->info = info;
+    }
+}
+
+// ------------------------------------------------------------------ packing
+MSA_DEV uint32_t pack_bf16(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+MSA_DEV float bf16_to_f(uint16_t x) { return __uint_as_float(((uint32_t)x) << 16); }
+
+MSA_DEV float2 unpack_bf16(uint32_t x)
+{
+    return make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
+}
+
+MSA_DEV uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+// ------------------------------------------------------------------ cp.async
+MSA_DEV void cp_async16(void *smem, const void *gmem)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem)), "l"(gmem));
+}
+// zero-fills the 16 smem bytes when !valid (src-size 0)
+MSA_DEV void cp_async16_zfill(void *smem, const void *gmem, bool valid)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(smem)), "l"(gmem),
+                 "r"(valid ? 16 : 0));
+}
+MSA_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+MSA_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
+
+// ------------------------------------------------------------------ ldmatrix
+MSA_DEV void ldsm_x4(uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3, const void *p)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(smem_u32(p)));
+}
+MSA_DEV void ldsm_x4_t(uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3, const void *p)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(smem_u32(p)));
+}
+MSA_DEV void ldsm_x2(uint32_t &r0, uint32_t &r1, const void *p)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n"
+                 : "=r"(r0), "=r"(r1)
+                 : "r"(smem_u32(p)));
+}
+MSA_DEV void ldsm_x2_t(uint32_t &r0, uint32_t &r1, const void *p)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];\n"
+                 : "=r"(r0), "=r"(r1)
+                 : "r"(smem_u32(p)));
+}
+
+// ------------------------------------------------------------------ mma.sync
+// D(16x8,f32) += A(16x16,bf16,row) * B(16x8,bf16,col)
+MSA_DEV void mma16816(float *c, const uint32_t *a, const uint32_t *b)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// ------------------------------------------------------------------ misc
+MSA_DEV float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+MSA_DEV float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// fp32 atomic add without a return value (compiles to a reduction)
+MSA_DEV void red_add(float *p, float v) { atomicAdd(p, v); }
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Order-preserving map of a finite fp32 to uint32 (larger float -> larger key).
+MSA_DEV uint32_t float_key(float f)
+{
+    uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+}  // namespace msa

@@ -1,0 +1,59 @@
+// msa_internal.h -- problem description and kernel launchers shared by the
+// C-ABI layer (api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace msa {
+
+struct Problem {
+    int B, Nq, Nk, q_offset, Hq, Hkv, G, d, d_idx, block, topk, nb;
+    long long kv_rows;     // rows per batch entry of k, v, k_idx (>= Nk)
+    float scale, scale_idx;
+    int num_sms;
+};
+
+using bf16 = __nv_bfloat16;
+
+// Counts kernel launches made by the library (read by msa_launch_count()).
+void note_launch(int n = 1);
+
+// Index branch: token scores + block max-pool.  bs: [B, Nq, Hkv, nb] fp32.
+cudaError_t launch_index_scores(const Problem &p, const bf16 *q_idx, const bf16 *k_idx, float *bs,
+                                DeviceStatus *st, cudaStream_t s);
+// Top-k block selection from block scores.  sel: [B, Hkv, Nq, topk].
+cudaError_t launch_block_topk(const Problem &p, const float *bs, int32_t *sel, DeviceStatus *st,
+                              cudaStream_t s);
+// Main branch forward.
+cudaError_t launch_sparse_attn_fwd(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *v,
+                                   const int32_t *sel, bf16 *o, float *lse, DeviceStatus *st,
+                                   cudaStream_t s);
+// KL forward: per-row KL and lse_idx, then the deterministic scalar mean.
+cudaError_t launch_kl_fwd(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *q_idx,
+                          const bf16 *k_idx, const int32_t *sel, const float *lse, float *lse_idx,
+                          float *kl_rows, DeviceStatus *st, cudaStream_t s);
+cudaError_t launch_kl_reduce(const Problem &p, const float *kl_rows, float kl_coef, float *kl_loss,
+                             cudaStream_t s);
+
+// Backward pieces.  Workspace carve-up is done by the caller (api.cu).
+struct BwdWork {
+    float *D;            // [B, Hq, Nq]    rowsum(dO * O)
+    float *dq_acc;       // [B, Nq, Hq, d]  fp32 accumulators
+    float *dqi_acc;      // [B, Nq, Hkv, d_idx]
+    float *dki_acc;      // [B, Nk, d_idx]
+    int32_t *bucket_cnt; // [B*Hkv*nb]
+    int32_t *bucket_off; // [B*Hkv*nb + 1]
+    int32_t *bucket_cur; // [B*Hkv*nb]
+    int32_t *bucket_q;   // [B*Hkv*Nq*topk]  query rows per (b, r, block)
+};
+cudaError_t launch_fused_bwd(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *v,
+                             const bf16 *o, const bf16 *d_o, const float *lse, const bf16 *q_idx,
+                             const bf16 *k_idx, const int32_t *sel, const float *lse_idx,
+                             float kl_coef, bf16 *dq, bf16 *dk, bf16 *dv, bf16 *dq_idx,
+                             bf16 *dk_idx, const BwdWork &w, DeviceStatus *st, cudaStream_t s);
+
+}  // namespace msa

@@ -1,0 +1,242 @@
+// sparse_attn_fwd.cu -- main branch of MSA: exact block-sparse GQA attention.
+//
+// "Sparse Attention · Part II", section 3.2: every query head of a group
+// attends, with its own logits, to the causally visible tokens of the
+// blocks selected for (query, group) and normalises over that set only.
+// Flash-style: scores, the running max/sum and the output accumulator stay
+// on chip (section 4.1 of the same page); each K/V tile is staged once in
+// shared memory and used by all G heads of the group (section 3.2 notes the
+// selected blocks' KV loads can be shared across the group's heads).
+//
+// One CTA (4 warps) per (b, i, r).  The selected blocks are cut into 64-token
+// chunks (the local block stops at the query); chunks stream through a
+// two-stage cp.async pipeline.  Warp w handles tokens [16w, 16w+16) of every
+// chunk with its own online softmax; the four partial states are merged at
+// the end.  MMA rows are the G heads (padded to 16).
+#include "msa_internal.h"
+
+namespace msa {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kChunk = 64;
+constexpr int kMaxChunks = 64;   // 2 chunks per block, topk <= 32
+
+template <int D>
+struct FwdSmem {
+    static constexpr int ROW = D * 2;                   // bytes per bf16 row
+    static constexpr int Q_BYTES = 16 * ROW;
+    static constexpr int KV_BYTES = kChunk * ROW;       // one K or V chunk
+    static constexpr int STAGE = 2 * KV_BYTES;          // K + V
+    static constexpr int OFF_STAGES = Q_BYTES;
+    static constexpr int OFF_CHUNKS = OFF_STAGES + 2 * STAGE;
+    static constexpr int SMEM = OFF_CHUNKS + kMaxChunks * 8;
+};
+
+template <int D>
+__device__ __forceinline__ int swz(int row, int ch)
+{
+    return row * (D * 2) + ((ch ^ (row & 7)) << 4);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads)
+sparse_attn_fwd_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restrict__ k,
+                       const bf16 *__restrict__ v, const int32_t *__restrict__ sel,
+                       bf16 *__restrict__ o, float *__restrict__ lse, DeviceStatus *st)
+{
+    using S = FwdSmem<D>;
+    constexpr int CH = D / 8;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t *sQ = smem;
+    int2 *chunks = reinterpret_cast<int2 *>(smem + S::OFF_CHUNKS);
+    __shared__ int n_chunks;
+
+    const int i = blockIdx.x, r = blockIdx.y, b = blockIdx.z;
+    const int G = p.G;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const long long pos = (long long)p.q_offset + i;
+    const int32_t *srow = sel + (((long long)b * p.Hkv + r) * p.Nq + i) * p.topk;
+
+    if (tid == 0) {
+        int n = 0;
+        for (int m = 0; m < p.topk; ++m) {
+            const int c = srow[m];
+            if (c < 0) continue;
+            if ((long long)c * 128 > pos) { report(st, kDevCheck, 31, c); continue; }
+            const long long start = (long long)c * 128;
+            const long long end = min(min(start + 128, pos + 1), (long long)p.Nk);
+            for (long long s0 = start; s0 < end && n < kMaxChunks; s0 += kChunk)
+                chunks[n++] = make_int2((int)s0, (int)min((long long)kChunk, end - s0));
+        }
+        n_chunks = n;
+    }
+    // Q rows of the group's heads (rows >= G are zero)
+    const bf16 *qrow = q + (((long long)b * p.Nq + i) * p.Hq + (long long)r * G) * D;
+    for (int idx = tid; idx < 16 * CH; idx += kThreads) {
+        const int row = idx / CH, ch = idx % CH;
+        cp_async16_zfill(sQ + swz<D>(row, ch), qrow + (row < G ? row : 0) * D + ch * 8, row < G);
+    }
+    cp_async_commit();
+    __syncthreads();
+    const int nc = n_chunks;
+
+    const bf16 *kb = k + ((long long)b * p.kv_rows * p.Hkv + r) * D;
+    const bf16 *vb = v + ((long long)b * p.kv_rows * p.Hkv + r) * D;
+    const long long jstride = (long long)p.Hkv * D;
+    auto load_chunk = [&](int ci, int stage) {
+        uint8_t *sk = smem + S::OFF_STAGES + stage * S::STAGE;
+        uint8_t *sv = sk + S::KV_BYTES;
+        const int2 cj = chunks[ci];
+        for (int idx = tid; idx < kChunk * CH; idx += kThreads) {
+            const int row = idx / CH, ch = idx % CH;
+            const bool ok = row < cj.y;
+            const long long j = cj.x + (ok ? row : 0);
+            cp_async16_zfill(sk + swz<D>(row, ch), kb + j * jstride + ch * 8, ok);
+            cp_async16_zfill(sv + swz<D>(row, ch), vb + j * jstride + ch * 8, ok);
+        }
+    };
+    if (nc > 0) load_chunk(0, 0);
+    cp_async_commit();
+
+    const int g = lane >> 2, t = lane & 3;
+    const float sl2 = p.scale * kLog2e;
+    uint32_t af[D / 16][4];
+    float acc_o[D / 8][4];
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) acc_o[n][0] = acc_o[n][1] = acc_o[n][2] = acc_o[n][3] = 0.f;
+    float m_run = -INFINITY, l_run = 0.f;   // row g (rows g+8 are padding)
+
+    for (int ci = 0; ci < nc; ++ci) {
+        const int stage = ci & 1;
+        if (ci + 1 < nc) load_chunk(ci + 1, stage ^ 1);
+        cp_async_commit();
+        cp_async_wait<1>();
+        __syncthreads();
+        if (ci == 0) {
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks)
+                ldsm_x4(af[ks][0], af[ks][1], af[ks][2], af[ks][3], sQ + swz<D>(lane & 15, ks * 2 + (lane >> 4)));
+        }
+        const uint8_t *sk = smem + S::OFF_STAGES + stage * S::STAGE;
+        const uint8_t *sv = sk + S::KV_BYTES;
+        const int len = chunks[ci].y;
+        const int kw = warp * 16;           // this warp's first token in the chunk
+        if (kw < len) {
+            float sc[2][4];
+#pragma unroll
+            for (int n = 0; n < 2; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                uint32_t b0[2], b1[2];
+                ldsm_x4(b0[0], b0[1], b1[0], b1[1],
+                        sk + swz<D>(kw + (lane & 7) + ((lane >> 4) << 3), ks * 2 + ((lane >> 3) & 1)));
+                mma16816(sc[0], af[ks], b0);
+                mma16816(sc[1], af[ks], b1);
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int kk = kw + n * 8 + 2 * t + e;
+                    sc[n][e] = kk < len ? sc[n][e] * sl2 : -INFINITY;
+                    mx = fmaxf(mx, sc[n][e]);
+                }
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float m_new = fmaxf(m_run, mx);          // finite: token kw is valid
+            const float alpha = exp2f(m_run - m_new);       // 0 when m_run = -inf
+            float ps = 0.f;
+            uint32_t pa[4];
+            float pv[2][2];
+#pragma unroll
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    pv[n][e] = exp2f(sc[n][e] - m_new);
+                    ps += pv[n][e];
+                }
+            pa[0] = pack_bf16(pv[0][0], pv[0][1]);
+            pa[1] = 0u;                                     // rows g+8: padding
+            pa[2] = pack_bf16(pv[1][0], pv[1][1]);
+            pa[3] = 0u;
+            l_run = l_run * alpha + ps;
+            m_run = m_new;
+#pragma unroll
+            for (int n = 0; n < D / 8; ++n) {
+                acc_o[n][0] *= alpha;
+                acc_o[n][1] *= alpha;
+            }
+#pragma unroll
+            for (int np = 0; np < D / 16; ++np) {
+                uint32_t b0[2], b1[2];
+                ldsm_x4_t(b0[0], b0[1], b1[0], b1[1],
+                          sv + swz<D>(kw + (lane & 7) + (((lane >> 3) & 1) << 3), np * 2 + (lane >> 4)));
+                mma16816(acc_o[np * 2], pa, b0);
+                mma16816(acc_o[np * 2 + 1], pa, b1);
+            }
+        }
+        __syncthreads();
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+
+    // merge the four warps' partial states (rows g < G only)
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+    float *sO = reinterpret_cast<float *>(smem + S::OFF_STAGES);     // [4][8][D]
+    float *sM = sO + 4 * 8 * D;                                       // [4][8]
+    float *sL = sM + 4 * 8;
+    if (g < G) {
+#pragma unroll
+        for (int n = 0; n < D / 8; ++n) {
+            sO[(warp * 8 + g) * D + n * 8 + 2 * t] = acc_o[n][0];
+            sO[(warp * 8 + g) * D + n * 8 + 2 * t + 1] = acc_o[n][1];
+        }
+        if (t == 0) {
+            sM[warp * 8 + g] = m_run;
+            sL[warp * 8 + g] = l_run;
+        }
+    }
+    __syncthreads();
+    for (int idx = tid; idx < G * D; idx += kThreads) {
+        const int h = idx / D, col = idx % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, sM[w * 8 + h]);
+        float L = 0.f, acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const float f = exp2f(sM[w * 8 + h] - M);
+            L += f * sL[w * 8 + h];
+            acc += f * sO[(w * 8 + h) * D + col];
+        }
+        const int hh = r * G + h;
+        o[(((long long)b * p.Nq + i) * p.Hq + hh) * D + col] = __float2bfloat16_rn(acc / L);
+        if (col == 0) lse[((long long)b * p.Hq + hh) * p.Nq + i] = (M + log2f(L)) * kLn2;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_sparse_attn_fwd(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *v,
+                                   const int32_t *sel, bf16 *o, float *lse, DeviceStatus *st,
+                                   cudaStream_t s)
+{
+    dim3 grid(p.Nq, p.Hkv, p.B);
+    if (p.d == 128) {
+        const int sm = FwdSmem<128>::SMEM;
+        cudaFuncSetAttribute(sparse_attn_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+        sparse_attn_fwd_kernel<128><<<grid, kThreads, sm, s>>>(p, q, k, v, sel, o, lse, st);
+        note_launch();
+    } else {
+        const int sm = FwdSmem<64>::SMEM;
+        cudaFuncSetAttribute(sparse_attn_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+        sparse_attn_fwd_kernel<64><<<grid, kThreads, sm, s>>>(p, q, k, v, sel, o, lse, st);
+        note_launch();
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace msa

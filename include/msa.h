@@ -1,0 +1,167 @@
+/*
+ * msa.h -- C-ABI of libmsa.so, the GB300 (sm_103a) implementation of the
+ * MiniMax Sparse Attention (MSA) layer's data-parallel hot path.
+ *
+ * The operator is the one defined in "Sparse Attention · Part II"
+ * (mtreviso.github.io/blog/sparse-attention-2.html), section 3.2 "MiniMax's
+ * MSA": an index branch scores every causally visible token with one index
+ * query per GQA group against a single index key head shared by all groups,
+ * max-pools the token scores into 128-token block scores and keeps, per
+ * query and group, the query's own (local) block plus the k-1 best earlier
+ * blocks; the main branch runs exact GQA softmax attention over the visible
+ * tokens of those blocks only; training adds the detached KL alignment loss
+ * of that section and the backward pass.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller, row-major
+ *     and contiguous in the layouts below.  bf16 tensors are passed as
+ *     `void*` to keep CUDA headers out of this file.
+ *   - The library never allocates, frees or synchronises.  Every call only
+ *     enqueues kernels on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and returns.
+ *   - Scratch memory ("workspace") comes from the caller: at least
+ *     msa_workspace_size(shape, op) bytes, 256-byte aligned.  Its first 256
+ *     bytes hold a device status word that the kernels set on a device-side
+ *     error (a wait that ran out, an index out of range);
+ *     msa_check_device_status() reads it.  Those 256 bytes must be zero
+ *     before the first call on a workspace (msa_check_device_status() zeroes
+ *     them again after reporting); the rest need not be initialised.  Calls
+ *     that share one workspace must be ordered on one stream.
+ *   - Errors: arguments are validated on the host before any launch; on
+ *     failure nothing is launched and the call returns a non-zero
+ *     msa_status; msa_last_error() then gives a message (per host thread).
+ *
+ * Shapes and layouts (B batch, Nq queries, Nk keys, Hq query heads, Hkv KV
+ * heads = GQA groups, G = Hq/Hkv, head h belongs to group h / G):
+ *   q, o, d_o, dq         [B, Nq, Hq, d]        bf16
+ *   k, v, dk, dv          [B, kv_rows, Hkv, d]  bf16 (rows >= Nk unused)
+ *   q_idx, dq_idx         [B, Nq, Hkv, d_idx]   bf16
+ *   k_idx, dk_idx         [B, kv_rows, d_idx]   bf16
+ *   sel_idx               [B, Hkv, Nq, topk]    int32, ascending block ids,
+ *                                               then -1 padding
+ *   block_scores          [B, Nq, Hkv, nb]      fp32, nb = ceil(Nk/block);
+ *                                               entry c of row i is defined
+ *                                               for c <= c0(i) only
+ *   lse                   [B, Hq, Nq]           fp32, natural log
+ *   lse_idx, kl_rows      [B, Hkv, Nq]          fp32
+ * Query row i sits at absolute position pos(i) = q_offset + i and sees key j
+ * iff j <= pos(i); its local block is c0(i) = pos(i) / block.  Requires
+ * Nk >= q_offset + Nq (every visible key exists).
+ *
+ * Supported (else MSA_ERR_UNSUPPORTED): block == 128; d, d_idx in {64, 128};
+ * 1 <= topk <= 32; Hq % Hkv == 0 with G in {1, 2, 4, 8}.
+ */
+#ifndef MSA_H
+#define MSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MSA_OK = 0,
+    MSA_ERR_INVALID_ARGUMENT = 1, /* null pointer, bad size, misaligned pointer */
+    MSA_ERR_UNSUPPORTED = 2,      /* valid shape outside what this build supports */
+    MSA_ERR_WORKSPACE = 3,        /* workspace too small */
+    MSA_ERR_CUDA = 4,             /* a kernel launch or CUDA query failed */
+    MSA_ERR_TIMEOUT = 5,          /* a device-side wait ran out (from msa_check_device_status) */
+    MSA_ERR_DEVICE = 6            /* another device-side check failed (msa_check_device_status) */
+} msa_status;
+
+typedef struct {
+    int B, Nq, Nk, q_offset, Hq, Hkv, d, d_idx, block, topk;
+    long long kv_rows;   /* rows per batch entry of k, v, k_idx and their grads; 0 -> Nk */
+    float scale;         /* main logit scale; 0 -> 1/sqrt(d) */
+    float scale_idx;     /* index score scale; 0 -> 1/sqrt(d_idx) */
+} msa_shape;
+
+enum {
+    MSA_OP_INDEX_SELECT = 0,
+    MSA_OP_SPARSE_ATTN_FWD = 1,
+    MSA_OP_KL_FWD = 2,
+    MSA_OP_FUSED_BWD = 3
+};
+
+/* Bytes of workspace `op` needs for `shape` (0 on an invalid shape). */
+size_t msa_workspace_size(const msa_shape *shape, int op);
+
+/*
+ * Index branch and selection (section 3.2: token scoring against the shared
+ * index key head, block max-pool, top-k with the local block reserved).
+ * For each batch b, query i and group r:
+ *   s_j   = scale_idx * <q_idx[b,i,r,:], k_idx[b,j,:]>   for j <= pos(i)
+ *   bs_c  = max over visible j in block c of s_j           (fp32)
+ *   sel   = {c0(i)} + the topk-1 blocks c < c0(i) of largest bs_c, ties to
+ *           the lower c; every visible block when c0(i)+1 <= topk.
+ * Writes sel_idx; also block_scores when it is not NULL (otherwise they live
+ * in the workspace).  No exp is taken: ranking uses raw scores.
+ */
+msa_status msa_index_select(const msa_shape *shape, const void *q_idx, const void *k_idx,
+                            int32_t *sel_idx, float *block_scores,
+                            void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Main branch (section 3.2): exact block-sparse GQA attention.  For head h
+ * of group r, over the token set T = {j <= pos(i) : j / block in sel_idx}:
+ *   l_j = scale * <q[b,i,h,:], k[b,j,r,:]>,  P = softmax_T(l),
+ *   o[b,i,h,:] = sum_j P_j v[b,j,r,:],       lse[b,h,i] = log sum_T exp(l_j).
+ * Each selected K/V block is staged once for all G heads of the group.
+ */
+msa_status msa_sparse_attn_fwd(const msa_shape *shape, const void *q, const void *k, const void *v,
+                               const int32_t *sel_idx, void *o, float *lse,
+                               void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * KL alignment loss (section 3.2, the L_KL equation).  Teacher
+ * Pt_j = (1/G) sum_{h in r} exp(l_{h,j} - lse[b,h,i]) (from the forward's
+ * lse; detached), student Ps = softmax_T(s) with s_j = scale_idx <q_idx, k_idx_j>:
+ *   lse_idx[b,r,i] = log sum_T exp(s_j)
+ *   kl_rows[b,r,i] = sum_T Pt_j (log Pt_j - s_j) + lse_idx    ( = KL(Pt||Ps) )
+ *   *kl_loss       = kl_coef / (B Nq Hkv) * sum of kl_rows   (device scalar)
+ * kl_rows may be NULL (then it lives in the workspace).  The sum is taken in
+ * a fixed order, so kl_loss is reproducible run to run.
+ */
+msa_status msa_kl_fwd(const msa_shape *shape, const void *q, const void *k, const void *q_idx,
+                      const void *k_idx, const int32_t *sel_idx, const float *lse, float kl_coef,
+                      float *lse_idx, float *kl_rows, float *kl_loss,
+                      void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Fused backward of  sum(d_o . o) + L_KL.  Main gradients (dq, dk, dv) are
+ * the softmax-attention backward over each query's selected token set; the
+ * index gradients use the expansion of the KL in the student logits,
+ * dL/ds_j = kl_coef/(B Nq Hkv) * (Ps_j - Pt_j), so neither distribution is
+ * stored.  The teacher and the selection carry no gradient; the index
+ * branch gets none from d_o (section 3.2 on the two detachments).  Uses the
+ * forward's o and lse and the KL forward's lse_idx.  Requires q_offset == 0
+ * and Nq == Nk (training layout).  dk, dv, dk_idx are fully written (zero
+ * for keys no query selected).
+ */
+msa_status msa_fused_bwd(const msa_shape *shape, const void *q, const void *k, const void *v,
+                         const void *o, const void *d_o, const float *lse, const void *q_idx,
+                         const void *k_idx, const int32_t *sel_idx, const float *lse_idx, float kl_coef,
+                         void *dq, void *dk, void *dv, void *dq_idx, void *dk_idx,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
+/* Message of the last failed call on this host thread ("" if none). */
+const char *msa_last_error(void);
+
+/* Synchronises `stream`, reads the device status word of `workspace`,
+ * returns MSA_OK, MSA_ERR_TIMEOUT or MSA_ERR_DEVICE, and clears the word. */
+msa_status msa_check_device_status(void *workspace, void *stream);
+
+/* Library version string. */
+const char *msa_version(void);
+
+/* Number of kernels this process has launched through the library so far
+ * (monotonic; for accounting launches in a timed region). */
+unsigned long long msa_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSA_H */

@@ -1,0 +1,95 @@
+"""The C-ABI library builds, loads and exports every symbol include/msa.h
+declares; host-side validation works without a GPU (no compute calls)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def libmsa():
+    from block_sparse_gqa_causal_gb300 import build
+    build.build()
+    from block_sparse_gqa_causal_gb300 import api
+    return api.lib()
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "msa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(msa_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_symbols()
+    for n in ("msa_index_select", "msa_sparse_attn_fwd", "msa_kl_fwd", "msa_fused_bwd", "msa_workspace_size",
+              "msa_last_error", "msa_check_device_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(libmsa):
+    for n in declared_symbols():
+        assert hasattr(libmsa, n), n
+
+
+def test_version_and_workspace_sizes(libmsa):
+    from block_sparse_gqa_causal_gb300 import api
+    assert "sm_103a" in api.version()
+    sh = api.Shape(B=1, Nq=131072, Nk=131072, Hq=64, Hkv=8, d=128, d_idx=128, topk=16)
+    # block scores: B*Nq*Hkv*nb fp32 + status word
+    assert api.workspace_size(sh, api.OP_INDEX_SELECT) >= 131072 * 8 * 1024 * 4 + 256
+    assert api.workspace_size(sh, api.OP_SPARSE_ATTN_FWD) == 256
+    assert api.workspace_size(sh, api.OP_KL_FWD) >= 131072 * 8 * 4
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("block", 64, 2), ("d", 96, 2), ("topk", 33, 2), ("Hkv", 3, 1), ("Nq", 0, 1), ("q_offset", 5, 1),
+    ("Hq", 48, 2),
+])
+def test_invalid_shapes_are_rejected_before_any_launch(libmsa, field, value, code):
+    from block_sparse_gqa_causal_gb300 import api
+    sh = api.Shape(B=1, Nq=256, Nk=256, Hq=8, Hkv=2, d=64, d_idx=64, topk=4)
+    setattr(sh, field, value)
+    if field == "Hq":
+        sh.Hkv = 3      # G = 16
+    fake = ctypes.c_void_p(1 << 20)   # never dereferenced: validation fails first
+    sel = ctypes.c_void_p(1 << 21)
+    rc = libmsa.msa_index_select(ctypes.byref(sh.c()), fake, fake, sel, None, fake, 1 << 30, None)
+    assert rc == code, (field, rc, libmsa.msa_last_error())
+    assert libmsa.msa_last_error().decode()
+
+
+def test_null_and_misaligned_pointers_are_rejected(libmsa):
+    from block_sparse_gqa_causal_gb300 import api
+    sh = api.Shape(B=1, Nq=256, Nk=256, Hq=8, Hkv=2, d=64, d_idx=64, topk=4)
+    good = ctypes.c_void_p(1 << 20)
+    rc = libmsa.msa_sparse_attn_fwd(ctypes.byref(sh.c()), None, good, good, good, good, good, good, 256, None)
+    assert rc == 1 and b"q is NULL" in libmsa.msa_last_error()
+    bad = ctypes.c_void_p((1 << 20) + 2)
+    rc = libmsa.msa_sparse_attn_fwd(ctypes.byref(sh.c()), bad, good, good, good, good, good, good, 256, None)
+    assert rc == 1 and b"aligned" in libmsa.msa_last_error()
+    rc = libmsa.msa_sparse_attn_fwd(ctypes.byref(sh.c()), good, good, good, good, good, good, good, 16, None)
+    assert rc == 3   # workspace too small
+
+
+def test_bwd_rejects_non_training_layout(libmsa):
+    from block_sparse_gqa_causal_gb300 import api
+    sh = api.Shape(B=1, Nq=3, Nk=256, Hq=8, Hkv=2, d=64, d_idx=64, topk=4, q_offset=253)
+    g = ctypes.c_void_p(1 << 20)
+    rc = libmsa.msa_fused_bwd(ctypes.byref(sh.c()), g, g, g, g, g, g, g, g, g, g, ctypes.c_float(1.0),
+                              g, g, g, g, g, g, 1 << 30, None)
+    assert rc == 2
+
+
+def test_product_path_has_no_oracle_or_fallback():
+    """The library binding never imports the oracle and has no CPU path."""
+    pkg = os.path.join(ROOT, "block_sparse_gqa_causal_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "msa_oracle" not in text, f
