@@ -4,18 +4,24 @@
 // to the lower block index.  No exponentials: scores are compared raw, since
 // softmax is monotone (the "exp-free" selection of the MSA summary page).
 //
-// One warp per (b, i, r) row.  A candidate is the 64-bit key
-//   (order-preserving bits of the fp32 score) << 32 | (0xFFFFFFFF - c)
-// so one unsigned compare ranks by score, then by lower index.  The warp
-// keeps its current best k-1 keys distributed over lanes (lane m holds the
-// m-th best) and streams the row in 32-wide coalesced chunks; only keys
-// above the current (k-1)-th best are inserted.
+// One warp per (b, i, r) row, streamed in segments of 32*R scores (R per
+// lane, coalesced loads all in flight).  Per segment, a conservative cutoff
+// (section 4.2 of the same page: the k-th largest of a subset of at least k
+// elements never exceeds the global k-th largest) is the (k-1)-th largest of
+// the 32 lane maxima; only scores at or above it, and above the current
+// (k-1)-th best, survive.  Survivors become 64-bit keys
+//   (order-preserving bits of the fp32 score) << 32 | (0xFFFFFFFF - c),
+// so one unsigned compare ranks by score then by lower index; they are
+// sorted 32 at a time and merged into the running top-(k-1), which is kept
+// sorted across the lanes.
 #include "msa_internal.h"
 
 namespace msa {
 namespace {
 
 constexpr int kWarps = 8;
+constexpr int kR = 16;                 // scores per lane per segment
+constexpr int kSeg = 32 * kR;
 
 __device__ __forceinline__ unsigned long long make_key(float s, int c)
 {
@@ -29,34 +35,85 @@ __device__ __forceinline__ unsigned long long shfl64(unsigned long long v, int s
     return ((unsigned long long)hi << 32) | lo;
 }
 
-__device__ __forceinline__ unsigned long long shfl64_up(unsigned long long v, int delta)
+__device__ __forceinline__ unsigned long long shfl64_xor(unsigned long long v, int m)
 {
-    const uint32_t lo = __shfl_up_sync(0xffffffffu, (uint32_t)v, delta);
-    const uint32_t hi = __shfl_up_sync(0xffffffffu, (uint32_t)(v >> 32), delta);
+    const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)v, m);
+    const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(v >> 32), m);
     return ((unsigned long long)hi << 32) | lo;
 }
 
-// ascending bitonic sort of one int per lane across the warp
-__device__ __forceinline__ int warp_sort_asc(int v, int lane)
+// descending bitonic sort of one 64-bit key per lane
+__device__ __forceinline__ unsigned long long sort_desc64(unsigned long long v, int lane)
 {
 #pragma unroll
     for (int size = 2; size <= 32; size <<= 1) {
 #pragma unroll
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            const int other = __shfl_xor_sync(0xffffffffu, v, stride);
-            const bool up = (lane & size) == 0 || size == 32;
+            const unsigned long long o = shfl64_xor(v, stride);
+            const bool desc = (lane & size) == 0 || size == 32;
             const bool lower = (lane & stride) == 0;
-            v = (lower == up) ? min(v, other) : max(v, other);
+            v = (lower == desc) ? (v > o ? v : o) : (v < o ? v : o);
         }
     }
     return v;
 }
 
+// a bitonic sequence across the lanes -> descending order
+__device__ __forceinline__ unsigned long long merge_desc64(unsigned long long v, int lane)
+{
+#pragma unroll
+    for (int stride = 16; stride > 0; stride >>= 1) {
+        const unsigned long long o = shfl64_xor(v, stride);
+        v = ((lane & stride) == 0) ? (v > o ? v : o) : (v < o ? v : o);
+    }
+    return v;
+}
+
+// descending bitonic sort of one float per lane
+__device__ __forceinline__ float sort_desc_f(float v, int lane)
+{
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const float o = __shfl_xor_sync(0xffffffffu, v, stride);
+            const bool desc = (lane & size) == 0 || size == 32;
+            const bool lower = (lane & stride) == 0;
+            v = (lower == desc) ? fmaxf(v, o) : fminf(v, o);
+        }
+    }
+    return v;
+}
+
+// ascending bitonic sort of one int per lane
+__device__ __forceinline__ int sort_asc_i(int v, int lane)
+{
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const int o = __shfl_xor_sync(0xffffffffu, v, stride);
+            const bool up = (lane & size) == 0 || size == 32;
+            const bool lower = (lane & stride) == 0;
+            v = (lower == up) ? min(v, o) : max(v, o);
+        }
+    }
+    return v;
+}
+
+__device__ __forceinline__ float key_value(unsigned long long key)
+{
+    const uint32_t u = (uint32_t)(key >> 32);
+    return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
+}
+
 __global__ void __launch_bounds__(kWarps * 32)
 block_topk_kernel(Problem p, const float *__restrict__ bs, int32_t *__restrict__ sel)
 {
+    __shared__ unsigned long long cand_buf[kWarps][kSeg];
     const int lane = threadIdx.x & 31;
-    const long long row = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const int wi = threadIdx.x >> 5;
+    const long long row = (long long)blockIdx.x * kWarps + wi;
     const long long rows = (long long)p.B * p.Nq * p.Hkv;
     if (row >= rows) return;
     const int r = (int)(row % p.Hkv);
@@ -73,26 +130,51 @@ block_topk_kernel(Problem p, const float *__restrict__ bs, int32_t *__restrict__
     }
     const int K1 = k - 1;            // slots the indexer chooses, 0..31
     const float *src = bs + row * p.nb;
-    unsigned long long best = 0ull;  // 0 is below every real key
-    for (int base = 0; base < c0; base += 32) {
-        const int c = base + lane;
-        const unsigned long long key = c < c0 ? make_key(__ldg(src + c), c) : 0ull;
-        unsigned long long thr = K1 > 0 ? shfl64(best, K1 - 1) : ~0ull;
-        unsigned mask = __ballot_sync(0xffffffffu, key > thr);
-        while (mask) {
-            const int srcl = __ffs(mask) - 1;
-            mask &= mask - 1;
-            const unsigned long long ck = shfl64(key, srcl);
-            if (!(ck > thr)) continue;
-            const int at = __popc(__ballot_sync(0xffffffffu, lane < K1 && best > ck));
-            const unsigned long long up = shfl64_up(best, 1);
-            if (lane > at) best = up;
-            else if (lane == at) best = ck;
-            thr = shfl64(best, K1 - 1);
+    unsigned long long *buf = cand_buf[wi];
+    unsigned long long best = 0ull;  // lane m: m-th best key so far (0 = empty)
+
+    for (int base = 0; K1 > 0 && base < c0; base += kSeg) {
+        float v[kR];
+#pragma unroll
+        for (int j = 0; j < kR; ++j) {
+            const int c = base + j * 32 + lane;
+            v[j] = c < c0 ? __ldg(src + c) : -INFINITY;
         }
+        float lmax = v[0];
+#pragma unroll
+        for (int j = 1; j < kR; ++j) lmax = fmaxf(lmax, v[j]);
+        const float tau = __shfl_sync(0xffffffffu, sort_desc_f(lmax, lane), K1 - 1);
+        const unsigned long long kth = shfl64(best, K1 - 1);
+        const float t_run = kth ? key_value(kth) : -INFINITY;
+        // survivors: >= the segment cutoff and strictly above the running
+        // (k-1)-th value (an equal value here has a larger index and loses)
+        int cnt = 0;
+#pragma unroll
+        for (int j = 0; j < kR; ++j) cnt += (v[j] >= tau && v[j] > t_run && v[j] != -INFINITY) ? 1 : 0;
+        int off = cnt;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, off, d);
+            if (lane >= d) off += o;
+        }
+        const int total = __shfl_sync(0xffffffffu, off, 31);
+        off -= cnt;
+        if (total == 0) continue;
+#pragma unroll
+        for (int j = 0; j < kR; ++j)
+            if (v[j] >= tau && v[j] > t_run && v[j] != -INFINITY) buf[off++] = make_key(v[j], base + j * 32 + lane);
+        __syncwarp();
+        for (int c32 = 0; c32 < total; c32 += 32) {
+            unsigned long long ck = (c32 + lane < total) ? buf[c32 + lane] : 0ull;
+            ck = sort_desc64(ck, lane);
+            // top 32 of two descending lists: pairwise max against the reversed list is bitonic
+            const unsigned long long rev = shfl64(ck, 31 - lane);
+            best = merge_desc64(best > rev ? best : rev, lane);
+        }
+        __syncwarp();
     }
     int id = lane < K1 ? (int)(0xFFFFFFFFu - (uint32_t)best) : (lane == K1 ? c0 : 0x7fffffff);
-    id = warp_sort_asc(id, lane);
+    id = sort_asc_i(id, lane);
     if (lane < k) out[lane] = id;
 }
 

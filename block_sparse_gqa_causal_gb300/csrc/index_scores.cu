@@ -1,179 +1,271 @@
-// index_scores.cu -- index branch of MSA: token scores and block max-pool.
+// index_scores.cu -- index branch of MSA: token scores and block max-pool,
+// on the 5th-generation tensor cores (tcgen05 + TMEM, operands by TMA).
 //
 // "Sparse Attention · Part II", section 3.2: per query and GQA group, the
 // group's index query is dotted with the index key head shared by all
 // groups over every causally visible token, and each 128-token block is
-// scored by its largest visible token score.  The N x N token scores never
-// leave the SM: each CTA reduces a 128 x 128 score tile to 128 block scores.
+// scored by its largest visible token score.  This is the only quadratic
+// stage of the layer.  The N x N token scores never leave the SM: each
+// 128 x 128 score tile lands in TMEM and is reduced there to 128 block
+// scores by the epilogue warps.
 //
-// Rows of the GEMM are "flat" (query, group) rows rho = i*Hkv + r of one
-// batch entry (q_idx [B, Nq, Hkv, d_idx] is exactly that matrix), so a tile
-// mixes the groups of a few queries and all of them share the K_idx block
-// in shared memory.  Columns are the 128 keys of one block.  A CTA owns 128
-// rows and walks the key blocks its rows can see (optionally a slice of
-// them, when few row tiles exist, e.g. in decode).
+// GEMM rows are the "flat" (query, group) rows rho = i*Hkv + r of one batch
+// entry (q_idx [B, Nq, Hkv, d_idx] is exactly that row-major matrix), so all
+// rows share the K_idx tile.  A CTA owns 256 rows (two M=128 tiles) and
+// walks the key blocks those rows can see (or a slice of them when there
+// are few row tiles, as in decode).  Roles:
+//   warp 0      TMA producer: Q tiles once, then K_idx blocks into a 4-deep ring
+//   warp 1      TMEM allocator and single-thread tcgen05.mma issuer
+//   warps 2..9  epilogue: TMEM -> registers, causal mask, row max, store
+// Two TMEM accumulator sets (2 tiles x 128 fp32 columns each) alternate so
+// the epilogue of block c overlaps the MMAs of block c+1.
 #include "msa_internal.h"
+#include "tc.cuh"
 
 namespace msa {
 namespace {
 
-constexpr int kRows = 128;
-constexpr int kThreads = 256;
+constexpr int kTileRows = 256;     // two M=128 tiles
+constexpr int kStages = 4;         // K_idx ring depth
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kSub = 128 * 128;    // one [128 rows][64 bf16] swizzled sub-tile, bytes
+constexpr uint32_t kIdesc = tc::idesc_bf16(128, 128);
 
 template <int DI>
-struct IdxTile {
-    static constexpr int CH = DI / 8;               // 16-byte chunks per row
-    static constexpr int BYTES = kRows * DI * 2;    // one [128][DI] bf16 tile
-    static constexpr int SMEM = 3 * BYTES;          // Q tile + 2 K_idx stages
+struct Smem {
+    static constexpr int KB = DI / 64;                       // 128-byte K sub-tiles per row
+    static constexpr int Q_BYTES = 2 * KB * kSub;
+    static constexpr int K_BYTES = KB * kSub;
+    static constexpr int OFF_K = Q_BYTES;
+    static constexpr int OFF_BAR = OFF_K + kStages * K_BYTES;
+    static constexpr int BYTES = OFF_BAR + 256;
+    // request at least ~120 KB so one CTA (which takes all 512 TMEM columns) runs per SM
+    static constexpr int ALLOC = (BYTES + 1024 > 120 * 1024 ? BYTES + 1024 : 120 * 1024);
 };
 
-// XOR-swizzled byte offset of 16-byte chunk `ch` of row `row` (kills the
-// 8-way bank conflicts of ldmatrix on 128/256-byte rows).
 template <int DI>
-__device__ __forceinline__ int swz(int row, int ch)
+__global__ void __launch_bounds__(kThreads, 1)
+index_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                       Problem p, float *__restrict__ bs, int span, DeviceStatus *st)
 {
-    return row * (DI * 2) + ((ch ^ (row & 7)) << 4);
-}
-
-template <int DI>
-__global__ void __launch_bounds__(kThreads, 2)
-index_scores_kernel(Problem p, const bf16 *__restrict__ q_idx, const bf16 *__restrict__ k_idx,
-                    float *__restrict__ bs, int splits)
-{
-    using T = IdxTile<DI>;
-    extern __shared__ __align__(128) uint8_t smem[];
+    using S = Smem<DI>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t *sQ = smem;
-    uint8_t *sK = smem + T::BYTES;
+    uint8_t *sK = smem + S::OFF_K;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::OFF_BAR);
+    uint64_t *full = bars, *empty = bars + kStages, *q_full = bars + 2 * kStages;
+    uint64_t *acc_full = q_full + 1, *acc_empty = acc_full + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 2);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int b = blockIdx.z;
     const int rows_total = p.Nq * p.Hkv;
-    const int tile = gridDim.x - 1 - blockIdx.x;   // long (late) tiles first
-    const int rho0 = tile * kRows;
-    const int rho_last = min(rho0 + kRows - 1, rows_total - 1);
-    const long long pos_first = (long long)p.q_offset + rho0 / p.Hkv;
-    const long long pos_last = (long long)p.q_offset + rho_last / p.Hkv;
+    const int tile = gridDim.x - 1 - blockIdx.x;     // heavy (late) tiles first
+    const int row0 = tile * kTileRows;
+    const int rows_here = min(kTileRows, rows_total - row0);
+    const int mt = rows_here > 128 ? 2 : 1;
+    const long long pos_first = (long long)p.q_offset + row0 / p.Hkv;
+    const long long pos_last = (long long)p.q_offset + (row0 + rows_here - 1) / p.Hkv;
     const int c_all = (int)(min(pos_last, (long long)p.Nk - 1) / 128) + 1;
-    const int span = (c_all + splits - 1) / splits;
     const int c_begin = blockIdx.y * span;
     const int c_end = min(c_all, c_begin + span);
     if (c_begin >= c_end) return;
+    const int nblk = c_end - c_begin;
 
-    const bf16 *qb = q_idx + (long long)b * rows_total * DI;
-    const bf16 *kb = k_idx + (long long)b * p.kv_rows * DI;
-    const int tid = threadIdx.x;
-
-    for (int idx = tid; idx < kRows * T::CH; idx += kThreads) {
-        const int row = idx / T::CH, ch = idx % T::CH;
-        const int rho = rho0 + row;
-        const bool ok = rho < rows_total;
-        cp_async16_zfill(sQ + swz<DI>(row, ch), qb + (long long)(ok ? rho : 0) * DI + ch * 8, ok);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            tc::mbar_init(&full[s], 1);
+            tc::mbar_init(&empty[s], 1);
+        }
+        tc::mbar_init(q_full, 1);
+        for (int a = 0; a < 2; ++a) {
+            tc::mbar_init(&acc_full[a], 1);
+            tc::mbar_init(&acc_empty[a], kEpiWarps);
+        }
+        *abort_flag = 0;
+        tc::fence_mbar_init();
     }
-    auto load_k = [&](int c, int stage) {
-        uint8_t *dst = sK + stage * T::BYTES;
-        for (int idx = tid; idx < kRows * T::CH; idx += kThreads) {
-            const int row = idx / T::CH, ch = idx % T::CH;
-            const long long j = (long long)c * 128 + row;
-            const bool ok = j < p.Nk;
-            cp_async16_zfill(dst + swz<DI>(row, ch), kb + (ok ? j : 0) * DI + ch * 8, ok);
-        }
-    };
-    load_k(c_begin, 0);
-    cp_async_commit();
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, 512);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
 
-    const int warp = tid >> 5, lane = tid & 31;
-    const int g = lane >> 2, t = lane & 3;
-    const int rA = warp * 16 + g, rB = rA + 8;
-    const int rhoA = rho0 + rA, rhoB = rho0 + rB;
-    const long long posA = (long long)p.q_offset + rhoA / p.Hkv;
-    const long long posB = (long long)p.q_offset + rhoB / p.Hkv;
-    const bool validA = rhoA < rows_total, validB = rhoB < rows_total;
-    float *outA = bs + ((long long)b * rows_total + rhoA) * p.nb;
-    float *outB = bs + ((long long)b * rows_total + rhoB) * p.nb;
-
-    uint32_t af[DI / 16][4];
-    for (int c = c_begin; c < c_end; ++c) {
-        const int stage = (c - c_begin) & 1;
-        if (c + 1 < c_end) load_k(c + 1, stage ^ 1);
-        cp_async_commit();
-        cp_async_wait<1>();
-        __syncthreads();
-        if (c == c_begin) {
-#pragma unroll
-            for (int ks = 0; ks < DI / 16; ++ks)
-                ldsm_x4(af[ks][0], af[ks][1], af[ks][2], af[ks][3],
-                        sQ + swz<DI>(warp * 16 + (lane & 15), ks * 2 + (lane >> 4)));
-        }
-        const uint8_t *sk = sK + stage * T::BYTES;
-        const long long j0 = (long long)c * 128;
-        const bool full = (j0 + 127 <= pos_first) && (j0 + 128 <= p.Nk);
-        float mA = -INFINITY, mB = -INFINITY;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            float acc[8][4];
-#pragma unroll
-            for (int n = 0; n < 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-#pragma unroll
-            for (int ks = 0; ks < DI / 16; ++ks) {
-#pragma unroll
-                for (int np = 0; np < 4; ++np) {
-                    const int key = half * 64 + np * 16 + (lane & 7) + ((lane >> 4) << 3);
-                    uint32_t b0[2], b1[2];
-                    ldsm_x4(b0[0], b0[1], b1[0], b1[1], sk + swz<DI>(key, ks * 2 + ((lane >> 3) & 1)));
-                    mma16816(acc[np * 2], af[ks], b0);
-                    mma16816(acc[np * 2 + 1], af[ks], b1);
-                }
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer
+            tc::prefetch_tmap(&tmap_q);
+            tc::prefetch_tmap(&tmap_k);
+            tc::mbar_arrive_expect_tx(q_full, mt * S::KB * kSub);
+            for (int m = 0; m < mt; ++m)
+                for (int kb = 0; kb < S::KB; ++kb)
+                    tc::tma_load_3d(sQ + (m * S::KB + kb) * kSub, &tmap_q, q_full, kb * 64, row0 + m * 128, b);
+            int issued = 0;
+            for (int n = 0; n < nblk; ++n) {
+                const int s = n % kStages;
+                const uint32_t ph = (uint32_t)(n / kStages) & 1u;
+                if (!tc::mbar_wait(&empty[s], ph ^ 1u, st, 11, abort_flag)) break;
+                tc::mbar_arrive_expect_tx(&full[s], S::KB * kSub);
+                for (int kb = 0; kb < S::KB; ++kb)
+                    tc::tma_load_3d(sK + s * S::K_BYTES + kb * kSub, &tmap_k, &full[s], kb * 64,
+                                    (c_begin + n) * 128, b);
+                issued = n + 1;
             }
+            if (*abort_flag) {
+                // let this CTA's own copies land before it exits (bounded waits)
+                tc::mbar_wait(q_full, 0, nullptr, 0, nullptr);
+                for (int n = max(0, issued - kStages); n < issued; ++n)
+                    tc::mbar_wait(&full[n % kStages], (uint32_t)(n / kStages) & 1u, nullptr, 0, nullptr);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------- MMA issuer
+            bool ok = tc::mbar_wait(q_full, 0, st, 12, abort_flag);
+            int issued = 0;
+            for (int n = 0; ok && n < nblk; ++n) {
+                const int s = n % kStages;
+                const uint32_t ph = (uint32_t)(n / kStages) & 1u;
+                const int a = n & 1;
+                const uint32_t aph = (uint32_t)(n >> 1) & 1u;
+                if (!tc::mbar_wait(&acc_empty[a], aph ^ 1u, st, 13, abort_flag)) break;
+                if (!tc::mbar_wait(&full[s], ph, st, 14, abort_flag)) break;
+                tc::fence_after_sync();
+                for (int m = 0; m < mt; ++m) {
+                    const uint32_t d = tmem + (uint32_t)((a * 2 + m) * 128);
 #pragma unroll
-            for (int n = 0; n < 8; ++n) {
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    float vA = acc[n][e], vB = acc[n][2 + e];
-                    if (!full) {
-                        const long long j = j0 + half * 64 + n * 8 + 2 * t + e;
-                        if (j > posA || j >= p.Nk) vA = -INFINITY;
-                        if (j > posB || j >= p.Nk) vB = -INFINITY;
+                    for (int ks = 0; ks < DI / 16; ++ks) {
+                        const int kb = ks >> 2, ko = (ks & 3) * 32;
+                        const uint64_t ad = tc::sdesc_k128(smem_u32(sQ + (m * S::KB + kb) * kSub + ko));
+                        const uint64_t bd = tc::sdesc_k128(smem_u32(sK + s * S::K_BYTES + kb * kSub + ko));
+                        tc::mma_bf16(d, ad, bd, kIdesc, ks > 0);
                     }
-                    mA = fmaxf(mA, vA);
-                    mB = fmaxf(mB, vB);
+                }
+                tc::mma_commit(&empty[s]);
+                tc::mma_commit(&acc_full[a]);
+                issued = n + 1;
+            }
+            if (*abort_flag && issued > 0) {
+                // MMAs complete in order: waiting for the last batch drains them all
+                const int n = issued - 1;
+                tc::mbar_wait(&acc_full[n & 1], (uint32_t)(n >> 1) & 1u, nullptr, 0, nullptr);
+            }
+        }
+    } else {
+        // ---------------- epilogue: warp -> (tile m, lane quarter q)
+        const int e = warp - 2;
+        const int m = e >> 2;
+        const int q = warp & 3;
+        const int row = m * 128 + q * 32 + lane;
+        const int rho = row0 + row;
+        const bool valid = rho < rows_total && m < mt;
+        const long long pos = (long long)p.q_offset + (valid ? rho / p.Hkv : 0);
+        const int c_last = valid ? (int)min((long long)c_end - 1, pos / 128) : -1;   // last block this row sees
+        float *out = bs + ((long long)b * rows_total + (valid ? rho : 0)) * p.nb;
+        const bool vec_ok = (p.nb & 7) == 0;
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        float grp[8];
+        for (int n0 = 0; n0 < nblk; n0 += 8) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int n = n0 + u;
+                grp[u] = 0.f;
+                if (n >= nblk) break;
+                const int a = n & 1;
+                const uint32_t aph = (uint32_t)(n >> 1) & 1u;
+                if (!tc::mbar_wait(&acc_full[a], aph, st, 15, abort_flag)) { n0 = nblk; break; }
+                tc::fence_after_sync();
+                const int c = c_begin + n;
+                const long long j0 = (long long)c * 128;
+                float mx = -INFINITY;
+                if (m < mt) {
+                    const bool full_vis = (j0 + 127 <= pos_first) && (j0 + 128 <= p.Nk);
+                    const uint32_t base = tmem + lane_base + (uint32_t)((a * 2 + m) * 128);
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch) {
+                        float v[32];
+                        tc::tmem_ld32(base + ch * 32, v);
+                        if (full_vis) {
+#pragma unroll
+                            for (int jj = 0; jj < 32; ++jj) mx = fmaxf(mx, v[jj]);
+                        } else {
+#pragma unroll
+                            for (int jj = 0; jj < 32; ++jj) {
+                                const long long j = j0 + ch * 32 + jj;
+                                if (j <= pos && j < p.Nk) mx = fmaxf(mx, v[jj]);
+                            }
+                        }
+                    }
+                }
+                grp[u] = mx * p.scale_idx;   // a positive scale commutes with max
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&acc_empty[a]);
+            }
+            // store this row's scores for blocks c_begin+n0 .. (at most 8)
+            const int c_lo = c_begin + n0;
+            const int c_hi = min(c_lo + 7, c_last);
+            if (valid && c_hi >= c_lo) {
+                if (vec_ok && c_hi == c_lo + 7) {
+                    float4 *o4 = reinterpret_cast<float4 *>(out + c_lo);
+                    o4[0] = make_float4(grp[0], grp[1], grp[2], grp[3]);
+                    o4[1] = make_float4(grp[4], grp[5], grp[6], grp[7]);
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        if (c_lo + u <= c_hi) out[c_lo + u] = grp[u];
                 }
             }
         }
-        mA = fmaxf(mA, __shfl_xor_sync(0xffffffffu, mA, 1));
-        mA = fmaxf(mA, __shfl_xor_sync(0xffffffffu, mA, 2));
-        mB = fmaxf(mB, __shfl_xor_sync(0xffffffffu, mB, 1));
-        mB = fmaxf(mB, __shfl_xor_sync(0xffffffffu, mB, 2));
-        if (t == 0) {
-            // scale after the max: a positive scale commutes with max
-            if (validA && j0 <= posA) outA[c] = mA * p.scale_idx;
-            if (validB && j0 <= posB) outB[c] = mB * p.scale_idx;
-        }
-        __syncthreads();
     }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int DI>
+cudaError_t launch_t(const Problem &p, const bf16 *q_idx, const bf16 *k_idx, float *bs, DeviceStatus *st,
+                     cudaStream_t s)
+{
+    using S = Smem<DI>;
+    const long long rows_total = (long long)p.Nq * p.Hkv;
+    CUtensorMap tq, tk;
+    cudaError_t e = make_tmap_bf16_3d(&tq, q_idx, DI, rows_total, p.B, DI * 2ull, rows_total * DI * 2ull, 64, 128);
+    if (e != cudaSuccess) return e;
+    e = make_tmap_bf16_3d(&tk, k_idx, DI, p.kv_rows, p.B, DI * 2ull, (unsigned long long)p.kv_rows * DI * 2ull, 64,
+                          128);
+    if (e != cudaSuccess) return e;
+    const int tiles = (int)((rows_total + kTileRows - 1) / kTileRows);
+    // split each tile's block range when there are too few tiles to fill the GPU
+    int splits = 1;
+    const long long ctas = (long long)tiles * p.B;
+    if (ctas < (long long)p.num_sms) splits = (int)min((long long)(p.nb + 7) / 8, (p.num_sms + ctas - 1) / ctas);
+    int span = (p.nb + splits - 1) / splits;
+    span = (span + 7) & ~7;                         // slices start on 8-block boundaries
+    splits = (p.nb + span - 1) / span;
+    e = cudaFuncSetAttribute(index_scores_tc_kernel<DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::ALLOC);
+    if (e != cudaSuccess) return e;
+    index_scores_tc_kernel<DI><<<dim3(tiles, splits, p.B), kThreads, S::ALLOC, s>>>(tq, tk, p, bs, span, st);
+    note_launch();
+    return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_index_scores(const Problem &p, const bf16 *q_idx, const bf16 *k_idx, float *bs,
-                                DeviceStatus *, cudaStream_t s)
+                                DeviceStatus *st, cudaStream_t s)
 {
-    const int rows_total = p.Nq * p.Hkv;
-    const int tiles = (rows_total + kRows - 1) / kRows;
-    int splits = 1;
-    const long long ctas = (long long)tiles * p.B;
-    if (ctas < 2LL * p.num_sms) splits = (int)min((long long)p.nb, (2LL * p.num_sms + ctas - 1) / ctas);
-    dim3 grid(tiles, splits, p.B);
-    if (p.d_idx == 128) {
-        const int sm = IdxTile<128>::SMEM;
-        cudaFuncSetAttribute(index_scores_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
-        index_scores_kernel<128><<<grid, kThreads, sm, s>>>(p, q_idx, k_idx, bs, splits);
-        note_launch();
-    } else {
-        const int sm = IdxTile<64>::SMEM;
-        cudaFuncSetAttribute(index_scores_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
-        index_scores_kernel<64><<<grid, kThreads, sm, s>>>(p, q_idx, k_idx, bs, splits);
-        note_launch();
-    }
-    return cudaGetLastError();
+    return p.d_idx == 128 ? launch_t<128>(p, q_idx, k_idx, bs, st, s) : launch_t<64>(p, q_idx, k_idx, bs, st, s);
 }
 
 }  // namespace msa

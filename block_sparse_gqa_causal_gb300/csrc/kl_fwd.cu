@@ -10,9 +10,9 @@
 // so neither distribution is stored.  The scalar loss is
 // kl_coef / (B Nq Hkv) * sum over rows, reduced in a fixed order.
 //
-// Same layout as the forward kernel: one CTA (4 warps) per (b, i, r),
-// 64-token chunks of K and K_idx in a two-stage cp.async pipeline, warp w
-// owns tokens [16w, 16w+16) of each chunk.
+// One CTA (4 warps) per (b, i, r), 64-token chunks of K and K_idx in a
+// two-stage cp.async pipeline, warp w owns tokens [16w, 16w+16) of each
+// chunk.
 #include "msa_internal.h"
 
 namespace msa {
@@ -24,8 +24,8 @@ constexpr int kMaxChunks = 64;
 
 template <int D, int DI>
 struct KlSmem {
-    static constexpr int Q_BYTES = 16 * D * 2;
-    static constexpr int QI_BYTES = 16 * DI * 2;
+    static constexpr int Q_BYTES = 8 * D * 2;        // the group's heads, zero rows past G
+    static constexpr int QI_BYTES = 8 * DI * 2;      // row 0: index query, rows 1..7 zero
     static constexpr int K_BYTES = kChunk * D * 2;
     static constexpr int KI_BYTES = kChunk * DI * 2;
     static constexpr int STAGE = K_BYTES + KI_BYTES;
@@ -41,6 +41,11 @@ __device__ __forceinline__ int swz(int row, int ch)
     return row * (W * 2) + ((ch ^ (row & 7)) << 4);
 }
 
+// Transposed tiles: MMA rows are 16 tokens, the 8 MMA columns are the
+// group's heads (S^T = K Q^T) or the index query (s^T = K_idx q_idx^T, column
+// 0).  Thread (g, t) of a warp then holds tokens g and g+8 for heads 2t, 2t+1;
+// the teacher is a sum over heads, i.e. over the 4 lanes of a quad, and the
+// per-token terms are spread over lanes t = 0 (token g) and t = 1 (token g+8).
 template <int D, int DI>
 __global__ void __launch_bounds__(kThreads)
 kl_fwd_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restrict__ k,
@@ -53,7 +58,7 @@ kl_fwd_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restrict__ k,
     int2 *chunks = reinterpret_cast<int2 *>(smem + S::OFF_CHUNKS);
     __shared__ int n_chunks;
     __shared__ float s_lse2[8];
-    __shared__ float red[4][4][4];   // [warp][lane t][A, B, m, l]
+    __shared__ float red[4][32][4];   // [warp][lane][A, B, m, l]
 
     const int i = blockIdx.x, r = blockIdx.y, b = blockIdx.z;
     const int G = p.G;
@@ -74,14 +79,14 @@ kl_fwd_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restrict__ k,
         }
         n_chunks = n;
     }
-    if (tid < G) s_lse2[tid] = lse[((long long)b * p.Hq + r * G + tid) * p.Nq + i] * kLog2e;
+    if (tid < 8) s_lse2[tid] = tid < G ? lse[((long long)b * p.Hq + r * G + tid) * p.Nq + i] * kLog2e : 0.f;
     const bf16 *qrow = q + (((long long)b * p.Nq + i) * p.Hq + (long long)r * G) * D;
-    for (int idx = tid; idx < 16 * (D / 8); idx += kThreads) {
+    for (int idx = tid; idx < 8 * (D / 8); idx += kThreads) {
         const int row = idx / (D / 8), ch = idx % (D / 8);
         cp_async16_zfill(smem + swz<D>(row, ch), qrow + (row < G ? row : 0) * D + ch * 8, row < G);
     }
     const bf16 *qirow = q_idx + (((long long)b * p.Nq + i) * p.Hkv + r) * DI;
-    for (int idx = tid; idx < 16 * (DI / 8); idx += kThreads) {
+    for (int idx = tid; idx < 8 * (DI / 8); idx += kThreads) {
         const int row = idx / (DI / 8), ch = idx % (DI / 8);
         cp_async16_zfill(smem + S::OFF_QI + swz<DI>(row, ch), qirow + ch * 8, row == 0);
     }
@@ -113,10 +118,12 @@ kl_fwd_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restrict__ k,
     const int g = lane >> 2, t = lane & 3;
     const float sl2 = p.scale * kLog2e;
     const float si2 = p.scale_idx * kLog2e;
-    const float lse2_g = g < G ? s_lse2[g] : 0.f;
     const float invG = 1.f / (float)G;
-    uint32_t af[D / 16][4], ai[DI / 16][4];
-    // per-lane partial sums (used by lanes g == 0): sum Pt log2 Pt, sum Pt s2, online lse of s2
+    const bool h0_ok = 2 * t < G, h1_ok = 2 * t + 1 < G;
+    const float lse2_0 = s_lse2[(2 * t) & 7], lse2_1 = s_lse2[(2 * t + 1) & 7];
+    // B fragments of the 8 head rows and of the index query, kept in registers
+    uint32_t bq[D / 16][2], bi[DI / 16][2];
+    // per-lane partial sums over the tokens it owns: sum Pt log2 Pt, sum Pt s2, online lse of s2
     float accA = 0.f, accB = 0.f, ms = -INFINITY, ls = 0.f;
 
     for (int ci = 0; ci < nc; ++ci) {
@@ -128,87 +135,79 @@ kl_fwd_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restrict__ k,
         if (ci == 0) {
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks)
-                ldsm_x4(af[ks][0], af[ks][1], af[ks][2], af[ks][3], smem + swz<D>(lane & 15, ks * 2 + (lane >> 4)));
+                ldsm_x2(bq[ks][0], bq[ks][1], smem + swz<D>(lane & 7, ks * 2 + ((lane >> 3) & 1)));
 #pragma unroll
             for (int ks = 0; ks < DI / 16; ++ks)
-                ldsm_x4(ai[ks][0], ai[ks][1], ai[ks][2], ai[ks][3],
-                        smem + S::OFF_QI + swz<DI>(lane & 15, ks * 2 + (lane >> 4)));
+                ldsm_x2(bi[ks][0], bi[ks][1], smem + S::OFF_QI + swz<DI>(lane & 7, ks * 2 + ((lane >> 3) & 1)));
         }
         const uint8_t *sk = smem + S::OFF_STAGES + stage * S::STAGE;
         const uint8_t *ski = sk + S::K_BYTES;
         const int len = chunks[ci].y;
         const int kw = warp * 16;
         if (kw < len) {
-            float sc[2][4], si[2][4];
-#pragma unroll
-            for (int n = 0; n < 2; ++n)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) sc[n][e] = si[n][e] = 0.f;
+            float sc[4] = {0.f, 0.f, 0.f, 0.f}, si[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
-                uint32_t b0[2], b1[2];
-                ldsm_x4(b0[0], b0[1], b1[0], b1[1],
-                        sk + swz<D>(kw + (lane & 7) + ((lane >> 4) << 3), ks * 2 + ((lane >> 3) & 1)));
-                mma16816(sc[0], af[ks], b0);
-                mma16816(sc[1], af[ks], b1);
+                uint32_t a[4];
+                ldsm_x4(a[0], a[1], a[2], a[3], sk + swz<D>(kw + (lane & 15), ks * 2 + (lane >> 4)));
+                mma16816(sc, a, bq[ks]);
             }
 #pragma unroll
             for (int ks = 0; ks < DI / 16; ++ks) {
-                uint32_t b0[2], b1[2];
-                ldsm_x4(b0[0], b0[1], b1[0], b1[1],
-                        ski + swz<DI>(kw + (lane & 7) + ((lane >> 4) << 3), ks * 2 + ((lane >> 3) & 1)));
-                mma16816(si[0], ai[ks], b0);
-                mma16816(si[1], ai[ks], b1);
+                uint32_t a[4];
+                ldsm_x4(a[0], a[1], a[2], a[3], ski + swz<DI>(kw + (lane & 15), ks * 2 + (lane >> 4)));
+                mma16816(si, a, bi[ks]);
             }
-#pragma unroll
-            for (int n = 0; n < 2; ++n)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int kk = kw + n * 8 + 2 * t + e;
-                    const bool ok = kk < len;
-                    // head g's weight of this token (0 for padding heads)
-                    float pt = (ok && g < G) ? exp2f(sc[n][e] * sl2 - lse2_g) : 0.f;
-                    pt += __shfl_xor_sync(0xffffffffu, pt, 4);
-                    pt += __shfl_xor_sync(0xffffffffu, pt, 8);
-                    pt += __shfl_xor_sync(0xffffffffu, pt, 16);
-                    pt *= invG;
-                    if (g == 0 && ok) {          // row 0 of the index tile is the index query
-                        const float s2 = si[n][e] * si2;
-                        if (pt > 0.f) accA += pt * log2f(pt);
-                        accB += pt * s2;
-                        const float mn = fmaxf(ms, s2);
-                        ls = ls * exp2f(ms - mn) + exp2f(s2 - mn);
-                        ms = mn;
-                    }
-                }
+            const bool okA = kw + g < len, okB = kw + g + 8 < len;     // tokens g and g+8
+            float pA = (okA && h0_ok ? exp2f(sc[0] * sl2 - lse2_0) : 0.f) + (okA && h1_ok ? exp2f(sc[1] * sl2 - lse2_1) : 0.f);
+            float pB = (okB && h0_ok ? exp2f(sc[2] * sl2 - lse2_0) : 0.f) + (okB && h1_ok ? exp2f(sc[3] * sl2 - lse2_1) : 0.f);
+            pA += __shfl_xor_sync(0xffffffffu, pA, 1);
+            pA += __shfl_xor_sync(0xffffffffu, pA, 2);
+            pB += __shfl_xor_sync(0xffffffffu, pB, 1);
+            pB += __shfl_xor_sync(0xffffffffu, pB, 2);
+            // index score of tokens g, g+8 sits in column 0 (lane t = 0 of the quad)
+            const float sA = __shfl_sync(0xffffffffu, si[0], lane & ~3);
+            const float sB = __shfl_sync(0xffffffffu, si[2], lane & ~3);
+            if (t < 2 && (t == 0 ? okA : okB)) {
+                const float pt = (t == 0 ? pA : pB) * invG;
+                const float s2 = (t == 0 ? sA : sB) * si2;
+                if (pt > 0.f) accA += pt * log2f(pt);
+                accB += pt * s2;
+                const float mn = fmaxf(ms, s2);
+                ls = ls * exp2f(ms - mn) + exp2f(s2 - mn);
+                ms = mn;
+            }
         }
         __syncthreads();
     }
     cp_async_wait<0>();
-    if (g == 0) {
-        red[warp][t][0] = accA;
-        red[warp][t][1] = accB;
-        red[warp][t][2] = ms;
-        red[warp][t][3] = ls;
-    }
+    red[warp][lane][0] = accA;
+    red[warp][lane][1] = accB;
+    red[warp][lane][2] = ms;
+    red[warp][lane][3] = ls;
     __syncthreads();
-    if (tid == 0) {
+    if (warp == 0) {
+        // lane u combines slot u of every warp, then a warp reduction
         float A = 0.f, Bs = 0.f, M = -INFINITY;
-        for (int w = 0; w < 4; ++w)
-            for (int u = 0; u < 4; ++u) {
-                A += red[w][u][0];
-                Bs += red[w][u][1];
-                M = fmaxf(M, red[w][u][2]);
-            }
+        for (int w = 0; w < 4; ++w) {
+            A += red[w][lane][0];
+            Bs += red[w][lane][1];
+            M = fmaxf(M, red[w][lane][2]);
+        }
+        A = warp_sum(A);
+        Bs = warp_sum(Bs);
+        M = warp_max(M);
         float L = 0.f;
         for (int w = 0; w < 4; ++w)
-            for (int u = 0; u < 4; ++u)
-                if (red[w][u][3] > 0.f) L += red[w][u][3] * exp2f(red[w][u][2] - M);
-        const float lse2_idx = M + log2f(L);
-        // KL in nats: (sum Pt log2 Pt - sum Pt s2 + lse2) * ln 2
-        const long long oi = ((long long)b * p.Hkv + r) * p.Nq + i;
-        lse_idx[oi] = lse2_idx * kLn2;
-        kl_rows[oi] = (A - Bs + lse2_idx) * kLn2;
+            if (red[w][lane][3] > 0.f) L += red[w][lane][3] * exp2f(red[w][lane][2] - M);
+        L = warp_sum(L);
+        if (lane == 0) {
+            const float lse2_idx = M + log2f(L);
+            // KL in nats: (sum Pt log2 Pt - sum Pt s2 + lse2) * ln 2
+            const long long oi = ((long long)b * p.Hkv + r) * p.Nq + i;
+            lse_idx[oi] = lse2_idx * kLn2;
+            kl_rows[oi] = (A - Bs + lse2_idx) * kLn2;
+        }
     }
 }
 

@@ -2,6 +2,7 @@
 // C-ABI layer (api.cu) and the kernel translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -21,6 +22,12 @@ using bf16 = __nv_bfloat16;
 
 // Counts kernel launches made by the library (read by msa_launch_count()).
 void note_launch(int n = 1);
+
+// 3-D bf16 TMA tensor map (dims innermost first, strides of dims 1 and 2
+// in bytes), box {box0, box1, 1}, 128-byte swizzle, zero fill out of bounds.
+cudaError_t make_tmap_bf16_3d(CUtensorMap *map, const void *base, unsigned long long d0, unsigned long long d1,
+                              unsigned long long d2, unsigned long long stride1_bytes,
+                              unsigned long long stride2_bytes, unsigned box0, unsigned box1);
 
 // Index branch: token scores + block max-pool.  bs: [B, Nq, Hkv, nb] fp32.
 cudaError_t launch_index_scores(const Problem &p, const bf16 *q_idx, const bf16 *k_idx, float *bs,
@@ -55,5 +62,11 @@ cudaError_t launch_fused_bwd(const Problem &p, const bf16 *q, const bf16 *k, con
                              const bf16 *k_idx, const int32_t *sel, const float *lse_idx,
                              float kl_coef, bf16 *dq, bf16 *dk, bf16 *dv, bf16 *dq_idx,
                              bf16 *dk_idx, const BwdWork &w, DeviceStatus *st, cudaStream_t s);
+
+// tcgen05 main backward kernel (d = d_idx = 128); the prep kernels run first.
+cudaError_t launch_fused_bwd_tc_main(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *v, const bf16 *d_o,
+                                     const float *lse, const bf16 *q_idx, const bf16 *k_idx, const float *lse_idx,
+                                     float kl_coef, const BwdWork &w, bf16 *dk, bf16 *dv, DeviceStatus *st,
+                                     cudaStream_t s);
 
 }  // namespace msa

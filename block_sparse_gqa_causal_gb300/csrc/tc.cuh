@@ -1,0 +1,193 @@
+// tc.cuh -- Blackwell (sm_100-family, here sm_103a) building blocks written
+// as inline PTX: mbarriers with bounded waits, TMA tile loads, TMEM
+// allocation, tcgen05.mma (kind::f16, bf16 in / fp32 accumulate in TMEM),
+// tcgen05.commit and tcgen05.ld.  Encodings follow the PTX ISA's
+// descriptions of the shared-memory matrix descriptor and the instruction
+// descriptor for .kind::f16.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace msa {
+namespace tc {
+
+// ------------------------------------------------------------------ mbarrier
+MSA_DEV void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count));
+}
+MSA_DEV void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;\n" ::); }
+MSA_DEV void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::); }
+
+MSA_DEV void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+MSA_DEV void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+MSA_DEV bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: gives up after ~2^26 polls (seconds), records a timeout in
+// the status word and returns false.  Callers then skip their remaining
+// work so the kernel ends instead of hanging.
+constexpr uint32_t kSpinLimit = 1u << 26;
+MSA_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, DeviceStatus *st, int site, volatile int *abort_flag)
+{
+    for (uint32_t it = 0; it < kSpinLimit; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 1023u) == 1023u && abort_flag && *abort_flag) return false;
+    }
+    report(st, kDevTimeout, site, (int)parity);
+    if (abort_flag) *abort_flag = 1;
+    return false;
+}
+
+// ------------------------------------------------------------------ TMA
+MSA_DEV void tma_load_3d(void *smem_dst, const CUtensorMap *map, uint64_t *bar, int x, int y, int z)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
+        "[%2];\n" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+MSA_DEV void prefetch_tmap(const CUtensorMap *map)
+{
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ------------------------------------------------------------------ TMEM
+// Allocation is warp-wide; the allocated column base is written to smem.
+MSA_DEV void tmem_alloc(uint32_t *smem_slot, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(smem_slot)),
+                 "r"(ncols));
+}
+MSA_DEV void tmem_relinquish() { asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::); }
+MSA_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols));
+}
+MSA_DEV void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::); }
+MSA_DEV void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::); }
+
+// ------------------------------------------------------------------ descriptors
+// Shared-memory matrix descriptor, K-major operand in the 128-byte swizzle
+// layout: rows of 128 bytes (64 bf16 of K), 8-row core groups 1024 bytes
+// apart (stride byte offset), leading byte offset unused for this layout
+// (encoded as 1), version field = 1, swizzle mode 2 (128B).  The tile base
+// must be 1024-byte aligned; advancing K by 16 elements inside the 128-byte
+// row adds 32 bytes to the start address.
+MSA_DEV uint64_t sdesc_k128(uint32_t smem_addr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);        // start address
+    d |= (uint64_t)1 << 16;                             // leading byte offset (unused)
+    d |= (uint64_t)(1024u >> 4) << 32;                  // stride byte offset
+    d |= (uint64_t)1 << 46;                             // version
+    d |= (uint64_t)2 << 61;                             // 128B swizzle
+    return d;
+}
+
+// Instruction descriptor for kind::f16 with bf16 A/B, fp32 D, both operands
+// K-major, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N)
+{
+    return (1u << 4)                       // D format f32
+           | (1u << 7)                     // A format bf16
+           | (1u << 10)                    // B format bf16
+           | ((uint32_t)(N >> 3) << 17)    // N / 8
+           | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
+MSA_DEV void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, bool accumulate)
+{
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate));
+}
+
+// Arrive on `bar` once every tcgen05.mma issued so far by this thread is done.
+MSA_DEV void mma_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// 32 lanes x 32 consecutive fp32 columns, waited for inside the same asm
+// statement so no instruction can read the registers before they land:
+// thread t of warp w gets TMEM lane 32*(w%4) + t, columns col..col+31.
+MSA_DEV void tmem_ld32(uint32_t taddr, float *v)
+{
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+        "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+
+// 32 lanes x 16 consecutive fp32 columns (same conventions as tmem_ld32).
+MSA_DEV void tmem_ld16(uint32_t taddr, float *v)
+{
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+        "tcgen05.wait::ld.sync.aligned;\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+// Shared-memory matrix descriptor with explicit byte offsets (128B swizzle).
+// For a K-major operand (rows = M/N, 128-byte rows of K) the stride byte
+// offset is the step between 8-row groups and the leading byte offset is
+// unused.  For an MN-major operand (rows = K, 128-byte rows holding 64
+// consecutive M/N elements) the leading byte offset is the step between
+// 64-element atoms along M/N and the stride byte offset the step between
+// 8-row groups along K.
+MSA_DEV uint64_t sdesc_sw128(uint32_t smem_addr, uint32_t lbo_bytes, uint32_t sbo_bytes)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// instruction-descriptor bits selecting MN-major A / B
+constexpr uint32_t kAMajorMN = 1u << 15;
+constexpr uint32_t kBMajorMN = 1u << 16;
+
+}  // namespace tc
+}  // namespace msa
