@@ -121,6 +121,8 @@ msa_status check_ws(void *ws, size_t ws_bytes, size_t need)
 
 namespace msa {
 void note_launch(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+msa_status problem_from_shape(const msa_shape *shape, Problem &p) { return make_problem(shape, p); }
+msa_status set_error(msa_status st, const char *msg) { return fail(st, "%s", msg); }
 }  // namespace msa
 
 extern "C" {

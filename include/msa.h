@@ -146,6 +146,28 @@ msa_status msa_fused_bwd(const msa_shape *shape, const void *q, const void *k, c
                          void *dq, void *dk, void *dv, void *dq_idx, void *dk_idx,
                          void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * Index selection without any allocation, for callers that cannot allocate
+ * device memory (a serving process whose memory pool is frozen after
+ * warm-up, or a plugin given only raw device pointers).  There is no
+ * counterpart of this call in the method's description: it computes exactly
+ * what msa_index_select computes (same kernels, same sel_idx), but its
+ * scratch for the block scores is a static device array inside the library
+ * instead of a caller workspace.  The caller still passes q_idx, k_idx and
+ * sel_idx (layouts as above); block scores are not returned.
+ *   - Limit: B * Nq * Hkv * ceil(Nk/block) * 4 bytes <= 64 MiB, else
+ *     MSA_ERR_WORKSPACE before any launch.  Every device that loads the
+ *     library holds that array (plus 256 bytes) until the process exits.
+ *   - All calls share the array and it keeps the last call's contents;
+ *     calls that overlap on the GPU race with each other.
+ *   - The first call on each device looks up the array's address with that
+ *     device current; make it before any stream capture.
+ *   - Device-side status is kept inside the array, cleared at every call,
+ *     and not reported by this entry point.
+ */
+msa_status msa_index_select_noalloc(const msa_shape *shape, const void *q_idx, const void *k_idx,
+                                    int32_t *sel_idx, void *stream);
+
 /* Message of the last failed call on this host thread ("" if none). */
 const char *msa_last_error(void);
 
