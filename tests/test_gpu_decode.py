@@ -1,0 +1,54 @@
+"""GPU parity of the decode path: one new query per sequence attends to a
+KV / K_idx cache through the same two entry points (Nq = 1, q_offset = pos,
+Nk = pos + 1, kv_rows = cache capacity).  The cache here holds 64K tokens
+(512 blocks, so selection ranks 511 earlier blocks and the index kernel
+splits the key range across CTAs); the last blocks are partial, as in the
+1M-token decode workload."""
+import numpy as np
+import pytest
+
+import oracle
+from msa_testutil import assert_close, bf16_to_np, check_selection, to_torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def decode_case():
+    from block_sparse_gqa_causal_gb300.inputs import make_inputs
+    from block_sparse_gqa_causal_gb300.workloads import DECODE_1M
+    w = DECODE_1M.scaled(name="decode_64k", B=2, N=65536, Hq=16, Hkv=4, decode_steps=200, seed=11)
+    return w, make_inputs(w)
+
+
+@pytest.mark.parametrize("step", [0, 57, 199])
+def test_decode_step_parity(decode_case, step):
+    import torch
+    from block_sparse_gqa_causal_gb300 import api
+    from block_sparse_gqa_causal_gb300.inputs import decode_position
+    w, x = decode_case
+    pos = decode_position(w, step)
+    q = np.ascontiguousarray(x["q"][:, step:step + 1])
+    qi = np.ascontiguousarray(x["q_idx"][:, step:step + 1])
+    sh = api.Shape(B=w.B, Nq=1, Nk=pos + 1, Hq=w.Hq, Hkv=w.Hkv, d=w.d, d_idx=w.d_idx, topk=w.topk, q_offset=pos,
+                   kv_rows=w.N)
+    t = {n: to_torch(a) for n, a in (("q", q), ("q_idx", qi), ("k", x["k"]), ("v", x["v"]), ("k_idx", x["k_idx"]))}
+    sel, bs = api.index_select(sh, t["q_idx"], t["k_idx"], return_scores=True)
+    o, lse = api.sparse_attn_fwd(sh, t["q"], t["k"], t["v"], sel)
+    torch.cuda.synchronize()
+
+    osh = oracle.Shape(B=w.B, Nq=1, Nk=pos + 1, Hq=w.Hq, Hkv=w.Hkv, d=w.d, d_idx=w.d_idx, topk=w.topk, q_offset=pos,
+                       kv_rows=w.N)
+    rows = np.arange(w.B)
+    bs_o = oracle.block_scores(osh, qi, x["k_idx"], rows)
+    bs_g = bs.cpu().numpy().reshape(w.B, w.Hkv, -1)
+    vis = np.isfinite(bs_o)
+    assert_close(bs_g[vis], bs_o[vis], "block scores", max_abs=2e-3, rel_l2=1e-4)
+    sel_np = sel.cpu().numpy()
+    sel_o = oracle.select(osh, bs_o, rows)
+    sel_g = sel_np[:, :, 0, :]
+    exact, tol = check_selection(w.topk, 128, pos, 1, rows, sel_g, sel_o, bs_o)
+    assert exact >= 1
+    o_ref, lse_ref = oracle.sparse_fwd(osh, q, x["k"], x["v"], sel_g, rows)
+    assert_close(bf16_to_np(o).reshape(o_ref.shape), o_ref, "o", bf16_out=True)
+    assert_close(lse.cpu().numpy().reshape(lse_ref.shape), lse_ref, "lse", max_abs=1e-3, rel_l2=1e-5)
