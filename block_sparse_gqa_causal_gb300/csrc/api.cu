@@ -92,8 +92,30 @@ struct Carve {
     }
 };
 
+// The forward and the KL group work by key block when the average selected
+// block is shared by enough queries to fill 128-row tiles (prefill); with few
+// queries per block (decode) they stream each query's blocks instead.
+bool fwd_keymajor(const Problem &p) { return (long long)p.Nq * p.topk >= 8LL * p.nb; }
+
 size_t bs_bytes(const Problem &p) { return align256((size_t)p.B * p.Nq * p.Hkv * p.nb * sizeof(float)); }
+
+size_t fwd_bytes(const Problem &p)
+{
+    if (!fwd_keymajor(p)) return 0;
+    const size_t rows = (size_t)p.B * p.Nq * p.Hq * p.topk;
+    const size_t nbk = (size_t)p.B * p.Hkv * p.nb;
+    return align256(rows * p.d * 2) + align256(rows * 8) + 3 * align256((nbk + 1) * 4) +
+           align256((size_t)p.B * p.Hkv * p.Nq * p.topk * 4);
+}
 size_t klrows_bytes(const Problem &p) { return align256((size_t)p.B * p.Hkv * p.Nq * sizeof(float)); }
+
+size_t kl_bytes(const Problem &p)
+{
+    if (!fwd_keymajor(p)) return 0;
+    const size_t nbk = (size_t)p.B * p.Hkv * p.nb;
+    return align256((size_t)p.B * p.Hkv * p.Nq * p.topk * 4 * 16) + 3 * align256((nbk + 1) * 4) +
+           align256((size_t)p.B * p.Hkv * p.Nq * p.topk * 4);
+}
 
 size_t bwd_bytes(const Problem &p)
 {
@@ -139,8 +161,8 @@ size_t msa_workspace_size(const msa_shape *shape, int op)
     if (make_problem(shape, p) != MSA_OK) return 0;
     switch (op) {
     case MSA_OP_INDEX_SELECT: return kStatusBytes + bs_bytes(p);
-    case MSA_OP_SPARSE_ATTN_FWD: return kStatusBytes;
-    case MSA_OP_KL_FWD: return kStatusBytes + klrows_bytes(p);
+    case MSA_OP_SPARSE_ATTN_FWD: return kStatusBytes + fwd_bytes(p);
+    case MSA_OP_KL_FWD: return kStatusBytes + klrows_bytes(p) + kl_bytes(p);
     case MSA_OP_FUSED_BWD: return kStatusBytes + bwd_bytes(p);
     default: fail(MSA_ERR_INVALID_ARGUMENT, "unknown op %d", op); return 0;
     }
@@ -182,11 +204,28 @@ msa_status msa_sparse_attn_fwd(const msa_shape *shape, const void *q, const void
     REQUIRE_PTR(o, "o");
     if (!sel_idx) return fail(MSA_ERR_INVALID_ARGUMENT, "sel_idx is NULL");
     if (!lse) return fail(MSA_ERR_INVALID_ARGUMENT, "lse is NULL");
-    st = check_ws(workspace, workspace_bytes, kStatusBytes);
+    st = check_ws(workspace, workspace_bytes, kStatusBytes + fwd_bytes(p));
     if (st != MSA_OK) return st;
-    cudaError_t e = launch_sparse_attn_fwd(p, static_cast<const bf16 *>(q), static_cast<const bf16 *>(k),
-                                           static_cast<const bf16 *>(v), sel_idx, static_cast<bf16 *>(o), lse,
-                                           static_cast<DeviceStatus *>(workspace), static_cast<cudaStream_t>(stream));
+    DeviceStatus *ds = static_cast<DeviceStatus *>(workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (fwd_keymajor(p)) {
+        Carve cv{static_cast<char *>(workspace)};
+        const size_t rows = (size_t)p.B * p.Nq * p.Hq * p.topk;
+        const size_t nbk = (size_t)p.B * p.Hkv * p.nb;
+        FwdWork w;
+        w.part = cv.take<bf16>(rows * p.d);
+        w.stats = cv.take<float2>(rows);
+        w.bucket_cnt = cv.take<int32_t>(nbk + 1);
+        w.bucket_off = cv.take<int32_t>(nbk + 1);
+        w.bucket_cur = cv.take<int32_t>(nbk + 1);
+        w.bucket_q = cv.take<int32_t>((size_t)p.B * p.Hkv * p.Nq * p.topk);
+        e = launch_sparse_fwd_keymajor(p, static_cast<const bf16 *>(q), static_cast<const bf16 *>(k),
+                                       static_cast<const bf16 *>(v), sel_idx, static_cast<bf16 *>(o), lse, w, ds, s);
+    } else {
+        e = launch_sparse_attn_fwd(p, static_cast<const bf16 *>(q), static_cast<const bf16 *>(k),
+                                   static_cast<const bf16 *>(v), sel_idx, static_cast<bf16 *>(o), lse, ds, s);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "sparse_attn_fwd launch");
     return MSA_OK;
 }
@@ -205,14 +244,29 @@ msa_status msa_kl_fwd(const msa_shape *shape, const void *q, const void *k, cons
     if (!sel_idx || !lse || !lse_idx || !kl_loss)
         return fail(MSA_ERR_INVALID_ARGUMENT, "sel_idx, lse, lse_idx and kl_loss must be non-NULL");
     if (!isfinite(kl_coef)) return fail(MSA_ERR_INVALID_ARGUMENT, "kl_coef must be finite");
-    st = check_ws(workspace, workspace_bytes, kStatusBytes + (kl_rows ? 0 : klrows_bytes(p)));
+    st = check_ws(workspace, workspace_bytes, kStatusBytes + (kl_rows ? 0 : klrows_bytes(p)) + kl_bytes(p));
     if (st != MSA_OK) return st;
     Carve cv{static_cast<char *>(workspace)};
     float *rows = kl_rows ? kl_rows : cv.take<float>((size_t)p.B * p.Hkv * p.Nq);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_kl_fwd(p, static_cast<const bf16 *>(q), static_cast<const bf16 *>(k),
-                                  static_cast<const bf16 *>(q_idx), static_cast<const bf16 *>(k_idx), sel_idx, lse,
-                                  lse_idx, rows, static_cast<DeviceStatus *>(workspace), s);
+    DeviceStatus *ds = static_cast<DeviceStatus *>(workspace);
+    cudaError_t e;
+    if (fwd_keymajor(p)) {
+        const size_t nbk = (size_t)p.B * p.Hkv * p.nb;
+        KlWork w;
+        w.part = cv.take<float4>((size_t)p.B * p.Hkv * p.Nq * p.topk * 4);
+        w.bucket_cnt = cv.take<int32_t>(nbk + 1);
+        w.bucket_off = cv.take<int32_t>(nbk + 1);
+        w.bucket_cur = cv.take<int32_t>(nbk + 1);
+        w.bucket_q = cv.take<int32_t>((size_t)p.B * p.Hkv * p.Nq * p.topk);
+        e = launch_kl_keymajor(p, static_cast<const bf16 *>(q), static_cast<const bf16 *>(k),
+                               static_cast<const bf16 *>(q_idx), static_cast<const bf16 *>(k_idx), sel_idx, lse,
+                               lse_idx, rows, w, ds, s);
+    } else {
+        e = launch_kl_fwd(p, static_cast<const bf16 *>(q), static_cast<const bf16 *>(k),
+                          static_cast<const bf16 *>(q_idx), static_cast<const bf16 *>(k_idx), sel_idx, lse, lse_idx,
+                          rows, ds, s);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "kl_fwd launch");
     e = launch_kl_reduce(p, rows, kl_coef, kl_loss, s);
     if (e != cudaSuccess) return cuda_fail(e, "kl_reduce launch");

@@ -88,7 +88,7 @@ __global__ void bucket_count_kernel(Problem p, const int32_t *__restrict__ sel, 
         const long long bri = x / p.topk;             // (b*Hkv + r)*Nq + i
         const int i = (int)(bri % p.Nq);
         const long long br = bri / p.Nq;
-        if (c >= p.nb || (long long)c * 128 > i) { report(st, kDevCheck, 51, c); continue; }
+        if (c >= p.nb || (long long)c * 128 > (long long)p.q_offset + i) { report(st, kDevCheck, 51, c); continue; }
         atomicAdd(&cnt[br * p.nb + c], 1);
     }
 }
@@ -128,7 +128,7 @@ __global__ void bucket_fill_kernel(Problem p, const int32_t *__restrict__ sel, c
         const long long bri = x / p.topk;
         const int i = (int)(bri % p.Nq);
         const long long br = bri / p.Nq;
-        if (c >= p.nb || (long long)c * 128 > i) continue;
+        if (c >= p.nb || (long long)c * 128 > (long long)p.q_offset + i) continue;
         const long long bucket = br * p.nb + c;
         const int slot = atomicAdd(&cur[bucket], 1);
         list[off[bucket] + slot] = i;
@@ -535,6 +535,23 @@ cudaError_t launch_main(const Problem &p, const bf16 *q, const bf16 *k, const bf
 
 }  // namespace
 
+cudaError_t launch_inverse_index(const Problem &p, const int32_t *sel, int32_t *cnt, int32_t *off, int32_t *cur,
+                                 int32_t *list, DeviceStatus *st, cudaStream_t s)
+{
+    cudaError_t e;
+    const long long nbk = (long long)p.B * p.Hkv * p.nb;
+    if ((e = cudaMemsetAsync(cnt, 0, (nbk + 1) * 4, s)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(cur, 0, (nbk + 1) * 4, s)) != cudaSuccess) return e;
+    const int grid_sel = 4 * p.num_sms;
+    bucket_count_kernel<<<grid_sel, 256, 0, s>>>(p, sel, cnt, st);
+    note_launch();
+    bucket_scan_kernel<<<1, 1024, 0, s>>>(cnt, off, (int)nbk);
+    note_launch();
+    bucket_fill_kernel<<<grid_sel, 256, 0, s>>>(p, sel, off, cur, list);
+    note_launch();
+    return cudaGetLastError();
+}
+
 cudaError_t launch_fused_bwd(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *v, const bf16 *o,
                              const bf16 *d_o, const float *lse, const bf16 *q_idx, const bf16 *k_idx,
                              const int32_t *sel, const float *lse_idx, float kl_coef, bf16 *dq, bf16 *dk, bf16 *dv,
@@ -548,20 +565,12 @@ cudaError_t launch_fused_bwd(const Problem &p, const bf16 *q, const bf16 *k, con
     if ((e = cudaMemsetAsync(w.dq_acc, 0, n_dq * 4, s)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(w.dqi_acc, 0, n_dqi * 4, s)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(w.dki_acc, 0, n_dki * 4, s)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(w.bucket_cnt, 0, (nbk + 1) * 4, s)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(w.bucket_cur, 0, (nbk + 1) * 4, s)) != cudaSuccess) return e;
 
     const long long rows = (long long)p.B * p.Nq * p.Hq;
     bwd_rowdot_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p, o, d_o, w.D);
     note_launch();
-    const int grid_sel = 4 * p.num_sms;
-    bucket_count_kernel<<<grid_sel, 256, 0, s>>>(p, sel, w.bucket_cnt, st);
-    note_launch();
-    bucket_scan_kernel<<<1, 1024, 0, s>>>(w.bucket_cnt, w.bucket_off, (int)nbk);
-    note_launch();
-    bucket_fill_kernel<<<grid_sel, 256, 0, s>>>(p, sel, w.bucket_off, w.bucket_cur, w.bucket_q);
-    note_launch();
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_inverse_index(p, sel, w.bucket_cnt, w.bucket_off, w.bucket_cur, w.bucket_q, st, s)) != cudaSuccess)
+        return e;
 
     if (p.d == 128 && p.d_idx == 128) e = launch_fused_bwd_tc_main(p, q, k, v, d_o, lse, q_idx, k_idx, lse_idx, kl_coef, w, dk, dv, st, s);
     else if (p.d == 128) e = launch_main<128, 64>(p, q, k, v, d_o, lse, q_idx, k_idx, lse_idx, kl_coef, w, dk, dv, s);

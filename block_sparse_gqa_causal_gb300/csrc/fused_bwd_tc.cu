@@ -47,7 +47,8 @@ constexpr int STG_DO = 8192;                     // dO:    2 x [32][64]
 constexpr int STG_QI = 16384;                    // q_idx: 2 x [16][64] (2 KB each)
 constexpr int STG_ROWS = 20480;
 constexpr int STG_BYTES = 21504;
-constexpr int OFF_BAR = OFF_STG + kStages * STG_BYTES;
+constexpr int OFF_RED = OFF_STG + kStages * STG_BYTES;   // fp32 staging [kNQ + kNQI][128] for the reductions
+constexpr int OFF_BAR = OFF_RED + (kNQ + kNQI) * D * 4;
 constexpr int SMEM_ALLOC = OFF_BAR + 512 + 1024;
 
 // TMEM columns
@@ -68,6 +69,17 @@ __device__ __forceinline__ int swz(int row, int ch) { return row * 128 + ((ch ^ 
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar)
 {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// qis[qq] for a runtime qq without spilling the array to local memory
+template <int N>
+__device__ __forceinline__ int qsel(const int (&qis)[N], int qq)
+{
+    int v = qis[0];
+#pragma unroll
+    for (int u = 1; u < N; ++u)
+        if (qq == u) v = qis[u];
+    return v;
 }
 
 template <int G>
@@ -100,7 +112,7 @@ fused_bwd_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restric
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             tc::mbar_init(&full[s], 64);                    // 32 cp.async arrivals + 32 row-data arrivals
-            tc::mbar_init(&empty[s], 1 + kEpiWarps);        // MMA commit + epilogue done with the rows
+            tc::mbar_init(&empty[s], 1 + kEpiWarps);        // grads MMAs done + epilogue has read the rows
         }
         tc::mbar_init(kv_full, 32);
         tc::mbar_init(s_full, 1);
@@ -144,40 +156,46 @@ fused_bwd_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restric
             StageRows *rows = reinterpret_cast<StageRows *>(stg + STG_ROWS);
             const int q0 = qbeg + m * QC;
             const int nq = min(QC, qend - q0);
-            // row data (plain stores, released by the plain arrival below)
+            // the chunk's query indices first (one global load each), then
+            // everything else addressed from shared memory
+            if (lane < kNQI) {
+                const bool okq = lane < nq;
+                rows->qi[lane] = okq ? bucket_q[q0 + lane] : 0;
+            }
+            if (lane == 0) rows->nq = nq;
+            __syncwarp();
             {
                 const int qq = lane / G, g = lane % G;
                 const bool ok = lane < QC * G && qq < nq;
-                const int i = ok ? bucket_q[q0 + qq] : 0;
+                const int i = rows->qi[qq < kNQI ? qq : 0];
                 const long long hi = ((long long)b * p.Hq + r * G + g) * p.Nq + i;
                 rows->lse2[lane] = ok ? lse[hi] * kLog2e : INFINITY;
                 rows->dd[lane] = ok ? Dg[hi] : 0.f;
                 if (lane < kNQI) {
                     const bool okq = lane < nq;
-                    const int iq = okq ? bucket_q[q0 + lane] : 0;
-                    rows->lsei2[lane] = okq ? lse_idx[((long long)b * p.Hkv + r) * p.Nq + iq] * kLog2e : INFINITY;
-                    rows->pos[lane] = okq ? iq : -1;     // training layout: q_offset == 0
-                    rows->qi[lane] = iq;
+                    rows->lsei2[lane] = okq ? lse_idx[((long long)b * p.Hkv + r) * p.Nq + rows->qi[lane]] * kLog2e
+                                            : INFINITY;
+                    rows->pos[lane] = okq ? rows->qi[lane] : -1;   // training layout: q_offset == 0
                 }
-                if (lane == 0) rows->nq = nq;
             }
-            // Q and dO rows: row rho = qq*G + g of the chunk
-            for (int idx = lane; idx < kNQ * 16; idx += 32) {
-                const int rho = idx >> 4, ch = idx & 15, h = ch >> 3, c8 = ch & 7;
+            // Q and dO rows (row rho = qq*G + g): 16 lanes per 256-byte row, 2 rows per step
+#pragma unroll 4
+            for (int it = 0; it < kNQ / 2; ++it) {
+                const int rho = it * 2 + (lane >> 4), ch = lane & 15;
                 const int qq = rho / G, g = rho % G;
                 const bool ok = rho < QC * G && qq < nq;
-                const int i = ok ? bucket_q[q0 + qq] : 0;
+                const int i = rows->qi[qq < kNQI ? qq : 0];
                 const long long off = (((long long)b * p.Nq + i) * p.Hq + (long long)r * G + g) * D + ch * 8;
-                const int o = h * (kNQ * 128) + swz(rho, c8);
+                const int o = (ch >> 3) * (kNQ * 128) + swz(rho, ch & 7);
                 cp_async16_zfill(stg + STG_Q + o, q + off, ok);
                 cp_async16_zfill(stg + STG_DO + o, d_o + off, ok);
             }
-            for (int idx = lane; idx < kNQI * 16; idx += 32) {
-                const int row = idx >> 4, ch = idx & 15, h = ch >> 3, c8 = ch & 7;
+#pragma unroll 4
+            for (int it = 0; it < kNQI / 2; ++it) {
+                const int row = it * 2 + (lane >> 4), ch = lane & 15;
                 const bool ok = row < nq;
-                const int i = ok ? bucket_q[q0 + row] : 0;
-                cp_async16_zfill(stg + STG_QI + h * (kNQI * 128) + swz(row, c8),
-                                 q_idx + (((long long)b * p.Nq + i) * p.Hkv + r) * DI + ch * 8, ok);
+                cp_async16_zfill(stg + STG_QI + (ch >> 3) * (kNQI * 128) + swz(row, ch & 7),
+                                 q_idx + (((long long)b * p.Nq + rows->qi[row]) * p.Hkv + r) * DI + ch * 8, ok);
             }
             cp_async_arrive_noinc(&full[s]);
             tc::mbar_arrive(&full[s]);
@@ -325,9 +343,17 @@ fused_bwd_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restric
             for (int c16 = 0; c16 < kNQI / 8; ++c16)
                 *reinterpret_cast<uint4 *>(sm + OFF_SIG + swz(kr, c16)) =
                     make_uint4(sg[c16 * 4], sg[c16 * 4 + 1], sg[c16 * 4 + 2], sg[c16 * 4 + 3]);
+            // keep what the reduction phase needs; the stage can then be refilled
+            const int nq = rows->nq;
+            int qis[QC];
+#pragma unroll
+            for (int u = 0; u < QC; ++u) qis[u] = rows->qi[u];
             tc::fence_proxy_async();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(p_full);
+            if (lane == 0) {
+                tc::mbar_arrive(p_full);
+                tc::mbar_arrive(&empty[n & 1]);
+            }
             // dQ^T, dQ_idx^T rows (this thread: feature kr)
             if (!tc::mbar_wait(dq_full, (uint32_t)n & 1u, st, 34, abort_flag)) { ok = false; break; }
             tc::fence_after_sync();
@@ -337,25 +363,34 @@ fused_bwd_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restric
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(dq_free);
-            const int nq = rows->nq;
+            // transpose this warp's 32 feature rows through shared memory so each
+            // reduction covers 16 contiguous bytes of one (query, head) row
+            float *red = reinterpret_cast<float *>(sm + OFF_RED) + quarter * ((kNQ + kNQI) * 32);
+            __syncwarp();
 #pragma unroll
-            for (int rr = 0; rr < kNQ; ++rr) {
+            for (int rr = 0; rr < kNQ; ++rr) red[rr * 32 + lane] = dqv[rr];
+#pragma unroll
+            for (int qq = 0; qq < kNQI; ++qq) red[(kNQ + qq) * 32 + lane] = dqiv[qq];
+            __syncwarp();
+            const int dbase = quarter * 32;
+            for (int x = lane; x < (QC * G) * 8; x += 32) {
+                const int rr = x >> 3, d4 = (x & 7) * 4;
                 const int qq = rr / G, g = rr % G;
-                if (qq < nq && rr < QC * G) {
-                    const int i = rows->qi[qq];
-                    red_add(dq_acc + (((long long)b * p.Nq + i) * p.Hq + (long long)r * G + g) * D + kr,
-                            p.scale * dqv[rr]);
+                if (qq < nq) {
+                    const float4 v4 = *reinterpret_cast<const float4 *>(red + rr * 32 + d4);
+                    atomicAdd(reinterpret_cast<float4 *>(dq_acc + (((long long)b * p.Nq + qsel(qis, qq)) * p.Hq +
+                                                                   (long long)r * G + g) * D + dbase + d4),
+                              make_float4(p.scale * v4.x, p.scale * v4.y, p.scale * v4.z, p.scale * v4.w));
                 }
             }
-#pragma unroll
-            for (int qq = 0; qq < kNQI; ++qq) {
-                if (qq < nq) {
-                    const int i = rows->qi[qq];
-                    red_add(dqi_acc + (((long long)b * p.Nq + i) * p.Hkv + r) * DI + kr, p.scale_idx * dqiv[qq]);
-                }
+            for (int x = lane; x < nq * 8; x += 32) {
+                const int qq = x >> 3, d4 = (x & 7) * 4;
+                const float4 v4 = *reinterpret_cast<const float4 *>(red + (kNQ + qq) * 32 + d4);
+                atomicAdd(reinterpret_cast<float4 *>(dqi_acc + (((long long)b * p.Nq + qsel(qis, qq)) * p.Hkv + r) * DI +
+                                                     dbase + d4),
+                          make_float4(p.scale_idx * v4.x, p.scale_idx * v4.y, p.scale_idx * v4.z, p.scale_idx * v4.w));
             }
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&empty[n & 1]);
         }
         // ---- dK, dV (owned) and dK_idx (shared by the groups) of this key
         if (ok && key_ok) {

@@ -1,0 +1,395 @@
+// kl_tc.cu -- KL alignment loss of MSA, key-major on the tcgen05 tensor cores.
+//
+// "Sparse Attention · Part II", section 3.2 (the L_KL equation): for query i
+// and group r over the selected token set T, with the detached teacher
+// Pt_j = (1/G) sum_h exp(l_{h,j} - lse_h) and the student Ps = softmax_T(s),
+//   KL = sum_j Pt_j log Pt_j - sum_j Pt_j s_j + log sum_j exp(s_j).
+// Every term is a sum over T, so it splits over the selected blocks.  As in
+// the key-major forward, one CTA keeps one 128-token block of K and K_idx of
+// one group on chip and takes the queries that selected it 128 (query, head)
+// rows at a time:
+//   S^T = K Q^T   (M = 128 keys, N = 128 (query, head) columns)
+//   s^T = K_idx q_idx^T   (M = 128 keys, N = the chunk's queries)
+// With keys on TMEM lanes, the teacher's average over the G heads of a query
+// is a sum of G adjacent columns inside one thread; each warp then reduces
+// its 32 keys and writes, per (query, group, selected block, warp),
+//   (sum Pt log2 Pt, sum Pt s2, max s2, sum 2^(s2 - max s2))   (s2 = s log2 e)
+// and a combine kernel folds a row's partials in a fixed order, so the loss
+// is reproducible and nothing is accumulated with atomics.
+#include "msa_internal.h"
+#include "tc.cuh"
+
+namespace msa {
+namespace {
+
+constexpr int kRows = 128;          // (query, head) columns per chunk
+constexpr int kKeys = 128;
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int SUB = 128 * 128;
+
+struct KlMeta {
+    int i[kRows];
+    int pos[kRows];
+    int slot[kRows];
+    float lse2[kRows];              // per (query, head) column: forward lse * log2(e)
+    int nq;
+};
+
+template <int D, int DI, int G>
+struct KlLayout {
+    static constexpr int QPC = kRows / G;                   // queries per chunk
+    static constexpr int NS = QPC < 16 ? 16 : QPC;          // index columns (MMA N >= 16)
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_KI = OFF_K + (D / 64) * SUB;
+    static constexpr int OFF_Q = OFF_KI + (DI / 64) * SUB;                  // 2 stages
+    static constexpr int QI_ROWS_BYTES = NS * 128;                          // one [NS][64] sub-tile
+    static constexpr int OFF_QI = OFF_Q + 2 * (D / 64) * SUB;               // 2 stages x DI/64 sub-tiles
+    static constexpr int OFF_META = OFF_QI + 2 * (DI / 64) * ((QI_ROWS_BYTES + 1023) & ~1023);
+    static constexpr int META_BYTES = (int)((sizeof(KlMeta) + 255) & ~size_t(255));
+    static constexpr int OFF_BAR = OFF_META + 2 * META_BYTES;
+    static constexpr int ALLOC = OFF_BAR + 256 + 1024;
+    static constexpr int QI_SUB = (QI_ROWS_BYTES + 1023) & ~1023;         // stride of q_idx sub-tiles
+    static constexpr uint32_t TM_S = 0, TM_SI = 256;
+};
+
+__device__ __forceinline__ int swz(int row, int ch) { return row * 128 + ((ch ^ (row & 7)) << 4); }
+
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Resolves the chunk's queries once: index, position and the slot of block c
+// in the query's selection (all loads issued before any is consumed).
+__device__ __forceinline__ void fill_meta(int *mi, int *mpos, int *mslot, int qpc, int nq, int q0,
+                                          const int32_t *__restrict__ bucket_q, const int32_t *__restrict__ sel,
+                                          const Problem &p, int b, int r, int c, int lane)
+{
+    for (int qq = lane; qq < qpc; qq += 32) {
+        int i = 0, pos = -1, slot = 0;
+        if (qq < nq) {
+            i = bucket_q[q0 + qq];
+            pos = p.q_offset + i;
+            const int32_t *srow = sel + (((long long)b * p.Hkv + r) * p.Nq + i) * p.topk;
+            int v[32];
+#pragma unroll
+            for (int t = 0; t < 32; ++t) v[t] = t < p.topk ? __ldg(srow + t) : -1;
+#pragma unroll
+            for (int t = 0; t < 32; ++t)
+                if (v[t] == c) slot = t;
+        }
+        mi[qq] = i;
+        mpos[qq] = pos;
+        mslot[qq] = slot;
+    }
+}
+
+template <int D, int DI, int G>
+__global__ void __launch_bounds__(kThreads, 1)
+kl_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 *__restrict__ q_idx,
+             const bf16 *__restrict__ k_idx, const int32_t *__restrict__ sel, const float *__restrict__ lse,
+             const int32_t *__restrict__ bucket_off, const int32_t *__restrict__ bucket_q,
+             float4 *__restrict__ part, DeviceStatus *st)
+{
+    using L = KlLayout<D, DI, G>;
+    constexpr int QPC = L::QPC, NS = L::NS;
+    const int c = blockIdx.x, r = blockIdx.y, b = blockIdx.z;
+    const long long bucket = ((long long)b * p.Hkv + r) * p.nb + c;
+    const int qbeg = bucket_off[bucket], qend = bucket_off[bucket + 1];
+    if (qend <= qbeg) return;
+    const int nch = (qend - qbeg + QPC - 1) / QPC;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
+    uint64_t *q_full = bars, *q_empty = bars + 2, *s_full = bars + 4, *s_free = bars + 6, *kv_full = bars + 8;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 9);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long j0 = (long long)c * kKeys;
+
+    if (threadIdx.x == 0) {
+        for (int a = 0; a < 2; ++a) {
+            tc::mbar_init(&q_full[a], 64);
+            tc::mbar_init(&q_empty[a], 1 + kEpiWarps);
+            tc::mbar_init(&s_full[a], 1);
+            tc::mbar_init(&s_free[a], kEpiWarps);
+        }
+        tc::mbar_init(kv_full, 32);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, 512);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ producer
+        const long long jstride = (long long)p.Hkv * D;
+        const bf16 *kb = k + ((long long)b * p.kv_rows * p.Hkv + r) * D;
+        const bf16 *kib = k_idx + (long long)b * p.kv_rows * DI;
+        for (int idx = lane; idx < kKeys * (D / 8); idx += 32) {
+            const int row = idx / (D / 8), ch = idx % (D / 8);
+            const bool ok = j0 + row < p.Nk;
+            const long long j = ok ? j0 + row : j0;
+            cp_async16_zfill(sm + L::OFF_K + (ch >> 3) * SUB + swz(row, ch & 7), kb + j * jstride + ch * 8, ok);
+        }
+        for (int idx = lane; idx < kKeys * (DI / 8); idx += 32) {
+            const int row = idx / (DI / 8), ch = idx % (DI / 8);
+            const bool ok = j0 + row < p.Nk;
+            const long long j = ok ? j0 + row : j0;
+            cp_async16_zfill(sm + L::OFF_KI + (ch >> 3) * SUB + swz(row, ch & 7), kib + j * DI + ch * 8, ok);
+        }
+        cp_async_arrive_noinc(kv_full);
+        for (int m = 0; m < nch; ++m) {
+            const int a = m & 1;
+            if (!tc::mbar_wait(&q_empty[a], ((uint32_t)(m >> 1) & 1u) ^ 1u, st, 81, abort_flag)) break;
+            KlMeta *meta = reinterpret_cast<KlMeta *>(sm + L::OFF_META + a * L::META_BYTES);
+            const int q0 = qbeg + m * QPC;
+            const int nq = min(QPC, qend - q0);
+            fill_meta(meta->i, meta->pos, meta->slot, QPC, nq, q0, bucket_q, sel, p, b, r, c, lane);
+            if (lane == 0) meta->nq = nq;
+            __syncwarp();
+            for (int rho = lane; rho < kRows; rho += 32) {
+                const int qq = rho / G, g = rho % G;
+                meta->lse2[rho] = qq < nq ? lse[((long long)b * p.Hq + r * G + g) * p.Nq + meta->i[qq]] * kLog2e
+                                          : INFINITY;
+            }
+            uint8_t *sq = sm + L::OFF_Q + a * ((D / 64) * SUB);
+            {
+                constexpr int CPR = D / 8, RPI = 32 / CPR;
+#pragma unroll 8
+                for (int it = 0; it < kRows / RPI; ++it) {
+                    const int rho = it * RPI + lane / CPR, ch = lane % CPR;
+                    const int qq = rho / G, g = rho % G;
+                    cp_async16_zfill(sq + (ch >> 3) * SUB + swz(rho, ch & 7),
+                                     q + (((long long)b * p.Nq + meta->i[qq]) * p.Hq + (long long)r * G + g) * D + ch * 8,
+                                     qq < nq);
+                }
+            }
+            uint8_t *sqi = sm + L::OFF_QI + a * ((DI / 64) * L::QI_SUB);
+            {
+                constexpr int CPR = DI / 8, RPI = 32 / CPR;
+#pragma unroll 4
+                for (int it = 0; it < NS / RPI; ++it) {
+                    const int row = it * RPI + lane / CPR, ch = lane % CPR;
+                    const bool ok = row < nq;
+                    cp_async16_zfill(sqi + (ch >> 3) * L::QI_SUB + swz(row, ch & 7),
+                                     q_idx + (((long long)b * p.Nq + (ok ? meta->i[row] : 0)) * p.Hkv + r) * DI + ch * 8,
+                                     ok);
+                }
+            }
+            cp_async_arrive_noinc(&q_full[a]);
+            tc::mbar_arrive(&q_full[a]);
+        }
+        cp_async_wait<0>();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            constexpr uint32_t I_S = tc::idesc_bf16(128, kRows);
+            constexpr uint32_t I_SI = tc::idesc_bf16(128, NS);
+            const uint32_t aK = smem_u32(sm + L::OFF_K), aKI = smem_u32(sm + L::OFF_KI);
+            bool ok = tc::mbar_wait(kv_full, 0, st, 82, abort_flag);
+            if (ok) tc::fence_proxy_async();
+            int issued = 0;
+            for (int n = 0; ok && n < nch; ++n) {
+                const int a = n & 1;
+                const uint32_t ph = (uint32_t)(n >> 1) & 1u;
+                if (!tc::mbar_wait(&q_full[a], ph, st, 83, abort_flag)) break;
+                if (!tc::mbar_wait(&s_free[a], ph ^ 1u, st, 84, abort_flag)) break;
+                tc::fence_proxy_async();
+                tc::fence_after_sync();
+                const uint32_t aQ = smem_u32(sm + L::OFF_Q + a * ((D / 64) * SUB));
+                const uint32_t aQI = smem_u32(sm + L::OFF_QI + a * ((DI / 64) * L::QI_SUB));
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks >> 2) * SUB + (ks & 3) * 32;
+                    tc::mma_bf16(tmem + L::TM_S + a * 128, tc::sdesc_k128(aK + off), tc::sdesc_k128(aQ + off), I_S,
+                                 ks > 0);
+                }
+#pragma unroll
+                for (int ks = 0; ks < DI / 16; ++ks) {
+                    tc::mma_bf16(tmem + L::TM_SI + a * 128, tc::sdesc_k128(aKI + (ks >> 2) * SUB + (ks & 3) * 32),
+                                 tc::sdesc_k128(aQI + (ks >> 2) * L::QI_SUB + (ks & 3) * 32), I_SI, ks > 0);
+                }
+                tc::mma_commit(&s_full[a]);
+                tc::mma_commit(&q_empty[a]);
+                issued = n + 1;
+            }
+            if (*abort_flag && issued > 0) {
+                const int m = issued - 1;
+                tc::mbar_wait(&s_full[m & 1], (uint32_t)(m >> 1) & 1u, nullptr, 0, nullptr);
+            }
+        }
+    } else {
+        // ------------------------------------------------ epilogue: one key per thread
+        const int quarter = warp & 3;
+        const int kr = quarter * 32 + lane;
+        const long long j = j0 + kr;
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const float sl2 = p.scale * kLog2e, si2 = p.scale_idx * kLog2e;
+        const float invG = 1.f / (float)G;
+        for (int n = 0; n < nch; ++n) {
+            const int a = n & 1;
+            const uint32_t ph = (uint32_t)(n >> 1) & 1u;
+            const KlMeta *meta = reinterpret_cast<const KlMeta *>(sm + L::OFF_META + a * L::META_BYTES);
+            if (!tc::mbar_wait(&q_full[a], ph, st, 91, abort_flag)) break;
+            if (!tc::mbar_wait(&s_full[a], ph, st, 92, abort_flag)) break;
+            tc::fence_after_sync();
+            const int nq = meta->nq;
+            // queries in groups of 32 / G per 32-column TMEM slice
+            constexpr int QS = (32 / G) > 0 ? 32 / G : 1;   // queries per slice
+#pragma unroll
+            for (int c32 = 0; c32 < kRows / 32; ++c32) {
+                float sv[32], si[32];
+                tc::tmem_ld32(tmem + lane_base + L::TM_S + a * 128 + c32 * 32, sv);
+                if (c32 * QS < NS) tc::tmem_ld32(tmem + lane_base + L::TM_SI + a * 128 + (c32 * QS / 32) * 32, si);
+                // per-key terms of every query in this slice, then all queries'
+                // warp reductions advanced together (independent shuffle chains)
+                float A[QS], Bv[QS], Mx[QS], s2v[QS];
+                bool visq[QS];
+#pragma unroll
+                for (int u = 0; u < QS; ++u) {
+                    const int qq = c32 * QS + u;
+                    const bool vis = qq < nq && j <= meta->pos[qq] && j < p.Nk;
+                    float pt = 0.f;
+#pragma unroll
+                    for (int g = 0; g < G; ++g)
+                        pt += vis ? exp2f(sv[u * G + g] * sl2 - meta->lse2[qq * G + g]) : 0.f;
+                    pt *= invG;
+                    const float s2 = vis ? si[qq & 31] * si2 : -INFINITY;
+                    A[u] = pt > 0.f ? pt * log2f(pt) : 0.f;
+                    Bv[u] = vis ? pt * s2 : 0.f;
+                    Mx[u] = s2;
+                    s2v[u] = s2;
+                    visq[u] = vis;
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+                    for (int u = 0; u < QS; ++u) {
+                        A[u] += __shfl_xor_sync(0xffffffffu, A[u], o);
+                        Bv[u] += __shfl_xor_sync(0xffffffffu, Bv[u], o);
+                        Mx[u] = fmaxf(Mx[u], __shfl_xor_sync(0xffffffffu, Mx[u], o));
+                    }
+                }
+                float Z[QS];
+#pragma unroll
+                for (int u = 0; u < QS; ++u) Z[u] = (visq[u] && Mx[u] != -INFINITY) ? exp2f(s2v[u] - Mx[u]) : 0.f;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+                    for (int u = 0; u < QS; ++u) Z[u] += __shfl_xor_sync(0xffffffffu, Z[u], o);
+                }
+                // lane u writes query u of the slice
+#pragma unroll
+                for (int u = 0; u < QS; ++u) {
+                    const int qq = c32 * QS + u;
+                    if (lane == (u & 31) && qq < nq) {
+                        const long long row = ((long long)b * p.Hkv + r) * p.Nq + meta->i[qq];
+                        part[(row * p.topk + meta->slot[qq]) * kEpiWarps + quarter] = make_float4(A[u], Bv[u], Mx[u], Z[u]);
+                    }
+                }
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                tc::mbar_arrive(&s_free[a]);
+                tc::mbar_arrive(&q_empty[a]);
+            }
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+// Thread per (b, r, i): fold the row's partials (slots in order, then warps).
+__global__ void kl_combine_kernel(Problem p, const int32_t *__restrict__ sel, const float4 *__restrict__ part,
+                                  float *__restrict__ lse_idx, float *__restrict__ kl_rows)
+{
+    const long long row = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (row >= (long long)p.B * p.Hkv * p.Nq) return;
+    const int i = (int)(row % p.Nq);
+    const long long pos = (long long)p.q_offset + i;
+    const int32_t *srow = sel + row * p.topk;
+    float A = 0.f, Bv = 0.f, M = -INFINITY;
+    for (int t = 0; t < p.topk; ++t) {
+        const int cc = srow[t];
+        if (cc < 0 || cc >= p.nb || (long long)cc * 128 > pos) continue;
+        for (int w = 0; w < kEpiWarps; ++w) {
+            const float4 v = part[(row * p.topk + t) * kEpiWarps + w];
+            A += v.x;
+            Bv += v.y;
+            M = fmaxf(M, v.z);
+        }
+    }
+    float Z = 0.f;
+    for (int t = 0; t < p.topk; ++t) {
+        const int cc = srow[t];
+        if (cc < 0 || cc >= p.nb || (long long)cc * 128 > pos) continue;
+        for (int w = 0; w < kEpiWarps; ++w) {
+            const float4 v = part[(row * p.topk + t) * kEpiWarps + w];
+            if (v.w > 0.f) Z += v.w * exp2f(v.z - M);
+        }
+    }
+    const float lse2 = M + log2f(Z);
+    lse_idx[row] = lse2 * kLn2;
+    kl_rows[row] = (A - Bv + lse2) * kLn2;
+}
+
+template <int D, int DI, int G>
+cudaError_t launch_ddg(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *q_idx, const bf16 *k_idx,
+                       const int32_t *sel, const float *lse, const KlWork &w, DeviceStatus *st, cudaStream_t s)
+{
+    using L = KlLayout<D, DI, G>;
+    cudaError_t e = cudaFuncSetAttribute(kl_tc_kernel<D, DI, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+    if (e != cudaSuccess) return e;
+    kl_tc_kernel<D, DI, G><<<dim3(p.nb, p.Hkv, p.B), kThreads, L::ALLOC, s>>>(p, q, k, q_idx, k_idx, sel, lse,
+                                                                             w.bucket_off, w.bucket_q, w.part, st);
+    note_launch();
+    return cudaGetLastError();
+}
+
+template <int D, int DI>
+cudaError_t launch_dd(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *q_idx, const bf16 *k_idx,
+                      const int32_t *sel, const float *lse, const KlWork &w, DeviceStatus *st, cudaStream_t s)
+{
+    switch (p.G) {
+    case 1: return launch_ddg<D, DI, 1>(p, q, k, q_idx, k_idx, sel, lse, w, st, s);
+    case 2: return launch_ddg<D, DI, 2>(p, q, k, q_idx, k_idx, sel, lse, w, st, s);
+    case 4: return launch_ddg<D, DI, 4>(p, q, k, q_idx, k_idx, sel, lse, w, st, s);
+    default: return launch_ddg<D, DI, 8>(p, q, k, q_idx, k_idx, sel, lse, w, st, s);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_kl_keymajor(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *q_idx, const bf16 *k_idx,
+                               const int32_t *sel, const float *lse, float *lse_idx, float *kl_rows, const KlWork &w,
+                               DeviceStatus *st, cudaStream_t s)
+{
+    cudaError_t e = launch_inverse_index(p, sel, w.bucket_cnt, w.bucket_off, w.bucket_cur, w.bucket_q, st, s);
+    if (e != cudaSuccess) return e;
+    if (p.d == 128 && p.d_idx == 128) e = launch_dd<128, 128>(p, q, k, q_idx, k_idx, sel, lse, w, st, s);
+    else if (p.d == 128) e = launch_dd<128, 64>(p, q, k, q_idx, k_idx, sel, lse, w, st, s);
+    else if (p.d_idx == 128) e = launch_dd<64, 128>(p, q, k, q_idx, k_idx, sel, lse, w, st, s);
+    else e = launch_dd<64, 64>(p, q, k, q_idx, k_idx, sel, lse, w, st, s);
+    if (e != cudaSuccess) return e;
+    const long long rows = (long long)p.B * p.Hkv * p.Nq;
+    kl_combine_kernel<<<(unsigned)((rows + 255) / 256), 256, 0, s>>>(p, sel, w.part, lse_idx, kl_rows);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace msa

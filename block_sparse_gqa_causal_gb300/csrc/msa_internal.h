@@ -35,7 +35,16 @@ cudaError_t launch_index_scores(const Problem &p, const bf16 *q_idx, const bf16 
 // Top-k block selection from block scores.  sel: [B, Hkv, Nq, topk].
 cudaError_t launch_block_topk(const Problem &p, const float *bs, int32_t *sel, DeviceStatus *st,
                               cudaStream_t s);
-// Main branch forward.
+// Key-major main branch forward (many queries per selected block).
+struct FwdWork {
+    bf16 *part;          // [B, Nq, Hq, topk, d] unnormalised partial outputs per selected block
+    float2 *stats;       // [B, Nq, Hq, topk] (row max in log2 units, row sum)
+    int32_t *bucket_cnt, *bucket_off, *bucket_cur, *bucket_q;
+};
+cudaError_t launch_sparse_fwd_keymajor(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *v,
+                                       const int32_t *sel, bf16 *o, float *lse, const FwdWork &w, DeviceStatus *st,
+                                       cudaStream_t s);
+// Main branch forward (query-major; few queries per selected block, e.g. decode).
 cudaError_t launch_sparse_attn_fwd(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *v,
                                    const int32_t *sel, bf16 *o, float *lse, DeviceStatus *st,
                                    cudaStream_t s);
@@ -43,6 +52,14 @@ cudaError_t launch_sparse_attn_fwd(const Problem &p, const bf16 *q, const bf16 *
 cudaError_t launch_kl_fwd(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *q_idx,
                           const bf16 *k_idx, const int32_t *sel, const float *lse, float *lse_idx,
                           float *kl_rows, DeviceStatus *st, cudaStream_t s);
+// Key-major KL forward (many queries per selected block).
+struct KlWork {
+    float4 *part;        // [B, Hkv, Nq, topk, 4] per-warp partial sums
+    int32_t *bucket_cnt, *bucket_off, *bucket_cur, *bucket_q;
+};
+cudaError_t launch_kl_keymajor(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *q_idx, const bf16 *k_idx,
+                               const int32_t *sel, const float *lse, float *lse_idx, float *kl_rows, const KlWork &w,
+                               DeviceStatus *st, cudaStream_t s);
 cudaError_t launch_kl_reduce(const Problem &p, const float *kl_rows, float kl_coef, float *kl_loss,
                              cudaStream_t s);
 
@@ -62,6 +79,11 @@ cudaError_t launch_fused_bwd(const Problem &p, const bf16 *q, const bf16 *k, con
                              const bf16 *k_idx, const int32_t *sel, const float *lse_idx,
                              float kl_coef, bf16 *dq, bf16 *dk, bf16 *dv, bf16 *dq_idx,
                              bf16 *dk_idx, const BwdWork &w, DeviceStatus *st, cudaStream_t s);
+
+// Inverse index: for every (b, group, block) the query rows that selected
+// it (count, exclusive scan into off[0..nbk], fill).  cnt / cur are zeroed here.
+cudaError_t launch_inverse_index(const Problem &p, const int32_t *sel, int32_t *cnt, int32_t *off, int32_t *cur,
+                                 int32_t *list, DeviceStatus *st, cudaStream_t s);
 
 // tcgen05 main backward kernel (d = d_idx = 128); the prep kernels run first.
 cudaError_t launch_fused_bwd_tc_main(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *v, const bf16 *d_o,

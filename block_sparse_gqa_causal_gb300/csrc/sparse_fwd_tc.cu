@@ -1,0 +1,441 @@
+// sparse_fwd_tc.cu -- main branch of MSA, key-major on the tcgen05 tensor cores.
+//
+// "Sparse Attention · Part II", section 3.2: each query head of a group
+// attends, with its own logits, to the visible tokens of the blocks selected
+// for (query, group), normalised over that set only.  Selection is per query,
+// so neighbouring queries pick mostly different blocks; gathering K/V per
+// query would move K+V of 16 blocks for every (query, group).  Instead the
+// work is grouped by key block (the varlen view of block-sparse attention
+// the MSA training-kernel write-up borrows from MoBA): one CTA keeps one
+// 128-token K/V block of one group on chip and runs full 128 x 128 tiles over
+// the (query, head) rows of every query that selected it:
+//   S = Q K^T (M = 128 rows, N = 128 keys),  P = exp2(S - m) (row max m),
+//   O_c = P V (unnormalised),  z = rowsum(P)
+// and writes O_c (bf16) with (m, z) for that (query, head, slot).  A combine
+// kernel then merges a row's slots exactly like a split-KV flash decode:
+//   M = max m_c,  O = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) z_c,
+//   lse = (M + log2 sum_c 2^(m_c - M) z_c) ln 2.
+//
+// Roles: warp 0 gathers Q rows with cp.async (+ mbarrier arrivals), warp 1
+// owns TMEM and issues the MMAs, warps 2..5 (one row each) do the softmax and
+// write the partials.  S and O accumulators are double-buffered in TMEM so
+// the S MMA of chunk n overlaps the epilogue of chunk n-1.
+#include "msa_internal.h"
+#include "tc.cuh"
+
+namespace msa {
+namespace {
+
+constexpr int kRows = 128;                  // (query, head) rows per chunk
+constexpr int kKeys = 128;
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int SUB = 128 * 128;              // [128 rows][64 bf16] swizzled sub-tile
+
+template <int D>
+struct FwdLayout {
+    static constexpr int KB = D / 64;
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = OFF_K + KB * SUB;
+    static constexpr int OFF_Q = OFF_V + KB * SUB;          // 2 stages x KB sub-tiles
+    static constexpr int OFF_P = OFF_Q + 2 * KB * SUB;      // 2 buffers x 2 sub-tiles (128 keys)
+    static constexpr int OFF_META = OFF_P + 2 * 2 * SUB;    // 2 stages x QueryMeta
+    static constexpr int OFF_BAR = OFF_META + 2 * 2048;
+    static constexpr int ALLOC = OFF_BAR + 256 + 1024;
+    static constexpr uint32_t TM_S = 0;                     // 2 x 128 columns
+    static constexpr uint32_t TM_O = 256;                   // 2 x D columns
+};
+
+struct QueryMeta {         // per chunk, per query slot of the chunk (<= 128 queries)
+    int i[kRows];          // query index
+    int pos[kRows];        // absolute position
+    int slot[kRows];       // position of this block in the query's selection
+    int nq;
+};
+
+__device__ __forceinline__ int swz(int row, int ch) { return row * 128 + ((ch ^ (row & 7)) << 4); }
+
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Resolves the chunk's queries once: index, position and the slot of block c
+// in the query's selection (all loads issued before any is consumed).
+__device__ __forceinline__ void fill_meta(int *mi, int *mpos, int *mslot, int qpc, int nq, int q0,
+                                          const int32_t *__restrict__ bucket_q, const int32_t *__restrict__ sel,
+                                          const Problem &p, int b, int r, int c, int lane)
+{
+    for (int qq = lane; qq < qpc; qq += 32) {
+        int i = 0, pos = -1, slot = 0;
+        if (qq < nq) {
+            i = bucket_q[q0 + qq];
+            pos = p.q_offset + i;
+            const int32_t *srow = sel + (((long long)b * p.Hkv + r) * p.Nq + i) * p.topk;
+            int v[32];
+#pragma unroll
+            for (int t = 0; t < 32; ++t) v[t] = t < p.topk ? __ldg(srow + t) : -1;
+#pragma unroll
+            for (int t = 0; t < 32; ++t)
+                if (v[t] == c) slot = t;
+        }
+        mi[qq] = i;
+        mpos[qq] = pos;
+        mslot[qq] = slot;
+    }
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads, 1)
+sparse_fwd_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 *__restrict__ v,
+                     const int32_t *__restrict__ sel, const int32_t *__restrict__ bucket_off,
+                     const int32_t *__restrict__ bucket_q, bf16 *__restrict__ part, float2 *__restrict__ stats,
+                     DeviceStatus *st)
+{
+    using L = FwdLayout<D>;
+    constexpr int QPC = kRows / G;                          // queries per chunk
+    const int c = blockIdx.x, r = blockIdx.y, b = blockIdx.z;
+    const long long bucket = ((long long)b * p.Hkv + r) * p.nb + c;
+    const int qbeg = bucket_off[bucket], qend = bucket_off[bucket + 1];
+    if (qend <= qbeg) return;                               // nobody selected this block
+    const int nch = (qend - qbeg + QPC - 1) / QPC;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
+    uint64_t *q_full = bars, *q_empty = bars + 2, *s_full = bars + 4, *s_free = bars + 6;
+    uint64_t *p_full = bars + 8, *p_free = bars + 10, *o_full = bars + 12, *o_free = bars + 14;
+    uint64_t *kv_full = bars + 16;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 17);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long j0 = (long long)c * kKeys;
+
+    if (threadIdx.x == 0) {
+        for (int a = 0; a < 2; ++a) {
+            tc::mbar_init(&q_full[a], 64);              // 32 cp.async arrivals + 32 metadata arrivals
+            tc::mbar_init(&q_empty[a], 1 + kEpiWarps);  // S MMAs done + epilogue has read the metadata
+            tc::mbar_init(&s_full[a], 1);
+            tc::mbar_init(&s_free[a], kEpiWarps);
+            tc::mbar_init(&p_full[a], kEpiWarps);
+            tc::mbar_init(&p_free[a], 1);
+            tc::mbar_init(&o_full[a], 1);
+            tc::mbar_init(&o_free[a], kEpiWarps);
+        }
+        tc::mbar_init(kv_full, 32);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, 512);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ producer
+        const long long jstride = (long long)p.Hkv * D;
+        const bf16 *kb = k + ((long long)b * p.kv_rows * p.Hkv + r) * D;
+        const bf16 *vb = v + ((long long)b * p.kv_rows * p.Hkv + r) * D;
+        for (int idx = lane; idx < kKeys * (D / 8); idx += 32) {
+            const int row = idx / (D / 8), ch = idx % (D / 8);
+            const bool ok = j0 + row < p.Nk;
+            const long long j = ok ? j0 + row : j0;
+            const int o = (ch >> 3) * SUB + swz(row, ch & 7);
+            cp_async16_zfill(sm + L::OFF_K + o, kb + j * jstride + ch * 8, ok);
+            cp_async16_zfill(sm + L::OFF_V + o, vb + j * jstride + ch * 8, ok);
+        }
+        cp_async_arrive_noinc(kv_full);
+        for (int m = 0; m < nch; ++m) {
+            const int a = m & 1;
+            if (!tc::mbar_wait(&q_empty[a], ((uint32_t)(m >> 1) & 1u) ^ 1u, st, 61, abort_flag)) break;
+            QueryMeta *meta = reinterpret_cast<QueryMeta *>(sm + L::OFF_META + a * 2048);
+            const int q0 = qbeg + m * QPC;
+            const int nq = min(QPC, qend - q0);
+            fill_meta(meta->i, meta->pos, meta->slot, QPC, nq, q0, bucket_q, sel, p, b, r, c, lane);
+            if (lane == 0) meta->nq = nq;
+            __syncwarp();
+            // Q rows: lanes cover whole 16-byte chunks of consecutive rows; the
+            // query index comes from the metadata just written (shared memory)
+            uint8_t *sq = sm + L::OFF_Q + a * (L::KB * SUB);
+            constexpr int CPR = D / 8;                     // 16-byte chunks per row
+            constexpr int RPI = 32 / CPR;                  // rows per iteration
+#pragma unroll 8
+            for (int it = 0; it < kRows / RPI; ++it) {
+                const int rho = it * RPI + lane / CPR, ch = lane % CPR;
+                const int qq = rho / G, g = rho % G;
+                const bool ok = qq < nq;
+                const int i = meta->i[qq];
+                cp_async16_zfill(sq + (ch >> 3) * SUB + swz(rho, ch & 7),
+                                 q + (((long long)b * p.Nq + i) * p.Hq + (long long)r * G + g) * D + ch * 8, ok);
+            }
+            cp_async_arrive_noinc(&q_full[a]);
+            tc::mbar_arrive(&q_full[a]);
+        }
+        cp_async_wait<0>();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            constexpr uint32_t I_S = tc::idesc_bf16(128, kKeys);
+            constexpr uint32_t I_O = tc::idesc_bf16(128, D) | tc::kBMajorMN;
+            const uint32_t aK = smem_u32(sm + L::OFF_K), aV = smem_u32(sm + L::OFF_V);
+            bool ok = tc::mbar_wait(kv_full, 0, st, 62, abort_flag);
+            if (ok) tc::fence_proxy_async();
+            int issued = 0;
+            for (int n = 0; ok && n <= nch; ++n) {
+                if (n < nch) {
+                    const int a = n & 1;
+                    const uint32_t ph = (uint32_t)(n >> 1) & 1u;
+                    if (!tc::mbar_wait(&q_full[a], ph, st, 63, abort_flag)) break;
+                    if (!tc::mbar_wait(&s_free[a], ph ^ 1u, st, 64, abort_flag)) break;
+                    tc::fence_proxy_async();
+                    tc::fence_after_sync();
+                    const uint32_t aQ = smem_u32(sm + L::OFF_Q + a * (L::KB * SUB));
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint32_t off = (ks >> 2) * SUB + (ks & 3) * 32;
+                        tc::mma_bf16(tmem + L::TM_S + a * 128, tc::sdesc_k128(aQ + off), tc::sdesc_k128(aK + off), I_S,
+                                     ks > 0);
+                    }
+                    tc::mma_commit(&s_full[a]);
+                    tc::mma_commit(&q_empty[a]);
+                }
+                if (n >= 1) {
+                    const int m = n - 1, a = m & 1;
+                    const uint32_t ph = (uint32_t)(m >> 1) & 1u;
+                    if (!tc::mbar_wait(&p_full[a], ph, st, 65, abort_flag)) break;
+                    if (!tc::mbar_wait(&o_free[a], ph ^ 1u, st, 66, abort_flag)) break;
+                    tc::fence_after_sync();
+                    const uint32_t aP = smem_u32(sm + L::OFF_P + a * (2 * SUB));
+#pragma unroll
+                    for (int ks = 0; ks < kKeys / 16; ++ks) {
+                        // A = P [rows][keys] K-major; B = V [keys][d] read MN-major (atoms of 64 d, 8-key groups)
+                        tc::mma_bf16(tmem + L::TM_O + a * D,
+                                     tc::sdesc_k128(aP + (ks >> 2) * SUB + (ks & 3) * 32),
+                                     tc::sdesc_sw128(aV + ks * 2048, SUB, 1024), I_O, ks > 0);
+                    }
+                    tc::mma_commit(&o_full[a]);
+                    tc::mma_commit(&p_free[a]);
+                    issued = n;
+                }
+            }
+            if (*abort_flag && issued > 0) {
+                const int m = issued - 1;
+                tc::mbar_wait(&o_full[m & 1], (uint32_t)(m >> 1) & 1u, nullptr, 0, nullptr);
+            }
+        }
+    } else {
+        // ------------------------------------------------ epilogue: one (query, head) row per thread
+        const int quarter = warp & 3;
+        const int rho = quarter * 32 + lane;
+        const int qq = rho / G, g = rho % G;
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const float sl2 = p.scale * kLog2e;
+        float pm = 0.f, pz = 0.f;            // (m, z) of the chunk whose output is pending
+        int pi = 0, pslot = 0;
+        bool pvalid = false;
+        bool ok = true;
+        // writes the partial output of chunk m (row data held in pm, pz, pi, pslot, pvalid)
+        auto emit = [&](int m) -> bool {
+            const int am = m & 1;
+            if (!tc::mbar_wait(&o_full[am], (uint32_t)(m >> 1) & 1u, st, 74, abort_flag)) return false;
+            tc::fence_after_sync();
+            const long long row = (((long long)b * p.Nq + pi) * p.Hq + (long long)r * G + g) * p.topk + pslot;
+            bf16 *dst = part + row * D;
+#pragma unroll
+            for (int c32 = 0; c32 < D / 32; ++c32) {
+                float ov[32];
+                tc::tmem_ld32(tmem + lane_base + L::TM_O + am * D + c32 * 32, ov);
+                if (pvalid) {
+#pragma unroll
+                    for (int x = 0; x < 32; x += 8)
+                        *reinterpret_cast<uint4 *>(dst + c32 * 32 + x) =
+                            make_uint4(pack_bf16(ov[x], ov[x + 1]), pack_bf16(ov[x + 2], ov[x + 3]),
+                                       pack_bf16(ov[x + 4], ov[x + 5]), pack_bf16(ov[x + 6], ov[x + 7]));
+                }
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&o_free[am]);
+            if (pvalid) stats[row] = make_float2(pm, pz);
+            return true;
+        };
+        for (int n = 0; ok && n < nch; ++n) {
+            const int a = n & 1;
+            const uint32_t ph = (uint32_t)(n >> 1) & 1u;
+            const QueryMeta *meta = reinterpret_cast<const QueryMeta *>(sm + L::OFF_META + a * 2048);
+            if (!tc::mbar_wait(&q_full[a], ph, st, 71, abort_flag)) { ok = false; break; }
+            if (!tc::mbar_wait(&s_full[a], ph, st, 72, abort_flag)) { ok = false; break; }
+            tc::fence_after_sync();
+            const bool valid = qq < meta->nq;
+            const long long pos = valid ? meta->pos[qq] : -1;
+            // last visible key of this block for this row, as an offset into the block
+            const int lim = (int)max(-1LL, min(min(pos, (long long)p.Nk - 1) - j0, (long long)kKeys - 1));
+            const uint32_t sbase = tmem + lane_base + L::TM_S + a * 128;
+            // pass 1: row max over the visible keys
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c32 = 0; c32 < 4; ++c32) {
+                float sv[32];
+                tc::tmem_ld32(sbase + c32 * 32, sv);
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj)
+                    if (c32 * 32 + jj <= lim) mx = fmaxf(mx, sv[jj]);
+            }
+            const float msafe = mx == -INFINITY ? 0.f : mx * sl2;
+            if (!tc::mbar_wait(&p_free[a], ph ^ 1u, st, 73, abort_flag)) { ok = false; break; }
+            // pass 2: P = exp2(s*scale*log2e - m) into the bf16 P tile, z = row sum
+            uint8_t *sp = sm + L::OFF_P + a * (2 * SUB);
+            float z = 0.f;
+#pragma unroll
+            for (int c32 = 0; c32 < 4; ++c32) {
+                float sv[32];
+                tc::tmem_ld32(sbase + c32 * 32, sv);
+                uint32_t pk[16];
+#pragma unroll
+                for (int jj = 0; jj < 32; jj += 2) {
+                    const int jo = c32 * 32 + jj;
+                    const float e0 = jo <= lim ? exp2f(sv[jj] * sl2 - msafe) : 0.f;
+                    const float e1 = jo + 1 <= lim ? exp2f(sv[jj + 1] * sl2 - msafe) : 0.f;
+                    z += e0 + e1;
+                    pk[jj / 2] = pack_bf16(e0, e1);
+                }
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    const int ch = c32 * 4 + c4;     // 16-byte chunk of the 256-byte row
+                    *reinterpret_cast<uint4 *>(sp + (ch >> 3) * SUB + swz(rho, ch & 7)) =
+                        make_uint4(pk[c4 * 4], pk[c4 * 4 + 1], pk[c4 * 4 + 2], pk[c4 * 4 + 3]);
+                }
+            }
+            const float cm = msafe, cz = z;
+            const bool cvalid = valid && mx != -INFINITY;
+            const int ci = valid ? meta->i[qq] : 0, cslot = valid ? meta->slot[qq] : 0;
+            tc::fence_before_sync();
+            tc::fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) {
+                tc::mbar_arrive(&s_free[a]);
+                tc::mbar_arrive(&p_full[a]);
+                tc::mbar_arrive(&q_empty[a]);     // this chunk's metadata now lives in registers
+            }
+            if (n >= 1 && !emit(n - 1)) { ok = false; break; }
+            pm = cm;
+            pz = cz;
+            pvalid = cvalid;
+            pi = ci;
+            pslot = cslot;
+        }
+        if (ok && nch > 0) emit(nch - 1);
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+// One warp per (b, i, h) row: merge the row's slots.
+template <int D>
+__global__ void __launch_bounds__(256)
+sparse_fwd_combine_kernel(Problem p, const int32_t *__restrict__ sel, const bf16 *__restrict__ part,
+                          const float2 *__restrict__ stats, bf16 *__restrict__ o, float *__restrict__ lse)
+{
+    const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= (long long)p.B * p.Nq * p.Hq) return;
+    const int h = (int)(row % p.Hq);
+    const long long bi = row / p.Hq;
+    const int i = (int)(bi % p.Nq), b = (int)(bi / p.Nq);
+    const int r = h / p.G;
+    const long long pos = (long long)p.q_offset + i;
+    const int32_t *srow = sel + (((long long)b * p.Hkv + r) * p.Nq + i) * p.topk;
+    // slot validity (same rule as the inverse index) and the row max
+    const int cl = lane < p.topk ? srow[lane] : -1;
+    const bool sv = cl >= 0 && cl < p.nb && (long long)cl * 128 <= pos;
+    const float2 mz = sv ? stats[row * p.topk + lane] : make_float2(-INFINITY, 0.f);
+    const float M = warp_max(mz.x);
+    const float w = sv ? exp2f(mz.x - M) : 0.f;
+    const float Z = warp_sum(w * mz.y);
+    constexpr int PER = D / 32;                 // features per lane
+    float acc[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+    const unsigned mask = __ballot_sync(0xffffffffu, sv);
+    for (unsigned m = mask; m; m &= m - 1) {
+        const int s = __ffs(m) - 1;
+        const float ws = __shfl_sync(0xffffffffu, w, s);
+        const bf16 *src = part + (row * p.topk + s) * D + lane * PER;
+        if constexpr (PER == 4) {
+            const uint2 u = *reinterpret_cast<const uint2 *>(src);
+            const float2 a0 = unpack_bf16(u.x), a1 = unpack_bf16(u.y);
+            acc[0] += ws * a0.x;
+            acc[1] += ws * a0.y;
+            acc[2] += ws * a1.x;
+            acc[3] += ws * a1.y;
+        } else {
+            const float2 a0 = unpack_bf16(*reinterpret_cast<const uint32_t *>(src));
+            acc[0] += ws * a0.x;
+            acc[1] += ws * a0.y;
+        }
+    }
+    const float inv = 1.f / Z;
+    bf16 *dst = o + row * D + lane * PER;
+    if constexpr (PER == 4) {
+        *reinterpret_cast<uint2 *>(dst) = make_uint2(pack_bf16(acc[0] * inv, acc[1] * inv),
+                                                     pack_bf16(acc[2] * inv, acc[3] * inv));
+    } else {
+        *reinterpret_cast<uint32_t *>(dst) = pack_bf16(acc[0] * inv, acc[1] * inv);
+    }
+    if (lane == 0) lse[((long long)b * p.Hq + h) * p.Nq + i] = (M + log2f(Z)) * kLn2;
+}
+
+template <int D, int G>
+cudaError_t launch_dg(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *v, const int32_t *sel,
+                      const FwdWork &w, DeviceStatus *st, cudaStream_t s)
+{
+    using L = FwdLayout<D>;
+    cudaError_t e = cudaFuncSetAttribute(sparse_fwd_tc_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+    if (e != cudaSuccess) return e;
+    sparse_fwd_tc_kernel<D, G><<<dim3(p.nb, p.Hkv, p.B), kThreads, L::ALLOC, s>>>(
+        p, q, k, v, sel, w.bucket_off, w.bucket_q, w.part, w.stats, st);
+    note_launch();
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *v, const int32_t *sel,
+                     const FwdWork &w, DeviceStatus *st, cudaStream_t s)
+{
+    switch (p.G) {
+    case 1: return launch_dg<D, 1>(p, q, k, v, sel, w, st, s);
+    case 2: return launch_dg<D, 2>(p, q, k, v, sel, w, st, s);
+    case 4: return launch_dg<D, 4>(p, q, k, v, sel, w, st, s);
+    default: return launch_dg<D, 8>(p, q, k, v, sel, w, st, s);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_sparse_fwd_keymajor(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *v,
+                                       const int32_t *sel, bf16 *o, float *lse, const FwdWork &w, DeviceStatus *st,
+                                       cudaStream_t s)
+{
+    cudaError_t e = launch_inverse_index(p, sel, w.bucket_cnt, w.bucket_off, w.bucket_cur, w.bucket_q, st, s);
+    if (e != cudaSuccess) return e;
+    e = p.d == 128 ? launch_d<128>(p, q, k, v, sel, w, st, s) : launch_d<64>(p, q, k, v, sel, w, st, s);
+    if (e != cudaSuccess) return e;
+    const long long rows = (long long)p.B * p.Nq * p.Hq;
+    if (p.d == 128)
+        sparse_fwd_combine_kernel<128><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p, sel, w.part, w.stats, o, lse);
+    else
+        sparse_fwd_combine_kernel<64><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p, sel, w.part, w.stats, o, lse);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace msa
