@@ -99,30 +99,43 @@ bool fwd_keymajor(const Problem &p) { return (long long)p.Nq * p.topk >= 8LL * p
 
 size_t bs_bytes(const Problem &p) { return align256((size_t)p.B * p.Nq * p.Hkv * p.nb * sizeof(float)); }
 
+// inverse index: counts, offsets, per-CTA scratch, query lists
+size_t index_bytes(const Problem &p)
+{
+    const size_t nbk = (size_t)p.B * p.Hkv * p.nb;
+    return 2 * align256((nbk + 1) * 4) + align256(inverse_index_scratch_ints(p) * 4) +
+           align256((size_t)p.B * p.Hkv * p.Nq * p.topk * 4);
+}
+
+template <class W>
+void carve_index(Carve &cv, const Problem &p, W &w)
+{
+    const size_t nbk = (size_t)p.B * p.Hkv * p.nb;
+    w.bucket_cnt = cv.take<int32_t>(nbk + 1);
+    w.bucket_off = cv.take<int32_t>(nbk + 1);
+    w.bucket_scratch = cv.take<int32_t>(inverse_index_scratch_ints(p));
+    w.bucket_q = cv.take<int32_t>((size_t)p.B * p.Hkv * p.Nq * p.topk);
+}
+
 size_t fwd_bytes(const Problem &p)
 {
     if (!fwd_keymajor(p)) return 0;
     const size_t rows = (size_t)p.B * p.Nq * p.Hq * p.topk;
-    const size_t nbk = (size_t)p.B * p.Hkv * p.nb;
-    return align256(rows * p.d * 2) + align256(rows * 8) + 3 * align256((nbk + 1) * 4) +
-           align256((size_t)p.B * p.Hkv * p.Nq * p.topk * 4);
+    return align256(rows * p.d * 2) + align256(rows * 8) + index_bytes(p);
 }
 size_t klrows_bytes(const Problem &p) { return align256((size_t)p.B * p.Hkv * p.Nq * sizeof(float)); }
 
 size_t kl_bytes(const Problem &p)
 {
     if (!fwd_keymajor(p)) return 0;
-    const size_t nbk = (size_t)p.B * p.Hkv * p.nb;
-    return align256((size_t)p.B * p.Hkv * p.Nq * p.topk * 4 * 16) + 3 * align256((nbk + 1) * 4) +
-           align256((size_t)p.B * p.Hkv * p.Nq * p.topk * 4);
+    return align256((size_t)p.B * p.Hkv * p.Nq * p.topk * 4 * 16) + index_bytes(p);
 }
 
 size_t bwd_bytes(const Problem &p)
 {
-    const size_t nbk = (size_t)p.B * p.Hkv * p.nb;
     return align256((size_t)p.B * p.Hq * p.Nq * 4) + align256((size_t)p.B * p.Nq * p.Hq * p.d * 4) +
            align256((size_t)p.B * p.Nq * p.Hkv * p.d_idx * 4) + align256((size_t)p.B * p.Nk * p.d_idx * 4) +
-           3 * align256((nbk + 1) * 4) + align256((size_t)p.B * p.Hkv * p.Nq * p.topk * 4);
+           index_bytes(p);
 }
 
 #define REQUIRE_PTR(ptr, name)                                                                         \
@@ -212,14 +225,10 @@ msa_status msa_sparse_attn_fwd(const msa_shape *shape, const void *q, const void
     if (fwd_keymajor(p)) {
         Carve cv{static_cast<char *>(workspace)};
         const size_t rows = (size_t)p.B * p.Nq * p.Hq * p.topk;
-        const size_t nbk = (size_t)p.B * p.Hkv * p.nb;
         FwdWork w;
         w.part = cv.take<bf16>(rows * p.d);
         w.stats = cv.take<float2>(rows);
-        w.bucket_cnt = cv.take<int32_t>(nbk + 1);
-        w.bucket_off = cv.take<int32_t>(nbk + 1);
-        w.bucket_cur = cv.take<int32_t>(nbk + 1);
-        w.bucket_q = cv.take<int32_t>((size_t)p.B * p.Hkv * p.Nq * p.topk);
+        carve_index(cv, p, w);
         e = launch_sparse_fwd_keymajor(p, static_cast<const bf16 *>(q), static_cast<const bf16 *>(k),
                                        static_cast<const bf16 *>(v), sel_idx, static_cast<bf16 *>(o), lse, w, ds, s);
     } else {
@@ -252,13 +261,9 @@ msa_status msa_kl_fwd(const msa_shape *shape, const void *q, const void *k, cons
     DeviceStatus *ds = static_cast<DeviceStatus *>(workspace);
     cudaError_t e;
     if (fwd_keymajor(p)) {
-        const size_t nbk = (size_t)p.B * p.Hkv * p.nb;
         KlWork w;
         w.part = cv.take<float4>((size_t)p.B * p.Hkv * p.Nq * p.topk * 4);
-        w.bucket_cnt = cv.take<int32_t>(nbk + 1);
-        w.bucket_off = cv.take<int32_t>(nbk + 1);
-        w.bucket_cur = cv.take<int32_t>(nbk + 1);
-        w.bucket_q = cv.take<int32_t>((size_t)p.B * p.Hkv * p.Nq * p.topk);
+        carve_index(cv, p, w);
         e = launch_kl_keymajor(p, static_cast<const bf16 *>(q), static_cast<const bf16 *>(k),
                                static_cast<const bf16 *>(q_idx), static_cast<const bf16 *>(k_idx), sel_idx, lse,
                                lse_idx, rows, w, ds, s);
@@ -306,10 +311,7 @@ msa_status msa_fused_bwd(const msa_shape *shape, const void *q, const void *k, c
     w.dq_acc = cv.take<float>((size_t)p.B * p.Nq * p.Hq * p.d);
     w.dqi_acc = cv.take<float>((size_t)p.B * p.Nq * p.Hkv * p.d_idx);
     w.dki_acc = cv.take<float>((size_t)p.B * p.Nk * p.d_idx);
-    w.bucket_cnt = cv.take<int32_t>(nbk + 1);
-    w.bucket_off = cv.take<int32_t>(nbk + 1);
-    w.bucket_cur = cv.take<int32_t>(nbk + 1);
-    w.bucket_q = cv.take<int32_t>((size_t)p.B * p.Hkv * p.Nq * p.topk);
+    carve_index(cv, p, w);
     cudaError_t e = launch_fused_bwd(p, static_cast<const bf16 *>(q), static_cast<const bf16 *>(k),
                                      static_cast<const bf16 *>(v), static_cast<const bf16 *>(o),
                                      static_cast<const bf16 *>(d_o), lse, static_cast<const bf16 *>(q_idx),

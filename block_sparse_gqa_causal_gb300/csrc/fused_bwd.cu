@@ -78,63 +78,6 @@ __global__ void bwd_rowdot_kernel(Problem p, const bf16 *__restrict__ o, const b
     }
 }
 
-__global__ void bucket_count_kernel(Problem p, const int32_t *__restrict__ sel, int32_t *__restrict__ cnt,
-                                    DeviceStatus *st)
-{
-    const long long n = (long long)p.B * p.Hkv * p.Nq * p.topk;
-    for (long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x; x < n; x += (long long)gridDim.x * blockDim.x) {
-        const int c = sel[x];
-        if (c < 0) continue;
-        const long long bri = x / p.topk;             // (b*Hkv + r)*Nq + i
-        const int i = (int)(bri % p.Nq);
-        const long long br = bri / p.Nq;
-        if (c >= p.nb || (long long)c * 128 > (long long)p.q_offset + i) { report(st, kDevCheck, 51, c); continue; }
-        atomicAdd(&cnt[br * p.nb + c], 1);
-    }
-}
-
-// exclusive scan of cnt[0..n) into off[0..n], single CTA of 1024 threads
-__global__ void __launch_bounds__(1024) bucket_scan_kernel(const int32_t *__restrict__ cnt, int32_t *__restrict__ off,
-                                                           int n)
-{
-    __shared__ int part[1024];
-    const int per = (n + 1023) / 1024;
-    const int lo = threadIdx.x * per, hi = min(n, lo + per);
-    int s = 0;
-    for (int x = lo; x < hi; ++x) s += cnt[x];
-    part[threadIdx.x] = s;
-    __syncthreads();
-    for (int d = 1; d < 1024; d <<= 1) {
-        const int v = threadIdx.x >= (unsigned)d ? part[threadIdx.x - d] : 0;
-        __syncthreads();
-        part[threadIdx.x] += v;
-        __syncthreads();
-    }
-    int run = threadIdx.x ? part[threadIdx.x - 1] : 0;
-    for (int x = lo; x < hi; ++x) {
-        off[x] = run;
-        run += cnt[x];
-    }
-    if (threadIdx.x == 1023) off[n] = part[1023];
-}
-
-__global__ void bucket_fill_kernel(Problem p, const int32_t *__restrict__ sel, const int32_t *__restrict__ off,
-                                   int32_t *__restrict__ cur, int32_t *__restrict__ list)
-{
-    const long long n = (long long)p.B * p.Hkv * p.Nq * p.topk;
-    for (long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x; x < n; x += (long long)gridDim.x * blockDim.x) {
-        const int c = sel[x];
-        if (c < 0) continue;
-        const long long bri = x / p.topk;
-        const int i = (int)(bri % p.Nq);
-        const long long br = bri / p.Nq;
-        if (c >= p.nb || (long long)c * 128 > (long long)p.q_offset + i) continue;
-        const long long bucket = br * p.nb + c;
-        const int slot = atomicAdd(&cur[bucket], 1);
-        list[off[bucket] + slot] = i;
-    }
-}
-
 __global__ void f32_to_bf16_kernel(const float *__restrict__ src, bf16 *__restrict__ dst, long long n)
 {
     for (long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x; x < n / 2; x += (long long)gridDim.x * blockDim.x) {
@@ -535,23 +478,6 @@ cudaError_t launch_main(const Problem &p, const bf16 *q, const bf16 *k, const bf
 
 }  // namespace
 
-cudaError_t launch_inverse_index(const Problem &p, const int32_t *sel, int32_t *cnt, int32_t *off, int32_t *cur,
-                                 int32_t *list, DeviceStatus *st, cudaStream_t s)
-{
-    cudaError_t e;
-    const long long nbk = (long long)p.B * p.Hkv * p.nb;
-    if ((e = cudaMemsetAsync(cnt, 0, (nbk + 1) * 4, s)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(cur, 0, (nbk + 1) * 4, s)) != cudaSuccess) return e;
-    const int grid_sel = 4 * p.num_sms;
-    bucket_count_kernel<<<grid_sel, 256, 0, s>>>(p, sel, cnt, st);
-    note_launch();
-    bucket_scan_kernel<<<1, 1024, 0, s>>>(cnt, off, (int)nbk);
-    note_launch();
-    bucket_fill_kernel<<<grid_sel, 256, 0, s>>>(p, sel, off, cur, list);
-    note_launch();
-    return cudaGetLastError();
-}
-
 cudaError_t launch_fused_bwd(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *v, const bf16 *o,
                              const bf16 *d_o, const float *lse, const bf16 *q_idx, const bf16 *k_idx,
                              const int32_t *sel, const float *lse_idx, float kl_coef, bf16 *dq, bf16 *dk, bf16 *dv,
@@ -569,7 +495,7 @@ cudaError_t launch_fused_bwd(const Problem &p, const bf16 *q, const bf16 *k, con
     const long long rows = (long long)p.B * p.Nq * p.Hq;
     bwd_rowdot_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p, o, d_o, w.D);
     note_launch();
-    if ((e = launch_inverse_index(p, sel, w.bucket_cnt, w.bucket_off, w.bucket_cur, w.bucket_q, st, s)) != cudaSuccess)
+    if ((e = launch_inverse_index(p, sel, w.bucket_cnt, w.bucket_off, w.bucket_scratch, w.bucket_q, st, s)) != cudaSuccess)
         return e;
 
     if (p.d == 128 && p.d_idx == 128) e = launch_fused_bwd_tc_main(p, q, k, v, d_o, lse, q_idx, k_idx, lse_idx, kl_coef, w, dk, dv, st, s);

@@ -291,10 +291,16 @@ fused_bwd_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restric
             if (!tc::mbar_wait(&full[n & 1], (uint32_t)(n >> 1) & 1u, st, 31, abort_flag)) { ok = false; break; }
             if (!tc::mbar_wait(s_full, (uint32_t)n & 1u, st, 32, abort_flag)) { ok = false; break; }
             tc::fence_after_sync();
-            float sv[kNQ], dp[kNQ], si[kNQI];
-            tc::tmem_ld32(tmem + lane_base + TM_S, sv);
-            tc::tmem_ld32(tmem + lane_base + TM_DP, dp);
-            tc::tmem_ld16(tmem + lane_base + TM_SI, si);
+            uint32_t svr[kNQ], dpr[kNQ], sir[kNQI];
+            tc::tmem_ld32_nowait(tmem + lane_base + TM_S, svr);
+            tc::tmem_ld32_nowait(tmem + lane_base + TM_DP, dpr);
+            tc::tmem_ld16_nowait(tmem + lane_base + TM_SI, sir);
+            tc::tmem_wait32(svr);
+            tc::tmem_wait32(dpr);
+            tc::tmem_wait16(sir);
+            const float *sv = reinterpret_cast<const float *>(svr);
+            const float *dp = reinterpret_cast<const float *>(dpr);
+            const float *si = reinterpret_cast<const float *>(sir);
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(tm_free);
@@ -311,7 +317,7 @@ fused_bwd_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restric
                     const int rr = rho + e;
                     const int qq = rr / G;
                     const bool vis = key_ok && qq < kNQI && j <= rows->pos[qq < kNQI ? qq : 0];
-                    pr[e] = vis ? exp2f(sv[rr] * sl2 - rows->lse2[rr]) : 0.f;
+                    pr[e] = vis ? tc::ex2(sv[rr] * sl2 - rows->lse2[rr]) : 0.f;
                     dsv[e] = pr[e] * (dp[rr] - rows->dd[rr]);
                     if (qq < kNQI) pt[qq] += pr[e];
                 }
@@ -326,7 +332,7 @@ fused_bwd_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restric
                 for (int e = 0; e < 2; ++e) {
                     const int qq = u + e;
                     const bool vis = key_ok && j <= rows->pos[qq];
-                    const float ps = vis ? exp2f(si[qq] * si2 - rows->lsei2[qq]) : 0.f;
+                    const float ps = vis ? tc::ex2(si[qq] * si2 - rows->lsei2[qq]) : 0.f;
                     ds2[e] = vis ? coef * (ps - pt[qq] * invG) : 0.f;
                 }
                 sg[u / 2] = pack_bf16(ds2[0], ds2[1]);
@@ -357,9 +363,13 @@ fused_bwd_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restric
             // dQ^T, dQ_idx^T rows (this thread: feature kr)
             if (!tc::mbar_wait(dq_full, (uint32_t)n & 1u, st, 34, abort_flag)) { ok = false; break; }
             tc::fence_after_sync();
-            float dqv[kNQ], dqiv[kNQI];
-            tc::tmem_ld32(tmem + lane_base + TM_DQ, dqv);
-            tc::tmem_ld16(tmem + lane_base + TM_DQI, dqiv);
+            uint32_t dqr[kNQ], dqir[kNQI];
+            tc::tmem_ld32_nowait(tmem + lane_base + TM_DQ, dqr);
+            tc::tmem_ld16_nowait(tmem + lane_base + TM_DQI, dqir);
+            tc::tmem_wait32(dqr);
+            tc::tmem_wait16(dqir);
+            const float *dqv = reinterpret_cast<const float *>(dqr);
+            const float *dqiv = reinterpret_cast<const float *>(dqir);
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(dq_free);
@@ -378,17 +388,16 @@ fused_bwd_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restric
                 const int qq = rr / G, g = rr % G;
                 if (qq < nq) {
                     const float4 v4 = *reinterpret_cast<const float4 *>(red + rr * 32 + d4);
-                    atomicAdd(reinterpret_cast<float4 *>(dq_acc + (((long long)b * p.Nq + qsel(qis, qq)) * p.Hq +
-                                                                   (long long)r * G + g) * D + dbase + d4),
-                              make_float4(p.scale * v4.x, p.scale * v4.y, p.scale * v4.z, p.scale * v4.w));
+                    tc::red_add_v4(dq_acc + (((long long)b * p.Nq + qsel(qis, qq)) * p.Hq + (long long)r * G + g) * D +
+                                       dbase + d4,
+                                   p.scale * v4.x, p.scale * v4.y, p.scale * v4.z, p.scale * v4.w);
                 }
             }
             for (int x = lane; x < nq * 8; x += 32) {
                 const int qq = x >> 3, d4 = (x & 7) * 4;
                 const float4 v4 = *reinterpret_cast<const float4 *>(red + (kNQ + qq) * 32 + d4);
-                atomicAdd(reinterpret_cast<float4 *>(dqi_acc + (((long long)b * p.Nq + qsel(qis, qq)) * p.Hkv + r) * DI +
-                                                     dbase + d4),
-                          make_float4(p.scale_idx * v4.x, p.scale_idx * v4.y, p.scale_idx * v4.z, p.scale_idx * v4.w));
+                tc::red_add_v4(dqi_acc + (((long long)b * p.Nq + qsel(qis, qq)) * p.Hkv + r) * DI + dbase + d4,
+                               p.scale_idx * v4.x, p.scale_idx * v4.y, p.scale_idx * v4.z, p.scale_idx * v4.w);
             }
             __syncwarp();
         }
@@ -421,9 +430,8 @@ fused_bwd_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restric
                     tc::tmem_ld32(tmem + lane_base + TM_DKI + c32 * 32, a);
 #pragma unroll
                     for (int x = 0; x < 32; x += 4)
-                        atomicAdd(reinterpret_cast<float4 *>(pki + c32 * 32 + x),
-                                  make_float4(p.scale_idx * a[x], p.scale_idx * a[x + 1], p.scale_idx * a[x + 2],
-                                              p.scale_idx * a[x + 3]));
+                        tc::red_add_v4(pki + c32 * 32 + x, p.scale_idx * a[x], p.scale_idx * a[x + 1],
+                                       p.scale_idx * a[x + 2], p.scale_idx * a[x + 3]);
                 }
             }
         }

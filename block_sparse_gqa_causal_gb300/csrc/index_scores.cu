@@ -188,17 +188,22 @@ index_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_
                     const bool full_vis = (j0 + 127 <= pos_first) && (j0 + 128 <= p.Nk);
                     const uint32_t base = tmem + lane_base + (uint32_t)((a * 2 + m) * 128);
 #pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) {
-                        float v[32];
-                        tc::tmem_ld32(base + ch * 32, v);
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t v0[32], v1[32];
+                        tc::tmem_ld32_nowait(base + h * 64, v0);
+                        tc::tmem_ld32_nowait(base + h * 64 + 32, v1);
+                        tc::tmem_wait32(v0);
+                        tc::tmem_wait32(v1);
                         if (full_vis) {
 #pragma unroll
-                            for (int jj = 0; jj < 32; ++jj) mx = fmaxf(mx, v[jj]);
+                            for (int jj = 0; jj < 32; ++jj)
+                                mx = fmaxf(mx, fmaxf(__uint_as_float(v0[jj]), __uint_as_float(v1[jj])));
                         } else {
 #pragma unroll
                             for (int jj = 0; jj < 32; ++jj) {
-                                const long long j = j0 + ch * 32 + jj;
-                                if (j <= pos && j < p.Nk) mx = fmaxf(mx, v[jj]);
+                                const long long j = j0 + h * 64 + jj;
+                                if (j <= pos && j < p.Nk) mx = fmaxf(mx, __uint_as_float(v0[jj]));
+                                if (j + 32 <= pos && j + 32 < p.Nk) mx = fmaxf(mx, __uint_as_float(v1[jj]));
                             }
                         }
                     }

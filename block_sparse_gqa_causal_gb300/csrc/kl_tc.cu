@@ -47,7 +47,9 @@ struct KlLayout {
     static constexpr int OFF_QI = OFF_Q + 2 * (D / 64) * SUB;               // 2 stages x DI/64 sub-tiles
     static constexpr int OFF_META = OFF_QI + 2 * (DI / 64) * ((QI_ROWS_BYTES + 1023) & ~1023);
     static constexpr int META_BYTES = (int)((sizeof(KlMeta) + 255) & ~size_t(255));
-    static constexpr int OFF_BAR = OFF_META + 2 * META_BYTES;
+    static constexpr int SG = (32 / G) < 8 ? (32 / G) : 8;              // queries per reduction group
+    static constexpr int OFF_RED = OFF_META + 2 * META_BYTES;             // per warp [3*SG][32] floats
+    static constexpr int OFF_BAR = OFF_RED + kEpiWarps * 3 * SG * 32 * 4;
     static constexpr int ALLOC = OFF_BAR + 256 + 1024;
     static constexpr int QI_SUB = (QI_ROWS_BYTES + 1023) & ~1023;         // stride of q_idx sub-tiles
     static constexpr uint32_t TM_S = 0, TM_SI = 256;
@@ -244,57 +246,75 @@ kl_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restrict__ k, 
             tc::fence_after_sync();
             const int nq = meta->nq;
             // queries in groups of 32 / G per 32-column TMEM slice
-            constexpr int QS = (32 / G) > 0 ? 32 / G : 1;   // queries per slice
+            constexpr int QS = 32 / G;            // queries per 32-column slice
+            constexpr int SG = L::SG;             // queries per reduction group
+            float *red = reinterpret_cast<float *>(sm + L::OFF_RED) + quarter * (3 * SG * 32);
 #pragma unroll
             for (int c32 = 0; c32 < kRows / 32; ++c32) {
-                float sv[32], si[32];
-                tc::tmem_ld32(tmem + lane_base + L::TM_S + a * 128 + c32 * 32, sv);
-                if (c32 * QS < NS) tc::tmem_ld32(tmem + lane_base + L::TM_SI + a * 128 + (c32 * QS / 32) * 32, si);
-                // per-key terms of every query in this slice, then all queries'
-                // warp reductions advanced together (independent shuffle chains)
-                float A[QS], Bv[QS], Mx[QS], s2v[QS];
-                bool visq[QS];
+                uint32_t sv[32], si[32];
+                tc::tmem_ld32_nowait(tmem + lane_base + L::TM_S + a * 128 + c32 * 32, sv);
+                tc::tmem_ld32_nowait(tmem + lane_base + L::TM_SI + a * 128 + ((c32 * QS) / 32) * 32, si);
+                tc::tmem_wait32(sv);
+                tc::tmem_wait32(si);
 #pragma unroll
-                for (int u = 0; u < QS; ++u) {
-                    const int qq = c32 * QS + u;
-                    const bool vis = qq < nq && j <= meta->pos[qq] && j < p.Nk;
-                    float pt = 0.f;
+                for (int sg = 0; sg < QS / SG; ++sg) {
+                    // per-key terms of SG queries -> shared memory, one row per (query, term)
+                    float s2v[SG];
+                    bool visv[SG];
 #pragma unroll
-                    for (int g = 0; g < G; ++g)
-                        pt += vis ? exp2f(sv[u * G + g] * sl2 - meta->lse2[qq * G + g]) : 0.f;
-                    pt *= invG;
-                    const float s2 = vis ? si[qq & 31] * si2 : -INFINITY;
-                    A[u] = pt > 0.f ? pt * log2f(pt) : 0.f;
-                    Bv[u] = vis ? pt * s2 : 0.f;
-                    Mx[u] = s2;
-                    s2v[u] = s2;
-                    visq[u] = vis;
-                }
+                    for (int u = 0; u < SG; ++u) {
+                        const int ql = sg * SG + u;                 // query within the slice
+                        const int qq = c32 * QS + ql;               // query within the chunk
+                        const bool vis = qq < nq && j <= meta->pos[qq] && j < p.Nk;
+                        float pt = 0.f;
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-#pragma unroll
-                    for (int u = 0; u < QS; ++u) {
-                        A[u] += __shfl_xor_sync(0xffffffffu, A[u], o);
-                        Bv[u] += __shfl_xor_sync(0xffffffffu, Bv[u], o);
-                        Mx[u] = fmaxf(Mx[u], __shfl_xor_sync(0xffffffffu, Mx[u], o));
+                        for (int g = 0; g < G; ++g)
+                            pt += vis ? tc::ex2(__uint_as_float(sv[ql * G + g]) * sl2 - meta->lse2[qq * G + g]) : 0.f;
+                        pt *= invG;
+                        const float s2 = vis ? __uint_as_float(si[qq & 31]) * si2 : -INFINITY;
+                        red[(u * 3 + 0) * 32 + lane] = pt > 0.f ? pt * tc::lg2(pt) : 0.f;
+                        red[(u * 3 + 1) * 32 + lane] = vis ? pt * s2 : 0.f;
+                        red[(u * 3 + 2) * 32 + lane] = s2;
+                        s2v[u] = s2;
+                        visv[u] = vis;
                     }
-                }
-                float Z[QS];
+                    __syncwarp();
+                    // lane l < 3*SG reduces row l over the warp's 32 keys (sum, sum, max)
+                    float res = 0.f;
+                    if (lane < 3 * SG) {
+                        const float *row = red + lane * 32;
+                        if (lane % 3 == 2) {
+                            float m = -INFINITY;
 #pragma unroll
-                for (int u = 0; u < QS; ++u) Z[u] = (visq[u] && Mx[u] != -INFINITY) ? exp2f(s2v[u] - Mx[u]) : 0.f;
+                            for (int k2 = 0; k2 < 32; ++k2) m = fmaxf(m, row[(k2 + lane) & 31]);
+                            res = m;
+                        } else {
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
+                            for (int k2 = 0; k2 < 32; ++k2) res += row[(k2 + lane) & 31];
+                        }
+                    }
+                    __syncwarp();
+                    float Mv[SG];
 #pragma unroll
-                    for (int u = 0; u < QS; ++u) Z[u] += __shfl_xor_sync(0xffffffffu, Z[u], o);
-                }
-                // lane u writes query u of the slice
+                    for (int u = 0; u < SG; ++u) {
+                        Mv[u] = __shfl_sync(0xffffffffu, res, u * 3 + 2);
+                        red[u * 32 + lane] = (visv[u] && Mv[u] != -INFINITY) ? tc::ex2(s2v[u] - Mv[u]) : 0.f;
+                    }
+                    __syncwarp();
+                    float Z = 0.f;
+                    if (lane < SG) {
 #pragma unroll
-                for (int u = 0; u < QS; ++u) {
-                    const int qq = c32 * QS + u;
-                    if (lane == (u & 31) && qq < nq) {
+                        for (int k2 = 0; k2 < 32; ++k2) Z += red[lane * 32 + ((k2 + lane) & 31)];
+                    }
+                    const float Aq = __shfl_sync(0xffffffffu, res, (lane % SG) * 3);
+                    const float Bq = __shfl_sync(0xffffffffu, res, (lane % SG) * 3 + 1);
+                    const float Mq = __shfl_sync(0xffffffffu, res, (lane % SG) * 3 + 2);
+                    const int qq = c32 * QS + sg * SG + lane;
+                    if (lane < SG && qq < nq) {
                         const long long row = ((long long)b * p.Hkv + r) * p.Nq + meta->i[qq];
-                        part[(row * p.topk + meta->slot[qq]) * kEpiWarps + quarter] = make_float4(A[u], Bv[u], Mx[u], Z[u]);
+                        part[(row * p.topk + meta->slot[qq]) * kEpiWarps + quarter] = make_float4(Aq, Bq, Mq, Z);
                     }
+                    __syncwarp();
                 }
             }
             tc::fence_before_sync();
@@ -379,7 +399,7 @@ cudaError_t launch_kl_keymajor(const Problem &p, const bf16 *q, const bf16 *k, c
                                const int32_t *sel, const float *lse, float *lse_idx, float *kl_rows, const KlWork &w,
                                DeviceStatus *st, cudaStream_t s)
 {
-    cudaError_t e = launch_inverse_index(p, sel, w.bucket_cnt, w.bucket_off, w.bucket_cur, w.bucket_q, st, s);
+    cudaError_t e = launch_inverse_index(p, sel, w.bucket_cnt, w.bucket_off, w.bucket_scratch, w.bucket_q, st, s);
     if (e != cudaSuccess) return e;
     if (p.d == 128 && p.d_idx == 128) e = launch_dd<128, 128>(p, q, k, q_idx, k_idx, sel, lse, w, st, s);
     else if (p.d == 128) e = launch_dd<128, 64>(p, q, k, q_idx, k_idx, sel, lse, w, st, s);

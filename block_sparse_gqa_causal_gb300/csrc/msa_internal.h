@@ -39,7 +39,7 @@ cudaError_t launch_block_topk(const Problem &p, const float *bs, int32_t *sel, D
 struct FwdWork {
     bf16 *part;          // [B, Nq, Hq, topk, d] unnormalised partial outputs per selected block
     float2 *stats;       // [B, Nq, Hq, topk] (row max in log2 units, row sum)
-    int32_t *bucket_cnt, *bucket_off, *bucket_cur, *bucket_q;
+    int32_t *bucket_cnt, *bucket_off, *bucket_scratch, *bucket_q;
 };
 cudaError_t launch_sparse_fwd_keymajor(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *v,
                                        const int32_t *sel, bf16 *o, float *lse, const FwdWork &w, DeviceStatus *st,
@@ -55,7 +55,7 @@ cudaError_t launch_kl_fwd(const Problem &p, const bf16 *q, const bf16 *k, const 
 // Key-major KL forward (many queries per selected block).
 struct KlWork {
     float4 *part;        // [B, Hkv, Nq, topk, 4] per-warp partial sums
-    int32_t *bucket_cnt, *bucket_off, *bucket_cur, *bucket_q;
+    int32_t *bucket_cnt, *bucket_off, *bucket_scratch, *bucket_q;
 };
 cudaError_t launch_kl_keymajor(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *q_idx, const bf16 *k_idx,
                                const int32_t *sel, const float *lse, float *lse_idx, float *kl_rows, const KlWork &w,
@@ -71,7 +71,7 @@ struct BwdWork {
     float *dki_acc;      // [B, Nk, d_idx]
     int32_t *bucket_cnt; // [B*Hkv*nb]
     int32_t *bucket_off; // [B*Hkv*nb + 1]
-    int32_t *bucket_cur; // [B*Hkv*nb]
+    int32_t *bucket_scratch; // inverse_index_scratch_ints(p)
     int32_t *bucket_q;   // [B*Hkv*Nq*topk]  query rows per (b, r, block)
 };
 cudaError_t launch_fused_bwd(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *v,
@@ -81,8 +81,10 @@ cudaError_t launch_fused_bwd(const Problem &p, const bf16 *q, const bf16 *k, con
                              bf16 *dk_idx, const BwdWork &w, DeviceStatus *st, cudaStream_t s);
 
 // Inverse index: for every (b, group, block) the query rows that selected
-// it (count, exclusive scan into off[0..nbk], fill).  cnt / cur are zeroed here.
-cudaError_t launch_inverse_index(const Problem &p, const int32_t *sel, int32_t *cnt, int32_t *off, int32_t *cur,
+// it.  cnt [nbk], off [nbk + 1], list [B*Hkv*Nq*topk]; scratch holds
+// inverse_index_scratch_ints(p) ints (per-CTA histograms and offsets).
+size_t inverse_index_scratch_ints(const Problem &p);
+cudaError_t launch_inverse_index(const Problem &p, const int32_t *sel, int32_t *cnt, int32_t *off, int32_t *scratch,
                                  int32_t *list, DeviceStatus *st, cudaStream_t s);
 
 // tcgen05 main backward kernel (d = d_idx = 128); the prep kernels run first.

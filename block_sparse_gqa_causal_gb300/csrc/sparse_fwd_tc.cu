@@ -246,15 +246,26 @@ sparse_fwd_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restri
             const long long row = (((long long)b * p.Nq + pi) * p.Hq + (long long)r * G + g) * p.topk + pslot;
             bf16 *dst = part + row * D;
 #pragma unroll
-            for (int c32 = 0; c32 < D / 32; ++c32) {
-                float ov[32];
-                tc::tmem_ld32(tmem + lane_base + L::TM_O + am * D + c32 * 32, ov);
+            for (int c64 = 0; c64 < D / 64; ++c64) {
+                uint32_t o0[32], o1[32];
+                tc::tmem_ld32_nowait(tmem + lane_base + L::TM_O + am * D + c64 * 64, o0);
+                tc::tmem_ld32_nowait(tmem + lane_base + L::TM_O + am * D + c64 * 64 + 32, o1);
+                tc::tmem_wait32(o0);
+                tc::tmem_wait32(o1);
                 if (pvalid) {
 #pragma unroll
-                    for (int x = 0; x < 32; x += 8)
-                        *reinterpret_cast<uint4 *>(dst + c32 * 32 + x) =
-                            make_uint4(pack_bf16(ov[x], ov[x + 1]), pack_bf16(ov[x + 2], ov[x + 3]),
-                                       pack_bf16(ov[x + 4], ov[x + 5]), pack_bf16(ov[x + 6], ov[x + 7]));
+                    for (int x = 0; x < 32; x += 8) {
+                        *reinterpret_cast<uint4 *>(dst + c64 * 64 + x) = make_uint4(
+                            pack_bf16(__uint_as_float(o0[x]), __uint_as_float(o0[x + 1])),
+                            pack_bf16(__uint_as_float(o0[x + 2]), __uint_as_float(o0[x + 3])),
+                            pack_bf16(__uint_as_float(o0[x + 4]), __uint_as_float(o0[x + 5])),
+                            pack_bf16(__uint_as_float(o0[x + 6]), __uint_as_float(o0[x + 7])));
+                        *reinterpret_cast<uint4 *>(dst + c64 * 64 + 32 + x) = make_uint4(
+                            pack_bf16(__uint_as_float(o1[x]), __uint_as_float(o1[x + 1])),
+                            pack_bf16(__uint_as_float(o1[x + 2]), __uint_as_float(o1[x + 3])),
+                            pack_bf16(__uint_as_float(o1[x + 4]), __uint_as_float(o1[x + 5])),
+                            pack_bf16(__uint_as_float(o1[x + 6]), __uint_as_float(o1[x + 7])));
+                    }
                 }
             }
             tc::fence_before_sync();
@@ -278,12 +289,22 @@ sparse_fwd_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restri
             // pass 1: row max over the visible keys
             float mx = -INFINITY;
 #pragma unroll
-            for (int c32 = 0; c32 < 4; ++c32) {
-                float sv[32];
-                tc::tmem_ld32(sbase + c32 * 32, sv);
+            for (int c64 = 0; c64 < 2; ++c64) {
+                uint32_t s0[32], s1[32];
+                tc::tmem_ld32_nowait(sbase + c64 * 64, s0);
+                tc::tmem_ld32_nowait(sbase + c64 * 64 + 32, s1);
+                tc::tmem_wait32(s0);
+                tc::tmem_wait32(s1);
+                if (lim >= c64 * 64 + 63) {
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj)
-                    if (c32 * 32 + jj <= lim) mx = fmaxf(mx, sv[jj]);
+                    for (int jj = 0; jj < 32; ++jj) mx = fmaxf(mx, fmaxf(__uint_as_float(s0[jj]), __uint_as_float(s1[jj])));
+                } else {
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj) {
+                        if (c64 * 64 + jj <= lim) mx = fmaxf(mx, __uint_as_float(s0[jj]));
+                        if (c64 * 64 + 32 + jj <= lim) mx = fmaxf(mx, __uint_as_float(s1[jj]));
+                    }
+                }
             }
             const float msafe = mx == -INFINITY ? 0.f : mx * sl2;
             if (!tc::mbar_wait(&p_free[a], ph ^ 1u, st, 73, abort_flag)) { ok = false; break; }
@@ -291,23 +312,30 @@ sparse_fwd_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restri
             uint8_t *sp = sm + L::OFF_P + a * (2 * SUB);
             float z = 0.f;
 #pragma unroll
-            for (int c32 = 0; c32 < 4; ++c32) {
-                float sv[32];
-                tc::tmem_ld32(sbase + c32 * 32, sv);
-                uint32_t pk[16];
+            for (int c64 = 0; c64 < 2; ++c64) {
+                uint32_t sr[2][32];
+                tc::tmem_ld32_nowait(sbase + c64 * 64, sr[0]);
+                tc::tmem_ld32_nowait(sbase + c64 * 64 + 32, sr[1]);
+                tc::tmem_wait32(sr[0]);
+                tc::tmem_wait32(sr[1]);
 #pragma unroll
-                for (int jj = 0; jj < 32; jj += 2) {
-                    const int jo = c32 * 32 + jj;
-                    const float e0 = jo <= lim ? exp2f(sv[jj] * sl2 - msafe) : 0.f;
-                    const float e1 = jo + 1 <= lim ? exp2f(sv[jj + 1] * sl2 - msafe) : 0.f;
-                    z += e0 + e1;
-                    pk[jj / 2] = pack_bf16(e0, e1);
-                }
+                for (int h = 0; h < 2; ++h) {
+                    const int c32 = c64 * 2 + h;
+                    uint32_t pk[16];
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    const int ch = c32 * 4 + c4;     // 16-byte chunk of the 256-byte row
-                    *reinterpret_cast<uint4 *>(sp + (ch >> 3) * SUB + swz(rho, ch & 7)) =
-                        make_uint4(pk[c4 * 4], pk[c4 * 4 + 1], pk[c4 * 4 + 2], pk[c4 * 4 + 3]);
+                    for (int jj = 0; jj < 32; jj += 2) {
+                        const int jo = c32 * 32 + jj;
+                        const float e0 = jo <= lim ? tc::ex2(__uint_as_float(sr[h][jj]) * sl2 - msafe) : 0.f;
+                        const float e1 = jo + 1 <= lim ? tc::ex2(__uint_as_float(sr[h][jj + 1]) * sl2 - msafe) : 0.f;
+                        z += e0 + e1;
+                        pk[jj / 2] = pack_bf16(e0, e1);
+                    }
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const int ch = c32 * 4 + c4;     // 16-byte chunk of the 256-byte row
+                        *reinterpret_cast<uint4 *>(sp + (ch >> 3) * SUB + swz(rho, ch & 7)) =
+                            make_uint4(pk[c4 * 4], pk[c4 * 4 + 1], pk[c4 * 4 + 2], pk[c4 * 4 + 3]);
+                    }
                 }
             }
             const float cm = msafe, cz = z;
@@ -425,7 +453,7 @@ cudaError_t launch_sparse_fwd_keymajor(const Problem &p, const bf16 *q, const bf
                                        const int32_t *sel, bf16 *o, float *lse, const FwdWork &w, DeviceStatus *st,
                                        cudaStream_t s)
 {
-    cudaError_t e = launch_inverse_index(p, sel, w.bucket_cnt, w.bucket_off, w.bucket_cur, w.bucket_q, st, s);
+    cudaError_t e = launch_inverse_index(p, sel, w.bucket_cnt, w.bucket_off, w.bucket_scratch, w.bucket_q, st, s);
     if (e != cudaSuccess) return e;
     e = p.d == 128 ? launch_d<128>(p, q, k, v, sel, w, st, s) : launch_d<64>(p, q, k, v, sel, w, st, s);
     if (e != cudaSuccess) return e;
