@@ -166,7 +166,7 @@ fused_bwd_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restrict__
             const int row = idx / (D / 8), ch = idx % (D / 8);
             const int qq = row / G, gg = row % G;
             const bool ok = qq < nq;
-            const int i = ok ? bucket_q[qc + qq] : 0;
+            const int i = ok ? entry_row(bucket_q[qc + qq]) : 0;
             const long long off = (((long long)b * p.Nq + i) * p.Hq + (long long)r * G + gg) * D + ch * 8;
             cp_async16_zfill(sQ + swz<D>(row, ch), q + off, ok);
             cp_async16_zfill(sdO + swz<D>(row, ch), d_o + off, ok);
@@ -174,14 +174,14 @@ fused_bwd_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restrict__
         for (int idx = tid; idx < QCP * (DI / 8); idx += kThreads) {
             const int row = idx / (DI / 8), ch = idx % (DI / 8);
             const bool ok = row < nq;
-            const int i = ok ? bucket_q[qc + row] : 0;
+            const int i = ok ? entry_row(bucket_q[qc + row]) : 0;
             cp_async16_zfill(sQi + swz<DI>(row, ch), q_idx + (((long long)b * p.Nq + i) * p.Hkv + r) * DI + ch * 8, ok);
         }
         cp_async_commit();
         for (int row = tid; row < kQH; row += kThreads) {
             const int qq = row / G, gg = row % G;
             if (qq < nq) {
-                const int i = bucket_q[qc + qq];
+                const int i = entry_row(bucket_q[qc + qq]);
                 const long long hi = ((long long)b * p.Hq + r * G + gg) * p.Nq + i;
                 sLse2[row] = lse[hi] * kLog2e;
                 sDd[row] = Dg[hi];
@@ -192,7 +192,7 @@ fused_bwd_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restrict__
         }
         for (int row = tid; row < QCP; row += kThreads) {
             if (row < nq) {
-                const int i = bucket_q[qc + row];
+                const int i = entry_row(bucket_q[qc + row]);
                 sLsei2[row] = lse_idx[((long long)b * p.Hkv + r) * p.Nq + i] * kLog2e;
                 sPos[row] = i;   // q_offset == 0
             } else {
@@ -302,7 +302,7 @@ fused_bwd_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restrict__
                 const int qh = warp * 16 + g + half8 * 8;
                 const int qq = qh / G, gg = qh % G;
                 if (qq < nq) {
-                    const int i = bucket_q[qc + qq];
+                    const int i = entry_row(bucket_q[qc + qq]);
                     float *dst = dq_acc + (((long long)b * p.Nq + i) * p.Hq + (long long)r * G + gg) * D + hc * (D / 2);
 #pragma unroll
                     for (int n = 0; n < D / 16; ++n) {
@@ -422,7 +422,7 @@ fused_bwd_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restrict__
                 for (int half8 = 0; half8 < 2; ++half8) {
                     const int qq = mt * 16 + g + half8 * 8;
                     if (qq < nq) {
-                        const int i = bucket_q[qc + qq];
+                        const int i = entry_row(bucket_q[qc + qq]);
                         float *dst = dqi_acc + (((long long)b * p.Nq + i) * p.Hkv + r) * DI + warp * (DI / 4);
 #pragma unroll
                         for (int n = 0; n < NT; ++n) {

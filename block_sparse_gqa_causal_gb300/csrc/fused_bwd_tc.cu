@@ -149,35 +149,36 @@ fused_bwd_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restric
             cp_async16_zfill(sm + OFF_KI + o, kib + j * DI + ch * 8, ok);
         }
         cp_async_arrive_noinc(kv_full);
+        // entries of chunk m are fetched during chunk m-1; the per-row values
+        // that depend on them are loaded before waiting for a free stage
+        int ent = lane < min(QC, qend - qbeg) ? __ldg(bucket_q + qbeg + lane) : 0;
         for (int m = 0; m < nch; ++m) {
             const int s = m & 1;
+            const int q0 = qbeg + m * QC;
+            const int nq = min(QC, qend - q0);
+            const int ent_next = (m + 1 < nch && lane < min(QC, qend - q0 - QC)) ? __ldg(bucket_q + q0 + QC + lane) : 0;
+            // row values: lane = (query, head) row for lse2 / dd, lane = query for lsei2
+            const int my_q = lane < kNQI && lane < nq ? entry_row(ent) : 0;
+            const int rq = lane / G, rg = lane % G;
+            const bool rok = lane < QC * G && rq < nq;
+            const int ri = __shfl_sync(0xffffffffu, entry_row(ent), rq < 32 ? rq : 0);
+            const long long hi = ((long long)b * p.Hq + r * G + rg) * p.Nq + ri;
+            const float v_lse2 = rok ? __ldg(lse + hi) * kLog2e : INFINITY;
+            const float v_dd = rok ? __ldg(Dg + hi) : 0.f;
+            const bool qok = lane < kNQI && lane < nq;
+            const float v_lsei2 = qok ? __ldg(lse_idx + ((long long)b * p.Hkv + r) * p.Nq + my_q) * kLog2e : INFINITY;
             if (!tc::mbar_wait(&empty[s], ((uint32_t)(m >> 1) & 1u) ^ 1u, st, 21, abort_flag)) break;
             uint8_t *stg = sm + OFF_STG + s * STG_BYTES;
             StageRows *rows = reinterpret_cast<StageRows *>(stg + STG_ROWS);
-            const int q0 = qbeg + m * QC;
-            const int nq = min(QC, qend - q0);
-            // the chunk's query indices first (one global load each), then
-            // everything else addressed from shared memory
             if (lane < kNQI) {
-                const bool okq = lane < nq;
-                rows->qi[lane] = okq ? bucket_q[q0 + lane] : 0;
+                rows->qi[lane] = my_q;
+                rows->lsei2[lane] = v_lsei2;
+                rows->pos[lane] = qok ? my_q : -1;        // training layout: q_offset == 0
             }
+            rows->lse2[lane] = v_lse2;
+            rows->dd[lane] = v_dd;
             if (lane == 0) rows->nq = nq;
             __syncwarp();
-            {
-                const int qq = lane / G, g = lane % G;
-                const bool ok = lane < QC * G && qq < nq;
-                const int i = rows->qi[qq < kNQI ? qq : 0];
-                const long long hi = ((long long)b * p.Hq + r * G + g) * p.Nq + i;
-                rows->lse2[lane] = ok ? lse[hi] * kLog2e : INFINITY;
-                rows->dd[lane] = ok ? Dg[hi] : 0.f;
-                if (lane < kNQI) {
-                    const bool okq = lane < nq;
-                    rows->lsei2[lane] = okq ? lse_idx[((long long)b * p.Hkv + r) * p.Nq + rows->qi[lane]] * kLog2e
-                                            : INFINITY;
-                    rows->pos[lane] = okq ? rows->qi[lane] : -1;   // training layout: q_offset == 0
-                }
-            }
             // Q and dO rows (row rho = qq*G + g): 16 lanes per 256-byte row, 2 rows per step
 #pragma unroll 4
             for (int it = 0; it < kNQ / 2; ++it) {
@@ -199,6 +200,7 @@ fused_bwd_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restric
             }
             cp_async_arrive_noinc(&full[s]);
             tc::mbar_arrive(&full[s]);
+            ent = ent_next;
         }
         cp_async_wait<0>();
     } else if (warp == 1) {

@@ -8,6 +8,8 @@
 // the fill kernel replays the same rows with shared-memory cursors.  Entries
 // that are not a valid selection for their row (a block after the query's
 // own, or beyond the keys) are reported through the status word and skipped.
+// Each list entry packs the query row with the slot of the block in that
+// row's selection (see pack_entry), so consumers need no search.
 #include "msa_internal.h"
 
 namespace msa {
@@ -104,7 +106,7 @@ __global__ void __launch_bounds__(kThreads) index_fill_kernel(Problem p, const i
         const int c = base[x];
         const int i = (int)(x / p.topk);
         if (!valid_sel(p, c, i)) continue;
-        list[atomicAdd(&cursor[c], 1)] = i;
+        list[atomicAdd(&cursor[c], 1)] = pack_entry(i, (int)(x % p.topk));
     }
 }
 

@@ -84,6 +84,10 @@ cudaError_t launch_fused_bwd(const Problem &p, const bf16 *q, const bf16 *k, con
 // it.  cnt [nbk], off [nbk + 1], list [B*Hkv*Nq*topk]; scratch holds
 // inverse_index_scratch_ints(p) ints (per-CTA histograms and offsets).
 size_t inverse_index_scratch_ints(const Problem &p);
+// list entry: query row i (< 2^26) and the slot (< 32) of the block in i's selection
+__host__ __device__ __forceinline__ int32_t pack_entry(int i, int slot) { return (int32_t)(((uint32_t)slot << 26) | (uint32_t)i); }
+__host__ __device__ __forceinline__ int entry_row(int32_t e) { return (int)((uint32_t)e & 0x3FFFFFFu); }
+__host__ __device__ __forceinline__ int entry_slot(int32_t e) { return (int)((uint32_t)e >> 26); }
 cudaError_t launch_inverse_index(const Problem &p, const int32_t *sel, int32_t *cnt, int32_t *off, int32_t *scratch,
                                  int32_t *list, DeviceStatus *st, cudaStream_t s);
 

@@ -60,28 +60,33 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar)
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(bar)) : "memory");
 }
 
-// Resolves the chunk's queries once: index, position and the slot of block c
-// in the query's selection (all loads issued before any is consumed).
-__device__ __forceinline__ void fill_meta(int *mi, int *mpos, int *mslot, int qpc, int nq, int q0,
-                                          const int32_t *__restrict__ bucket_q, const int32_t *__restrict__ sel,
-                                          const Problem &p, int b, int r, int c, int lane)
+// Bucket entries of one chunk: lane handles query slots lane, lane+32, ...
+template <int EPL>
+__device__ __forceinline__ void load_entries(int (&e)[EPL], const int32_t *__restrict__ bucket_q, int q0, int nq,
+                                             int lane)
 {
-    for (int qq = lane; qq < qpc; qq += 32) {
-        int i = 0, pos = -1, slot = 0;
-        if (qq < nq) {
-            i = bucket_q[q0 + qq];
-            pos = p.q_offset + i;
-            const int32_t *srow = sel + (((long long)b * p.Hkv + r) * p.Nq + i) * p.topk;
-            int v[32];
 #pragma unroll
-            for (int t = 0; t < 32; ++t) v[t] = t < p.topk ? __ldg(srow + t) : -1;
+    for (int t = 0; t < EPL; ++t) {
+        const int qq = lane + 32 * t;
+        e[t] = qq < nq ? __ldg(bucket_q + q0 + qq) : 0;
+    }
+}
+
+// Writes the chunk's metadata (query row, position, slot) from its entries.
+template <int EPL>
+__device__ __forceinline__ void store_meta(int *mi, int *mpos, int *mslot, const int (&e)[EPL], int qpc, int nq,
+                                           const Problem &p, int lane)
+{
 #pragma unroll
-            for (int t = 0; t < 32; ++t)
-                if (v[t] == c) slot = t;
+    for (int t = 0; t < EPL; ++t) {
+        const int qq = lane + 32 * t;
+        if (qq < qpc) {
+            const bool ok = qq < nq;
+            const int i = ok ? entry_row(e[t]) : 0;
+            mi[qq] = i;
+            mpos[qq] = ok ? p.q_offset + i : -1;
+            mslot[qq] = ok ? entry_slot(e[t]) : 0;
         }
-        mi[qq] = i;
-        mpos[qq] = pos;
-        mslot[qq] = slot;
     }
 }
 
@@ -149,13 +154,18 @@ sparse_fwd_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restri
             cp_async16_zfill(sm + L::OFF_V + o, vb + j * jstride + ch * 8, ok);
         }
         cp_async_arrive_noinc(kv_full);
+        constexpr int EPL = (QPC + 31) / 32;
+        int ent[EPL], ent_next[EPL];
+        load_entries(ent, bucket_q, qbeg, min(QPC, qend - qbeg), lane);
         for (int m = 0; m < nch; ++m) {
             const int a = m & 1;
-            if (!tc::mbar_wait(&q_empty[a], ((uint32_t)(m >> 1) & 1u) ^ 1u, st, 61, abort_flag)) break;
-            QueryMeta *meta = reinterpret_cast<QueryMeta *>(sm + L::OFF_META + a * 2048);
             const int q0 = qbeg + m * QPC;
             const int nq = min(QPC, qend - q0);
-            fill_meta(meta->i, meta->pos, meta->slot, QPC, nq, q0, bucket_q, sel, p, b, r, c, lane);
+            // the next chunk's entries are fetched before waiting for a free stage
+            if (m + 1 < nch) load_entries(ent_next, bucket_q, q0 + QPC, min(QPC, qend - q0 - QPC), lane);
+            if (!tc::mbar_wait(&q_empty[a], ((uint32_t)(m >> 1) & 1u) ^ 1u, st, 61, abort_flag)) break;
+            QueryMeta *meta = reinterpret_cast<QueryMeta *>(sm + L::OFF_META + a * 2048);
+            store_meta(meta->i, meta->pos, meta->slot, ent, QPC, nq, p, lane);
             if (lane == 0) meta->nq = nq;
             __syncwarp();
             // Q rows: lanes cover whole 16-byte chunks of consecutive rows; the
@@ -174,6 +184,8 @@ sparse_fwd_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restri
             }
             cp_async_arrive_noinc(&q_full[a]);
             tc::mbar_arrive(&q_full[a]);
+#pragma unroll
+            for (int t = 0; t < EPL; ++t) ent[t] = ent_next[t];
         }
         cp_async_wait<0>();
     } else if (warp == 1) {
