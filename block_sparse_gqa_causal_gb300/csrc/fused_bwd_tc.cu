@@ -84,9 +84,11 @@ __device__ __forceinline__ int qsel(const int (&qis)[N], int qq)
 
 template <int G>
 __global__ void __launch_bounds__(kThreads, 1)
-fused_bwd_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 *__restrict__ v,
+fused_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_do,
+                    const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                    const __grid_constant__ CUtensorMap tmap_ki, Problem p, const bf16 *__restrict__ q,
                     const bf16 *__restrict__ d_o, const float *__restrict__ lse, const bf16 *__restrict__ q_idx,
-                    const bf16 *__restrict__ k_idx, const float *__restrict__ lse_idx, float kl_coef,
+                    const float *__restrict__ lse_idx, float kl_coef,
                     const float *__restrict__ Dg, const int32_t *__restrict__ bucket_off,
                     const int32_t *__restrict__ bucket_q, bf16 *__restrict__ dk, bf16 *__restrict__ dv,
                     float *__restrict__ dq_acc, float *__restrict__ dqi_acc, float *__restrict__ dki_acc,
@@ -101,7 +103,8 @@ fused_bwd_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restric
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(dq_free + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
-    const int c = blockIdx.x, r = blockIdx.y, b = blockIdx.z;
+    // x = group, y = key block: the heavy early blocks of every group start first
+    const int r = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
     constexpr int QC = (kNQ / G < kNQI) ? kNQ / G : kNQI;   // queries per chunk
     const long long j0 = (long long)c * kKeys;
     const long long bucket = ((long long)b * p.Hkv + r) * p.nb + c;
@@ -111,10 +114,12 @@ fused_bwd_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restric
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            tc::mbar_init(&full[s], 64);                    // 32 cp.async arrivals + 32 row-data arrivals
+            // 32 cp.async arrivals + 32 row-data arrivals (+ lane 0's expect_tx
+            // arrival for the TMA-loaded Q and dO rows when G == 8)
+            tc::mbar_init(&full[s], G == 8 ? 65 : 64);
             tc::mbar_init(&empty[s], 1 + kEpiWarps);        // grads MMAs done + epilogue has read the rows
         }
-        tc::mbar_init(kv_full, 32);
+        tc::mbar_init(kv_full, 1);
         tc::mbar_init(s_full, 1);
         tc::mbar_init(tm_free, kEpiWarps);
         tc::mbar_init(p_full, kEpiWarps);
@@ -134,21 +139,28 @@ fused_bwd_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restric
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ------------------------------------------------ producer (cp.async)
-        const long long jstride = (long long)p.Hkv * D;
-        const bf16 *kb = k + ((long long)b * p.kv_rows * p.Hkv + r) * D;
-        const bf16 *vb = v + ((long long)b * p.kv_rows * p.Hkv + r) * D;
-        const bf16 *kib = k_idx + (long long)b * p.kv_rows * DI;
-        for (int idx = lane; idx < kKeys * 16; idx += 32) {
-            const int row = idx >> 4, ch = idx & 15, h = ch >> 3, c8 = ch & 7;
-            const bool ok = j0 + row < p.Nk;
-            const long long j = ok ? j0 + row : j0;
-            const int o = h * SUB + swz(row, c8);
-            cp_async16_zfill(sm + OFF_K + o, kb + j * jstride + ch * 8, ok);
-            cp_async16_zfill(sm + OFF_V + o, vb + j * jstride + ch * 8, ok);
-            cp_async16_zfill(sm + OFF_KI + o, kib + j * DI + ch * 8, ok);
+        // ------------------------------------------------ producer
+        // K, V and K_idx tiles of this (b, group, block) by TMA; rows past Nk read as zeros
+        if (lane == 0) {
+            tc::prefetch_tmap(&tmap_q);
+            tc::prefetch_tmap(&tmap_do);
+            tc::mbar_arrive_expect_tx(kv_full, 6 * SUB);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                tc::tma_load_4d(sm + OFF_K + h * SUB, &tmap_k, kv_full, h * 64, r, (int)j0, b);
+                tc::tma_load_4d(sm + OFF_V + h * SUB, &tmap_v, kv_full, h * 64, r, (int)j0, b);
+                tc::tma_load_3d(sm + OFF_KI + h * SUB, &tmap_ki, kv_full, h * 64, (int)j0, b);
+            }
         }
-        cp_async_arrive_noinc(kv_full);
+        if constexpr (QC < kNQI) {
+            // q_idx rows QC..kNQI-1 of both stages are never loaded: zero them once
+            for (int x = lane; x < kStages * 2 * (kNQI - QC) * 8; x += 32) {
+                const int st_ = x / (2 * (kNQI - QC) * 8), y = x % (2 * (kNQI - QC) * 8);
+                const int h = y / ((kNQI - QC) * 8), row = QC + (y / 8) % (kNQI - QC), ch = y % 8;
+                *reinterpret_cast<uint4 *>(sm + OFF_STG + st_ * STG_BYTES + STG_QI + h * (kNQI * 128) + swz(row, ch)) =
+                    make_uint4(0, 0, 0, 0);
+            }
+        }
         // entries of chunk m are fetched during chunk m-1; the per-row values
         // that depend on them are loaded before waiting for a free stage
         int ent = lane < min(QC, qend - qbeg) ? __ldg(bucket_q + qbeg + lane) : 0;
@@ -179,24 +191,41 @@ fused_bwd_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restric
             rows->dd[lane] = v_dd;
             if (lane == 0) rows->nq = nq;
             __syncwarp();
-            // Q and dO rows (row rho = qq*G + g): 16 lanes per 256-byte row, 2 rows per step
+            if constexpr (G == 8) {
+                // Q and dO: one TMA box {64 features, 8 heads} per query and half
+                // (1024 bytes, on a swizzle-pattern boundary); padding slots read
+                // rows past the end of the tensors (zero fill)
+                if (lane == 0) tc::mbar_arrive_expect_tx(&full[s], 2 * kNQ * D * 2);
+                __syncwarp();
+                if (lane < 2 * QC) {
+                    const int qq = lane >> 1, h = lane & 1;
+                    const int z = qq < nq ? b * p.Nq + rows->qi[qq] : p.B * p.Nq;
+                    tc::tma_load_3d(stg + STG_Q + h * (kNQ * 128) + qq * 1024, &tmap_q, &full[s], h * 64, r * G, z);
+                    tc::tma_load_3d(stg + STG_DO + h * (kNQ * 128) + qq * 1024, &tmap_do, &full[s], h * 64, r * G, z);
+                }
+            } else {
+                // Q and dO rows (row rho = qq*G + g): 16 lanes per 256-byte row, 2 rows per step
 #pragma unroll 4
-            for (int it = 0; it < kNQ / 2; ++it) {
-                const int rho = it * 2 + (lane >> 4), ch = lane & 15;
-                const int qq = rho / G, g = rho % G;
-                const bool ok = rho < QC * G && qq < nq;
-                const int i = rows->qi[qq < kNQI ? qq : 0];
-                const long long off = (((long long)b * p.Nq + i) * p.Hq + (long long)r * G + g) * D + ch * 8;
-                const int o = (ch >> 3) * (kNQ * 128) + swz(rho, ch & 7);
-                cp_async16_zfill(stg + STG_Q + o, q + off, ok);
-                cp_async16_zfill(stg + STG_DO + o, d_o + off, ok);
+                for (int it = 0; it < kNQ / 2; ++it) {
+                    const int rho = it * 2 + (lane >> 4), ch = lane & 15;
+                    const int qq = rho / G, g = rho % G;
+                    const bool ok = rho < QC * G && qq < nq;
+                    const int i = rows->qi[qq < kNQI ? qq : 0];
+                    const long long off = (((long long)b * p.Nq + i) * p.Hq + (long long)r * G + g) * D + ch * 8;
+                    const int o = (ch >> 3) * (kNQ * 128) + swz(rho, ch & 7);
+                    cp_async16_zfill(stg + STG_Q + o, q + off, ok);
+                    cp_async16_zfill(stg + STG_DO + o, d_o + off, ok);
+                }
             }
-#pragma unroll 4
-            for (int it = 0; it < kNQI / 2; ++it) {
+            // q_idx rows of the chunk's queries (zero for padding slots)
+#pragma unroll
+            for (int it = 0; it < (QC * 16 + 31) / 32; ++it) {
                 const int row = it * 2 + (lane >> 4), ch = lane & 15;
-                const bool ok = row < nq;
-                cp_async16_zfill(stg + STG_QI + (ch >> 3) * (kNQI * 128) + swz(row, ch & 7),
-                                 q_idx + (((long long)b * p.Nq + rows->qi[row]) * p.Hkv + r) * DI + ch * 8, ok);
+                if (row < QC) {
+                    const bool ok = row < nq;
+                    cp_async16_zfill(stg + STG_QI + (ch >> 3) * (kNQI * 128) + swz(row, ch & 7),
+                                     q_idx + (((long long)b * p.Nq + rows->qi[row]) * p.Hkv + r) * DI + ch * 8, ok);
+                }
             }
             cp_async_arrive_noinc(&full[s]);
             tc::mbar_arrive(&full[s]);
@@ -454,9 +483,29 @@ cudaError_t launch_g(const Problem &p, const bf16 *q, const bf16 *k, const bf16 
 {
     cudaError_t e = cudaFuncSetAttribute(fused_bwd_tc_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    fused_bwd_tc_kernel<G><<<dim3(p.nb, p.Hkv, p.B), kThreads, SMEM_ALLOC, s>>>(
-        p, q, k, v, d_o, lse, q_idx, k_idx, lse_idx, kl_coef, w.D, w.bucket_off, w.bucket_q, dk, dv, w.dq_acc,
-        w.dqi_acc, w.dki_acc, st);
+    CUtensorMap tq, tdo, tk, tv, tki;
+    {
+        const unsigned long long dq[3] = {(unsigned long long)D, (unsigned long long)p.Hq, (unsigned long long)p.B * p.Nq};
+        const unsigned long long sq[2] = {D * 2ull, (unsigned long long)p.Hq * D * 2ull};
+        const unsigned bq[3] = {64, (unsigned)G, 1};
+        if ((e = make_tmap_bf16(&tq, q, 3, dq, sq, bq)) != cudaSuccess) return e;
+        if ((e = make_tmap_bf16(&tdo, d_o, 3, dq, sq, bq)) != cudaSuccess) return e;
+        // K/V as [B][Nk][Hkv][D], K_idx as [B][Nk][DI] (rows past Nk are out of bounds)
+        const unsigned long long dk4[4] = {(unsigned long long)D, (unsigned long long)p.Hkv, (unsigned long long)p.Nk,
+                                           (unsigned long long)p.B};
+        const unsigned long long sk[3] = {D * 2ull, (unsigned long long)p.Hkv * D * 2ull,
+                                          (unsigned long long)p.kv_rows * p.Hkv * D * 2ull};
+        const unsigned bk[4] = {64, 1, (unsigned)kKeys, 1};
+        if ((e = make_tmap_bf16(&tk, k, 4, dk4, sk, bk)) != cudaSuccess) return e;
+        if ((e = make_tmap_bf16(&tv, v, 4, dk4, sk, bk)) != cudaSuccess) return e;
+        const unsigned long long di[3] = {(unsigned long long)DI, (unsigned long long)p.Nk, (unsigned long long)p.B};
+        const unsigned long long si[2] = {DI * 2ull, (unsigned long long)p.kv_rows * DI * 2ull};
+        const unsigned bi[3] = {64, (unsigned)kKeys, 1};
+        if ((e = make_tmap_bf16(&tki, k_idx, 3, di, si, bi)) != cudaSuccess) return e;
+    }
+    fused_bwd_tc_kernel<G><<<dim3(p.Hkv, p.nb, p.B), kThreads, SMEM_ALLOC, s>>>(
+        tq, tdo, tk, tv, tki, p, q, d_o, lse, q_idx, lse_idx, kl_coef, w.D, w.bucket_off, w.bucket_q, dk, dv,
+        w.dq_acc, w.dqi_acc, w.dki_acc, st);
     note_launch();
     return cudaGetLastError();
 }

@@ -94,14 +94,16 @@ __device__ __forceinline__ void store_meta(int *mi, int *mpos, int *mslot, const
 
 template <int D, int DI, int G>
 __global__ void __launch_bounds__(kThreads, 1)
-kl_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 *__restrict__ q_idx,
-             const bf16 *__restrict__ k_idx, const int32_t *__restrict__ sel, const float *__restrict__ lse,
+kl_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+             const __grid_constant__ CUtensorMap tmap_ki, Problem p, const bf16 *__restrict__ q,
+             const bf16 *__restrict__ q_idx, const float *__restrict__ lse,
              const int32_t *__restrict__ bucket_off, const int32_t *__restrict__ bucket_q,
              float4 *__restrict__ part, DeviceStatus *st)
 {
     using L = KlLayout<D, DI, G>;
     constexpr int QPC = L::QPC, NS = L::NS;
-    const int c = blockIdx.x, r = blockIdx.y, b = blockIdx.z;
+    // x = group, y = key block: the heavy early blocks of every group start first
+    const int r = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
     const long long bucket = ((long long)b * p.Hkv + r) * p.nb + c;
     const int qbeg = bucket_off[bucket], qend = bucket_off[bucket + 1];
     if (qend <= qbeg) return;
@@ -118,12 +120,14 @@ kl_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restrict__ k, 
 
     if (threadIdx.x == 0) {
         for (int a = 0; a < 2; ++a) {
-            tc::mbar_init(&q_full[a], 64);
+            // 32 cp.async arrivals + 32 metadata arrivals (+ lane 0's expect_tx
+            // arrival for the TMA-loaded Q rows when G == 8)
+            tc::mbar_init(&q_full[a], G == 8 ? 65 : 64);
             tc::mbar_init(&q_empty[a], 1 + kEpiWarps);
             tc::mbar_init(&s_full[a], 1);
             tc::mbar_init(&s_free[a], kEpiWarps);
         }
-        tc::mbar_init(kv_full, 32);
+        tc::mbar_init(kv_full, 1);
         *abort_flag = 0;
         tc::fence_mbar_init();
     }
@@ -138,42 +142,68 @@ kl_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restrict__ k, 
 
     if (warp == 0) {
         // ------------------------------------------------ producer
-        const long long jstride = (long long)p.Hkv * D;
-        const bf16 *kb = k + ((long long)b * p.kv_rows * p.Hkv + r) * D;
-        const bf16 *kib = k_idx + (long long)b * p.kv_rows * DI;
-        for (int idx = lane; idx < kKeys * (D / 8); idx += 32) {
-            const int row = idx / (D / 8), ch = idx % (D / 8);
-            const bool ok = j0 + row < p.Nk;
-            const long long j = ok ? j0 + row : j0;
-            cp_async16_zfill(sm + L::OFF_K + (ch >> 3) * SUB + swz(row, ch & 7), kb + j * jstride + ch * 8, ok);
+        // K and K_idx tiles of this (b, group, block) by TMA; rows past Nk read as zeros
+        if (lane == 0) {
+            tc::prefetch_tmap(&tmap_q);
+            tc::mbar_arrive_expect_tx(kv_full, (D / 64 + DI / 64) * SUB);
+#pragma unroll
+            for (int kb = 0; kb < D / 64; ++kb)
+                tc::tma_load_4d(sm + L::OFF_K + kb * SUB, &tmap_k, kv_full, kb * 64, r, (int)j0, b);
+#pragma unroll
+            for (int kb = 0; kb < DI / 64; ++kb)
+                tc::tma_load_3d(sm + L::OFF_KI + kb * SUB, &tmap_ki, kv_full, kb * 64, (int)j0, b);
         }
-        for (int idx = lane; idx < kKeys * (DI / 8); idx += 32) {
-            const int row = idx / (DI / 8), ch = idx % (DI / 8);
-            const bool ok = j0 + row < p.Nk;
-            const long long j = ok ? j0 + row : j0;
-            cp_async16_zfill(sm + L::OFF_KI + (ch >> 3) * SUB + swz(row, ch & 7), kib + j * DI + ch * 8, ok);
-        }
-        cp_async_arrive_noinc(kv_full);
         constexpr int EPL = (QPC + 31) / 32;
+        constexpr int RPL = kRows / 32;                       // (query, head) rows per lane
         int ent[EPL], ent_next[EPL];
         load_entries(ent, bucket_q, qbeg, min(QPC, qend - qbeg), lane);
         for (int m = 0; m < nch; ++m) {
             const int a = m & 1;
             const int q0 = qbeg + m * QPC;
             const int nq = min(QPC, qend - q0);
+            // this chunk's LSE values and the next chunk's entries are fetched
+            // before waiting for a free stage
+            float lv[RPL];
+#pragma unroll
+            for (int t = 0; t < RPL; ++t) {
+                const int rho = lane + 32 * t, qq = rho / G, g = rho % G;
+                int e = 0;
+#pragma unroll
+                for (int u = 0; u < EPL; ++u) {
+                    const int v = __shfl_sync(0xffffffffu, ent[u], qq & 31);
+                    if ((qq >> 5) == u) e = v;
+                }
+                lv[t] = qq < nq ? __ldg(lse + ((long long)b * p.Hq + r * G + g) * p.Nq + entry_row(e)) : 0.f;
+            }
             if (m + 1 < nch) load_entries(ent_next, bucket_q, q0 + QPC, min(QPC, qend - q0 - QPC), lane);
             if (!tc::mbar_wait(&q_empty[a], ((uint32_t)(m >> 1) & 1u) ^ 1u, st, 81, abort_flag)) break;
             KlMeta *meta = reinterpret_cast<KlMeta *>(sm + L::OFF_META + a * L::META_BYTES);
             store_meta(meta->i, meta->pos, meta->slot, ent, QPC, nq, p, lane);
             if (lane == 0) meta->nq = nq;
-            __syncwarp();
-            for (int rho = lane; rho < kRows; rho += 32) {
-                const int qq = rho / G, g = rho % G;
-                meta->lse2[rho] = qq < nq ? lse[((long long)b * p.Hq + r * G + g) * p.Nq + meta->i[qq]] * kLog2e
-                                          : INFINITY;
+#pragma unroll
+            for (int t = 0; t < RPL; ++t) {
+                const int rho = lane + 32 * t;
+                meta->lse2[rho] = rho / G < nq ? lv[t] * kLog2e : INFINITY;
             }
+            __syncwarp();
             uint8_t *sq = sm + L::OFF_Q + a * ((D / 64) * SUB);
-            {
+            if constexpr (G == 8) {
+                // one TMA box {64 features, 8 heads} per query and 64-feature half:
+                // 1024 bytes, so every box starts on a swizzle-pattern boundary.
+                // Padding slots read rows past the end of q (zero fill).
+                if (lane == 0) tc::mbar_arrive_expect_tx(&q_full[a], kRows * D * 2);
+                __syncwarp();
+#pragma unroll
+                for (int t = 0; t < EPL; ++t) {
+                    const int qq = lane + 32 * t;
+                    if (qq < QPC) {
+                        const int z = qq < nq ? b * p.Nq + entry_row(ent[t]) : p.B * p.Nq;
+#pragma unroll
+                        for (int kb = 0; kb < D / 64; ++kb)
+                            tc::tma_load_3d(sq + kb * SUB + qq * (G * 128), &tmap_q, &q_full[a], kb * 64, r * G, z);
+                    }
+                }
+            } else {
                 constexpr int CPR = D / 8, RPI = 32 / CPR;
 #pragma unroll 8
                 for (int it = 0; it < kRows / RPI; ++it) {
@@ -386,7 +416,25 @@ cudaError_t launch_ddg(const Problem &p, const bf16 *q, const bf16 *k, const bf1
     using L = KlLayout<D, DI, G>;
     cudaError_t e = cudaFuncSetAttribute(kl_tc_kernel<D, DI, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
-    kl_tc_kernel<D, DI, G><<<dim3(p.nb, p.Hkv, p.B), kThreads, L::ALLOC, s>>>(p, q, k, q_idx, k_idx, sel, lse,
+    CUtensorMap tq, tk, tki;
+    {
+        const unsigned long long dq[3] = {(unsigned long long)D, (unsigned long long)p.Hq, (unsigned long long)p.B * p.Nq};
+        const unsigned long long sq[2] = {D * 2ull, (unsigned long long)p.Hq * D * 2ull};
+        const unsigned bq[3] = {64, (unsigned)G, 1};
+        if ((e = make_tmap_bf16(&tq, q, 3, dq, sq, bq)) != cudaSuccess) return e;
+        // K as [B][Nk][Hkv][D], K_idx as [B][Nk][DI] (rows past Nk are out of bounds)
+        const unsigned long long dk[4] = {(unsigned long long)D, (unsigned long long)p.Hkv, (unsigned long long)p.Nk,
+                                          (unsigned long long)p.B};
+        const unsigned long long sk[3] = {D * 2ull, (unsigned long long)p.Hkv * D * 2ull,
+                                          (unsigned long long)p.kv_rows * p.Hkv * D * 2ull};
+        const unsigned bk[4] = {64, 1, (unsigned)kKeys, 1};
+        if ((e = make_tmap_bf16(&tk, k, 4, dk, sk, bk)) != cudaSuccess) return e;
+        const unsigned long long di[3] = {(unsigned long long)DI, (unsigned long long)p.Nk, (unsigned long long)p.B};
+        const unsigned long long si[2] = {DI * 2ull, (unsigned long long)p.kv_rows * DI * 2ull};
+        const unsigned bi[3] = {64, (unsigned)kKeys, 1};
+        if ((e = make_tmap_bf16(&tki, k_idx, 3, di, si, bi)) != cudaSuccess) return e;
+    }
+    kl_tc_kernel<D, DI, G><<<dim3(p.Hkv, p.nb, p.B), kThreads, L::ALLOC, s>>>(tq, tk, tki, p, q, q_idx, lse,
                                                                              w.bucket_off, w.bucket_q, w.part, st);
     note_launch();
     return cudaGetLastError();

@@ -28,6 +28,9 @@ void note_launch(int n = 1);
 cudaError_t make_tmap_bf16_3d(CUtensorMap *map, const void *base, unsigned long long d0, unsigned long long d1,
                               unsigned long long d2, unsigned long long stride1_bytes,
                               unsigned long long stride2_bytes, unsigned box0, unsigned box1);
+// Same for rank 1..5: dims innermost first, rank-1 strides in bytes, box per dim.
+cudaError_t make_tmap_bf16(CUtensorMap *map, const void *base, int rank, const unsigned long long *dims,
+                           const unsigned long long *strides_bytes, const unsigned *box);
 
 // Index branch: token scores + block max-pool.  bs: [B, Nq, Hkv, nb] fp32.
 cudaError_t launch_index_scores(const Problem &p, const bf16 *q_idx, const bf16 *k_idx, float *bs,

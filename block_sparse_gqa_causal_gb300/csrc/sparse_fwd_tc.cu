@@ -92,14 +92,16 @@ __device__ __forceinline__ void store_meta(int *mi, int *mpos, int *mslot, const
 
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
-sparse_fwd_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restrict__ k, const bf16 *__restrict__ v,
-                     const int32_t *__restrict__ sel, const int32_t *__restrict__ bucket_off,
+sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                     const __grid_constant__ CUtensorMap tmap_v, Problem p, const bf16 *__restrict__ q,
+                     const int32_t *__restrict__ bucket_off,
                      const int32_t *__restrict__ bucket_q, bf16 *__restrict__ part, float2 *__restrict__ stats,
                      DeviceStatus *st)
 {
     using L = FwdLayout<D>;
     constexpr int QPC = kRows / G;                          // queries per chunk
-    const int c = blockIdx.x, r = blockIdx.y, b = blockIdx.z;
+    // x = group, y = key block: the heavy early blocks of every group start first
+    const int r = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
     const long long bucket = ((long long)b * p.Hkv + r) * p.nb + c;
     const int qbeg = bucket_off[bucket], qend = bucket_off[bucket + 1];
     if (qend <= qbeg) return;                               // nobody selected this block
@@ -118,7 +120,9 @@ sparse_fwd_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restri
 
     if (threadIdx.x == 0) {
         for (int a = 0; a < 2; ++a) {
-            tc::mbar_init(&q_full[a], 64);              // 32 cp.async arrivals + 32 metadata arrivals
+            // G == 8: lane 0's expect_tx arrival + 32 metadata arrivals (TMA bytes);
+            // otherwise 32 cp.async arrivals + 32 metadata arrivals
+            tc::mbar_init(&q_full[a], G == 8 ? 33 : 64);
             tc::mbar_init(&q_empty[a], 1 + kEpiWarps);  // S MMAs done + epilogue has read the metadata
             tc::mbar_init(&s_full[a], 1);
             tc::mbar_init(&s_free[a], kEpiWarps);
@@ -127,7 +131,7 @@ sparse_fwd_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restri
             tc::mbar_init(&o_full[a], 1);
             tc::mbar_init(&o_free[a], kEpiWarps);
         }
-        tc::mbar_init(kv_full, 32);
+        tc::mbar_init(kv_full, 1);
         *abort_flag = 0;
         tc::fence_mbar_init();
     }
@@ -142,18 +146,16 @@ sparse_fwd_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restri
 
     if (warp == 0) {
         // ------------------------------------------------ producer
-        const long long jstride = (long long)p.Hkv * D;
-        const bf16 *kb = k + ((long long)b * p.kv_rows * p.Hkv + r) * D;
-        const bf16 *vb = v + ((long long)b * p.kv_rows * p.Hkv + r) * D;
-        for (int idx = lane; idx < kKeys * (D / 8); idx += 32) {
-            const int row = idx / (D / 8), ch = idx % (D / 8);
-            const bool ok = j0 + row < p.Nk;
-            const long long j = ok ? j0 + row : j0;
-            const int o = (ch >> 3) * SUB + swz(row, ch & 7);
-            cp_async16_zfill(sm + L::OFF_K + o, kb + j * jstride + ch * 8, ok);
-            cp_async16_zfill(sm + L::OFF_V + o, vb + j * jstride + ch * 8, ok);
+        // K and V tiles of this (b, group, block) by TMA; rows past Nk read as zeros
+        if (lane == 0) {
+            tc::prefetch_tmap(&tmap_q);
+            tc::mbar_arrive_expect_tx(kv_full, 2 * L::KB * SUB);
+#pragma unroll
+            for (int kb = 0; kb < L::KB; ++kb) {
+                tc::tma_load_4d(sm + L::OFF_K + kb * SUB, &tmap_k, kv_full, kb * 64, r, (int)j0, b);
+                tc::tma_load_4d(sm + L::OFF_V + kb * SUB, &tmap_v, kv_full, kb * 64, r, (int)j0, b);
+            }
         }
-        cp_async_arrive_noinc(kv_full);
         constexpr int EPL = (QPC + 31) / 32;
         int ent[EPL], ent_next[EPL];
         load_entries(ent, bucket_q, qbeg, min(QPC, qend - qbeg), lane);
@@ -168,22 +170,41 @@ sparse_fwd_tc_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restri
             store_meta(meta->i, meta->pos, meta->slot, ent, QPC, nq, p, lane);
             if (lane == 0) meta->nq = nq;
             __syncwarp();
-            // Q rows: lanes cover whole 16-byte chunks of consecutive rows; the
-            // query index comes from the metadata just written (shared memory)
             uint8_t *sq = sm + L::OFF_Q + a * (L::KB * SUB);
-            constexpr int CPR = D / 8;                     // 16-byte chunks per row
-            constexpr int RPI = 32 / CPR;                  // rows per iteration
+            if constexpr (G == 8) {
+                // one TMA box {64 features, 8 heads} per query and 64-feature half:
+                // 1024 bytes, so every box starts on a swizzle-pattern boundary.
+                // Padding slots read rows past the end of q (zero fill).
+                if (lane == 0) tc::mbar_arrive_expect_tx(&q_full[a], kRows * D * 2);
+                __syncwarp();
+#pragma unroll
+                for (int t = 0; t < EPL; ++t) {
+                    const int qq = lane + 32 * t;
+                    if (qq < QPC) {
+                        const int z = qq < nq ? b * p.Nq + entry_row(ent[t]) : p.B * p.Nq;
+#pragma unroll
+                        for (int kb = 0; kb < L::KB; ++kb)
+                            tc::tma_load_3d(sq + kb * SUB + qq * (G * 128), &tmap_q, &q_full[a], kb * 64, r * G, z);
+                    }
+                }
+                tc::mbar_arrive(&q_full[a]);
+            } else {
+                // Q rows: lanes cover whole 16-byte chunks of consecutive rows; the
+                // query index comes from the metadata just written (shared memory)
+                constexpr int CPR = D / 8;                     // 16-byte chunks per row
+                constexpr int RPI = 32 / CPR;                  // rows per iteration
 #pragma unroll 8
-            for (int it = 0; it < kRows / RPI; ++it) {
-                const int rho = it * RPI + lane / CPR, ch = lane % CPR;
-                const int qq = rho / G, g = rho % G;
-                const bool ok = qq < nq;
-                const int i = meta->i[qq];
-                cp_async16_zfill(sq + (ch >> 3) * SUB + swz(rho, ch & 7),
-                                 q + (((long long)b * p.Nq + i) * p.Hq + (long long)r * G + g) * D + ch * 8, ok);
+                for (int it = 0; it < kRows / RPI; ++it) {
+                    const int rho = it * RPI + lane / CPR, ch = lane % CPR;
+                    const int qq = rho / G, g = rho % G;
+                    const bool ok = qq < nq;
+                    const int i = meta->i[qq];
+                    cp_async16_zfill(sq + (ch >> 3) * SUB + swz(rho, ch & 7),
+                                     q + (((long long)b * p.Nq + i) * p.Hq + (long long)r * G + g) * D + ch * 8, ok);
+                }
+                cp_async_arrive_noinc(&q_full[a]);
+                tc::mbar_arrive(&q_full[a]);
             }
-            cp_async_arrive_noinc(&q_full[a]);
-            tc::mbar_arrive(&q_full[a]);
 #pragma unroll
             for (int t = 0; t < EPL; ++t) ent[t] = ent_next[t];
         }
@@ -441,8 +462,23 @@ cudaError_t launch_dg(const Problem &p, const bf16 *q, const bf16 *k, const bf16
     using L = FwdLayout<D>;
     cudaError_t e = cudaFuncSetAttribute(sparse_fwd_tc_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
-    sparse_fwd_tc_kernel<D, G><<<dim3(p.nb, p.Hkv, p.B), kThreads, L::ALLOC, s>>>(
-        p, q, k, v, sel, w.bucket_off, w.bucket_q, w.part, w.stats, st);
+    CUtensorMap tq, tk, tv;
+    {
+        const unsigned long long dq[3] = {(unsigned long long)D, (unsigned long long)p.Hq, (unsigned long long)p.B * p.Nq};
+        const unsigned long long sq[2] = {D * 2ull, (unsigned long long)p.Hq * D * 2ull};
+        const unsigned bq[3] = {64, (unsigned)G, 1};
+        if ((e = make_tmap_bf16(&tq, q, 3, dq, sq, bq)) != cudaSuccess) return e;
+        // K/V as [B][Nk][Hkv][D] (rows past Nk, even inside kv_rows, are out of bounds)
+        const unsigned long long dk[4] = {(unsigned long long)D, (unsigned long long)p.Hkv, (unsigned long long)p.Nk,
+                                          (unsigned long long)p.B};
+        const unsigned long long sk[3] = {D * 2ull, (unsigned long long)p.Hkv * D * 2ull,
+                                          (unsigned long long)p.kv_rows * p.Hkv * D * 2ull};
+        const unsigned bk[4] = {64, 1, (unsigned)kKeys, 1};
+        if ((e = make_tmap_bf16(&tk, k, 4, dk, sk, bk)) != cudaSuccess) return e;
+        if ((e = make_tmap_bf16(&tv, v, 4, dk, sk, bk)) != cudaSuccess) return e;
+    }
+    sparse_fwd_tc_kernel<D, G><<<dim3(p.Hkv, p.nb, p.B), kThreads, L::ALLOC, s>>>(
+        tq, tk, tv, p, q, w.bucket_off, w.bucket_q, w.part, w.stats, st);
     note_launch();
     return cudaGetLastError();
 }
