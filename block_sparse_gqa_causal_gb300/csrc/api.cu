@@ -131,11 +131,18 @@ size_t kl_bytes(const Problem &p)
     return align256((size_t)p.B * p.Hkv * p.Nq * p.topk * 4 * 16) + index_bytes(p);
 }
 
+// backward: D, dK_idx accumulators, the inverse index, and either the
+// per-slot partials + teacher (tcgen05 path) or fp32 dQ / dq_idx accumulators
 size_t bwd_bytes(const Problem &p)
 {
-    return align256((size_t)p.B * p.Hq * p.Nq * 4) + align256((size_t)p.B * p.Nq * p.Hq * p.d * 4) +
-           align256((size_t)p.B * p.Nq * p.Hkv * p.d_idx * 4) + align256((size_t)p.B * p.Nk * p.d_idx * 4) +
-           index_bytes(p);
+    size_t n = align256((size_t)p.B * p.Hq * p.Nq * 4) + align256((size_t)p.B * p.Nk * p.d_idx * 4) + index_bytes(p);
+    const size_t slots = (size_t)p.B * p.Nq * p.topk;
+    if (bwd_tc(p))
+        n += align256(slots * p.Hq * p.d * 2) + align256(slots * p.Hkv * p.d_idx * 2) +
+             align256(slots * p.Hkv * 128 * 2);
+    else
+        n += align256((size_t)p.B * p.Nq * p.Hq * p.d * 4) + align256((size_t)p.B * p.Nq * p.Hkv * p.d_idx * 4);
+    return n;
 }
 
 #define REQUIRE_PTR(ptr, name)                                                                         \
@@ -305,13 +312,19 @@ msa_status msa_fused_bwd(const msa_shape *shape, const void *q, const void *k, c
     st = check_ws(workspace, workspace_bytes, kStatusBytes + bwd_bytes(p));
     if (st != MSA_OK) return st;
     Carve cv{static_cast<char *>(workspace)};
-    const size_t nbk = (size_t)p.B * p.Hkv * p.nb;
-    BwdWork w;
+    BwdWork w{};
     w.D = cv.take<float>((size_t)p.B * p.Hq * p.Nq);
-    w.dq_acc = cv.take<float>((size_t)p.B * p.Nq * p.Hq * p.d);
-    w.dqi_acc = cv.take<float>((size_t)p.B * p.Nq * p.Hkv * p.d_idx);
     w.dki_acc = cv.take<float>((size_t)p.B * p.Nk * p.d_idx);
     carve_index(cv, p, w);
+    const size_t slots = (size_t)p.B * p.Nq * p.topk;
+    if (bwd_tc(p)) {
+        w.dq_part = cv.take<bf16>(slots * p.Hq * p.d);
+        w.dqi_part = cv.take<bf16>(slots * p.Hkv * p.d_idx);
+        w.pt = cv.take<__half>(slots * p.Hkv * 128);
+    } else {
+        w.dq_acc = cv.take<float>((size_t)p.B * p.Nq * p.Hq * p.d);
+        w.dqi_acc = cv.take<float>((size_t)p.B * p.Nq * p.Hkv * p.d_idx);
+    }
     cudaError_t e = launch_fused_bwd(p, static_cast<const bf16 *>(q), static_cast<const bf16 *>(k),
                                      static_cast<const bf16 *>(v), static_cast<const bf16 *>(o),
                                      static_cast<const bf16 *>(d_o), lse, static_cast<const bf16 *>(q_idx),

@@ -1,0 +1,380 @@
+// bwd_index_tc.cu -- index-branch backward of MSA on the tcgen05 tensor cores
+// (d_idx = 128), key-major.
+//
+// "Sparse Attention · Part II", section 3.2: the index branch learns only
+// from the KL alignment loss, with the teacher detached.  Expanding the KL,
+// its gradient with respect to the index logit s_j of a selected key is
+//     dKL/ds_j = Ps_j - Pt_j,
+// Ps the index softmax over the selected set (normalised by lse_idx) and Pt
+// the teacher, which the main-branch backward kernel leaves per (bucket
+// entry, key).  One CTA owns one 128-key block of K_idx for one (b, group)
+// and walks the bucket's queries in chunks of 128, keys as the MMA's M:
+//   s^T = K_idx q_idx^T                              (M = 128 keys, N = 128 queries)
+//   dsig = coef (exp2(s*scale_idx*log2e - lse_idx*log2e) - Pt) on visible keys
+//   dq_idx^T = K_idx^T dsig^T                        (M = 128 features, N = 128 queries)
+//   dK_idx += dsig^T q_idx                           (M = 128 keys, N = 128 features)
+// dq_idx leaves as bf16 partial rows per (query, group, slot), summed by the
+// combine kernel; dK_idx (shared by all groups) is added to an fp32 buffer
+// once per CTA.  coef = kl_coef / (B * Nq * Hkv), the mean over (query,
+// group) rows of the per-row KL.
+//
+// Roles: warp 0 gathers q_idx rows (cp.async) and row data, warp 1 owns TMEM
+// and issues the MMAs, warps 2..9 are the epilogue (TMEM lanes 32*(w%4)..,
+// query columns half (w-2)/4).  s^T and dsig^T are double-buffered.
+#include <cuda_fp16.h>
+
+#include "msa_internal.h"
+#include "tc.cuh"
+
+namespace msa {
+namespace {
+
+constexpr int DI = 128;
+constexpr int kKeys = 128;
+constexpr int kQ = 128;                        // queries per chunk
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int SUB = 128 * 128;                 // [128 rows][64 bf16] swizzled sub-tile
+constexpr int OFF_KI = 0;                      // K_idx: 2 feature halves
+constexpr int OFF_STG = OFF_KI + 2 * SUB;      // 2 stages x q_idx [128 queries][128 features]
+constexpr int OFF_SIG = OFF_STG + 4 * SUB;     // 2 buffers x dsig^T [128 keys][128 queries]
+constexpr int OFF_META = OFF_SIG + 4 * SUB;
+
+struct Meta {
+    float lsei2[kQ];        // lse_idx * log2(e) (+inf for padding)
+    int pos[kQ];            // position (-1 for padding)
+    int qi[kQ];
+    int slot[kQ];
+    int e0;                 // bucket-list index of the chunk's first entry
+    int nq;
+};
+constexpr int META_BYTES = (int)((sizeof(Meta) + 127) & ~size_t(127));
+constexpr int OFF_BAR = OFF_META + 2 * META_BYTES;
+constexpr int ALLOC = OFF_BAR + 256 + 1024;
+
+constexpr uint32_t TM_S = 0, TM_DKI = 256, TM_DQI = 384;   // TM_S: 2 x 128
+
+__device__ __forceinline__ int swz(int row, int ch) { return row * 128 + ((ch ^ (row & 7)) << 4); }
+
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool wwait(uint64_t *bar, uint32_t parity, DeviceStatus *st, int site,
+                                      volatile int *abort_flag)
+{
+    const bool r = tc::mbar_wait(bar, parity, st, site, abort_flag);
+    return __all_sync(0xffffffffu, r);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, const bf16 *__restrict__ q_idx,
+                    const float *__restrict__ lse_idx, float coef, const int32_t *__restrict__ bucket_off,
+                    const int32_t *__restrict__ bucket_q, const __half *__restrict__ pt,
+                    bf16 *__restrict__ dqi_part, float *__restrict__ dki_acc, DeviceStatus *st)
+{
+    const int r = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
+    const long long bucket = ((long long)b * p.Hkv + r) * p.nb + c;
+    const int qbeg = bucket_off[bucket], qend = bucket_off[bucket + 1];
+    if (qend <= qbeg) return;                          // no query selected this block: nothing to add
+    const int nch = (qend - qbeg + kQ - 1) / kQ;
+    const long long j0 = (long long)c * kKeys;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
+    uint64_t *full = bars, *empty = bars + 2, *s_full = bars + 4, *s_free = bars + 6;
+    uint64_t *g_full = bars + 8, *g_free = bars + 10;
+    uint64_t *dq_full = bars + 12, *dq_free = bars + 13, *kv_full = bars + 14, *done = bars + 15;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int a = 0; a < 2; ++a) {
+            tc::mbar_init(&full[a], 64);               // 32 cp.async arrivals + 32 row-data arrivals
+            tc::mbar_init(&empty[a], 1 + kEpiWarps);
+            tc::mbar_init(&s_full[a], 1);
+            tc::mbar_init(&s_free[a], kEpiWarps);
+            tc::mbar_init(&g_full[a], kEpiWarps);
+            tc::mbar_init(&g_free[a], 1);
+        }
+        tc::mbar_init(dq_full, 1);
+        tc::mbar_init(dq_free, kEpiWarps);
+        tc::mbar_init(kv_full, 1);
+        tc::mbar_init(done, 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, 512);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ producer
+        if (lane == 0) {
+            tc::mbar_arrive_expect_tx(kv_full, 2 * SUB);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) tc::tma_load_3d(sm + OFF_KI + h * SUB, &tmap_ki, kv_full, h * 64, (int)j0, b);
+        }
+        int ent[4], ent_next[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) ent[t] = lane + 32 * t < qend - qbeg ? __ldg(bucket_q + qbeg + lane + 32 * t) : 0;
+        for (int m = 0; m < nch; ++m) {
+            const int s = m & 1;
+            const int q0 = qbeg + m * kQ;
+            const int nq = min(kQ, qend - q0);
+            float vl[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+                vl[t] = lane + 32 * t < nq
+                            ? __ldg(lse_idx + ((long long)b * p.Hkv + r) * p.Nq + entry_row(ent[t])) * kLog2e
+                            : INFINITY;
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+                ent_next[t] = lane + 32 * t < qend - q0 - kQ ? __ldg(bucket_q + q0 + kQ + lane + 32 * t) : 0;
+            if (!tc::mbar_wait(&empty[s], ((uint32_t)(m >> 1) & 1u) ^ 1u, st, 121, abort_flag)) break;
+            Meta *meta = reinterpret_cast<Meta *>(sm + OFF_META + s * META_BYTES);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int qq = lane + 32 * t;
+                const bool ok = qq < nq;
+                const int i = ok ? entry_row(ent[t]) : 0;
+                meta->lsei2[qq] = vl[t];
+                meta->qi[qq] = i;
+                meta->pos[qq] = ok ? p.q_offset + i : -1;
+                meta->slot[qq] = ok ? entry_slot(ent[t]) : 0;
+            }
+            if (lane == 0) {
+                meta->e0 = q0;
+                meta->nq = nq;
+            }
+            // q_idx rows: lane covers 16-byte chunk lane%16 of rows 2*it + lane/16;
+            // a row's entry is held by lane row%32 in ent[row/32]
+            uint8_t *sq = sm + OFF_STG + s * (2 * SUB);
+#pragma unroll
+            for (int it = 0; it < kQ / 2; ++it) {
+                const int row = it * 2 + (lane >> 4), ch = lane & 15;
+                const int e = __shfl_sync(0xffffffffu, ent[it >> 4], row & 31);
+                cp_async16_zfill(sq + (ch >> 3) * SUB + swz(row, ch & 7),
+                                 q_idx + (((long long)b * p.Nq + entry_row(e)) * p.Hkv + r) * DI + ch * 8, row < nq);
+            }
+            cp_async_arrive_noinc(&full[s]);
+            tc::mbar_arrive(&full[s]);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) ent[t] = ent_next[t];
+        }
+        cp_async_wait<0>();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            constexpr uint32_t I_S = tc::idesc_bf16(128, kQ);
+            constexpr uint32_t I_DKI = tc::idesc_bf16(128, DI) | tc::kBMajorMN;
+            constexpr uint32_t I_DQI = tc::idesc_bf16(128, kQ) | tc::kAMajorMN | tc::kBMajorMN;
+            const uint32_t aKI = smem_u32(sm + OFF_KI);
+            auto issue_s = [&](int n) {
+                const uint32_t sq = smem_u32(sm + OFF_STG + (n & 1) * (2 * SUB));
+#pragma unroll
+                for (int ks = 0; ks < DI / 16; ++ks) {
+                    const uint32_t off = (ks >> 2) * SUB + (ks & 3) * 32;
+                    tc::mma_bf16(tmem + TM_S + (n & 1) * kQ, tc::sdesc_k128(aKI + off), tc::sdesc_k128(sq + off), I_S,
+                                 ks > 0);
+                }
+                tc::mma_commit(&s_full[n & 1]);
+            };
+            auto issue_g = [&](int n) {
+                const int pb = n & 1;
+                const uint32_t sq = smem_u32(sm + OFF_STG + (n & 1) * (2 * SUB));
+                const uint32_t sg = smem_u32(sm + OFF_SIG + pb * (2 * SUB));
+                // dq_idx^T = K_idx^T dsig^T: both operands read MN-major; K = 128 keys
+#pragma unroll
+                for (int ks = 0; ks < kKeys / 16; ++ks)
+                    tc::mma_bf16(tmem + TM_DQI, tc::sdesc_sw128(aKI + ks * 2048, SUB, 1024),
+                                 tc::sdesc_sw128(sg + ks * 2048, SUB, 1024), I_DQI, ks > 0);
+                tc::mma_commit(dq_full);
+                // dK_idx += dsig^T q_idx: A K-major over queries, B = q_idx read MN-major; K = 128 queries
+#pragma unroll
+                for (int ks = 0; ks < kQ / 16; ++ks)
+                    tc::mma_bf16(tmem + TM_DKI, tc::sdesc_k128(sg + (ks >> 2) * SUB + (ks & 3) * 32),
+                                 tc::sdesc_sw128(sq + ks * 2048, SUB, 1024), I_DKI, n > 0 || ks > 0);
+                tc::mma_commit(&empty[n & 1]);
+                tc::mma_commit(&g_free[pb]);
+            };
+            bool ok = tc::mbar_wait(kv_full, 0, st, 122, abort_flag);
+            if (ok) {
+                ok = tc::mbar_wait(&full[0], 0, st, 123, abort_flag);
+                if (ok) {
+                    tc::fence_proxy_async();
+                    tc::fence_after_sync();
+                    issue_s(0);
+                }
+            }
+            for (int n = 0; ok && n < nch; ++n) {
+                if (n + 1 < nch) {
+                    const int m = n + 1;
+                    if (!tc::mbar_wait(&full[m & 1], (uint32_t)(m >> 1) & 1u, st, 124, abort_flag)) break;
+                    if (m >= 2 && !tc::mbar_wait(&s_free[m & 1], ((uint32_t)(m >> 1) & 1u) ^ 1u, st, 125, abort_flag))
+                        break;
+                    tc::fence_proxy_async();
+                    tc::fence_after_sync();
+                    issue_s(m);
+                }
+                if (!tc::mbar_wait(&g_full[n & 1], (uint32_t)(n >> 1) & 1u, st, 126, abort_flag)) break;
+                if (n >= 1 && !tc::mbar_wait(dq_free, (uint32_t)(n - 1) & 1u, st, 127, abort_flag)) break;
+                tc::fence_after_sync();
+                issue_g(n);
+            }
+            tc::mma_commit(done);
+            tc::mbar_wait(done, 0, nullptr, 0, nullptr);
+        }
+    } else {
+        // ------------------------------------------------ epilogue
+        const int qd = warp & 3, hf = (warp - 2) >> 2;
+        const int kr = qd * 32 + lane;              // key (s^T phase) or feature (dq_idx^T phase)
+        const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+        const long long j = j0 + kr;
+        const bool key_ok = j < p.Nk;
+        const float si2 = p.scale_idx * kLog2e;
+        const int cb = hf * 64;                     // first query column of this warp
+        long long rp_prev[2] = {-1, -1};            // partial rows of columns cb + lane, cb + 32 + lane
+        bool ok = true;
+        auto drain = [&](int m) -> bool {
+            if (!wwait(dq_full, (uint32_t)m & 1u, st, 131, abort_flag)) return false;
+            tc::fence_after_sync();
+            uint32_t v0[32], v1[32];
+            tc::tmem_ld32_nowait(tmem + lane_base + TM_DQI + cb, v0);
+            tc::tmem_ld32_nowait(tmem + lane_base + TM_DQI + cb + 32, v1);
+            tc::tmem_wait32(v0);
+            tc::tmem_wait32(v1);
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(dq_free);
+            bf16 *dst = dqi_part + kr;
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc) {
+                const long long a0 = __shfl_sync(0xffffffffu, rp_prev[0], cc);
+                const long long a1 = __shfl_sync(0xffffffffu, rp_prev[1], cc);
+                if (a0 >= 0) dst[a0 * DI] = __float2bfloat16_rn(p.scale_idx * __uint_as_float(v0[cc]));
+                if (a1 >= 0) dst[a1 * DI] = __float2bfloat16_rn(p.scale_idx * __uint_as_float(v1[cc]));
+            }
+            return true;
+        };
+        for (int n = 0; ok && n < nch; ++n) {
+            const int s = n & 1, pb = n & 1;
+            const Meta *meta = reinterpret_cast<const Meta *>(sm + OFF_META + s * META_BYTES);
+            if (!wwait(&full[s], (uint32_t)(n >> 1) & 1u, st, 132, abort_flag)) { ok = false; break; }
+            const int nq = meta->nq, e0 = meta->e0;
+            // teacher values of this key for the warp's 64 queries
+            float ptv[64];
+#pragma unroll
+            for (int cc = 0; cc < 64; ++cc) {
+                const int u = cb + cc;
+                ptv[cc] = u < nq ? __half2float(pt[(long long)(e0 + u) * kKeys + kr]) : 0.f;
+            }
+            if (!wwait(&s_full[s], (uint32_t)(n >> 1) & 1u, st, 133, abort_flag)) { ok = false; break; }
+            tc::fence_after_sync();
+            uint32_t s0[32], s1[32];
+            tc::tmem_ld32_nowait(tmem + lane_base + TM_S + s * kQ + cb, s0);
+            tc::tmem_ld32_nowait(tmem + lane_base + TM_S + s * kQ + cb + 32, s1);
+            long long rp_cur[2];
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const int u = cb + 32 * t + lane;
+                rp_cur[t] = u < nq ? (((long long)b * p.Nq + meta->qi[u]) * p.Hkv + r) * p.topk + meta->slot[u] : -1;
+            }
+            tc::tmem_wait32(s0);
+            tc::tmem_wait32(s1);
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&s_free[s]);
+            uint32_t sg[32];
+#pragma unroll
+            for (int cc = 0; cc < 64; cc += 4) {
+                const float4 l4 = *reinterpret_cast<const float4 *>(meta->lsei2 + cb + cc);
+                const int4 p4 = *reinterpret_cast<const int4 *>(meta->pos + cb + cc);
+                const float l2[4] = {l4.x, l4.y, l4.z, l4.w};
+                const int ps[4] = {p4.x, p4.y, p4.z, p4.w};
+                float g2[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int col = cc + e;
+                    const float sv = __uint_as_float(col < 32 ? s0[col] : s1[col - 32]);
+                    const bool vis = key_ok && j <= (long long)ps[e];
+                    g2[e] = vis ? coef * (tc::ex2(sv * si2 - l2[e]) - ptv[col]) : 0.f;
+                }
+                sg[cc / 2] = pack_bf16(g2[0], g2[1]);
+                sg[cc / 2 + 1] = pack_bf16(g2[2], g2[3]);
+            }
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&empty[s]);   // the stage's row data is no longer read
+            if (n >= 2 && !wwait(&g_free[pb], ((uint32_t)(n >> 1) & 1u) ^ 1u, st, 134, abort_flag)) { ok = false; break; }
+            uint8_t *dst = sm + OFF_SIG + pb * (2 * SUB) + hf * SUB;   // query half hf = sub-tile hf
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch)
+                *reinterpret_cast<uint4 *>(dst + swz(kr, ch)) =
+                    make_uint4(sg[ch * 4], sg[ch * 4 + 1], sg[ch * 4 + 2], sg[ch * 4 + 3]);
+            tc::fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&g_full[pb]);
+            if (n >= 1 && !drain(n - 1)) { ok = false; break; }
+            rp_prev[0] = rp_cur[0];
+            rp_prev[1] = rp_cur[1];
+        }
+        if (ok) ok = drain(nch - 1);
+        if (ok) {
+            const int m = nch - 1;
+            ok = wwait(&g_free[m & 1], (uint32_t)(m >> 1) & 1u, st, 135, abort_flag);
+            tc::fence_after_sync();
+        }
+        if (ok) {
+            // dK_idx of this key, features cb .. cb+63 (the column half doubles as the feature half)
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                uint32_t a[32];
+                tc::tmem_ld32_nowait(tmem + lane_base + TM_DKI + cb + h2 * 32, a);
+                tc::tmem_wait32(a);
+                if (key_ok) {
+                    float *dst = dki_acc + ((long long)b * p.Nk + j) * DI + cb + h2 * 32;
+#pragma unroll
+                    for (int x = 0; x < 32; x += 4)
+                        tc::red_add_v4(dst + x, p.scale_idx * __uint_as_float(a[x]), p.scale_idx * __uint_as_float(a[x + 1]),
+                                       p.scale_idx * __uint_as_float(a[x + 2]), p.scale_idx * __uint_as_float(a[x + 3]));
+                }
+            }
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_index_tc(const Problem &p, const bf16 *q_idx, const bf16 *k_idx, const float *lse_idx,
+                                float kl_coef, const BwdWork &w, DeviceStatus *st, cudaStream_t s)
+{
+    cudaError_t e = cudaFuncSetAttribute(bwd_index_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ALLOC);
+    if (e != cudaSuccess) return e;
+    CUtensorMap tki;
+    const unsigned long long di[3] = {(unsigned long long)DI, (unsigned long long)p.Nk, (unsigned long long)p.B};
+    const unsigned long long si[2] = {DI * 2ull, (unsigned long long)p.kv_rows * DI * 2ull};
+    const unsigned bi[3] = {64, (unsigned)kKeys, 1};
+    if ((e = make_tmap_bf16(&tki, k_idx, 3, di, si, bi)) != cudaSuccess) return e;
+    const float coef = kl_coef / ((float)p.B * (float)p.Nq * (float)p.Hkv);
+    bwd_index_tc_kernel<<<dim3(p.Hkv, p.nb, p.B), kThreads, ALLOC, s>>>(tki, p, q_idx, lse_idx, coef, w.bucket_off,
+                                                                       w.bucket_q, w.pt, w.dqi_part, w.dki_acc, st);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace msa

@@ -1,0 +1,520 @@
+// bwd_main_tc.cu -- main-branch backward of MSA on the tcgen05 tensor cores
+// (d = 128), key-major.
+//
+// "Sparse Attention · Part II", section 3.2: the main branch's gradients come
+// from dO alone (the selection is not differentiated).  One CTA owns one
+// 128-key block c of one (b, group r) and walks the queries that selected c
+// (the inverse index) in chunks of 64 (query, head) rows.  With the keys as
+// the MMA's M dimension, per chunk:
+//   S^T = K Q^T,  dP^T = V dO^T                   (M = 128 keys, N = 64 rows)
+//   P = exp2(S*scale*log2e - lse*log2e) on the keys each row may see,
+//   dS = P (dP - D),  D = rowsum(dO * O)
+//   dQ^T = K^T dS^T                                (M = 128 features, N = 64 rows)
+//   dV += P^T dO,  dK += dS^T Q                    (M = 128 keys, N = 128 features)
+// dV and dK stay in TMEM for the whole bucket and are written once (one
+// owner, no atomics).  A chunk's dQ leaves as one bf16 partial row per
+// (query, head, slot); a combine kernel sums a row's slots (the split-KV
+// pattern of the forward).  The KL teacher (the mean over the group's heads
+// of P) falls out of the same tile: the heads of one query are consecutive
+// columns of a thread's row, so it is a register sum, written as fp16 per
+// (bucket entry, key) for the index-branch backward.
+//
+// Roles: warp 0 loads (TMA), warp 1 owns TMEM and issues the MMAs, warps
+// 2..9 are the epilogue: warp w serves TMEM lanes 32*(w%4).. (keys, or
+// features for dQ^T) and column half (w-2)/4 of the chunk's 64 rows.  dQ^T
+// and the P/dS tiles are double-buffered, so the epilogue's work on chunk
+// n overlaps the MMAs of chunks n-1 and n+1.
+#include <cuda_fp16.h>
+
+#include "msa_internal.h"
+#include "tc.cuh"
+
+namespace msa {
+namespace {
+
+constexpr int D = 128;
+constexpr int kKeys = 128;
+constexpr int kRows = 64;                       // (query, head) rows per chunk
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int SUBK = kKeys * 128;               // [128 keys][64 bf16] swizzled sub-tile
+// A [64 rows][128 d] tile is stored as 8-row groups of {d 0..63, d 64..127}
+// (1024-byte swizzle atoms): row rho, half h at (rho/8)*2048 + h*1024 + (rho%8)*128.
+// With groups of 8 heads one query's rows form one group, which one TMA box fills.
+constexpr int TILE_R = kRows * D * 2;
+constexpr int OFF_K = 0;
+constexpr int OFF_V = OFF_K + 2 * SUBK;
+constexpr int OFF_STG = OFF_V + 2 * SUBK;       // 2 stages x {Q, dO}
+constexpr int STG_BYTES = 2 * TILE_R;
+constexpr int OFF_P = OFF_STG + 2 * STG_BYTES;  // 2 buffers of P^T  [128 keys][64 rows]
+constexpr int OFF_DS = OFF_P + 2 * SUBK;        // 2 buffers of dS^T [128 keys][64 rows]
+constexpr int OFF_META = OFF_DS + 2 * SUBK;
+
+struct Meta {                 // per stage
+    float lse2[kRows];        // lse * log2(e) of each row (+inf for padding)
+    float dd[kRows];          // rowsum(dO * O)
+    int pos[kRows];           // position of each query slot (-1 for padding)
+    int qi[kRows];            // query index
+    int slot[kRows];          // slot of this block in the query's selection
+    int e0;                   // bucket-list index of the chunk's first entry
+    int nq;                   // queries in the chunk
+};
+constexpr int META_BYTES = (int)((sizeof(Meta) + 127) & ~size_t(127));
+constexpr int OFF_BAR = OFF_META + 2 * META_BYTES;
+constexpr int ALLOC = OFF_BAR + 256 + 1024;
+
+constexpr uint32_t TM_DV = 0, TM_DK = 128, TM_S = 256, TM_DP = 320, TM_DQ = 384;   // TM_DQ: 2 x 64
+
+__device__ __forceinline__ int swz(int row, int ch) { return row * 128 + ((ch ^ (row & 7)) << 4); }
+__device__ __forceinline__ int roff(int rho, int half, int ch)
+{
+    return (rho >> 3) * 2048 + half * 1024 + (rho & 7) * 128 + (((ch ^ rho) & 7) << 4);
+}
+
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Bounded wait whose outcome is the same on every lane of the warp, so the
+// warp-collective TMEM loads that follow are never split.
+__device__ __forceinline__ bool wwait(uint64_t *bar, uint32_t parity, DeviceStatus *st, int site,
+                                      volatile int *abort_flag)
+{
+    const bool r = tc::mbar_wait(bar, parity, st, site, abort_flag);
+    return __all_sync(0xffffffffu, r);
+}
+
+template <int EPL>
+__device__ __forceinline__ void load_entries(int (&e)[EPL], const int32_t *__restrict__ bucket_q, int q0, int nq,
+                                             int lane)
+{
+#pragma unroll
+    for (int t = 0; t < EPL; ++t) {
+        const int qq = lane + 32 * t;
+        e[t] = qq < nq ? __ldg(bucket_q + q0 + qq) : 0;
+    }
+}
+
+template <int G>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_do,
+                   const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v, Problem p,
+                   const bf16 *__restrict__ q, const bf16 *__restrict__ d_o, const float *__restrict__ lse,
+                   const float *__restrict__ Dg, const int32_t *__restrict__ bucket_off,
+                   const int32_t *__restrict__ bucket_q, bf16 *__restrict__ dk, bf16 *__restrict__ dv,
+                   bf16 *__restrict__ dq_part, __half *__restrict__ pt_out, DeviceStatus *st)
+{
+    constexpr int QC = kRows / G;                 // queries per chunk
+    constexpr int EPL = (QC + 31) / 32;           // bucket entries per producer lane
+    // x = group, y = key block: the heavy early blocks of every group start first
+    const int r = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
+    const long long bucket = ((long long)b * p.Hkv + r) * p.nb + c;
+    const int qbeg = bucket_off[bucket], qend = bucket_off[bucket + 1];
+    const int nch = (qend - qbeg + QC - 1) / QC;
+    const long long j0 = (long long)c * kKeys;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
+    uint64_t *full = bars, *empty = bars + 2, *p_full = bars + 4, *p_free = bars + 6;
+    uint64_t *dq_full = bars + 8, *dq_free = bars + 10;
+    uint64_t *kv_full = bars + 12, *s_full = bars + 13, *tm_free = bars + 14, *done = bars + 15;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int a = 0; a < 2; ++a) {
+            // G == 8: lane 0's expect_tx arrival + 32 row-data arrivals;
+            // otherwise 32 cp.async arrivals + 32 row-data arrivals
+            tc::mbar_init(&full[a], G == 8 ? 33 : 64);
+            tc::mbar_init(&empty[a], 1 + kEpiWarps);   // grads MMAs done + epilogue has read the row data
+            tc::mbar_init(&p_full[a], kEpiWarps);
+            tc::mbar_init(&p_free[a], 1);
+            tc::mbar_init(&dq_full[a], 1);
+            tc::mbar_init(&dq_free[a], kEpiWarps);
+        }
+        tc::mbar_init(kv_full, 1);
+        tc::mbar_init(s_full, 1);
+        tc::mbar_init(tm_free, kEpiWarps);
+        tc::mbar_init(done, 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, 512);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ producer
+        // K and V tiles by TMA; rows past Nk read as zeros
+        if (lane == 0) {
+            tc::prefetch_tmap(&tmap_q);
+            tc::prefetch_tmap(&tmap_do);
+            tc::mbar_arrive_expect_tx(kv_full, 4 * SUBK);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                tc::tma_load_4d(sm + OFF_K + h * SUBK, &tmap_k, kv_full, h * 64, r, (int)j0, b);
+                tc::tma_load_4d(sm + OFF_V + h * SUBK, &tmap_v, kv_full, h * 64, r, (int)j0, b);
+            }
+        }
+        int ent[EPL], ent_next[EPL];
+        load_entries(ent, bucket_q, qbeg, min(QC, qend - qbeg), lane);
+        for (int m = 0; m < nch; ++m) {
+            const int s = m & 1;
+            const int q0 = qbeg + m * QC;
+            const int nq = min(QC, qend - q0);
+            // this chunk's per-row values and the next chunk's entries are
+            // fetched before waiting for a free stage
+            float vl[2], vd[2];
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const int rho = lane + 32 * t, qq = rho / G, g = rho % G;
+                int e = 0;
+#pragma unroll
+                for (int u = 0; u < EPL; ++u) {
+                    const int x = __shfl_sync(0xffffffffu, ent[u], qq & 31);
+                    if ((qq >> 5) == u) e = x;
+                }
+                const bool ok = qq < nq;
+                const long long hi = ((long long)b * p.Hq + r * G + g) * p.Nq + entry_row(e);
+                vl[t] = ok ? __ldg(lse + hi) * kLog2e : INFINITY;
+                vd[t] = ok ? __ldg(Dg + hi) : 0.f;
+            }
+            if (m + 1 < nch) load_entries(ent_next, bucket_q, q0 + QC, min(QC, qend - q0 - QC), lane);
+            if (!tc::mbar_wait(&empty[s], ((uint32_t)(m >> 1) & 1u) ^ 1u, st, 101, abort_flag)) break;
+            Meta *meta = reinterpret_cast<Meta *>(sm + OFF_META + s * META_BYTES);
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                meta->lse2[lane + 32 * t] = vl[t];
+                meta->dd[lane + 32 * t] = vd[t];
+            }
+#pragma unroll
+            for (int t = 0; t < EPL; ++t) {
+                const int qq = lane + 32 * t;
+                if (qq < QC) {
+                    const bool ok = qq < nq;
+                    const int i = ok ? entry_row(ent[t]) : 0;
+                    meta->qi[qq] = i;
+                    meta->pos[qq] = ok ? p.q_offset + i : -1;
+                    meta->slot[qq] = ok ? entry_slot(ent[t]) : 0;
+                }
+            }
+            if (lane == 0) {
+                meta->e0 = q0;
+                meta->nq = nq;
+            }
+            __syncwarp();
+            uint8_t *sq = sm + OFF_STG + s * STG_BYTES, *sdo = sq + TILE_R;
+            if constexpr (G == 8) {
+                // one TMA box {64 features, 8 heads, 2 halves} per query and
+                // tensor fills one 2048-byte row group; padding slots read
+                // rows past the end (zero fill)
+                if (lane == 0) tc::mbar_arrive_expect_tx(&full[s], 2 * TILE_R);
+                __syncwarp();
+                if (lane < QC) {
+                    const int z = lane < nq ? b * p.Nq + entry_row(ent[0]) : p.B * p.Nq;
+                    tc::tma_load_4d(sq + lane * 2048, &tmap_q, &full[s], 0, r * G, 0, z);
+                    tc::tma_load_4d(sdo + lane * 2048, &tmap_do, &full[s], 0, r * G, 0, z);
+                }
+            } else {
+                // 64 rows x 16 chunks per tensor: lane covers chunk lane%16 of rows 2*it + lane/16
+#pragma unroll 4
+                for (int it = 0; it < kRows / 2; ++it) {
+                    const int rho = it * 2 + (lane >> 4), ch = lane & 15;
+                    const int qq = rho / G, g = rho % G;
+                    const bool ok = qq < nq;
+                    const long long off =
+                        (((long long)b * p.Nq + meta->qi[qq]) * p.Hq + (long long)r * G + g) * D + ch * 8;
+                    const int o = roff(rho, ch >> 3, ch & 7);
+                    cp_async16_zfill(sq + o, q + off, ok);
+                    cp_async16_zfill(sdo + o, d_o + off, ok);
+                }
+                cp_async_arrive_noinc(&full[s]);
+            }
+            tc::mbar_arrive(&full[s]);
+#pragma unroll
+            for (int t = 0; t < EPL; ++t) ent[t] = ent_next[t];
+        }
+        cp_async_wait<0>();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            constexpr uint32_t I_S = tc::idesc_bf16(128, kRows);
+            constexpr uint32_t I_DKV = tc::idesc_bf16(128, 128) | tc::kBMajorMN;
+            constexpr uint32_t I_DQ = tc::idesc_bf16(128, kRows) | tc::kAMajorMN | tc::kBMajorMN;
+            const uint32_t aK = smem_u32(sm + OFF_K), aV = smem_u32(sm + OFF_V);
+            auto issue_scores = [&](int n) {
+                const uint32_t sq = smem_u32(sm + OFF_STG + (n & 1) * STG_BYTES), sdo = sq + TILE_R;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t h = ks >> 2, ko = (ks & 3) * 32;
+                    // B = Q / dO rows (K-major, 8-row groups 2048 bytes apart)
+                    tc::mma_bf16(tmem + TM_S, tc::sdesc_k128(aK + h * SUBK + ko),
+                                 tc::sdesc_sw128(sq + h * 1024 + ko, 16, 2048), I_S, ks > 0);
+                    tc::mma_bf16(tmem + TM_DP, tc::sdesc_k128(aV + h * SUBK + ko),
+                                 tc::sdesc_sw128(sdo + h * 1024 + ko, 16, 2048), I_S, ks > 0);
+                }
+                tc::mma_commit(s_full);
+            };
+            auto issue_grads = [&](int n) {
+                const int pb = n & 1;
+                const uint32_t sq = smem_u32(sm + OFF_STG + (n & 1) * STG_BYTES), sdo = sq + TILE_R;
+                const uint32_t aP = smem_u32(sm + OFF_P + pb * SUBK), aDS = smem_u32(sm + OFF_DS + pb * SUBK);
+                // dQ^T = K^T dS^T: A = K read MN-major (64-feature atoms SUBK apart),
+                // B = dS^T [keys][rows] read MN-major; K = 128 keys
+#pragma unroll
+                for (int ks = 0; ks < kKeys / 16; ++ks)
+                    tc::mma_bf16(tmem + TM_DQ + pb * kRows, tc::sdesc_sw128(aK + ks * 2048, SUBK, 1024),
+                                 tc::sdesc_sw128(aDS + ks * 2048, SUBK, 1024), I_DQ, ks > 0);
+                tc::mma_commit(&dq_full[pb]);
+                // dV += P^T dO, dK += dS^T Q: B = dO / Q read MN-major (feature
+                // halves 1024 bytes apart, 8-row groups 2048 apart); K = 64 rows
+#pragma unroll
+                for (int ks = 0; ks < kRows / 16; ++ks) {
+                    const bool acc = n > 0 || ks > 0;
+                    tc::mma_bf16(tmem + TM_DV, tc::sdesc_k128(aP + ks * 32), tc::sdesc_sw128(sdo + ks * 4096, 1024, 2048),
+                                 I_DKV, acc);
+                    tc::mma_bf16(tmem + TM_DK, tc::sdesc_k128(aDS + ks * 32), tc::sdesc_sw128(sq + ks * 4096, 1024, 2048),
+                                 I_DKV, acc);
+                }
+                tc::mma_commit(&empty[n & 1]);
+                tc::mma_commit(&p_free[pb]);
+            };
+            bool ok = tc::mbar_wait(kv_full, 0, st, 102, abort_flag);
+            if (ok && nch > 0) {
+                ok = tc::mbar_wait(&full[0], 0, st, 103, abort_flag);
+                if (ok) {
+                    tc::fence_proxy_async();
+                    tc::fence_after_sync();
+                    issue_scores(0);
+                }
+            }
+            for (int n = 0; ok && n < nch; ++n) {
+                if (n + 1 < nch) {
+                    if (!tc::mbar_wait(&full[(n + 1) & 1], (uint32_t)((n + 1) >> 1) & 1u, st, 104, abort_flag)) break;
+                    if (!tc::mbar_wait(tm_free, (uint32_t)n & 1u, st, 105, abort_flag)) break;
+                    tc::fence_proxy_async();
+                    tc::fence_after_sync();
+                    issue_scores(n + 1);
+                }
+                if (!tc::mbar_wait(&p_full[n & 1], (uint32_t)(n >> 1) & 1u, st, 106, abort_flag)) break;
+                if (n >= 2 && !tc::mbar_wait(&dq_free[n & 1], ((uint32_t)(n >> 1) & 1u) ^ 1u, st, 107, abort_flag))
+                    break;
+                tc::fence_after_sync();
+                issue_grads(n);
+            }
+            // every MMA issued above has completed once `done` fires
+            tc::mma_commit(done);
+            tc::mbar_wait(done, 0, nullptr, 0, nullptr);
+        }
+    } else {
+        // ------------------------------------------------ epilogue
+        const int qd = warp & 3, hf = (warp - 2) >> 2;
+        const int kr = qd * 32 + lane;             // key (S/dP/P/dS phase) or feature (dQ phase)
+        const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+        const long long j = j0 + kr;
+        const bool key_ok = j < p.Nk;
+        const float sl2 = p.scale * kLog2e;
+        const float invG = 1.f / (float)G;
+        constexpr int NQH = 32 / G;                // query slots among this warp's 32 columns
+        const int cb = hf * 32;                    // first column (row of the chunk) of this warp
+        long long ridx_prev = -1;                  // partial row of column cb + lane of the chunk being drained
+        bool ok = true;
+        // writes the dQ partial rows of chunk m (row indices held in ridx_prev)
+        auto drain_dq = [&](int m) -> bool {
+            const int pb = m & 1;
+            if (!wwait(&dq_full[pb], (uint32_t)(m >> 1) & 1u, st, 111, abort_flag)) return false;
+            tc::fence_after_sync();
+            uint32_t v[32];
+            tc::tmem_ld32_nowait(tmem + lane_base + TM_DQ + pb * kRows + cb, v);
+            tc::tmem_wait32(v);
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&dq_free[pb]);
+            bf16 *dst = dq_part + kr;              // this thread's feature
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc) {
+                const long long rix = __shfl_sync(0xffffffffu, ridx_prev, cc);
+                if (rix >= 0) dst[rix * D] = __float2bfloat16_rn(p.scale * __uint_as_float(v[cc]));
+            }
+            return true;
+        };
+        for (int n = 0; ok && n < nch; ++n) {
+            const int s = n & 1, pb = n & 1;
+            const Meta *meta = reinterpret_cast<const Meta *>(sm + OFF_META + s * META_BYTES);
+            if (!wwait(&full[s], (uint32_t)(n >> 1) & 1u, st, 112, abort_flag)) { ok = false; break; }
+            if (!wwait(s_full, (uint32_t)n & 1u, st, 113, abort_flag)) { ok = false; break; }
+            tc::fence_after_sync();
+            uint32_t sv[32], dp[32];
+            tc::tmem_ld32_nowait(tmem + lane_base + TM_S + cb, sv);
+            tc::tmem_ld32_nowait(tmem + lane_base + TM_DP + cb, dp);
+            // row data while the loads land
+            float l2[32], dd[32];
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+                const float4 a = reinterpret_cast<const float4 *>(meta->lse2 + cb)[x];
+                const float4 e = reinterpret_cast<const float4 *>(meta->dd + cb)[x];
+                l2[4 * x] = a.x; l2[4 * x + 1] = a.y; l2[4 * x + 2] = a.z; l2[4 * x + 3] = a.w;
+                dd[4 * x] = e.x; dd[4 * x + 1] = e.y; dd[4 * x + 2] = e.z; dd[4 * x + 3] = e.w;
+            }
+            int pos[NQH];
+#pragma unroll
+            for (int u = 0; u < NQH; ++u) pos[u] = meta->pos[cb / G + u];
+            const int nq = meta->nq, e0 = meta->e0;
+            long long ridx_cur;
+            {
+                const int rho = cb + lane, qq = rho / G, g = rho % G;
+                ridx_cur = qq < nq ? ((((long long)b * p.Nq + meta->qi[qq]) * p.Hq + (long long)r * G + g) * p.topk +
+                                      meta->slot[qq])
+                                   : -1;
+            }
+            tc::tmem_wait32(sv);
+            tc::tmem_wait32(dp);
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                tc::mbar_arrive(tm_free);
+                tc::mbar_arrive(&empty[s]);       // the row data now lives in registers
+            }
+            // P^T, dS^T of this key against the warp's 32 rows; teacher sums
+            uint32_t pk[16], dk2[16];
+            float ptq[NQH];
+#pragma unroll
+            for (int u = 0; u < NQH; ++u) ptq[u] = 0.f;
+#pragma unroll
+            for (int cc = 0; cc < 32; cc += 2) {
+                float pr[2], ds[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int col = cc + e, u = col / G;
+                    const bool vis = key_ok && j <= (long long)pos[u];
+                    pr[e] = vis ? tc::ex2(__uint_as_float(sv[col]) * sl2 - l2[col]) : 0.f;
+                    ds[e] = pr[e] * (__uint_as_float(dp[col]) - dd[col]);
+                    ptq[u] += pr[e];
+                }
+                pk[cc / 2] = pack_bf16(pr[0], pr[1]);
+                dk2[cc / 2] = pack_bf16(ds[0], ds[1]);
+            }
+#pragma unroll
+            for (int u = 0; u < NQH; ++u) {
+                const int qq = cb / G + u;
+                if (qq < nq) pt_out[(long long)(e0 + qq) * kKeys + kr] = __float2half_rn(ptq[u] * invG);
+            }
+            if (n >= 2 && !wwait(&p_free[pb], ((uint32_t)(n >> 1) & 1u) ^ 1u, st, 114, abort_flag)) { ok = false; break; }
+            uint8_t *sp = sm + OFF_P + pb * SUBK, *sd = sm + OFF_DS + pb * SUBK;
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+                const int ch = hf * 4 + c4;
+                *reinterpret_cast<uint4 *>(sp + swz(kr, ch)) =
+                    make_uint4(pk[c4 * 4], pk[c4 * 4 + 1], pk[c4 * 4 + 2], pk[c4 * 4 + 3]);
+                *reinterpret_cast<uint4 *>(sd + swz(kr, ch)) =
+                    make_uint4(dk2[c4 * 4], dk2[c4 * 4 + 1], dk2[c4 * 4 + 2], dk2[c4 * 4 + 3]);
+            }
+            tc::fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&p_full[pb]);
+            if (n >= 1 && !drain_dq(n - 1)) { ok = false; break; }
+            ridx_prev = ridx_cur;
+        }
+        if (ok && nch > 0) ok = drain_dq(nch - 1);
+        // ---- dK, dV of this key (this warp: features hf*64 .. hf*64+63)
+        if (ok && nch > 0) {
+            // the last chunk's buffer release follows every MMA of the bucket
+            const int m = nch - 1;
+            ok = wwait(&p_free[m & 1], (uint32_t)(m >> 1) & 1u, st, 115, abort_flag);
+            tc::fence_after_sync();
+        }
+        if (ok) {
+            bf16 *pk_ = dk + (((long long)b * p.kv_rows + j) * p.Hkv + r) * D + hf * 64;
+            bf16 *pv_ = dv + (((long long)b * p.kv_rows + j) * p.Hkv + r) * D + hf * 64;
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                uint32_t a[32], g2[32];
+                if (nch > 0) {
+                    tc::tmem_ld32_nowait(tmem + lane_base + TM_DV + hf * 64 + h2 * 32, a);
+                    tc::tmem_ld32_nowait(tmem + lane_base + TM_DK + hf * 64 + h2 * 32, g2);
+                    tc::tmem_wait32(a);
+                    tc::tmem_wait32(g2);
+                } else {
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) a[x] = g2[x] = 0u;
+                }
+                if (key_ok) {
+#pragma unroll
+                    for (int x = 0; x < 32; x += 8) {
+                        *reinterpret_cast<uint4 *>(pv_ + h2 * 32 + x) = make_uint4(
+                            pack_bf16(__uint_as_float(a[x]), __uint_as_float(a[x + 1])),
+                            pack_bf16(__uint_as_float(a[x + 2]), __uint_as_float(a[x + 3])),
+                            pack_bf16(__uint_as_float(a[x + 4]), __uint_as_float(a[x + 5])),
+                            pack_bf16(__uint_as_float(a[x + 6]), __uint_as_float(a[x + 7])));
+                        *reinterpret_cast<uint4 *>(pk_ + h2 * 32 + x) = make_uint4(
+                            pack_bf16(p.scale * __uint_as_float(g2[x]), p.scale * __uint_as_float(g2[x + 1])),
+                            pack_bf16(p.scale * __uint_as_float(g2[x + 2]), p.scale * __uint_as_float(g2[x + 3])),
+                            pack_bf16(p.scale * __uint_as_float(g2[x + 4]), p.scale * __uint_as_float(g2[x + 5])),
+                            pack_bf16(p.scale * __uint_as_float(g2[x + 6]), p.scale * __uint_as_float(g2[x + 7])));
+                    }
+                }
+            }
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int G>
+cudaError_t launch_g(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *v, const bf16 *d_o, const float *lse,
+                     const BwdWork &w, bf16 *dk, bf16 *dv, DeviceStatus *st, cudaStream_t s)
+{
+    cudaError_t e = cudaFuncSetAttribute(bwd_main_tc_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, ALLOC);
+    if (e != cudaSuccess) return e;
+    CUtensorMap tq, tdo, tk, tv;
+    {
+        // Q / dO as {d within a half, head, half, query row}: one box {64, G, 2, 1}
+        // is a query's G head rows in both feature halves
+        const unsigned long long dq4[4] = {64, (unsigned long long)p.Hq, 2, (unsigned long long)p.B * p.Nq};
+        const unsigned long long sq4[3] = {D * 2ull, 128ull, (unsigned long long)p.Hq * D * 2ull};
+        const unsigned bq4[4] = {64, (unsigned)G, 2, 1};
+        if ((e = make_tmap_bf16(&tq, q, 4, dq4, sq4, bq4)) != cudaSuccess) return e;
+        if ((e = make_tmap_bf16(&tdo, d_o, 4, dq4, sq4, bq4)) != cudaSuccess) return e;
+        // K/V as [B][Nk][Hkv][D] (rows past Nk are out of bounds)
+        const unsigned long long dk4[4] = {(unsigned long long)D, (unsigned long long)p.Hkv, (unsigned long long)p.Nk,
+                                           (unsigned long long)p.B};
+        const unsigned long long sk[3] = {D * 2ull, (unsigned long long)p.Hkv * D * 2ull,
+                                          (unsigned long long)p.kv_rows * p.Hkv * D * 2ull};
+        const unsigned bk[4] = {64, 1, (unsigned)kKeys, 1};
+        if ((e = make_tmap_bf16(&tk, k, 4, dk4, sk, bk)) != cudaSuccess) return e;
+        if ((e = make_tmap_bf16(&tv, v, 4, dk4, sk, bk)) != cudaSuccess) return e;
+    }
+    bwd_main_tc_kernel<G><<<dim3(p.Hkv, p.nb, p.B), kThreads, ALLOC, s>>>(
+        tq, tdo, tk, tv, p, q, d_o, lse, w.D, w.bucket_off, w.bucket_q, dk, dv, w.dq_part, w.pt, st);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_main_tc(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *v, const bf16 *d_o,
+                               const float *lse, const BwdWork &w, bf16 *dk, bf16 *dv, DeviceStatus *st,
+                               cudaStream_t s)
+{
+    switch (p.G) {
+    case 1: return launch_g<1>(p, q, k, v, d_o, lse, w, dk, dv, st, s);
+    case 2: return launch_g<2>(p, q, k, v, d_o, lse, w, dk, dv, st, s);
+    case 4: return launch_g<4>(p, q, k, v, d_o, lse, w, dk, dv, st, s);
+    default: return launch_g<8>(p, q, k, v, d_o, lse, w, dk, dv, st, s);
+    }
+}
+
+}  // namespace msa

@@ -86,6 +86,53 @@ __global__ void f32_to_bf16_kernel(const float *__restrict__ src, bf16 *__restri
     }
 }
 
+// Sums the per-slot partial rows of one output row (one warp per row):
+// out[row] = sum over the valid slots s of part[row * topk + s].  Rows are
+// (b, i, h) over H heads; head h belongs to group h / Gh, whose selection
+// decides which slots hold a partial (same validity rule as the inverse
+// index).  DD = row length (128 or 64).
+template <int DD>
+__global__ void __launch_bounds__(256)
+bwd_combine_kernel(Problem p, const int32_t *__restrict__ sel, const bf16 *__restrict__ part, bf16 *__restrict__ out,
+                   int H, int Gh)
+{
+    const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= (long long)p.B * p.Nq * H) return;
+    const int h = (int)(row % H);
+    const long long bi = row / H;
+    const int i = (int)(bi % p.Nq), b = (int)(bi / p.Nq);
+    const long long pos = (long long)p.q_offset + i;
+    const int32_t *srow = sel + (((long long)b * p.Hkv + h / Gh) * p.Nq + i) * p.topk;
+    const int cl = lane < p.topk ? srow[lane] : -1;
+    const bool sv = cl >= 0 && cl < p.nb && (long long)cl * 128 <= pos;
+    constexpr int PER = DD / 32;
+    float acc[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+    for (unsigned m = __ballot_sync(0xffffffffu, sv); m; m &= m - 1) {
+        const int s = __ffs(m) - 1;
+        const bf16 *src = part + (row * p.topk + s) * DD + lane * PER;
+        if constexpr (PER == 4) {
+            const uint2 u = *reinterpret_cast<const uint2 *>(src);
+            const float2 a0 = unpack_bf16(u.x), a1 = unpack_bf16(u.y);
+            acc[0] += a0.x;
+            acc[1] += a0.y;
+            acc[2] += a1.x;
+            acc[3] += a1.y;
+        } else {
+            const float2 a0 = unpack_bf16(*reinterpret_cast<const uint32_t *>(src));
+            acc[0] += a0.x;
+            acc[1] += a0.y;
+        }
+    }
+    bf16 *dst = out + row * DD + lane * PER;
+    if constexpr (PER == 4)
+        *reinterpret_cast<uint2 *>(dst) = make_uint2(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]));
+    else
+        *reinterpret_cast<uint32_t *>(dst) = pack_bf16(acc[0], acc[1]);
+}
+
 // ------------------------------------------------------------------ main
 template <int D, int DI>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -484,12 +531,14 @@ cudaError_t launch_fused_bwd(const Problem &p, const bf16 *q, const bf16 *k, con
                              bf16 *dq_idx, bf16 *dk_idx, const BwdWork &w, DeviceStatus *st, cudaStream_t s)
 {
     cudaError_t e;
-    const long long nbk = (long long)p.B * p.Hkv * p.nb;
     const long long n_dq = (long long)p.B * p.Nq * p.Hq * p.d;
     const long long n_dqi = (long long)p.B * p.Nq * p.Hkv * p.d_idx;
     const long long n_dki = (long long)p.B * p.Nk * p.d_idx;
-    if ((e = cudaMemsetAsync(w.dq_acc, 0, n_dq * 4, s)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(w.dqi_acc, 0, n_dqi * 4, s)) != cudaSuccess) return e;
+    const bool tc = bwd_tc(p);
+    if (!tc) {
+        if ((e = cudaMemsetAsync(w.dq_acc, 0, n_dq * 4, s)) != cudaSuccess) return e;
+        if ((e = cudaMemsetAsync(w.dqi_acc, 0, n_dqi * 4, s)) != cudaSuccess) return e;
+    }
     if ((e = cudaMemsetAsync(w.dki_acc, 0, n_dki * 4, s)) != cudaSuccess) return e;
 
     const long long rows = (long long)p.B * p.Nq * p.Hq;
@@ -498,16 +547,25 @@ cudaError_t launch_fused_bwd(const Problem &p, const bf16 *q, const bf16 *k, con
     if ((e = launch_inverse_index(p, sel, w.bucket_cnt, w.bucket_off, w.bucket_scratch, w.bucket_q, st, s)) != cudaSuccess)
         return e;
 
-    if (p.d == 128 && p.d_idx == 128) e = launch_fused_bwd_tc_main(p, q, k, v, d_o, lse, q_idx, k_idx, lse_idx, kl_coef, w, dk, dv, st, s);
-    else if (p.d == 128) e = launch_main<128, 64>(p, q, k, v, d_o, lse, q_idx, k_idx, lse_idx, kl_coef, w, dk, dv, s);
-    else if (p.d_idx == 128) e = launch_main<64, 128>(p, q, k, v, d_o, lse, q_idx, k_idx, lse_idx, kl_coef, w, dk, dv, s);
-    else e = launch_main<64, 64>(p, q, k, v, d_o, lse, q_idx, k_idx, lse_idx, kl_coef, w, dk, dv, s);
-    if (e != cudaSuccess) return e;
-
-    f32_to_bf16_kernel<<<4 * p.num_sms, 256, 0, s>>>(w.dq_acc, dq, n_dq);
-    note_launch();
-    f32_to_bf16_kernel<<<4 * p.num_sms, 256, 0, s>>>(w.dqi_acc, dq_idx, n_dqi);
-    note_launch();
+    if (tc) {
+        // main branch first: it leaves the teacher per (bucket entry, key) for the index branch
+        if ((e = launch_bwd_main_tc(p, q, k, v, d_o, lse, w, dk, dv, st, s)) != cudaSuccess) return e;
+        if ((e = launch_bwd_index_tc(p, q_idx, k_idx, lse_idx, kl_coef, w, st, s)) != cudaSuccess) return e;
+        bwd_combine_kernel<128><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p, sel, w.dq_part, dq, p.Hq, p.G);
+        note_launch();
+        const long long rows_i = (long long)p.B * p.Nq * p.Hkv;
+        bwd_combine_kernel<128><<<(unsigned)((rows_i + 7) / 8), 256, 0, s>>>(p, sel, w.dqi_part, dq_idx, p.Hkv, 1);
+        note_launch();
+    } else {
+        if (p.d == 128) e = launch_main<128, 64>(p, q, k, v, d_o, lse, q_idx, k_idx, lse_idx, kl_coef, w, dk, dv, s);
+        else if (p.d_idx == 128) e = launch_main<64, 128>(p, q, k, v, d_o, lse, q_idx, k_idx, lse_idx, kl_coef, w, dk, dv, s);
+        else e = launch_main<64, 64>(p, q, k, v, d_o, lse, q_idx, k_idx, lse_idx, kl_coef, w, dk, dv, s);
+        if (e != cudaSuccess) return e;
+        f32_to_bf16_kernel<<<4 * p.num_sms, 256, 0, s>>>(w.dq_acc, dq, n_dq);
+        note_launch();
+        f32_to_bf16_kernel<<<4 * p.num_sms, 256, 0, s>>>(w.dqi_acc, dq_idx, n_dqi);
+        note_launch();
+    }
     f32_to_bf16_kernel<<<4 * p.num_sms, 256, 0, s>>>(w.dki_acc, dk_idx, n_dki);
     note_launch();
     return cudaGetLastError();

@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -69,9 +70,12 @@ cudaError_t launch_kl_reduce(const Problem &p, const float *kl_rows, float kl_co
 // Backward pieces.  Workspace carve-up is done by the caller (api.cu).
 struct BwdWork {
     float *D;            // [B, Hq, Nq]    rowsum(dO * O)
-    float *dq_acc;       // [B, Nq, Hq, d]  fp32 accumulators
-    float *dqi_acc;      // [B, Nq, Hkv, d_idx]
+    float *dq_acc;       // [B, Nq, Hq, d]  fp32 accumulators (mma.sync path)
+    float *dqi_acc;      // [B, Nq, Hkv, d_idx]              (mma.sync path)
     float *dki_acc;      // [B, Nk, d_idx]
+    bf16 *dq_part;       // [B, Nq, Hq, topk, d]      dQ per selected block (tcgen05 path)
+    bf16 *dqi_part;      // [B, Nq, Hkv, topk, d_idx] dq_idx per selected block (tcgen05 path)
+    __half *pt;          // [B*Hkv*Nq*topk entries, 128] teacher per (bucket entry, key) (tcgen05 path)
     int32_t *bucket_cnt; // [B*Hkv*nb]
     int32_t *bucket_off; // [B*Hkv*nb + 1]
     int32_t *bucket_scratch; // inverse_index_scratch_ints(p)
@@ -94,10 +98,14 @@ __host__ __device__ __forceinline__ int entry_slot(int32_t e) { return (int)((ui
 cudaError_t launch_inverse_index(const Problem &p, const int32_t *sel, int32_t *cnt, int32_t *off, int32_t *scratch,
                                  int32_t *list, DeviceStatus *st, cudaStream_t s);
 
-// tcgen05 main backward kernel (d = d_idx = 128); the prep kernels run first.
-cudaError_t launch_fused_bwd_tc_main(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *v, const bf16 *d_o,
-                                     const float *lse, const bf16 *q_idx, const bf16 *k_idx, const float *lse_idx,
-                                     float kl_coef, const BwdWork &w, bf16 *dk, bf16 *dv, DeviceStatus *st,
-                                     cudaStream_t s);
+// The backward runs on the tcgen05 kernels when d = d_idx = 128.
+inline bool bwd_tc(const Problem &p) { return p.d == 128 && p.d_idx == 128; }
+// tcgen05 main-branch backward (d = 128): dK, dV, dQ partials, teacher per entry.
+cudaError_t launch_bwd_main_tc(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *v, const bf16 *d_o,
+                               const float *lse, const BwdWork &w, bf16 *dk, bf16 *dv, DeviceStatus *st,
+                               cudaStream_t s);
+// tcgen05 index-branch backward (d_idx = 128): dq_idx partials, dK_idx into w.dki_acc.
+cudaError_t launch_bwd_index_tc(const Problem &p, const bf16 *q_idx, const bf16 *k_idx, const float *lse_idx,
+                                float kl_coef, const BwdWork &w, DeviceStatus *st, cudaStream_t s);
 
 }  // namespace msa

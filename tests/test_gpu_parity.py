@@ -28,6 +28,10 @@ CASES = [
     ("k_ge_nb", 1, 640, 640, 0, 8, 2, 64, 64, 8),
     ("decode_like", 2, 3, 2000, 1997, 8, 2, 64, 64, 4),
     ("chunked_prefill", 1, 300, 1100, 800, 8, 4, 128, 128, 4),
+    ("g8_d128_b2_ragged", 2, 1000, 1000, 0, 16, 2, 128, 128, 4),
+    ("g4_d128_ragged", 1, 1100, 1100, 0, 8, 2, 128, 128, 4),
+    ("g2_d128", 1, 700, 700, 0, 4, 2, 128, 128, 5),
+    ("g1_d128", 1, 800, 800, 0, 2, 2, 128, 128, 3),
 ]
 TRAIN_CASES = [c for c in CASES if c[4] == 0 and c[2] == c[3]]
 
