@@ -62,6 +62,56 @@ def useful_flops(w, positions=None):
     return f
 
 
+def kernel_work(w):
+    """Algorithmic work of one launch of each library kernel that can
+    dominate a step: (FLOPs, 'tensor') for the contractions, (bytes, 'hbm')
+    for the streaming kernels.  Closed forms over the selected work."""
+    pos = np.arange(w.N, dtype=np.int64)
+    T = tokens_per_row(w, pos).astype(np.float64)
+    nsel = np.minimum(w.topk, pos // w.block + 1).astype(np.float64)     # valid selected blocks per row
+    vis_blocks = (pos // w.block + 1).astype(np.float64)
+    B = w.B
+    work = {
+        "index_scores_tc_kernel": (B * float(np.sum(2.0 * w.d_idx * (pos + 1) * w.Hkv)), "tensor"),
+        "sparse_fwd_tc_kernel": (B * float(np.sum(4.0 * w.d * T * w.Hq)), "tensor"),
+        "kl_tc_kernel": (B * float(np.sum(2.0 * w.d * T * w.Hq + 2.0 * w.d_idx * T * w.Hkv)), "tensor"),
+        "bwd_main_tc_kernel": (B * float(np.sum(10.0 * w.d * T * w.Hq)), "tensor"),
+        "bwd_index_tc_kernel": (B * float(np.sum(6.0 * w.d_idx * T * w.Hkv)), "tensor"),
+        # block scores of the visible blocks in, indices out
+        "block_topk_kernel": (B * w.Hkv * float(np.sum(vis_blocks * 4.0 + w.topk * 4.0)), "hbm"),
+        # bf16 partial rows + (m, z) per valid slot in, bf16 row + lse out
+        "sparse_fwd_combine_kernel": (B * w.Hq * float(np.sum(nsel * (2.0 * w.d + 8.0) + 2.0 * w.d + 4.0)), "hbm"),
+        # dQ and dq_idx: bf16 partial rows per valid slot in, one bf16 row out
+        "bwd_combine_kernel": (B * float(np.sum((nsel + 1.0) * 2.0 * (w.d * w.Hq + w.d_idx * w.Hkv))), "hbm"),
+    }
+    return work
+
+
+def kernel_traffic(kernel, w):
+    """DRAM bytes per launch of `kernel` (dram__bytes_read.sum +
+    dram__bytes_write.sum) from the committed ncu summary of that kernel,
+    scaled from the captured case to this workload by the units the kernel
+    processes; None when no summary exists or when the kernel's source has
+    changed since the counters were taken (the summary records its hash)."""
+    import hashlib
+    import re
+    prof = os.path.join(ROOT, "profiles", f"{kernel}.md")
+    if not os.path.exists(prof):
+        return None
+    m = re.search(r"traffic-per-unit: (\S+) bytes per (\S+); source (\S+) sha1 (\w+)", open(prof).read())
+    if not m:
+        return None
+    per_unit, unit, src, sha = float(m.group(1)), m.group(2), m.group(3), m.group(4)
+    path = os.path.join(ROOT, src)
+    if not os.path.exists(path) or hashlib.sha1(open(path, "rb").read()).hexdigest() != sha:
+        return None
+    if unit != "slot":
+        return None
+    pos = np.arange(w.N, dtype=np.int64)
+    slots = w.B * w.Hkv * float(np.sum(np.minimum(w.topk, pos // w.block + 1)))   # (query, group, block) entries
+    return round(per_unit * slots)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -244,6 +294,7 @@ def main():
     barrier(world)
     torch.cuda.synchronize(dev)
     launches0 = api.launch_count()
+    api.kernel_timing(True)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
@@ -252,6 +303,8 @@ def main():
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     launches = api.launch_count() - launches0
+    ktimes = api.kernel_times()          # per kernel: (launches, total ms) over the timed steps
+    api.kernel_timing(False)
     barrier(world)
     clk = clocks.stop()
     elapsed_ms = t_start.elapsed_time(t_end)
@@ -292,17 +345,32 @@ def main():
                "ms_per_step": round(e2e_ms, 3), "tokens_per_s": round(world * w.B * w.N / (e2e_ms * 1e-3), 1),
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": 4}
 
-    # ---- roofline of the dominant kernel (the phase that takes longest)
+    # ---- roofline of the dominant kernel (longest total device time in the
+    # timed region, from CUDA events recorded around each launch on its stream)
     peaks = load_peaks()
     phase_flops = {"index_select": fl["index"], "sparse_attn_fwd": fl["fwd"], "kl_fwd": fl["kl"], "fused_bwd": fl["bwd"]}
-    kernel_of = {"index_select": "index_scores_kernel (+ block_topk_kernel)", "sparse_attn_fwd": "sparse_attn_fwd_kernel",
-                 "kl_fwd": "kl_fwd_kernel (+ kl_reduce_kernel)", "fused_bwd": "fused_bwd_kernel (+ prep/finalize kernels)"}
-    dom = max(phase_ms, key=phase_ms.get)
-    ach = phase_flops[dom] / (phase_ms[dom] * 1e-3) / 1e12
-    roofline = {"kernel": kernel_of[dom], "bound": "tensor", "achieved": round(ach, 2),
-                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4),
-                "frac_of_sustained": round(ach / peaks["bf16_tflops_sustained"], 4),
-                "peak_source": peaks["source"] + " burst bf16", "traffic": None}
+    work = kernel_work(w)
+    dom = max(ktimes, key=lambda k: ktimes[k][1])
+    n_l, tot_ms = ktimes[dom]
+    per_launch_ms = tot_ms / n_l
+    units, bound = work.get(dom, (None, None))
+    if units is None:
+        roofline = {"kernel": dom, "bound": None, "achieved": None, "peak": None, "unit": None, "frac": None,
+                    "traffic": None, "launch_ms": round(per_launch_ms, 3)}
+    elif bound == "tensor":
+        ach = units / (per_launch_ms * 1e-3) / 1e12
+        roofline = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 2), "peak": peaks["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4),
+                    "frac_of_sustained": round(ach / peaks["bf16_tflops_sustained"], 4),
+                    "peak_source": peaks["source"] + " burst bf16", "traffic": kernel_traffic(dom, w),
+                    "algorithmic_per_launch": units, "launch_ms": round(per_launch_ms, 3)}
+    else:
+        ach = units / (per_launch_ms * 1e-3) / 1e9
+        roofline = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4), "peak_source": peaks["source"] + " copy",
+                    "traffic": kernel_traffic(dom, w), "algorithmic_per_launch": units,
+                    "launch_ms": round(per_launch_ms, 3)}
+    kernels_ms = {k: round(v[1] / args.steps, 3) for k, v in sorted(ktimes.items(), key=lambda kv: -kv[1][1])}
 
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and world == 1:
@@ -325,6 +393,7 @@ def main():
             "phases_ms": {k: round(v, 3) for k, v in phase_ms.items()},
             "phases_tflops": {k: round(phase_flops[k] / (phase_ms[k] * 1e-3) / 1e12, 2) for k in phase_ms},
             "useful_tflop_per_step": round(step_flops / 1e12, 4),
+            "kernels_ms_per_step": kernels_ms,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
             "clocks": clk, "impl": "ours",
         }

@@ -99,6 +99,10 @@ def lib() -> ctypes.CDLL:
             L.msa_last_error.restype = ctypes.c_char_p
             L.msa_version.restype = ctypes.c_char_p
             L.msa_launch_count.restype = ctypes.c_ulonglong
+            L.msa_kernel_timing.argtypes = [ctypes.c_int]
+            L.msa_kernel_timing.restype = ctypes.c_int
+            L.msa_kernel_timing_report.argtypes = [ctypes.c_char_p, sz]
+            L.msa_kernel_timing_report.restype = sz
             _lib = L
         return _lib
 
@@ -226,6 +230,26 @@ def fused_bwd(shape: Shape, q, k, v, o, d_o, lse, q_idx, k_idx, sel_idx, lse_idx
 def check_device_status(workspace, stream=None) -> None:
     """msa_check_device_status: raises MsaError on a recorded device-side error."""
     _check(lib().msa_check_device_status(_ptr(workspace), _stream(stream)))
+
+
+def kernel_timing(enable: bool) -> bool:
+    """msa_kernel_timing: bracket each library kernel with CUDA events on its
+    stream while enabled (clears earlier records); returns the previous setting."""
+    return bool(lib().msa_kernel_timing(1 if enable else 0))
+
+
+def kernel_times() -> dict:
+    """msa_kernel_timing_report: {kernel name: (launches, total ms)} of the
+    launches recorded since timing was last switched."""
+    L = lib()
+    need = int(L.msa_kernel_timing_report(None, 0))
+    buf = ctypes.create_string_buffer(need)
+    L.msa_kernel_timing_report(buf, need)
+    out = {}
+    for line in buf.value.decode().splitlines():
+        name, n, ms = line.split()
+        out[name] = (int(n), float(ms))
+    return out
 
 
 def launch_count() -> int:

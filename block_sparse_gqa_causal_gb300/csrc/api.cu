@@ -3,9 +3,12 @@
 #include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
+#include <string.h>
 
 #include <atomic>
+#include <mutex>
 #include <string>
+#include <vector>
 
 #include "msa.h"
 #include "msa_internal.h"
@@ -163,6 +166,39 @@ msa_status check_ws(void *ws, size_t ws_bytes, size_t need)
 
 namespace msa {
 void note_launch(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+
+namespace {
+struct TimingRec {
+    std::string name;
+    cudaEvent_t a = nullptr, b = nullptr;
+};
+std::mutex g_tmu;
+bool g_timing = false;
+std::vector<TimingRec> g_trecs;   // events are created once and reused
+size_t g_tused = 0;
+}  // namespace
+
+TimedLaunch::TimedLaunch(const char *name, cudaStream_t s) : slot(-1), stream(s)
+{
+    std::lock_guard<std::mutex> lk(g_tmu);
+    if (!g_timing) return;
+    if (g_tused == g_trecs.size()) {
+        TimingRec r;
+        if (cudaEventCreate(&r.a) != cudaSuccess || cudaEventCreate(&r.b) != cudaSuccess) return;
+        g_trecs.push_back(r);
+    }
+    TimingRec &r = g_trecs[g_tused];
+    r.name = name;
+    if (cudaEventRecord(r.a, s) != cudaSuccess) return;
+    slot = (long)g_tused++;
+}
+
+TimedLaunch::~TimedLaunch()
+{
+    if (slot < 0) return;
+    std::lock_guard<std::mutex> lk(g_tmu);
+    cudaEventRecord(g_trecs[(size_t)slot].b, stream);
+}
 msa_status problem_from_shape(const msa_shape *shape, Problem &p) { return make_problem(shape, p); }
 msa_status set_error(msa_status st, const char *msg) { return fail(st, "%s", msg); }
 }  // namespace msa
@@ -174,6 +210,43 @@ const char *msa_version(void) { return "msa-gb300 0.1 (sm_103a)"; }
 const char *msa_last_error(void) { return g_err.c_str(); }
 
 unsigned long long msa_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int msa_kernel_timing(int enable)
+{
+    std::lock_guard<std::mutex> lk(g_tmu);
+    const int prev = g_timing ? 1 : 0;
+    g_timing = enable != 0;
+    g_tused = 0;
+    return prev;
+}
+
+size_t msa_kernel_timing_report(char *buf, size_t len)
+{
+    std::lock_guard<std::mutex> lk(g_tmu);
+    std::vector<std::pair<std::string, std::pair<long, double>>> agg;
+    for (size_t x = 0; x < g_tused; ++x) {
+        TimingRec &r = g_trecs[x];
+        float ms = 0.f;
+        if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) ms = -1.f;
+        size_t k = 0;
+        while (k < agg.size() && agg[k].first != r.name) ++k;
+        if (k == agg.size()) agg.push_back({r.name, {0, 0.0}});
+        agg[k].second.first += 1;
+        agg[k].second.second += ms < 0.f ? 0.0 : (double)ms;
+    }
+    std::string out;
+    char line[256];
+    for (auto &e : agg) {
+        snprintf(line, sizeof line, "%s %ld %.6f\n", e.first.c_str(), e.second.first, e.second.second);
+        out += line;
+    }
+    if (buf && len) {
+        const size_t n = out.size() < len - 1 ? out.size() : len - 1;
+        memcpy(buf, out.data(), n);
+        buf[n] = 0;
+    }
+    return out.size() + 1;
+}
 
 size_t msa_workspace_size(const msa_shape *shape, int op)
 {

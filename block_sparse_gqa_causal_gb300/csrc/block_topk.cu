@@ -185,7 +185,10 @@ cudaError_t launch_block_topk(const Problem &p, const float *bs, int32_t *sel, D
 {
     const long long rows = (long long)p.B * p.Nq * p.Hkv;
     const long long grid = (rows + kWarps - 1) / kWarps;
-    block_topk_kernel<<<(unsigned)grid, kWarps * 32, 0, s>>>(p, bs, sel);
+    {
+        TimedLaunch timed_("block_topk_kernel", s);
+        block_topk_kernel<<<(unsigned)grid, kWarps * 32, 0, s>>>(p, bs, sel);
+    }
     note_launch();
     return cudaGetLastError();
 }

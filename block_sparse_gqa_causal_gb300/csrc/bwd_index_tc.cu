@@ -371,8 +371,11 @@ cudaError_t launch_bwd_index_tc(const Problem &p, const bf16 *q_idx, const bf16 
     const unsigned bi[3] = {64, (unsigned)kKeys, 1};
     if ((e = make_tmap_bf16(&tki, k_idx, 3, di, si, bi)) != cudaSuccess) return e;
     const float coef = kl_coef / ((float)p.B * (float)p.Nq * (float)p.Hkv);
-    bwd_index_tc_kernel<<<dim3(p.Hkv, p.nb, p.B), kThreads, ALLOC, s>>>(tki, p, q_idx, lse_idx, coef, w.bucket_off,
-                                                                       w.bucket_q, w.pt, w.dqi_part, w.dki_acc, st);
+    {
+        TimedLaunch timed_("bwd_index_tc_kernel", s);
+        bwd_index_tc_kernel<<<dim3(p.Hkv, p.nb, p.B), kThreads, ALLOC, s>>>(tki, p, q_idx, lse_idx, coef, w.bucket_off,
+                                                                           w.bucket_q, w.pt, w.dqi_part, w.dki_acc, st);
+    }
     note_launch();
     return cudaGetLastError();
 }

@@ -497,8 +497,11 @@ cudaError_t launch_g(const Problem &p, const bf16 *q, const bf16 *k, const bf16 
         if ((e = make_tmap_bf16(&tk, k, 4, dk4, sk, bk)) != cudaSuccess) return e;
         if ((e = make_tmap_bf16(&tv, v, 4, dk4, sk, bk)) != cudaSuccess) return e;
     }
-    bwd_main_tc_kernel<G><<<dim3(p.Hkv, p.nb, p.B), kThreads, ALLOC, s>>>(
-        tq, tdo, tk, tv, p, q, d_o, lse, w.D, w.bucket_off, w.bucket_q, dk, dv, w.dq_part, w.pt, st);
+    {
+        TimedLaunch timed_("bwd_main_tc_kernel", s);
+        bwd_main_tc_kernel<G><<<dim3(p.Hkv, p.nb, p.B), kThreads, ALLOC, s>>>(
+            tq, tdo, tk, tv, p, q, d_o, lse, w.D, w.bucket_off, w.bucket_q, dk, dv, w.dq_part, w.pt, st);
+    }
     note_launch();
     return cudaGetLastError();
 }

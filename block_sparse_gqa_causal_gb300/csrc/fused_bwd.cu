@@ -516,9 +516,12 @@ cudaError_t launch_main(const Problem &p, const bf16 *q, const bf16 *k, const bf
     const int sm = BwdSmem<D, DI>::SMEM;
     cudaError_t e = cudaFuncSetAttribute(fused_bwd_kernel<D, DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
     if (e != cudaSuccess) return e;
-    fused_bwd_kernel<D, DI><<<dim3(p.nb * 2, p.Hkv, p.B), kThreads, sm, s>>>(
-        p, q, k, v, d_o, lse, q_idx, k_idx, lse_idx, kl_coef, w.D, w.bucket_off, w.bucket_q, dk, dv, w.dq_acc,
-        w.dqi_acc, w.dki_acc);
+    {
+        TimedLaunch timed_("fused_bwd_kernel", s);
+        fused_bwd_kernel<D, DI><<<dim3(p.nb * 2, p.Hkv, p.B), kThreads, sm, s>>>(
+            p, q, k, v, d_o, lse, q_idx, k_idx, lse_idx, kl_coef, w.D, w.bucket_off, w.bucket_q, dk, dv, w.dq_acc,
+            w.dqi_acc, w.dki_acc);
+    }
     note_launch();
     return cudaGetLastError();
 }
@@ -542,7 +545,10 @@ cudaError_t launch_fused_bwd(const Problem &p, const bf16 *q, const bf16 *k, con
     if ((e = cudaMemsetAsync(w.dki_acc, 0, n_dki * 4, s)) != cudaSuccess) return e;
 
     const long long rows = (long long)p.B * p.Nq * p.Hq;
-    bwd_rowdot_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p, o, d_o, w.D);
+    {
+        TimedLaunch timed_("bwd_rowdot_kernel", s);
+        bwd_rowdot_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p, o, d_o, w.D);
+    }
     note_launch();
     if ((e = launch_inverse_index(p, sel, w.bucket_cnt, w.bucket_off, w.bucket_scratch, w.bucket_q, st, s)) != cudaSuccess)
         return e;
@@ -551,22 +557,37 @@ cudaError_t launch_fused_bwd(const Problem &p, const bf16 *q, const bf16 *k, con
         // main branch first: it leaves the teacher per (bucket entry, key) for the index branch
         if ((e = launch_bwd_main_tc(p, q, k, v, d_o, lse, w, dk, dv, st, s)) != cudaSuccess) return e;
         if ((e = launch_bwd_index_tc(p, q_idx, k_idx, lse_idx, kl_coef, w, st, s)) != cudaSuccess) return e;
-        bwd_combine_kernel<128><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p, sel, w.dq_part, dq, p.Hq, p.G);
+        {
+            TimedLaunch timed_("bwd_combine_kernel", s);
+            bwd_combine_kernel<128><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p, sel, w.dq_part, dq, p.Hq, p.G);
+        }
         note_launch();
         const long long rows_i = (long long)p.B * p.Nq * p.Hkv;
-        bwd_combine_kernel<128><<<(unsigned)((rows_i + 7) / 8), 256, 0, s>>>(p, sel, w.dqi_part, dq_idx, p.Hkv, 1);
+        {
+            TimedLaunch timed_("bwd_combine_kernel", s);
+            bwd_combine_kernel<128><<<(unsigned)((rows_i + 7) / 8), 256, 0, s>>>(p, sel, w.dqi_part, dq_idx, p.Hkv, 1);
+        }
         note_launch();
     } else {
         if (p.d == 128) e = launch_main<128, 64>(p, q, k, v, d_o, lse, q_idx, k_idx, lse_idx, kl_coef, w, dk, dv, s);
         else if (p.d_idx == 128) e = launch_main<64, 128>(p, q, k, v, d_o, lse, q_idx, k_idx, lse_idx, kl_coef, w, dk, dv, s);
         else e = launch_main<64, 64>(p, q, k, v, d_o, lse, q_idx, k_idx, lse_idx, kl_coef, w, dk, dv, s);
         if (e != cudaSuccess) return e;
-        f32_to_bf16_kernel<<<4 * p.num_sms, 256, 0, s>>>(w.dq_acc, dq, n_dq);
+        {
+            TimedLaunch timed_("f32_to_bf16_kernel", s);
+            f32_to_bf16_kernel<<<4 * p.num_sms, 256, 0, s>>>(w.dq_acc, dq, n_dq);
+        }
         note_launch();
-        f32_to_bf16_kernel<<<4 * p.num_sms, 256, 0, s>>>(w.dqi_acc, dq_idx, n_dqi);
+        {
+            TimedLaunch timed_("f32_to_bf16_kernel", s);
+            f32_to_bf16_kernel<<<4 * p.num_sms, 256, 0, s>>>(w.dqi_acc, dq_idx, n_dqi);
+        }
         note_launch();
     }
-    f32_to_bf16_kernel<<<4 * p.num_sms, 256, 0, s>>>(w.dki_acc, dk_idx, n_dki);
+    {
+        TimedLaunch timed_("f32_to_bf16_kernel", s);
+        f32_to_bf16_kernel<<<4 * p.num_sms, 256, 0, s>>>(w.dki_acc, dk_idx, n_dki);
+    }
     note_launch();
     return cudaGetLastError();
 }

@@ -260,7 +260,10 @@ cudaError_t launch_t(const Problem &p, const bf16 *q_idx, const bf16 *k_idx, flo
     splits = (p.nb + span - 1) / span;
     e = cudaFuncSetAttribute(index_scores_tc_kernel<DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::ALLOC);
     if (e != cudaSuccess) return e;
-    index_scores_tc_kernel<DI><<<dim3(tiles, splits, p.B), kThreads, S::ALLOC, s>>>(tq, tk, p, bs, span, st);
+    {
+        TimedLaunch timed_("index_scores_tc_kernel", s);
+        index_scores_tc_kernel<DI><<<dim3(tiles, splits, p.B), kThreads, S::ALLOC, s>>>(tq, tk, p, bs, span, st);
+    }
     note_launch();
     return cudaGetLastError();
 }

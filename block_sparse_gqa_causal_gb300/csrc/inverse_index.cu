@@ -133,13 +133,25 @@ cudaError_t launch_inverse_index(const Problem &p, const int32_t *sel, int32_t *
         if ((e = cudaFuncSetAttribute(index_fill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm)) != cudaSuccess) return e;
     }
     const dim3 grid(nct, p.B * p.Hkv);
-    index_count_kernel<<<grid, kThreads, sm, s>>>(p, sel, nct, cta_hist, st);
+    {
+        TimedLaunch timed_("index_count_kernel", s);
+        index_count_kernel<<<grid, kThreads, sm, s>>>(p, sel, nct, cta_hist, st);
+    }
     note_launch();
-    index_cta_scan_kernel<<<(unsigned)((nbk + 255) / 256), 256, 0, s>>>(p, nct, cta_hist, cta_base, cnt);
+    {
+        TimedLaunch timed_("index_cta_scan_kernel", s);
+        index_cta_scan_kernel<<<(unsigned)((nbk + 255) / 256), 256, 0, s>>>(p, nct, cta_hist, cta_base, cnt);
+    }
     note_launch();
-    index_bucket_scan_kernel<<<1, 1024, 0, s>>>(cnt, off, (int)nbk);
+    {
+        TimedLaunch timed_("index_bucket_scan_kernel", s);
+        index_bucket_scan_kernel<<<1, 1024, 0, s>>>(cnt, off, (int)nbk);
+    }
     note_launch();
-    index_fill_kernel<<<grid, kThreads, sm, s>>>(p, sel, nct, cta_base, off, list);
+    {
+        TimedLaunch timed_("index_fill_kernel", s);
+        index_fill_kernel<<<grid, kThreads, sm, s>>>(p, sel, nct, cta_base, off, list);
+    }
     note_launch();
     return cudaGetLastError();
 }

@@ -233,8 +233,11 @@ cudaError_t launch_kl_t(const Problem &p, const bf16 *q, const bf16 *k, const bf
 {
     const int sm = KlSmem<D, DI>::SMEM;
     cudaFuncSetAttribute(kl_fwd_kernel<D, DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
-    kl_fwd_kernel<D, DI><<<dim3(p.Nq, p.Hkv, p.B), kThreads, sm, s>>>(p, q, k, q_idx, k_idx, sel, lse, lse_idx,
-                                                                      kl_rows, st);
+    {
+        TimedLaunch timed_("kl_fwd_kernel", s);
+        kl_fwd_kernel<D, DI><<<dim3(p.Nq, p.Hkv, p.B), kThreads, sm, s>>>(p, q, k, q_idx, k_idx, sel, lse, lse_idx,
+                                                                          kl_rows, st);
+    }
     note_launch();
     return cudaGetLastError();
 }
@@ -256,7 +259,10 @@ cudaError_t launch_kl_reduce(const Problem &p, const float *kl_rows, float kl_co
 {
     const long long n = (long long)p.B * p.Hkv * p.Nq;
     const double scale = (double)kl_coef / (double)n;
-    kl_reduce_kernel<<<1, 1024, 0, s>>>(kl_rows, n, (float)scale, kl_loss);
+    {
+        TimedLaunch timed_("kl_reduce_kernel", s);
+        kl_reduce_kernel<<<1, 1024, 0, s>>>(kl_rows, n, (float)scale, kl_loss);
+    }
     note_launch();
     return cudaGetLastError();
 }

@@ -434,8 +434,11 @@ cudaError_t launch_ddg(const Problem &p, const bf16 *q, const bf16 *k, const bf1
         const unsigned bi[3] = {64, (unsigned)kKeys, 1};
         if ((e = make_tmap_bf16(&tki, k_idx, 3, di, si, bi)) != cudaSuccess) return e;
     }
-    kl_tc_kernel<D, DI, G><<<dim3(p.Hkv, p.nb, p.B), kThreads, L::ALLOC, s>>>(tq, tk, tki, p, q, q_idx, lse,
-                                                                             w.bucket_off, w.bucket_q, w.part, st);
+    {
+        TimedLaunch timed_("kl_tc_kernel", s);
+        kl_tc_kernel<D, DI, G><<<dim3(p.Hkv, p.nb, p.B), kThreads, L::ALLOC, s>>>(tq, tk, tki, p, q, q_idx, lse,
+                                                                                 w.bucket_off, w.bucket_q, w.part, st);
+    }
     note_launch();
     return cudaGetLastError();
 }
@@ -466,7 +469,10 @@ cudaError_t launch_kl_keymajor(const Problem &p, const bf16 *q, const bf16 *k, c
     else e = launch_dd<64, 64>(p, q, k, q_idx, k_idx, sel, lse, w, st, s);
     if (e != cudaSuccess) return e;
     const long long rows = (long long)p.B * p.Hkv * p.Nq;
-    kl_combine_kernel<<<(unsigned)((rows + 255) / 256), 256, 0, s>>>(p, sel, w.part, lse_idx, kl_rows);
+    {
+        TimedLaunch timed_("kl_combine_kernel", s);
+        kl_combine_kernel<<<(unsigned)((rows + 255) / 256), 256, 0, s>>>(p, sel, w.part, lse_idx, kl_rows);
+    }
     note_launch();
     return cudaGetLastError();
 }

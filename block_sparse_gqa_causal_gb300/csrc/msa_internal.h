@@ -24,6 +24,18 @@ using bf16 = __nv_bfloat16;
 // Counts kernel launches made by the library (read by msa_launch_count()).
 void note_launch(int n = 1);
 
+// Kernel timing hook (off unless msa_kernel_timing(1) is in effect): while
+// alive, brackets the launch issued in its scope with CUDA events recorded on
+// the launch's stream, filed under the kernel's name.
+struct TimedLaunch {
+    TimedLaunch(const char *name, cudaStream_t s);
+    ~TimedLaunch();
+    TimedLaunch(const TimedLaunch &) = delete;
+    TimedLaunch &operator=(const TimedLaunch &) = delete;
+    long slot;
+    cudaStream_t stream;
+};
+
 // 3-D bf16 TMA tensor map (dims innermost first, strides of dims 1 and 2
 // in bytes), box {box0, box1, 1}, 128-byte swizzle, zero fill out of bounds.
 cudaError_t make_tmap_bf16_3d(CUtensorMap *map, const void *base, unsigned long long d0, unsigned long long d1,

@@ -228,12 +228,18 @@ cudaError_t launch_sparse_attn_fwd(const Problem &p, const bf16 *q, const bf16 *
     if (p.d == 128) {
         const int sm = FwdSmem<128>::SMEM;
         cudaFuncSetAttribute(sparse_attn_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
-        sparse_attn_fwd_kernel<128><<<grid, kThreads, sm, s>>>(p, q, k, v, sel, o, lse, st);
+        {
+            TimedLaunch timed_("sparse_attn_fwd_kernel", s);
+            sparse_attn_fwd_kernel<128><<<grid, kThreads, sm, s>>>(p, q, k, v, sel, o, lse, st);
+        }
         note_launch();
     } else {
         const int sm = FwdSmem<64>::SMEM;
         cudaFuncSetAttribute(sparse_attn_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
-        sparse_attn_fwd_kernel<64><<<grid, kThreads, sm, s>>>(p, q, k, v, sel, o, lse, st);
+        {
+            TimedLaunch timed_("sparse_attn_fwd_kernel", s);
+            sparse_attn_fwd_kernel<64><<<grid, kThreads, sm, s>>>(p, q, k, v, sel, o, lse, st);
+        }
         note_launch();
     }
     return cudaGetLastError();

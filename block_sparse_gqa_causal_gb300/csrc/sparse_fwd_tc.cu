@@ -477,8 +477,11 @@ cudaError_t launch_dg(const Problem &p, const bf16 *q, const bf16 *k, const bf16
         if ((e = make_tmap_bf16(&tk, k, 4, dk, sk, bk)) != cudaSuccess) return e;
         if ((e = make_tmap_bf16(&tv, v, 4, dk, sk, bk)) != cudaSuccess) return e;
     }
-    sparse_fwd_tc_kernel<D, G><<<dim3(p.Hkv, p.nb, p.B), kThreads, L::ALLOC, s>>>(
-        tq, tk, tv, p, q, w.bucket_off, w.bucket_q, w.part, w.stats, st);
+    {
+        TimedLaunch timed_("sparse_fwd_tc_kernel", s);
+        sparse_fwd_tc_kernel<D, G><<<dim3(p.Hkv, p.nb, p.B), kThreads, L::ALLOC, s>>>(
+            tq, tk, tv, p, q, w.bucket_off, w.bucket_q, w.part, w.stats, st);
+    }
     note_launch();
     return cudaGetLastError();
 }
@@ -507,9 +510,15 @@ cudaError_t launch_sparse_fwd_keymajor(const Problem &p, const bf16 *q, const bf
     if (e != cudaSuccess) return e;
     const long long rows = (long long)p.B * p.Nq * p.Hq;
     if (p.d == 128)
-        sparse_fwd_combine_kernel<128><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p, sel, w.part, w.stats, o, lse);
+        {
+            TimedLaunch timed_("sparse_fwd_combine_kernel", s);
+            sparse_fwd_combine_kernel<128><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p, sel, w.part, w.stats, o, lse);
+        }
     else
-        sparse_fwd_combine_kernel<64><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p, sel, w.part, w.stats, o, lse);
+        {
+            TimedLaunch timed_("sparse_fwd_combine_kernel", s);
+            sparse_fwd_combine_kernel<64><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p, sel, w.part, w.stats, o, lse);
+        }
     note_launch();
     return cudaGetLastError();
 }

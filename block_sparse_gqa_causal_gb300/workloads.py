@@ -61,3 +61,8 @@ BY_NAME = {w.name: w for w in ALL}
 TRAIN_128K = PREFILL_128K.scaled(name="train_n128k", kl=True, train=True,
                                  notes="prefill_n128k shapes with KL and fused backward")
 BY_NAME[TRAIN_128K.name] = TRAIN_128K
+# The same head layout at 8K tokens: the small case for detailed profiles
+# (inputs still larger than L2, a few GB on the device).
+TRAIN_8K_H64 = PREFILL_128K.scaled(name="train_n8k_h64", N=8192, seed=5, kl=True, train=True,
+                                   notes="train_n128k head layout at 8,192 tokens")
+BY_NAME[TRAIN_8K_H64.name] = TRAIN_8K_H64

@@ -182,6 +182,19 @@ const char *msa_version(void);
  * (monotonic; for accounting launches in a timed region). */
 unsigned long long msa_launch_count(void);
 
+/* Kernel timing, a measurement aid with no counterpart in the method.
+ * msa_kernel_timing(1) makes every later call bracket each kernel it launches
+ * with a pair of CUDA events recorded on the call's stream (the events are
+ * created on first use and reused); msa_kernel_timing(0) stops it.  Either
+ * call forgets what was recorded before; the return value is the previous
+ * setting.  Off by default: then no event is created or recorded. */
+int msa_kernel_timing(int enable);
+
+/* Waits for the recorded events and writes one line per kernel name,
+ * "<kernel> <launches> <total milliseconds>\n", into buf (at most len bytes,
+ * NUL-terminated).  Returns the size the whole report needs, NUL included. */
+size_t msa_kernel_timing_report(char *buf, size_t len);
+
 #ifdef __cplusplus
 }
 #endif
