@@ -49,7 +49,9 @@ struct Meta {
     int nq;
 };
 constexpr int META_BYTES = (int)((sizeof(Meta) + 127) & ~size_t(127));
-constexpr int OFF_BAR = OFF_META + 2 * META_BYTES;
+constexpr int OFF_STAGE = OFF_META + 2 * META_BYTES;   // per epilogue warp: dq_idx [64 rows][32 features] bf16
+constexpr int STAGE_BYTES = 64 * 64;
+constexpr int OFF_BAR = OFF_STAGE + kEpiWarps * STAGE_BYTES;
 constexpr int ALLOC = OFF_BAR + 256 + 1024;
 
 constexpr uint32_t TM_S = 0, TM_DKI = 256, TM_DQI = 384;   // TM_S: 2 x 128
@@ -255,14 +257,25 @@ bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, cons
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(dq_free);
-            bf16 *dst = dqi_part + kr;
+            // transpose the warp's [32 features][64 queries] block through shared
+            // memory, then write 64 contiguous bytes per row with 16-byte stores
+            uint8_t *stage = sm + OFF_STAGE + (warp - 2) * STAGE_BYTES;
 #pragma unroll
             for (int cc = 0; cc < 32; ++cc) {
-                const long long a0 = __shfl_sync(0xffffffffu, rp_prev[0], cc);
-                const long long a1 = __shfl_sync(0xffffffffu, rp_prev[1], cc);
-                if (a0 >= 0) dst[a0 * DI] = __float2bfloat16_rn(p.scale_idx * __uint_as_float(v0[cc]));
-                if (a1 >= 0) dst[a1 * DI] = __float2bfloat16_rn(p.scale_idx * __uint_as_float(v1[cc]));
+                *reinterpret_cast<bf16 *>(stage + cc * 64 + lane * 2) =
+                    __float2bfloat16_rn(p.scale_idx * __uint_as_float(v0[cc]));
+                *reinterpret_cast<bf16 *>(stage + (32 + cc) * 64 + lane * 2) =
+                    __float2bfloat16_rn(p.scale_idx * __uint_as_float(v1[cc]));
             }
+            __syncwarp();
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                const int row = it * 8 + (lane >> 2), q4 = lane & 3;
+                const long long rix = __shfl_sync(0xffffffffu, rp_prev[it >> 2], row & 31);
+                const uint4 x = *reinterpret_cast<const uint4 *>(stage + row * 64 + q4 * 16);
+                if (rix >= 0) *reinterpret_cast<uint4 *>(dqi_part + rix * DI + qd * 32 + q4 * 8) = x;
+            }
+            __syncwarp();
             return true;
         };
         for (int n = 0; ok && n < nch; ++n) {

@@ -44,11 +44,13 @@ constexpr int SUBK = kKeys * 128;               // [128 keys][64 bf16] swizzled 
 constexpr int TILE_R = kRows * D * 2;
 constexpr int OFF_K = 0;
 constexpr int OFF_V = OFF_K + 2 * SUBK;
-constexpr int OFF_STG = OFF_V + 2 * SUBK;       // 2 stages x {Q, dO}
+constexpr int kStages = 3;                      // Q/dO stages
+constexpr int kPBuf = 1;                        // P/dS tile buffers
+constexpr int OFF_STG = OFF_V + 2 * SUBK;       // kStages x {Q, dO}
 constexpr int STG_BYTES = 2 * TILE_R;
-constexpr int OFF_P = OFF_STG + 2 * STG_BYTES;  // 2 buffers of P^T  [128 keys][64 rows]
-constexpr int OFF_DS = OFF_P + 2 * SUBK;        // 2 buffers of dS^T [128 keys][64 rows]
-constexpr int OFF_META = OFF_DS + 2 * SUBK;
+constexpr int OFF_P = OFF_STG + kStages * STG_BYTES;   // P^T  [128 keys][64 rows] per buffer
+constexpr int OFF_DS = OFF_P + kPBuf * SUBK;           // dS^T [128 keys][64 rows] per buffer
+constexpr int OFF_META = OFF_DS + kPBuf * SUBK;
 
 struct Meta {                 // per stage
     float lse2[kRows];        // lse * log2(e) of each row (+inf for padding)
@@ -60,7 +62,9 @@ struct Meta {                 // per stage
     int nq;                   // queries in the chunk
 };
 constexpr int META_BYTES = (int)((sizeof(Meta) + 127) & ~size_t(127));
-constexpr int OFF_BAR = OFF_META + 2 * META_BYTES;
+constexpr int OFF_STAGE = OFF_META + kStages * META_BYTES;   // per epilogue warp: dQ [32 rows][32 features] bf16
+constexpr int STAGE_BYTES = 32 * 64;
+constexpr int OFF_BAR = OFF_STAGE + kEpiWarps * STAGE_BYTES;
 constexpr int ALLOC = OFF_BAR + 256 + 1024;
 
 constexpr uint32_t TM_DV = 0, TM_DK = 128, TM_S = 256, TM_DP = 320, TM_DQ = 384;   // TM_DQ: 2 x 64
@@ -117,21 +121,25 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
-    uint64_t *full = bars, *empty = bars + 2, *p_full = bars + 4, *p_free = bars + 6;
-    uint64_t *dq_full = bars + 8, *dq_free = bars + 10;
-    uint64_t *kv_full = bars + 12, *s_full = bars + 13, *tm_free = bars + 14, *done = bars + 15;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
+    uint64_t *full = bars, *empty = bars + 3, *p_full = bars + 6, *p_free = bars + 8;
+    uint64_t *dq_full = bars + 10, *dq_free = bars + 12;
+    uint64_t *kv_full = bars + 14, *s_full = bars + 15, *tm_free = bars + 16, *done = bars + 17;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 18);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int a = 0; a < 2; ++a) {
+        for (int a = 0; a < kStages; ++a) {
             // G == 8: lane 0's expect_tx arrival + 32 row-data arrivals;
             // otherwise 32 cp.async arrivals + 32 row-data arrivals
             tc::mbar_init(&full[a], G == 8 ? 33 : 64);
             tc::mbar_init(&empty[a], 1 + kEpiWarps);   // grads MMAs done + epilogue has read the row data
+        }
+        for (int a = 0; a < kPBuf; ++a) {
             tc::mbar_init(&p_full[a], kEpiWarps);
             tc::mbar_init(&p_free[a], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
             tc::mbar_init(&dq_full[a], 1);
             tc::mbar_init(&dq_free[a], kEpiWarps);
         }
@@ -167,7 +175,7 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         int ent[EPL], ent_next[EPL];
         load_entries(ent, bucket_q, qbeg, min(QC, qend - qbeg), lane);
         for (int m = 0; m < nch; ++m) {
-            const int s = m & 1;
+            const int s = m % kStages;
             const int q0 = qbeg + m * QC;
             const int nq = min(QC, qend - q0);
             // this chunk's per-row values and the next chunk's entries are
@@ -188,7 +196,7 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 vd[t] = ok ? __ldg(Dg + hi) : 0.f;
             }
             if (m + 1 < nch) load_entries(ent_next, bucket_q, q0 + QC, min(QC, qend - q0 - QC), lane);
-            if (!tc::mbar_wait(&empty[s], ((uint32_t)(m >> 1) & 1u) ^ 1u, st, 101, abort_flag)) break;
+            if (!tc::mbar_wait(&empty[s], ((uint32_t)(m / kStages) & 1u) ^ 1u, st, 101, abort_flag)) break;
             Meta *meta = reinterpret_cast<Meta *>(sm + OFF_META + s * META_BYTES);
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
@@ -251,7 +259,7 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             constexpr uint32_t I_DQ = tc::idesc_bf16(128, kRows) | tc::kAMajorMN | tc::kBMajorMN;
             const uint32_t aK = smem_u32(sm + OFF_K), aV = smem_u32(sm + OFF_V);
             auto issue_scores = [&](int n) {
-                const uint32_t sq = smem_u32(sm + OFF_STG + (n & 1) * STG_BYTES), sdo = sq + TILE_R;
+                const uint32_t sq = smem_u32(sm + OFF_STG + (n % kStages) * STG_BYTES), sdo = sq + TILE_R;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t h = ks >> 2, ko = (ks & 3) * 32;
@@ -264,16 +272,16 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 tc::mma_commit(s_full);
             };
             auto issue_grads = [&](int n) {
-                const int pb = n & 1;
-                const uint32_t sq = smem_u32(sm + OFF_STG + (n & 1) * STG_BYTES), sdo = sq + TILE_R;
+                const int pb = n % kPBuf, qb = n & 1;
+                const uint32_t sq = smem_u32(sm + OFF_STG + (n % kStages) * STG_BYTES), sdo = sq + TILE_R;
                 const uint32_t aP = smem_u32(sm + OFF_P + pb * SUBK), aDS = smem_u32(sm + OFF_DS + pb * SUBK);
                 // dQ^T = K^T dS^T: A = K read MN-major (64-feature atoms SUBK apart),
                 // B = dS^T [keys][rows] read MN-major; K = 128 keys
 #pragma unroll
                 for (int ks = 0; ks < kKeys / 16; ++ks)
-                    tc::mma_bf16(tmem + TM_DQ + pb * kRows, tc::sdesc_sw128(aK + ks * 2048, SUBK, 1024),
+                    tc::mma_bf16(tmem + TM_DQ + qb * kRows, tc::sdesc_sw128(aK + ks * 2048, SUBK, 1024),
                                  tc::sdesc_sw128(aDS + ks * 2048, SUBK, 1024), I_DQ, ks > 0);
-                tc::mma_commit(&dq_full[pb]);
+                tc::mma_commit(&dq_full[qb]);
                 // dV += P^T dO, dK += dS^T Q: B = dO / Q read MN-major (feature
                 // halves 1024 bytes apart, 8-row groups 2048 apart); K = 64 rows
 #pragma unroll
@@ -284,31 +292,45 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                     tc::mma_bf16(tmem + TM_DK, tc::sdesc_k128(aDS + ks * 32), tc::sdesc_sw128(sq + ks * 4096, 1024, 2048),
                                  I_DKV, acc);
                 }
-                tc::mma_commit(&empty[n & 1]);
+                tc::mma_commit(&empty[n % kStages]);
                 tc::mma_commit(&p_free[pb]);
             };
             bool ok = tc::mbar_wait(kv_full, 0, st, 102, abort_flag);
-            if (ok && nch > 0) {
-                ok = tc::mbar_wait(&full[0], 0, st, 103, abort_flag);
-                if (ok) {
+            if (ok) tc::fence_proxy_async();
+            // Issue in whichever order the inputs become ready: the scores of the
+            // next chunk need its Q/dO stage and the epilogue's release of S/dP;
+            // the gradients of chunk n need its P/dS tiles (and, for the dQ^T
+            // buffer, the drain of chunk n-2).  Waiting for one while the other
+            // is ready would leave the tensor pipe idle: the next stage is only
+            // loaded once the gradients that read the older one have completed.
+            int ns = 0, ng = 0;            // next chunk to issue scores / gradients for
+            uint32_t idle = 0;
+            while (ok && ng < nch) {
+                bool did = false;
+                if (ns < nch && tc::mbar_try_wait(&full[ns % kStages], (uint32_t)(ns / kStages) & 1u) &&
+                    (ns == 0 || tc::mbar_try_wait(tm_free, (uint32_t)(ns - 1) & 1u))) {
                     tc::fence_proxy_async();
                     tc::fence_after_sync();
-                    issue_scores(0);
+                    issue_scores(ns);
+                    ++ns;
+                    did = true;
                 }
-            }
-            for (int n = 0; ok && n < nch; ++n) {
-                if (n + 1 < nch) {
-                    if (!tc::mbar_wait(&full[(n + 1) & 1], (uint32_t)((n + 1) >> 1) & 1u, st, 104, abort_flag)) break;
-                    if (!tc::mbar_wait(tm_free, (uint32_t)n & 1u, st, 105, abort_flag)) break;
-                    tc::fence_proxy_async();
+                if (ng < ns && tc::mbar_try_wait(&p_full[ng % kPBuf], (uint32_t)(ng / kPBuf) & 1u) &&
+                    (ng < 2 || tc::mbar_try_wait(&dq_free[ng & 1], ((uint32_t)(ng >> 1) & 1u) ^ 1u))) {
                     tc::fence_after_sync();
-                    issue_scores(n + 1);
+                    issue_grads(ng);
+                    ++ng;
+                    did = true;
                 }
-                if (!tc::mbar_wait(&p_full[n & 1], (uint32_t)(n >> 1) & 1u, st, 106, abort_flag)) break;
-                if (n >= 2 && !tc::mbar_wait(&dq_free[n & 1], ((uint32_t)(n >> 1) & 1u) ^ 1u, st, 107, abort_flag))
-                    break;
-                tc::fence_after_sync();
-                issue_grads(n);
+                if (did) {
+                    idle = 0;
+                } else if (++idle >= tc::kSpinLimit) {
+                    report(st, kDevTimeout, 104, ns * 65536 + ng);
+                    *abort_flag = 1;
+                    ok = false;
+                } else if ((idle & 1023u) == 1023u && *abort_flag) {
+                    ok = false;
+                }
             }
             // every MMA issued above has completed once `done` fires
             tc::mma_commit(done);
@@ -338,18 +360,28 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&dq_free[pb]);
-            bf16 *dst = dq_part + kr;              // this thread's feature
+            // transpose the warp's [32 features][32 rows] block through shared
+            // memory, then write 64 contiguous bytes per row with 16-byte stores
+            uint8_t *stage = sm + OFF_STAGE + (warp - 2) * STAGE_BYTES;
 #pragma unroll
-            for (int cc = 0; cc < 32; ++cc) {
-                const long long rix = __shfl_sync(0xffffffffu, ridx_prev, cc);
-                if (rix >= 0) dst[rix * D] = __float2bfloat16_rn(p.scale * __uint_as_float(v[cc]));
+            for (int cc = 0; cc < 32; ++cc)
+                *reinterpret_cast<bf16 *>(stage + cc * 64 + lane * 2) =
+                    __float2bfloat16_rn(p.scale * __uint_as_float(v[cc]));
+            __syncwarp();
+#pragma unroll
+            for (int it = 0; it < 4; ++it) {
+                const int row = it * 8 + (lane >> 2), q4 = lane & 3;
+                const long long rix = __shfl_sync(0xffffffffu, ridx_prev, row);
+                const uint4 x = *reinterpret_cast<const uint4 *>(stage + row * 64 + q4 * 16);
+                if (rix >= 0) *reinterpret_cast<uint4 *>(dq_part + rix * D + qd * 32 + q4 * 8) = x;
             }
+            __syncwarp();
             return true;
         };
         for (int n = 0; ok && n < nch; ++n) {
-            const int s = n & 1, pb = n & 1;
+            const int s = n % kStages, pb = n % kPBuf;
             const Meta *meta = reinterpret_cast<const Meta *>(sm + OFF_META + s * META_BYTES);
-            if (!wwait(&full[s], (uint32_t)(n >> 1) & 1u, st, 112, abort_flag)) { ok = false; break; }
+            if (!wwait(&full[s], (uint32_t)(n / kStages) & 1u, st, 112, abort_flag)) { ok = false; break; }
             if (!wwait(s_full, (uint32_t)n & 1u, st, 113, abort_flag)) { ok = false; break; }
             tc::fence_after_sync();
             uint32_t sv[32], dp[32];
@@ -407,7 +439,10 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 const int qq = cb / G + u;
                 if (qq < nq) pt_out[(long long)(e0 + qq) * kKeys + kr] = __float2half_rn(ptq[u] * invG);
             }
-            if (n >= 2 && !wwait(&p_free[pb], ((uint32_t)(n >> 1) & 1u) ^ 1u, st, 114, abort_flag)) { ok = false; break; }
+            if (n >= kPBuf && !wwait(&p_free[pb], (uint32_t)((n - kPBuf) / kPBuf) & 1u, st, 114, abort_flag)) {
+                ok = false;
+                break;
+            }
             uint8_t *sp = sm + OFF_P + pb * SUBK, *sd = sm + OFF_DS + pb * SUBK;
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
@@ -428,7 +463,7 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         if (ok && nch > 0) {
             // the last chunk's buffer release follows every MMA of the bucket
             const int m = nch - 1;
-            ok = wwait(&p_free[m & 1], (uint32_t)(m >> 1) & 1u, st, 115, abort_flag);
+            ok = wwait(&p_free[m % kPBuf], (uint32_t)(m / kPBuf) & 1u, st, 115, abort_flag);
             tc::fence_after_sync();
         }
         if (ok) {

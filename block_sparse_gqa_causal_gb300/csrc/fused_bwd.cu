@@ -55,26 +55,45 @@ struct BwdSmem {
 };
 
 // ------------------------------------------------------------------ prep
-__global__ void bwd_rowdot_kernel(Problem p, const bf16 *__restrict__ o, const bf16 *__restrict__ d_o,
-                                  float *__restrict__ D)
+// D[b, h, i] = sum_e dO * O over one (b, i, h) row.  A warp covers 8 rows;
+// each lane loads 16 bytes of O and dO per row (all loads in flight), lanes
+// sharing a row reduce with shuffles.  DD = d.
+template <int DD>
+__global__ void __launch_bounds__(256) bwd_rowdot_kernel(Problem p, const bf16 *__restrict__ o,
+                                                         const bf16 *__restrict__ d_o, float *__restrict__ D)
 {
-    // one warp per (b, i, h) row: D[b, h, i] = sum_e dO * O
-    const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    constexpr int LPR = DD / 8;                  // lanes per row
+    constexpr int RPI = 32 / LPR;                // rows per load instruction
+    constexpr int NT = 8 / RPI;
     const int lane = threadIdx.x & 31;
-    if (row >= (long long)p.B * p.Nq * p.Hq) return;
-    const uint32_t *po = reinterpret_cast<const uint32_t *>(o + row * p.d);
-    const uint32_t *pd = reinterpret_cast<const uint32_t *>(d_o + row * p.d);
-    float acc = 0.f;
-    for (int e = lane; e < p.d / 2; e += 32) {
-        const float2 a = unpack_bf16(po[e]), c = unpack_bf16(pd[e]);
-        acc += a.x * c.x + a.y * c.y;
+    const long long nrows = (long long)p.B * p.Nq * p.Hq;
+    const long long row0 = ((long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 8;
+    uint4 a[NT], c[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        const long long row = row0 + t * RPI + lane / LPR;
+        const bool ok = row < nrows;
+        a[t] = ok ? __ldg(reinterpret_cast<const uint4 *>(o + row * DD) + lane % LPR) : make_uint4(0, 0, 0, 0);
+        c[t] = ok ? __ldg(reinterpret_cast<const uint4 *>(d_o + row * DD) + lane % LPR) : make_uint4(0, 0, 0, 0);
     }
-    acc = warp_sum(acc);
-    if (lane == 0) {
-        const int h = (int)(row % p.Hq);
-        const long long bi = row / p.Hq;
-        const int i = (int)(bi % p.Nq), b = (int)(bi / p.Nq);
-        D[((long long)b * p.Hq + h) * p.Nq + i] = acc;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        const uint32_t aw[4] = {a[t].x, a[t].y, a[t].z, a[t].w}, cw[4] = {c[t].x, c[t].y, c[t].z, c[t].w};
+        float acc = 0.f;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+            const float2 x = unpack_bf16(aw[q4]), y = unpack_bf16(cw[q4]);
+            acc += x.x * y.x + x.y * y.y;
+        }
+#pragma unroll
+        for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        const long long row = row0 + t * RPI + lane / LPR;
+        if (lane % LPR == 0 && row < nrows) {
+            const int h = (int)(row % p.Hq);
+            const long long bi = row / p.Hq;
+            const int i = (int)(bi % p.Nq), b = (int)(bi / p.Nq);
+            D[((long long)b * p.Hq + h) * p.Nq + i] = acc;
+        }
     }
 }
 
@@ -90,12 +109,17 @@ __global__ void f32_to_bf16_kernel(const float *__restrict__ src, bf16 *__restri
 // out[row] = sum over the valid slots s of part[row * topk + s].  Rows are
 // (b, i, h) over H heads; head h belongs to group h / Gh, whose selection
 // decides which slots hold a partial (same validity rule as the inverse
-// index).  DD = row length (128 or 64).
+// index).  A row's partials are contiguous: each lane loads 16 bytes of
+// several slots at once (DD/8 lanes per slot), and lanes holding the same
+// features of different slots add up with shuffles.  DD = 128 or 64.
 template <int DD>
 __global__ void __launch_bounds__(256)
 bwd_combine_kernel(Problem p, const int32_t *__restrict__ sel, const bf16 *__restrict__ part, bf16 *__restrict__ out,
                    int H, int Gh)
 {
+    constexpr int LPS = DD / 8;                 // lanes per slot row
+    constexpr int SPI = 32 / LPS;               // slots per load instruction
+    constexpr int NI = 32 / SPI;                // instructions to cover 32 slots
     const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= (long long)p.B * p.Nq * H) return;
@@ -105,32 +129,35 @@ bwd_combine_kernel(Problem p, const int32_t *__restrict__ sel, const bf16 *__res
     const long long pos = (long long)p.q_offset + i;
     const int32_t *srow = sel + (((long long)b * p.Hkv + h / Gh) * p.Nq + i) * p.topk;
     const int cl = lane < p.topk ? srow[lane] : -1;
-    const bool sv = cl >= 0 && cl < p.nb && (long long)cl * 128 <= pos;
-    constexpr int PER = DD / 32;
-    float acc[PER];
+    const unsigned mask = __ballot_sync(0xffffffffu, cl >= 0 && cl < p.nb && (long long)cl * 128 <= pos);
+    const uint4 *src = reinterpret_cast<const uint4 *>(part + row * p.topk * DD);
+    float acc[8];
 #pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-    for (unsigned m = __ballot_sync(0xffffffffu, sv); m; m &= m - 1) {
-        const int s = __ffs(m) - 1;
-        const bf16 *src = part + (row * p.topk + s) * DD + lane * PER;
-        if constexpr (PER == 4) {
-            const uint2 u = *reinterpret_cast<const uint2 *>(src);
-            const float2 a0 = unpack_bf16(u.x), a1 = unpack_bf16(u.y);
-            acc[0] += a0.x;
-            acc[1] += a0.y;
-            acc[2] += a1.x;
-            acc[3] += a1.y;
-        } else {
-            const float2 a0 = unpack_bf16(*reinterpret_cast<const uint32_t *>(src));
-            acc[0] += a0.x;
-            acc[1] += a0.y;
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    uint4 u[NI];
+#pragma unroll
+    for (int t = 0; t < NI; ++t) {
+        const int s = t * SPI + lane / LPS;
+        u[t] = (t * SPI < p.topk && ((mask >> s) & 1u)) ? __ldg(src + s * LPS + lane % LPS) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int t = 0; t < NI; ++t) {
+        const uint32_t w[4] = {u[t].x, u[t].y, u[t].z, u[t].w};
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+            const float2 x = unpack_bf16(w[q4]);
+            acc[2 * q4] += x.x;
+            acc[2 * q4 + 1] += x.y;
         }
     }
-    bf16 *dst = out + row * DD + lane * PER;
-    if constexpr (PER == 4)
-        *reinterpret_cast<uint2 *>(dst) = make_uint2(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]));
-    else
-        *reinterpret_cast<uint32_t *>(dst) = pack_bf16(acc[0], acc[1]);
+#pragma unroll
+    for (int off = LPS; off < 32; off <<= 1)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
+    if (lane < LPS)
+        reinterpret_cast<uint4 *>(out + row * DD)[lane] =
+            make_uint4(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]), pack_bf16(acc[4], acc[5]),
+                       pack_bf16(acc[6], acc[7]));
 }
 
 // ------------------------------------------------------------------ main
@@ -547,7 +574,8 @@ cudaError_t launch_fused_bwd(const Problem &p, const bf16 *q, const bf16 *k, con
     const long long rows = (long long)p.B * p.Nq * p.Hq;
     {
         TimedLaunch timed_("bwd_rowdot_kernel", s);
-        bwd_rowdot_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p, o, d_o, w.D);
+        if (p.d == 128) bwd_rowdot_kernel<128><<<(unsigned)((rows + 63) / 64), 256, 0, s>>>(p, o, d_o, w.D);
+        else bwd_rowdot_kernel<64><<<(unsigned)((rows + 63) / 64), 256, 0, s>>>(p, o, d_o, w.D);
     }
     note_launch();
     if ((e = launch_inverse_index(p, sel, w.bucket_cnt, w.bucket_off, w.bucket_scratch, w.bucket_q, st, s)) != cudaSuccess)

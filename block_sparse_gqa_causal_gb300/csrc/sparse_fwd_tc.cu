@@ -272,12 +272,17 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         bool pvalid = false;
         bool ok = true;
         // writes the partial output of chunk m (row data held in pm, pz, pi, pslot, pvalid)
+        // writes the partial output of chunk m (row data held in pm, pz, pi, pslot,
+        // pvalid).  The rows go through this warp's rows of the chunk's P tile
+        // (free once the O MMA that read it has completed) so that each store
+        // covers whole 256-byte partial rows.
         auto emit = [&](int m) -> bool {
             const int am = m & 1;
             if (!tc::mbar_wait(&o_full[am], (uint32_t)(m >> 1) & 1u, st, 74, abort_flag)) return false;
             tc::fence_after_sync();
-            const long long row = (((long long)b * p.Nq + pi) * p.Hq + (long long)r * G + g) * p.topk + pslot;
-            bf16 *dst = part + row * D;
+            const long long prow =
+                pvalid ? (((long long)b * p.Nq + pi) * p.Hq + (long long)r * G + g) * p.topk + pslot : -1;
+            uint8_t *stg = sm + L::OFF_P + am * (2 * SUB);
 #pragma unroll
             for (int c64 = 0; c64 < D / 64; ++c64) {
                 uint32_t o0[32], o1[32];
@@ -285,26 +290,34 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                 tc::tmem_ld32_nowait(tmem + lane_base + L::TM_O + am * D + c64 * 64 + 32, o1);
                 tc::tmem_wait32(o0);
                 tc::tmem_wait32(o1);
-                if (pvalid) {
 #pragma unroll
-                    for (int x = 0; x < 32; x += 8) {
-                        *reinterpret_cast<uint4 *>(dst + c64 * 64 + x) = make_uint4(
-                            pack_bf16(__uint_as_float(o0[x]), __uint_as_float(o0[x + 1])),
-                            pack_bf16(__uint_as_float(o0[x + 2]), __uint_as_float(o0[x + 3])),
-                            pack_bf16(__uint_as_float(o0[x + 4]), __uint_as_float(o0[x + 5])),
-                            pack_bf16(__uint_as_float(o0[x + 6]), __uint_as_float(o0[x + 7])));
-                        *reinterpret_cast<uint4 *>(dst + c64 * 64 + 32 + x) = make_uint4(
-                            pack_bf16(__uint_as_float(o1[x]), __uint_as_float(o1[x + 1])),
-                            pack_bf16(__uint_as_float(o1[x + 2]), __uint_as_float(o1[x + 3])),
-                            pack_bf16(__uint_as_float(o1[x + 4]), __uint_as_float(o1[x + 5])),
-                            pack_bf16(__uint_as_float(o1[x + 6]), __uint_as_float(o1[x + 7])));
-                    }
+                for (int x = 0; x < 32; x += 8) {
+                    const int c0 = c64 * 8 + x / 8, c1 = c0 + 4;      // 16-byte chunks of the row
+                    *reinterpret_cast<uint4 *>(stg + (c0 >> 3) * SUB + swz(rho, c0 & 7)) = make_uint4(
+                        pack_bf16(__uint_as_float(o0[x]), __uint_as_float(o0[x + 1])),
+                        pack_bf16(__uint_as_float(o0[x + 2]), __uint_as_float(o0[x + 3])),
+                        pack_bf16(__uint_as_float(o0[x + 4]), __uint_as_float(o0[x + 5])),
+                        pack_bf16(__uint_as_float(o0[x + 6]), __uint_as_float(o0[x + 7])));
+                    *reinterpret_cast<uint4 *>(stg + (c1 >> 3) * SUB + swz(rho, c1 & 7)) = make_uint4(
+                        pack_bf16(__uint_as_float(o1[x]), __uint_as_float(o1[x + 1])),
+                        pack_bf16(__uint_as_float(o1[x + 2]), __uint_as_float(o1[x + 3])),
+                        pack_bf16(__uint_as_float(o1[x + 4]), __uint_as_float(o1[x + 5])),
+                        pack_bf16(__uint_as_float(o1[x + 6]), __uint_as_float(o1[x + 7])));
                 }
             }
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&o_free[am]);
-            if (pvalid) stats[row] = make_float2(pm, pz);
+            constexpr int CPR = D / 8, RPI = 32 / CPR;              // chunks per row, rows per store
+#pragma unroll
+            for (int it = 0; it < 32 / RPI; ++it) {
+                const int rr = it * RPI + lane / CPR, ch = lane % CPR, rho2 = quarter * 32 + rr;
+                const long long rix = __shfl_sync(0xffffffffu, prow, rr);
+                const uint4 x = *reinterpret_cast<const uint4 *>(stg + (ch >> 3) * SUB + swz(rho2, ch & 7));
+                if (rix >= 0) *reinterpret_cast<uint4 *>(part + rix * D + ch * 8) = x;
+            }
+            __syncwarp();
+            if (pvalid) stats[prow] = make_float2(pm, pz);
             return true;
         };
         for (int n = 0; ok && n < nch; ++n) {
@@ -400,12 +413,18 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     }
 }
 
-// One warp per (b, i, h) row: merge the row's slots.
+// One warp per (b, i, h) row: merge the row's slots.  The row's partials are
+// contiguous; every lane loads 16 bytes of several slots at once (D/8 lanes
+// per slot, all loads in flight while the slot weights are reduced), and
+// lanes holding the same features of different slots add up with shuffles.
 template <int D>
 __global__ void __launch_bounds__(256)
 sparse_fwd_combine_kernel(Problem p, const int32_t *__restrict__ sel, const bf16 *__restrict__ part,
                           const float2 *__restrict__ stats, bf16 *__restrict__ o, float *__restrict__ lse)
 {
+    constexpr int LPS = D / 8;                  // lanes per slot row
+    constexpr int SPI = 32 / LPS;               // slots per load instruction
+    constexpr int NI = 32 / SPI;
     const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= (long long)p.B * p.Nq * p.Hq) return;
@@ -415,43 +434,44 @@ sparse_fwd_combine_kernel(Problem p, const int32_t *__restrict__ sel, const bf16
     const int r = h / p.G;
     const long long pos = (long long)p.q_offset + i;
     const int32_t *srow = sel + (((long long)b * p.Hkv + r) * p.Nq + i) * p.topk;
-    // slot validity (same rule as the inverse index) and the row max
+    // slot validity (same rule as the inverse index)
     const int cl = lane < p.topk ? srow[lane] : -1;
     const bool sv = cl >= 0 && cl < p.nb && (long long)cl * 128 <= pos;
+    const unsigned mask = __ballot_sync(0xffffffffu, sv);
+    const uint4 *src = reinterpret_cast<const uint4 *>(part + row * p.topk * D);
+    uint4 u[NI];
+#pragma unroll
+    for (int t = 0; t < NI; ++t) {
+        const int s = t * SPI + lane / LPS;
+        u[t] = (t * SPI < p.topk && ((mask >> s) & 1u)) ? __ldg(src + s * LPS + lane % LPS) : make_uint4(0, 0, 0, 0);
+    }
     const float2 mz = sv ? stats[row * p.topk + lane] : make_float2(-INFINITY, 0.f);
     const float M = warp_max(mz.x);
     const float w = sv ? exp2f(mz.x - M) : 0.f;
     const float Z = warp_sum(w * mz.y);
-    constexpr int PER = D / 32;                 // features per lane
-    float acc[PER];
+    float acc[8];
 #pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-    const unsigned mask = __ballot_sync(0xffffffffu, sv);
-    for (unsigned m = mask; m; m &= m - 1) {
-        const int s = __ffs(m) - 1;
-        const float ws = __shfl_sync(0xffffffffu, w, s);
-        const bf16 *src = part + (row * p.topk + s) * D + lane * PER;
-        if constexpr (PER == 4) {
-            const uint2 u = *reinterpret_cast<const uint2 *>(src);
-            const float2 a0 = unpack_bf16(u.x), a1 = unpack_bf16(u.y);
-            acc[0] += ws * a0.x;
-            acc[1] += ws * a0.y;
-            acc[2] += ws * a1.x;
-            acc[3] += ws * a1.y;
-        } else {
-            const float2 a0 = unpack_bf16(*reinterpret_cast<const uint32_t *>(src));
-            acc[0] += ws * a0.x;
-            acc[1] += ws * a0.y;
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+    for (int t = 0; t < NI; ++t) {
+        const float ws = __shfl_sync(0xffffffffu, w, (t * SPI + lane / LPS) & 31);
+        const uint32_t wd[4] = {u[t].x, u[t].y, u[t].z, u[t].w};
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+            const float2 x = unpack_bf16(wd[q4]);
+            acc[2 * q4] += ws * x.x;
+            acc[2 * q4 + 1] += ws * x.y;
         }
     }
+#pragma unroll
+    for (int off = LPS; off < 32; off <<= 1)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
     const float inv = 1.f / Z;
-    bf16 *dst = o + row * D + lane * PER;
-    if constexpr (PER == 4) {
-        *reinterpret_cast<uint2 *>(dst) = make_uint2(pack_bf16(acc[0] * inv, acc[1] * inv),
-                                                     pack_bf16(acc[2] * inv, acc[3] * inv));
-    } else {
-        *reinterpret_cast<uint32_t *>(dst) = pack_bf16(acc[0] * inv, acc[1] * inv);
-    }
+    if (lane < LPS)
+        reinterpret_cast<uint4 *>(o + row * D)[lane] =
+            make_uint4(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv),
+                       pack_bf16(acc[4] * inv, acc[5] * inv), pack_bf16(acc[6] * inv, acc[7] * inv));
     if (lane == 0) lse[((long long)b * p.Hq + h) * p.Nq + i] = (M + log2f(Z)) * kLn2;
 }
 
