@@ -131,7 +131,7 @@ size_t klrows_bytes(const Problem &p) { return align256((size_t)p.B * p.Hkv * p.
 size_t kl_bytes(const Problem &p)
 {
     if (!fwd_keymajor(p)) return 0;
-    return align256((size_t)p.B * p.Hkv * p.Nq * p.topk * 4 * 16) + index_bytes(p);
+    return align256(kl_part_count(p) * 16) + align256((size_t)p.B * p.Hkv * p.Nq * p.topk * 128 * 2) + index_bytes(p);
 }
 
 // backward: D, dK_idx accumulators, the inverse index, and either the
@@ -342,7 +342,8 @@ msa_status msa_kl_fwd(const msa_shape *shape, const void *q, const void *k, cons
     cudaError_t e;
     if (fwd_keymajor(p)) {
         KlWork w;
-        w.part = cv.take<float4>((size_t)p.B * p.Hkv * p.Nq * p.topk * 4);
+        w.part = cv.take<float4>(kl_part_count(p));
+        w.pt = cv.take<__half>((size_t)p.B * p.Hkv * p.Nq * p.topk * 128);
         carve_index(cv, p, w);
         e = launch_kl_keymajor(p, static_cast<const bf16 *>(q), static_cast<const bf16 *>(k),
                                static_cast<const bf16 *>(q_idx), static_cast<const bf16 *>(k_idx), sel_idx, lse,

@@ -70,9 +70,12 @@ cudaError_t launch_kl_fwd(const Problem &p, const bf16 *q, const bf16 *k, const 
                           float *kl_rows, DeviceStatus *st, cudaStream_t s);
 // Key-major KL forward (many queries per selected block).
 struct KlWork {
-    float4 *part;        // [B, Hkv, Nq, topk, 4] per-warp partial sums
+    float4 *part;        // [B, Hkv, Nq, topk, kl_part_count / (B*Hkv*Nq*topk)] partial sums
+    __half *pt;          // [B*Hkv*Nq*topk entries, 128] teacher per (bucket entry, key)
     int32_t *bucket_cnt, *bucket_off, *bucket_scratch, *bucket_q;
 };
+// float4 partials the key-major KL writes (several per (query, group, slot))
+size_t kl_part_count(const Problem &p);
 cudaError_t launch_kl_keymajor(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *q_idx, const bf16 *k_idx,
                                const int32_t *sel, const float *lse, float *lse_idx, float *kl_rows, const KlWork &w,
                                DeviceStatus *st, cudaStream_t s);
