@@ -118,8 +118,10 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     const int nch = (qend - qbeg + QC - 1) / QC;
     const long long j0 = (long long)c * kKeys;
 
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // offset from the __shared__ array itself, so every access through `sm`
+    // stays a shared-memory access (no generic addressing)
+    uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
     uint64_t *full = bars, *empty = bars + 3, *p_full = bars + 6, *p_free = bars + 8;
     uint64_t *dq_full = bars + 10, *dq_free = bars + 12;

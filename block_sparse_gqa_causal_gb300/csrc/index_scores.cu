@@ -50,8 +50,10 @@ index_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_
                        Problem p, float *__restrict__ bs, int span, DeviceStatus *st)
 {
     using S = Smem<DI>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // offset from the __shared__ array itself, so every access through `smem`
+    // stays a shared-memory access (no generic addressing)
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sQ = smem;
     uint8_t *sK = smem + S::OFF_K;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::OFF_BAR);

@@ -110,8 +110,10 @@ kl_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     const int nch = (qend - qbeg + QPC - 1) / QPC;
     const long long j0 = (long long)c * kKeys;
 
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // offset from the __shared__ array itself, so every access through `sm`
+    // stays a shared-memory access (no generic addressing)
+    uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
     uint64_t *full = bars, *empty = bars + kStages, *s_full = bars + 2 * kStages, *s_free = s_full + 2;
     uint64_t *kv_full = s_free + 2, *done = kv_full + 1;
@@ -253,7 +255,7 @@ kl_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         const bool key_ok = j < p.Nk;
         const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
         const float sl2 = p.scale * kLog2e, invG = 1.f / (float)G;
-        constexpr int QH = 32 / G;                  // queries per 32 columns
+        constexpr int QH = 64 / G;                  // queries among this warp's 64 columns
         for (int n = 0; n < nch; ++n) {
             const Meta *meta = reinterpret_cast<const Meta *>(sm + L::OFF_META + (n % kStages) * L::META_BYTES);
             if (!wwait(&full[n % kStages], (uint32_t)(n / kStages) & 1u, st, 91, abort_flag)) break;
@@ -262,37 +264,43 @@ kl_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             uint32_t sv[2][32];
             tc::tmem_ld32_nowait(tmem + lane_base + (n & 1) * kRows + hf * 64, sv[0]);
             tc::tmem_ld32_nowait(tmem + lane_base + (n & 1) * kRows + hf * 64 + 32, sv[1]);
+            // row data into registers while the loads land
+            float l2[64];
+#pragma unroll
+            for (int x = 0; x < 16; ++x) {
+                const float4 l4 = reinterpret_cast<const float4 *>(meta->lse2 + hf * 64)[x];
+                l2[4 * x] = l4.x; l2[4 * x + 1] = l4.y; l2[4 * x + 2] = l4.z; l2[4 * x + 3] = l4.w;
+            }
+            unsigned long long vmask = 0;           // bit u: this key is visible to query u of the half
+#pragma unroll
+            for (int u = 0; u < QH; ++u)
+                vmask |= (key_ok && j <= (long long)meta->pos[hf * QH + u]) ? (1ull << u) : 0ull;
             const int nq = meta->nq, e0 = meta->e0;
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&empty[n % kStages]);   // row data now in registers
             tc::tmem_wait32(sv[0]);
             tc::tmem_wait32(sv[1]);
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&s_free[n & 1]);
+            float e[64];
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                const int cb = hf * 64 + h2 * 32;   // first (query, head) row of these 32 columns
-                float pt[QH];
+            for (int col = 0; col < 64; ++col)
+                e[col] = tc::ex2(__uint_as_float(sv[col >> 5][col & 31]) * sl2 - l2[col]);
 #pragma unroll
-                for (int u = 0; u < QH; ++u) pt[u] = 0.f;
+            for (int u = 0; u < QH; ++u) {
+                // pairwise sum over the query's G heads (adjacent columns)
+                float t[G];
 #pragma unroll
-                for (int x = 0; x < 8; ++x) {
-                    const float4 l4 = reinterpret_cast<const float4 *>(meta->lse2 + cb)[x];
-                    const float l2[4] = {l4.x, l4.y, l4.z, l4.w};
+                for (int g = 0; g < G; ++g) t[g] = e[u * G + g];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int col = 4 * x + e, u = col / G;
-                        const bool vis = key_ok && j <= (long long)meta->pos[cb / G + u];
-                        pt[u] += vis ? tc::ex2(__uint_as_float(sv[h2][col]) * sl2 - l2[e]) : 0.f;
-                    }
-                }
+                for (int w = G / 2; w > 0; w >>= 1)
 #pragma unroll
-                for (int u = 0; u < QH; ++u) {
-                    const int qq = cb / G + u;
-                    if (qq < nq) pt_out[(long long)(e0 + qq) * kKeys + kr] = __float2half_rn(pt[u] * invG);
-                }
+                    for (int g = 0; g < w; ++g) t[g] += t[g + w];
+                const int qq = hf * QH + u;
+                const bool vis = (vmask >> u) & 1ull;
+                if (qq < nq) pt_out[(long long)(e0 + qq) * kKeys + kr] = __float2half_rn(vis ? t[0] * invG : 0.f);
             }
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&empty[n % kStages]);
         }
     }
 
@@ -337,8 +345,10 @@ kl_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, const
     const int nch = (qend - qbeg + kQ - 1) / kQ;
     const long long j0 = (long long)c * kKeys;
 
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // offset from the __shared__ array itself, so every access through `sm`
+    // stays a shared-memory access (no generic addressing)
+    uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
     uint64_t *full = bars, *empty = bars + kStages, *s_full = bars + 2 * kStages, *s_free = s_full + 2;
     uint64_t *kv_full = s_free + 2, *done = kv_full + 1;

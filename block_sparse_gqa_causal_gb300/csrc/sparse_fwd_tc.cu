@@ -107,8 +107,10 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     if (qend <= qbeg) return;                               // nobody selected this block
     const int nch = (qend - qbeg + QPC - 1) / QPC;
 
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // offset from the __shared__ array itself, so every access through `sm`
+    // stays a shared-memory access (no generic addressing)
+    uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
     uint64_t *q_full = bars, *q_empty = bars + 2, *s_full = bars + 4, *s_free = bars + 6;
     uint64_t *p_full = bars + 8, *p_free = bars + 10, *o_full = bars + 12, *o_free = bars + 14;
