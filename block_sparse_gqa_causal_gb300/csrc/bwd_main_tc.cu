@@ -174,35 +174,40 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 tc::tma_load_4d(sm + OFF_V + h * SUBK, &tmap_v, kv_full, h * 64, r, (int)j0, b);
             }
         }
-        int ent[EPL], ent_next[EPL];
-        load_entries(ent, bucket_q, qbeg, min(QC, qend - qbeg), lane);
-        for (int m = 0; m < nch; ++m) {
-            const int s = m % kStages;
-            const int q0 = qbeg + m * QC;
-            const int nq = min(QC, qend - q0);
-            // this chunk's per-row values and the next chunk's entries are
-            // fetched before waiting for a free stage
-            float vl[2], vd[2];
+        // Entries run two chunks ahead and the rows' LSE and D one chunk ahead,
+        // so no load is waited for on the way to the next stage.
+        auto load_rows = [&](float (&vl)[2], float (&vd)[2], const int (&e_)[EPL], int nqx) {
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
                 const int rho = lane + 32 * t, qq = rho / G, g = rho % G;
                 int e = 0;
 #pragma unroll
                 for (int u = 0; u < EPL; ++u) {
-                    const int x = __shfl_sync(0xffffffffu, ent[u], qq & 31);
+                    const int x = __shfl_sync(0xffffffffu, e_[u], qq & 31);
                     if ((qq >> 5) == u) e = x;
                 }
-                const bool ok = qq < nq;
+                const bool ok = qq < nqx;
                 const long long hi = ((long long)b * p.Hq + r * G + g) * p.Nq + entry_row(e);
-                vl[t] = ok ? __ldg(lse + hi) * kLog2e : INFINITY;
+                vl[t] = ok ? __ldg(lse + hi) : INFINITY;
                 vd[t] = ok ? __ldg(Dg + hi) : 0.f;
             }
-            if (m + 1 < nch) load_entries(ent_next, bucket_q, q0 + QC, min(QC, qend - q0 - QC), lane);
+        };
+        int ent[EPL], ent1[EPL], ent2[EPL];
+        load_entries(ent, bucket_q, qbeg, min(QC, qend - qbeg), lane);
+        load_entries(ent1, bucket_q, qbeg + QC, min(QC, qend - qbeg - QC), lane);
+        float vl[2], vd[2], vl_next[2], vd_next[2];
+        load_rows(vl, vd, ent, min(QC, qend - qbeg));
+        for (int m = 0; m < nch; ++m) {
+            const int s = m % kStages;
+            const int q0 = qbeg + m * QC;
+            const int nq = min(QC, qend - q0);
+            load_entries(ent2, bucket_q, q0 + 2 * QC, min(QC, qend - q0 - 2 * QC), lane);
+            if (m + 1 < nch) load_rows(vl_next, vd_next, ent1, min(QC, qend - q0 - QC));
             if (!tc::mbar_wait(&empty[s], ((uint32_t)(m / kStages) & 1u) ^ 1u, st, 101, abort_flag)) break;
             Meta *meta = reinterpret_cast<Meta *>(sm + OFF_META + s * META_BYTES);
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
-                meta->lse2[lane + 32 * t] = vl[t];
+                meta->lse2[lane + 32 * t] = vl[t] * kLog2e;
                 meta->dd[lane + 32 * t] = vd[t];
             }
 #pragma unroll
@@ -250,7 +255,15 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             }
             tc::mbar_arrive(&full[s]);
 #pragma unroll
-            for (int t = 0; t < EPL; ++t) ent[t] = ent_next[t];
+            for (int t = 0; t < EPL; ++t) {
+                ent[t] = ent1[t];
+                ent1[t] = ent2[t];
+            }
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                vl[t] = vl_next[t];
+                vd[t] = vd_next[t];
+            }
         }
         cp_async_wait<0>();
     } else if (warp == 1) {

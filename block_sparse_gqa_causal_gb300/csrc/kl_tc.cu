@@ -155,31 +155,36 @@ kl_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             for (int h = 0; h < L::H; ++h)
                 tc::tma_load_4d(sm + L::OFF_K + h * SUB, &tmap_k, kv_full, h * 64, r, (int)j0, b);
         }
-        int ent[EPL], ent_next[EPL];
-        load_entries(ent, bucket_q, qbeg, min(QPC, qend - qbeg), lane);
-        for (int m = 0; m < nch; ++m) {
-            const int s = m % kStages;
-            const int q0 = qbeg + m * QPC;
-            const int nq = min(QPC, qend - q0);
-            // LSE of this chunk's rows and the next chunk's entries before the wait
-            float vl[4];
+        // Entries run two chunks ahead and the rows' LSE one chunk ahead, so
+        // no load is waited for on the way to the next stage.
+        auto load_lse = [&](float (&vl)[4], const int (&e_)[EPL], int nqx) {
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
                 const int rho = lane + 32 * t, qq = rho / G, g = rho % G;
                 int e = 0;
 #pragma unroll
                 for (int u = 0; u < EPL; ++u) {
-                    const int x = __shfl_sync(0xffffffffu, ent[u], qq & 31);
+                    const int x = __shfl_sync(0xffffffffu, e_[u], qq & 31);
                     if ((qq >> 5) == u) e = x;
                 }
-                vl[t] = qq < nq ? __ldg(lse + ((long long)b * p.Hq + r * G + g) * p.Nq + entry_row(e)) * kLog2e
-                                : INFINITY;
+                vl[t] = qq < nqx ? __ldg(lse + ((long long)b * p.Hq + r * G + g) * p.Nq + entry_row(e)) : INFINITY;
             }
-            if (m + 1 < nch) load_entries(ent_next, bucket_q, q0 + QPC, min(QPC, qend - q0 - QPC), lane);
+        };
+        int ent[EPL], ent1[EPL], ent2[EPL];
+        load_entries(ent, bucket_q, qbeg, min(QPC, qend - qbeg), lane);
+        load_entries(ent1, bucket_q, qbeg + QPC, min(QPC, qend - qbeg - QPC), lane);
+        float vl[4], vl_next[4];
+        load_lse(vl, ent, min(QPC, qend - qbeg));
+        for (int m = 0; m < nch; ++m) {
+            const int s = m % kStages;
+            const int q0 = qbeg + m * QPC;
+            const int nq = min(QPC, qend - q0);
+            load_entries(ent2, bucket_q, q0 + 2 * QPC, min(QPC, qend - q0 - 2 * QPC), lane);
+            if (m + 1 < nch) load_lse(vl_next, ent1, min(QPC, qend - q0 - QPC));
             if (!tc::mbar_wait(&empty[s], ((uint32_t)(m / kStages) & 1u) ^ 1u, st, 81, abort_flag)) break;
             Meta *meta = reinterpret_cast<Meta *>(sm + L::OFF_META + s * L::META_BYTES);
 #pragma unroll
-            for (int t = 0; t < 4; ++t) meta->lse2[lane + 32 * t] = vl[t];
+            for (int t = 0; t < 4; ++t) meta->lse2[lane + 32 * t] = vl[t] * kLog2e;
 #pragma unroll
             for (int t = 0; t < EPL; ++t) {
                 const int qq = lane + 32 * t;
@@ -219,7 +224,12 @@ kl_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             }
             tc::mbar_arrive(&full[s]);
 #pragma unroll
-            for (int t = 0; t < EPL; ++t) ent[t] = ent_next[t];
+            for (int t = 0; t < EPL; ++t) {
+                ent[t] = ent1[t];
+                ent1[t] = ent2[t];
+            }
+#pragma unroll
+            for (int t = 0; t < 4; ++t) vl[t] = vl_next[t];
         }
         cp_async_wait<0>();
     } else if (warp == 1) {

@@ -37,6 +37,8 @@ struct FwdLayout {
     static constexpr int KB = D / 64;
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = OFF_K + KB * SUB;
+    // Q stage: [128 rows][D] as 8-row groups of KB feature halves (1024-byte
+    // swizzle atoms): row rho, half h at (rho/8)*KB*1024 + h*1024 + (rho%8)*128
     static constexpr int OFF_Q = OFF_V + KB * SUB;          // 2 stages x KB sub-tiles
     static constexpr int OFF_P = OFF_Q + 2 * KB * SUB;      // 2 buffers x 2 sub-tiles (128 keys)
     static constexpr int OFF_META = OFF_P + 2 * 2 * SUB;    // 2 stages x QueryMeta
@@ -174,20 +176,14 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             __syncwarp();
             uint8_t *sq = sm + L::OFF_Q + a * (L::KB * SUB);
             if constexpr (G == 8) {
-                // one TMA box {64 features, 8 heads} per query and 64-feature half:
-                // 1024 bytes, so every box starts on a swizzle-pattern boundary.
-                // Padding slots read rows past the end of q (zero fill).
+                // one TMA box {64 features, 8 heads, KB halves} per query fills its
+                // row group (1024-byte aligned).  Padding slots read rows past the
+                // end of q (zero fill).
                 if (lane == 0) tc::mbar_arrive_expect_tx(&q_full[a], kRows * D * 2);
                 __syncwarp();
-#pragma unroll
-                for (int t = 0; t < EPL; ++t) {
-                    const int qq = lane + 32 * t;
-                    if (qq < QPC) {
-                        const int z = qq < nq ? b * p.Nq + entry_row(ent[t]) : p.B * p.Nq;
-#pragma unroll
-                        for (int kb = 0; kb < L::KB; ++kb)
-                            tc::tma_load_3d(sq + kb * SUB + qq * (G * 128), &tmap_q, &q_full[a], kb * 64, r * G, z);
-                    }
+                if (lane < QPC) {
+                    const int z = lane < nq ? b * p.Nq + entry_row(ent[0]) : p.B * p.Nq;
+                    tc::tma_load_4d(sq + lane * (L::KB * 1024), &tmap_q, &q_full[a], 0, r * G, 0, z);
                 }
                 tc::mbar_arrive(&q_full[a]);
             } else {
@@ -201,7 +197,7 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                     const int qq = rho / G, g = rho % G;
                     const bool ok = qq < nq;
                     const int i = meta->i[qq];
-                    cp_async16_zfill(sq + (ch >> 3) * SUB + swz(rho, ch & 7),
+                    cp_async16_zfill(sq + (rho >> 3) * (L::KB * 1024) + (ch >> 3) * 1024 + swz(rho & 7, ch & 7),
                                      q + (((long long)b * p.Nq + i) * p.Hq + (long long)r * G + g) * D + ch * 8, ok);
                 }
                 cp_async_arrive_noinc(&q_full[a]);
@@ -231,9 +227,10 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                     const uint32_t aQ = smem_u32(sm + L::OFF_Q + a * (L::KB * SUB));
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint32_t off = (ks >> 2) * SUB + (ks & 3) * 32;
-                        tc::mma_bf16(tmem + L::TM_S + a * 128, tc::sdesc_k128(aQ + off), tc::sdesc_k128(aK + off), I_S,
-                                     ks > 0);
+                        const uint32_t h = ks >> 2, ko = (ks & 3) * 32;
+                        // A = Q rows (K-major, 8-row groups KB KB apart), B = K
+                        tc::mma_bf16(tmem + L::TM_S + a * 128, tc::sdesc_sw128(aQ + h * 1024 + ko, 16, L::KB * 1024),
+                                     tc::sdesc_k128(aK + h * SUB + ko), I_S, ks > 0);
                     }
                     tc::mma_commit(&s_full[a]);
                     tc::mma_commit(&q_empty[a]);
@@ -486,10 +483,13 @@ cudaError_t launch_dg(const Problem &p, const bf16 *q, const bf16 *k, const bf16
     if (e != cudaSuccess) return e;
     CUtensorMap tq, tk, tv;
     {
-        const unsigned long long dq[3] = {(unsigned long long)D, (unsigned long long)p.Hq, (unsigned long long)p.B * p.Nq};
-        const unsigned long long sq[2] = {D * 2ull, (unsigned long long)p.Hq * D * 2ull};
-        const unsigned bq[3] = {64, (unsigned)G, 1};
-        if ((e = make_tmap_bf16(&tq, q, 3, dq, sq, bq)) != cudaSuccess) return e;
+        // Q as {d within a half, head, half, query row}: one box {64, G, D/64, 1}
+        // is a query's G head rows in every feature half
+        const unsigned long long dq4[4] = {64, (unsigned long long)p.Hq, (unsigned long long)(D / 64),
+                                           (unsigned long long)p.B * p.Nq};
+        const unsigned long long sq4[3] = {D * 2ull, 128ull, (unsigned long long)p.Hq * D * 2ull};
+        const unsigned bq4[4] = {64, (unsigned)G, (unsigned)(D / 64), 1};
+        if ((e = make_tmap_bf16(&tq, q, 4, dq4, sq4, bq4)) != cudaSuccess) return e;
         // K/V as [B][Nk][Hkv][D] (rows past Nk, even inside kv_rows, are out of bounds)
         const unsigned long long dk[4] = {(unsigned long long)D, (unsigned long long)p.Hkv, (unsigned long long)p.Nk,
                                           (unsigned long long)p.B};
