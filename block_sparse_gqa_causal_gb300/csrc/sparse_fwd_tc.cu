@@ -28,7 +28,8 @@ namespace {
 
 constexpr int kRows = 128;                  // (query, head) rows per chunk
 constexpr int kKeys = 128;
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 8;                // two warpgroups, taking alternate chunks
+constexpr int kWgWarps = 4;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr int SUB = 128 * 128;              // [128 rows][64 bf16] swizzled sub-tile
 
@@ -56,6 +57,15 @@ struct QueryMeta {         // per chunk, per query slot of the chunk (<= 128 que
 };
 
 __device__ __forceinline__ int swz(int row, int ch) { return row * 128 + ((ch ^ (row & 7)) << 4); }
+
+// Bounded wait with the same outcome on every lane (warp-collective TMEM
+// loads follow).
+__device__ __forceinline__ bool wwait(uint64_t *bar, uint32_t parity, DeviceStatus *st, int site,
+                                      volatile int *abort_flag)
+{
+    const bool r = tc::mbar_wait(bar, parity, st, site, abort_flag);
+    return __all_sync(0xffffffffu, r);
+}
 
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar)
 {
@@ -116,8 +126,8 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
     uint64_t *q_full = bars, *q_empty = bars + 2, *s_full = bars + 4, *s_free = bars + 6;
     uint64_t *p_full = bars + 8, *p_free = bars + 10, *o_full = bars + 12, *o_free = bars + 14;
-    uint64_t *kv_full = bars + 16;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 17);
+    uint64_t *kv_full = bars + 16, *done = bars + 17;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 18);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long j0 = (long long)c * kKeys;
@@ -127,15 +137,17 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             // G == 8: lane 0's expect_tx arrival + 32 metadata arrivals (TMA bytes);
             // otherwise 32 cp.async arrivals + 32 metadata arrivals
             tc::mbar_init(&q_full[a], G == 8 ? 33 : 64);
-            tc::mbar_init(&q_empty[a], 1 + kEpiWarps);  // S MMAs done + epilogue has read the metadata
+            // buffer a belongs to epilogue warpgroup a (chunks n with n % 2 == a)
+            tc::mbar_init(&q_empty[a], 1 + kWgWarps);   // S MMAs done + epilogue has read the metadata
             tc::mbar_init(&s_full[a], 1);
-            tc::mbar_init(&s_free[a], kEpiWarps);
-            tc::mbar_init(&p_full[a], kEpiWarps);
+            tc::mbar_init(&s_free[a], kWgWarps);
+            tc::mbar_init(&p_full[a], kWgWarps);
             tc::mbar_init(&p_free[a], 1);
             tc::mbar_init(&o_full[a], 1);
-            tc::mbar_init(&o_free[a], kEpiWarps);
+            tc::mbar_init(&o_free[a], kWgWarps);
         }
         tc::mbar_init(kv_full, 1);
+        tc::mbar_init(done, 1);
         *abort_flag = 0;
         tc::fence_mbar_init();
     }
@@ -215,53 +227,71 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             const uint32_t aK = smem_u32(sm + L::OFF_K), aV = smem_u32(sm + L::OFF_V);
             bool ok = tc::mbar_wait(kv_full, 0, st, 62, abort_flag);
             if (ok) tc::fence_proxy_async();
-            int issued = 0;
-            for (int n = 0; ok && n <= nch; ++n) {
-                if (n < nch) {
-                    const int a = n & 1;
-                    const uint32_t ph = (uint32_t)(n >> 1) & 1u;
-                    if (!tc::mbar_wait(&q_full[a], ph, st, 63, abort_flag)) break;
-                    if (!tc::mbar_wait(&s_free[a], ph ^ 1u, st, 64, abort_flag)) break;
+            auto issue_s = [&](int n) {
+                const int a = n & 1;
+                const uint32_t aQ = smem_u32(sm + L::OFF_Q + a * (L::KB * SUB));
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t h = ks >> 2, ko = (ks & 3) * 32;
+                    // A = Q rows (K-major, 8-row groups KB KB apart), B = K
+                    tc::mma_bf16(tmem + L::TM_S + a * 128, tc::sdesc_sw128(aQ + h * 1024 + ko, 16, L::KB * 1024),
+                                 tc::sdesc_k128(aK + h * SUB + ko), I_S, ks > 0);
+                }
+                tc::mma_commit(&s_full[a]);
+                tc::mma_commit(&q_empty[a]);
+            };
+            auto issue_o = [&](int m) {
+                const int a = m & 1;
+                const uint32_t aP = smem_u32(sm + L::OFF_P + a * (2 * SUB));
+#pragma unroll
+                for (int ks = 0; ks < kKeys / 16; ++ks) {
+                    // A = P [rows][keys] K-major; B = V [keys][d] read MN-major (atoms of 64 d, 8-key groups)
+                    tc::mma_bf16(tmem + L::TM_O + a * D, tc::sdesc_k128(aP + (ks >> 2) * SUB + (ks & 3) * 32),
+                                 tc::sdesc_sw128(aV + ks * 2048, SUB, 1024), I_O, ks > 0);
+                }
+                tc::mma_commit(&o_full[a]);
+                tc::mma_commit(&p_free[a]);
+            };
+            // The two epilogue warpgroups run chunks n and n+1 at once, so S of
+            // one chunk and O of another are issued in whichever order their
+            // inputs become ready.
+            int ns = 0, no = 0;
+            uint32_t idle = 0;
+            while (ok && no < nch) {
+                bool did = false;
+                if (ns < nch && tc::mbar_try_wait(&q_full[ns & 1], (uint32_t)(ns >> 1) & 1u) &&
+                    (ns < 2 || tc::mbar_try_wait(&s_free[ns & 1], ((uint32_t)(ns >> 1) & 1u) ^ 1u))) {
                     tc::fence_proxy_async();
                     tc::fence_after_sync();
-                    const uint32_t aQ = smem_u32(sm + L::OFF_Q + a * (L::KB * SUB));
-#pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint32_t h = ks >> 2, ko = (ks & 3) * 32;
-                        // A = Q rows (K-major, 8-row groups KB KB apart), B = K
-                        tc::mma_bf16(tmem + L::TM_S + a * 128, tc::sdesc_sw128(aQ + h * 1024 + ko, 16, L::KB * 1024),
-                                     tc::sdesc_k128(aK + h * SUB + ko), I_S, ks > 0);
-                    }
-                    tc::mma_commit(&s_full[a]);
-                    tc::mma_commit(&q_empty[a]);
+                    issue_s(ns);
+                    ++ns;
+                    did = true;
                 }
-                if (n >= 1) {
-                    const int m = n - 1, a = m & 1;
-                    const uint32_t ph = (uint32_t)(m >> 1) & 1u;
-                    if (!tc::mbar_wait(&p_full[a], ph, st, 65, abort_flag)) break;
-                    if (!tc::mbar_wait(&o_free[a], ph ^ 1u, st, 66, abort_flag)) break;
+                if (no < ns && tc::mbar_try_wait(&p_full[no & 1], (uint32_t)(no >> 1) & 1u) &&
+                    (no < 2 || tc::mbar_try_wait(&o_free[no & 1], ((uint32_t)(no >> 1) & 1u) ^ 1u))) {
                     tc::fence_after_sync();
-                    const uint32_t aP = smem_u32(sm + L::OFF_P + a * (2 * SUB));
-#pragma unroll
-                    for (int ks = 0; ks < kKeys / 16; ++ks) {
-                        // A = P [rows][keys] K-major; B = V [keys][d] read MN-major (atoms of 64 d, 8-key groups)
-                        tc::mma_bf16(tmem + L::TM_O + a * D,
-                                     tc::sdesc_k128(aP + (ks >> 2) * SUB + (ks & 3) * 32),
-                                     tc::sdesc_sw128(aV + ks * 2048, SUB, 1024), I_O, ks > 0);
-                    }
-                    tc::mma_commit(&o_full[a]);
-                    tc::mma_commit(&p_free[a]);
-                    issued = n;
+                    issue_o(no);
+                    ++no;
+                    did = true;
+                }
+                if (did) {
+                    idle = 0;
+                } else if (++idle >= tc::kSpinLimit) {
+                    report(st, kDevTimeout, 63, ns * 65536 + no);
+                    *abort_flag = 1;
+                    ok = false;
+                } else if ((idle & 1023u) == 1023u && *abort_flag) {
+                    ok = false;
                 }
             }
-            if (*abort_flag && issued > 0) {
-                const int m = issued - 1;
-                tc::mbar_wait(&o_full[m & 1], (uint32_t)(m >> 1) & 1u, nullptr, 0, nullptr);
-            }
+            // every MMA issued above has completed once `done` fires
+            tc::mma_commit(done);
+            tc::mbar_wait(done, 0, nullptr, 0, nullptr);
         }
     } else {
         // ------------------------------------------------ epilogue: one (query, head) row per thread
-        const int quarter = warp & 3;
+        // warpgroup wg takes chunks wg, wg + 2, ... (TMEM and smem buffers wg)
+        const int quarter = warp & 3, wg = (warp - 2) >> 2;
         const int rho = quarter * 32 + lane;
         const int qq = rho / G, g = rho % G;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
@@ -277,7 +307,7 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         // covers whole 256-byte partial rows.
         auto emit = [&](int m) -> bool {
             const int am = m & 1;
-            if (!tc::mbar_wait(&o_full[am], (uint32_t)(m >> 1) & 1u, st, 74, abort_flag)) return false;
+            if (!wwait(&o_full[am], (uint32_t)(m >> 1) & 1u, st, 74, abort_flag)) return false;
             tc::fence_after_sync();
             const long long prow =
                 pvalid ? (((long long)b * p.Nq + pi) * p.Hq + (long long)r * G + g) * p.topk + pslot : -1;
@@ -319,12 +349,12 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             if (pvalid) stats[prow] = make_float2(pm, pz);
             return true;
         };
-        for (int n = 0; ok && n < nch; ++n) {
+        for (int n = wg; ok && n < nch; n += 2) {
             const int a = n & 1;
             const uint32_t ph = (uint32_t)(n >> 1) & 1u;
             const QueryMeta *meta = reinterpret_cast<const QueryMeta *>(sm + L::OFF_META + a * 2048);
-            if (!tc::mbar_wait(&q_full[a], ph, st, 71, abort_flag)) { ok = false; break; }
-            if (!tc::mbar_wait(&s_full[a], ph, st, 72, abort_flag)) { ok = false; break; }
+            if (!wwait(&q_full[a], ph, st, 71, abort_flag)) { ok = false; break; }
+            if (!wwait(&s_full[a], ph, st, 72, abort_flag)) { ok = false; break; }
             tc::fence_after_sync();
             const bool valid = qq < meta->nq;
             const long long pos = valid ? meta->pos[qq] : -1;
@@ -352,7 +382,10 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                 }
             }
             const float msafe = mx == -INFINITY ? 0.f : mx * sl2;
-            if (!tc::mbar_wait(&p_free[a], ph ^ 1u, st, 73, abort_flag)) { ok = false; break; }
+            // this warpgroup's previous chunk leaves first: its output is staged
+            // through the P tile that this chunk's P is about to overwrite
+            if (n >= 2 && !emit(n - 2)) { ok = false; break; }
+            if (!wwait(&p_free[a], ph ^ 1u, st, 73, abort_flag)) { ok = false; break; }
             // pass 2: P = exp2(s*scale*log2e - m) into the bf16 P tile, z = row sum
             uint8_t *sp = sm + L::OFF_P + a * (2 * SUB);
             float z = 0.f;
@@ -394,14 +427,14 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                 tc::mbar_arrive(&p_full[a]);
                 tc::mbar_arrive(&q_empty[a]);     // this chunk's metadata now lives in registers
             }
-            if (n >= 1 && !emit(n - 1)) { ok = false; break; }
             pm = cm;
             pz = cz;
             pvalid = cvalid;
             pi = ci;
             pslot = cslot;
         }
-        if (ok && nch > 0) emit(nch - 1);
+        const int last = nch - 1 - ((nch - 1 - wg) & 1);      // this warpgroup's last chunk
+        if (ok && last >= 0) emit(last);
     }
 
     tc::fence_before_sync();
