@@ -358,6 +358,9 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             tc::fence_after_sync();
             const bool valid = qq < meta->nq;
             const long long pos = valid ? meta->pos[qq] : -1;
+            const int ci = valid ? meta->i[qq] : 0, cslot = valid ? meta->slot[qq] : 0;
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&q_empty[a]);     // this chunk's metadata now lives in registers
             // last visible key of this block for this row, as an offset into the block
             const int lim = (int)max(-1LL, min(min(pos, (long long)p.Nk - 1) - j0, (long long)kKeys - 1));
             const uint32_t sbase = tmem + lane_base + L::TM_S + a * 128;
@@ -418,14 +421,12 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             }
             const float cm = msafe, cz = z;
             const bool cvalid = valid && mx != -INFINITY;
-            const int ci = valid ? meta->i[qq] : 0, cslot = valid ? meta->slot[qq] : 0;
             tc::fence_before_sync();
             tc::fence_proxy_async();
             __syncwarp();
             if (lane == 0) {
                 tc::mbar_arrive(&s_free[a]);
                 tc::mbar_arrive(&p_full[a]);
-                tc::mbar_arrive(&q_empty[a]);     // this chunk's metadata now lives in registers
             }
             pm = cm;
             pz = cz;
