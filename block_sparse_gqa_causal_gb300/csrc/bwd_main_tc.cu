@@ -322,16 +322,16 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             uint32_t idle = 0;
             while (ok && ng < nch) {
                 bool did = false;
-                if (ns < nch && tc::mbar_try_wait(&full[ns % kStages], (uint32_t)(ns / kStages) & 1u) &&
-                    (ns == 0 || tc::mbar_try_wait(tm_free, (uint32_t)(ns - 1) & 1u))) {
+                if (ns < nch && tc::mbar_test(&full[ns % kStages], (uint32_t)(ns / kStages) & 1u) &&
+                    (ns == 0 || tc::mbar_test(tm_free, (uint32_t)(ns - 1) & 1u))) {
                     tc::fence_proxy_async();
                     tc::fence_after_sync();
                     issue_scores(ns);
                     ++ns;
                     did = true;
                 }
-                if (ng < ns && tc::mbar_try_wait(&p_full[ng % kPBuf], (uint32_t)(ng / kPBuf) & 1u) &&
-                    (ng < 2 || tc::mbar_try_wait(&dq_free[ng & 1], ((uint32_t)(ng >> 1) & 1u) ^ 1u))) {
+                if (ng < ns && tc::mbar_test(&p_full[ng % kPBuf], (uint32_t)(ng / kPBuf) & 1u) &&
+                    (ng < 2 || tc::mbar_test(&dq_free[ng & 1], ((uint32_t)(ng >> 1) & 1u) ^ 1u))) {
                     tc::fence_after_sync();
                     issue_grads(ng);
                     ++ng;

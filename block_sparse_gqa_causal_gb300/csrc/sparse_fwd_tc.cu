@@ -259,16 +259,16 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             uint32_t idle = 0;
             while (ok && no < nch) {
                 bool did = false;
-                if (ns < nch && tc::mbar_try_wait(&q_full[ns & 1], (uint32_t)(ns >> 1) & 1u) &&
-                    (ns < 2 || tc::mbar_try_wait(&s_free[ns & 1], ((uint32_t)(ns >> 1) & 1u) ^ 1u))) {
+                if (ns < nch && tc::mbar_test(&q_full[ns & 1], (uint32_t)(ns >> 1) & 1u) &&
+                    (ns < 2 || tc::mbar_test(&s_free[ns & 1], ((uint32_t)(ns >> 1) & 1u) ^ 1u))) {
                     tc::fence_proxy_async();
                     tc::fence_after_sync();
                     issue_s(ns);
                     ++ns;
                     did = true;
                 }
-                if (no < ns && tc::mbar_try_wait(&p_full[no & 1], (uint32_t)(no >> 1) & 1u) &&
-                    (no < 2 || tc::mbar_try_wait(&o_free[no & 1], ((uint32_t)(no >> 1) & 1u) ^ 1u))) {
+                if (no < ns && tc::mbar_test(&p_full[no & 1], (uint32_t)(no >> 1) & 1u) &&
+                    (no < 2 || tc::mbar_test(&o_free[no & 1], ((uint32_t)(no >> 1) & 1u) ^ 1u))) {
                     tc::fence_after_sync();
                     issue_o(no);
                     ++no;

@@ -42,6 +42,19 @@ MSA_DEV bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// Non-blocking probe (test_wait never suspends the thread): for loops that
+// poll several barriers and act on whichever is ready first.
+MSA_DEV bool mbar_test(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait: gives up after ~2^26 polls (seconds), records a timeout in
 // the status word and returns false.  Callers then skip their remaining
 // work so the kernel ends instead of hanging.
