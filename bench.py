@@ -358,12 +358,26 @@ def main():
         roofline = {"kernel": dom, "bound": None, "achieved": None, "peak": None, "unit": None, "frac": None,
                     "traffic": None, "launch_ms": round(per_launch_ms, 3)}
     elif bound == "tensor":
-        ach = units / (per_launch_ms * 1e-3) / 1e12
-        roofline = {"kernel": dom, "bound": "tensor", "achieved": round(ach, 2), "peak": peaks["bf16_tflops"],
-                    "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4),
-                    "frac_of_sustained": round(ach / peaks["bf16_tflops_sustained"], 4),
-                    "peak_source": peaks["source"] + " burst bf16", "traffic": kernel_traffic(dom, w),
-                    "algorithmic_per_launch": units, "launch_ms": round(per_launch_ms, 3)}
+        # a contraction whose measured DRAM traffic would take longer at the copy
+        # peak than its FLOPs at the tensor peak is bound by HBM: report that roofline
+        traffic = kernel_traffic(dom, w)
+        t_tensor = units / (peaks["bf16_tflops"] * 1e12)
+        t_hbm = traffic / (peaks["hbm_gbs"] * 1e9) if traffic else 0.0
+        ach_t = units / (per_launch_ms * 1e-3) / 1e12
+        tensor_side = {"achieved": round(ach_t, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                       "frac": round(ach_t / peaks["bf16_tflops"], 4),
+                       "frac_of_sustained": round(ach_t / peaks["bf16_tflops_sustained"], 4),
+                       "peak_source": peaks["source"] + " burst bf16", "algorithmic_per_launch": units}
+        if traffic and t_hbm > t_tensor:
+            ach = traffic / (per_launch_ms * 1e-3) / 1e9
+            roofline = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
+                        "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4), "peak_source": peaks["source"] + " copy",
+                        "traffic": traffic, "launch_ms": round(per_launch_ms, 3),
+                        "note": "DRAM traffic at the copy peak outlasts the FLOPs at the bf16 peak",
+                        "tensor": tensor_side}
+        else:
+            roofline = {"kernel": dom, "bound": "tensor", **tensor_side, "traffic": traffic,
+                        "launch_ms": round(per_launch_ms, 3)}
     else:
         ach = units / (per_launch_ms * 1e-3) / 1e9
         roofline = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
