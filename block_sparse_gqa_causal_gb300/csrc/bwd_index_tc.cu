@@ -36,9 +36,10 @@ constexpr int kEpiWarps = 8;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr int SUB = 128 * 128;                 // [128 rows][64 bf16] swizzled sub-tile
 constexpr int OFF_KI = 0;                      // K_idx: 2 feature halves
-constexpr int OFF_STG = OFF_KI + 2 * SUB;      // 2 stages x q_idx [128 queries][128 features]
-constexpr int OFF_SIG = OFF_STG + 4 * SUB;     // 2 buffers x dsig^T [128 keys][128 queries]
-constexpr int OFF_META = OFF_SIG + 4 * SUB;
+constexpr int kStages = 3;                     // q_idx stages
+constexpr int OFF_STG = OFF_KI + 2 * SUB;      // kStages x q_idx [128 queries][128 features]
+constexpr int OFF_SIG = OFF_STG + kStages * 2 * SUB;   // dsig^T [128 keys][128 queries]
+constexpr int OFF_META = OFF_SIG + 2 * SUB;
 
 struct Meta {
     float lsei2[kQ];        // lse_idx * log2(e) (+inf for padding)
@@ -49,7 +50,7 @@ struct Meta {
     int nq;
 };
 constexpr int META_BYTES = (int)((sizeof(Meta) + 127) & ~size_t(127));
-constexpr int OFF_STAGE = OFF_META + 2 * META_BYTES;   // per epilogue warp: dq_idx [64 rows][32 features] bf16
+constexpr int OFF_STAGE = OFF_META + kStages * META_BYTES;   // per epilogue warp: dq_idx [64 rows][32 features] bf16
 constexpr int STAGE_BYTES = 64 * 64;
 constexpr int OFF_BAR = OFF_STAGE + kEpiWarps * STAGE_BYTES;
 constexpr int ALLOC = OFF_BAR + 256 + 1024;
@@ -74,6 +75,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, const bf16 *__restrict__ q_idx,
                     const float *__restrict__ lse_idx, float coef, const int32_t *__restrict__ bucket_off,
                     const int32_t *__restrict__ bucket_q, const __half *__restrict__ pt,
+                    const int32_t *__restrict__ pt_off,
                     bf16 *__restrict__ dqi_part, float *__restrict__ dki_acc, DeviceStatus *st)
 {
     const int r = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
@@ -88,22 +90,24 @@ bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, cons
     // stays a shared-memory access (no generic addressing)
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
-    uint64_t *full = bars, *empty = bars + 2, *s_full = bars + 4, *s_free = bars + 6;
-    uint64_t *g_full = bars + 8, *g_free = bars + 10;
+    uint64_t *full = bars, *empty = bars + 3, *s_full = bars + 6, *s_free = bars + 8;
+    uint64_t *g_full = bars + 10, *g_free = bars + 11;
     uint64_t *dq_full = bars + 12, *dq_free = bars + 13, *kv_full = bars + 14, *done = bars + 15;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int a = 0; a < 2; ++a) {
+        for (int a = 0; a < kStages; ++a) {
             tc::mbar_init(&full[a], 64);               // 32 cp.async arrivals + 32 row-data arrivals
             tc::mbar_init(&empty[a], 1 + kEpiWarps);
+        }
+        for (int a = 0; a < 2; ++a) {
             tc::mbar_init(&s_full[a], 1);
             tc::mbar_init(&s_free[a], kEpiWarps);
-            tc::mbar_init(&g_full[a], kEpiWarps);
-            tc::mbar_init(&g_free[a], 1);
         }
+        tc::mbar_init(g_full, kEpiWarps);
+        tc::mbar_init(g_free, 1);
         tc::mbar_init(dq_full, 1);
         tc::mbar_init(dq_free, kEpiWarps);
         tc::mbar_init(kv_full, 1);
@@ -127,30 +131,36 @@ bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, cons
 #pragma unroll
             for (int h = 0; h < 2; ++h) tc::tma_load_3d(sm + OFF_KI + h * SUB, &tmap_ki, kv_full, h * 64, (int)j0, b);
         }
-        int ent[4], ent_next[4];
+        // entries two chunks ahead, lse_idx one chunk ahead; lane l gathers whole
+        // q_idx rows l, l+32, l+64, l+96 of a chunk (its own entries)
+        auto load_ent = [&](int (&e)[4], int q0, int nqx) {
 #pragma unroll
-        for (int t = 0; t < 4; ++t) ent[t] = lane + 32 * t < qend - qbeg ? __ldg(bucket_q + qbeg + lane + 32 * t) : 0;
+            for (int t = 0; t < 4; ++t) e[t] = lane + 32 * t < nqx ? __ldg(bucket_q + q0 + lane + 32 * t) : 0;
+        };
+        auto load_lse = [&](float (&vl)[4], const int (&e)[4], int nqx) {
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+                vl[t] = lane + 32 * t < nqx ? __ldg(lse_idx + ((long long)b * p.Hkv + r) * p.Nq + entry_row(e[t])) : INFINITY;
+        };
+        int ent[4], ent1[4], ent2[4];
+        float vl[4], vl_next[4];
+        load_ent(ent, qbeg, qend - qbeg);
+        load_ent(ent1, qbeg + kQ, qend - qbeg - kQ);
+        load_lse(vl, ent, qend - qbeg);
         for (int m = 0; m < nch; ++m) {
-            const int s = m & 1;
+            const int s = m % kStages;
             const int q0 = qbeg + m * kQ;
             const int nq = min(kQ, qend - q0);
-            float vl[4];
-#pragma unroll
-            for (int t = 0; t < 4; ++t)
-                vl[t] = lane + 32 * t < nq
-                            ? __ldg(lse_idx + ((long long)b * p.Hkv + r) * p.Nq + entry_row(ent[t])) * kLog2e
-                            : INFINITY;
-#pragma unroll
-            for (int t = 0; t < 4; ++t)
-                ent_next[t] = lane + 32 * t < qend - q0 - kQ ? __ldg(bucket_q + q0 + kQ + lane + 32 * t) : 0;
-            if (!tc::mbar_wait(&empty[s], ((uint32_t)(m >> 1) & 1u) ^ 1u, st, 121, abort_flag)) break;
+            load_ent(ent2, q0 + 2 * kQ, qend - q0 - 2 * kQ);
+            if (m + 1 < nch) load_lse(vl_next, ent1, qend - q0 - kQ);
+            if (!tc::mbar_wait(&empty[s], ((uint32_t)(m / kStages) & 1u) ^ 1u, st, 121, abort_flag)) break;
             Meta *meta = reinterpret_cast<Meta *>(sm + OFF_META + s * META_BYTES);
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
                 const int qq = lane + 32 * t;
                 const bool ok = qq < nq;
                 const int i = ok ? entry_row(ent[t]) : 0;
-                meta->lsei2[qq] = vl[t];
+                meta->lsei2[qq] = vl[t] * kLog2e;
                 meta->qi[qq] = i;
                 meta->pos[qq] = ok ? p.q_offset + i : -1;
                 meta->slot[qq] = ok ? entry_slot(ent[t]) : 0;
@@ -159,20 +169,23 @@ bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, cons
                 meta->e0 = q0;
                 meta->nq = nq;
             }
-            // q_idx rows: lane covers 16-byte chunk lane%16 of rows 2*it + lane/16;
-            // a row's entry is held by lane row%32 in ent[row/32]
             uint8_t *sq = sm + OFF_STG + s * (2 * SUB);
 #pragma unroll
-            for (int it = 0; it < kQ / 2; ++it) {
-                const int row = it * 2 + (lane >> 4), ch = lane & 15;
-                const int e = __shfl_sync(0xffffffffu, ent[it >> 4], row & 31);
-                cp_async16_zfill(sq + (ch >> 3) * SUB + swz(row, ch & 7),
-                                 q_idx + (((long long)b * p.Nq + entry_row(e)) * p.Hkv + r) * DI + ch * 8, row < nq);
+            for (int t = 0; t < 4; ++t) {
+                const int row = lane + 32 * t;
+                const bf16 *src = q_idx + (((long long)b * p.Nq + entry_row(ent[t])) * p.Hkv + r) * DI;
+#pragma unroll
+                for (int ch = 0; ch < DI / 8; ++ch)
+                    cp_async16_zfill(sq + (ch >> 3) * SUB + swz(row, ch & 7), src + ch * 8, row < nq);
             }
             cp_async_arrive_noinc(&full[s]);
             tc::mbar_arrive(&full[s]);
 #pragma unroll
-            for (int t = 0; t < 4; ++t) ent[t] = ent_next[t];
+            for (int t = 0; t < 4; ++t) {
+                ent[t] = ent1[t];
+                ent1[t] = ent2[t];
+                vl[t] = vl_next[t];
+            }
         }
         cp_async_wait<0>();
     } else if (warp == 1) {
@@ -183,7 +196,7 @@ bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, cons
             constexpr uint32_t I_DQI = tc::idesc_bf16(128, kQ) | tc::kAMajorMN | tc::kBMajorMN;
             const uint32_t aKI = smem_u32(sm + OFF_KI);
             auto issue_s = [&](int n) {
-                const uint32_t sq = smem_u32(sm + OFF_STG + (n & 1) * (2 * SUB));
+                const uint32_t sq = smem_u32(sm + OFF_STG + (n % kStages) * (2 * SUB));
 #pragma unroll
                 for (int ks = 0; ks < DI / 16; ++ks) {
                     const uint32_t off = (ks >> 2) * SUB + (ks & 3) * 32;
@@ -193,9 +206,8 @@ bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, cons
                 tc::mma_commit(&s_full[n & 1]);
             };
             auto issue_g = [&](int n) {
-                const int pb = n & 1;
-                const uint32_t sq = smem_u32(sm + OFF_STG + (n & 1) * (2 * SUB));
-                const uint32_t sg = smem_u32(sm + OFF_SIG + pb * (2 * SUB));
+                const uint32_t sq = smem_u32(sm + OFF_STG + (n % kStages) * (2 * SUB));
+                const uint32_t sg = smem_u32(sm + OFF_SIG);
                 // dq_idx^T = K_idx^T dsig^T: both operands read MN-major; K = 128 keys
 #pragma unroll
                 for (int ks = 0; ks < kKeys / 16; ++ks)
@@ -207,8 +219,8 @@ bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, cons
                 for (int ks = 0; ks < kQ / 16; ++ks)
                     tc::mma_bf16(tmem + TM_DKI, tc::sdesc_k128(sg + (ks >> 2) * SUB + (ks & 3) * 32),
                                  tc::sdesc_sw128(sq + ks * 2048, SUB, 1024), I_DKI, n > 0 || ks > 0);
-                tc::mma_commit(&empty[n & 1]);
-                tc::mma_commit(&g_free[pb]);
+                tc::mma_commit(&empty[n % kStages]);
+                tc::mma_commit(g_free);
             };
             bool ok = tc::mbar_wait(kv_full, 0, st, 122, abort_flag);
             if (ok) {
@@ -222,14 +234,14 @@ bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, cons
             for (int n = 0; ok && n < nch; ++n) {
                 if (n + 1 < nch) {
                     const int m = n + 1;
-                    if (!tc::mbar_wait(&full[m & 1], (uint32_t)(m >> 1) & 1u, st, 124, abort_flag)) break;
+                    if (!tc::mbar_wait(&full[m % kStages], (uint32_t)(m / kStages) & 1u, st, 124, abort_flag)) break;
                     if (m >= 2 && !tc::mbar_wait(&s_free[m & 1], ((uint32_t)(m >> 1) & 1u) ^ 1u, st, 125, abort_flag))
                         break;
                     tc::fence_proxy_async();
                     tc::fence_after_sync();
                     issue_s(m);
                 }
-                if (!tc::mbar_wait(&g_full[n & 1], (uint32_t)(n >> 1) & 1u, st, 126, abort_flag)) break;
+                if (!tc::mbar_wait(g_full, (uint32_t)n & 1u, st, 126, abort_flag)) break;
                 if (n >= 1 && !tc::mbar_wait(dq_free, (uint32_t)(n - 1) & 1u, st, 127, abort_flag)) break;
                 tc::fence_after_sync();
                 issue_g(n);
@@ -281,22 +293,25 @@ bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, cons
             return true;
         };
         for (int n = 0; ok && n < nch; ++n) {
-            const int s = n & 1, pb = n & 1;
+            const int s = n % kStages, sb = n & 1;
             const Meta *meta = reinterpret_cast<const Meta *>(sm + OFF_META + s * META_BYTES);
-            if (!wwait(&full[s], (uint32_t)(n >> 1) & 1u, st, 132, abort_flag)) { ok = false; break; }
-            const int nq = meta->nq, e0 = meta->e0;
+            if (!wwait(&full[s], (uint32_t)(n / kStages) & 1u, st, 132, abort_flag)) { ok = false; break; }
+            const int nq = meta->nq;
             // teacher values of this key for the warp's 64 queries
-            float ptv[64];
+            // chunk n is block n of the bucket's key-major teacher layout: this key's
+            // 64 values are contiguous (padding entries beyond nq are masked below)
+            uint4 tv[8];
+            {
+                const uint4 *src = reinterpret_cast<const uint4 *>(
+                    pt + ((long long)pt_off[bucket] + (long long)n * 128) * kKeys + kr * 128 + cb);
 #pragma unroll
-            for (int cc = 0; cc < 64; ++cc) {
-                const int u = cb + cc;
-                ptv[cc] = u < nq ? __half2float(pt[(long long)(e0 + u) * kKeys + kr]) : 0.f;
+                for (int x = 0; x < 8; ++x) tv[x] = __ldg(src + x);
             }
-            if (!wwait(&s_full[s], (uint32_t)(n >> 1) & 1u, st, 133, abort_flag)) { ok = false; break; }
+            if (!wwait(&s_full[sb], (uint32_t)(n >> 1) & 1u, st, 133, abort_flag)) { ok = false; break; }
             tc::fence_after_sync();
             uint32_t s0[32], s1[32];
-            tc::tmem_ld32_nowait(tmem + lane_base + TM_S + s * kQ + cb, s0);
-            tc::tmem_ld32_nowait(tmem + lane_base + TM_S + s * kQ + cb + 32, s1);
+            tc::tmem_ld32_nowait(tmem + lane_base + TM_S + sb * kQ + cb, s0);
+            tc::tmem_ld32_nowait(tmem + lane_base + TM_S + sb * kQ + cb + 32, s1);
             long long rp_cur[2];
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
@@ -307,7 +322,7 @@ bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, cons
             tc::tmem_wait32(s1);
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&s_free[s]);
+            if (lane == 0) tc::mbar_arrive(&s_free[sb]);
             uint32_t sg[32];
 #pragma unroll
             for (int cc = 0; cc < 64; cc += 4) {
@@ -321,22 +336,25 @@ bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, cons
                     const int col = cc + e;
                     const float sv = __uint_as_float(col < 32 ? s0[col] : s1[col - 32]);
                     const bool vis = key_ok && j <= (long long)ps[e];
-                    g2[e] = vis ? coef * (tc::ex2(sv * si2 - l2[e]) - ptv[col]) : 0.f;
+                    const __half2 h2 = *reinterpret_cast<const __half2 *>(
+                        reinterpret_cast<const uint32_t *>(&tv[col >> 3]) + ((col & 7) >> 1));
+                    const float ptv = (col & 1) ? __high2float(h2) : __low2float(h2);
+                    g2[e] = vis ? coef * (tc::ex2(sv * si2 - l2[e]) - ptv) : 0.f;
                 }
                 sg[cc / 2] = pack_bf16(g2[0], g2[1]);
                 sg[cc / 2 + 1] = pack_bf16(g2[2], g2[3]);
             }
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&empty[s]);   // the stage's row data is no longer read
-            if (n >= 2 && !wwait(&g_free[pb], ((uint32_t)(n >> 1) & 1u) ^ 1u, st, 134, abort_flag)) { ok = false; break; }
-            uint8_t *dst = sm + OFF_SIG + pb * (2 * SUB) + hf * SUB;   // query half hf = sub-tile hf
+            if (n >= 1 && !wwait(g_free, (uint32_t)(n - 1) & 1u, st, 134, abort_flag)) { ok = false; break; }
+            uint8_t *dst = sm + OFF_SIG + hf * SUB;                   // query half hf = sub-tile hf
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch)
                 *reinterpret_cast<uint4 *>(dst + swz(kr, ch)) =
                     make_uint4(sg[ch * 4], sg[ch * 4 + 1], sg[ch * 4 + 2], sg[ch * 4 + 3]);
             tc::fence_proxy_async();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&g_full[pb]);
+            if (lane == 0) tc::mbar_arrive(g_full);
             if (n >= 1 && !drain(n - 1)) { ok = false; break; }
             rp_prev[0] = rp_cur[0];
             rp_prev[1] = rp_cur[1];
@@ -344,7 +362,7 @@ bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, cons
         if (ok) ok = drain(nch - 1);
         if (ok) {
             const int m = nch - 1;
-            ok = wwait(&g_free[m & 1], (uint32_t)(m >> 1) & 1u, st, 135, abort_flag);
+            ok = wwait(g_free, (uint32_t)m & 1u, st, 135, abort_flag);
             tc::fence_after_sync();
         }
         if (ok) {
@@ -389,7 +407,7 @@ cudaError_t launch_bwd_index_tc(const Problem &p, const bf16 *q_idx, const bf16 
     {
         TimedLaunch timed_("bwd_index_tc_kernel", s);
         bwd_index_tc_kernel<<<dim3(p.Hkv, p.nb, p.B), kThreads, ALLOC, s>>>(tki, p, q_idx, lse_idx, coef, w.bucket_off,
-                                                                           w.bucket_q, w.pt, w.dqi_part, w.dki_acc, st);
+                                                                           w.bucket_q, w.pt, w.pt_off, w.dqi_part, w.dki_acc, st);
     }
     note_launch();
     return cudaGetLastError();

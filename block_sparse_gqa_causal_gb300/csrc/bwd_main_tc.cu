@@ -107,7 +107,8 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                    const bf16 *__restrict__ q, const bf16 *__restrict__ d_o, const float *__restrict__ lse,
                    const float *__restrict__ Dg, const int32_t *__restrict__ bucket_off,
                    const int32_t *__restrict__ bucket_q, bf16 *__restrict__ dk, bf16 *__restrict__ dv,
-                   bf16 *__restrict__ dq_part, __half *__restrict__ pt_out, DeviceStatus *st)
+                   bf16 *__restrict__ dq_part, __half *__restrict__ pt_out, const int32_t *__restrict__ pt_off,
+                   DeviceStatus *st)
 {
     constexpr int QC = kRows / G;                 // queries per chunk
     constexpr int EPL = (QC + 31) / 32;           // bucket entries per producer lane
@@ -449,10 +450,25 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 pk[cc / 2] = pack_bf16(pr[0], pr[1]);
                 dk2[cc / 2] = pack_bf16(ds[0], ds[1]);
             }
+            {
+                // this key's teacher for the warp's NQH queries: consecutive entries
+                // of one 128-entry block (chunks start at multiples of QC), one store
+                const int t = e0 - qbeg + cb / G;
+                __half *dst = pt_out + ((long long)pt_off[bucket] + (t & ~127)) * kKeys + kr * 128 + (t & 127);
+                uint32_t hv[NQH / 2];
 #pragma unroll
-            for (int u = 0; u < NQH; ++u) {
-                const int qq = cb / G + u;
-                if (qq < nq) pt_out[(long long)(e0 + qq) * kKeys + kr] = __float2half_rn(ptq[u] * invG);
+                for (int u = 0; u < NQH; u += 2) {
+                    const __half2 h2 = __floats2half2_rn(cb / G + u < nq ? ptq[u] * invG : 0.f,
+                                                         cb / G + u + 1 < nq ? ptq[u + 1] * invG : 0.f);
+                    hv[u / 2] = *reinterpret_cast<const uint32_t *>(&h2);
+                }
+                if constexpr (NQH == 4) {
+                    *reinterpret_cast<uint2 *>(dst) = make_uint2(hv[0], hv[1]);
+                } else {
+#pragma unroll
+                    for (int x = 0; x < NQH / 8; ++x)
+                        reinterpret_cast<uint4 *>(dst)[x] = make_uint4(hv[4 * x], hv[4 * x + 1], hv[4 * x + 2], hv[4 * x + 3]);
+                }
             }
             if (n >= kPBuf && !wwait(&p_free[pb], (uint32_t)((n - kPBuf) / kPBuf) & 1u, st, 114, abort_flag)) {
                 ok = false;
@@ -550,7 +566,7 @@ cudaError_t launch_g(const Problem &p, const bf16 *q, const bf16 *k, const bf16 
     {
         TimedLaunch timed_("bwd_main_tc_kernel", s);
         bwd_main_tc_kernel<G><<<dim3(p.Hkv, p.nb, p.B), kThreads, ALLOC, s>>>(
-            tq, tdo, tk, tv, p, q, d_o, lse, w.D, w.bucket_off, w.bucket_q, dk, dv, w.dq_part, w.pt, st);
+            tq, tdo, tk, tv, p, q, d_o, lse, w.D, w.bucket_off, w.bucket_q, dk, dv, w.dq_part, w.pt, w.pt_off, st);
     }
     note_launch();
     return cudaGetLastError();

@@ -97,6 +97,32 @@ __global__ void __launch_bounds__(256) bwd_rowdot_kernel(Problem p, const bf16 *
     }
 }
 
+// pt_off[x] = sum over buckets y < x of cnt[y] rounded up to 128 (x = 0..n),
+// single CTA of 1024 threads
+__global__ void __launch_bounds__(1024) bwd_pad_scan_kernel(const int32_t *__restrict__ cnt,
+                                                            int32_t *__restrict__ off, int n)
+{
+    __shared__ int part[1024];
+    const int per = (n + 1023) / 1024;
+    const int lo = threadIdx.x * per, hi = min(n, lo + per);
+    int s = 0;
+    for (int x = lo; x < hi; ++x) s += (cnt[x] + 127) & ~127;
+    part[threadIdx.x] = s;
+    __syncthreads();
+    for (int d = 1; d < 1024; d <<= 1) {
+        const int v = threadIdx.x >= (unsigned)d ? part[threadIdx.x - d] : 0;
+        __syncthreads();
+        part[threadIdx.x] += v;
+        __syncthreads();
+    }
+    int run = threadIdx.x ? part[threadIdx.x - 1] : 0;
+    for (int x = lo; x < hi; ++x) {
+        off[x] = run;
+        run += (cnt[x] + 127) & ~127;
+    }
+    if (threadIdx.x == 1023) off[n] = part[1023];
+}
+
 __global__ void f32_to_bf16_kernel(const float *__restrict__ src, bf16 *__restrict__ dst, long long n)
 {
     for (long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x; x < n / 2; x += (long long)gridDim.x * blockDim.x) {
@@ -582,6 +608,11 @@ cudaError_t launch_fused_bwd(const Problem &p, const bf16 *q, const bf16 *k, con
         return e;
 
     if (tc) {
+        {
+            TimedLaunch timed_("bwd_pad_scan_kernel", s);
+            bwd_pad_scan_kernel<<<1, 1024, 0, s>>>(w.bucket_cnt, w.pt_off, (int)((long long)p.B * p.Hkv * p.nb));
+        }
+        note_launch();
         // main branch first: it leaves the teacher per (bucket entry, key) for the index branch
         if ((e = launch_bwd_main_tc(p, q, k, v, d_o, lse, w, dk, dv, st, s)) != cudaSuccess) return e;
         if ((e = launch_bwd_index_tc(p, q_idx, k_idx, lse_idx, kl_coef, w, st, s)) != cudaSuccess) return e;

@@ -418,15 +418,15 @@ kl_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, const
                 meta->e0 = q0;
                 meta->nq = nq;
             }
-            // q_idx rows: a row's entry is held by lane row%32 in ent[row/32]
+            // q_idx rows: lane l gathers whole rows l, l+32, l+64, l+96 (its own entries)
             uint8_t *sq = sm + L::OFF_Q + s * (L::H * SUB);
-            constexpr int CPR = DI / 8, RPI = 32 / CPR;
 #pragma unroll
-            for (int it = 0; it < kQ / RPI; ++it) {
-                const int row = it * RPI + lane / CPR, ch = lane % CPR;
-                const int e = __shfl_sync(0xffffffffu, ent[(it * RPI) >> 5], row & 31);
-                cp_async16_zfill(sq + (ch >> 3) * SUB + swz(row, ch & 7),
-                                 q_idx + (((long long)b * p.Nq + entry_row(e)) * p.Hkv + r) * DI + ch * 8, row < nq);
+            for (int t = 0; t < 4; ++t) {
+                const int row = lane + 32 * t;
+                const bf16 *src = q_idx + (((long long)b * p.Nq + entry_row(ent[t])) * p.Hkv + r) * DI;
+#pragma unroll
+                for (int ch = 0; ch < DI / 8; ++ch)
+                    cp_async16_zfill(sq + (ch >> 3) * SUB + swz(row, ch & 7), src + ch * 8, row < nq);
             }
             cp_async_arrive_noinc(&full[s]);
             tc::mbar_arrive(&full[s]);
