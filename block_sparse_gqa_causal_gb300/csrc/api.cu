@@ -142,7 +142,7 @@ size_t bwd_bytes(const Problem &p)
     const size_t slots = (size_t)p.B * p.Nq * p.topk;
     if (bwd_tc(p))
         n += align256(slots * p.Hq * p.d * 2) + align256(slots * p.Hkv * p.d_idx * 2) +
-             align256((slots * p.Hkv + (size_t)128 * p.B * p.Hkv * p.nb) * 128 * 2) +
+             align256((slots * p.Hkv + (size_t)8 * p.B * p.Hkv * p.nb) * 128 * 2) +
              align256(((size_t)p.B * p.Hkv * p.nb + 1) * 4);
     else
         n += align256((size_t)p.B * p.Nq * p.Hq * p.d * 4) + align256((size_t)p.B * p.Nq * p.Hkv * p.d_idx * 4);
@@ -395,7 +395,7 @@ msa_status msa_fused_bwd(const msa_shape *shape, const void *q, const void *k, c
     if (bwd_tc(p)) {
         w.dq_part = cv.take<bf16>(slots * p.Hq * p.d);
         w.dqi_part = cv.take<bf16>(slots * p.Hkv * p.d_idx);
-        w.pt = cv.take<__half>((slots * p.Hkv + (size_t)128 * p.B * p.Hkv * p.nb) * 128);
+        w.pt = cv.take<__half>((slots * p.Hkv + (size_t)8 * p.B * p.Hkv * p.nb) * 128);
         w.pt_off = cv.take<int32_t>((size_t)p.B * p.Hkv * p.nb + 1);
     } else {
         w.dq_acc = cv.take<float>((size_t)p.B * p.Nq * p.Hq * p.d);

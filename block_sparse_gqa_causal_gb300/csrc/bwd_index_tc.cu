@@ -298,14 +298,13 @@ bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, cons
             if (!wwait(&full[s], (uint32_t)(n / kStages) & 1u, st, 132, abort_flag)) { ok = false; break; }
             const int nq = meta->nq;
             // teacher values of this key for the warp's 64 queries
-            // chunk n is block n of the bucket's key-major teacher layout: this key's
-            // 64 values are contiguous (padding entries beyond nq are masked below)
+            // the teacher of this key for entries 128n + cb .. + 63: eight 8-entry
+            // groups, 16 bytes each (padding entries beyond nq are masked below)
             uint4 tv[8];
             {
-                const uint4 *src = reinterpret_cast<const uint4 *>(
-                    pt + ((long long)pt_off[bucket] + (long long)n * 128) * kKeys + kr * 128 + cb);
+                const __half *src = pt + ((long long)pt_off[bucket] + (long long)n * 128 + cb) * kKeys + kr * 8;
 #pragma unroll
-                for (int x = 0; x < 8; ++x) tv[x] = __ldg(src + x);
+                for (int x = 0; x < 8; ++x) tv[x] = __ldg(reinterpret_cast<const uint4 *>(src + (long long)x * 8 * kKeys));
             }
             if (!wwait(&s_full[sb], (uint32_t)(n >> 1) & 1u, st, 133, abort_flag)) { ok = false; break; }
             tc::fence_after_sync();

@@ -451,10 +451,10 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 dk2[cc / 2] = pack_bf16(ds[0], ds[1]);
             }
             {
-                // this key's teacher for the warp's NQH queries: consecutive entries
-                // of one 128-entry block (chunks start at multiples of QC), one store
+                // this key's teacher for the warp's NQH queries (consecutive entries,
+                // 4-aligned): 8 bytes into one 8-entry group, or 16 bytes per group
                 const int t = e0 - qbeg + cb / G;
-                __half *dst = pt_out + ((long long)pt_off[bucket] + (t & ~127)) * kKeys + kr * 128 + (t & 127);
+                __half *dst = pt_out + ((long long)pt_off[bucket] + (t & ~7)) * kKeys + kr * 8 + (t & 7);
                 uint32_t hv[NQH / 2];
 #pragma unroll
                 for (int u = 0; u < NQH; u += 2) {
@@ -462,12 +462,16 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                                                          cb / G + u + 1 < nq ? ptq[u + 1] * invG : 0.f);
                     hv[u / 2] = *reinterpret_cast<const uint32_t *>(&h2);
                 }
+                // only groups holding a valid entry: the rest may lie past this
+                // bucket's region (its count is rounded up to 8 entries only)
                 if constexpr (NQH == 4) {
-                    *reinterpret_cast<uint2 *>(dst) = make_uint2(hv[0], hv[1]);
+                    if (cb / G < nq) *reinterpret_cast<uint2 *>(dst) = make_uint2(hv[0], hv[1]);
                 } else {
 #pragma unroll
                     for (int x = 0; x < NQH / 8; ++x)
-                        reinterpret_cast<uint4 *>(dst)[x] = make_uint4(hv[4 * x], hv[4 * x + 1], hv[4 * x + 2], hv[4 * x + 3]);
+                        if (cb / G + 8 * x < nq)
+                            *reinterpret_cast<uint4 *>(dst + (long long)x * 8 * kKeys) =
+                                make_uint4(hv[4 * x], hv[4 * x + 1], hv[4 * x + 2], hv[4 * x + 3]);
                 }
             }
             if (n >= kPBuf && !wwait(&p_free[pb], (uint32_t)((n - kPBuf) / kPBuf) & 1u, st, 114, abort_flag)) {

@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(256) bwd_rowdot_kernel(Problem p, const bf16 *
     }
 }
 
-// pt_off[x] = sum over buckets y < x of cnt[y] rounded up to 128 (x = 0..n),
+// pt_off[x] = sum over buckets y < x of cnt[y] rounded up to 8 (x = 0..n),
 // single CTA of 1024 threads
 __global__ void __launch_bounds__(1024) bwd_pad_scan_kernel(const int32_t *__restrict__ cnt,
                                                             int32_t *__restrict__ off, int n)
@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(1024) bwd_pad_scan_kernel(const int32_t *__res
     const int per = (n + 1023) / 1024;
     const int lo = threadIdx.x * per, hi = min(n, lo + per);
     int s = 0;
-    for (int x = lo; x < hi; ++x) s += (cnt[x] + 127) & ~127;
+    for (int x = lo; x < hi; ++x) s += (cnt[x] + 7) & ~7;
     part[threadIdx.x] = s;
     __syncthreads();
     for (int d = 1; d < 1024; d <<= 1) {
@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(1024) bwd_pad_scan_kernel(const int32_t *__res
     int run = threadIdx.x ? part[threadIdx.x - 1] : 0;
     for (int x = lo; x < hi; ++x) {
         off[x] = run;
-        run += (cnt[x] + 127) & ~127;
+        run += (cnt[x] + 7) & ~7;
     }
     if (threadIdx.x == 1023) off[n] = part[1023];
 }

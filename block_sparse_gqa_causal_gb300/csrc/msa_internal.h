@@ -90,9 +90,9 @@ struct BwdWork {
     float *dki_acc;      // [B, Nk, d_idx]
     bf16 *dq_part;       // [B, Nq, Hq, topk, d]      dQ per selected block (tcgen05 path)
     bf16 *dqi_part;      // [B, Nq, Hkv, topk, d_idx] dq_idx per selected block (tcgen05 path)
-    // teacher per (bucket entry, key), key-major within blocks of 128 entries of a
-    // bucket: entry t of bucket x at [(pt_off[x] + (t & ~127)) * 128 + key * 128 + (t & 127)]
-    // (tcgen05 path); pt_off[x] = sum over earlier buckets of their counts rounded up to 128
+    // teacher per (bucket entry, key), key-major within groups of 8 entries of a
+    // bucket: entry t of bucket x at [(pt_off[x] + (t & ~7)) * 128 + key * 8 + (t & 7)]
+    // (tcgen05 path); pt_off[x] = sum over earlier buckets of their counts rounded up to 8
     __half *pt;
     int32_t *pt_off;     // [B*Hkv*nb + 1]
     int32_t *bucket_cnt; // [B*Hkv*nb]
