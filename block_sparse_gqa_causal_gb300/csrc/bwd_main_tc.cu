@@ -36,7 +36,8 @@ constexpr int D = 128;
 constexpr int kKeys = 128;
 constexpr int kRows = 64;                       // (query, head) rows per chunk
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kGradWarp = 2 + kEpiWarps;         // the second MMA issuer (gradients)
+constexpr int kThreads = 32 * (3 + kEpiWarps);
 constexpr int SUBK = kKeys * 128;               // [128 keys][64 bf16] swizzled sub-tile
 // A [64 rows][128 d] tile is stored as 8-row groups of {d 0..63, d 64..127}
 // (1024-byte swizzle atoms): row rho, half h at (rho/8)*2048 + h*1024 + (rho%8)*128.
@@ -149,7 +150,7 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         tc::mbar_init(kv_full, 1);
         tc::mbar_init(s_full, 1);
         tc::mbar_init(tm_free, kEpiWarps);
-        tc::mbar_init(done, 1);
+        tc::mbar_init(done, 2);                        // both MMA issuers
         *abort_flag = 0;
         tc::fence_mbar_init();
     }
@@ -271,8 +272,6 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
             constexpr uint32_t I_S = tc::idesc_bf16(128, kRows);
-            constexpr uint32_t I_DKV = tc::idesc_bf16(128, 128) | tc::kBMajorMN;
-            constexpr uint32_t I_DQ = tc::idesc_bf16(128, kRows) | tc::kAMajorMN | tc::kBMajorMN;
             const uint32_t aK = smem_u32(sm + OFF_K), aV = smem_u32(sm + OFF_V);
             auto issue_scores = [&](int n) {
                 const uint32_t sq = smem_u32(sm + OFF_STG + (n % kStages) * STG_BYTES), sdo = sq + TILE_R;
@@ -287,6 +286,29 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 }
                 tc::mma_commit(s_full);
             };
+            // Scores here, gradients on warp kGradWarp: the two streams touch
+            // disjoint TMEM and shared memory, are ordered only through the
+            // mbarriers, and issuing them from two threads overlaps their issue.
+            bool ok = tc::mbar_wait(kv_full, 0, st, 102, abort_flag);
+            if (ok) tc::fence_proxy_async();
+            for (int ns = 0; ok && ns < nch; ++ns) {
+                if (!tc::mbar_wait(&full[ns % kStages], (uint32_t)(ns / kStages) & 1u, st, 103, abort_flag)) break;
+                if (ns > 0 && !tc::mbar_wait(tm_free, (uint32_t)(ns - 1) & 1u, st, 104, abort_flag)) break;
+                tc::fence_proxy_async();
+                tc::fence_after_sync();
+                issue_scores(ns);
+            }
+            // every MMA this thread issued has completed once `done` fires (it also
+            // waits for the gradient issuer's commit)
+            tc::mma_commit(done);
+            tc::mbar_wait(done, 0, nullptr, 0, nullptr);
+        }
+    } else if (warp == kGradWarp) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer: gradients
+            constexpr uint32_t I_DKV = tc::idesc_bf16(128, 128) | tc::kBMajorMN;
+            constexpr uint32_t I_DQ = tc::idesc_bf16(128, kRows) | tc::kAMajorMN | tc::kBMajorMN;
+            const uint32_t aK = smem_u32(sm + OFF_K);
             auto issue_grads = [&](int n) {
                 const int pb = n % kPBuf, qb = n & 1;
                 const uint32_t sq = smem_u32(sm + OFF_STG + (n % kStages) * STG_BYTES), sdo = sq + TILE_R;
@@ -311,48 +333,17 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 tc::mma_commit(&empty[n % kStages]);
                 tc::mma_commit(&p_free[pb]);
             };
-            bool ok = tc::mbar_wait(kv_full, 0, st, 102, abort_flag);
-            if (ok) tc::fence_proxy_async();
-            // Issue in whichever order the inputs become ready: the scores of the
-            // next chunk need its Q/dO stage and the epilogue's release of S/dP;
-            // the gradients of chunk n need its P/dS tiles (and, for the dQ^T
-            // buffer, the drain of chunk n-2).  Waiting for one while the other
-            // is ready would leave the tensor pipe idle: the next stage is only
-            // loaded once the gradients that read the older one have completed.
-            int ns = 0, ng = 0;            // next chunk to issue scores / gradients for
-            uint32_t idle = 0;
-            while (ok && ng < nch) {
-                bool did = false;
-                if (ns < nch && tc::mbar_test(&full[ns % kStages], (uint32_t)(ns / kStages) & 1u) &&
-                    (ns == 0 || tc::mbar_test(tm_free, (uint32_t)(ns - 1) & 1u))) {
-                    tc::fence_proxy_async();
-                    tc::fence_after_sync();
-                    issue_scores(ns);
-                    ++ns;
-                    did = true;
-                }
-                if (ng < ns && tc::mbar_test(&p_full[ng % kPBuf], (uint32_t)(ng / kPBuf) & 1u) &&
-                    (ng < 2 || tc::mbar_test(&dq_free[ng & 1], ((uint32_t)(ng >> 1) & 1u) ^ 1u))) {
-                    tc::fence_after_sync();
-                    issue_grads(ng);
-                    ++ng;
-                    did = true;
-                }
-                if (did) {
-                    idle = 0;
-                } else if (++idle >= tc::kSpinLimit) {
-                    report(st, kDevTimeout, 104, ns * 65536 + ng);
-                    *abort_flag = 1;
-                    ok = false;
-                } else if ((idle & 1023u) == 1023u && *abort_flag) {
-                    ok = false;
-                }
+            bool ok = tc::mbar_wait(kv_full, 0, st, 105, abort_flag);
+            for (int ng = 0; ok && ng < nch; ++ng) {
+                if (!tc::mbar_wait(&p_full[ng % kPBuf], (uint32_t)(ng / kPBuf) & 1u, st, 106, abort_flag)) break;
+                if (ng >= 2 && !tc::mbar_wait(&dq_free[ng & 1], ((uint32_t)(ng >> 1) & 1u) ^ 1u, st, 107, abort_flag))
+                    break;
+                tc::fence_after_sync();
+                issue_grads(ng);
             }
-            // every MMA issued above has completed once `done` fires
             tc::mma_commit(done);
-            tc::mbar_wait(done, 0, nullptr, 0, nullptr);
         }
-    } else {
+    } else if (warp < kGradWarp) {
         // ------------------------------------------------ epilogue
         const int qd = warp & 3, hf = (warp - 2) >> 2;
         const int kr = qd * 32 + lane;             // key (S/dP/P/dS phase) or feature (dQ phase)
