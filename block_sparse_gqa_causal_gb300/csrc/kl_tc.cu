@@ -30,7 +30,8 @@ constexpr int kKeys = 128;
 constexpr int kRows = 128;                 // teacher pass: (query, head) rows per chunk
 constexpr int kQ = 128;                    // index pass: queries per chunk
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kProd2 = 2 + kEpiWarps;      // second producer warp: the two take alternate chunks
+constexpr int kThreads = 32 * (3 + kEpiWarps);
 constexpr int kStages = 3;
 constexpr int kParts = 2;                  // partials per (query, group, slot): the two key halves
 constexpr int SUB = 128 * 128;             // [128 rows][64 bf16] swizzled sub-tile
@@ -146,9 +147,10 @@ kl_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        // ------------------------------------------------ producer
-        if (lane == 0) {
+    if (warp == 0 || warp == kProd2) {
+        // ------------------------------------------------ producers (warp 0: even chunks, kProd2: odd)
+        const int pw = warp == 0 ? 0 : 1;
+        if (pw == 0 && lane == 0) {
             tc::prefetch_tmap(&tmap_q);
             tc::mbar_arrive_expect_tx(kv_full, L::H * SUB);
 #pragma unroll
@@ -171,16 +173,17 @@ kl_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             }
         };
         int ent[EPL], ent1[EPL], ent2[EPL];
-        load_entries(ent, bucket_q, qbeg, min(QPC, qend - qbeg), lane);
-        load_entries(ent1, bucket_q, qbeg + QPC, min(QPC, qend - qbeg - QPC), lane);
+        const int qb0 = qbeg + pw * QPC;           // this producer's first chunk
+        load_entries(ent, bucket_q, qb0, min(QPC, qend - qb0), lane);
+        load_entries(ent1, bucket_q, qb0 + 2 * QPC, min(QPC, qend - qb0 - 2 * QPC), lane);
         float vl[4], vl_next[4];
-        load_lse(vl, ent, min(QPC, qend - qbeg));
-        for (int m = 0; m < nch; ++m) {
+        load_lse(vl, ent, min(QPC, qend - qb0));
+        for (int m = pw; m < nch; m += 2) {
             const int s = m % kStages;
             const int q0 = qbeg + m * QPC;
             const int nq = min(QPC, qend - q0);
-            load_entries(ent2, bucket_q, q0 + 2 * QPC, min(QPC, qend - q0 - 2 * QPC), lane);
-            if (m + 1 < nch) load_lse(vl_next, ent1, min(QPC, qend - q0 - QPC));
+            load_entries(ent2, bucket_q, q0 + 4 * QPC, min(QPC, qend - q0 - 4 * QPC), lane);
+            if (m + 2 < nch) load_lse(vl_next, ent1, min(QPC, qend - q0 - 2 * QPC));
             if (!tc::mbar_wait(&empty[s], ((uint32_t)(m / kStages) & 1u) ^ 1u, st, 81, abort_flag)) break;
             Meta *meta = reinterpret_cast<Meta *>(sm + L::OFF_META + s * L::META_BYTES);
 #pragma unroll
@@ -257,7 +260,7 @@ kl_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             tc::mma_commit(done);
             tc::mbar_wait(done, 0, nullptr, 0, nullptr);
         }
-    } else {
+    } else if (warp < kProd2) {
         // ------------------------------------------------ epilogue: one key per thread
         const int qd = warp & 3, hf = (warp - 2) >> 2;
         const int kr = qd * 32 + lane;
@@ -389,20 +392,21 @@ kl_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, const
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        // ------------------------------------------------ producer
-        if (lane == 0) {
+    if (warp == 0 || warp == kProd2) {
+        // ------------------------------------------------ producers (warp 0: even chunks, kProd2: odd)
+        const int pw = warp == 0 ? 0 : 1;
+        if (pw == 0 && lane == 0) {
             tc::mbar_arrive_expect_tx(kv_full, L::H * SUB);
 #pragma unroll
             for (int h = 0; h < L::H; ++h) tc::tma_load_3d(sm + L::OFF_KI + h * SUB, &tmap_ki, kv_full, h * 64, (int)j0, b);
         }
         int ent[4], ent_next[4];
-        load_entries(ent, bucket_q, qbeg, min(kQ, qend - qbeg), lane);
-        for (int m = 0; m < nch; ++m) {
+        load_entries(ent, bucket_q, qbeg + pw * kQ, min(kQ, qend - qbeg - pw * kQ), lane);
+        for (int m = pw; m < nch; m += 2) {
             const int s = m % kStages;
             const int q0 = qbeg + m * kQ;
             const int nq = min(kQ, qend - q0);
-            if (m + 1 < nch) load_entries(ent_next, bucket_q, q0 + kQ, min(kQ, qend - q0 - kQ), lane);
+            if (m + 2 < nch) load_entries(ent_next, bucket_q, q0 + 2 * kQ, min(kQ, qend - q0 - 2 * kQ), lane);
             if (!tc::mbar_wait(&empty[s], ((uint32_t)(m / kStages) & 1u) ^ 1u, st, 85, abort_flag)) break;
             Meta *meta = reinterpret_cast<Meta *>(sm + L::OFF_META + s * L::META_BYTES);
 #pragma unroll
@@ -458,7 +462,7 @@ kl_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, const
             tc::mma_commit(done);
             tc::mbar_wait(done, 0, nullptr, 0, nullptr);
         }
-    } else {
+    } else if (warp < kProd2) {
         // ------------------------------------------------ epilogue: one query per thread, 64 keys
         const int qd = warp & 3, hf = (warp - 2) >> 2;
         const int u = qd * 32 + lane;               // query slot in the chunk (TMEM lane)
