@@ -33,7 +33,8 @@ constexpr int DI = 128;
 constexpr int kKeys = 128;
 constexpr int kQ = 128;                        // queries per chunk
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kProd2 = 2 + kEpiWarps;          // second producer warp: the two take alternate chunks
+constexpr int kThreads = 32 * (3 + kEpiWarps);
 constexpr int SUB = 128 * 128;                 // [128 rows][64 bf16] swizzled sub-tile
 constexpr int OFF_KI = 0;                      // K_idx: 2 feature halves
 constexpr int kStages = 3;                     // q_idx stages
@@ -124,9 +125,10 @@ bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, cons
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        // ------------------------------------------------ producer
-        if (lane == 0) {
+    if (warp == 0 || warp == kProd2) {
+        // ------------------------------------------------ producers (warp 0: even chunks, kProd2: odd)
+        const int pw = warp == 0 ? 0 : 1;
+        if (pw == 0 && lane == 0) {
             tc::mbar_arrive_expect_tx(kv_full, 2 * SUB);
 #pragma unroll
             for (int h = 0; h < 2; ++h) tc::tma_load_3d(sm + OFF_KI + h * SUB, &tmap_ki, kv_full, h * 64, (int)j0, b);
@@ -144,15 +146,16 @@ bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, cons
         };
         int ent[4], ent1[4], ent2[4];
         float vl[4], vl_next[4];
-        load_ent(ent, qbeg, qend - qbeg);
-        load_ent(ent1, qbeg + kQ, qend - qbeg - kQ);
-        load_lse(vl, ent, qend - qbeg);
-        for (int m = 0; m < nch; ++m) {
+        const int qb0 = qbeg + pw * kQ;             // this producer's first chunk
+        load_ent(ent, qb0, qend - qb0);
+        load_ent(ent1, qb0 + 2 * kQ, qend - qb0 - 2 * kQ);
+        load_lse(vl, ent, qend - qb0);
+        for (int m = pw; m < nch; m += 2) {
             const int s = m % kStages;
             const int q0 = qbeg + m * kQ;
             const int nq = min(kQ, qend - q0);
-            load_ent(ent2, q0 + 2 * kQ, qend - q0 - 2 * kQ);
-            if (m + 1 < nch) load_lse(vl_next, ent1, qend - q0 - kQ);
+            load_ent(ent2, q0 + 4 * kQ, qend - q0 - 4 * kQ);
+            if (m + 2 < nch) load_lse(vl_next, ent1, qend - q0 - 2 * kQ);
             if (!tc::mbar_wait(&empty[s], ((uint32_t)(m / kStages) & 1u) ^ 1u, st, 121, abort_flag)) break;
             Meta *meta = reinterpret_cast<Meta *>(sm + OFF_META + s * META_BYTES);
 #pragma unroll
@@ -249,7 +252,7 @@ bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, cons
             tc::mma_commit(done);
             tc::mbar_wait(done, 0, nullptr, 0, nullptr);
         }
-    } else {
+    } else if (warp < kProd2) {
         // ------------------------------------------------ epilogue
         const int qd = warp & 3, hf = (warp - 2) >> 2;
         const int kr = qd * 32 + lane;              // key (s^T phase) or feature (dq_idx^T phase)

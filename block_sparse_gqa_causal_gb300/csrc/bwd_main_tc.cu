@@ -37,7 +37,8 @@ constexpr int kKeys = 128;
 constexpr int kRows = 64;                       // (query, head) rows per chunk
 constexpr int kEpiWarps = 8;
 constexpr int kGradWarp = 2 + kEpiWarps;         // the second MMA issuer (gradients)
-constexpr int kThreads = 32 * (3 + kEpiWarps);
+constexpr int kProd2 = 3 + kEpiWarps;            // second producer warp: the two take alternate chunks
+constexpr int kThreads = 32 * (4 + kEpiWarps);
 constexpr int SUBK = kKeys * 128;               // [128 keys][64 bf16] swizzled sub-tile
 // A [64 rows][128 d] tile is stored as 8-row groups of {d 0..63, d 64..127}
 // (1024-byte swizzle atoms): row rho, half h at (rho/8)*2048 + h*1024 + (rho%8)*128.
@@ -163,10 +164,11 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        // ------------------------------------------------ producer
+    if (warp == 0 || warp == kProd2) {
+        // ------------------------------------------------ producers (warp 0: even chunks, kProd2: odd)
         // K and V tiles by TMA; rows past Nk read as zeros
-        if (lane == 0) {
+        const int pw = warp == 0 ? 0 : 1;
+        if (pw == 0 && lane == 0) {
             tc::prefetch_tmap(&tmap_q);
             tc::prefetch_tmap(&tmap_do);
             tc::mbar_arrive_expect_tx(kv_full, 4 * SUBK);
@@ -195,16 +197,17 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             }
         };
         int ent[EPL], ent1[EPL], ent2[EPL];
-        load_entries(ent, bucket_q, qbeg, min(QC, qend - qbeg), lane);
-        load_entries(ent1, bucket_q, qbeg + QC, min(QC, qend - qbeg - QC), lane);
+        const int qb0 = qbeg + pw * QC;              // this producer's first chunk
+        load_entries(ent, bucket_q, qb0, min(QC, qend - qb0), lane);
+        load_entries(ent1, bucket_q, qb0 + 2 * QC, min(QC, qend - qb0 - 2 * QC), lane);
         float vl[2], vd[2], vl_next[2], vd_next[2];
-        load_rows(vl, vd, ent, min(QC, qend - qbeg));
-        for (int m = 0; m < nch; ++m) {
+        load_rows(vl, vd, ent, min(QC, qend - qb0));
+        for (int m = pw; m < nch; m += 2) {
             const int s = m % kStages;
             const int q0 = qbeg + m * QC;
             const int nq = min(QC, qend - q0);
-            load_entries(ent2, bucket_q, q0 + 2 * QC, min(QC, qend - q0 - 2 * QC), lane);
-            if (m + 1 < nch) load_rows(vl_next, vd_next, ent1, min(QC, qend - q0 - QC));
+            load_entries(ent2, bucket_q, q0 + 4 * QC, min(QC, qend - q0 - 4 * QC), lane);
+            if (m + 2 < nch) load_rows(vl_next, vd_next, ent1, min(QC, qend - q0 - 2 * QC));
             if (!tc::mbar_wait(&empty[s], ((uint32_t)(m / kStages) & 1u) ^ 1u, st, 101, abort_flag)) break;
             Meta *meta = reinterpret_cast<Meta *>(sm + OFF_META + s * META_BYTES);
 #pragma unroll

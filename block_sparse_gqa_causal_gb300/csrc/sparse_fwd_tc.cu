@@ -30,7 +30,8 @@ constexpr int kRows = 128;                  // (query, head) rows per chunk
 constexpr int kKeys = 128;
 constexpr int kEpiWarps = 8;                // two warpgroups, taking alternate chunks
 constexpr int kWgWarps = 4;
-constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kProd2 = 2 + kEpiWarps;        // second producer warp: the two take alternate chunks
+constexpr int kThreads = 32 * (3 + kEpiWarps);
 constexpr int SUB = 128 * 128;              // [128 rows][64 bf16] swizzled sub-tile
 
 template <int D>
@@ -160,10 +161,11 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        // ------------------------------------------------ producer
+    if (warp == 0 || warp == kProd2) {
+        // ------------------------------------------------ producers (warp 0: even chunks, kProd2: odd)
         // K and V tiles of this (b, group, block) by TMA; rows past Nk read as zeros
-        if (lane == 0) {
+        const int pw = warp == 0 ? 0 : 1;
+        if (pw == 0 && lane == 0) {
             tc::prefetch_tmap(&tmap_q);
             tc::mbar_arrive_expect_tx(kv_full, 2 * L::KB * SUB);
 #pragma unroll
@@ -174,13 +176,13 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         }
         constexpr int EPL = (QPC + 31) / 32;
         int ent[EPL], ent_next[EPL];
-        load_entries(ent, bucket_q, qbeg, min(QPC, qend - qbeg), lane);
-        for (int m = 0; m < nch; ++m) {
+        load_entries(ent, bucket_q, qbeg + pw * QPC, min(QPC, qend - qbeg - pw * QPC), lane);
+        for (int m = pw; m < nch; m += 2) {
             const int a = m & 1;
             const int q0 = qbeg + m * QPC;
             const int nq = min(QPC, qend - q0);
             // the next chunk's entries are fetched before waiting for a free stage
-            if (m + 1 < nch) load_entries(ent_next, bucket_q, q0 + QPC, min(QPC, qend - q0 - QPC), lane);
+            if (m + 2 < nch) load_entries(ent_next, bucket_q, q0 + 2 * QPC, min(QPC, qend - q0 - 2 * QPC), lane);
             if (!tc::mbar_wait(&q_empty[a], ((uint32_t)(m >> 1) & 1u) ^ 1u, st, 61, abort_flag)) break;
             QueryMeta *meta = reinterpret_cast<QueryMeta *>(sm + L::OFF_META + a * 2048);
             store_meta(meta->i, meta->pos, meta->slot, ent, QPC, nq, p, lane);
@@ -288,7 +290,7 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             tc::mma_commit(done);
             tc::mbar_wait(done, 0, nullptr, 0, nullptr);
         }
-    } else {
+    } else if (warp < kProd2) {
         // ------------------------------------------------ epilogue: one (query, head) row per thread
         // warpgroup wg takes chunks wg, wg + 2, ... (TMEM and smem buffers wg)
         const int quarter = warp & 3, wg = (warp - 2) >> 2;
