@@ -8,7 +8,7 @@
 // the MMA's M dimension, per chunk:
 //   S^T = K Q^T,  dP^T = V dO^T                   (M = 128 keys, N = 64 rows)
 //   P = exp2(S*scale*log2e - lse*log2e) on the keys each row may see,
-//   dS = P (dP - D),  D = rowsum(dO * O)
+//   dS = scale * P (dP - D),  D = rowsum(dO * O)   (the softmax scale folded in)
 //   dQ^T = K^T dS^T                                (M = 128 features, N = 64 rows)
 //   dV += P^T dO,  dK += dS^T Q                    (M = 128 keys, N = 128 features)
 // dV and dK stay in TMEM for the whole bucket and are written once (one
@@ -19,11 +19,16 @@
 // columns of a thread's row, so it is a register sum, written as fp16 per
 // (bucket entry, key) for the index-branch backward.
 //
-// Roles: warp 0 loads (TMA), warp 1 owns TMEM and issues the MMAs, warps
-// 2..9 are the epilogue: warp w serves TMEM lanes 32*(w%4).. (keys, or
-// features for dQ^T) and column half (w-2)/4 of the chunk's 64 rows.  dQ^T
-// and the P/dS tiles are double-buffered, so the epilogue's work on chunk
-// n overlaps the MMAs of chunks n-1 and n+1.
+// Roles: warps 0 and 11 load (TMA; alternate chunks), warp 1 owns TMEM and
+// issues the score MMAs, warp 10 the gradient MMAs, warps 2..9 are the
+// epilogue: warp w serves TMEM lanes 32*(w%4).. (keys) and column half
+// (w-2)/4 of the chunk's 64 rows.  Warps 12..15 drain dQ^T (lanes are
+// features) into the partial rows, off the epilogue's critical loop; the
+// epilogue hands them each chunk's partial-row indices through a small ring.
+// TMEM holds dV, dK and two 128-column slots; chunk n uses slot n%2 for S^T
+// and dP^T, and its dQ^T then overwrites the S^T half (the epilogue has read
+// it by then).  The slot is free again once the drain has read dQ^T, so the
+// scores of chunk n+1 run while the epilogue works on chunk n.
 #include <cuda_fp16.h>
 
 #include "msa_internal.h"
@@ -38,7 +43,9 @@ constexpr int kRows = 64;                       // (query, head) rows per chunk
 constexpr int kEpiWarps = 8;
 constexpr int kGradWarp = 2 + kEpiWarps;         // the second MMA issuer (gradients)
 constexpr int kProd2 = 3 + kEpiWarps;            // second producer warp: the two take alternate chunks
-constexpr int kThreads = 32 * (4 + kEpiWarps);
+constexpr int kDrainWarps = 4;                   // dQ^T drain: warps 4+kEpiWarps .. (one per TMEM lane quarter)
+constexpr int kThreads = 32 * (4 + kEpiWarps + kDrainWarps);
+constexpr int kRx = 4;                           // ring of chunk partial-row index lists
 constexpr int SUBK = kKeys * 128;               // [128 keys][64 bf16] swizzled sub-tile
 // A [64 rows][128 d] tile is stored as 8-row groups of {d 0..63, d 64..127}
 // (1024-byte swizzle atoms): row rho, half h at (rho/8)*2048 + h*1024 + (rho%8)*128.
@@ -56,7 +63,7 @@ constexpr int OFF_META = OFF_DS + kPBuf * SUBK;
 
 struct Meta {                 // per stage
     float lse2[kRows];        // lse * log2(e) of each row (+inf for padding)
-    float dd[kRows];          // rowsum(dO * O)
+    float dd[kRows];          // scale * rowsum(dO * O)
     int pos[kRows];           // position of each query slot (-1 for padding)
     int qi[kRows];            // query index
     int slot[kRows];          // slot of this block in the query's selection
@@ -64,12 +71,12 @@ struct Meta {                 // per stage
     int nq;                   // queries in the chunk
 };
 constexpr int META_BYTES = (int)((sizeof(Meta) + 127) & ~size_t(127));
-constexpr int OFF_STAGE = OFF_META + kStages * META_BYTES;   // per epilogue warp: dQ [32 rows][32 features] bf16
-constexpr int STAGE_BYTES = 32 * 64;
-constexpr int OFF_BAR = OFF_STAGE + kEpiWarps * STAGE_BYTES;
+constexpr int OFF_RIDX = OFF_META + kStages * META_BYTES;    // kRx x [64 rows] partial-row index (-1: padding)
+constexpr int OFF_BAR = OFF_RIDX + kRx * kRows * 8;
 constexpr int ALLOC = OFF_BAR + 256 + 1024;
 
-constexpr uint32_t TM_DV = 0, TM_DK = 128, TM_S = 256, TM_DP = 320, TM_DQ = 384;   // TM_DQ: 2 x 64
+// slot a: S^T (later dQ^T) at TM_SLOT + 128a, dP^T 64 columns above it
+constexpr uint32_t TM_DV = 0, TM_DK = 128, TM_SLOT = 256, TM_DP_OFF = 64;
 
 __device__ __forceinline__ int swz(int row, int ch) { return row * 128 + ((ch ^ (row & 7)) << 4); }
 __device__ __forceinline__ int roff(int rho, int half, int ch)
@@ -127,9 +134,11 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
     uint64_t *full = bars, *empty = bars + 3, *p_full = bars + 6, *p_free = bars + 8;
-    uint64_t *dq_full = bars + 10, *dq_free = bars + 12;
-    uint64_t *kv_full = bars + 14, *s_full = bars + 15, *tm_free = bars + 16, *done = bars + 17;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 18);
+    uint64_t *dq_full = bars + 10, *slot_free = bars + 12;
+    uint64_t *kv_full = bars + 14, *s_full = bars + 15, *done = bars + 17;   // s_full: 2 (one per slot)
+    uint64_t *rx_full = bars + 18, *rx_free = bars + 18 + kRx;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 18 + 2 * kRx);
+    long long *ridx_ring = reinterpret_cast<long long *>(sm + OFF_RIDX);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -145,12 +154,15 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             tc::mbar_init(&p_free[a], 1);
         }
         for (int a = 0; a < 2; ++a) {
+            tc::mbar_init(&s_full[a], 1);
             tc::mbar_init(&dq_full[a], 1);
-            tc::mbar_init(&dq_free[a], kEpiWarps);
+            tc::mbar_init(&slot_free[a], kDrainWarps);
+        }
+        for (int a = 0; a < kRx; ++a) {
+            tc::mbar_init(&rx_full[a], 2);              // the two epilogue warps of lane quarter 0
+            tc::mbar_init(&rx_free[a], kDrainWarps);
         }
         tc::mbar_init(kv_full, 1);
-        tc::mbar_init(s_full, 1);
-        tc::mbar_init(tm_free, kEpiWarps);
         tc::mbar_init(done, 2);                        // both MMA issuers
         *abort_flag = 0;
         tc::fence_mbar_init();
@@ -213,7 +225,7 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
                 meta->lse2[lane + 32 * t] = vl[t] * kLog2e;
-                meta->dd[lane + 32 * t] = vd[t];
+                meta->dd[lane + 32 * t] = vd[t] * p.scale;
             }
 #pragma unroll
             for (int t = 0; t < EPL; ++t) {
@@ -275,19 +287,20 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
             constexpr uint32_t I_S = tc::idesc_bf16(128, kRows);
-            const uint32_t aK = smem_u32(sm + OFF_K), aV = smem_u32(sm + OFF_V);
+            const uint64_t dK = tc::sdesc_k128(smem_u32(sm + OFF_K)), dV = tc::sdesc_k128(smem_u32(sm + OFF_V));
             auto issue_scores = [&](int n) {
-                const uint32_t sq = smem_u32(sm + OFF_STG + (n % kStages) * STG_BYTES), sdo = sq + TILE_R;
+                // B = Q / dO rows (K-major, 8-row groups 2048 bytes apart)
+                const uint32_t sq = smem_u32(sm + OFF_STG + (n % kStages) * STG_BYTES);
+                const uint64_t dQ = tc::sdesc_sw128(sq, 16, 2048), dDO = tc::sdesc_sw128(sq + TILE_R, 16, 2048);
+                const uint32_t ts = tmem + TM_SLOT + (n & 1) * 128;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t h = ks >> 2, ko = (ks & 3) * 32;
-                    // B = Q / dO rows (K-major, 8-row groups 2048 bytes apart)
-                    tc::mma_bf16(tmem + TM_S, tc::sdesc_k128(aK + h * SUBK + ko),
-                                 tc::sdesc_sw128(sq + h * 1024 + ko, 16, 2048), I_S, ks > 0);
-                    tc::mma_bf16(tmem + TM_DP, tc::sdesc_k128(aV + h * SUBK + ko),
-                                 tc::sdesc_sw128(sdo + h * 1024 + ko, 16, 2048), I_S, ks > 0);
+                    tc::mma_bf16(ts, tc::desc_adv(dK, h * SUBK + ko), tc::desc_adv(dQ, h * 1024 + ko), I_S, ks > 0);
+                    tc::mma_bf16(ts + TM_DP_OFF, tc::desc_adv(dV, h * SUBK + ko), tc::desc_adv(dDO, h * 1024 + ko), I_S,
+                                 ks > 0);
                 }
-                tc::mma_commit(s_full);
+                tc::mma_commit(&s_full[n & 1]);
             };
             // Scores here, gradients on warp kGradWarp: the two streams touch
             // disjoint TMEM and shared memory, are ordered only through the
@@ -296,7 +309,10 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             if (ok) tc::fence_proxy_async();
             for (int ns = 0; ok && ns < nch; ++ns) {
                 if (!tc::mbar_wait(&full[ns % kStages], (uint32_t)(ns / kStages) & 1u, st, 103, abort_flag)) break;
-                if (ns > 0 && !tc::mbar_wait(tm_free, (uint32_t)(ns - 1) & 1u, st, 104, abort_flag)) break;
+                // the slot's previous chunk (ns-2) has had its dQ^T drained
+                if (ns >= 2 &&
+                    !tc::mbar_wait(&slot_free[ns & 1], (uint32_t)((ns >> 1) - 1) & 1u, st, 104, abort_flag))
+                    break;
                 tc::fence_proxy_async();
                 tc::fence_after_sync();
                 issue_scores(ns);
@@ -311,27 +327,30 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             // ------------------------------------------------ MMA issuer: gradients
             constexpr uint32_t I_DKV = tc::idesc_bf16(128, 128) | tc::kBMajorMN;
             constexpr uint32_t I_DQ = tc::idesc_bf16(128, kRows) | tc::kAMajorMN | tc::kBMajorMN;
-            const uint32_t aK = smem_u32(sm + OFF_K);
+            static_assert(kPBuf == 1, "the P / dS descriptors below assume one buffer");
+            const uint64_t dKT = tc::sdesc_sw128(smem_u32(sm + OFF_K), SUBK, 1024);
+            const uint64_t dDST = tc::sdesc_sw128(smem_u32(sm + OFF_DS), SUBK, 1024);
+            const uint64_t dP = tc::sdesc_k128(smem_u32(sm + OFF_P)), dDS = tc::sdesc_k128(smem_u32(sm + OFF_DS));
             auto issue_grads = [&](int n) {
-                const int pb = n % kPBuf, qb = n & 1;
-                const uint32_t sq = smem_u32(sm + OFF_STG + (n % kStages) * STG_BYTES), sdo = sq + TILE_R;
-                const uint32_t aP = smem_u32(sm + OFF_P + pb * SUBK), aDS = smem_u32(sm + OFF_DS + pb * SUBK);
-                // dQ^T = K^T dS^T: A = K read MN-major (64-feature atoms SUBK apart),
-                // B = dS^T [keys][rows] read MN-major; K = 128 keys
+                const int pb = n % kPBuf;
+                const uint32_t sq = smem_u32(sm + OFF_STG + (n % kStages) * STG_BYTES);
+                const uint64_t dQm = tc::sdesc_sw128(sq, 1024, 2048), dDOm = tc::sdesc_sw128(sq + TILE_R, 1024, 2048);
+                // dQ^T = K^T dS^T first (its drain frees the slot for chunk n+2), into
+                // the S^T half of the chunk's slot (read by the epilogue before it
+                // signalled p_full): A = K read MN-major (64-feature atoms SUBK
+                // apart), B = dS^T [keys][rows] MN-major; K = 128 keys
 #pragma unroll
                 for (int ks = 0; ks < kKeys / 16; ++ks)
-                    tc::mma_bf16(tmem + TM_DQ + qb * kRows, tc::sdesc_sw128(aK + ks * 2048, SUBK, 1024),
-                                 tc::sdesc_sw128(aDS + ks * 2048, SUBK, 1024), I_DQ, ks > 0);
-                tc::mma_commit(&dq_full[qb]);
+                    tc::mma_bf16(tmem + TM_SLOT + (n & 1) * 128, tc::desc_adv(dKT, ks * 2048),
+                                 tc::desc_adv(dDST, ks * 2048), I_DQ, ks > 0);
+                tc::mma_commit(&dq_full[n & 1]);
                 // dV += P^T dO, dK += dS^T Q: B = dO / Q read MN-major (feature
                 // halves 1024 bytes apart, 8-row groups 2048 apart); K = 64 rows
 #pragma unroll
                 for (int ks = 0; ks < kRows / 16; ++ks) {
                     const bool acc = n > 0 || ks > 0;
-                    tc::mma_bf16(tmem + TM_DV, tc::sdesc_k128(aP + ks * 32), tc::sdesc_sw128(sdo + ks * 4096, 1024, 2048),
-                                 I_DKV, acc);
-                    tc::mma_bf16(tmem + TM_DK, tc::sdesc_k128(aDS + ks * 32), tc::sdesc_sw128(sq + ks * 4096, 1024, 2048),
-                                 I_DKV, acc);
+                    tc::mma_bf16(tmem + TM_DV, tc::desc_adv(dP, ks * 32), tc::desc_adv(dDOm, ks * 4096), I_DKV, acc);
+                    tc::mma_bf16(tmem + TM_DK, tc::desc_adv(dDS, ks * 32), tc::desc_adv(dQm, ks * 4096), I_DKV, acc);
                 }
                 tc::mma_commit(&empty[n % kStages]);
                 tc::mma_commit(&p_free[pb]);
@@ -339,12 +358,39 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             bool ok = tc::mbar_wait(kv_full, 0, st, 105, abort_flag);
             for (int ng = 0; ok && ng < nch; ++ng) {
                 if (!tc::mbar_wait(&p_full[ng % kPBuf], (uint32_t)(ng / kPBuf) & 1u, st, 106, abort_flag)) break;
-                if (ng >= 2 && !tc::mbar_wait(&dq_free[ng & 1], ((uint32_t)(ng >> 1) & 1u) ^ 1u, st, 107, abort_flag))
-                    break;
                 tc::fence_after_sync();
                 issue_grads(ng);
             }
             tc::mma_commit(done);
+        }
+    } else if (warp >= 4 + kEpiWarps) {
+        // ------------------------------------------------ dQ^T drain: features 32*qd.. of all 64 rows
+        const int qd = warp & 3;
+        const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+        bf16 *col = dq_part + qd * 32 + lane;
+        for (int m = 0; m < nch; ++m) {
+            const int pb = m & 1, x = m % kRx;
+            if (!wwait(&rx_full[x], (uint32_t)(m / kRx) & 1u, st, 117, abort_flag)) break;
+            if (!wwait(&dq_full[pb], (uint32_t)(m >> 1) & 1u, st, 111, abort_flag)) break;
+            tc::fence_after_sync();
+            uint32_t v0[32], v1[32];
+            tc::tmem_ld32_nowait(tmem + lane_base + TM_SLOT + pb * 128, v0);
+            tc::tmem_ld32_nowait(tmem + lane_base + TM_SLOT + pb * 128 + 32, v1);
+            tc::tmem_wait32(v0);
+            tc::tmem_wait32(v1);
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&slot_free[pb]);
+            // one row per step: the warp's 32 lanes write 64 contiguous bytes of it
+            const long long *rx = ridx_ring + x * kRows;
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc) {
+                const long long r0 = rx[cc], r1 = rx[32 + cc];
+                if (r0 >= 0) col[r0 * D] = __float2bfloat16_rn(__uint_as_float(v0[cc]));
+                if (r1 >= 0) col[r1 * D] = __float2bfloat16_rn(__uint_as_float(v1[cc]));
+            }
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&rx_free[x]);
         }
     } else if (warp < kGradWarp) {
         // ------------------------------------------------ epilogue
@@ -357,55 +403,19 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         const float invG = 1.f / (float)G;
         constexpr int NQH = 32 / G;                // query slots among this warp's 32 columns
         const int cb = hf * 32;                    // first column (row of the chunk) of this warp
-        long long ridx_prev = -1;                  // partial row of column cb + lane of the chunk being drained
+        const long long pt_base = pt_off[bucket];  // this bucket's first teacher row
         bool ok = true;
-        // writes the dQ partial rows of chunk m (row indices held in ridx_prev)
-        auto drain_dq = [&](int m) -> bool {
-            const int pb = m & 1;
-            if (!wwait(&dq_full[pb], (uint32_t)(m >> 1) & 1u, st, 111, abort_flag)) return false;
-            tc::fence_after_sync();
-            uint32_t v[32];
-            tc::tmem_ld32_nowait(tmem + lane_base + TM_DQ + pb * kRows + cb, v);
-            tc::tmem_wait32(v);
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&dq_free[pb]);
-            // transpose the warp's [32 features][32 rows] block through shared
-            // memory, then write 64 contiguous bytes per row with 16-byte stores
-            uint8_t *stage = sm + OFF_STAGE + (warp - 2) * STAGE_BYTES;
-#pragma unroll
-            for (int cc = 0; cc < 32; ++cc)
-                *reinterpret_cast<bf16 *>(stage + cc * 64 + lane * 2) =
-                    __float2bfloat16_rn(p.scale * __uint_as_float(v[cc]));
-            __syncwarp();
-#pragma unroll
-            for (int it = 0; it < 4; ++it) {
-                const int row = it * 8 + (lane >> 2), q4 = lane & 3;
-                const long long rix = __shfl_sync(0xffffffffu, ridx_prev, row);
-                const uint4 x = *reinterpret_cast<const uint4 *>(stage + row * 64 + q4 * 16);
-                if (rix >= 0) *reinterpret_cast<uint4 *>(dq_part + rix * D + qd * 32 + q4 * 8) = x;
-            }
-            __syncwarp();
-            return true;
-        };
         for (int n = 0; ok && n < nch; ++n) {
             const int s = n % kStages, pb = n % kPBuf;
             const Meta *meta = reinterpret_cast<const Meta *>(sm + OFF_META + s * META_BYTES);
             if (!wwait(&full[s], (uint32_t)(n / kStages) & 1u, st, 112, abort_flag)) { ok = false; break; }
-            if (!wwait(s_full, (uint32_t)n & 1u, st, 113, abort_flag)) { ok = false; break; }
+            if (!wwait(&s_full[n & 1], (uint32_t)(n >> 1) & 1u, st, 113, abort_flag)) { ok = false; break; }
             tc::fence_after_sync();
             uint32_t sv[32], dp[32];
-            tc::tmem_ld32_nowait(tmem + lane_base + TM_S + cb, sv);
-            tc::tmem_ld32_nowait(tmem + lane_base + TM_DP + cb, dp);
-            // row data while the loads land
-            float l2[32], dd[32];
-#pragma unroll
-            for (int x = 0; x < 8; ++x) {
-                const float4 a = reinterpret_cast<const float4 *>(meta->lse2 + cb)[x];
-                const float4 e = reinterpret_cast<const float4 *>(meta->dd + cb)[x];
-                l2[4 * x] = a.x; l2[4 * x + 1] = a.y; l2[4 * x + 2] = a.z; l2[4 * x + 3] = a.w;
-                dd[4 * x] = e.x; dd[4 * x + 1] = e.y; dd[4 * x + 2] = e.z; dd[4 * x + 3] = e.w;
-            }
+            const uint32_t ts = tmem + lane_base + TM_SLOT + (n & 1) * 128 + cb;
+            tc::tmem_ld32_nowait(ts, sv);
+            tc::tmem_ld32_nowait(ts + TM_DP_OFF, dp);
+            // row data while the loads land (LSE and D are read in the loop below)
             int pos[NQH];
 #pragma unroll
             for (int u = 0; u < NQH; ++u) pos[u] = meta->pos[cb / G + u];
@@ -419,12 +429,6 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             }
             tc::tmem_wait32(sv);
             tc::tmem_wait32(dp);
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) {
-                tc::mbar_arrive(tm_free);
-                tc::mbar_arrive(&empty[s]);       // the row data now lives in registers
-            }
             // P^T, dS^T of this key against the warp's 32 rows; teacher sums
             uint32_t pk[16], dk2[16];
             float ptq[NQH];
@@ -433,22 +437,27 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
 #pragma unroll
             for (int cc = 0; cc < 32; cc += 2) {
                 float pr[2], ds[2];
+                const float2 l2 = *reinterpret_cast<const float2 *>(meta->lse2 + cb + cc);
+                const float2 dd = *reinterpret_cast<const float2 *>(meta->dd + cb + cc);
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int col = cc + e, u = col / G;
                     const bool vis = key_ok && j <= (long long)pos[u];
-                    pr[e] = vis ? tc::ex2(__uint_as_float(sv[col]) * sl2 - l2[col]) : 0.f;
-                    ds[e] = pr[e] * (__uint_as_float(dp[col]) - dd[col]);
+                    pr[e] = vis ? tc::ex2(__uint_as_float(sv[col]) * sl2 - (e ? l2.y : l2.x)) : 0.f;
+                    // dS carries the softmax scale, so dQ and dK need no rescaling
+                    ds[e] = pr[e] * fmaf(__uint_as_float(dp[col]), p.scale, -(e ? dd.y : dd.x));
                     ptq[u] += pr[e];
                 }
                 pk[cc / 2] = pack_bf16(pr[0], pr[1]);
                 dk2[cc / 2] = pack_bf16(ds[0], ds[1]);
             }
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&empty[s]);   // done with the stage's row data
             {
                 // this key's teacher for the warp's NQH queries (consecutive entries,
                 // 4-aligned): 8 bytes into one 8-entry group, or 16 bytes per group
                 const int t = e0 - qbeg + cb / G;
-                __half *dst = pt_out + ((long long)pt_off[bucket] + (t & ~7)) * kKeys + kr * 8 + (t & 7);
+                __half *dst = pt_out + (pt_base + (t & ~7)) * kKeys + kr * 8 + (t & 7);
                 uint32_t hv[NQH / 2];
 #pragma unroll
                 for (int u = 0; u < NQH; u += 2) {
@@ -472,6 +481,16 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 ok = false;
                 break;
             }
+            if (qd == 0) {
+                // this chunk's partial-row indices for the dQ drain
+                if (n >= kRx && !wwait(&rx_free[n % kRx], (uint32_t)((n / kRx) - 1) & 1u, st, 116, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                ridx_ring[(n % kRx) * kRows + cb + lane] = ridx_cur;
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&rx_full[n % kRx]);
+            }
             uint8_t *sp = sm + OFF_P + pb * SUBK, *sd = sm + OFF_DS + pb * SUBK;
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
@@ -482,12 +501,10 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                     make_uint4(dk2[c4 * 4], dk2[c4 * 4 + 1], dk2[c4 * 4 + 2], dk2[c4 * 4 + 3]);
             }
             tc::fence_proxy_async();
+            tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&p_full[pb]);
-            if (n >= 1 && !drain_dq(n - 1)) { ok = false; break; }
-            ridx_prev = ridx_cur;
         }
-        if (ok && nch > 0) ok = drain_dq(nch - 1);
         // ---- dK, dV of this key (this warp: features hf*64 .. hf*64+63)
         if (ok && nch > 0) {
             // the last chunk's buffer release follows every MMA of the bucket
@@ -519,10 +536,10 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                             pack_bf16(__uint_as_float(a[x + 4]), __uint_as_float(a[x + 5])),
                             pack_bf16(__uint_as_float(a[x + 6]), __uint_as_float(a[x + 7])));
                         *reinterpret_cast<uint4 *>(pk_ + h2 * 32 + x) = make_uint4(
-                            pack_bf16(p.scale * __uint_as_float(g2[x]), p.scale * __uint_as_float(g2[x + 1])),
-                            pack_bf16(p.scale * __uint_as_float(g2[x + 2]), p.scale * __uint_as_float(g2[x + 3])),
-                            pack_bf16(p.scale * __uint_as_float(g2[x + 4]), p.scale * __uint_as_float(g2[x + 5])),
-                            pack_bf16(p.scale * __uint_as_float(g2[x + 6]), p.scale * __uint_as_float(g2[x + 7])));
+                            pack_bf16(__uint_as_float(g2[x]), __uint_as_float(g2[x + 1])),
+                            pack_bf16(__uint_as_float(g2[x + 2]), __uint_as_float(g2[x + 3])),
+                            pack_bf16(__uint_as_float(g2[x + 4]), __uint_as_float(g2[x + 5])),
+                            pack_bf16(__uint_as_float(g2[x + 6]), __uint_as_float(g2[x + 7])));
                     }
                 }
             }

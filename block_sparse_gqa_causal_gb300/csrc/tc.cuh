@@ -206,6 +206,20 @@ MSA_DEV uint64_t sdesc_sw128(uint32_t smem_addr, uint32_t lbo_bytes, uint32_t sb
     return d;
 }
 
+// Advance a shared-memory descriptor by a byte offset (a multiple of 16).
+// The start address sits in the low 14 bits in 16-byte units and no
+// shared-memory address (< 256 KB) carries out of that field, so one 32-bit
+// add on the low word does it: the MMA issuers precompute their base
+// descriptors once and advance them with this single add per instruction,
+// which keeps a lone issuing thread ahead of the tensor pipe.
+MSA_DEV uint64_t desc_adv(uint64_t d, uint32_t bytes)
+{
+    const uint32_t lo = (uint32_t)d + (bytes >> 4), hi = (uint32_t)(d >> 32);
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};\n" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+
 // instruction-descriptor bits selecting MN-major A / B
 constexpr uint32_t kAMajorMN = 1u << 15;
 constexpr uint32_t kBMajorMN = 1u << 16;
