@@ -197,31 +197,31 @@ bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, cons
             constexpr uint32_t I_S = tc::idesc_bf16(128, kQ);
             constexpr uint32_t I_DKI = tc::idesc_bf16(128, DI) | tc::kBMajorMN;
             constexpr uint32_t I_DQI = tc::idesc_bf16(128, kQ) | tc::kAMajorMN | tc::kBMajorMN;
-            const uint32_t aKI = smem_u32(sm + OFF_KI);
+            const uint32_t aKI = smem_u32(sm + OFF_KI), sg = smem_u32(sm + OFF_SIG);
+            const uint64_t dKI = tc::sdesc_k128(aKI), dKIT = tc::sdesc_sw128(aKI, SUB, 1024);
+            const uint64_t dSGT = tc::sdesc_sw128(sg, SUB, 1024), dSG = tc::sdesc_k128(sg);
             auto issue_s = [&](int n) {
-                const uint32_t sq = smem_u32(sm + OFF_STG + (n % kStages) * (2 * SUB));
+                const uint64_t dQ = tc::sdesc_k128(smem_u32(sm + OFF_STG + (n % kStages) * (2 * SUB)));
 #pragma unroll
                 for (int ks = 0; ks < DI / 16; ++ks) {
                     const uint32_t off = (ks >> 2) * SUB + (ks & 3) * 32;
-                    tc::mma_bf16(tmem + TM_S + (n & 1) * kQ, tc::sdesc_k128(aKI + off), tc::sdesc_k128(sq + off), I_S,
-                                 ks > 0);
+                    tc::mma_bf16(tmem + TM_S + (n & 1) * kQ, tc::desc_adv(dKI, off), tc::desc_adv(dQ, off), I_S, ks > 0);
                 }
                 tc::mma_commit(&s_full[n & 1]);
             };
             auto issue_g = [&](int n) {
-                const uint32_t sq = smem_u32(sm + OFF_STG + (n % kStages) * (2 * SUB));
-                const uint32_t sg = smem_u32(sm + OFF_SIG);
+                const uint64_t dQm = tc::sdesc_sw128(smem_u32(sm + OFF_STG + (n % kStages) * (2 * SUB)), SUB, 1024);
                 // dq_idx^T = K_idx^T dsig^T: both operands read MN-major; K = 128 keys
 #pragma unroll
                 for (int ks = 0; ks < kKeys / 16; ++ks)
-                    tc::mma_bf16(tmem + TM_DQI, tc::sdesc_sw128(aKI + ks * 2048, SUB, 1024),
-                                 tc::sdesc_sw128(sg + ks * 2048, SUB, 1024), I_DQI, ks > 0);
+                    tc::mma_bf16(tmem + TM_DQI, tc::desc_adv(dKIT, ks * 2048), tc::desc_adv(dSGT, ks * 2048), I_DQI,
+                                 ks > 0);
                 tc::mma_commit(dq_full);
                 // dK_idx += dsig^T q_idx: A K-major over queries, B = q_idx read MN-major; K = 128 queries
 #pragma unroll
                 for (int ks = 0; ks < kQ / 16; ++ks)
-                    tc::mma_bf16(tmem + TM_DKI, tc::sdesc_k128(sg + (ks >> 2) * SUB + (ks & 3) * 32),
-                                 tc::sdesc_sw128(sq + ks * 2048, SUB, 1024), I_DKI, n > 0 || ks > 0);
+                    tc::mma_bf16(tmem + TM_DKI, tc::desc_adv(dSG, (ks >> 2) * SUB + (ks & 3) * 32),
+                                 tc::desc_adv(dQm, ks * 2048), I_DKI, n > 0 || ks > 0);
                 tc::mma_commit(&empty[n % kStages]);
                 tc::mma_commit(g_free);
             };

@@ -130,6 +130,7 @@ index_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_
         if (lane == 0) {
             // ---------------- MMA issuer
             bool ok = tc::mbar_wait(q_full, 0, st, 12, abort_flag);
+            const uint64_t dq = tc::sdesc_k128(smem_u32(sQ));
             int issued = 0;
             for (int n = 0; ok && n < nblk; ++n) {
                 const int s = n % kStages;
@@ -139,14 +140,13 @@ index_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_
                 if (!tc::mbar_wait(&acc_empty[a], aph ^ 1u, st, 13, abort_flag)) break;
                 if (!tc::mbar_wait(&full[s], ph, st, 14, abort_flag)) break;
                 tc::fence_after_sync();
+                const uint64_t dk = tc::sdesc_k128(smem_u32(sK + s * S::K_BYTES));
                 for (int m = 0; m < mt; ++m) {
                     const uint32_t d = tmem + (uint32_t)((a * 2 + m) * 128);
 #pragma unroll
                     for (int ks = 0; ks < DI / 16; ++ks) {
-                        const int kb = ks >> 2, ko = (ks & 3) * 32;
-                        const uint64_t ad = tc::sdesc_k128(smem_u32(sQ + (m * S::KB + kb) * kSub + ko));
-                        const uint64_t bd = tc::sdesc_k128(smem_u32(sK + s * S::K_BYTES + kb * kSub + ko));
-                        tc::mma_bf16(d, ad, bd, kIdesc, ks > 0);
+                        const uint32_t off = (ks >> 2) * kSub + (ks & 3) * 32;
+                        tc::mma_bf16(d, tc::desc_adv(dq, m * S::KB * kSub + off), tc::desc_adv(dk, off), kIdesc, ks > 0);
                     }
                 }
                 tc::mma_commit(&empty[s]);

@@ -239,20 +239,20 @@ kl_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
             constexpr uint32_t I_S = tc::idesc_bf16(128, kRows);
-            const uint32_t aK = smem_u32(sm + L::OFF_K);
+            const uint64_t dK = tc::sdesc_k128(smem_u32(sm + L::OFF_K));
             bool ok = tc::mbar_wait(kv_full, 0, st, 82, abort_flag);
             for (int n = 0; ok && n < nch; ++n) {
                 if (!tc::mbar_wait(&full[n % kStages], (uint32_t)(n / kStages) & 1u, st, 83, abort_flag)) break;
                 if (n >= 2 && !tc::mbar_wait(&s_free[n & 1], ((uint32_t)(n >> 1) & 1u) ^ 1u, st, 84, abort_flag)) break;
                 tc::fence_proxy_async();
                 tc::fence_after_sync();
-                const uint32_t sq = smem_u32(sm + L::OFF_Q + (n % kStages) * L::TILE);
+                const uint64_t dQ = tc::sdesc_sw128(smem_u32(sm + L::OFF_Q + (n % kStages) * L::TILE), 16, L::H * 1024);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t h = ks >> 2, ko = (ks & 3) * 32;
                     // B = Q rows, K-major, 8-row groups (D/64) KB apart
-                    tc::mma_bf16(tmem + (n & 1) * kRows, tc::sdesc_k128(aK + h * SUB + ko),
-                                 tc::sdesc_sw128(sq + h * 1024 + ko, 16, L::H * 1024), I_S, ks > 0);
+                    tc::mma_bf16(tmem + (n & 1) * kRows, tc::desc_adv(dK, h * SUB + ko), tc::desc_adv(dQ, h * 1024 + ko),
+                                 I_S, ks > 0);
                 }
                 tc::mma_commit(&s_full[n & 1]);
                 tc::mma_commit(&empty[n % kStages]);
@@ -442,19 +442,18 @@ kl_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, const
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer: s = q_idx K_idx^T
             constexpr uint32_t I_S = tc::idesc_bf16(128, kKeys);
-            const uint32_t aKI = smem_u32(sm + L::OFF_KI);
+            const uint64_t dKI = tc::sdesc_k128(smem_u32(sm + L::OFF_KI));
             bool ok = tc::mbar_wait(kv_full, 0, st, 86, abort_flag);
             for (int n = 0; ok && n < nch; ++n) {
                 if (!tc::mbar_wait(&full[n % kStages], (uint32_t)(n / kStages) & 1u, st, 87, abort_flag)) break;
                 if (n >= 2 && !tc::mbar_wait(&s_free[n & 1], ((uint32_t)(n >> 1) & 1u) ^ 1u, st, 88, abort_flag)) break;
                 tc::fence_proxy_async();
                 tc::fence_after_sync();
-                const uint32_t sq = smem_u32(sm + L::OFF_Q + (n % kStages) * (L::H * SUB));
+                const uint64_t dQ = tc::sdesc_k128(smem_u32(sm + L::OFF_Q + (n % kStages) * (L::H * SUB)));
 #pragma unroll
                 for (int ks = 0; ks < DI / 16; ++ks) {
                     const uint32_t off = (ks >> 2) * SUB + (ks & 3) * 32;
-                    tc::mma_bf16(tmem + (n & 1) * kKeys, tc::sdesc_k128(sq + off), tc::sdesc_k128(aKI + off), I_S,
-                                 ks > 0);
+                    tc::mma_bf16(tmem + (n & 1) * kKeys, tc::desc_adv(dQ, off), tc::desc_adv(dKI, off), I_S, ks > 0);
                 }
                 tc::mma_commit(&s_full[n & 1]);
                 tc::mma_commit(&empty[n % kStages]);

@@ -226,30 +226,33 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             // ------------------------------------------------ MMA issuer
             constexpr uint32_t I_S = tc::idesc_bf16(128, kKeys);
             constexpr uint32_t I_O = tc::idesc_bf16(128, D) | tc::kBMajorMN;
-            const uint32_t aK = smem_u32(sm + L::OFF_K), aV = smem_u32(sm + L::OFF_V);
+            const uint64_t dK = tc::sdesc_k128(smem_u32(sm + L::OFF_K));
+            const uint64_t dV = tc::sdesc_sw128(smem_u32(sm + L::OFF_V), SUB, 1024);
+            const uint64_t dQ0 = tc::sdesc_sw128(smem_u32(sm + L::OFF_Q), 16, L::KB * 1024);
+            const uint64_t dP0 = tc::sdesc_k128(smem_u32(sm + L::OFF_P));
             bool ok = tc::mbar_wait(kv_full, 0, st, 62, abort_flag);
             if (ok) tc::fence_proxy_async();
             auto issue_s = [&](int n) {
                 const int a = n & 1;
-                const uint32_t aQ = smem_u32(sm + L::OFF_Q + a * (L::KB * SUB));
+                const uint64_t dQ = tc::desc_adv(dQ0, a * (L::KB * SUB));
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t h = ks >> 2, ko = (ks & 3) * 32;
                     // A = Q rows (K-major, 8-row groups KB KB apart), B = K
-                    tc::mma_bf16(tmem + L::TM_S + a * 128, tc::sdesc_sw128(aQ + h * 1024 + ko, 16, L::KB * 1024),
-                                 tc::sdesc_k128(aK + h * SUB + ko), I_S, ks > 0);
+                    tc::mma_bf16(tmem + L::TM_S + a * 128, tc::desc_adv(dQ, h * 1024 + ko), tc::desc_adv(dK, h * SUB + ko),
+                                 I_S, ks > 0);
                 }
                 tc::mma_commit(&s_full[a]);
                 tc::mma_commit(&q_empty[a]);
             };
             auto issue_o = [&](int m) {
                 const int a = m & 1;
-                const uint32_t aP = smem_u32(sm + L::OFF_P + a * (2 * SUB));
+                const uint64_t dP = tc::desc_adv(dP0, a * (2 * SUB));
 #pragma unroll
                 for (int ks = 0; ks < kKeys / 16; ++ks) {
                     // A = P [rows][keys] K-major; B = V [keys][d] read MN-major (atoms of 64 d, 8-key groups)
-                    tc::mma_bf16(tmem + L::TM_O + a * D, tc::sdesc_k128(aP + (ks >> 2) * SUB + (ks & 3) * 32),
-                                 tc::sdesc_sw128(aV + ks * 2048, SUB, 1024), I_O, ks > 0);
+                    tc::mma_bf16(tmem + L::TM_O + a * D, tc::desc_adv(dP, (ks >> 2) * SUB + (ks & 3) * 32),
+                                 tc::desc_adv(dV, ks * 2048), I_O, ks > 0);
                 }
                 tc::mma_commit(&o_full[a]);
                 tc::mma_commit(&p_free[a]);
