@@ -47,14 +47,18 @@ def tokens_per_row(w, pos):
 
 
 def useful_flops(w, positions=None):
-    """Closed-form useful FLOPs per phase for one pass (all batch entries)."""
+    """Closed-form useful FLOPs per phase for one pass (all batch entries).
+    The KL's teacher needs the main-branch probabilities, which the backward
+    recomputes anyway (its S = QK^T, counted under "bwd"); the training step
+    takes the teacher's sums from there, so "kl" counts only the index
+    scores over the selected tokens (lse_idx)."""
     pos = np.arange(w.N, dtype=np.float64) if positions is None else np.asarray(positions, dtype=np.float64)
     T = tokens_per_row(w, pos.astype(np.int64)).astype(np.float64)
     B = w.B
     f = {
         "index": B * float(np.sum(2.0 * w.d_idx * (pos + 1) * w.Hkv)),
         "fwd": B * float(np.sum(4.0 * w.d * T * w.Hq)),
-        "kl": B * float(np.sum(2.0 * w.d * T * w.Hq + 2.0 * w.d_idx * T * w.Hkv)),
+        "kl": B * float(np.sum(2.0 * w.d_idx * T * w.Hkv)),
         "bwd": B * float(np.sum(10.0 * w.d * T * w.Hq + 6.0 * w.d_idx * T * w.Hkv)),
     }
     if not w.train:
@@ -74,7 +78,7 @@ def kernel_work(w):
     work = {
         "index_scores_tc_kernel": (B * float(np.sum(2.0 * w.d_idx * (pos + 1) * w.Hkv)), "tensor"),
         "sparse_fwd_tc_kernel": (B * float(np.sum(4.0 * w.d * T * w.Hq)), "tensor"),
-        "kl_tc_kernel": (B * float(np.sum(2.0 * w.d * T * w.Hq + 2.0 * w.d_idx * T * w.Hkv)), "tensor"),
+        "kl_index_tc_kernel": (B * float(np.sum(2.0 * w.d_idx * T * w.Hkv)), "tensor"),
         "bwd_main_tc_kernel": (B * float(np.sum(10.0 * w.d * T * w.Hq)), "tensor"),
         "bwd_index_tc_kernel": (B * float(np.sum(6.0 * w.d_idx * T * w.Hkv)), "tensor"),
         # block scores of the visible blocks in, indices out
@@ -262,7 +266,9 @@ def main():
     lse_idx = torch.empty((w.B, w.Hkv, w.N), dtype=torch.float32, device=dev)
     kl_rows = torch.empty((w.B, w.Hkv, w.N), dtype=torch.float32, device=dev)
     kl_loss = torch.empty((), dtype=torch.float32, device=dev)
-    ws = {op: api.new_workspace(sh, op, dev) for op in range(4 if w.train else 2)}
+    ws = {op: api.new_workspace(sh, op, dev) for op in range(3 if w.train else 2)}
+    if w.train:
+        ws[3] = api.new_workspace(sh, api.OP_FUSED_BWD_KL, dev)
     grads = tuple(torch.empty_like(d[n]) for n in ("q", "k", "v", "q_idx", "k_idx")) if w.train else None
     stream = torch.cuda.current_stream(dev)
 
@@ -273,11 +279,13 @@ def main():
         api.sparse_attn_fwd(sh, x["q"], x["k"], x["v"], sel, o=o, lse=lse, workspace=ws[1])
         if ev: ev[2].record(stream)
         if w.train:
-            api.kl_fwd(sh, x["q"], x["k"], x["q_idx"], x["k_idx"], sel, lse, 1.0, lse_idx=lse_idx,
-                       kl_rows=kl_rows, kl_loss=kl_loss, workspace=ws[2])
+            # lse_idx first (the backward needs it); the KL loss of the step comes
+            # out of the fused backward, which recomputes the teacher anyway
+            api.kl_fwd(sh, x["q"], x["k"], x["q_idx"], x["k_idx"], sel, lse, 1.0, lse_idx=lse_idx, lse_only=True,
+                       workspace=ws[2])
             if ev: ev[3].record(stream)
             api.fused_bwd(sh, x["q"], x["k"], x["v"], o, x["d_o"], lse, x["q_idx"], x["k_idx"], sel, lse_idx, 1.0,
-                          grads=grads, workspace=ws[3])
+                          grads=grads, with_kl=True, kl_rows=kl_rows, kl_loss=kl_loss, workspace=ws[3])
             if ev: ev[4].record(stream)
 
     for _ in range(args.warmup):

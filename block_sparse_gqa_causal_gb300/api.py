@@ -19,10 +19,11 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmsa.so")
 
-OP_INDEX_SELECT, OP_SPARSE_ATTN_FWD, OP_KL_FWD, OP_FUSED_BWD = 0, 1, 2, 3
+OP_INDEX_SELECT, OP_SPARSE_ATTN_FWD, OP_KL_FWD, OP_FUSED_BWD, OP_FUSED_BWD_KL = 0, 1, 2, 3, 4
 STATUS = {0: "MSA_OK", 1: "MSA_ERR_INVALID_ARGUMENT", 2: "MSA_ERR_UNSUPPORTED", 3: "MSA_ERR_WORKSPACE",
           4: "MSA_ERR_CUDA", 5: "MSA_ERR_TIMEOUT", 6: "MSA_ERR_DEVICE"}
 EXPORTS = ("msa_workspace_size", "msa_index_select", "msa_sparse_attn_fwd", "msa_kl_fwd", "msa_fused_bwd",
+           "msa_fused_bwd_kl",
            "msa_last_error", "msa_check_device_status", "msa_version", "msa_launch_count")
 
 
@@ -92,8 +93,9 @@ def lib() -> ctypes.CDLL:
             L.msa_sparse_attn_fwd.argtypes = [S, P, P, P, P, P, P, P, sz, P]
             L.msa_kl_fwd.argtypes = [S, P, P, P, P, P, P, f, P, P, P, P, sz, P]
             L.msa_fused_bwd.argtypes = [S, P, P, P, P, P, P, P, P, P, P, f, P, P, P, P, P, P, sz, P]
+            L.msa_fused_bwd_kl.argtypes = [S, P, P, P, P, P, P, P, P, P, P, f, P, P, P, P, P, P, P, P, sz, P]
             L.msa_check_device_status.argtypes = [P, P]
-            for fn in ("msa_index_select", "msa_sparse_attn_fwd", "msa_kl_fwd", "msa_fused_bwd",
+            for fn in ("msa_index_select", "msa_sparse_attn_fwd", "msa_kl_fwd", "msa_fused_bwd", "msa_fused_bwd_kl",
                        "msa_check_device_status"):
                 getattr(L, fn).restype = ctypes.c_int
             L.msa_last_error.restype = ctypes.c_char_p
@@ -183,8 +185,10 @@ def sparse_attn_fwd(shape: Shape, q, k, v, sel_idx, *, o=None, lse=None, workspa
 
 
 def kl_fwd(shape: Shape, q, k, q_idx, k_idx, sel_idx, lse, kl_coef: float = 1.0, *, lse_idx=None, kl_rows=None,
-           kl_loss=None, want_rows=True, workspace=None, stream=None):
-    """msa_kl_fwd.  Returns (kl_loss scalar tensor, lse_idx [B,Hkv,Nq], kl_rows [B,Hkv,Nq] or None)."""
+           kl_loss=None, want_rows=True, lse_only=False, workspace=None, stream=None):
+    """msa_kl_fwd.  Returns (kl_loss scalar tensor, lse_idx [B,Hkv,Nq], kl_rows [B,Hkv,Nq] or None).
+    lse_only: compute lse_idx alone (kl_loss and kl_rows are None); the
+    training step's form, whose loss then comes from fused_bwd(..., with_kl=True)."""
     s = shape
     _need(q, "q", (s.B, s.Nq, s.Hq, s.d), torch.bfloat16)
     _need(k, "k", (s.B, s.rows_kv, s.Hkv, s.d), torch.bfloat16)
@@ -194,9 +198,12 @@ def kl_fwd(shape: Shape, q, k, q_idx, k_idx, sel_idx, lse, kl_coef: float = 1.0,
     _need(lse, "lse", (s.B, s.Hq, s.Nq), torch.float32)
     dev = q.device
     lse_idx = torch.empty((s.B, s.Hkv, s.Nq), dtype=torch.float32, device=dev) if lse_idx is None else lse_idx
-    if want_rows and kl_rows is None:
-        kl_rows = torch.empty((s.B, s.Hkv, s.Nq), dtype=torch.float32, device=dev)
-    kl_loss = torch.empty((), dtype=torch.float32, device=dev) if kl_loss is None else kl_loss
+    if lse_only:
+        kl_rows = kl_loss = None
+    else:
+        if want_rows and kl_rows is None:
+            kl_rows = torch.empty((s.B, s.Hkv, s.Nq), dtype=torch.float32, device=dev)
+        kl_loss = torch.empty((), dtype=torch.float32, device=dev) if kl_loss is None else kl_loss
     ws = _ws(workspace, s, OP_KL_FWD, dev)
     _check(lib().msa_kl_fwd(ctypes.byref(s.c()), _ptr(q), _ptr(k), _ptr(q_idx), _ptr(k_idx), _ptr(sel_idx),
                             _ptr(lse), ctypes.c_float(kl_coef), _ptr(lse_idx), _ptr(kl_rows), _ptr(kl_loss),
@@ -205,8 +212,11 @@ def kl_fwd(shape: Shape, q, k, q_idx, k_idx, sel_idx, lse, kl_coef: float = 1.0,
 
 
 def fused_bwd(shape: Shape, q, k, v, o, d_o, lse, q_idx, k_idx, sel_idx, lse_idx, kl_coef: float = 1.0, *,
-              grads=None, workspace=None, stream=None):
-    """msa_fused_bwd.  Returns (dq, dk, dv, dq_idx, dk_idx) bf16."""
+              grads=None, with_kl=False, kl_rows=None, kl_loss=None, workspace=None, stream=None):
+    """msa_fused_bwd.  Returns (dq, dk, dv, dq_idx, dk_idx) bf16.
+    with_kl: msa_fused_bwd_kl, which also gives the step's KL loss; returns
+    (dq, dk, dv, dq_idx, dk_idx, kl_loss, kl_rows), kl_rows None unless a
+    [B,Hkv,Nq] fp32 tensor is passed for it."""
     s = shape
     for t, n, shp in ((q, "q", (s.B, s.Nq, s.Hq, s.d)), (o, "o", (s.B, s.Nq, s.Hq, s.d)),
                       (d_o, "d_o", (s.B, s.Nq, s.Hq, s.d)), (k, "k", (s.B, s.Nk, s.Hkv, s.d)),
@@ -219,6 +229,16 @@ def fused_bwd(shape: Shape, q, k, v, o, d_o, lse, q_idx, k_idx, sel_idx, lse_idx
     if grads is None:
         grads = tuple(torch.empty_like(t) for t in (q, k, v, q_idx, k_idx))
     dq, dk, dv, dqi, dki = grads
+    if with_kl:
+        kl_loss = torch.empty((), dtype=torch.float32, device=q.device) if kl_loss is None else kl_loss
+        if kl_rows is not None:
+            _need(kl_rows, "kl_rows", (s.B, s.Hkv, s.Nq), torch.float32)
+        ws = _ws(workspace, s, OP_FUSED_BWD_KL, q.device)
+        _check(lib().msa_fused_bwd_kl(ctypes.byref(s.c()), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(d_o), _ptr(lse),
+                                      _ptr(q_idx), _ptr(k_idx), _ptr(sel_idx), _ptr(lse_idx), ctypes.c_float(kl_coef),
+                                      _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dqi), _ptr(dki), _ptr(kl_rows), _ptr(kl_loss),
+                                      _ptr(ws), ws.numel(), _stream(stream)))
+        return dq, dk, dv, dqi, dki, kl_loss, kl_rows
     ws = _ws(workspace, s, OP_FUSED_BWD, q.device)
     _check(lib().msa_fused_bwd(ctypes.byref(s.c()), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(d_o), _ptr(lse),
                                _ptr(q_idx), _ptr(k_idx), _ptr(sel_idx), _ptr(lse_idx), ctypes.c_float(kl_coef),

@@ -149,6 +149,16 @@ size_t bwd_bytes(const Problem &p)
     return n;
 }
 
+// KL of the fused backward: rows (when the caller gives none) and either the
+// per-slot partials of the tensor-core backward or the KL forward's own
+// scratch (with an lse_idx it recomputes)
+size_t bwdkl_bytes(const Problem &p)
+{
+    const size_t rows = (size_t)p.B * p.Hkv * p.Nq;
+    if (bwd_tc(p)) return klrows_bytes(p) + 2 * align256(rows * p.topk * 16);
+    return klrows_bytes(p) + kl_bytes(p) + align256(rows * 4);
+}
+
 #define REQUIRE_PTR(ptr, name)                                                                         \
     do {                                                                                               \
         if (!(ptr)) return fail(MSA_ERR_INVALID_ARGUMENT, "%s is NULL", name);                         \
@@ -258,6 +268,7 @@ size_t msa_workspace_size(const msa_shape *shape, int op)
     case MSA_OP_SPARSE_ATTN_FWD: return kStatusBytes + fwd_bytes(p);
     case MSA_OP_KL_FWD: return kStatusBytes + klrows_bytes(p) + kl_bytes(p);
     case MSA_OP_FUSED_BWD: return kStatusBytes + bwd_bytes(p);
+    case MSA_OP_FUSED_BWD_KL: return kStatusBytes + bwd_bytes(p) + bwdkl_bytes(p);
     default: fail(MSA_ERR_INVALID_ARGUMENT, "unknown op %d", op); return 0;
     }
 }
@@ -320,6 +331,39 @@ msa_status msa_sparse_attn_fwd(const msa_shape *shape, const void *q, const void
     return MSA_OK;
 }
 
+}  // extern "C"
+
+namespace {
+// KL forward on carved workspace.  rows == nullptr: lse_idx only (no teacher
+// pass, key-major path; the fallback path computes rows into `scratch_rows`).
+// kl_loss == nullptr: no reduction.
+cudaError_t kl_forward(const Problem &p, const void *q, const void *k, const void *q_idx, const void *k_idx,
+                       const int32_t *sel_idx, const float *lse, float kl_coef, float *lse_idx, float *rows,
+                       float *scratch_rows, float *kl_loss, Carve &cv, DeviceStatus *ds, cudaStream_t s)
+{
+    cudaError_t e;
+    if (fwd_keymajor(p)) {
+        KlWork w;
+        w.part = cv.take<float4>(kl_part_count(p));
+        __half *pt = cv.take<__half>((size_t)p.B * p.Hkv * p.Nq * p.topk * 128);
+        w.pt = rows ? pt : nullptr;
+        carve_index(cv, p, w);
+        e = launch_kl_keymajor(p, static_cast<const bf16 *>(q), static_cast<const bf16 *>(k),
+                               static_cast<const bf16 *>(q_idx), static_cast<const bf16 *>(k_idx), sel_idx, lse,
+                               lse_idx, rows, w, ds, s);
+    } else {
+        if (!rows) rows = scratch_rows;
+        e = launch_kl_fwd(p, static_cast<const bf16 *>(q), static_cast<const bf16 *>(k),
+                          static_cast<const bf16 *>(q_idx), static_cast<const bf16 *>(k_idx), sel_idx, lse, lse_idx,
+                          rows, ds, s);
+    }
+    if (e != cudaSuccess || !kl_loss) return e;
+    return launch_kl_reduce(p, rows, kl_coef, kl_loss, s);
+}
+}  // namespace
+
+extern "C" {
+
 msa_status msa_kl_fwd(const msa_shape *shape, const void *q, const void *k, const void *q_idx, const void *k_idx,
                       const int32_t *sel_idx, const float *lse, float kl_coef, float *lse_idx, float *kl_rows,
                       float *kl_loss, void *workspace, size_t workspace_bytes, void *stream)
@@ -331,39 +375,30 @@ msa_status msa_kl_fwd(const msa_shape *shape, const void *q, const void *k, cons
     REQUIRE_PTR(k, "k");
     REQUIRE_PTR(q_idx, "q_idx");
     REQUIRE_PTR(k_idx, "k_idx");
-    if (!sel_idx || !lse || !lse_idx || !kl_loss)
-        return fail(MSA_ERR_INVALID_ARGUMENT, "sel_idx, lse, lse_idx and kl_loss must be non-NULL");
+    if (!sel_idx || !lse || !lse_idx) return fail(MSA_ERR_INVALID_ARGUMENT, "sel_idx, lse and lse_idx must be non-NULL");
+    const bool lse_only = !kl_rows && !kl_loss;
+    if (!lse_only && !kl_loss)
+        return fail(MSA_ERR_INVALID_ARGUMENT, "kl_loss is NULL (pass kl_rows and kl_loss both NULL for lse_idx only)");
     if (!isfinite(kl_coef)) return fail(MSA_ERR_INVALID_ARGUMENT, "kl_coef must be finite");
     st = check_ws(workspace, workspace_bytes, kStatusBytes + (kl_rows ? 0 : klrows_bytes(p)) + kl_bytes(p));
     if (st != MSA_OK) return st;
     Carve cv{static_cast<char *>(workspace)};
-    float *rows = kl_rows ? kl_rows : cv.take<float>((size_t)p.B * p.Hkv * p.Nq);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    DeviceStatus *ds = static_cast<DeviceStatus *>(workspace);
-    cudaError_t e;
-    if (fwd_keymajor(p)) {
-        KlWork w;
-        w.part = cv.take<float4>(kl_part_count(p));
-        w.pt = cv.take<__half>((size_t)p.B * p.Hkv * p.Nq * p.topk * 128);
-        carve_index(cv, p, w);
-        e = launch_kl_keymajor(p, static_cast<const bf16 *>(q), static_cast<const bf16 *>(k),
-                               static_cast<const bf16 *>(q_idx), static_cast<const bf16 *>(k_idx), sel_idx, lse,
-                               lse_idx, rows, w, ds, s);
-    } else {
-        e = launch_kl_fwd(p, static_cast<const bf16 *>(q), static_cast<const bf16 *>(k),
-                          static_cast<const bf16 *>(q_idx), static_cast<const bf16 *>(k_idx), sel_idx, lse, lse_idx,
-                          rows, ds, s);
-    }
+    float *scratch = kl_rows ? nullptr : cv.take<float>((size_t)p.B * p.Hkv * p.Nq);
+    float *rows = kl_rows ? kl_rows : (lse_only ? nullptr : scratch);
+    cudaError_t e = kl_forward(p, q, k, q_idx, k_idx, sel_idx, lse, kl_coef, lse_idx, rows, scratch, kl_loss, cv,
+                               static_cast<DeviceStatus *>(workspace), static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "kl_fwd launch");
-    e = launch_kl_reduce(p, rows, kl_coef, kl_loss, s);
-    if (e != cudaSuccess) return cuda_fail(e, "kl_reduce launch");
     return MSA_OK;
 }
 
-msa_status msa_fused_bwd(const msa_shape *shape, const void *q, const void *k, const void *v, const void *o,
-                         const void *d_o, const float *lse, const void *q_idx, const void *k_idx,
-                         const int32_t *sel_idx, const float *lse_idx, float kl_coef, void *dq, void *dk, void *dv,
-                         void *dq_idx, void *dk_idx, void *workspace, size_t workspace_bytes, void *stream)
+}  // extern "C"
+
+namespace {
+msa_status fused_bwd_impl(const msa_shape *shape, const void *q, const void *k, const void *v, const void *o,
+                          const void *d_o, const float *lse, const void *q_idx, const void *k_idx,
+                          const int32_t *sel_idx, const float *lse_idx, float kl_coef, void *dq, void *dk, void *dv,
+                          void *dq_idx, void *dk_idx, bool with_kl, float *kl_rows, float *kl_loss, void *workspace,
+                          size_t workspace_bytes, void *stream)
 {
     Problem p;
     msa_status st = make_problem(shape, p);
@@ -383,10 +418,13 @@ msa_status msa_fused_bwd(const msa_shape *shape, const void *q, const void *k, c
     REQUIRE_PTR(dq_idx, "dq_idx");
     REQUIRE_PTR(dk_idx, "dk_idx");
     if (!sel_idx || !lse || !lse_idx) return fail(MSA_ERR_INVALID_ARGUMENT, "sel_idx, lse and lse_idx must be non-NULL");
+    if (with_kl && !kl_loss) return fail(MSA_ERR_INVALID_ARGUMENT, "kl_loss is NULL");
     if (!isfinite(kl_coef)) return fail(MSA_ERR_INVALID_ARGUMENT, "kl_coef must be finite");
-    st = check_ws(workspace, workspace_bytes, kStatusBytes + bwd_bytes(p));
+    st = check_ws(workspace, workspace_bytes, kStatusBytes + bwd_bytes(p) + (with_kl ? bwdkl_bytes(p) : 0));
     if (st != MSA_OK) return st;
     Carve cv{static_cast<char *>(workspace)};
+    DeviceStatus *ds = static_cast<DeviceStatus *>(workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
     BwdWork w{};
     w.D = cv.take<float>((size_t)p.B * p.Hq * p.Nq);
     w.dki_acc = cv.take<float>((size_t)p.B * p.Nk * p.d_idx);
@@ -401,15 +439,52 @@ msa_status msa_fused_bwd(const msa_shape *shape, const void *q, const void *k, c
         w.dq_acc = cv.take<float>((size_t)p.B * p.Nq * p.Hq * p.d);
         w.dqi_acc = cv.take<float>((size_t)p.B * p.Nq * p.Hkv * p.d_idx);
     }
-    cudaError_t e = launch_fused_bwd(p, static_cast<const bf16 *>(q), static_cast<const bf16 *>(k),
-                                     static_cast<const bf16 *>(v), static_cast<const bf16 *>(o),
-                                     static_cast<const bf16 *>(d_o), lse, static_cast<const bf16 *>(q_idx),
-                                     static_cast<const bf16 *>(k_idx), sel_idx, lse_idx, kl_coef,
-                                     static_cast<bf16 *>(dq), static_cast<bf16 *>(dk), static_cast<bf16 *>(dv),
-                                     static_cast<bf16 *>(dq_idx), static_cast<bf16 *>(dk_idx), w,
-                                     static_cast<DeviceStatus *>(workspace), static_cast<cudaStream_t>(stream));
+    float *rows = nullptr;
+    cudaError_t e;
+    if (with_kl) {
+        rows = kl_rows ? kl_rows : cv.take<float>((size_t)p.B * p.Hkv * p.Nq);
+        if (bwd_tc(p)) {
+            w.kla = cv.take<float>(slots * p.Hkv * 4);
+            w.klb = cv.take<float>(slots * p.Hkv * 4);
+            w.kl_rows = rows;
+        } else {
+            // no tensor-core backward: the KL forward's passes give the rows
+            float *lse_scratch = cv.take<float>((size_t)p.B * p.Hkv * p.Nq);
+            e = kl_forward(p, q, k, q_idx, k_idx, sel_idx, lse, kl_coef, lse_scratch, rows, rows, nullptr, cv, ds, s);
+            if (e != cudaSuccess) return cuda_fail(e, "fused_bwd_kl: KL passes");
+        }
+    }
+    e = launch_fused_bwd(p, static_cast<const bf16 *>(q), static_cast<const bf16 *>(k), static_cast<const bf16 *>(v),
+                         static_cast<const bf16 *>(o), static_cast<const bf16 *>(d_o), lse,
+                         static_cast<const bf16 *>(q_idx), static_cast<const bf16 *>(k_idx), sel_idx, lse_idx, kl_coef,
+                         static_cast<bf16 *>(dq), static_cast<bf16 *>(dk), static_cast<bf16 *>(dv),
+                         static_cast<bf16 *>(dq_idx), static_cast<bf16 *>(dk_idx), w, ds, s);
     if (e != cudaSuccess) return cuda_fail(e, "fused_bwd launch");
+    if (with_kl && (e = launch_kl_reduce(p, rows, kl_coef, kl_loss, s)) != cudaSuccess)
+        return cuda_fail(e, "kl_reduce launch");
     return MSA_OK;
+}
+}  // namespace
+
+extern "C" {
+
+msa_status msa_fused_bwd(const msa_shape *shape, const void *q, const void *k, const void *v, const void *o,
+                         const void *d_o, const float *lse, const void *q_idx, const void *k_idx,
+                         const int32_t *sel_idx, const float *lse_idx, float kl_coef, void *dq, void *dk, void *dv,
+                         void *dq_idx, void *dk_idx, void *workspace, size_t workspace_bytes, void *stream)
+{
+    return fused_bwd_impl(shape, q, k, v, o, d_o, lse, q_idx, k_idx, sel_idx, lse_idx, kl_coef, dq, dk, dv, dq_idx,
+                          dk_idx, false, nullptr, nullptr, workspace, workspace_bytes, stream);
+}
+
+msa_status msa_fused_bwd_kl(const msa_shape *shape, const void *q, const void *k, const void *v, const void *o,
+                            const void *d_o, const float *lse, const void *q_idx, const void *k_idx,
+                            const int32_t *sel_idx, const float *lse_idx, float kl_coef, void *dq, void *dk, void *dv,
+                            void *dq_idx, void *dk_idx, float *kl_rows, float *kl_loss, void *workspace,
+                            size_t workspace_bytes, void *stream)
+{
+    return fused_bwd_impl(shape, q, k, v, o, d_o, lse, q_idx, k_idx, sel_idx, lse_idx, kl_coef, dq, dk, dv, dq_idx,
+                          dk_idx, true, kl_rows, kl_loss, workspace, workspace_bytes, stream);
 }
 
 msa_status msa_check_device_status(void *workspace, void *stream)

@@ -16,7 +16,10 @@
 // dq_idx leaves as bf16 partial rows per (query, group, slot), summed by the
 // combine kernel; dK_idx (shared by all groups) is added to an fp32 buffer
 // once per CTA.  coef = kl_coef / (B * Nq * Hkv), the mean over (query,
-// group) rows of the per-row KL.
+// group) rows of the per-row KL.  When asked for the loss, the same tile
+// also gives sum_j Pt_j s_j log2(e) of each (query, group, selected block),
+// one partial per lane quarter of keys (a transposing warp sum), which with
+// the main branch's sum of Pt log2 Pt and lse_idx makes the KL of each row.
 //
 // Roles: warp 0 gathers q_idx rows (cp.async) and row data, warp 1 owns TMEM
 // and issues the MMAs, warps 2..9 are the epilogue (TMEM lanes 32*(w%4)..,
@@ -77,7 +80,8 @@ bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, cons
                     const float *__restrict__ lse_idx, float coef, const int32_t *__restrict__ bucket_off,
                     const int32_t *__restrict__ bucket_q, const __half *__restrict__ pt,
                     const int32_t *__restrict__ pt_off,
-                    bf16 *__restrict__ dqi_part, float *__restrict__ dki_acc, DeviceStatus *st)
+                    bf16 *__restrict__ dqi_part, float *__restrict__ dki_acc, float *__restrict__ klb,
+                    DeviceStatus *st)
 {
     const int r = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
     const long long bucket = ((long long)b * p.Hkv + r) * p.nb + c;
@@ -314,11 +318,12 @@ bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, cons
             uint32_t s0[32], s1[32];
             tc::tmem_ld32_nowait(tmem + lane_base + TM_S + sb * kQ + cb, s0);
             tc::tmem_ld32_nowait(tmem + lane_base + TM_S + sb * kQ + cb + 32, s1);
-            long long rp_cur[2];
+            long long rp_cur[2], kl_cur[2];
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
                 const int u = cb + 32 * t + lane;
                 rp_cur[t] = u < nq ? (((long long)b * p.Nq + meta->qi[u]) * p.Hkv + r) * p.topk + meta->slot[u] : -1;
+                kl_cur[t] = u < nq ? (((long long)b * p.Hkv + r) * p.Nq + meta->qi[u]) * p.topk + meta->slot[u] : -1;
             }
             tc::tmem_wait32(s0);
             tc::tmem_wait32(s1);
@@ -327,24 +332,34 @@ bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, cons
             if (lane == 0) tc::mbar_arrive(&s_free[sb]);
             uint32_t sg[32];
 #pragma unroll
-            for (int cc = 0; cc < 64; cc += 4) {
-                const float4 l4 = *reinterpret_cast<const float4 *>(meta->lsei2 + cb + cc);
-                const int4 p4 = *reinterpret_cast<const int4 *>(meta->pos + cb + cc);
-                const float l2[4] = {l4.x, l4.y, l4.z, l4.w};
-                const int ps[4] = {p4.x, p4.y, p4.z, p4.w};
-                float g2[4];
+            for (int t = 0; t < 2; ++t) {
+                float bs[32];                       // Pt s log2(e) per query column (KL partial)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int col = cc + e;
-                    const float sv = __uint_as_float(col < 32 ? s0[col] : s1[col - 32]);
-                    const bool vis = key_ok && j <= (long long)ps[e];
-                    const __half2 h2 = *reinterpret_cast<const __half2 *>(
-                        reinterpret_cast<const uint32_t *>(&tv[col >> 3]) + ((col & 7) >> 1));
-                    const float ptv = (col & 1) ? __high2float(h2) : __low2float(h2);
-                    g2[e] = vis ? coef * (tc::ex2(sv * si2 - l2[e]) - ptv) : 0.f;
+                for (int cc = 32 * t; cc < 32 * t + 32; cc += 4) {
+                    const float4 l4 = *reinterpret_cast<const float4 *>(meta->lsei2 + cb + cc);
+                    const int4 p4 = *reinterpret_cast<const int4 *>(meta->pos + cb + cc);
+                    const float l2[4] = {l4.x, l4.y, l4.z, l4.w};
+                    const int ps[4] = {p4.x, p4.y, p4.z, p4.w};
+                    float g2[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int col = cc + e;
+                        const float sv = __uint_as_float(col < 32 ? s0[col] : s1[col - 32]);
+                        const bool vis = key_ok && j <= (long long)ps[e];
+                        const __half2 h2 = *reinterpret_cast<const __half2 *>(
+                            reinterpret_cast<const uint32_t *>(&tv[col >> 3]) + ((col & 7) >> 1));
+                        const float ptv = (col & 1) ? __high2float(h2) : __low2float(h2);
+                        g2[e] = vis ? coef * (tc::ex2(sv * si2 - l2[e]) - ptv) : 0.f;
+                        bs[col & 31] = vis ? ptv * (sv * si2) : 0.f;
+                    }
+                    sg[cc / 2] = pack_bf16(g2[0], g2[1]);
+                    sg[cc / 2 + 1] = pack_bf16(g2[2], g2[3]);
                 }
-                sg[cc / 2] = pack_bf16(g2[0], g2[1]);
-                sg[cc / 2 + 1] = pack_bf16(g2[2], g2[3]);
+                if (klb) {
+                    float tot[1];
+                    lane_colsum(bs, lane, tot);             // lane l: column cb + 32 t + l
+                    if (kl_cur[t] >= 0) klb[kl_cur[t] * 4 + qd] = tot[0];
+                }
             }
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&empty[s]);   // the stage's row data is no longer read
@@ -409,7 +424,8 @@ cudaError_t launch_bwd_index_tc(const Problem &p, const bf16 *q_idx, const bf16 
     {
         TimedLaunch timed_("bwd_index_tc_kernel", s);
         bwd_index_tc_kernel<<<dim3(p.Hkv, p.nb, p.B), kThreads, ALLOC, s>>>(tki, p, q_idx, lse_idx, coef, w.bucket_off,
-                                                                           w.bucket_q, w.pt, w.pt_off, w.dqi_part, w.dki_acc, st);
+                                                                           w.bucket_q, w.pt, w.pt_off, w.dqi_part, w.dki_acc,
+                                                                           w.klb, st);
     }
     note_launch();
     return cudaGetLastError();

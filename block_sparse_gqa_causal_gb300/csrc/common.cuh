@@ -47,6 +47,33 @@ MSA_DEV float2 unpack_bf16(uint32_t x)
 
 MSA_DEV uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
+// ------------------------------------------------------------------ warp sums
+// Column sums across a warp.  Each lane holds v[0..N), one value per column;
+// afterwards out[h] on lane l is the sum over all 32 lanes of column
+// (l mod min(N, 32)) + 32 h.  Each exchange step halves the per-lane array:
+// a lane keeps the columns whose next index bit equals its own lane bit and
+// adds in its partner's copy of them (N - 1 shuffles for N <= 32, where the
+// remaining lane bits are then summed by xor steps).  v is overwritten.
+template <int N>
+MSA_DEV void lane_colsum(float (&v)[N], int lane, float (&out)[(N + 31) / 32])
+{
+    static_assert(N >= 1 && (N & (N - 1)) == 0 && N <= 64, "N must be a power of two up to 64");
+    constexpr int W = N < 32 ? N : 32;
+#pragma unroll
+    for (int o = 1; o < W; o <<= 1) {
+        const bool hi = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < N / (2 * o); ++i) {
+            const float a = v[2 * i], c = v[2 * i + 1];
+            v[i] = (hi ? c : a) + __shfl_xor_sync(0xffffffffu, hi ? a : c, o);
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < (N + 31) / 32; ++h) out[h] = v[h];
+#pragma unroll
+    for (int o = W; o < 32; o <<= 1) out[0] += __shfl_xor_sync(0xffffffffu, out[0], o);
+}
+
 // ------------------------------------------------------------------ cp.async
 MSA_DEV void cp_async16(void *smem, const void *gmem)
 {

@@ -616,6 +616,7 @@ cudaError_t launch_fused_bwd(const Problem &p, const bf16 *q, const bf16 *k, con
         // main branch first: it leaves the teacher per (bucket entry, key) for the index branch
         if ((e = launch_bwd_main_tc(p, q, k, v, d_o, lse, w, dk, dv, st, s)) != cudaSuccess) return e;
         if ((e = launch_bwd_index_tc(p, q_idx, k_idx, lse_idx, kl_coef, w, st, s)) != cudaSuccess) return e;
+        if (w.kla && (e = launch_bwd_kl_combine(p, sel, lse_idx, w.kla, w.klb, w.kl_rows, s)) != cudaSuccess) return e;
         {
             TimedLaunch timed_("bwd_combine_kernel", s);
             bwd_combine_kernel<128><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p, sel, w.dq_part, dq, p.Hq, p.G);

@@ -18,6 +18,11 @@
 //     per (query, group, selected block, half of the keys).
 // A combine kernel folds a row's partials in a fixed order, so the loss is
 // reproducible and nothing is accumulated with atomics.
+//
+// Training runs only the index pass without the teacher (max and sum of
+// 2^s2, i.e. lse_idx, which the backward needs first): the fused backward
+// recomputes the teacher anyway and folds the two teacher sums of the loss
+// into its own tiles, and bwd_kl_combine_kernel below assembles the rows.
 #include <cuda_fp16.h>
 
 #include "msa_internal.h"
@@ -343,7 +348,7 @@ struct IndexLayout {
     static constexpr int ALLOC = OFF_BAR + 256 + 1024;
 };
 
-template <int DI>
+template <int DI, bool kTeacher>
 __global__ void __launch_bounds__(kThreads, 1)
 kl_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, const bf16 *__restrict__ q_idx,
                    const int32_t *__restrict__ bucket_off, const int32_t *__restrict__ bucket_q,
@@ -477,9 +482,11 @@ kl_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, const
             const int qi = meta->qi[u], slot = meta->slot[u];
             // the teacher's 64 values for this query and key half
             uint4 tv[8];
-            const uint4 *src = reinterpret_cast<const uint4 *>(pt + (long long)(e0 + (valid ? u : 0)) * kKeys + hf * 64);
+            if constexpr (kTeacher) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(pt + (long long)(e0 + (valid ? u : 0)) * kKeys + hf * 64);
 #pragma unroll
-            for (int x = 0; x < 8; ++x) tv[x] = valid ? __ldg(src + x) : make_uint4(0, 0, 0, 0);
+                for (int x = 0; x < 8; ++x) tv[x] = valid ? __ldg(src + x) : make_uint4(0, 0, 0, 0);
+            }
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&empty[n % kStages]);   // row data read
             if (!wwait(&s_full[n & 1], (uint32_t)(n >> 1) & 1u, st, 94, abort_flag)) break;
@@ -501,7 +508,13 @@ kl_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, const
             float A = 0.f, Bv = 0.f, Z = 0.f;
 #pragma unroll
             for (int x = 0; x < 64; x += 8) {
-                const uint32_t w4[4] = {tv[x / 8].x, tv[x / 8].y, tv[x / 8].z, tv[x / 8].w};
+                uint32_t w4[4] = {0u, 0u, 0u, 0u};
+                if constexpr (kTeacher) {
+                    w4[0] = tv[x / 8].x;
+                    w4[1] = tv[x / 8].y;
+                    w4[2] = tv[x / 8].z;
+                    w4[3] = tv[x / 8].w;
+                }
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int col = x + e;
@@ -510,8 +523,10 @@ kl_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, const
                     const float ptv = (e & 1) ? __high2float(h2) : __low2float(h2);
                     if (col < nvis) {
                         Z += tc::ex2(s2 - M);
-                        Bv += ptv * s2;
-                        A += ptv > 0.f ? ptv * tc::lg2(ptv) : 0.f;
+                        if constexpr (kTeacher) {
+                            Bv += ptv * s2;
+                            A += ptv > 0.f ? ptv * tc::lg2(ptv) : 0.f;
+                        }
                     }
                 }
             }
@@ -562,7 +577,29 @@ __global__ void kl_combine_kernel(Problem p, const int32_t *__restrict__ sel, co
     }
     const float lse2 = M + log2f(Z);
     lse_idx[row] = lse2 * kLn2;
-    kl_rows[row] = (A - Bv + lse2) * kLn2;
+    if (kl_rows) kl_rows[row] = (A - Bv + lse2) * kLn2;
+}
+
+// KL of each (query, group) row from the fused backward's partials: per valid
+// slot four key-quarter sums of Pt log2 Pt (kla) and of Pt s log2 e (klb);
+// KL = (A - B) ln 2 + lse_idx.  Fixed order, no atomics.
+__global__ void bwd_kl_combine_kernel(Problem p, const int32_t *__restrict__ sel, const float *__restrict__ lse_idx,
+                                      const float4 *__restrict__ kla, const float4 *__restrict__ klb,
+                                      float *__restrict__ kl_rows)
+{
+    const long long row = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (row >= (long long)p.B * p.Hkv * p.Nq) return;
+    const long long pos = (long long)p.q_offset + (row % p.Nq);
+    const int32_t *srow = sel + row * p.topk;
+    float A = 0.f, Bv = 0.f;
+    for (int t = 0; t < p.topk; ++t) {
+        const int cc = srow[t];
+        if (cc < 0 || cc >= p.nb || (long long)cc * 128 > pos) continue;
+        const float4 a = kla[row * p.topk + t], b = klb[row * p.topk + t];
+        A += (a.x + a.y) + (a.z + a.w);
+        Bv += (b.x + b.y) + (b.z + b.w);
+    }
+    kl_rows[row] = (A - Bv) * kLn2 + lse_idx[row];
 }
 
 template <int D, int G>
@@ -610,12 +647,13 @@ cudaError_t launch_teacher_d(const Problem &p, const bf16 *q, const bf16 *k, con
     }
 }
 
-template <int DI>
+template <int DI, bool kTeacher>
 cudaError_t launch_index(const Problem &p, const bf16 *q_idx, const bf16 *k_idx, const KlWork &w, DeviceStatus *st,
                          cudaStream_t s)
 {
     using L = IndexLayout<DI>;
-    cudaError_t e = cudaFuncSetAttribute(kl_index_tc_kernel<DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+    cudaError_t e =
+        cudaFuncSetAttribute(kl_index_tc_kernel<DI, kTeacher>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
     CUtensorMap tki;
     const unsigned long long di[3] = {(unsigned long long)DI, (unsigned long long)p.Nk, (unsigned long long)p.B};
@@ -624,8 +662,8 @@ cudaError_t launch_index(const Problem &p, const bf16 *q_idx, const bf16 *k_idx,
     if ((e = make_tmap_bf16(&tki, k_idx, 3, di, si, bi)) != cudaSuccess) return e;
     {
         TimedLaunch timed_("kl_index_tc_kernel", s);
-        kl_index_tc_kernel<DI><<<dim3(p.Hkv, p.nb, p.B), kThreads, L::ALLOC, s>>>(tki, p, q_idx, w.bucket_off,
-                                                                                w.bucket_q, w.pt, w.part, st);
+        kl_index_tc_kernel<DI, kTeacher><<<dim3(p.Hkv, p.nb, p.B), kThreads, L::ALLOC, s>>>(
+            tki, p, q_idx, w.bucket_off, w.bucket_q, w.pt, w.part, st);
     }
     note_launch();
     return cudaGetLastError();
@@ -641,14 +679,34 @@ cudaError_t launch_kl_keymajor(const Problem &p, const bf16 *q, const bf16 *k, c
 {
     cudaError_t e = launch_inverse_index(p, sel, w.bucket_cnt, w.bucket_off, w.bucket_scratch, w.bucket_q, st, s);
     if (e != cudaSuccess) return e;
-    e = p.d == 128 ? launch_teacher_d<128>(p, q, k, lse, w, st, s) : launch_teacher_d<64>(p, q, k, lse, w, st, s);
-    if (e != cudaSuccess) return e;
-    e = p.d_idx == 128 ? launch_index<128>(p, q_idx, k_idx, w, st, s) : launch_index<64>(p, q_idx, k_idx, w, st, s);
+    if (w.pt) {
+        e = p.d == 128 ? launch_teacher_d<128>(p, q, k, lse, w, st, s) : launch_teacher_d<64>(p, q, k, lse, w, st, s);
+        if (e != cudaSuccess) return e;
+        e = p.d_idx == 128 ? launch_index<128, true>(p, q_idx, k_idx, w, st, s)
+                           : launch_index<64, true>(p, q_idx, k_idx, w, st, s);
+    } else {
+        // lse_idx only (kl_rows must be nullptr)
+        e = p.d_idx == 128 ? launch_index<128, false>(p, q_idx, k_idx, w, st, s)
+                           : launch_index<64, false>(p, q_idx, k_idx, w, st, s);
+    }
     if (e != cudaSuccess) return e;
     const long long rows = (long long)p.B * p.Hkv * p.Nq;
     {
         TimedLaunch timed_("kl_combine_kernel", s);
         kl_combine_kernel<<<(unsigned)((rows + 255) / 256), 256, 0, s>>>(p, sel, w.part, lse_idx, kl_rows);
+    }
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_kl_combine(const Problem &p, const int32_t *sel, const float *lse_idx, const float *kla,
+                                  const float *klb, float *kl_rows, cudaStream_t s)
+{
+    const long long rows = (long long)p.B * p.Hkv * p.Nq;
+    {
+        TimedLaunch timed_("bwd_kl_combine_kernel", s);
+        bwd_kl_combine_kernel<<<(unsigned)((rows + 255) / 256), 256, 0, s>>>(
+            p, sel, lse_idx, reinterpret_cast<const float4 *>(kla), reinterpret_cast<const float4 *>(klb), kl_rows);
     }
     note_launch();
     return cudaGetLastError();

@@ -71,7 +71,7 @@ cudaError_t launch_kl_fwd(const Problem &p, const bf16 *q, const bf16 *k, const 
 // Key-major KL forward (many queries per selected block).
 struct KlWork {
     float4 *part;        // [B, Hkv, Nq, topk, kl_part_count / (B*Hkv*Nq*topk)] partial sums
-    __half *pt;          // [B*Hkv*Nq*topk entries, 128] teacher per (bucket entry, key)
+    __half *pt;          // [B*Hkv*Nq*topk entries, 128] teacher per (bucket entry, key); nullptr: lse_idx only
     int32_t *bucket_cnt, *bucket_off, *bucket_scratch, *bucket_q;
 };
 // float4 partials the key-major KL writes (several per (query, group, slot))
@@ -81,6 +81,9 @@ cudaError_t launch_kl_keymajor(const Problem &p, const bf16 *q, const bf16 *k, c
                                DeviceStatus *st, cudaStream_t s);
 cudaError_t launch_kl_reduce(const Problem &p, const float *kl_rows, float kl_coef, float *kl_loss,
                              cudaStream_t s);
+// KL rows from the fused backward's partials (BwdWork::kla / klb) and lse_idx
+cudaError_t launch_bwd_kl_combine(const Problem &p, const int32_t *sel, const float *lse_idx, const float *kla,
+                                  const float *klb, float *kl_rows, cudaStream_t s);
 
 // Backward pieces.  Workspace carve-up is done by the caller (api.cu).
 struct BwdWork {
@@ -95,6 +98,11 @@ struct BwdWork {
     // (tcgen05 path); pt_off[x] = sum over earlier buckets of their counts rounded up to 8
     __half *pt;
     int32_t *pt_off;     // [B*Hkv*nb + 1]
+    // KL loss partials per ((b, r, query), slot) and lane quarter of the block's
+    // keys (tcgen05 path; nullptr when the loss is not asked for):
+    // kla = sum Pt log2 Pt (main-branch backward), klb = sum Pt s log2(e) (index branch)
+    float *kla, *klb;
+    float *kl_rows;      // [B, Hkv, Nq] KL rows assembled from kla / klb (when kla is set)
     int32_t *bucket_cnt; // [B*Hkv*nb]
     int32_t *bucket_off; // [B*Hkv*nb + 1]
     int32_t *bucket_scratch; // inverse_index_scratch_ints(p)

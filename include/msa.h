@@ -82,7 +82,8 @@ enum {
     MSA_OP_INDEX_SELECT = 0,
     MSA_OP_SPARSE_ATTN_FWD = 1,
     MSA_OP_KL_FWD = 2,
-    MSA_OP_FUSED_BWD = 3
+    MSA_OP_FUSED_BWD = 3,
+    MSA_OP_FUSED_BWD_KL = 4
 };
 
 /* Bytes of workspace `op` needs for `shape` (0 on an invalid shape). */
@@ -123,6 +124,8 @@ msa_status msa_sparse_attn_fwd(const msa_shape *shape, const void *q, const void
  *   *kl_loss       = kl_coef / (B Nq Hkv) * sum of kl_rows   (device scalar)
  * kl_rows may be NULL (then it lives in the workspace).  The sum is taken in
  * a fixed order, so kl_loss is reproducible run to run.
+ * With kl_rows and kl_loss both NULL only lse_idx is computed (no teacher
+ * pass): the training step's form, where msa_fused_bwd_kl returns the loss.
  */
 msa_status msa_kl_fwd(const msa_shape *shape, const void *q, const void *k, const void *q_idx,
                       const void *k_idx, const int32_t *sel_idx, const float *lse, float kl_coef,
@@ -145,6 +148,24 @@ msa_status msa_fused_bwd(const msa_shape *shape, const void *q, const void *k, c
                          const void *k_idx, const int32_t *sel_idx, const float *lse_idx, float kl_coef,
                          void *dq, void *dk, void *dv, void *dq_idx, void *dk_idx,
                          void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * msa_fused_bwd plus the KL loss of the same step (section 3.2): the values
+ * msa_kl_fwd would give for kl_rows and *kl_loss (same definitions, same
+ * lse_idx), computed from the backward's own recomputation of the teacher,
+ * so a training step runs msa_kl_fwd in its lse_idx-only form (kl_rows and
+ * kl_loss NULL) and gets the loss here without a separate teacher pass.
+ * kl_loss (device scalar) must be non-NULL; kl_rows may be NULL (then it
+ * lives in the workspace).  Workspace: msa_workspace_size(MSA_OP_FUSED_BWD_KL).
+ * Where the tensor-core backward does not apply (d or d_idx of 64) the loss
+ * is computed by the KL forward's own passes inside this call.
+ */
+msa_status msa_fused_bwd_kl(const msa_shape *shape, const void *q, const void *k, const void *v,
+                            const void *o, const void *d_o, const float *lse, const void *q_idx,
+                            const void *k_idx, const int32_t *sel_idx, const float *lse_idx, float kl_coef,
+                            void *dq, void *dk, void *dv, void *dq_idx, void *dk_idx,
+                            float *kl_rows, float *kl_loss,
+                            void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Index selection without any allocation, for callers that cannot allocate
