@@ -155,7 +155,7 @@ size_t bwd_bytes(const Problem &p)
 size_t bwdkl_bytes(const Problem &p)
 {
     const size_t rows = (size_t)p.B * p.Hkv * p.Nq;
-    if (bwd_tc(p)) return klrows_bytes(p) + 2 * align256(rows * p.topk * 16);
+    if (bwd_tc(p)) return klrows_bytes(p) + align256(rows * p.topk * 4) + align256(rows * p.topk * 16);
     return klrows_bytes(p) + kl_bytes(p) + align256(rows * 4);
 }
 
@@ -444,7 +444,7 @@ msa_status fused_bwd_impl(const msa_shape *shape, const void *q, const void *k, 
     if (with_kl) {
         rows = kl_rows ? kl_rows : cv.take<float>((size_t)p.B * p.Hkv * p.Nq);
         if (bwd_tc(p)) {
-            w.kla = cv.take<float>(slots * p.Hkv * 4);
+            w.kla = cv.take<float>(slots * p.Hkv);
             w.klb = cv.take<float>(slots * p.Hkv * 4);
             w.kl_rows = rows;
         } else {

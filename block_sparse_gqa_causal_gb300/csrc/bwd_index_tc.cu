@@ -16,10 +16,10 @@
 // dq_idx leaves as bf16 partial rows per (query, group, slot), summed by the
 // combine kernel; dK_idx (shared by all groups) is added to an fp32 buffer
 // once per CTA.  coef = kl_coef / (B * Nq * Hkv), the mean over (query,
-// group) rows of the per-row KL.  When asked for the loss, the same tile
-// also gives sum_j Pt_j s_j log2(e) of each (query, group, selected block),
-// one partial per lane quarter of keys (a transposing warp sum), which with
-// the main branch's sum of Pt log2 Pt and lse_idx makes the KL of each row.
+// group) rows of the per-row KL.  The kKL instantiation also gives the loss
+// term sum_j Pt_j s_j log2(e) of each (query, group, selected block), one
+// partial per lane quarter of keys (a transposing warp sum); with the
+// teacher's sum of Pt log2 Pt and lse_idx it makes the KL of each row.
 //
 // Roles: warp 0 gathers q_idx rows (cp.async) and row data, warp 1 owns TMEM
 // and issues the MMAs, warps 2..9 are the epilogue (TMEM lanes 32*(w%4)..,
@@ -75,6 +75,7 @@ __device__ __forceinline__ bool wwait(uint64_t *bar, uint32_t parity, DeviceStat
     return __all_sync(0xffffffffu, r);
 }
 
+template <bool kKL>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, const bf16 *__restrict__ q_idx,
                     const float *__restrict__ lse_idx, float coef, const int32_t *__restrict__ bucket_off,
@@ -333,7 +334,7 @@ bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, cons
             uint32_t sg[32];
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
-                float bs[32];                       // Pt s log2(e) per query column (KL partial)
+                float lv[6];                        // streaming warp sum of Pt s log2(e) (KL partial)
 #pragma unroll
                 for (int cc = 32 * t; cc < 32 * t + 32; cc += 4) {
                     const float4 l4 = *reinterpret_cast<const float4 *>(meta->lsei2 + cb + cc);
@@ -350,15 +351,13 @@ bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, cons
                             reinterpret_cast<const uint32_t *>(&tv[col >> 3]) + ((col & 7) >> 1));
                         const float ptv = (col & 1) ? __high2float(h2) : __low2float(h2);
                         g2[e] = vis ? coef * (tc::ex2(sv * si2 - l2[e]) - ptv) : 0.f;
-                        bs[col & 31] = vis ? ptv * (sv * si2) : 0.f;
+                        if constexpr (kKL) colsum32_push(lv, vis ? ptv * (sv * si2) : 0.f, col & 31, lane);
                     }
                     sg[cc / 2] = pack_bf16(g2[0], g2[1]);
                     sg[cc / 2 + 1] = pack_bf16(g2[2], g2[3]);
                 }
-                if (klb) {
-                    float tot[1];
-                    lane_colsum(bs, lane, tot);             // lane l: column cb + 32 t + l
-                    if (kl_cur[t] >= 0) klb[kl_cur[t] * 4 + qd] = tot[0];
+                if constexpr (kKL) {
+                    if (kl_cur[t] >= 0) klb[kl_cur[t] * 4 + qd] = lv[5];   // lane l: column cb + 32 t + l
                 }
             }
             __syncwarp();
@@ -413,7 +412,8 @@ bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, cons
 cudaError_t launch_bwd_index_tc(const Problem &p, const bf16 *q_idx, const bf16 *k_idx, const float *lse_idx,
                                 float kl_coef, const BwdWork &w, DeviceStatus *st, cudaStream_t s)
 {
-    cudaError_t e = cudaFuncSetAttribute(bwd_index_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ALLOC);
+    auto kern = w.klb ? bwd_index_tc_kernel<true> : bwd_index_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, ALLOC);
     if (e != cudaSuccess) return e;
     CUtensorMap tki;
     const unsigned long long di[3] = {(unsigned long long)DI, (unsigned long long)p.Nk, (unsigned long long)p.B};
@@ -423,7 +423,7 @@ cudaError_t launch_bwd_index_tc(const Problem &p, const bf16 *q_idx, const bf16 
     const float coef = kl_coef / ((float)p.B * (float)p.Nq * (float)p.Hkv);
     {
         TimedLaunch timed_("bwd_index_tc_kernel", s);
-        bwd_index_tc_kernel<<<dim3(p.Hkv, p.nb, p.B), kThreads, ALLOC, s>>>(tki, p, q_idx, lse_idx, coef, w.bucket_off,
+        kern<<<dim3(p.Hkv, p.nb, p.B), kThreads, ALLOC, s>>>(tki, p, q_idx, lse_idx, coef, w.bucket_off,
                                                                            w.bucket_q, w.pt, w.pt_off, w.dqi_part, w.dki_acc,
                                                                            w.klb, st);
     }

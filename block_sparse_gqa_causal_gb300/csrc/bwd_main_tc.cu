@@ -17,10 +17,7 @@
 // pattern of the forward).  The KL teacher (the mean over the group's heads
 // of P) falls out of the same tile: the heads of one query are consecutive
 // columns of a thread's row, so it is a register sum, written as fp16 per
-// (bucket entry, key) for the index-branch backward.  When asked for the KL
-// loss, the same sums also give sum_j Pt_j log2 Pt_j of each (query, group,
-// selected block) -- one partial per lane quarter of keys -- so the loss
-// needs no separate teacher pass.
+// (bucket entry, key) for the index-branch backward (and the KL loss terms).
 //
 // Roles: warps 0 and 11 load (TMA; alternate chunks), warp 1 owns TMEM and
 // issues the score MMAs, warp 10 the gradient MMAs, warps 2..9 are the
@@ -120,7 +117,7 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                    const float *__restrict__ Dg, const int32_t *__restrict__ bucket_off,
                    const int32_t *__restrict__ bucket_q, bf16 *__restrict__ dk, bf16 *__restrict__ dv,
                    bf16 *__restrict__ dq_part, __half *__restrict__ pt_out, const int32_t *__restrict__ pt_off,
-                   float *__restrict__ kla, DeviceStatus *st)
+                   DeviceStatus *st)
 {
     constexpr int QC = kRows / G;                 // queries per chunk
     constexpr int EPL = (QC + 31) / 32;           // bucket entries per producer lane
@@ -423,16 +420,12 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
 #pragma unroll
             for (int u = 0; u < NQH; ++u) pos[u] = meta->pos[cb / G + u];
             const int nq = meta->nq, e0 = meta->e0;
-            long long ridx_cur, kl_cur = -1;
+            long long ridx_cur;
             {
                 const int rho = cb + lane, qq = rho / G, g = rho % G;
                 ridx_cur = qq < nq ? ((((long long)b * p.Nq + meta->qi[qq]) * p.Hq + (long long)r * G + g) * p.topk +
                                       meta->slot[qq])
                                    : -1;
-                // KL partial of query cb/G + lane (lanes < NQH): [(b, r, query), slot][lane quarter]
-                const int qk = cb / G + lane;
-                if (kla && lane < NQH && qk < nq)
-                    kl_cur = (((long long)b * p.Hkv + r) * p.Nq + meta->qi[qk]) * p.topk + meta->slot[qk];
             }
             tc::tmem_wait32(sv);
             tc::tmem_wait32(dp);
@@ -460,17 +453,6 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             }
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&empty[s]);   // done with the stage's row data
-            if (kla) {
-                // this key quarter's sum of Pt log2 Pt for each of the warp's queries
-                float av[NQH], tot[1];
-#pragma unroll
-                for (int u = 0; u < NQH; ++u) {
-                    const float ptv = ptq[u] * invG;
-                    av[u] = ptv > 0.f ? ptv * tc::lg2(ptv) : 0.f;
-                }
-                lane_colsum(av, lane, tot);
-                if (kl_cur >= 0) kla[kl_cur * 4 + qd] = tot[0];
-            }
             {
                 // this key's teacher for the warp's NQH queries (consecutive entries,
                 // 4-aligned): 8 bytes into one 8-entry group, or 16 bytes per group
@@ -599,7 +581,7 @@ cudaError_t launch_g(const Problem &p, const bf16 *q, const bf16 *k, const bf16 
     {
         TimedLaunch timed_("bwd_main_tc_kernel", s);
         bwd_main_tc_kernel<G><<<dim3(p.Hkv, p.nb, p.B), kThreads, ALLOC, s>>>(
-            tq, tdo, tk, tv, p, q, d_o, lse, w.D, w.bucket_off, w.bucket_q, dk, dv, w.dq_part, w.pt, w.pt_off, w.kla, st);
+            tq, tdo, tk, tv, p, q, d_o, lse, w.D, w.bucket_off, w.bucket_q, dk, dv, w.dq_part, w.pt, w.pt_off, st);
     }
     note_launch();
     return cudaGetLastError();

@@ -74,6 +74,34 @@ MSA_DEV void lane_colsum(float (&v)[N], int lane, float (&out)[(N + 31) / 32])
     for (int o = W; o < 32; o <<= 1) out[0] += __shfl_xor_sync(0xffffffffu, out[0], o);
 }
 
+// Streaming form of lane_colsum<32>: feed the values of columns c = 0..31 in
+// order (c a constant after unrolling).  Pairs are combined as soon as both
+// exist, so at most one pending value per level stays live (lv[0..4]); after
+// column 31, lv[5] on lane l holds the sum over the warp of column l.
+MSA_DEV void colsum32_push(float (&lv)[6], float x, int c, int lane)
+{
+    if ((c & 1) == 0) {
+        lv[0] = x;
+        return;
+    }
+    float cur = x;
+#pragma unroll
+    for (int k = 0; k < 5; ++k) {
+        const int o = 1 << k;
+        const bool hi = (lane & o) != 0;
+        const float a = lv[k];
+        cur = (hi ? cur : a) + __shfl_xor_sync(0xffffffffu, hi ? a : cur, o);
+        if (k == 4) {
+            lv[5] = cur;
+            return;
+        }
+        if (((c >> (k + 1)) & 1) == 0) {
+            lv[k + 1] = cur;
+            return;
+        }
+    }
+}
+
 // ------------------------------------------------------------------ cp.async
 MSA_DEV void cp_async16(void *smem, const void *gmem)
 {

@@ -97,6 +97,64 @@ __global__ void __launch_bounds__(256) bwd_rowdot_kernel(Problem p, const bf16 *
     }
 }
 
+// Teacher term of the KL loss (section 3.2, the L_KL equation): for every
+// (query, group, selected block), sum over the block's keys of Pt log2 Pt,
+// read back from the teacher the main-branch backward left per (bucket
+// entry, key) in groups of 8 entries ([group][key][8 entries], fp16).  One
+// CTA per bucket, four groups per step (two 16-byte loads in flight per
+// thread): thread k of a half reads key k's 8 entries of a group, each warp
+// sums its 32 keys per entry with a transposing warp sum, and the four warps
+// of a half add up in shared memory.  Writes kla[((b, r, query), slot)].
+__global__ void __launch_bounds__(256) bwd_teacher_entropy_kernel(Problem p, const int32_t *__restrict__ bucket_off,
+                                                                  const int32_t *__restrict__ bucket_q,
+                                                                  const __half *__restrict__ pt,
+                                                                  const int32_t *__restrict__ pt_off,
+                                                                  float *__restrict__ kla)
+{
+    const int r = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
+    const long long bucket = ((long long)b * p.Hkv + r) * p.nb + c;
+    const int qbeg = bucket_off[bucket], n = bucket_off[bucket + 1] - qbeg;
+    if (n <= 0) return;
+    const long long base = pt_off[bucket];
+    __shared__ float part[2][2][8][8];               // [step parity][sub-step][warp][entry]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int half = threadIdx.x >> 7, key = threadIdx.x & 127;
+    for (int g0 = 0, it = 0; g0 < n; g0 += 32, ++it) {
+        uint4 raw[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int g = g0 + 16 * j + 8 * half;    // this thread's group of 8 entries
+            raw[j] = g < n ? __ldg(reinterpret_cast<const uint4 *>(pt + (base + g) * 128 + key * 8))
+                           : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            float v[8];
+            const __half2 *h = reinterpret_cast<const __half2 *>(&raw[j]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __half22float2(h[e]);
+                v[2 * e] = f.x > 0.f ? f.x * __log2f(f.x) : 0.f;
+                v[2 * e + 1] = f.y > 0.f ? f.y * __log2f(f.y) : 0.f;
+            }
+            float tot[1];
+            lane_colsum(v, lane, tot);               // lane l: entry l % 8 of the warp's 32 keys
+            if (lane < 8) part[it & 1][j][warp][lane] = tot[0];
+        }
+        __syncthreads();                             // the other parity buffer keeps the next step race-free
+        if (threadIdx.x < 32) {
+            const int j = threadIdx.x >> 4, hh = (threadIdx.x >> 3) & 1, e = threadIdx.x & 7;
+            const int t = g0 + 16 * j + 8 * hh + e;
+            if (t < n) {
+                const float a = (part[it & 1][j][4 * hh][e] + part[it & 1][j][4 * hh + 1][e]) +
+                                (part[it & 1][j][4 * hh + 2][e] + part[it & 1][j][4 * hh + 3][e]);
+                const int ent = bucket_q[qbeg + t];
+                kla[(((long long)b * p.Hkv + r) * p.Nq + entry_row(ent)) * p.topk + entry_slot(ent)] = a;
+            }
+        }
+    }
+}
+
 // pt_off[x] = sum over buckets y < x of cnt[y] rounded up to 8 (x = 0..n),
 // single CTA of 1024 threads
 __global__ void __launch_bounds__(1024) bwd_pad_scan_kernel(const int32_t *__restrict__ cnt,
@@ -616,7 +674,15 @@ cudaError_t launch_fused_bwd(const Problem &p, const bf16 *q, const bf16 *k, con
         // main branch first: it leaves the teacher per (bucket entry, key) for the index branch
         if ((e = launch_bwd_main_tc(p, q, k, v, d_o, lse, w, dk, dv, st, s)) != cudaSuccess) return e;
         if ((e = launch_bwd_index_tc(p, q_idx, k_idx, lse_idx, kl_coef, w, st, s)) != cudaSuccess) return e;
-        if (w.kla && (e = launch_bwd_kl_combine(p, sel, lse_idx, w.kla, w.klb, w.kl_rows, s)) != cudaSuccess) return e;
+        if (w.kla) {
+            {
+                TimedLaunch timed_("bwd_teacher_entropy_kernel", s);
+                bwd_teacher_entropy_kernel<<<dim3(p.Hkv, p.nb, p.B), 256, 0, s>>>(p, w.bucket_off, w.bucket_q, w.pt,
+                                                                                 w.pt_off, w.kla);
+            }
+            note_launch();
+            if ((e = launch_bwd_kl_combine(p, sel, lse_idx, w.kla, w.klb, w.kl_rows, s)) != cudaSuccess) return e;
+        }
         {
             TimedLaunch timed_("bwd_combine_kernel", s);
             bwd_combine_kernel<128><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p, sel, w.dq_part, dq, p.Hq, p.G);

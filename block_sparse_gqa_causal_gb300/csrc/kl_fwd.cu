@@ -215,8 +215,17 @@ __global__ void __launch_bounds__(1024) kl_reduce_kernel(const float *__restrict
                                                           float scale, float *__restrict__ out)
 {
     __shared__ double part[1024];
+    // runs of 16 coalesced rows summed in fp32 (4 independent chains), each
+    // run added into a double: few fp64 adds, a fixed order, fp64-level total
     double acc = 0.0;
-    for (long long x = threadIdx.x; x < n; x += 1024) acc += (double)kl_rows[x];
+    long long x = threadIdx.x;
+    for (; x + 15 * 1024 < n; x += 16 * 1024) {
+        float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int u = 0; u < 16; ++u) a[u & 3] += kl_rows[x + (long long)u * 1024];
+        acc += (double)((a[0] + a[1]) + (a[2] + a[3]));
+    }
+    for (; x < n; x += 1024) acc += (double)kl_rows[x];
     part[threadIdx.x] = acc;
     __syncthreads();
     for (int s = 512; s > 0; s >>= 1) {

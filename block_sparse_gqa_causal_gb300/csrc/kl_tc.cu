@@ -581,10 +581,10 @@ __global__ void kl_combine_kernel(Problem p, const int32_t *__restrict__ sel, co
 }
 
 // KL of each (query, group) row from the fused backward's partials: per valid
-// slot four key-quarter sums of Pt log2 Pt (kla) and of Pt s log2 e (klb);
-// KL = (A - B) ln 2 + lse_idx.  Fixed order, no atomics.
+// slot the sum of Pt log2 Pt (kla) and four key-quarter sums of Pt s log2 e
+// (klb); KL = (A - B) ln 2 + lse_idx.  Fixed order, no atomics.
 __global__ void bwd_kl_combine_kernel(Problem p, const int32_t *__restrict__ sel, const float *__restrict__ lse_idx,
-                                      const float4 *__restrict__ kla, const float4 *__restrict__ klb,
+                                      const float *__restrict__ kla, const float4 *__restrict__ klb,
                                       float *__restrict__ kl_rows)
 {
     const long long row = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -595,8 +595,8 @@ __global__ void bwd_kl_combine_kernel(Problem p, const int32_t *__restrict__ sel
     for (int t = 0; t < p.topk; ++t) {
         const int cc = srow[t];
         if (cc < 0 || cc >= p.nb || (long long)cc * 128 > pos) continue;
-        const float4 a = kla[row * p.topk + t], b = klb[row * p.topk + t];
-        A += (a.x + a.y) + (a.z + a.w);
+        const float4 b = klb[row * p.topk + t];
+        A += kla[row * p.topk + t];
         Bv += (b.x + b.y) + (b.z + b.w);
     }
     kl_rows[row] = (A - Bv) * kLn2 + lse_idx[row];
@@ -706,7 +706,7 @@ cudaError_t launch_bwd_kl_combine(const Problem &p, const int32_t *sel, const fl
     {
         TimedLaunch timed_("bwd_kl_combine_kernel", s);
         bwd_kl_combine_kernel<<<(unsigned)((rows + 255) / 256), 256, 0, s>>>(
-            p, sel, lse_idx, reinterpret_cast<const float4 *>(kla), reinterpret_cast<const float4 *>(klb), kl_rows);
+            p, sel, lse_idx, kla, reinterpret_cast<const float4 *>(klb), kl_rows);
     }
     note_launch();
     return cudaGetLastError();

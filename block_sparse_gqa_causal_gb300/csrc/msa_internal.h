@@ -98,9 +98,9 @@ struct BwdWork {
     // (tcgen05 path); pt_off[x] = sum over earlier buckets of their counts rounded up to 8
     __half *pt;
     int32_t *pt_off;     // [B*Hkv*nb + 1]
-    // KL loss partials per ((b, r, query), slot) and lane quarter of the block's
-    // keys (tcgen05 path; nullptr when the loss is not asked for):
-    // kla = sum Pt log2 Pt (main-branch backward), klb = sum Pt s log2(e) (index branch)
+    // KL loss terms per ((b, r, query), slot) (tcgen05 path; nullptr when the
+    // loss is not asked for): kla = sum Pt log2 Pt over the block's keys (one
+    // float), klb = sum Pt s log2(e) per lane quarter of the keys (four floats)
     float *kla, *klb;
     float *kl_rows;      // [B, Hkv, Nq] KL rows assembled from kla / klb (when kla is set)
     int32_t *bucket_cnt; // [B*Hkv*nb]

@@ -219,4 +219,4 @@ def test_fused_bwd_kl_parity(case):
     # the queries inside a block's list (hence of dK / dV accumulation) and the
     # fallback path's fp32 atomics vary run to run
     for a, b, n in zip(res["grads_kl"], res["grads"], ("dq", "dk", "dv", "dq_idx", "dk_idx")):
-        assert_close(a, b, n + " (fused_bwd_kl vs fused_bwd)", max_abs=1e-2, rel_l2=1e-3)
+        assert_close(a, b, n + " (fused_bwd_kl vs fused_bwd)", rel_l2=1e-3, bf16_out=True)
