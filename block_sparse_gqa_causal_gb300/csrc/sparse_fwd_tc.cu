@@ -462,7 +462,7 @@ sparse_fwd_combine_kernel(Problem p, const int32_t *__restrict__ sel, const bf16
 {
     constexpr int LPS = D / 8;                  // lanes per slot row
     constexpr int SPI = 32 / LPS;               // slots per load instruction
-    constexpr int NI = 32 / SPI;
+    constexpr int GI = 16 / SPI;                // load instructions per group of 16 slots
     const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= (long long)p.B * p.Nq * p.Hq) return;
@@ -472,33 +472,45 @@ sparse_fwd_combine_kernel(Problem p, const int32_t *__restrict__ sel, const bf16
     const int r = h / p.G;
     const long long pos = (long long)p.q_offset + i;
     const int32_t *srow = sel + (((long long)b * p.Hkv + r) * p.Nq + i) * p.topk;
+    const uint4 *src = reinterpret_cast<const uint4 *>(part + row * p.topk * D);
+    auto load_group = [&](uint4 (&u)[GI], int g0) {
+#pragma unroll
+        for (int t = 0; t < GI; ++t) {
+            const int s = g0 + t * SPI + lane / LPS;
+            u[t] = s < p.topk ? __ldg(src + s * LPS + lane % LPS) : make_uint4(0, 0, 0, 0);
+        }
+    };
+    // the first 16 slots' partial rows are requested before the selection and
+    // the slot statistics arrive (invalid slots are masked below, their bytes
+    // never written), so a row costs one memory round trip
+    uint4 u[GI];
+    load_group(u, 0);
+    const float2 mz_raw = lane < p.topk ? __ldg(stats + row * p.topk + lane) : make_float2(-INFINITY, 0.f);
     // slot validity (same rule as the inverse index)
-    const int cl = lane < p.topk ? srow[lane] : -1;
+    const int cl = lane < p.topk ? __ldg(srow + lane) : -1;
     const bool sv = cl >= 0 && cl < p.nb && (long long)cl * 128 <= pos;
     const unsigned mask = __ballot_sync(0xffffffffu, sv);
-    const uint4 *src = reinterpret_cast<const uint4 *>(part + row * p.topk * D);
-    uint4 u[NI];
-#pragma unroll
-    for (int t = 0; t < NI; ++t) {
-        const int s = t * SPI + lane / LPS;
-        u[t] = (t * SPI < p.topk && ((mask >> s) & 1u)) ? __ldg(src + s * LPS + lane % LPS) : make_uint4(0, 0, 0, 0);
-    }
-    const float2 mz = sv ? stats[row * p.topk + lane] : make_float2(-INFINITY, 0.f);
+    const float2 mz = sv ? mz_raw : make_float2(-INFINITY, 0.f);
     const float M = warp_max(mz.x);
     const float w = sv ? exp2f(mz.x - M) : 0.f;
     const float Z = warp_sum(w * mz.y);
     float acc[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    for (int g0 = 0; g0 < p.topk; g0 += 16) {
+        if (g0 > 0) load_group(u, g0);
 #pragma unroll
-    for (int t = 0; t < NI; ++t) {
-        const float ws = __shfl_sync(0xffffffffu, w, (t * SPI + lane / LPS) & 31);
-        const uint32_t wd[4] = {u[t].x, u[t].y, u[t].z, u[t].w};
+        for (int t = 0; t < GI; ++t) {
+            const int s = (g0 + t * SPI + lane / LPS) & 31;
+            const float ws = __shfl_sync(0xffffffffu, w, s);
+            if (!((mask >> s) & 1u)) continue;
+            const uint32_t wd[4] = {u[t].x, u[t].y, u[t].z, u[t].w};
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-            const float2 x = unpack_bf16(wd[q4]);
-            acc[2 * q4] += ws * x.x;
-            acc[2 * q4 + 1] += ws * x.y;
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const float2 x = unpack_bf16(wd[q4]);
+                acc[2 * q4] += ws * x.x;
+                acc[2 * q4 + 1] += ws * x.y;
+            }
         }
     }
 #pragma unroll
