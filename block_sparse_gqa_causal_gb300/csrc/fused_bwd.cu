@@ -203,7 +203,7 @@ bwd_combine_kernel(Problem p, const int32_t *__restrict__ sel, const bf16 *__res
 {
     constexpr int LPS = DD / 8;                 // lanes per slot row
     constexpr int SPI = 32 / LPS;               // slots per load instruction
-    constexpr int NI = 32 / SPI;                // instructions to cover 32 slots
+    constexpr int GI = 16 / SPI;                // load instructions per group of 16 slots
     const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= (long long)p.B * p.Nq * H) return;
@@ -212,26 +212,35 @@ bwd_combine_kernel(Problem p, const int32_t *__restrict__ sel, const bf16 *__res
     const int i = (int)(bi % p.Nq), b = (int)(bi / p.Nq);
     const long long pos = (long long)p.q_offset + i;
     const int32_t *srow = sel + (((long long)b * p.Hkv + h / Gh) * p.Nq + i) * p.topk;
-    const int cl = lane < p.topk ? srow[lane] : -1;
-    const unsigned mask = __ballot_sync(0xffffffffu, cl >= 0 && cl < p.nb && (long long)cl * 128 <= pos);
     const uint4 *src = reinterpret_cast<const uint4 *>(part + row * p.topk * DD);
+    auto load_group = [&](uint4 (&u)[GI], int g0) {
+#pragma unroll
+        for (int t = 0; t < GI; ++t) {
+            const int s = g0 + t * SPI + lane / LPS;
+            u[t] = s < p.topk ? __ldg(src + s * LPS + lane % LPS) : make_uint4(0, 0, 0, 0);
+        }
+    };
+    // the first 16 slots are requested before the selection arrives (invalid
+    // slots are masked below, their bytes never written): one round trip
+    uint4 u[GI];
+    load_group(u, 0);
+    const int cl = lane < p.topk ? __ldg(srow + lane) : -1;
+    const unsigned mask = __ballot_sync(0xffffffffu, cl >= 0 && cl < p.nb && (long long)cl * 128 <= pos);
     float acc[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-    uint4 u[NI];
+    for (int g0 = 0; g0 < p.topk; g0 += 16) {
+        if (g0 > 0) load_group(u, g0);
 #pragma unroll
-    for (int t = 0; t < NI; ++t) {
-        const int s = t * SPI + lane / LPS;
-        u[t] = (t * SPI < p.topk && ((mask >> s) & 1u)) ? __ldg(src + s * LPS + lane % LPS) : make_uint4(0, 0, 0, 0);
-    }
+        for (int t = 0; t < GI; ++t) {
+            if (!((mask >> ((g0 + t * SPI + lane / LPS) & 31)) & 1u)) continue;
+            const uint32_t w[4] = {u[t].x, u[t].y, u[t].z, u[t].w};
 #pragma unroll
-    for (int t = 0; t < NI; ++t) {
-        const uint32_t w[4] = {u[t].x, u[t].y, u[t].z, u[t].w};
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-            const float2 x = unpack_bf16(w[q4]);
-            acc[2 * q4] += x.x;
-            acc[2 * q4 + 1] += x.y;
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const float2 x = unpack_bf16(w[q4]);
+                acc[2 * q4] += x.x;
+                acc[2 * q4 + 1] += x.y;
+            }
         }
     }
 #pragma unroll
