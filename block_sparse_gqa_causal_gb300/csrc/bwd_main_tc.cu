@@ -26,8 +26,11 @@
 // features) into the partial rows, off the epilogue's critical loop; the
 // epilogue hands them each chunk's partial-row indices through a small ring.
 // TMEM holds dV, dK and two 128-column slots; chunk n uses slot n%2 for S^T
-// and dP^T, and its dQ^T then overwrites the S^T half (the epilogue has read
-// it by then).  The slot is free again once the drain has read dQ^T, so the
+// and dP^T.  The epilogue writes P^T and dS^T (bf16) back over the S^T half,
+// where the dV and dK MMAs read them as their A operand; dQ^T then
+// overwrites that half (issued after dV, dK by the same thread, so in
+// order).  dS^T also goes to shared memory (double-buffered), the B operand
+// of dQ^T.  The slot is free again once the drain has read dQ^T, so the
 // scores of chunk n+1 run while the epilogue works on chunk n.
 #include <cuda_fp16.h>
 
@@ -54,12 +57,11 @@ constexpr int TILE_R = kRows * D * 2;
 constexpr int OFF_K = 0;
 constexpr int OFF_V = OFF_K + 2 * SUBK;
 constexpr int kStages = 3;                      // Q/dO stages
-constexpr int kPBuf = 1;                        // P/dS tile buffers
+constexpr int kDsBuf = 2;                       // dS^T tile buffers (shared memory)
 constexpr int OFF_STG = OFF_V + 2 * SUBK;       // kStages x {Q, dO}
 constexpr int STG_BYTES = 2 * TILE_R;
-constexpr int OFF_P = OFF_STG + kStages * STG_BYTES;   // P^T  [128 keys][64 rows] per buffer
-constexpr int OFF_DS = OFF_P + kPBuf * SUBK;           // dS^T [128 keys][64 rows] per buffer
-constexpr int OFF_META = OFF_DS + kPBuf * SUBK;
+constexpr int OFF_DS = OFF_STG + kStages * STG_BYTES;  // dS^T [128 keys][64 rows] per buffer
+constexpr int OFF_META = OFF_DS + kDsBuf * SUBK;
 
 struct Meta {                 // per stage
     float lse2[kRows];        // lse * log2(e) of each row (+inf for padding)
@@ -75,7 +77,9 @@ constexpr int OFF_RIDX = OFF_META + kStages * META_BYTES;    // kRx x [64 rows] 
 constexpr int OFF_BAR = OFF_RIDX + kRx * kRows * 8;
 constexpr int ALLOC = OFF_BAR + 256 + 1024;
 
-// slot a: S^T (later dQ^T) at TM_SLOT + 128a, dP^T 64 columns above it
+// slot a: S^T at TM_SLOT + 128a (then P^T, dS^T: warp half hf writes its 32
+// rows' P^T at columns 32hf..32hf+15 and dS^T at 32hf+16.., packed bf16;
+// then dQ^T), dP^T 64 columns above it
 constexpr uint32_t TM_DV = 0, TM_DK = 128, TM_SLOT = 256, TM_DP_OFF = 64;
 
 __device__ __forceinline__ int swz(int row, int ch) { return row * 128 + ((ch ^ (row & 7)) << 4); }
@@ -133,7 +137,7 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     // stays a shared-memory access (no generic addressing)
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + OFF_BAR);
-    uint64_t *full = bars, *empty = bars + 3, *p_full = bars + 6, *p_free = bars + 8;
+    uint64_t *full = bars, *empty = bars + 3, *p_full = bars + 6, *ds_free = bars + 8;   // p_full, ds_free: 2 each
     uint64_t *dq_full = bars + 10, *slot_free = bars + 12;
     uint64_t *kv_full = bars + 14, *s_full = bars + 15, *done = bars + 17;   // s_full: 2 (one per slot)
     uint64_t *rx_full = bars + 18, *rx_free = bars + 18 + kRx;
@@ -149,9 +153,9 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             tc::mbar_init(&full[a], G == 8 ? 33 : 64);
             tc::mbar_init(&empty[a], 1 + kEpiWarps);   // grads MMAs done + epilogue has read the row data
         }
-        for (int a = 0; a < kPBuf; ++a) {
+        for (int a = 0; a < kDsBuf; ++a) {
             tc::mbar_init(&p_full[a], kEpiWarps);
-            tc::mbar_init(&p_free[a], 1);
+            tc::mbar_init(&ds_free[a], 1);
         }
         for (int a = 0; a < 2; ++a) {
             tc::mbar_init(&s_full[a], 1);
@@ -327,37 +331,38 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             // ------------------------------------------------ MMA issuer: gradients
             constexpr uint32_t I_DKV = tc::idesc_bf16(128, 128) | tc::kBMajorMN;
             constexpr uint32_t I_DQ = tc::idesc_bf16(128, kRows) | tc::kAMajorMN | tc::kBMajorMN;
-            static_assert(kPBuf == 1, "the P / dS descriptors below assume one buffer");
             const uint64_t dKT = tc::sdesc_sw128(smem_u32(sm + OFF_K), SUBK, 1024);
-            const uint64_t dDST = tc::sdesc_sw128(smem_u32(sm + OFF_DS), SUBK, 1024);
-            const uint64_t dP = tc::sdesc_k128(smem_u32(sm + OFF_P)), dDS = tc::sdesc_k128(smem_u32(sm + OFF_DS));
+            const uint64_t dDST0 = tc::sdesc_sw128(smem_u32(sm + OFF_DS), SUBK, 1024);
             auto issue_grads = [&](int n) {
-                const int pb = n % kPBuf;
+                const int db = n % kDsBuf;
+                const uint32_t ts = tmem + TM_SLOT + (n & 1) * 128;
                 const uint32_t sq = smem_u32(sm + OFF_STG + (n % kStages) * STG_BYTES);
                 const uint64_t dQm = tc::sdesc_sw128(sq, 1024, 2048), dDOm = tc::sdesc_sw128(sq + TILE_R, 1024, 2048);
-                // dQ^T = K^T dS^T first (its drain frees the slot for chunk n+2), into
-                // the S^T half of the chunk's slot (read by the epilogue before it
-                // signalled p_full): A = K read MN-major (64-feature atoms SUBK
-                // apart), B = dS^T [keys][rows] MN-major; K = 128 keys
-#pragma unroll
-                for (int ks = 0; ks < kKeys / 16; ++ks)
-                    tc::mma_bf16(tmem + TM_SLOT + (n & 1) * 128, tc::desc_adv(dKT, ks * 2048),
-                                 tc::desc_adv(dDST, ks * 2048), I_DQ, ks > 0);
-                tc::mma_commit(&dq_full[n & 1]);
-                // dV += P^T dO, dK += dS^T Q: B = dO / Q read MN-major (feature
-                // halves 1024 bytes apart, 8-row groups 2048 apart); K = 64 rows
+                // dV += P^T dO, dK += dS^T Q: A = P^T / dS^T from the slot (rows 16ks..
+                // of the K dimension: warp half ks/2, 8 packed columns per step), B =
+                // dO / Q read MN-major (feature halves 1024 bytes apart, 8-row groups
+                // 2048 apart); K = 64 rows
 #pragma unroll
                 for (int ks = 0; ks < kRows / 16; ++ks) {
                     const bool acc = n > 0 || ks > 0;
-                    tc::mma_bf16(tmem + TM_DV, tc::desc_adv(dP, ks * 32), tc::desc_adv(dDOm, ks * 4096), I_DKV, acc);
-                    tc::mma_bf16(tmem + TM_DK, tc::desc_adv(dDS, ks * 32), tc::desc_adv(dQm, ks * 4096), I_DKV, acc);
+                    const uint32_t col = (ks >> 1) * 32 + (ks & 1) * 8;
+                    tc::mma_bf16_ts(tmem + TM_DV, ts + col, tc::desc_adv(dDOm, ks * 4096), I_DKV, acc);
+                    tc::mma_bf16_ts(tmem + TM_DK, ts + col + 16, tc::desc_adv(dQm, ks * 4096), I_DKV, acc);
                 }
                 tc::mma_commit(&empty[n % kStages]);
-                tc::mma_commit(&p_free[pb]);
+                // dQ^T = K^T dS^T over the slot's S^T half (in order after the MMAs
+                // above have read it): A = K read MN-major (64-feature atoms SUBK
+                // apart), B = dS^T [keys][rows] MN-major; K = 128 keys
+                const uint64_t dDST = tc::desc_adv(dDST0, db * SUBK);
+#pragma unroll
+                for (int ks = 0; ks < kKeys / 16; ++ks)
+                    tc::mma_bf16(ts, tc::desc_adv(dKT, ks * 2048), tc::desc_adv(dDST, ks * 2048), I_DQ, ks > 0);
+                tc::mma_commit(&dq_full[n & 1]);
+                tc::mma_commit(&ds_free[db]);
             };
             bool ok = tc::mbar_wait(kv_full, 0, st, 105, abort_flag);
             for (int ng = 0; ok && ng < nch; ++ng) {
-                if (!tc::mbar_wait(&p_full[ng % kPBuf], (uint32_t)(ng / kPBuf) & 1u, st, 106, abort_flag)) break;
+                if (!tc::mbar_wait(&p_full[ng % kDsBuf], (uint32_t)(ng / kDsBuf) & 1u, st, 106, abort_flag)) break;
                 tc::fence_after_sync();
                 issue_grads(ng);
             }
@@ -406,7 +411,7 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         const long long pt_base = pt_off[bucket];  // this bucket's first teacher row
         bool ok = true;
         for (int n = 0; ok && n < nch; ++n) {
-            const int s = n % kStages, pb = n % kPBuf;
+            const int s = n % kStages, db = n % kDsBuf;
             const Meta *meta = reinterpret_cast<const Meta *>(sm + OFF_META + s * META_BYTES);
             if (!wwait(&full[s], (uint32_t)(n / kStages) & 1u, st, 112, abort_flag)) { ok = false; break; }
             if (!wwait(&s_full[n & 1], (uint32_t)(n >> 1) & 1u, st, 113, abort_flag)) { ok = false; break; }
@@ -477,7 +482,10 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                                 make_uint4(hv[4 * x], hv[4 * x + 1], hv[4 * x + 2], hv[4 * x + 3]);
                 }
             }
-            if (n >= kPBuf && !wwait(&p_free[pb], (uint32_t)((n - kPBuf) / kPBuf) & 1u, st, 114, abort_flag)) {
+            // P^T and dS^T over this warp's own S^T columns (read above) for the dV / dK MMAs
+            tc::tmem_st16(ts, pk);
+            tc::tmem_st16(ts + 16, dk2);
+            if (n >= kDsBuf && !wwait(&ds_free[db], (uint32_t)((n - kDsBuf) / kDsBuf) & 1u, st, 114, abort_flag)) {
                 ok = false;
                 break;
             }
@@ -491,25 +499,24 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&rx_full[n % kRx]);
             }
-            uint8_t *sp = sm + OFF_P + pb * SUBK, *sd = sm + OFF_DS + pb * SUBK;
+            uint8_t *sd = sm + OFF_DS + db * SUBK;
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
                 const int ch = hf * 4 + c4;
-                *reinterpret_cast<uint4 *>(sp + swz(kr, ch)) =
-                    make_uint4(pk[c4 * 4], pk[c4 * 4 + 1], pk[c4 * 4 + 2], pk[c4 * 4 + 3]);
                 *reinterpret_cast<uint4 *>(sd + swz(kr, ch)) =
                     make_uint4(dk2[c4 * 4], dk2[c4 * 4 + 1], dk2[c4 * 4 + 2], dk2[c4 * 4 + 3]);
             }
             tc::fence_proxy_async();
+            tc::tmem_wait_st();
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&p_full[pb]);
+            if (lane == 0) tc::mbar_arrive(&p_full[db]);
         }
         // ---- dK, dV of this key (this warp: features hf*64 .. hf*64+63)
         if (ok && nch > 0) {
             // the last chunk's buffer release follows every MMA of the bucket
             const int m = nch - 1;
-            ok = wwait(&p_free[m % kPBuf], (uint32_t)(m / kPBuf) & 1u, st, 115, abort_flag);
+            ok = wwait(&ds_free[m % kDsBuf], (uint32_t)(m / kDsBuf) & 1u, st, 115, abort_flag);
             tc::fence_after_sync();
         }
         if (ok) {

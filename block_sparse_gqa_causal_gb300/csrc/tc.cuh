@@ -145,6 +145,17 @@ MSA_DEV void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate));
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T: A (M x K, K-major) read from tensor
+// memory -- row m in lane m, 16-bit elements packed two per 32-bit column in
+// K order (lower K in the low half) -- B through its shared-memory descriptor.
+MSA_DEV void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc, bool accumulate)
+{
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate));
+}
+
 // Arrive on `bar` once every tcgen05.mma issued so far by this thread is done.
 MSA_DEV void mma_commit(uint64_t *bar)
 {
@@ -249,6 +260,19 @@ MSA_DEV void tmem_ld16_nowait(uint32_t taddr, uint32_t *r)
         : "r"(taddr)
         : "memory");
 }
+// 32 lanes x 16 consecutive 32-bit columns from registers (thread t of warp
+// w writes lane 32*(w%4) + t); complete once tmem_wait_st returns.
+MSA_DEV void tmem_st16(uint32_t taddr, const uint32_t *r)
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+MSA_DEV void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
+
 MSA_DEV void tmem_wait32(uint32_t *r)
 {
     asm volatile("tcgen05.wait::ld.sync.aligned;\n"
