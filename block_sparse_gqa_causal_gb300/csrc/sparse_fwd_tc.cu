@@ -16,10 +16,13 @@
 //   M = max m_c,  O = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) z_c,
 //   lse = (M + log2 sum_c 2^(m_c - M) z_c) ln 2.
 //
-// Roles: warp 0 gathers Q rows with cp.async (+ mbarrier arrivals), warp 1
-// owns TMEM and issues the MMAs, warps 2..5 (one row each) do the softmax and
-// write the partials.  S and O accumulators are double-buffered in TMEM so
-// the S MMA of chunk n overlaps the epilogue of chunk n-1.
+// Roles: warps 0 and 10 load (alternate chunks), warp 1 owns TMEM and issues
+// the MMAs, warps 2..9 (two warpgroups on alternate chunks, one row per
+// thread) do the softmax and write the partials.  S and O accumulators are
+// double-buffered in TMEM; P (bf16) is written back over its own S columns
+// and read from there as the A operand of the O MMA, so P never touches
+// shared memory (an S MMA into that buffer is issued only after the O MMA
+// that reads it, and MMAs of one thread run in order).
 #include "msa_internal.h"
 #include "tc.cuh"
 
@@ -42,7 +45,7 @@ struct FwdLayout {
     // Q stage: [128 rows][D] as 8-row groups of KB feature halves (1024-byte
     // swizzle atoms): row rho, half h at (rho/8)*KB*1024 + h*1024 + (rho%8)*128
     static constexpr int OFF_Q = OFF_V + KB * SUB;          // 2 stages x KB sub-tiles
-    static constexpr int OFF_P = OFF_Q + 2 * KB * SUB;      // 2 buffers x 2 sub-tiles (128 keys)
+    static constexpr int OFF_P = OFF_Q + 2 * KB * SUB;      // 2 x output staging [128 rows][D] bf16
     static constexpr int OFF_META = OFF_P + 2 * 2 * SUB;    // 2 stages x QueryMeta
     static constexpr int OFF_BAR = OFF_META + 2 * 2048;
     static constexpr int ALLOC = OFF_BAR + 256 + 1024;
@@ -126,7 +129,7 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::OFF_BAR);
     uint64_t *q_full = bars, *q_empty = bars + 2, *s_full = bars + 4, *s_free = bars + 6;
-    uint64_t *p_full = bars + 8, *p_free = bars + 10, *o_full = bars + 12, *o_free = bars + 14;
+    uint64_t *p_full = bars + 8, *o_full = bars + 12, *o_free = bars + 14;
     uint64_t *kv_full = bars + 16, *done = bars + 17;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 18);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -143,7 +146,6 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             tc::mbar_init(&s_full[a], 1);
             tc::mbar_init(&s_free[a], kWgWarps);
             tc::mbar_init(&p_full[a], kWgWarps);
-            tc::mbar_init(&p_free[a], 1);
             tc::mbar_init(&o_full[a], 1);
             tc::mbar_init(&o_free[a], kWgWarps);
         }
@@ -229,7 +231,6 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             const uint64_t dK = tc::sdesc_k128(smem_u32(sm + L::OFF_K));
             const uint64_t dV = tc::sdesc_sw128(smem_u32(sm + L::OFF_V), SUB, 1024);
             const uint64_t dQ0 = tc::sdesc_sw128(smem_u32(sm + L::OFF_Q), 16, L::KB * 1024);
-            const uint64_t dP0 = tc::sdesc_k128(smem_u32(sm + L::OFF_P));
             bool ok = tc::mbar_wait(kv_full, 0, st, 62, abort_flag);
             if (ok) tc::fence_proxy_async();
             auto issue_s = [&](int n) {
@@ -247,15 +248,14 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             };
             auto issue_o = [&](int m) {
                 const int a = m & 1;
-                const uint64_t dP = tc::desc_adv(dP0, a * (2 * SUB));
 #pragma unroll
                 for (int ks = 0; ks < kKeys / 16; ++ks) {
-                    // A = P [rows][keys] K-major; B = V [keys][d] read MN-major (atoms of 64 d, 8-key groups)
-                    tc::mma_bf16(tmem + L::TM_O + a * D, tc::desc_adv(dP, (ks >> 2) * SUB + (ks & 3) * 32),
-                                 tc::desc_adv(dV, ks * 2048), I_O, ks > 0);
+                    // A = P [rows][keys] from TMEM (16 keys = 8 packed columns per
+                    // step); B = V [keys][d] read MN-major (atoms of 64 d, 8-key groups)
+                    tc::mma_bf16_ts(tmem + L::TM_O + a * D, tmem + L::TM_S + a * 128 + ks * 8, tc::desc_adv(dV, ks * 2048),
+                                    I_O, ks > 0);
                 }
                 tc::mma_commit(&o_full[a]);
-                tc::mma_commit(&p_free[a]);
             };
             // The two epilogue warpgroups run chunks n and n+1 at once, so S of
             // one chunk and O of another are issued in whichever order their
@@ -264,7 +264,8 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             uint32_t idle = 0;
             while (ok && no < nch) {
                 bool did = false;
-                if (ns < nch && tc::mbar_test(&q_full[ns & 1], (uint32_t)(ns >> 1) & 1u) &&
+                // S(ns) overwrites the TMEM buffer holding P(ns-2): only after O(ns-2) is issued
+                if (ns < nch && (ns < 2 || no >= ns - 1) && tc::mbar_test(&q_full[ns & 1], (uint32_t)(ns >> 1) & 1u) &&
                     (ns < 2 || tc::mbar_test(&s_free[ns & 1], ((uint32_t)(ns >> 1) & 1u) ^ 1u))) {
                     tc::fence_proxy_async();
                     tc::fence_after_sync();
@@ -305,11 +306,9 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         int pi = 0, pslot = 0;
         bool pvalid = false;
         bool ok = true;
-        // writes the partial output of chunk m (row data held in pm, pz, pi, pslot, pvalid)
         // writes the partial output of chunk m (row data held in pm, pz, pi, pslot,
-        // pvalid).  The rows go through this warp's rows of the chunk's P tile
-        // (free once the O MMA that read it has completed) so that each store
-        // covers whole 256-byte partial rows.
+        // pvalid).  The rows go through this warpgroup's staging tile so that each
+        // store covers whole 256-byte partial rows.
         auto emit = [&](int m) -> bool {
             const int am = m & 1;
             if (!wwait(&o_full[am], (uint32_t)(m >> 1) & 1u, st, 74, abort_flag)) return false;
@@ -390,12 +389,8 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                 }
             }
             const float msafe = mx == -INFINITY ? 0.f : mx * sl2;
-            // this warpgroup's previous chunk leaves first: its output is staged
-            // through the P tile that this chunk's P is about to overwrite
-            if (n >= 2 && !emit(n - 2)) { ok = false; break; }
-            if (!wwait(&p_free[a], ph ^ 1u, st, 73, abort_flag)) { ok = false; break; }
-            // pass 2: P = exp2(s*scale*log2e - m) into the bf16 P tile, z = row sum
-            uint8_t *sp = sm + L::OFF_P + a * (2 * SUB);
+            // pass 2: P = exp2(s*scale*log2e - m) as bf16 over the row's own S
+            // columns (keys 32c..32c+31 -> packed columns 16c..16c+15), z = row sum
             float z = 0.f;
 #pragma unroll
             for (int c64 = 0; c64 < 2; ++c64) {
@@ -416,23 +411,20 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                         z += e0 + e1;
                         pk[jj / 2] = pack_bf16(e0, e1);
                     }
-#pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4) {
-                        const int ch = c32 * 4 + c4;     // 16-byte chunk of the 256-byte row
-                        *reinterpret_cast<uint4 *>(sp + (ch >> 3) * SUB + swz(rho, ch & 7)) =
-                            make_uint4(pk[c4 * 4], pk[c4 * 4 + 1], pk[c4 * 4 + 2], pk[c4 * 4 + 3]);
-                    }
+                    tc::tmem_st16(sbase + c32 * 16, pk);
                 }
             }
             const float cm = msafe, cz = z;
             const bool cvalid = valid && mx != -INFINITY;
+            tc::tmem_wait_st();
             tc::fence_before_sync();
-            tc::fence_proxy_async();
             __syncwarp();
             if (lane == 0) {
                 tc::mbar_arrive(&s_free[a]);
                 tc::mbar_arrive(&p_full[a]);
             }
+            // this warpgroup's previous chunk leaves now, while the O MMA of this one runs
+            if (n >= 2 && !emit(n - 2)) { ok = false; break; }
             pm = cm;
             pz = cz;
             pvalid = cvalid;
