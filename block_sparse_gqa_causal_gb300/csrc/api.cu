@@ -286,13 +286,12 @@ msa_status msa_index_select(const msa_shape *shape, const void *q_idx, const voi
     st = check_ws(workspace, workspace_bytes, kStatusBytes + (block_scores ? 0 : bs_bytes(p)));
     if (st != MSA_OK) return st;
     Carve cv{static_cast<char *>(workspace)};
-    float *bs = block_scores ? block_scores : cv.take<float>((size_t)p.B * p.Nq * p.Hkv * p.nb);
+    float *scratch = block_scores ? nullptr : cv.take<float>((size_t)p.B * p.Nq * p.Hkv * p.nb);
     DeviceStatus *ds = static_cast<DeviceStatus *>(workspace);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_index_scores(p, static_cast<const bf16 *>(q_idx), static_cast<const bf16 *>(k_idx), bs, ds, s);
-    if (e != cudaSuccess) return cuda_fail(e, "index_scores launch");
-    e = launch_block_topk(p, bs, sel_idx, ds, s);
-    if (e != cudaSuccess) return cuda_fail(e, "block_topk launch");
+    cudaError_t e = launch_index_select(p, static_cast<const bf16 *>(q_idx), static_cast<const bf16 *>(k_idx),
+                                        block_scores, scratch, sel_idx, ds, s);
+    if (e != cudaSuccess) return cuda_fail(e, "index_select launch");
     return MSA_OK;
 }
 

@@ -19,6 +19,13 @@
 //   warps 2..9  epilogue: TMEM -> registers, causal mask, row max, store
 // Two TMEM accumulator sets (2 tiles x 128 fp32 columns each) alternate so
 // the epilogue of block c overlaps the MMAs of block c+1.
+//
+// When a CTA sees every block of its rows and k <= 16 the selection happens
+// here too: each epilogue thread owns one row and keeps the 16 best earlier
+// blocks in registers (sorted by score, then lower index: a later block
+// enters only with a strictly larger score), so the block scores need not
+// round-trip through memory; the k-1 best plus the local block are written
+// in ascending order, as the separate top-k kernel does.
 #include "msa_internal.h"
 #include "tc.cuh"
 
@@ -47,7 +54,7 @@ struct Smem {
 template <int DI>
 __global__ void __launch_bounds__(kThreads, 1)
 index_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-                       Problem p, float *__restrict__ bs, int span, DeviceStatus *st)
+                       Problem p, float *__restrict__ bs, int32_t *__restrict__ sel, int span, DeviceStatus *st)
 {
     using S = Smem<DI>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -169,7 +176,16 @@ index_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_
         const bool valid = rho < rows_total && m < mt;
         const long long pos = (long long)p.q_offset + (valid ? rho / p.Hkv : 0);
         const int c_last = valid ? (int)min((long long)c_end - 1, pos / 128) : -1;   // last block this row sees
-        float *out = bs + ((long long)b * rows_total + (valid ? rho : 0)) * p.nb;
+        const int c0 = (int)(pos / 128);           // the row's local block
+        float *out = bs ? bs + ((long long)b * rows_total + (valid ? rho : 0)) * p.nb : nullptr;
+        // fused selection: the 16 best earlier blocks, descending by score
+        float tv[16];
+        int ti[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+            tv[x] = -INFINITY;
+            ti[x] = 0;
+        }
         const bool vec_ok = (p.nb & 7) == 0;
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         float grp[8];
@@ -211,6 +227,27 @@ index_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_
                     }
                 }
                 grp[u] = mx * p.scale_idx;   // a positive scale commutes with max
+                if (sel) {
+                    const int c = c_begin + n;
+                    const float sc = (valid && c < c0) ? grp[u] : -INFINITY;
+                    if (__any_sync(0xffffffffu, sc > tv[15])) {
+                        if (sc > tv[15]) {
+                            tv[15] = sc;
+                            ti[15] = c;
+                        }
+#pragma unroll
+                        for (int x = 15; x > 0; --x) {
+                            if (tv[x] > tv[x - 1]) {
+                                const float t0 = tv[x];
+                                tv[x] = tv[x - 1];
+                                tv[x - 1] = t0;
+                                const int t1 = ti[x];
+                                ti[x] = ti[x - 1];
+                                ti[x - 1] = t1;
+                            }
+                        }
+                    }
+                }
                 tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&acc_empty[a]);
@@ -218,7 +255,7 @@ index_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_
             // store this row's scores for blocks c_begin+n0 .. (at most 8)
             const int c_lo = c_begin + n0;
             const int c_hi = min(c_lo + 7, c_last);
-            if (valid && c_hi >= c_lo) {
+            if (out && valid && c_hi >= c_lo) {
                 if (vec_ok && c_hi == c_lo + 7) {
                     float4 *o4 = reinterpret_cast<float4 *>(out + c_lo);
                     o4[0] = make_float4(grp[0], grp[1], grp[2], grp[3]);
@@ -230,6 +267,34 @@ index_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_
                 }
             }
         }
+        if (sel && valid) {
+            const int k = p.topk, i = rho / p.Hkv, r = rho % p.Hkv;
+            int32_t *o = sel + (((long long)b * p.Hkv + r) * p.Nq + i) * k;
+            int id[16];
+#pragma unroll
+            for (int x = 0; x < 16; ++x)
+                id[x] = c0 + 1 <= k ? (x <= c0 ? x : 0x7fffffff) : (x < k - 1 ? ti[x] : (x == k - 1 ? c0 : 0x7fffffff));
+            // ascending bitonic network over the 16 registers
+#pragma unroll
+            for (int size = 2; size <= 16; size <<= 1)
+#pragma unroll
+                for (int stride = size >> 1; stride > 0; stride >>= 1)
+#pragma unroll
+                    for (int x = 0; x < 16; ++x) {
+                        const int y = x ^ stride;
+                        if (y > x) {
+                            const bool up = (x & size) == 0;
+                            if ((id[x] > id[y]) == up) {
+                                const int t = id[x];
+                                id[x] = id[y];
+                                id[y] = t;
+                            }
+                        }
+                    }
+#pragma unroll
+            for (int x = 0; x < 16; ++x)
+                if (x < k) o[x] = id[x] == 0x7fffffff ? -1 : id[x];
+        }
     }
 
     tc::fence_before_sync();
@@ -240,8 +305,25 @@ index_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_
     }
 }
 
+// Row tiles and the block range each CTA covers: a tile's range is split
+// when there are too few tiles to fill the GPU (slices start on 8-block
+// boundaries).
+void plan_grid(const Problem &p, int &tiles, int &splits, int &span)
+{
+    const long long rows_total = (long long)p.Nq * p.Hkv;
+    tiles = (int)((rows_total + kTileRows - 1) / kTileRows);
+    splits = 1;
+    const long long ctas = (long long)tiles * p.B;
+    if (ctas < (long long)p.num_sms) splits = (int)min((long long)(p.nb + 7) / 8, (p.num_sms + ctas - 1) / ctas);
+    span = (p.nb + splits - 1) / splits;
+    span = (span + 7) & ~7;
+    splits = (p.nb + span - 1) / span;
+}
+
+// bs: scores out (nullptr: not stored); sel: selection out (fused form; the
+// caller has checked that it applies)
 template <int DI>
-cudaError_t launch_t(const Problem &p, const bf16 *q_idx, const bf16 *k_idx, float *bs, DeviceStatus *st,
+cudaError_t launch_t(const Problem &p, const bf16 *q_idx, const bf16 *k_idx, float *bs, int32_t *sel, DeviceStatus *st,
                      cudaStream_t s)
 {
     using S = Smem<DI>;
@@ -252,19 +334,13 @@ cudaError_t launch_t(const Problem &p, const bf16 *q_idx, const bf16 *k_idx, flo
     e = make_tmap_bf16_3d(&tk, k_idx, DI, p.kv_rows, p.B, DI * 2ull, (unsigned long long)p.kv_rows * DI * 2ull, 64,
                           128);
     if (e != cudaSuccess) return e;
-    const int tiles = (int)((rows_total + kTileRows - 1) / kTileRows);
-    // split each tile's block range when there are too few tiles to fill the GPU
-    int splits = 1;
-    const long long ctas = (long long)tiles * p.B;
-    if (ctas < (long long)p.num_sms) splits = (int)min((long long)(p.nb + 7) / 8, (p.num_sms + ctas - 1) / ctas);
-    int span = (p.nb + splits - 1) / splits;
-    span = (span + 7) & ~7;                         // slices start on 8-block boundaries
-    splits = (p.nb + span - 1) / span;
+    int tiles, splits, span;
+    plan_grid(p, tiles, splits, span);
     e = cudaFuncSetAttribute(index_scores_tc_kernel<DI>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::ALLOC);
     if (e != cudaSuccess) return e;
     {
         TimedLaunch timed_("index_scores_tc_kernel", s);
-        index_scores_tc_kernel<DI><<<dim3(tiles, splits, p.B), kThreads, S::ALLOC, s>>>(tq, tk, p, bs, span, st);
+        index_scores_tc_kernel<DI><<<dim3(tiles, splits, p.B), kThreads, S::ALLOC, s>>>(tq, tk, p, bs, sel, span, st);
     }
     note_launch();
     return cudaGetLastError();
@@ -275,7 +351,22 @@ cudaError_t launch_t(const Problem &p, const bf16 *q_idx, const bf16 *k_idx, flo
 cudaError_t launch_index_scores(const Problem &p, const bf16 *q_idx, const bf16 *k_idx, float *bs,
                                 DeviceStatus *st, cudaStream_t s)
 {
-    return p.d_idx == 128 ? launch_t<128>(p, q_idx, k_idx, bs, st, s) : launch_t<64>(p, q_idx, k_idx, bs, st, s);
+    return p.d_idx == 128 ? launch_t<128>(p, q_idx, k_idx, bs, nullptr, st, s)
+                          : launch_t<64>(p, q_idx, k_idx, bs, nullptr, st, s);
+}
+
+cudaError_t launch_index_select(const Problem &p, const bf16 *q_idx, const bf16 *k_idx, float *bs_out,
+                                float *bs_scratch, int32_t *sel, DeviceStatus *st, cudaStream_t s)
+{
+    int tiles, splits, span;
+    plan_grid(p, tiles, splits, span);
+    if (splits == 1 && p.topk <= 16)   // every CTA sees all blocks of its rows: fused selection
+        return p.d_idx == 128 ? launch_t<128>(p, q_idx, k_idx, bs_out, sel, st, s)
+                              : launch_t<64>(p, q_idx, k_idx, bs_out, sel, st, s);
+    float *bs = bs_out ? bs_out : bs_scratch;
+    cudaError_t e = launch_index_scores(p, q_idx, k_idx, bs, st, s);
+    if (e != cudaSuccess) return e;
+    return launch_block_topk(p, bs, sel, st, s);
 }
 
 }  // namespace msa

@@ -51,6 +51,11 @@ cudaError_t launch_index_scores(const Problem &p, const bf16 *q_idx, const bf16 
 // Top-k block selection from block scores.  sel: [B, Hkv, Nq, topk].
 cudaError_t launch_block_topk(const Problem &p, const float *bs, int32_t *sel, DeviceStatus *st,
                               cudaStream_t s);
+// Index scores + selection: fused into the score kernel when every CTA sees
+// all blocks of its rows and topk <= 16 (scores stored only if bs_out is set),
+// else scores to bs_out (or bs_scratch) and the separate top-k kernel.
+cudaError_t launch_index_select(const Problem &p, const bf16 *q_idx, const bf16 *k_idx, float *bs_out,
+                                float *bs_scratch, int32_t *sel, DeviceStatus *st, cudaStream_t s);
 // Key-major main branch forward (many queries per selected block).
 struct FwdWork {
     bf16 *part;          // [B, Nq, Hq, topk, d] unnormalised partial outputs per selected block

@@ -96,8 +96,8 @@ extern "C" msa_status msa_index_select_noalloc(const msa_shape *shape, const voi
     if (e != cudaSuccess) return set_error(MSA_ERR_CUDA, cudaGetErrorString(e));
     DeviceStatus *ds = static_cast<DeviceStatus *>(scratch);
     float *bs = reinterpret_cast<float *>(static_cast<char *>(scratch) + kStatusBytes);
-    e = launch_index_scores(p, static_cast<const bf16 *>(q_idx), static_cast<const bf16 *>(k_idx), bs, ds, s);
-    if (e == cudaSuccess) e = launch_block_topk(p, bs, sel_idx, ds, s);
+    e = launch_index_select(p, static_cast<const bf16 *>(q_idx), static_cast<const bf16 *>(k_idx), nullptr, bs,
+                            sel_idx, ds, s);
     if (e != cudaSuccess) return set_error(MSA_ERR_CUDA, cudaGetErrorString(e));
     return MSA_OK;
 }
