@@ -26,6 +26,8 @@
 // query columns half (w-2)/4).  s^T and dsig^T are double-buffered.
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "msa_internal.h"
 #include "tc.cuh"
 
@@ -332,34 +334,56 @@ bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, cons
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&s_free[sb]);
             uint32_t sg[32];
+            // no per-element mask where every query of the warp's 64 sees the whole block
+            const int pmin = __reduce_min_sync(0xffffffffu, min(meta->pos[cb + lane], meta->pos[cb + 32 + lane]));
+            const bool all_vis = (long long)pmin >= j0 + kKeys - 1 && j0 + kKeys <= p.Nk;
+            const int ji = (int)min(j, (long long)INT_MAX);
+            auto dsig_tile = [&](auto all_tag) {
+                constexpr bool kAll = decltype(all_tag)::value;
 #pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                float lv[6];                        // streaming warp sum of Pt s log2(e) (KL partial)
+                for (int t = 0; t < 2; ++t) {
+                    [[maybe_unused]] float lv[6];   // streaming warp sum of Pt s log2(e) (KL partial)
 #pragma unroll
-                for (int cc = 32 * t; cc < 32 * t + 32; cc += 4) {
-                    const float4 l4 = *reinterpret_cast<const float4 *>(meta->lsei2 + cb + cc);
-                    const int4 p4 = *reinterpret_cast<const int4 *>(meta->pos + cb + cc);
-                    const float l2[4] = {l4.x, l4.y, l4.z, l4.w};
-                    const int ps[4] = {p4.x, p4.y, p4.z, p4.w};
-                    float g2[4];
+                    for (int cc = 32 * t; cc < 32 * t + 32; cc += 4) {
+                        const float4 l4 = *reinterpret_cast<const float4 *>(meta->lsei2 + cb + cc);
+                        int ps[4] = {0, 0, 0, 0};
+                        if constexpr (!kAll) {
+                            const int4 p4 = *reinterpret_cast<const int4 *>(meta->pos + cb + cc);
+                            ps[0] = p4.x;
+                            ps[1] = p4.y;
+                            ps[2] = p4.z;
+                            ps[3] = p4.w;
+                        }
+                        const float l2[4] = {l4.x, l4.y, l4.z, l4.w};
+                        float g2[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int col = cc + e;
-                        const float sv = __uint_as_float(col < 32 ? s0[col] : s1[col - 32]);
-                        const bool vis = key_ok && j <= (long long)ps[e];
-                        const __half2 h2 = *reinterpret_cast<const __half2 *>(
-                            reinterpret_cast<const uint32_t *>(&tv[col >> 3]) + ((col & 7) >> 1));
-                        const float ptv = (col & 1) ? __high2float(h2) : __low2float(h2);
-                        g2[e] = vis ? coef * (tc::ex2(sv * si2 - l2[e]) - ptv) : 0.f;
-                        if constexpr (kKL) colsum32_push(lv, vis ? ptv * (sv * si2) : 0.f, col & 31, lane);
+                        for (int e = 0; e < 4; ++e) {
+                            const int col = cc + e;
+                            const float sv = __uint_as_float(col < 32 ? s0[col] : s1[col - 32]);
+                            const __half2 h2 = *reinterpret_cast<const __half2 *>(
+                                reinterpret_cast<const uint32_t *>(&tv[col >> 3]) + ((col & 7) >> 1));
+                            const float ptv = (col & 1) ? __high2float(h2) : __low2float(h2);
+                            const float gv = coef * (tc::ex2(sv * si2 - l2[e]) - ptv);
+                            [[maybe_unused]] const float bv = kKL ? ptv * (sv * si2) : 0.f;
+                            if constexpr (kAll) {
+                                g2[e] = gv;
+                                if constexpr (kKL) colsum32_push(lv, bv, col & 31, lane);
+                            } else {
+                                const bool vis = key_ok && ji <= ps[e];
+                                g2[e] = vis ? gv : 0.f;
+                                if constexpr (kKL) colsum32_push(lv, vis ? bv : 0.f, col & 31, lane);
+                            }
+                        }
+                        sg[cc / 2] = pack_bf16(g2[0], g2[1]);
+                        sg[cc / 2 + 1] = pack_bf16(g2[2], g2[3]);
                     }
-                    sg[cc / 2] = pack_bf16(g2[0], g2[1]);
-                    sg[cc / 2 + 1] = pack_bf16(g2[2], g2[3]);
+                    if constexpr (kKL) {
+                        if (kl_cur[t] >= 0) klb[kl_cur[t] * 4 + qd] = lv[5];   // lane l: column cb + 32 t + l
+                    }
                 }
-                if constexpr (kKL) {
-                    if (kl_cur[t] >= 0) klb[kl_cur[t] * 4 + qd] = lv[5];   // lane l: column cb + 32 t + l
-                }
-            }
+            };
+            if (all_vis) dsig_tile(std::true_type{});
+            else dsig_tile(std::false_type{});
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&empty[s]);   // the stage's row data is no longer read
             if (n >= 1 && !wwait(g_free, (uint32_t)(n - 1) & 1u, st, 134, abort_flag)) { ok = false; break; }

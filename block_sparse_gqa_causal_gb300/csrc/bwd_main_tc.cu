@@ -34,6 +34,8 @@
 // scores of chunk n+1 run while the epilogue works on chunk n.
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "msa_internal.h"
 #include "tc.cuh"
 
@@ -434,28 +436,43 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             }
             tc::tmem_wait32(sv);
             tc::tmem_wait32(dp);
-            // P^T, dS^T of this key against the warp's 32 rows; teacher sums
+            // P^T, dS^T of this key against the warp's 32 rows; teacher sums.  The
+            // mask is needed only where some row of the warp does not see the whole
+            // block (a bucket's local-block queries, its padded tail, the last block)
             uint32_t pk[16], dk2[16];
             float ptq[NQH];
+            int lim[NQH];                              // last visible key offset per query (-1: none)
+            int minpos = pos[0];
 #pragma unroll
-            for (int u = 0; u < NQH; ++u) ptq[u] = 0.f;
-#pragma unroll
-            for (int cc = 0; cc < 32; cc += 2) {
-                float pr[2], ds[2];
-                const float2 l2 = *reinterpret_cast<const float2 *>(meta->lse2 + cb + cc);
-                const float2 dd = *reinterpret_cast<const float2 *>(meta->dd + cb + cc);
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int col = cc + e, u = col / G;
-                    const bool vis = key_ok && j <= (long long)pos[u];
-                    pr[e] = vis ? tc::ex2(__uint_as_float(sv[col]) * sl2 - (e ? l2.y : l2.x)) : 0.f;
-                    // dS carries the softmax scale, so dQ and dK need no rescaling
-                    ds[e] = pr[e] * fmaf(__uint_as_float(dp[col]), p.scale, -(e ? dd.y : dd.x));
-                    ptq[u] += pr[e];
-                }
-                pk[cc / 2] = pack_bf16(pr[0], pr[1]);
-                dk2[cc / 2] = pack_bf16(ds[0], ds[1]);
+            for (int u = 0; u < NQH; ++u) {
+                ptq[u] = 0.f;
+                minpos = min(minpos, pos[u]);
+                lim[u] = (int)max(-1LL, min(min((long long)pos[u], (long long)p.Nk - 1) - j0, (long long)kKeys - 1));
             }
+            const bool all_vis = (long long)minpos >= j0 + kKeys - 1 && j0 + kKeys <= p.Nk;
+            auto softmax_grad = [&](auto all_tag) {
+                constexpr bool kAll = decltype(all_tag)::value;
+#pragma unroll
+                for (int cc = 0; cc < 32; cc += 2) {
+                    float pr[2], ds[2];
+                    const float2 l2 = *reinterpret_cast<const float2 *>(meta->lse2 + cb + cc);
+                    const float2 dd = *reinterpret_cast<const float2 *>(meta->dd + cb + cc);
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int col = cc + e, u = col / G;
+                        const float x = tc::ex2(__uint_as_float(sv[col]) * sl2 - (e ? l2.y : l2.x));
+                        if constexpr (kAll) pr[e] = x;
+                        else pr[e] = kr <= lim[u] ? x : 0.f;
+                        // dS carries the softmax scale, so dQ and dK need no rescaling
+                        ds[e] = pr[e] * fmaf(__uint_as_float(dp[col]), p.scale, -(e ? dd.y : dd.x));
+                        ptq[u] += pr[e];
+                    }
+                    pk[cc / 2] = pack_bf16(pr[0], pr[1]);
+                    dk2[cc / 2] = pack_bf16(ds[0], ds[1]);
+                }
+            };
+            if (all_vis) softmax_grad(std::true_type{});
+            else softmax_grad(std::false_type{});
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&empty[s]);   // done with the stage's row data
             {

@@ -23,6 +23,8 @@
 // and read from there as the A operand of the O MMA, so P never touches
 // shared memory (an S MMA into that buffer is issued only after the O MMA
 // that reads it, and MMAs of one thread run in order).
+#include <type_traits>
+
 #include "msa_internal.h"
 #include "tc.cuh"
 
@@ -369,7 +371,7 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             const int lim = (int)max(-1LL, min(min(pos, (long long)p.Nk - 1) - j0, (long long)kKeys - 1));
             const uint32_t sbase = tmem + lane_base + L::TM_S + a * 128;
             // pass 1: row max over the visible keys
-            float mx = -INFINITY;
+            float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // four independent max chains
 #pragma unroll
             for (int c64 = 0; c64 < 2; ++c64) {
                 uint32_t s0[32], s1[32];
@@ -379,42 +381,55 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                 tc::tmem_wait32(s1);
                 if (lim >= c64 * 64 + 63) {
 #pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) mx = fmaxf(mx, fmaxf(__uint_as_float(s0[jj]), __uint_as_float(s1[jj])));
+                    for (int jj = 0; jj < 32; ++jj)
+                        mq[jj & 3] = fmaxf(mq[jj & 3], fmaxf(__uint_as_float(s0[jj]), __uint_as_float(s1[jj])));
                 } else {
 #pragma unroll
                     for (int jj = 0; jj < 32; ++jj) {
-                        if (c64 * 64 + jj <= lim) mx = fmaxf(mx, __uint_as_float(s0[jj]));
-                        if (c64 * 64 + 32 + jj <= lim) mx = fmaxf(mx, __uint_as_float(s1[jj]));
+                        if (c64 * 64 + jj <= lim) mq[jj & 3] = fmaxf(mq[jj & 3], __uint_as_float(s0[jj]));
+                        if (c64 * 64 + 32 + jj <= lim) mq[jj & 3] = fmaxf(mq[jj & 3], __uint_as_float(s1[jj]));
                     }
                 }
             }
+            const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
             const float msafe = mx == -INFINITY ? 0.f : mx * sl2;
             // pass 2: P = exp2(s*scale*log2e - m) as bf16 over the row's own S
             // columns (keys 32c..32c+31 -> packed columns 16c..16c+15), z = row sum
-            float z = 0.f;
+            // (no mask where every row of the warp sees the whole block; four
+            // partial sums keep the row-sum chain short)
+            float zp[4] = {0.f, 0.f, 0.f, 0.f};
+            auto pass2 = [&](auto all_tag) {
+                constexpr bool kAll = decltype(all_tag)::value;
 #pragma unroll
-            for (int c64 = 0; c64 < 2; ++c64) {
-                uint32_t sr[2][32];
-                tc::tmem_ld32_nowait(sbase + c64 * 64, sr[0]);
-                tc::tmem_ld32_nowait(sbase + c64 * 64 + 32, sr[1]);
-                tc::tmem_wait32(sr[0]);
-                tc::tmem_wait32(sr[1]);
+                for (int c64 = 0; c64 < 2; ++c64) {
+                    uint32_t sr[2][32];
+                    tc::tmem_ld32_nowait(sbase + c64 * 64, sr[0]);
+                    tc::tmem_ld32_nowait(sbase + c64 * 64 + 32, sr[1]);
+                    tc::tmem_wait32(sr[0]);
+                    tc::tmem_wait32(sr[1]);
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int c32 = c64 * 2 + h;
-                    uint32_t pk[16];
+                    for (int h = 0; h < 2; ++h) {
+                        const int c32 = c64 * 2 + h;
+                        uint32_t pk[16];
 #pragma unroll
-                    for (int jj = 0; jj < 32; jj += 2) {
-                        const int jo = c32 * 32 + jj;
-                        const float e0 = jo <= lim ? tc::ex2(__uint_as_float(sr[h][jj]) * sl2 - msafe) : 0.f;
-                        const float e1 = jo + 1 <= lim ? tc::ex2(__uint_as_float(sr[h][jj + 1]) * sl2 - msafe) : 0.f;
-                        z += e0 + e1;
-                        pk[jj / 2] = pack_bf16(e0, e1);
+                        for (int jj = 0; jj < 32; jj += 2) {
+                            const int jo = c32 * 32 + jj;
+                            float e0 = tc::ex2(__uint_as_float(sr[h][jj]) * sl2 - msafe);
+                            float e1 = tc::ex2(__uint_as_float(sr[h][jj + 1]) * sl2 - msafe);
+                            if constexpr (!kAll) {
+                                e0 = jo <= lim ? e0 : 0.f;
+                                e1 = jo + 1 <= lim ? e1 : 0.f;
+                            }
+                            zp[(jj >> 1) & 3] += e0 + e1;
+                            pk[jj / 2] = pack_bf16(e0, e1);
+                        }
+                        tc::tmem_st16(sbase + c32 * 16, pk);
                     }
-                    tc::tmem_st16(sbase + c32 * 16, pk);
                 }
-            }
-            const float cm = msafe, cz = z;
+            };
+            if (__all_sync(0xffffffffu, lim >= kKeys - 1)) pass2(std::true_type{});
+            else pass2(std::false_type{});
+            const float cm = msafe, cz = (zp[0] + zp[1]) + (zp[2] + zp[3]);
             const bool cvalid = valid && mx != -INFINITY;
             tc::tmem_wait_st();
             tc::fence_before_sync();
