@@ -122,7 +122,13 @@ void carve_index(Carve &cv, const Problem &p, W &w)
 
 size_t fwd_bytes(const Problem &p)
 {
-    if (!fwd_keymajor(p)) return 0;
+    if (!fwd_keymajor(p)) {
+        // split-KV partial states (decode: too few rows to fill the GPU)
+        const int ns = sparse_attn_splits(p);
+        if (ns == 1) return 0;
+        const size_t rows = (size_t)p.B * p.Nq * p.Hq * ns;
+        return align256(rows * p.d * 4 + rows * 8);
+    }
     const size_t rows = (size_t)p.B * p.Nq * p.Hq * p.topk;
     return align256(rows * p.d * 2) + align256(rows * 8) + index_bytes(p);
 }
@@ -323,8 +329,13 @@ msa_status msa_sparse_attn_fwd(const msa_shape *shape, const void *q, const void
         e = launch_sparse_fwd_keymajor(p, static_cast<const bf16 *>(q), static_cast<const bf16 *>(k),
                                        static_cast<const bf16 *>(v), sel_idx, static_cast<bf16 *>(o), lse, w, ds, s);
     } else {
+        float *split_ws = nullptr;
+        if (sparse_attn_splits(p) > 1) {
+            Carve cv{static_cast<char *>(workspace)};
+            split_ws = cv.take<float>(fwd_bytes(p) / 4);
+        }
         e = launch_sparse_attn_fwd(p, static_cast<const bf16 *>(q), static_cast<const bf16 *>(k),
-                                   static_cast<const bf16 *>(v), sel_idx, static_cast<bf16 *>(o), lse, ds, s);
+                                   static_cast<const bf16 *>(v), sel_idx, static_cast<bf16 *>(o), lse, split_ws, ds, s);
     }
     if (e != cudaSuccess) return cuda_fail(e, "sparse_attn_fwd launch");
     return MSA_OK;

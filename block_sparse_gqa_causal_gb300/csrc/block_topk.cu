@@ -107,33 +107,13 @@ __device__ __forceinline__ float key_value(unsigned long long key)
     return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
 }
 
-__global__ void __launch_bounds__(kWarps * 32)
-block_topk_kernel(Problem p, const float *__restrict__ bs, int32_t *__restrict__ sel)
+// One warp's running top-(k-1) over the segments base0, base0 + step, ... of
+// a row's earlier blocks [0, c0); best (lane m: m-th best key, 0 = empty)
+// is updated in place.  buf: this warp's kSeg-key scratch.
+__device__ __forceinline__ void warp_topk(const float *__restrict__ src, int c0, int K1, int base0, int step,
+                                          unsigned long long *buf, unsigned long long &best, int lane)
 {
-    __shared__ unsigned long long cand_buf[kWarps][kSeg];
-    const int lane = threadIdx.x & 31;
-    const int wi = threadIdx.x >> 5;
-    const long long row = (long long)blockIdx.x * kWarps + wi;
-    const long long rows = (long long)p.B * p.Nq * p.Hkv;
-    if (row >= rows) return;
-    const int r = (int)(row % p.Hkv);
-    const long long bi = row / p.Hkv;
-    const int i = (int)(bi % p.Nq), b = (int)(bi / p.Nq);
-    const long long pos = (long long)p.q_offset + i;
-    const int c0 = (int)(pos / 128);
-    const int k = p.topk;
-    int32_t *out = sel + (((long long)b * p.Hkv + r) * p.Nq + i) * k;
-
-    if (c0 + 1 <= k) {               // every visible block is selected
-        if (lane < k) out[lane] = lane <= c0 ? lane : -1;
-        return;
-    }
-    const int K1 = k - 1;            // slots the indexer chooses, 0..31
-    const float *src = bs + row * p.nb;
-    unsigned long long *buf = cand_buf[wi];
-    unsigned long long best = 0ull;  // lane m: m-th best key so far (0 = empty)
-
-    for (int base = 0; K1 > 0 && base < c0; base += kSeg) {
+    for (int base = base0; K1 > 0 && base < c0; base += step) {
         float v[kR];
 #pragma unroll
         for (int j = 0; j < kR; ++j) {
@@ -173,9 +153,78 @@ block_topk_kernel(Problem p, const float *__restrict__ bs, int32_t *__restrict__
         }
         __syncwarp();
     }
+}
+
+// the k-1 chosen blocks plus the local block, ascending, into out
+__device__ __forceinline__ void write_selection(int32_t *out, unsigned long long best, int K1, int c0, int k, int lane)
+{
     int id = lane < K1 ? (int)(0xFFFFFFFFu - (uint32_t)best) : (lane == K1 ? c0 : 0x7fffffff);
     id = sort_asc_i(id, lane);
     if (lane < k) out[lane] = id;
+}
+
+__global__ void __launch_bounds__(kWarps * 32)
+block_topk_kernel(Problem p, const float *__restrict__ bs, int32_t *__restrict__ sel)
+{
+    __shared__ unsigned long long cand_buf[kWarps][kSeg];
+    const int lane = threadIdx.x & 31;
+    const int wi = threadIdx.x >> 5;
+    const long long row = (long long)blockIdx.x * kWarps + wi;
+    const long long rows = (long long)p.B * p.Nq * p.Hkv;
+    if (row >= rows) return;
+    const int r = (int)(row % p.Hkv);
+    const long long bi = row / p.Hkv;
+    const int i = (int)(bi % p.Nq), b = (int)(bi / p.Nq);
+    const long long pos = (long long)p.q_offset + i;
+    const int c0 = (int)(pos / 128);
+    const int k = p.topk;
+    int32_t *out = sel + (((long long)b * p.Hkv + r) * p.Nq + i) * k;
+
+    if (c0 + 1 <= k) {               // every visible block is selected
+        if (lane < k) out[lane] = lane <= c0 ? lane : -1;
+        return;
+    }
+    const int K1 = k - 1;            // slots the indexer chooses, 0..31
+    unsigned long long best = 0ull;  // lane m: m-th best key so far (0 = empty)
+    warp_topk(bs + row * p.nb, c0, K1, 0, kSeg, cand_buf[wi], best, lane);
+    write_selection(out, best, K1, c0, k, lane);
+}
+
+// Few rows with many blocks (decode): one CTA of kWarps warps per row, warp w
+// taking segments w, w + kWarps, ...; warp 0 then merges the warps' lists
+// (each sorted descending) with the same bitonic merge.
+__global__ void __launch_bounds__(kWarps * 32)
+block_topk_split_kernel(Problem p, const float *__restrict__ bs, int32_t *__restrict__ sel)
+{
+    __shared__ unsigned long long cand_buf[kWarps][kSeg];
+    __shared__ unsigned long long lists[kWarps][32];
+    const int lane = threadIdx.x & 31;
+    const int wi = threadIdx.x >> 5;
+    const long long row = blockIdx.x;
+    const int r = (int)(row % p.Hkv);
+    const long long bi = row / p.Hkv;
+    const int i = (int)(bi % p.Nq), b = (int)(bi / p.Nq);
+    const long long pos = (long long)p.q_offset + i;
+    const int c0 = (int)(pos / 128);
+    const int k = p.topk;
+    int32_t *out = sel + (((long long)b * p.Hkv + r) * p.Nq + i) * k;
+    if (c0 + 1 <= k) {
+        if (wi == 0 && lane < k) out[lane] = lane <= c0 ? lane : -1;
+        return;
+    }
+    const int K1 = k - 1;
+    unsigned long long best = 0ull;
+    warp_topk(bs + row * p.nb, c0, K1, wi * kSeg, kWarps * kSeg, cand_buf[wi], best, lane);
+    lists[wi][lane] = best;
+    __syncthreads();
+    if (wi == 0) {
+#pragma unroll 1
+        for (int w = 1; w < kWarps; ++w) {
+            const unsigned long long rev = lists[w][31 - lane];
+            best = merge_desc64(best > rev ? best : rev, lane);
+        }
+        write_selection(out, best, K1, c0, k, lane);
+    }
 }
 
 }  // namespace
@@ -184,8 +233,12 @@ cudaError_t launch_block_topk(const Problem &p, const float *bs, int32_t *sel, D
                               cudaStream_t s)
 {
     const long long rows = (long long)p.B * p.Nq * p.Hkv;
-    const long long grid = (rows + kWarps - 1) / kWarps;
-    {
+    if (rows * 4 < (long long)p.num_sms && p.nb > 4 * kSeg) {
+        // few long rows: a CTA per row
+        TimedLaunch timed_("block_topk_kernel", s);
+        block_topk_split_kernel<<<(unsigned)rows, kWarps * 32, 0, s>>>(p, bs, sel);
+    } else {
+        const long long grid = (rows + kWarps - 1) / kWarps;
         TimedLaunch timed_("block_topk_kernel", s);
         block_topk_kernel<<<(unsigned)grid, kWarps * 32, 0, s>>>(p, bs, sel);
     }

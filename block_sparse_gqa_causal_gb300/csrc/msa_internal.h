@@ -66,8 +66,11 @@ cudaError_t launch_sparse_fwd_keymajor(const Problem &p, const bf16 *q, const bf
                                        const int32_t *sel, bf16 *o, float *lse, const FwdWork &w, DeviceStatus *st,
                                        cudaStream_t s);
 // Main branch forward (query-major; few queries per selected block, e.g. decode).
+// split_ws: [B*Nq*Hq*nsplit*d] fp32 partial outputs + [B*Nq*Hq*nsplit] float2 (m, l),
+// nsplit = sparse_attn_splits(p); nullptr runs one CTA per (b, i, r)
+int sparse_attn_splits(const Problem &p);
 cudaError_t launch_sparse_attn_fwd(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *v,
-                                   const int32_t *sel, bf16 *o, float *lse, DeviceStatus *st,
+                                   const int32_t *sel, bf16 *o, float *lse, float *split_ws, DeviceStatus *st,
                                    cudaStream_t s);
 // KL forward: per-row KL and lse_idx, then the deterministic scalar mean.
 cudaError_t launch_kl_fwd(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *q_idx,

@@ -8,11 +8,17 @@
 // shared memory and used by all G heads of the group (section 3.2 notes the
 // selected blocks' KV loads can be shared across the group's heads).
 //
-// One CTA (4 warps) per (b, i, r).  The selected blocks are cut into 64-token
-// chunks (the local block stops at the query); chunks stream through a
-// two-stage cp.async pipeline.  Warp w handles tokens [16w, 16w+16) of every
-// chunk with its own online softmax; the four partial states are merged at
-// the end.  MMA rows are the G heads (padded to 16).
+// One CTA (4 warps) per (b, i, r), or, when those are too few to fill the
+// GPU (decode), nsplit CTAs per (b, i, r) each taking a contiguous share of
+// the row's chunks (split-KV, as in flash decoding): they write unnormalised
+// partial states that sparse_attn_merge_kernel folds.  The selected blocks
+// are cut into 64-token chunks (the local block stops at the query); chunks
+// stream through a two-stage cp.async pipeline.  Warp w handles tokens
+// [16w, 16w+16) of every chunk with its own online softmax; the four partial
+// states are merged at the end.  MMA rows are the G heads (padded to 16).
+#include <algorithm>
+#include <type_traits>
+
 #include "msa_internal.h"
 
 namespace msa {
@@ -43,7 +49,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreads)
 sparse_attn_fwd_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__restrict__ k,
                        const bf16 *__restrict__ v, const int32_t *__restrict__ sel,
-                       bf16 *__restrict__ o, float *__restrict__ lse, DeviceStatus *st)
+                       bf16 *__restrict__ o, float *__restrict__ lse, int nsplit, float *__restrict__ part_o,
+                       float2 *__restrict__ part_ml, DeviceStatus *st)
 {
     using S = FwdSmem<D>;
     constexpr int CH = D / 8;
@@ -52,7 +59,7 @@ sparse_attn_fwd_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__rest
     int2 *chunks = reinterpret_cast<int2 *>(smem + S::OFF_CHUNKS);
     __shared__ int n_chunks;
 
-    const int i = blockIdx.x, r = blockIdx.y, b = blockIdx.z;
+    const int i = blockIdx.x / nsplit, sp = blockIdx.x % nsplit, r = blockIdx.y, b = blockIdx.z;
     const int G = p.G;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const long long pos = (long long)p.q_offset + i;
@@ -79,7 +86,9 @@ sparse_attn_fwd_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__rest
     }
     cp_async_commit();
     __syncthreads();
-    const int nc = n_chunks;
+    // this CTA's share of the row's chunks
+    const int c_lo = (int)((long long)n_chunks * sp / nsplit), c_hi = (int)((long long)n_chunks * (sp + 1) / nsplit);
+    const int nc = c_hi - c_lo;
 
     const bf16 *kb = k + ((long long)b * p.kv_rows * p.Hkv + r) * D;
     const bf16 *vb = v + ((long long)b * p.kv_rows * p.Hkv + r) * D;
@@ -87,7 +96,7 @@ sparse_attn_fwd_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__rest
     auto load_chunk = [&](int ci, int stage) {
         uint8_t *sk = smem + S::OFF_STAGES + stage * S::STAGE;
         uint8_t *sv = sk + S::KV_BYTES;
-        const int2 cj = chunks[ci];
+        const int2 cj = chunks[c_lo + ci];
         for (int idx = tid; idx < kChunk * CH; idx += kThreads) {
             const int row = idx / CH, ch = idx % CH;
             const bool ok = row < cj.y;
@@ -120,7 +129,7 @@ sparse_attn_fwd_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__rest
         }
         const uint8_t *sk = smem + S::OFF_STAGES + stage * S::STAGE;
         const uint8_t *sv = sk + S::KV_BYTES;
-        const int len = chunks[ci].y;
+        const int len = chunks[c_lo + ci].y;
         const int kw = warp * 16;           // this warp's first token in the chunk
         if (kw < len) {
             float sc[2][4];
@@ -208,40 +217,109 @@ sparse_attn_fwd_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__rest
         float L = 0.f, acc = 0.f;
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
-            const float f = exp2f(sM[w * 8 + h] - M);
+            const float f = M == -INFINITY ? 0.f : exp2f(sM[w * 8 + h] - M);
             L += f * sL[w * 8 + h];
             acc += f * sO[(w * 8 + h) * D + col];
         }
         const int hh = r * G + h;
-        o[(((long long)b * p.Nq + i) * p.Hq + hh) * D + col] = __float2bfloat16_rn(acc / L);
-        if (col == 0) lse[((long long)b * p.Hq + hh) * p.Nq + i] = (M + log2f(L)) * kLn2;
+        const long long orow = ((long long)b * p.Nq + i) * p.Hq + hh;
+        if (nsplit == 1) {
+            o[orow * D + col] = __float2bfloat16_rn(acc / L);
+            if (col == 0) lse[((long long)b * p.Hq + hh) * p.Nq + i] = (M + log2f(L)) * kLn2;
+        } else {
+            // unnormalised partial state of this share (M = -inf, L = 0 when it holds no token)
+            part_o[(orow * nsplit + sp) * D + col] = acc;
+            if (col == 0) part_ml[orow * nsplit + sp] = make_float2(M, L);
+        }
+    }
+}
+
+// Folds the nsplit partial states of one (b, i, h) row: warp per row.
+template <int D>
+__global__ void __launch_bounds__(256) sparse_attn_merge_kernel(Problem p, int nsplit, const float *__restrict__ part_o,
+                                                                const float2 *__restrict__ part_ml,
+                                                                bf16 *__restrict__ o, float *__restrict__ lse)
+{
+    const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= (long long)p.B * p.Nq * p.Hq) return;
+    const float2 ml = lane < nsplit ? part_ml[row * nsplit + lane] : make_float2(-INFINITY, 0.f);
+    float M = ml.x;
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
+    const float f = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
+    float L = f * ml.y;
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o2);
+    constexpr int PER = D / 32;
+    float acc[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+    // eight shares' rows in flight at a time
+    for (int s0 = 0; s0 < nsplit; s0 += 8) {
+        float x[8][PER];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const float *src = part_o + (row * nsplit + min(s0 + u, nsplit - 1)) * D;
+#pragma unroll
+            for (int e = 0; e < PER; ++e) x[u][e] = __ldg(src + lane + 32 * e);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const float w = s0 + u < nsplit ? __shfl_sync(0xffffffffu, f, (s0 + u) & 31) : 0.f;
+#pragma unroll
+            for (int e = 0; e < PER; ++e) acc[e] = w != 0.f ? fmaf(w, x[u][e], acc[e]) : acc[e];
+        }
+    }
+    const float inv = 1.f / L;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) o[row * D + lane + 32 * e] = __float2bfloat16_rn(acc[e] * inv);
+    if (lane == 0) {
+        const int h = (int)(row % p.Hq);
+        const long long bi = row / p.Hq;
+        const int i = (int)(bi % p.Nq), b = (int)(bi / p.Nq);
+        lse[((long long)b * p.Hq + h) * p.Nq + i] = (M + log2f(L)) * kLn2;
     }
 }
 
 }  // namespace
 
+int sparse_attn_splits(const Problem &p)
+{
+    const long long ctas = (long long)p.Nq * p.Hkv * p.B;
+    if (ctas >= p.num_sms) return 1;
+    // at most 32 shares (the merge holds one per lane) and at most one per 64-token chunk
+    return (int)std::min<long long>(std::min<long long>(32, 2LL * p.topk), (2LL * p.num_sms + ctas - 1) / ctas);
+}
+
 cudaError_t launch_sparse_attn_fwd(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *v,
-                                   const int32_t *sel, bf16 *o, float *lse, DeviceStatus *st,
+                                   const int32_t *sel, bf16 *o, float *lse, float *split_ws, DeviceStatus *st,
                                    cudaStream_t s)
 {
-    dim3 grid(p.Nq, p.Hkv, p.B);
-    if (p.d == 128) {
-        const int sm = FwdSmem<128>::SMEM;
-        cudaFuncSetAttribute(sparse_attn_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+    const int nsplit = split_ws ? sparse_attn_splits(p) : 1;
+    const long long rows = (long long)p.B * p.Nq * p.Hq;
+    float *part_o = split_ws;
+    float2 *part_ml = split_ws ? reinterpret_cast<float2 *>(split_ws + rows * nsplit * p.d) : nullptr;
+    dim3 grid(p.Nq * nsplit, p.Hkv, p.B);
+    auto run = [&](auto dtag) {
+        constexpr int D = decltype(dtag)::value;
+        const int sm = FwdSmem<D>::SMEM;
+        cudaFuncSetAttribute(sparse_attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
         {
             TimedLaunch timed_("sparse_attn_fwd_kernel", s);
-            sparse_attn_fwd_kernel<128><<<grid, kThreads, sm, s>>>(p, q, k, v, sel, o, lse, st);
+            sparse_attn_fwd_kernel<D><<<grid, kThreads, sm, s>>>(p, q, k, v, sel, o, lse, nsplit, part_o, part_ml, st);
         }
         note_launch();
-    } else {
-        const int sm = FwdSmem<64>::SMEM;
-        cudaFuncSetAttribute(sparse_attn_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
-        {
-            TimedLaunch timed_("sparse_attn_fwd_kernel", s);
-            sparse_attn_fwd_kernel<64><<<grid, kThreads, sm, s>>>(p, q, k, v, sel, o, lse, st);
+        if (nsplit > 1) {
+            {
+                TimedLaunch timed_("sparse_attn_merge_kernel", s);
+                sparse_attn_merge_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p, nsplit, part_o, part_ml, o, lse);
+            }
+            note_launch();
         }
-        note_launch();
-    }
+    };
+    if (p.d == 128) run(std::integral_constant<int, 128>{});
+    else run(std::integral_constant<int, 64>{});
     return cudaGetLastError();
 }
 

@@ -52,3 +52,37 @@ def test_decode_step_parity(decode_case, step):
     o_ref, lse_ref = oracle.sparse_fwd(osh, q, x["k"], x["v"], sel_g, rows)
     assert_close(bf16_to_np(o).reshape(o_ref.shape), o_ref, "o", bf16_out=True)
     assert_close(lse.cpu().numpy().reshape(lse_ref.shape), lse_ref, "lse", max_abs=1e-3, rel_l2=1e-5)
+
+
+def test_decode_long_cache_split_selection():
+    """A cache of 2,088 blocks with two (query, group) rows: the selection runs
+    one CTA per row (segments spread over its warps, then merged) and the
+    forward splits each row's chunks over several CTAs (split-KV)."""
+    import torch
+    from block_sparse_gqa_causal_gb300 import api
+    from block_sparse_gqa_causal_gb300.inputs import f32_to_bf16_bits
+    B, Hq, Hkv, d, k = 1, 4, 2, 64, 16
+    cap = 2088 * 128
+    pos = cap - 37                                   # the last block is partial
+    rng = np.random.default_rng(23)
+    bf = lambda shape: f32_to_bf16_bits(rng.standard_normal(shape).astype(np.float32))
+    x = {"q": bf((B, 1, Hq, d)), "q_idx": bf((B, 1, Hkv, d)), "k": bf((B, cap, Hkv, d)), "v": bf((B, cap, Hkv, d)),
+         "k_idx": bf((B, cap, d))}
+    sh = api.Shape(B=B, Nq=1, Nk=pos + 1, Hq=Hq, Hkv=Hkv, d=d, d_idx=d, topk=k, q_offset=pos, kv_rows=cap)
+    t = {n: to_torch(a) for n, a in x.items()}
+    sel, bs = api.index_select(sh, t["q_idx"], t["k_idx"], return_scores=True)
+    o, lse = api.sparse_attn_fwd(sh, t["q"], t["k"], t["v"], sel)
+    torch.cuda.synchronize()
+    osh = oracle.Shape(B=B, Nq=1, Nk=pos + 1, Hq=Hq, Hkv=Hkv, d=d, d_idx=d, topk=k, q_offset=pos, kv_rows=cap)
+    rows = np.arange(B)
+    bs_o = oracle.block_scores(osh, x["q_idx"], x["k_idx"], rows)
+    bs_g = bs.cpu().numpy().reshape(B, Hkv, -1)
+    vis = np.isfinite(bs_o)
+    assert_close(bs_g[vis], bs_o[vis], "block scores", max_abs=2e-3, rel_l2=1e-4)
+    sel_g = sel.cpu().numpy()[:, :, 0, :]
+    sel_o = oracle.select(osh, bs_o, rows)
+    exact, tol = check_selection(k, 128, pos, 1, rows, sel_g, sel_o, bs_o)
+    assert exact >= 1
+    o_ref, lse_ref = oracle.sparse_fwd(osh, x["q"], x["k"], x["v"], sel_g, rows)
+    assert_close(bf16_to_np(o).reshape(o_ref.shape), o_ref, "o", bf16_out=True)
+    assert_close(lse.cpu().numpy().reshape(lse_ref.shape), lse_ref, "lse", max_abs=1e-3, rel_l2=1e-5)
