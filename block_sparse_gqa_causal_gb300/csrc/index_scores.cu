@@ -204,7 +204,10 @@ index_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_
                 float mx = -INFINITY;
                 if (m < mt) {
                     const bool full_vis = (j0 + 127 <= pos_first) && (j0 + 128 <= p.Nk);
+                    // last visible key offset of the block for this row (masked blocks only)
+                    const int lim = (int)max(-1LL, min(min(pos, (long long)p.Nk - 1) - j0, 127LL));
                     const uint32_t base = tmem + lane_base + (uint32_t)((a * 2 + m) * 128);
+                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // four independent max chains
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         uint32_t v0[32], v1[32];
@@ -212,19 +215,30 @@ index_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_
                         tc::tmem_ld32_nowait(base + h * 64 + 32, v1);
                         tc::tmem_wait32(v0);
                         tc::tmem_wait32(v1);
+                        if (h == 1) {
+                            // the accumulator is in registers: hand it back to the MMA
+                            tc::fence_before_sync();
+                            __syncwarp();
+                            if (lane == 0) tc::mbar_arrive(&acc_empty[a]);
+                        }
                         if (full_vis) {
 #pragma unroll
                             for (int jj = 0; jj < 32; ++jj)
-                                mx = fmaxf(mx, fmaxf(__uint_as_float(v0[jj]), __uint_as_float(v1[jj])));
+                                m4[jj & 3] = fmaxf(m4[jj & 3], fmaxf(__uint_as_float(v0[jj]), __uint_as_float(v1[jj])));
                         } else {
 #pragma unroll
                             for (int jj = 0; jj < 32; ++jj) {
-                                const long long j = j0 + h * 64 + jj;
-                                if (j <= pos && j < p.Nk) mx = fmaxf(mx, __uint_as_float(v0[jj]));
-                                if (j + 32 <= pos && j + 32 < p.Nk) mx = fmaxf(mx, __uint_as_float(v1[jj]));
+                                const int jo = h * 64 + jj;
+                                const float a0 = jo <= lim ? __uint_as_float(v0[jj]) : -INFINITY;
+                                const float a1 = jo + 32 <= lim ? __uint_as_float(v1[jj]) : -INFINITY;
+                                m4[jj & 3] = fmaxf(m4[jj & 3], fmaxf(a0, a1));
                             }
                         }
                     }
+                    mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                } else {
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&acc_empty[a]);
                 }
                 grp[u] = mx * p.scale_idx;   // a positive scale commutes with max
                 if (sel) {
@@ -248,9 +262,6 @@ index_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_
                         }
                     }
                 }
-                tc::fence_before_sync();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&acc_empty[a]);
             }
             // store this row's scores for blocks c_begin+n0 .. (at most 8)
             const int c_lo = c_begin + n0;
