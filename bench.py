@@ -266,37 +266,38 @@ def main():
     lse_idx = torch.empty((w.B, w.Hkv, w.N), dtype=torch.float32, device=dev)
     kl_rows = torch.empty((w.B, w.Hkv, w.N), dtype=torch.float32, device=dev)
     kl_loss = torch.empty((), dtype=torch.float32, device=dev)
-    ws = {op: api.new_workspace(sh, op, dev) for op in range(3 if w.train else 2)}
     if w.train:
-        ws[3] = api.new_workspace(sh, api.OP_FUSED_BWD_KL, dev)
+        ws = {"step": api.new_workspace(sh, api.OP_TRAIN_STEP, dev)}
+    else:
+        ws = {op: api.new_workspace(sh, op, dev) for op in range(2)}
     grads = tuple(torch.empty_like(d[n]) for n in ("q", "k", "v", "q_idx", "k_idx")) if w.train else None
     stream = torch.cuda.current_stream(dev)
 
+    step_out = None
+    if w.train:
+        step_out = {"sel": sel, "o": o, "lse": lse, "lse_idx": lse_idx, "kl_rows": kl_rows, "kl_loss": kl_loss,
+                    "dq": grads[0], "dk": grads[1], "dv": grads[2], "dq_idx": grads[3], "dk_idx": grads[4]}
+
     def step(ev=None, x=d):
         if ev: ev[0].record(stream)
-        api.index_select(sh, x["q_idx"], x["k_idx"], sel_idx=sel, workspace=ws[0])
-        if ev: ev[1].record(stream)
-        api.sparse_attn_fwd(sh, x["q"], x["k"], x["v"], sel, o=o, lse=lse, workspace=ws[1])
-        if ev: ev[2].record(stream)
         if w.train:
-            # lse_idx first (the backward needs it); the KL loss of the step comes
-            # out of the fused backward, which recomputes the teacher anyway
-            api.kl_fwd(sh, x["q"], x["k"], x["q_idx"], x["k_idx"], sel, lse, 1.0, lse_idx=lse_idx, lse_only=True,
-                       workspace=ws[2])
-            if ev: ev[3].record(stream)
-            api.fused_bwd(sh, x["q"], x["k"], x["v"], o, x["d_o"], lse, x["q_idx"], x["k_idx"], sel, lse_idx, 1.0,
-                          grads=grads, with_kl=True, kl_rows=kl_rows, kl_loss=kl_loss, workspace=ws[3])
-            if ev: ev[4].record(stream)
+            # one call: selection, forward, lse_idx, fused backward with the step's KL
+            # loss (the backward recomputes the teacher anyway), one inverse index
+            api.train_step(sh, x["q"], x["k"], x["v"], x["q_idx"], x["k_idx"], x["d_o"], 1.0, out=step_out,
+                           workspace=ws["step"])
+        else:
+            api.index_select(sh, x["q_idx"], x["k_idx"], sel_idx=sel, workspace=ws[0])
+            api.sparse_attn_fwd(sh, x["q"], x["k"], x["v"], sel, o=o, lse=lse, workspace=ws[1])
+        if ev: ev[1].record(stream)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
-    for op in ws:
-        api.check_device_status(ws[op])
+    for key in ws:
+        api.check_device_status(ws[key])
 
     # ---- device-resident timed region
-    nph = 5 if w.train else 3
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nph)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     clocks = ClockSampler(dev.index if world == 1 else local)
     clocks.start()
     barrier(world)
@@ -317,8 +318,18 @@ def main():
     clk = clocks.stop()
     elapsed_ms = t_start.elapsed_time(t_end)
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
-    phase_names = ["index_select", "sparse_attn_fwd", "kl_fwd", "fused_bwd"][: nph - 1]
-    phase_ms = {n: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j, n in enumerate(phase_names)}
+    # per phase: the library's kernels grouped by the step they belong to (the one-call
+    # training step leaves no boundary between phases to put events on)
+    phase_of = {"index_scores_tc_kernel": "index_select", "block_topk_kernel": "index_select",
+                "sparse_fwd_tc_kernel": "sparse_attn_fwd", "sparse_fwd_combine_kernel": "sparse_attn_fwd",
+                "sparse_attn_fwd_kernel": "sparse_attn_fwd", "sparse_attn_merge_kernel": "sparse_attn_fwd",
+                "index_count_kernel": "sparse_attn_fwd", "index_cta_scan_kernel": "sparse_attn_fwd",
+                "index_bucket_scan_kernel": "sparse_attn_fwd", "index_fill_kernel": "sparse_attn_fwd",
+                "kl_index_tc_kernel": "kl_fwd", "kl_combine_kernel": "kl_fwd"}
+    phase_names = ["index_select", "sparse_attn_fwd"] + (["kl_fwd", "fused_bwd"] if w.train else [])
+    phase_ms = {n: 0.0 for n in phase_names}
+    for kname, (_, tot) in ktimes.items():
+        phase_ms[phase_of.get(kname, "fused_bwd" if w.train else "sparse_attn_fwd")] += tot / args.steps
 
     fl = useful_flops(w)
     step_flops = sum(fl.values())

@@ -1,5 +1,6 @@
 // api.cu -- the C-ABI of libmsa.so (declared in include/msa.h): argument
 // validation, workspace carve-up and kernel launches on the caller's stream.
+#include <algorithm>
 #include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
@@ -165,6 +166,24 @@ size_t bwdkl_bytes(const Problem &p)
     return klrows_bytes(p) + kl_bytes(p) + align256(rows * 4);
 }
 
+// one training step: the shared inverse index, scores scratch (unfused
+// selection only), forward partials, the KL index pass's partials, the
+// backward with its KL terms; shapes outside the shared-index path run the
+// four phases one after another in the same workspace, so the largest suffices
+bool train_shared_index(const Problem &p) { return fwd_keymajor(p) && bwd_tc(p); }
+size_t train_bytes(const Problem &p)
+{
+    if (!train_shared_index(p)) {
+        size_t n = bs_bytes(p);
+        n = std::max(n, fwd_bytes(p));
+        n = std::max(n, klrows_bytes(p) + kl_bytes(p));
+        return std::max(n, bwd_bytes(p) + bwdkl_bytes(p));
+    }
+    const size_t rows = (size_t)p.B * p.Nq * p.Hq * p.topk;
+    return index_bytes(p) + (index_select_fused(p) ? 0 : bs_bytes(p)) + align256(rows * p.d * 2) + align256(rows * 8) +
+           align256(kl_part_count(p) * 16) + bwd_bytes(p) - index_bytes(p) + bwdkl_bytes(p);
+}
+
 #define REQUIRE_PTR(ptr, name)                                                                         \
     do {                                                                                               \
         if (!(ptr)) return fail(MSA_ERR_INVALID_ARGUMENT, "%s is NULL", name);                         \
@@ -275,6 +294,7 @@ size_t msa_workspace_size(const msa_shape *shape, int op)
     case MSA_OP_KL_FWD: return kStatusBytes + klrows_bytes(p) + kl_bytes(p);
     case MSA_OP_FUSED_BWD: return kStatusBytes + bwd_bytes(p);
     case MSA_OP_FUSED_BWD_KL: return kStatusBytes + bwd_bytes(p) + bwdkl_bytes(p);
+    case MSA_OP_TRAIN_STEP: return kStatusBytes + train_bytes(p);
     default: fail(MSA_ERR_INVALID_ARGUMENT, "unknown op %d", op); return 0;
     }
 }
@@ -495,6 +515,94 @@ msa_status msa_fused_bwd_kl(const msa_shape *shape, const void *q, const void *k
 {
     return fused_bwd_impl(shape, q, k, v, o, d_o, lse, q_idx, k_idx, sel_idx, lse_idx, kl_coef, dq, dk, dv, dq_idx,
                           dk_idx, true, kl_rows, kl_loss, workspace, workspace_bytes, stream);
+}
+
+msa_status msa_train_step(const msa_shape *shape, const void *q, const void *k, const void *v, const void *q_idx,
+                          const void *k_idx, const void *d_o, float kl_coef, int32_t *sel_idx, void *o, float *lse,
+                          float *lse_idx, float *kl_rows, float *kl_loss, void *dq, void *dk, void *dv, void *dq_idx,
+                          void *dk_idx, void *workspace, size_t workspace_bytes, void *stream)
+{
+    Problem p;
+    msa_status st = make_problem(shape, p);
+    if (st != MSA_OK) return st;
+    if (p.q_offset != 0 || p.Nq != p.Nk || p.kv_rows != p.Nk)
+        return fail(MSA_ERR_UNSUPPORTED, "train_step needs q_offset == 0, Nq == Nk and kv_rows == Nk");
+    REQUIRE_PTR(q, "q");
+    REQUIRE_PTR(k, "k");
+    REQUIRE_PTR(v, "v");
+    REQUIRE_PTR(q_idx, "q_idx");
+    REQUIRE_PTR(k_idx, "k_idx");
+    REQUIRE_PTR(d_o, "d_o");
+    REQUIRE_PTR(o, "o");
+    REQUIRE_PTR(dq, "dq");
+    REQUIRE_PTR(dk, "dk");
+    REQUIRE_PTR(dv, "dv");
+    REQUIRE_PTR(dq_idx, "dq_idx");
+    REQUIRE_PTR(dk_idx, "dk_idx");
+    if (!sel_idx || !lse || !lse_idx || !kl_loss)
+        return fail(MSA_ERR_INVALID_ARGUMENT, "sel_idx, lse, lse_idx and kl_loss must be non-NULL");
+    if (!isfinite(kl_coef)) return fail(MSA_ERR_INVALID_ARGUMENT, "kl_coef must be finite");
+    st = check_ws(workspace, workspace_bytes, kStatusBytes + train_bytes(p));
+    if (st != MSA_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!train_shared_index(p)) {
+        // the four phases in turn, each carving the same workspace
+        if ((st = msa_index_select(shape, q_idx, k_idx, sel_idx, nullptr, workspace, workspace_bytes, stream)) != MSA_OK)
+            return st;
+        if ((st = msa_sparse_attn_fwd(shape, q, k, v, sel_idx, o, lse, workspace, workspace_bytes, stream)) != MSA_OK)
+            return st;
+        if ((st = msa_kl_fwd(shape, q, k, q_idx, k_idx, sel_idx, lse, kl_coef, lse_idx, nullptr, nullptr, workspace,
+                             workspace_bytes, stream)) != MSA_OK)
+            return st;
+        return msa_fused_bwd_kl(shape, q, k, v, o, d_o, lse, q_idx, k_idx, sel_idx, lse_idx, kl_coef, dq, dk, dv, dq_idx,
+                                dk_idx, kl_rows, kl_loss, workspace, workspace_bytes, stream);
+    }
+    DeviceStatus *ds = static_cast<DeviceStatus *>(workspace);
+    Carve cv{static_cast<char *>(workspace)};
+    BwdWork w{};
+    carve_index(cv, p, w);
+    float *bs_scratch = index_select_fused(p) ? nullptr : cv.take<float>((size_t)p.B * p.Nq * p.Hkv * p.nb);
+    const size_t rows = (size_t)p.B * p.Nq * p.Hq * p.topk;
+    FwdWork fw;
+    fw.part = cv.take<bf16>(rows * p.d);
+    fw.stats = cv.take<float2>(rows);
+    KlWork kw;
+    kw.part = cv.take<float4>(kl_part_count(p));
+    kw.pt = nullptr;                                   // lse_idx only: the loss comes from the backward
+    w.D = cv.take<float>((size_t)p.B * p.Hq * p.Nq);
+    w.dki_acc = cv.take<float>((size_t)p.B * p.Nk * p.d_idx);
+    const size_t slots = (size_t)p.B * p.Nq * p.topk;
+    w.dq_part = cv.take<bf16>(slots * p.Hq * p.d);
+    w.dqi_part = cv.take<bf16>(slots * p.Hkv * p.d_idx);
+    w.pt = cv.take<__half>((slots * p.Hkv + (size_t)8 * p.B * p.Hkv * p.nb) * 128);
+    w.pt_off = cv.take<int32_t>((size_t)p.B * p.Hkv * p.nb + 1);
+    float *rows_kl = kl_rows ? kl_rows : cv.take<float>((size_t)p.B * p.Hkv * p.Nq);
+    w.kla = cv.take<float>(slots * p.Hkv);
+    w.klb = cv.take<float>(slots * p.Hkv * 4);
+    w.kl_rows = rows_kl;
+    // one inverse index of the selection serves the forward, the KL pass and the backward
+    fw.bucket_cnt = kw.bucket_cnt = w.bucket_cnt;
+    fw.bucket_off = kw.bucket_off = w.bucket_off;
+    fw.bucket_scratch = kw.bucket_scratch = w.bucket_scratch;
+    fw.bucket_q = kw.bucket_q = w.bucket_q;
+    fw.index_ready = kw.index_ready = w.index_ready = true;
+    const bf16 *bq = static_cast<const bf16 *>(q), *bk = static_cast<const bf16 *>(k), *bv = static_cast<const bf16 *>(v);
+    const bf16 *bqi = static_cast<const bf16 *>(q_idx), *bki = static_cast<const bf16 *>(k_idx);
+    cudaError_t e = launch_index_select(p, bqi, bki, nullptr, bs_scratch, sel_idx, ds, s);
+    if (e != cudaSuccess) return cuda_fail(e, "train_step: selection");
+    if ((e = launch_inverse_index(p, sel_idx, w.bucket_cnt, w.bucket_off, w.bucket_scratch, w.bucket_q, ds, s)) != cudaSuccess)
+        return cuda_fail(e, "train_step: inverse index");
+    if ((e = launch_sparse_fwd_keymajor(p, bq, bk, bv, sel_idx, static_cast<bf16 *>(o), lse, fw, ds, s)) != cudaSuccess)
+        return cuda_fail(e, "train_step: forward");
+    if ((e = launch_kl_keymajor(p, bq, bk, bqi, bki, sel_idx, lse, lse_idx, nullptr, kw, ds, s)) != cudaSuccess)
+        return cuda_fail(e, "train_step: lse_idx");
+    if ((e = launch_fused_bwd(p, bq, bk, bv, static_cast<const bf16 *>(o), static_cast<const bf16 *>(d_o), lse, bqi, bki,
+                              sel_idx, lse_idx, kl_coef, static_cast<bf16 *>(dq), static_cast<bf16 *>(dk),
+                              static_cast<bf16 *>(dv), static_cast<bf16 *>(dq_idx), static_cast<bf16 *>(dk_idx), w, ds,
+                              s)) != cudaSuccess)
+        return cuda_fail(e, "train_step: backward");
+    if ((e = launch_kl_reduce(p, rows_kl, kl_coef, kl_loss, s)) != cudaSuccess) return cuda_fail(e, "train_step: loss");
+    return MSA_OK;
 }
 
 msa_status msa_check_device_status(void *workspace, void *stream)

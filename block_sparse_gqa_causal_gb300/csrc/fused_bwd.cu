@@ -671,7 +671,8 @@ cudaError_t launch_fused_bwd(const Problem &p, const bf16 *q, const bf16 *k, con
         else bwd_rowdot_kernel<64><<<(unsigned)((rows + 63) / 64), 256, 0, s>>>(p, o, d_o, w.D);
     }
     note_launch();
-    if ((e = launch_inverse_index(p, sel, w.bucket_cnt, w.bucket_off, w.bucket_scratch, w.bucket_q, st, s)) != cudaSuccess)
+    if (!w.index_ready &&
+        (e = launch_inverse_index(p, sel, w.bucket_cnt, w.bucket_off, w.bucket_scratch, w.bucket_q, st, s)) != cudaSuccess)
         return e;
 
     if (tc) {

@@ -366,12 +366,17 @@ cudaError_t launch_index_scores(const Problem &p, const bf16 *q_idx, const bf16 
                           : launch_t<64>(p, q_idx, k_idx, bs, nullptr, st, s);
 }
 
-cudaError_t launch_index_select(const Problem &p, const bf16 *q_idx, const bf16 *k_idx, float *bs_out,
-                                float *bs_scratch, int32_t *sel, DeviceStatus *st, cudaStream_t s)
+bool index_select_fused(const Problem &p)
 {
     int tiles, splits, span;
     plan_grid(p, tiles, splits, span);
-    if (splits == 1 && p.topk <= 16)   // every CTA sees all blocks of its rows: fused selection
+    return splits == 1 && p.topk <= 16;   // every CTA sees all blocks of its rows
+}
+
+cudaError_t launch_index_select(const Problem &p, const bf16 *q_idx, const bf16 *k_idx, float *bs_out,
+                                float *bs_scratch, int32_t *sel, DeviceStatus *st, cudaStream_t s)
+{
+    if (index_select_fused(p))   // every CTA sees all blocks of its rows: fused selection
         return p.d_idx == 128 ? launch_t<128>(p, q_idx, k_idx, bs_out, sel, st, s)
                               : launch_t<64>(p, q_idx, k_idx, bs_out, sel, st, s);
     float *bs = bs_out ? bs_out : bs_scratch;

@@ -677,7 +677,8 @@ cudaError_t launch_kl_keymajor(const Problem &p, const bf16 *q, const bf16 *k, c
                                const int32_t *sel, const float *lse, float *lse_idx, float *kl_rows, const KlWork &w,
                                DeviceStatus *st, cudaStream_t s)
 {
-    cudaError_t e = launch_inverse_index(p, sel, w.bucket_cnt, w.bucket_off, w.bucket_scratch, w.bucket_q, st, s);
+    cudaError_t e = w.index_ready ? cudaSuccess
+                                  : launch_inverse_index(p, sel, w.bucket_cnt, w.bucket_off, w.bucket_scratch, w.bucket_q, st, s);
     if (e != cudaSuccess) return e;
     if (w.pt) {
         e = p.d == 128 ? launch_teacher_d<128>(p, q, k, lse, w, st, s) : launch_teacher_d<64>(p, q, k, lse, w, st, s);

@@ -56,11 +56,14 @@ cudaError_t launch_block_topk(const Problem &p, const float *bs, int32_t *sel, D
 // else scores to bs_out (or bs_scratch) and the separate top-k kernel.
 cudaError_t launch_index_select(const Problem &p, const bf16 *q_idx, const bf16 *k_idx, float *bs_out,
                                 float *bs_scratch, int32_t *sel, DeviceStatus *st, cudaStream_t s);
+// true when launch_index_select runs the fused form (no score scratch needed)
+bool index_select_fused(const Problem &p);
 // Key-major main branch forward (many queries per selected block).
 struct FwdWork {
     bf16 *part;          // [B, Nq, Hq, topk, d] unnormalised partial outputs per selected block
     float2 *stats;       // [B, Nq, Hq, topk] (row max in log2 units, row sum)
     int32_t *bucket_cnt, *bucket_off, *bucket_scratch, *bucket_q;
+    bool index_ready = false;   // the inverse index of sel is already in bucket_* (built once per step)
 };
 cudaError_t launch_sparse_fwd_keymajor(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *v,
                                        const int32_t *sel, bf16 *o, float *lse, const FwdWork &w, DeviceStatus *st,
@@ -81,6 +84,7 @@ struct KlWork {
     float4 *part;        // [B, Hkv, Nq, topk, kl_part_count / (B*Hkv*Nq*topk)] partial sums
     __half *pt;          // [B*Hkv*Nq*topk entries, 128] teacher per (bucket entry, key); nullptr: lse_idx only
     int32_t *bucket_cnt, *bucket_off, *bucket_scratch, *bucket_q;
+    bool index_ready = false;
 };
 // float4 partials the key-major KL writes (several per (query, group, slot))
 size_t kl_part_count(const Problem &p);
@@ -115,6 +119,7 @@ struct BwdWork {
     int32_t *bucket_off; // [B*Hkv*nb + 1]
     int32_t *bucket_scratch; // inverse_index_scratch_ints(p)
     int32_t *bucket_q;   // [B*Hkv*Nq*topk]  query rows per (b, r, block)
+    bool index_ready;    // bucket_* already hold the inverse index of sel
 };
 cudaError_t launch_fused_bwd(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *v,
                              const bf16 *o, const bf16 *d_o, const float *lse, const bf16 *q_idx,

@@ -584,7 +584,8 @@ cudaError_t launch_sparse_fwd_keymajor(const Problem &p, const bf16 *q, const bf
                                        const int32_t *sel, bf16 *o, float *lse, const FwdWork &w, DeviceStatus *st,
                                        cudaStream_t s)
 {
-    cudaError_t e = launch_inverse_index(p, sel, w.bucket_cnt, w.bucket_off, w.bucket_scratch, w.bucket_q, st, s);
+    cudaError_t e = w.index_ready ? cudaSuccess
+                                  : launch_inverse_index(p, sel, w.bucket_cnt, w.bucket_off, w.bucket_scratch, w.bucket_q, st, s);
     if (e != cudaSuccess) return e;
     e = p.d == 128 ? launch_d<128>(p, q, k, v, sel, w, st, s) : launch_d<64>(p, q, k, v, sel, w, st, s);
     if (e != cudaSuccess) return e;

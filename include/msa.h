@@ -83,7 +83,8 @@ enum {
     MSA_OP_SPARSE_ATTN_FWD = 1,
     MSA_OP_KL_FWD = 2,
     MSA_OP_FUSED_BWD = 3,
-    MSA_OP_FUSED_BWD_KL = 4
+    MSA_OP_FUSED_BWD_KL = 4,
+    MSA_OP_TRAIN_STEP = 5
 };
 
 /* Bytes of workspace `op` needs for `shape` (0 on an invalid shape). */
@@ -166,6 +167,23 @@ msa_status msa_fused_bwd_kl(const msa_shape *shape, const void *q, const void *k
                             void *dq, void *dk, void *dv, void *dq_idx, void *dk_idx,
                             float *kl_rows, float *kl_loss,
                             void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * One training step of the layer (section 3.2): msa_index_select, then
+ * msa_sparse_attn_fwd, msa_kl_fwd in its lse_idx-only form and
+ * msa_fused_bwd_kl, with their definitions, layouts and outputs (sel_idx,
+ * o, lse, lse_idx, kl_rows (may be NULL), *kl_loss, and the five gradients
+ * from d_o).  On the key-major tensor-core path (prefill with >= 8 queries
+ * per selected block on average, d = d_idx = 128) the per-block query lists
+ * of the selection are built once for all phases; elsewhere the phases run
+ * one after another.  Training layout only (q_offset == 0, Nq == Nk,
+ * kv_rows == Nk).  Workspace: msa_workspace_size(MSA_OP_TRAIN_STEP).
+ */
+msa_status msa_train_step(const msa_shape *shape, const void *q, const void *k, const void *v,
+                          const void *q_idx, const void *k_idx, const void *d_o, float kl_coef,
+                          int32_t *sel_idx, void *o, float *lse, float *lse_idx, float *kl_rows,
+                          float *kl_loss, void *dq, void *dk, void *dv, void *dq_idx, void *dk_idx,
+                          void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Index selection without any allocation, for callers that cannot allocate

@@ -1,8 +1,9 @@
 """Parity at the benchmark's full size, in the launch configuration bench.py
 times: train_n128k (B=1, N=131,072, Hq=64, Hkv=8, d=d_idx=128, k=16, the
-bench's seeded inputs), run as one training step -- selection fused into the
-index kernel with no stored scores, the key-major forward, the lse_idx-only
-KL pass, the fused backward that returns the KL loss.
+bench's seeded inputs), run as the bench runs it: one msa_train_step call --
+selection fused into the index kernel with no stored scores, one inverse
+index, the key-major forward, the lse_idx-only KL pass, the fused backward
+that returns the KL loss.
 
 The oracle recomputes sampled outputs one row (or one key block) at a time:
 the selection, O and LSE, lse_idx, the KL of each sampled row, dq and dq_idx
@@ -35,18 +36,13 @@ def step():
     names = ["q", "k", "v", "q_idx", "k_idx", "d_o"]
     d = {n: torch.from_numpy(x[n].view(np.int16)).view(torch.bfloat16).to(dev) for n in names}
     sh = api.Shape(B=w.B, Nq=w.N, Nk=w.N, Hq=w.Hq, Hkv=w.Hkv, d=w.d, d_idx=w.d_idx, topk=w.topk)
-    # the bench's step, call for call
-    sel = torch.empty((w.B, w.Hkv, w.N, w.topk), dtype=torch.int32, device=dev)
-    api.index_select(sh, d["q_idx"], d["k_idx"], sel_idx=sel)
-    o, lse = api.sparse_attn_fwd(sh, d["q"], d["k"], d["v"], sel)
-    _, lse_idx, _ = api.kl_fwd(sh, d["q"], d["k"], d["q_idx"], d["k_idx"], sel, lse, KL_COEF, lse_only=True)
-    kl_rows = torch.empty((w.B, w.Hkv, w.N), dtype=torch.float32, device=dev)
-    out = api.fused_bwd(sh, d["q"], d["k"], d["v"], o, d["d_o"], lse, d["q_idx"], d["k_idx"], sel, lse_idx, KL_COEF,
-                        with_kl=True, kl_rows=kl_rows)
+    # the bench's step
+    out = api.train_step(sh, d["q"], d["k"], d["v"], d["q_idx"], d["k_idx"], d["d_o"], KL_COEF)
     torch.cuda.synchronize()
-    res = {"sel": sel.cpu().numpy(), "o": bf16_to_np(o), "lse": lse.cpu().numpy(), "lse_idx": lse_idx.cpu().numpy(),
-           "kl_rows": kl_rows.cpu().numpy(), "kl_loss": float(out[5].item()),
-           "grads": [bf16_to_np(g) for g in out[:5]]}
+    res = {"sel": out["sel"].cpu().numpy(), "o": bf16_to_np(out["o"]), "lse": out["lse"].cpu().numpy(),
+           "lse_idx": out["lse_idx"].cpu().numpy(), "kl_rows": out["kl_rows"].cpu().numpy(),
+           "kl_loss": float(out["kl_loss"].item()),
+           "grads": [bf16_to_np(out[n]) for n in ("dq", "dk", "dv", "dq_idx", "dk_idx")]}
     osh = oracle.Shape(B=w.B, Nq=w.N, Nk=w.N, Hq=w.Hq, Hkv=w.Hkv, d=w.d, d_idx=w.d_idx, topk=w.topk)
     rng = np.random.default_rng(2024)
     fixed = [0, 1, 127, 128, 129, 2047, 2048, 2049, 65535, 65536, w.N - 129, w.N - 1]

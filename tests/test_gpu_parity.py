@@ -81,6 +81,9 @@ def run_case(case, seed=0):
         res["grads_kl"] = [bf16_to_np(g) for g in out[:5]]
         res["kl_loss_bwd"] = float(out[5].item())
         res["kl_rows_bwd"] = out[6].cpu().numpy()
+        # the same step through the one-call entry point
+        ts = api.train_step(sh, t["q"], t["k"], t["v"], t["q_idx"], t["k_idx"], t["d_o"], 0.75)
+        res["train_step"] = {n: (bf16_to_np(v) if v.dtype == torch.bfloat16 else v.cpu().numpy()) for n, v in ts.items()}
     ws = api.new_workspace(sh, api.OP_INDEX_SELECT)
     api.check_device_status(ws)
     torch.cuda.synchronize()
@@ -220,3 +223,21 @@ def test_fused_bwd_kl_parity(case):
     # fallback path's fp32 atomics vary run to run
     for a, b, n in zip(res["grads_kl"], res["grads"], ("dq", "dk", "dv", "dq_idx", "dk_idx")):
         assert_close(a, b, n + " (fused_bwd_kl vs fused_bwd)", rel_l2=1e-3, bf16_out=True)
+
+
+@pytest.mark.parametrize("case", TRAIN_CASES, ids=[c[0] for c in TRAIN_CASES])
+def test_train_step_matches_the_phase_calls(case):
+    """msa_train_step (one inverse index for all phases) gives what the four
+    separate calls give: the selection, forward, lse_idx and KL exactly (same
+    kernels, fixed reduction orders), the gradients within bf16 rounding (the
+    order of queries inside a block's list, hence of dK/dV accumulation, varies)."""
+    x, osh, res = run_case(case)
+    ts = res["train_step"]
+    assert np.array_equal(ts["sel"], res["sel"])
+    assert np.array_equal(ts["o"], res["o"])
+    assert np.array_equal(ts["lse"], res["lse"])
+    assert np.array_equal(ts["lse_idx"], res["lse_idx_only"])
+    assert_close(ts["kl_rows"], res["kl_rows_bwd"], "kl_rows (train_step)", max_abs=1e-5, rel_l2=1e-6)
+    assert abs(float(ts["kl_loss"]) - res["kl_loss_bwd"]) <= 1e-5 * abs(res["kl_loss_bwd"]) + 1e-7
+    for n, ref in zip(("dq", "dk", "dv", "dq_idx", "dk_idx"), res["grads"]):
+        assert_close(ts[n], ref, n + " (train_step)", rel_l2=1e-3, bf16_out=True)
