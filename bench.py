@@ -68,27 +68,44 @@ def useful_flops(w, positions=None):
 
 def kernel_work(w):
     """Algorithmic work of one launch of each library kernel that can
-    dominate a step: (FLOPs, 'tensor') for the contractions, (bytes, 'hbm')
-    for the streaming kernels.  Closed forms over the selected work."""
+    dominate a step, closed forms over the selected work: {"flops": F,
+    "bytes": B}, either may be None.  Bytes count what the algorithm must
+    move through HBM once: per selected (query, group, block) slot the rows a
+    key-major kernel gathers and the partial rows it writes, per (group,
+    block) bucket the K/V-side tiles it reads and writes."""
     pos = np.arange(w.N, dtype=np.int64)
     T = tokens_per_row(w, pos).astype(np.float64)
     nsel = np.minimum(w.topk, pos // w.block + 1).astype(np.float64)     # valid selected blocks per row
     vis_blocks = (pos // w.block + 1).astype(np.float64)
-    B = w.B
-    work = {
-        "index_scores_tc_kernel": (B * float(np.sum(2.0 * w.d_idx * (pos + 1) * w.Hkv)), "tensor"),
-        "sparse_fwd_tc_kernel": (B * float(np.sum(4.0 * w.d * T * w.Hq)), "tensor"),
-        "kl_index_tc_kernel": (B * float(np.sum(2.0 * w.d_idx * T * w.Hkv)), "tensor"),
-        "bwd_main_tc_kernel": (B * float(np.sum(10.0 * w.d * T * w.Hq)), "tensor"),
-        "bwd_index_tc_kernel": (B * float(np.sum(6.0 * w.d_idx * T * w.Hkv)), "tensor"),
+    B, G, d, di = w.B, w.G, w.d, w.d_idx
+    slots = B * w.Hkv * float(np.sum(nsel))                              # (query, group, block) slots
+    buckets = B * w.Hkv * float(w.nb)                                    # (group, block) buckets
+    return {
+        "index_scores_tc_kernel": {"flops": B * float(np.sum(2.0 * di * (pos + 1) * w.Hkv)), "bytes": None},
+        # Q rows gathered, bf16 partial row + (m, z) written per slot; K, V per bucket
+        "sparse_fwd_tc_kernel": {"flops": B * float(np.sum(4.0 * d * T * w.Hq)),
+                                 "bytes": slots * (G * d * 2.0 + G * d * 2.0 + G * 8.0) + buckets * 2 * 128 * d * 2.0},
+        "kl_index_tc_kernel": {"flops": B * float(np.sum(2.0 * di * T * w.Hkv)),
+                               "bytes": slots * (di * 2.0 + 4.0 + 32.0) + buckets * 128 * di * 2.0},
+        # Q and dO rows gathered, dQ partial row + teacher row written, LSE and D read
+        # per slot; K, V read and dK, dV written per bucket
+        "bwd_main_tc_kernel": {"flops": B * float(np.sum(10.0 * d * T * w.Hq)),
+                               "bytes": slots * (2 * G * d * 2.0 + G * d * 2.0 + 128 * 2.0 + G * 8.0)
+                               + buckets * 4 * 128 * d * 2.0},
+        # q_idx row gathered, teacher row read, dq_idx partial row written per slot;
+        # K_idx read and dK_idx added (fp32) per bucket
+        "bwd_index_tc_kernel": {"flops": B * float(np.sum(6.0 * di * T * w.Hkv)),
+                                "bytes": slots * (di * 2.0 + 128 * 2.0 + di * 2.0 + 4.0)
+                                + buckets * 128 * di * (2.0 + 8.0)},
         # block scores of the visible blocks in, indices out
-        "block_topk_kernel": (B * w.Hkv * float(np.sum(vis_blocks * 4.0 + w.topk * 4.0)), "hbm"),
+        "block_topk_kernel": {"flops": None, "bytes": B * w.Hkv * float(np.sum(vis_blocks * 4.0 + w.topk * 4.0))},
         # bf16 partial rows + (m, z) per valid slot in, bf16 row + lse out
-        "sparse_fwd_combine_kernel": (B * w.Hq * float(np.sum(nsel * (2.0 * w.d + 8.0) + 2.0 * w.d + 4.0)), "hbm"),
+        "sparse_fwd_combine_kernel": {"flops": None,
+                                      "bytes": B * w.Hq * float(np.sum(nsel * (2.0 * d + 8.0) + 2.0 * d + 4.0))},
         # dQ and dq_idx: bf16 partial rows per valid slot in, one bf16 row out
-        "bwd_combine_kernel": (B * float(np.sum((nsel + 1.0) * 2.0 * (w.d * w.Hq + w.d_idx * w.Hkv))), "hbm"),
+        "bwd_combine_kernel": {"flops": None,
+                               "bytes": B * float(np.sum((nsel + 1.0) * 2.0 * (d * w.Hq + di * w.Hkv)))},
     }
-    return work
 
 
 def kernel_traffic(kernel, w):
@@ -394,37 +411,34 @@ def main():
     dom = max(ktimes, key=lambda k: ktimes[k][1])
     n_l, tot_ms = ktimes[dom]
     per_launch_ms = tot_ms / n_l
-    units, bound = work.get(dom, (None, None))
-    if units is None:
+    wk = work.get(dom)
+    if wk is None:
         roofline = {"kernel": dom, "bound": None, "achieved": None, "peak": None, "unit": None, "frac": None,
                     "traffic": None, "launch_ms": round(per_launch_ms, 3)}
-    elif bound == "tensor":
-        # a contraction whose measured DRAM traffic would take longer at the copy
-        # peak than its FLOPs at the tensor peak is bound by HBM: report that roofline
-        traffic = kernel_traffic(dom, w)
-        t_tensor = units / (peaks["bf16_tflops"] * 1e12)
-        t_hbm = traffic / (peaks["hbm_gbs"] * 1e9) if traffic else 0.0
-        ach_t = units / (per_launch_ms * 1e-3) / 1e12
-        tensor_side = {"achieved": round(ach_t, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                       "frac": round(ach_t / peaks["bf16_tflops"], 4),
-                       "frac_of_sustained": round(ach_t / peaks["bf16_tflops_sustained"], 4),
-                       "peak_source": peaks["source"] + " burst bf16", "algorithmic_per_launch": units}
-        if traffic and t_hbm > t_tensor:
-            ach = traffic / (per_launch_ms * 1e-3) / 1e9
-            roofline = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
-                        "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4), "peak_source": peaks["source"] + " copy",
-                        "traffic": traffic, "launch_ms": round(per_launch_ms, 3),
-                        "note": "DRAM traffic at the copy peak outlasts the FLOPs at the bf16 peak",
-                        "tensor": tensor_side}
-        else:
-            roofline = {"kernel": dom, "bound": "tensor", **tensor_side, "traffic": traffic,
-                        "launch_ms": round(per_launch_ms, 3)}
     else:
-        ach = units / (per_launch_ms * 1e-3) / 1e9
-        roofline = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
-                    "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4), "peak_source": peaks["source"] + " copy",
-                    "traffic": kernel_traffic(dom, w), "algorithmic_per_launch": units,
+        # the binding roofline: algorithmic bytes at the copy peak against FLOPs at
+        # the bf16 peak, whichever takes longer; the other side rides along
+        fl, by = wk["flops"], wk["bytes"]
+        t_tensor = fl / (peaks["bf16_tflops"] * 1e12) if fl else 0.0
+        t_hbm = by / (peaks["hbm_gbs"] * 1e9) if by else 0.0
+        sides = {}
+        if fl:
+            ach_t = fl / (per_launch_ms * 1e-3) / 1e12
+            sides["tensor"] = {"achieved": round(ach_t, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                               "frac": round(ach_t / peaks["bf16_tflops"], 4),
+                               "frac_of_sustained": round(ach_t / peaks["bf16_tflops_sustained"], 4),
+                               "peak_source": peaks["source"] + " burst bf16", "algorithmic_per_launch": fl}
+        if by:
+            ach_h = by / (per_launch_ms * 1e-3) / 1e9
+            sides["hbm"] = {"achieved": round(ach_h, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                            "frac": round(ach_h / peaks["hbm_gbs"], 4), "peak_source": peaks["source"] + " copy",
+                            "algorithmic_per_launch": by}
+        bound = "hbm" if t_hbm > t_tensor else "tensor"
+        other = "tensor" if bound == "hbm" else "hbm"
+        roofline = {"kernel": dom, "bound": bound, **sides[bound], "traffic": kernel_traffic(dom, w),
                     "launch_ms": round(per_launch_ms, 3)}
+        if other in sides:
+            roofline[other] = sides[other]
     kernels_ms = {k: round(v[1] / args.steps, 3) for k, v in sorted(ktimes.items(), key=lambda kv: -kv[1][1])}
 
     cpu = None
