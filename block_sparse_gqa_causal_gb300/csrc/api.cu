@@ -101,7 +101,8 @@ struct Carve {
 // queries per block (decode) they stream each query's blocks instead.
 bool fwd_keymajor(const Problem &p) { return (long long)p.Nq * p.topk >= 8LL * p.nb; }
 
-size_t bs_bytes(const Problem &p) { return align256((size_t)p.B * p.Nq * p.Hkv * p.nb * sizeof(float)); }
+// selection scratch: block scores, or the split selection's candidate keys
+size_t bs_bytes(const Problem &p) { return align256(index_select_scratch_floats(p) * sizeof(float)); }
 
 // inverse index: counts, offsets, per-CTA scratch, query lists
 size_t index_bytes(const Problem &p)
@@ -312,7 +313,7 @@ msa_status msa_index_select(const msa_shape *shape, const void *q_idx, const voi
     st = check_ws(workspace, workspace_bytes, kStatusBytes + (block_scores ? 0 : bs_bytes(p)));
     if (st != MSA_OK) return st;
     Carve cv{static_cast<char *>(workspace)};
-    float *scratch = block_scores ? nullptr : cv.take<float>((size_t)p.B * p.Nq * p.Hkv * p.nb);
+    float *scratch = block_scores ? nullptr : cv.take<float>(index_select_scratch_floats(p));
     DeviceStatus *ds = static_cast<DeviceStatus *>(workspace);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_index_select(p, static_cast<const bf16 *>(q_idx), static_cast<const bf16 *>(k_idx),
@@ -561,7 +562,7 @@ msa_status msa_train_step(const msa_shape *shape, const void *q, const void *k, 
     Carve cv{static_cast<char *>(workspace)};
     BwdWork w{};
     carve_index(cv, p, w);
-    float *bs_scratch = index_select_fused(p) ? nullptr : cv.take<float>((size_t)p.B * p.Nq * p.Hkv * p.nb);
+    float *bs_scratch = index_select_fused(p) ? nullptr : cv.take<float>(index_select_scratch_floats(p));
     const size_t rows = (size_t)p.B * p.Nq * p.Hq * p.topk;
     FwdWork fw;
     fw.part = cv.take<bf16>(rows * p.d);

@@ -23,52 +23,6 @@ constexpr int kWarps = 8;
 constexpr int kR = 16;                 // scores per lane per segment
 constexpr int kSeg = 32 * kR;
 
-__device__ __forceinline__ unsigned long long make_key(float s, int c)
-{
-    return ((unsigned long long)float_key(s) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)c);
-}
-
-__device__ __forceinline__ unsigned long long shfl64(unsigned long long v, int src)
-{
-    const uint32_t lo = __shfl_sync(0xffffffffu, (uint32_t)v, src);
-    const uint32_t hi = __shfl_sync(0xffffffffu, (uint32_t)(v >> 32), src);
-    return ((unsigned long long)hi << 32) | lo;
-}
-
-__device__ __forceinline__ unsigned long long shfl64_xor(unsigned long long v, int m)
-{
-    const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)v, m);
-    const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(v >> 32), m);
-    return ((unsigned long long)hi << 32) | lo;
-}
-
-// descending bitonic sort of one 64-bit key per lane
-__device__ __forceinline__ unsigned long long sort_desc64(unsigned long long v, int lane)
-{
-#pragma unroll
-    for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            const unsigned long long o = shfl64_xor(v, stride);
-            const bool desc = (lane & size) == 0 || size == 32;
-            const bool lower = (lane & stride) == 0;
-            v = (lower == desc) ? (v > o ? v : o) : (v < o ? v : o);
-        }
-    }
-    return v;
-}
-
-// a bitonic sequence across the lanes -> descending order
-__device__ __forceinline__ unsigned long long merge_desc64(unsigned long long v, int lane)
-{
-#pragma unroll
-    for (int stride = 16; stride > 0; stride >>= 1) {
-        const unsigned long long o = shfl64_xor(v, stride);
-        v = ((lane & stride) == 0) ? (v > o ? v : o) : (v < o ? v : o);
-    }
-    return v;
-}
-
 // descending bitonic sort of one float per lane
 __device__ __forceinline__ float sort_desc_f(float v, int lane)
 {
@@ -142,7 +96,7 @@ __device__ __forceinline__ void warp_topk(const float *__restrict__ src, int c0,
         if (total == 0) continue;
 #pragma unroll
         for (int j = 0; j < kR; ++j)
-            if (v[j] >= tau && v[j] > t_run && v[j] != -INFINITY) buf[off++] = make_key(v[j], base + j * 32 + lane);
+            if (v[j] >= tau && v[j] > t_run && v[j] != -INFINITY) buf[off++] = block_key(v[j], base + j * 32 + lane);
         __syncwarp();
         for (int c32 = 0; c32 < total; c32 += 32) {
             unsigned long long ck = (c32 + lane < total) ? buf[c32 + lane] : 0ull;
@@ -227,7 +181,76 @@ block_topk_split_kernel(Problem p, const float *__restrict__ bs, int32_t *__rest
     }
 }
 
+// Decode with the fused selection: the score kernel's CTA for slice y of a
+// row's blocks left that row's 16 best keys of the slice, in descending
+// order, at cand[(row * slices + y) * 16 ..] (0 = no block).  The row's k-1
+// best blocks are among them (each slice keeps at least k-1).  One CTA per
+// row: warp w takes the slice pairs w, w + 8, ... (all its loads issued
+// before any merge); the two descending lists of a pair, the second
+// reversed, form a bitonic sequence, sorted by one bitonic merge and merged
+// into the warp's running top-32; warp 0 then merges the warps' lists.
+constexpr int kMergeBatch = 4;   // slice pairs per warp per batch of loads
+
+__global__ void __launch_bounds__(kWarps * 32)
+block_topk_merge_kernel(Problem p, const unsigned long long *__restrict__ cand, int slices, int32_t *__restrict__ sel)
+{
+    __shared__ unsigned long long lists[kWarps][32];
+    const int lane = threadIdx.x & 31;
+    const int wi = threadIdx.x >> 5;
+    const long long row = blockIdx.x;
+    const int r = (int)(row % p.Hkv);
+    const long long bi = row / p.Hkv;
+    const int i = (int)(bi % p.Nq), b = (int)(bi / p.Nq);
+    const long long pos = (long long)p.q_offset + i;
+    const int c0 = (int)(pos / 128);
+    const int k = p.topk;
+    int32_t *out = sel + (((long long)b * p.Hkv + r) * p.Nq + i) * k;
+    if (c0 + 1 <= k) {
+        if (wi == 0 && lane < k) out[lane] = lane <= c0 ? lane : -1;
+        return;
+    }
+    const unsigned long long *src = cand + row * slices * 16;
+    const int pairs = (slices + 1) / 2;
+    unsigned long long best = 0ull;
+    for (int t0 = wi; t0 < pairs; t0 += kWarps * kMergeBatch) {
+        unsigned long long ck[kMergeBatch];
+#pragma unroll
+        for (int t = 0; t < kMergeBatch; ++t) {
+            const int y = 2 * (t0 + t * kWarps) + (lane >> 4);
+            ck[t] = y < slices ? __ldg(src + (long long)y * 16 + (lane & 15)) : 0ull;
+        }
+#pragma unroll
+        for (int t = 0; t < kMergeBatch; ++t) {
+            const unsigned long long v = merge_desc64(shfl64(ck[t], lane < 16 ? lane : 47 - lane), lane);
+            const unsigned long long rev = shfl64(v, 31 - lane);
+            best = merge_desc64(best > rev ? best : rev, lane);
+        }
+    }
+    lists[wi][lane] = best;
+    __syncthreads();
+    if (wi == 0) {
+#pragma unroll 1
+        for (int w = 1; w < kWarps; ++w) {
+            const unsigned long long rev = lists[w][31 - lane];
+            best = merge_desc64(best > rev ? best : rev, lane);
+        }
+        write_selection(out, best, k - 1, c0, k, lane);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_block_topk_merge(const Problem &p, const unsigned long long *cand, int slices, int32_t *sel,
+                                    cudaStream_t s)
+{
+    const long long rows = (long long)p.B * p.Nq * p.Hkv;
+    {
+        TimedLaunch timed_("block_topk_merge_kernel", s);
+        block_topk_merge_kernel<<<(unsigned)rows, kWarps * 32, 0, s>>>(p, cand, slices, sel);
+    }
+    note_launch();
+    return cudaGetLastError();
+}
 
 cudaError_t launch_block_topk(const Problem &p, const float *bs, int32_t *sel, DeviceStatus *,
                               cudaStream_t s)

@@ -181,4 +181,58 @@ MSA_DEV uint32_t float_key(float f)
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Ranking key of a candidate block: score first, then the lower block index
+// (one unsigned compare orders by (score desc, index asc)); 0 means "none".
+MSA_DEV unsigned long long block_key(float s, int c)
+{
+    return ((unsigned long long)float_key(s) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)c);
+}
+
+MSA_DEV unsigned long long shfl64(unsigned long long v, int src)
+{
+    const uint32_t lo = __shfl_sync(0xffffffffu, (uint32_t)v, src);
+    const uint32_t hi = __shfl_sync(0xffffffffu, (uint32_t)(v >> 32), src);
+    return ((unsigned long long)hi << 32) | lo;
+}
+
+MSA_DEV unsigned long long shfl64_xor(unsigned long long v, int m)
+{
+    const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)v, m);
+    const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(v >> 32), m);
+    return ((unsigned long long)hi << 32) | lo;
+}
+
+// descending bitonic sort of one 64-bit key per lane
+MSA_DEV unsigned long long sort_desc64(unsigned long long v, int lane)
+{
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const unsigned long long o = shfl64_xor(v, stride);
+            const bool desc = (lane & size) == 0 || size == 32;
+            const bool lower = (lane & stride) == 0;
+            v = (lower == desc) ? (v > o ? v : o) : (v < o ? v : o);
+        }
+    }
+    return v;
+}
+
+// a bitonic sequence across the lanes -> descending order
+MSA_DEV unsigned long long merge_desc64(unsigned long long v, int lane)
+{
+#pragma unroll
+    for (int stride = 16; stride > 0; stride >>= 1) {
+        const unsigned long long o = shfl64_xor(v, stride);
+        v = ((lane & stride) == 0) ? (v > o ? v : o) : (v < o ? v : o);
+    }
+    return v;
+}
+
+// Barrier `id` (1..15) over `nthreads` threads (a multiple of 32) of the CTA.
+MSA_DEV void named_bar_sync(int id, int nthreads)
+{
+    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 }  // namespace msa

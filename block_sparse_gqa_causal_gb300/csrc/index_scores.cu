@@ -25,7 +25,13 @@
 // blocks in registers (sorted by score, then lower index: a later block
 // enters only with a strictly larger score), so the block scores need not
 // round-trip through memory; the k-1 best plus the local block are written
-// in ascending order, as the separate top-k kernel does.
+// in ascending order, as the separate top-k kernel does.  When a row's
+// blocks are split across CTAs (decode: few rows, long rows) the block
+// scores of the CTA's slice stay in shared memory; after the last block
+// each epilogue warp takes a row and leaves the slice's 16 best as ranking
+// keys (warp bitonic sorts), and a small kernel merges the slices' lists.
+#include <algorithm>
+
 #include "msa_internal.h"
 #include "tc.cuh"
 
@@ -38,6 +44,7 @@ constexpr int kEpiWarps = 8;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr int kSub = 128 * 128;    // one [128 rows][64 bf16] swizzled sub-tile, bytes
 constexpr uint32_t kIdesc = tc::idesc_bf16(128, 128);
+constexpr int kSelFloats = 7168;   // split selection: block scores of the CTA's rows x slice
 
 template <int DI>
 struct Smem {
@@ -46,7 +53,8 @@ struct Smem {
     static constexpr int K_BYTES = KB * kSub;
     static constexpr int OFF_K = Q_BYTES;
     static constexpr int OFF_BAR = OFF_K + kStages * K_BYTES;
-    static constexpr int BYTES = OFF_BAR + 256;
+    static constexpr int OFF_SBS = OFF_BAR + 256;
+    static constexpr int BYTES = OFF_SBS + kSelFloats * 4;
     // request at least ~120 KB so one CTA (which takes all 512 TMEM columns) runs per SM
     static constexpr int ALLOC = (BYTES + 1024 > 120 * 1024 ? BYTES + 1024 : 120 * 1024);
 };
@@ -54,7 +62,8 @@ struct Smem {
 template <int DI>
 __global__ void __launch_bounds__(kThreads, 1)
 index_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-                       Problem p, float *__restrict__ bs, int32_t *__restrict__ sel, int span, DeviceStatus *st)
+                       Problem p, float *__restrict__ bs, int32_t *__restrict__ sel,
+                       unsigned long long *__restrict__ cand, int span, DeviceStatus *st)
 {
     using S = Smem<DI>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -64,6 +73,7 @@ index_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_
     uint8_t *sQ = smem;
     uint8_t *sK = smem + S::OFF_K;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S::OFF_BAR);
+    float *sbs = reinterpret_cast<float *>(smem + S::OFF_SBS);
     uint64_t *full = bars, *empty = bars + kStages, *q_full = bars + 2 * kStages;
     uint64_t *acc_full = q_full + 1, *acc_empty = acc_full + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 2);
@@ -266,6 +276,11 @@ index_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_
             // store this row's scores for blocks c_begin+n0 .. (at most 8)
             const int c_lo = c_begin + n0;
             const int c_hi = min(c_lo + 7, c_last);
+            if (cand && valid) {
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (n0 + u < nblk) sbs[row * span + n0 + u] = grp[u];
+            }
             if (out && valid && c_hi >= c_lo) {
                 if (vec_ok && c_hi == c_lo + 7) {
                     float4 *o4 = reinterpret_cast<float4 *>(out + c_lo);
@@ -276,6 +291,26 @@ index_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_
                     for (int u = 0; u < 8; ++u)
                         if (c_lo + u <= c_hi) out[c_lo + u] = grp[u];
                 }
+            }
+        }
+        if (cand) {
+            // the slice's 16 best earlier blocks of each row, descending, as
+            // ranking keys: warp e takes rows e, e + 8, ..., 32 scores at a time
+            // sorted and merged into a running top-32
+            named_bar_sync(1, kEpiWarps * 32);
+            for (int rl = e; rl < rows_here; rl += kEpiWarps) {
+                const int rr = row0 + rl;
+                const long long pr = (long long)p.q_offset + rr / p.Hkv;
+                const int ce = (int)min((long long)c_end, pr / 128) - c_begin;   // slice blocks before c0
+                unsigned long long best = 0ull;
+                for (int nn = 0; nn < ce; nn += 32) {
+                    const int n = nn + lane;
+                    unsigned long long key = n < ce ? block_key(sbs[rl * span + n], c_begin + n) : 0ull;
+                    key = sort_desc64(key, lane);
+                    const unsigned long long rev = shfl64(key, 31 - lane);
+                    best = merge_desc64(best > rev ? best : rev, lane);
+                }
+                if (lane < 16) cand[(((long long)b * rows_total + rr) * gridDim.y + blockIdx.y) * 16 + lane] = best;
             }
         }
         if (sel && valid) {
@@ -332,10 +367,11 @@ void plan_grid(const Problem &p, int &tiles, int &splits, int &span)
 }
 
 // bs: scores out (nullptr: not stored); sel: selection out (fused form; the
-// caller has checked that it applies)
+// caller has checked that it applies); cand: per-slice candidate keys out
+// (split form)
 template <int DI>
-cudaError_t launch_t(const Problem &p, const bf16 *q_idx, const bf16 *k_idx, float *bs, int32_t *sel, DeviceStatus *st,
-                     cudaStream_t s)
+cudaError_t launch_t(const Problem &p, const bf16 *q_idx, const bf16 *k_idx, float *bs, int32_t *sel,
+                     unsigned long long *cand, DeviceStatus *st, cudaStream_t s)
 {
     using S = Smem<DI>;
     const long long rows_total = (long long)p.Nq * p.Hkv;
@@ -351,7 +387,7 @@ cudaError_t launch_t(const Problem &p, const bf16 *q_idx, const bf16 *k_idx, flo
     if (e != cudaSuccess) return e;
     {
         TimedLaunch timed_("index_scores_tc_kernel", s);
-        index_scores_tc_kernel<DI><<<dim3(tiles, splits, p.B), kThreads, S::ALLOC, s>>>(tq, tk, p, bs, sel, span, st);
+        index_scores_tc_kernel<DI><<<dim3(tiles, splits, p.B), kThreads, S::ALLOC, s>>>(tq, tk, p, bs, sel, cand, span, st);
     }
     note_launch();
     return cudaGetLastError();
@@ -362,8 +398,30 @@ cudaError_t launch_t(const Problem &p, const bf16 *q_idx, const bf16 *k_idx, flo
 cudaError_t launch_index_scores(const Problem &p, const bf16 *q_idx, const bf16 *k_idx, float *bs,
                                 DeviceStatus *st, cudaStream_t s)
 {
-    return p.d_idx == 128 ? launch_t<128>(p, q_idx, k_idx, bs, nullptr, st, s)
-                          : launch_t<64>(p, q_idx, k_idx, bs, nullptr, st, s);
+    return p.d_idx == 128 ? launch_t<128>(p, q_idx, k_idx, bs, nullptr, nullptr, st, s)
+                          : launch_t<64>(p, q_idx, k_idx, bs, nullptr, nullptr, st, s);
+}
+
+// Split selection: rows split across CTAs, k <= 16, and each CTA's rows x
+// slice of block scores fit the shared-memory buffer.
+bool index_select_split(const Problem &p)
+{
+    int tiles, splits, span;
+    plan_grid(p, tiles, splits, span);
+    const long long rows = std::min((long long)kTileRows, (long long)p.Nq * p.Hkv);
+    return splits > 1 && p.topk <= 16 && rows * span <= kSelFloats;
+}
+
+size_t index_select_scratch_floats(const Problem &p)
+{
+    const size_t rows = (size_t)p.B * p.Nq * p.Hkv;
+    size_t n = rows * (size_t)p.nb;                              // block scores
+    if (index_select_split(p)) {
+        int tiles, splits, span;
+        plan_grid(p, tiles, splits, span);
+        n = std::max(n, rows * (size_t)splits * 16 * 2);   // 16 8-byte keys per (row, slice)
+    }
+    return n;
 }
 
 bool index_select_fused(const Problem &p)
@@ -377,8 +435,20 @@ cudaError_t launch_index_select(const Problem &p, const bf16 *q_idx, const bf16 
                                 float *bs_scratch, int32_t *sel, DeviceStatus *st, cudaStream_t s)
 {
     if (index_select_fused(p))   // every CTA sees all blocks of its rows: fused selection
-        return p.d_idx == 128 ? launch_t<128>(p, q_idx, k_idx, bs_out, sel, st, s)
-                              : launch_t<64>(p, q_idx, k_idx, bs_out, sel, st, s);
+        return p.d_idx == 128 ? launch_t<128>(p, q_idx, k_idx, bs_out, sel, nullptr, st, s)
+                              : launch_t<64>(p, q_idx, k_idx, bs_out, sel, nullptr, st, s);
+    if (!bs_out && bs_scratch && index_select_split(p)) {
+        // rows split across CTAs, scores not wanted: each CTA leaves its slice's
+        // 16 best blocks per row (the scratch holds index_select_scratch_floats),
+        // then a second kernel merges the slices' lists
+        int tiles, splits, span;
+        plan_grid(p, tiles, splits, span);
+        unsigned long long *cand = reinterpret_cast<unsigned long long *>(bs_scratch);
+        cudaError_t e = p.d_idx == 128 ? launch_t<128>(p, q_idx, k_idx, nullptr, nullptr, cand, st, s)
+                                       : launch_t<64>(p, q_idx, k_idx, nullptr, nullptr, cand, st, s);
+        if (e != cudaSuccess) return e;
+        return launch_block_topk_merge(p, cand, splits, sel, s);
+    }
     float *bs = bs_out ? bs_out : bs_scratch;
     cudaError_t e = launch_index_scores(p, q_idx, k_idx, bs, st, s);
     if (e != cudaSuccess) return e;

@@ -51,6 +51,10 @@ cudaError_t launch_index_scores(const Problem &p, const bf16 *q_idx, const bf16 
 // Top-k block selection from block scores.  sel: [B, Hkv, Nq, topk].
 cudaError_t launch_block_topk(const Problem &p, const float *bs, int32_t *sel, DeviceStatus *st,
                               cudaStream_t s);
+// Merge of per-slice candidate lists (16 descending block keys per (row,
+// slice)) into the selection: the second half of the fused decode selection.
+cudaError_t launch_block_topk_merge(const Problem &p, const unsigned long long *cand, int slices, int32_t *sel,
+                                    cudaStream_t s);
 // Index scores + selection: fused into the score kernel when every CTA sees
 // all blocks of its rows and topk <= 16 (scores stored only if bs_out is set),
 // else scores to bs_out (or bs_scratch) and the separate top-k kernel.
@@ -58,6 +62,12 @@ cudaError_t launch_index_select(const Problem &p, const bf16 *q_idx, const bf16 
                                 float *bs_scratch, int32_t *sel, DeviceStatus *st, cudaStream_t s);
 // true when launch_index_select runs the fused form (no score scratch needed)
 bool index_select_fused(const Problem &p);
+// true when launch_index_select, with no scores wanted, selects in the
+// split form (rows split across CTAs; per-slice candidates, then a merge)
+bool index_select_split(const Problem &p);
+// fp32 words of bs_scratch launch_index_select may use when bs_out is null:
+// the block scores, or the per-slice candidate keys of the split form
+size_t index_select_scratch_floats(const Problem &p);
 // Key-major main branch forward (many queries per selected block).
 struct FwdWork {
     bf16 *part;          // [B, Nq, Hq, topk, d] unnormalised partial outputs per selected block

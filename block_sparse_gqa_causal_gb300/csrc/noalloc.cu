@@ -13,8 +13,10 @@
 //
 // Limits and sharing:
 //   * the array holds a 256-byte status word plus kScratchScoreBytes of
-//     block scores (B * Nq * Hkv * nb * 4 bytes must fit; larger shapes are
-//     rejected with MSA_ERR_WORKSPACE before any launch);
+//     selection scratch: the block scores (B * Nq * Hkv * nb * 4 bytes) or,
+//     when a row's blocks are split across CTAs, 128 bytes of candidate keys
+//     per (row, slice), whichever is larger, must fit; larger shapes are
+//     rejected with MSA_ERR_WORKSPACE before any launch;
 //   * every device that loads the library holds the array until the process
 //     exits;
 //   * all calls share the one array: calls whose work overlaps on the GPU
@@ -76,11 +78,11 @@ extern "C" msa_status msa_index_select_noalloc(const msa_shape *shape, const voi
     Problem p;
     msa_status st = problem_from_shape(shape, p);
     if (st != MSA_OK) return st;
-    const size_t need = (size_t)p.B * p.Nq * p.Hkv * p.nb * sizeof(float);
+    const size_t need = index_select_scratch_floats(p) * sizeof(float);
     if (need > kScratchScoreBytes) {
         char msg[256];
         snprintf(msg, sizeof msg,
-                 "msa_index_select_noalloc: block scores need %zu bytes, the static scratch holds %zu "
+                 "msa_index_select_noalloc: the selection scratch needs %zu bytes, the static array holds %zu "
                  "(B*Nq*Hkv*ceil(Nk/block)*4 must be <= 64 MiB)", need, kScratchScoreBytes);
         return set_error(MSA_ERR_WORKSPACE, msg);
     }

@@ -98,8 +98,12 @@ size_t msa_workspace_size(const msa_shape *shape, int op);
  *   bs_c  = max over visible j in block c of s_j           (fp32)
  *   sel   = {c0(i)} + the topk-1 blocks c < c0(i) of largest bs_c, ties to
  *           the lower c; every visible block when c0(i)+1 <= topk.
- * Writes sel_idx; also block_scores when it is not NULL (otherwise they live
- * in the workspace).  No exp is taken: ranking uses raw scores.
+ * Writes sel_idx; also block_scores when it is not NULL.  Otherwise the
+ * scores never reach memory when topk <= 16: the score kernel ranks them in
+ * its epilogue (when a row's blocks are split across CTAs, as in decode, each
+ * CTA leaves its slice's 16 best in the workspace and a merge kernel picks
+ * the row's selection); with topk > 16 they live in the workspace.  The
+ * result is the same either way.  No exp is taken: ranking uses raw scores.
  */
 msa_status msa_index_select(const msa_shape *shape, const void *q_idx, const void *k_idx,
                             int32_t *sel_idx, float *block_scores,
@@ -191,12 +195,16 @@ msa_status msa_train_step(const msa_shape *shape, const void *q, const void *k, 
  * warm-up, or a plugin given only raw device pointers).  There is no
  * counterpart of this call in the method's description: it computes exactly
  * what msa_index_select computes (same kernels, same sel_idx), but its
- * scratch for the block scores is a static device array inside the library
- * instead of a caller workspace.  The caller still passes q_idx, k_idx and
- * sel_idx (layouts as above); block scores are not returned.
- *   - Limit: B * Nq * Hkv * ceil(Nk/block) * 4 bytes <= 64 MiB, else
- *     MSA_ERR_WORKSPACE before any launch.  Every device that loads the
- *     library holds that array (plus 256 bytes) until the process exits.
+ * selection scratch (block scores, or the per-slice candidate lists of a
+ * split row) is a static device array inside the library instead of a
+ * caller workspace.  The caller still passes q_idx, k_idx and sel_idx
+ * (layouts as above); block scores are not returned.
+ *   - Limit: the scratch msa_workspace_size(MSA_OP_INDEX_SELECT) counts
+ *     beyond its 256-byte status word -- B * Nq * Hkv * ceil(Nk/block) * 4
+ *     bytes, or 128 bytes per (row, slice) when rows are split across CTAs,
+ *     whichever is larger -- must be <= 64 MiB, else MSA_ERR_WORKSPACE before
+ *     any launch.  Every device that loads the library holds that array
+ *     (plus 256 bytes) until the process exits.
  *   - All calls share the array and it keeps the last call's contents;
  *     calls that overlap on the GPU race with each other.
  *   - The first call on each device looks up the array's address with that

@@ -86,3 +86,73 @@ def test_decode_long_cache_split_selection():
     o_ref, lse_ref = oracle.sparse_fwd(osh, x["q"], x["k"], x["v"], sel_g, rows)
     assert_close(bf16_to_np(o).reshape(o_ref.shape), o_ref, "o", bf16_out=True)
     assert_close(lse.cpu().numpy().reshape(lse_ref.shape), lse_ref, "lse", max_abs=1e-3, rel_l2=1e-5)
+
+
+@pytest.mark.parametrize("step", [0, 57, 199])
+def test_decode_split_fused_selection_matches_scores_path(decode_case, step):
+    """Without block scores asked for, a decode row's blocks are ranked in the
+    score kernel's epilogue, each CTA keeping its slice's 16 best, and a merge
+    kernel picks the row's selection.  It must equal the selection made from
+    the stored scores (same fp32 scores, same tie rule) and the oracle's."""
+    import torch
+    from block_sparse_gqa_causal_gb300 import api
+    from block_sparse_gqa_causal_gb300.inputs import decode_position
+    w, x = decode_case
+    pos = decode_position(w, step)
+    qi = np.ascontiguousarray(x["q_idx"][:, step:step + 1])
+    sh = api.Shape(B=w.B, Nq=1, Nk=pos + 1, Hq=w.Hq, Hkv=w.Hkv, d=w.d, d_idx=w.d_idx, topk=w.topk, q_offset=pos,
+                   kv_rows=w.N)
+    tqi, tki = to_torch(qi), to_torch(x["k_idx"])
+    sel_f = api.index_select(sh, tqi, tki)
+    sel_s, _ = api.index_select(sh, tqi, tki, return_scores=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(sel_f.cpu().numpy(), sel_s.cpu().numpy())
+    osh = oracle.Shape(B=w.B, Nq=1, Nk=pos + 1, Hq=w.Hq, Hkv=w.Hkv, d=w.d, d_idx=w.d_idx, topk=w.topk, q_offset=pos,
+                       kv_rows=w.N)
+    rows = np.arange(w.B)
+    bs_o = oracle.block_scores(osh, qi, x["k_idx"], rows)
+    sel_o = oracle.select(osh, bs_o, rows)
+    exact, tol = check_selection(w.topk, 128, pos, 1, rows, sel_f.cpu().numpy()[:, :, 0, :], sel_o, bs_o)
+    assert exact >= 1
+
+
+def test_decode_split_fused_selection_ties_go_to_lower_blocks():
+    """Every K_idx row equal: all block scores tie exactly, across the CTAs'
+    slices too, so the selection is blocks 0..k-2 plus the local block."""
+    import torch
+    from block_sparse_gqa_causal_gb300 import api
+    from block_sparse_gqa_causal_gb300.inputs import f32_to_bf16_bits
+    B, Hkv, d, k = 2, 2, 64, 16
+    cap = 700 * 128
+    rng = np.random.default_rng(5)
+    qi = f32_to_bf16_bits(rng.standard_normal((B, 1, Hkv, d)).astype(np.float32))
+    row = f32_to_bf16_bits(rng.standard_normal((1, 1, d)).astype(np.float32))
+    ki = np.ascontiguousarray(np.broadcast_to(row, (B, cap, d)))
+    for pos in (cap - 1, cap - 200, 31 * 128 + 5):
+        sh = api.Shape(B=B, Nq=1, Nk=pos + 1, Hq=Hkv, Hkv=Hkv, d=d, d_idx=d, topk=k, q_offset=pos, kv_rows=cap)
+        sel = api.index_select(sh, to_torch(qi), to_torch(ki))
+        torch.cuda.synchronize()
+        want = np.array(list(range(k - 1)) + [pos // 128], dtype=np.int32)
+        assert np.array_equal(sel.cpu().numpy().reshape(B * Hkv, k), np.broadcast_to(want, (B * Hkv, k)))
+
+
+@pytest.mark.slow
+def test_decode_1m_split_fused_selection_matches_scores_path():
+    """The benchmark's decode shape (4 sequences, 1,048,576-token caches, 8
+    groups) at its last step: the split-fused selection equals the one made
+    from the stored scores, and every row is a valid selection."""
+    import torch
+    from block_sparse_gqa_causal_gb300 import api
+    from block_sparse_gqa_causal_gb300.inputs import f32_to_bf16_bits
+    B, Hkv, d, k, cap = 4, 8, 128, 16, 1048576
+    pos = cap - 1
+    g = torch.Generator(device="cuda").manual_seed(17)
+    qi = torch.randn(B, 1, Hkv, d, device="cuda", generator=g).bfloat16()
+    ki = torch.randn(B, cap, d, device="cuda", generator=g).bfloat16()
+    sh = api.Shape(B=B, Nq=1, Nk=pos + 1, Hq=64, Hkv=Hkv, d=d, d_idx=d, topk=k, q_offset=pos, kv_rows=cap)
+    sel_f = api.index_select(sh, qi, ki)
+    sel_s, _ = api.index_select(sh, qi, ki, return_scores=True)
+    torch.cuda.synchronize()
+    s = sel_f.cpu().numpy().reshape(B * Hkv, k)
+    assert np.array_equal(s, sel_s.cpu().numpy().reshape(B * Hkv, k))
+    assert np.all(s[:, -1] == pos // 128) and np.all(np.diff(s, axis=1) > 0) and np.all(s >= 0)
