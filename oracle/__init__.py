@@ -10,7 +10,8 @@ Two builds of the same source: liboracle_bf16.so takes bf16 bit patterns
 (uint16), liboracle_f64.so takes float64 inputs (finite-difference checks).
 
 Parity pins (tests/test_oracle.py): brute-force block max-pool and a full
-sort for selection; dense causal GQA attention when every visible block is
+sort for selection; the block-mask word of section 4.3's worked example
+(tests/golden/) and set unions for the mask and its traversal; dense causal GQA attention when every visible block is
 selected; dense attention under an explicit block mask; the renormalisation
 error bound of section 2; KL >= 0, KL = 0 for a built teacher == student
 case and KL against scipy's relative entropy; gradients against central
@@ -91,8 +92,10 @@ def _lib(kind: str):
             lib.orc_kl.argtypes = [S, P, P, P, P, P, i, P, P, P]
             lib.orc_bwd_rows.argtypes = [S, P, P, P, P, P, P, P, d, i, P, P, P]
             lib.orc_bwd_keys.argtypes = [S, P, P, P, P, P, P, P, d, i, P, P, P, P]
+            lib.orc_block_mask.argtypes = [S, P, P]
+            lib.orc_mask_walk.argtypes = [P, i, P]
             for f in ("orc_block_scores", "orc_select", "orc_sparse_fwd", "orc_kl", "orc_bwd_rows", "orc_bwd_keys",
-                      "orc_num_threads"):
+                      "orc_block_mask", "orc_mask_walk", "orc_num_threads"):
                 getattr(lib, f).restype = ctypes.c_int
             _loaded[kind] = lib
         return _loaded[kind]
@@ -146,6 +149,26 @@ def select(shape: Shape, bs, rows=None) -> np.ndarray:
     if _lib("bf16").orc_select(ctypes.byref(sh), _in(bs), len(rows), _in(rows), _in(out)) != 0:
         raise ValueError("topk above the oracle's limit of 64")
     return out
+
+
+def block_mask(shape: Shape, sel_full) -> np.ndarray:
+    """Block mask of a selection [B, Hkv, Nq, topk] (section 4.3): uint32
+    words [B, Hkv, ceil(Nq/128), ceil(nb/32)], bit c%32 of word c/32 set when
+    some query of the 128-row tile selected block c."""
+    sel_full = _c(sel_full, np.int32)
+    T, W = (shape.Nq + 127) // 128, (shape.nb + 31) // 32
+    out = np.empty((shape.B, shape.Hkv, T, W), dtype=np.uint32)
+    sh = shape.c()
+    _lib("bf16").orc_block_mask(ctypes.byref(sh), _in(sel_full), _in(out))
+    return out
+
+
+def mask_walk(words) -> np.ndarray:
+    """The active blocks of one tile's mask words, in visiting order."""
+    words = _c(np.asarray(words, dtype=np.uint32).reshape(-1), np.uint32)
+    out = np.empty(32 * max(1, len(words)), dtype=np.int32)
+    n = _lib("bf16").orc_mask_walk(_in(words), len(words), _in(out))
+    return out[:n].copy()
 
 
 def sel_rows_from_full(shape: Shape, sel_full, rows) -> np.ndarray:

@@ -488,6 +488,67 @@ int orc_bwd_keys(const orc_shape *s, const orc_in *q, const orc_in *k, const orc
 }
 
 /* Number of OpenMP threads the oracle runs with (for reporting). */
+/* ------------------------------------------------------------------------ */
+/* Block mask of a selection ("Sparse Attention · Part II", section 4.3,
+ * "Turn support into a block mask").  A query tile is 128 consecutive query
+ * rows i of one (batch, group); the tile's bit for key block c is set when
+ * some query of the tile selected c.  Flags are packed 32 to an unsigned
+ * word: block c lives in word c/32 at bit c%32, set by OR-ing 1 << (c%32).
+ * Bits of blocks >= nb (the tail of the last word) stay zero; -1 entries of
+ * the selection (padding) set nothing.
+ * sel  [B, Hkv, Nq, topk]  ->  mask [B, Hkv, ceil(Nq/128), ceil(nb/32)]      */
+int orc_block_mask(const orc_shape *s, const int32_t *sel, uint32_t *mask)
+{
+    const int nb = nblocks(s);
+    const int W = (nb + 31) / 32;
+    const int T = (s->Nq + 127) / 128;
+    memset(mask, 0, sizeof(uint32_t) * (size_t)s->B * s->Hkv * T * W);
+    for (int b = 0; b < s->B; ++b)
+        for (int r = 0; r < s->Hkv; ++r)
+            for (int i = 0; i < s->Nq; ++i) {
+                const int32_t *row = sel + (((long long)b * s->Hkv + r) * s->Nq + i) * s->topk;
+                uint32_t *words = mask + (((long long)b * s->Hkv + r) * T + i / 128) * W;
+                for (int m = 0; m < s->topk; ++m) {
+                    const int c = row[m];
+                    if (c < 0 || c >= nb) continue;
+                    words[c / 32] |= 1u << (c % 32);
+                }
+            }
+    return 0;
+}
+
+/* The traversal of the same section: for each word, count its set bits and
+ * visit them by rank, the n-th set bit found by scanning the word from bit
+ * 0; the visited block is 32*w + bit.  Writes the active blocks in visiting
+ * (ascending) order to out and returns how many there are.                  */
+static int popcount32(uint32_t x)
+{
+    int n = 0;
+    for (int bit = 0; bit < 32; ++bit) n += (int)((x >> bit) & 1u);
+    return n;
+}
+
+static int nth_set_bit(uint32_t x, int rank)
+{
+    int seen = 0;
+    for (int bit = 0; bit < 32; ++bit)
+        if ((x >> bit) & 1u) {
+            if (seen == rank) return bit;
+            ++seen;
+        }
+    return -1;
+}
+
+int orc_mask_walk(const uint32_t *words, int n_words, int32_t *out)
+{
+    int n = 0;
+    for (int w = 0; w < n_words; ++w) {
+        const int count = popcount32(words[w]);
+        for (int rank = 0; rank < count; ++rank) out[n++] = 32 * w + nth_set_bit(words[w], rank);
+    }
+    return n;
+}
+
 int orc_num_threads(void)
 {
     int n = 1;

@@ -322,3 +322,59 @@ def test_bwd_keys_subset_equals_rows_of_full():
 def test_bf16_rounding_is_nearest_even():
     x = np.array([1.0, 1.0 + 2**-8, 1.0 + 3 * 2**-8, -2.5, 1.0 + 2**-9], dtype=np.float32)
     assert f32_to_bf16_bits(x).tolist() == [0x3F80, 0x3F80, 0x3F82, 0xC020, 0x3F80]
+
+
+def _golden(name):
+    import os
+    vals = {}
+    with open(os.path.join(os.path.dirname(__file__), "golden", name)) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            key, val = line.split(":", 1)
+            vals[key.strip()] = val.strip()
+    return vals
+
+
+def test_block_mask_worked_example():
+    """The block-mask word printed for the first query block of section 4.3's
+    figure: key tiles 0, 3, 6 active -> 01001001 = 73, walk visits 0, 3, 6."""
+    g = _golden("block_mask_example.txt")
+    nb = int(g["num_key_blocks"])
+    active = [int(x) for x in g["active_blocks"].split()]
+    sh = oracle.Shape(B=1, Nq=128, Nk=nb * 128, Hq=1, Hkv=1, d=16, d_idx=16, topk=2, q_offset=(nb - 1) * 128)
+    sel = np.full((1, 1, 128, 2), -1, dtype=np.int32)
+    sel[0, 0, 0] = [active[0], active[1]]          # two queries of the tile share the three blocks
+    sel[0, 0, 77] = [active[2], -1]
+    sel[0, 0, 5] = [active[1], -1]
+    m = oracle.block_mask(sh, sel)
+    assert m.shape == (1, 1, 1, 1)
+    assert int(m[0, 0, 0, 0]) == int(g["word"])
+    assert format(int(m[0, 0, 0, 0]) & 0xFF, "08b") == g["low_byte_binary"]
+    walk = oracle.mask_walk(m[0, 0, 0])
+    assert walk.tolist() == active and len(walk) == int(g["popcount"])
+
+
+def test_block_mask_is_the_tile_union_and_walk_visits_it_in_order():
+    """Brute force on random selections: per (b, group, 128-row tile), the walk
+    of the mask words is the sorted union of the tile's selected blocks;
+    padding (-1) and ids >= nb set nothing, so the last word's unused bits
+    stay zero; an empty word is visited zero times."""
+    rng = np.random.default_rng(8)
+    for B, Nq, nk_blocks, Hkv, k in [(1, 300, 40, 2, 4), (2, 129, 64, 1, 3), (1, 1, 97, 3, 16)]:
+        sh = oracle.Shape(B=B, Nq=Nq, Nk=nk_blocks * 128 - 5, Hq=Hkv, Hkv=Hkv, d=16, d_idx=16, topk=k)
+        nb = sh.nb
+        sel = rng.integers(-1, nb, size=(B, Hkv, Nq, k)).astype(np.int32)
+        sel[..., 0] = np.where(rng.random((B, Hkv, Nq)) < 0.1, nb + 3, sel[..., 0])   # out of range: ignored
+        m = oracle.block_mask(sh, sel)
+        T, W = (Nq + 127) // 128, (nb + 31) // 32
+        assert m.shape == (B, Hkv, T, W)
+        for b in range(B):
+            for r in range(Hkv):
+                for t in range(T):
+                    ids = sel[b, r, 128 * t:128 * (t + 1)].reshape(-1)
+                    union = sorted({int(c) for c in ids if 0 <= c < nb})
+                    assert oracle.mask_walk(m[b, r, t]).tolist() == union
+                    if nb % 32:
+                        assert int(m[b, r, t, W - 1]) >> (nb % 32) == 0
+    assert oracle.mask_walk(np.zeros(3, dtype=np.uint32)).tolist() == []
