@@ -133,6 +133,23 @@ def kernel_traffic(kernel, w):
     return round(per_unit * slots)
 
 
+def selection_stats(w, x, sh, sel):
+    """Statistics of one step's selection (outside any timed region): active
+    key blocks per 128-query tile of a group, from the block mask's per-tile
+    counts (msa_block_mask), and the share of (query, group) rows whose
+    selection holds one of the group's planted needle blocks."""
+    import torch
+    from block_sparse_gqa_causal_gb300 import api
+    _, cnt = api.block_mask(sh, sel, counts=True)
+    stats = {"mean_active_blocks_per_128_query_tile": round(cnt.double().mean().item(), 2),
+             "max_active_blocks_per_128_query_tile": int(cnt.max().item()), "topk": w.topk}
+    if "needles" in x:
+        nd = torch.from_numpy(np.ascontiguousarray(x["needles"], dtype=np.int32)).to(sel.device)   # [B, Hkv, n]
+        hit = (sel.unsqueeze(-1) == nd[:, :, None, None, :]).any(-1).any(-1)                       # [B, Hkv, Nq]
+        stats["rows_selecting_a_needle_frac"] = round(hit.double().mean().item(), 4)
+    return stats
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -338,6 +355,7 @@ def main():
     # per phase: the library's kernels grouped by the step they belong to (the one-call
     # training step leaves no boundary between phases to put events on)
     phase_of = {"index_scores_tc_kernel": "index_select", "block_topk_kernel": "index_select",
+                "block_topk_merge_kernel": "index_select",
                 "sparse_fwd_tc_kernel": "sparse_attn_fwd", "sparse_fwd_combine_kernel": "sparse_attn_fwd",
                 "sparse_attn_fwd_kernel": "sparse_attn_fwd", "sparse_attn_merge_kernel": "sparse_attn_fwd",
                 "index_count_kernel": "sparse_attn_fwd", "index_cta_scan_kernel": "sparse_attn_fwd",
@@ -440,6 +458,7 @@ def main():
         if other in sides:
             roofline[other] = sides[other]
     kernels_ms = {k: round(v[1] / args.steps, 3) for k, v in sorted(ktimes.items(), key=lambda kv: -kv[1][1])}
+    sel_stats = selection_stats(w, x, sh, sel) if rank == 0 else None
 
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and world == 1:
@@ -463,6 +482,7 @@ def main():
             "phases_tflops": {k: round(phase_flops[k] / (phase_ms[k] * 1e-3) / 1e12, 2) for k in phase_ms},
             "useful_tflop_per_step": round(step_flops / 1e12, 4),
             "kernels_ms_per_step": kernels_ms,
+            "selection": sel_stats,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
             "clocks": clk, "impl": "ours",
         }

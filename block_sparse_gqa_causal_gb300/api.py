@@ -23,7 +23,7 @@ OP_INDEX_SELECT, OP_SPARSE_ATTN_FWD, OP_KL_FWD, OP_FUSED_BWD, OP_FUSED_BWD_KL, O
 STATUS = {0: "MSA_OK", 1: "MSA_ERR_INVALID_ARGUMENT", 2: "MSA_ERR_UNSUPPORTED", 3: "MSA_ERR_WORKSPACE",
           4: "MSA_ERR_CUDA", 5: "MSA_ERR_TIMEOUT", 6: "MSA_ERR_DEVICE"}
 EXPORTS = ("msa_workspace_size", "msa_index_select", "msa_sparse_attn_fwd", "msa_kl_fwd", "msa_fused_bwd",
-           "msa_fused_bwd_kl", "msa_train_step",
+           "msa_fused_bwd_kl", "msa_train_step", "msa_block_mask",
            "msa_last_error", "msa_check_device_status", "msa_version", "msa_launch_count")
 
 
@@ -96,8 +96,9 @@ def lib() -> ctypes.CDLL:
             L.msa_fused_bwd_kl.argtypes = [S, P, P, P, P, P, P, P, P, P, P, f, P, P, P, P, P, P, P, P, sz, P]
             L.msa_train_step.argtypes = [S, P, P, P, P, P, P, f, P, P, P, P, P, P, P, P, P, P, P, P, sz, P]
             L.msa_check_device_status.argtypes = [P, P]
+            L.msa_block_mask.argtypes = [S, P, P, P, P, P]
             for fn in ("msa_index_select", "msa_sparse_attn_fwd", "msa_kl_fwd", "msa_fused_bwd", "msa_fused_bwd_kl",
-                       "msa_train_step", "msa_check_device_status"):
+                       "msa_train_step", "msa_check_device_status", "msa_block_mask"):
                 getattr(L, fn).restype = ctypes.c_int
             L.msa_last_error.restype = ctypes.c_char_p
             L.msa_version.restype = ctypes.c_char_p
@@ -274,6 +275,24 @@ def train_step(shape: Shape, q, k, v, q_idx, k_idx, d_o, kl_coef: float = 1.0, *
                                 _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dq_idx"]), _ptr(out["dk_idx"]), _ptr(ws),
                                 ws.numel(), _stream(stream)))
     return out
+
+
+def block_mask(shape: Shape, sel_idx, *, counts=False, blocks=False, stream=None):
+    """msa_block_mask.  Returns the mask words [B, Hkv, ceil(Nq/128),
+    ceil(nb/32)] as int32 (the uint32 bit patterns), plus the per-tile
+    active-block counts [B, Hkv, T] and the ascending active-block lists
+    [B, Hkv, T, nb] (-1 padded) when asked for."""
+    s = shape
+    _need(sel_idx, "sel_idx", (s.B, s.Hkv, s.Nq, s.topk), torch.int32)
+    T, W = (s.Nq + 127) // 128, (s.nb + 31) // 32
+    dev = sel_idx.device
+    mask = torch.empty((s.B, s.Hkv, T, W), dtype=torch.int32, device=dev)
+    cnt = torch.empty((s.B, s.Hkv, T), dtype=torch.int32, device=dev) if counts else None
+    blk = torch.empty((s.B, s.Hkv, T, s.nb), dtype=torch.int32, device=dev) if blocks else None
+    _check(lib().msa_block_mask(ctypes.byref(s.c()), _ptr(sel_idx), _ptr(mask), _ptr(cnt), _ptr(blk),
+                                _stream(stream)))
+    out = (mask,) + ((cnt,) if counts else ()) + ((blk,) if blocks else ())
+    return out[0] if len(out) == 1 else out
 
 
 def check_device_status(workspace, stream=None) -> None:

@@ -395,6 +395,22 @@ cudaError_t kl_forward(const Problem &p, const void *q, const void *k, const voi
 
 extern "C" {
 
+msa_status msa_block_mask(const msa_shape *shape, const int32_t *sel_idx, uint32_t *mask, int32_t *tile_counts,
+                          int32_t *tile_blocks, void *stream)
+{
+    Problem p;
+    msa_status st = make_problem(shape, p);
+    if (st != MSA_OK) return st;
+    if (!sel_idx || !mask) return fail(MSA_ERR_INVALID_ARGUMENT, "sel_idx and mask must be non-NULL");
+    if (((uintptr_t)sel_idx | (uintptr_t)mask | (uintptr_t)tile_counts | (uintptr_t)tile_blocks) & 3u)
+        return fail(MSA_ERR_INVALID_ARGUMENT, "sel_idx, mask, tile_counts and tile_blocks must be 4-byte aligned");
+    if (block_mask_smem_bytes(p) > 160 * 1024)
+        return fail(MSA_ERR_UNSUPPORTED, "block_mask: %d key blocks, more than the supported 655,328", p.nb);
+    cudaError_t e = launch_block_mask(p, sel_idx, mask, tile_counts, tile_blocks, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "block_mask launch");
+    return MSA_OK;
+}
+
 msa_status msa_kl_fwd(const msa_shape *shape, const void *q, const void *k, const void *q_idx, const void *k_idx,
                       const int32_t *sel_idx, const float *lse, float kl_coef, float *lse_idx, float *kl_rows,
                       float *kl_loss, void *workspace, size_t workspace_bytes, void *stream)

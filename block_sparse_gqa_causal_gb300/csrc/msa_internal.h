@@ -51,6 +51,11 @@ cudaError_t launch_index_scores(const Problem &p, const bf16 *q_idx, const bf16 
 // Top-k block selection from block scores.  sel: [B, Hkv, Nq, topk].
 cudaError_t launch_block_topk(const Problem &p, const float *bs, int32_t *sel, DeviceStatus *st,
                               cudaStream_t s);
+// Block mask of a selection (uint32 words per 128-query tile, one bit per
+// key block), optionally each tile's active-block count and ascending list.
+size_t block_mask_smem_bytes(const Problem &p);
+cudaError_t launch_block_mask(const Problem &p, const int32_t *sel, uint32_t *mask, int32_t *counts, int32_t *active,
+                              cudaStream_t s);
 // Merge of per-slice candidate lists (16 descending block keys per (row,
 // slice)) into the selection: the second half of the fused decode selection.
 cudaError_t launch_block_topk_merge(const Problem &p, const unsigned long long *cand, int slices, int32_t *sel,

@@ -215,6 +215,27 @@ msa_status msa_train_step(const msa_shape *shape, const void *q, const void *k, 
 msa_status msa_index_select_noalloc(const msa_shape *shape, const void *q_idx, const void *k_idx,
                                     int32_t *sel_idx, void *stream);
 
+/*
+ * Block mask of a selection (section 4.3, "Turn support into a block mask").
+ * A query tile is 128 consecutive query rows i of one (batch b, group r),
+ * T = ceil(Nq/128) tiles per (b, r); its mask has one bit per key block c,
+ * set when some query of the tile selected c (the OR-union of the tile's
+ * selections), packed 32 to a word: block c is bit c%32 of word c/32.
+ *   sel_idx      [B, Hkv, Nq, topk] int32 (as msa_index_select writes it);
+ *                -1 entries are padding; ids >= nb are ignored.
+ *   mask         [B, Hkv, T, W] uint32, W = ceil(nb/32), nb = ceil(Nk/block);
+ *                the bits of blocks >= nb in the last word are zero.
+ *   tile_counts  [B, Hkv, T] int32, the number of set bits (active blocks)
+ *                per tile; may be NULL.
+ *   tile_blocks  [B, Hkv, T, nb] int32, each tile's active blocks in
+ *                ascending order (the traversal: per word, count the set
+ *                bits, visit them by rank), then -1; may be NULL.
+ * Caller-owned device memory, 4-byte aligned; no workspace; asynchronous on
+ * stream.  nb above 655,328 -> MSA_ERR_UNSUPPORTED.
+ */
+msa_status msa_block_mask(const msa_shape *shape, const int32_t *sel_idx, uint32_t *mask, int32_t *tile_counts,
+                          int32_t *tile_blocks, void *stream);
+
 /* Message of the last failed call on this host thread ("" if none). */
 const char *msa_last_error(void);
 

@@ -81,6 +81,19 @@ def test_null_and_misaligned_pointers_are_rejected(libmsa):
     assert rc == 3   # workspace too small
 
 
+def test_block_mask_rejects_bad_arguments_before_any_launch(libmsa):
+    from block_sparse_gqa_causal_gb300 import api
+    sh = api.Shape(B=1, Nq=256, Nk=256, Hq=8, Hkv=2, d=64, d_idx=64, topk=4)
+    good = ctypes.c_void_p(1 << 20)
+    rc = libmsa.msa_block_mask(ctypes.byref(sh.c()), None, good, None, None, None)
+    assert rc == 1 and b"non-NULL" in libmsa.msa_last_error()
+    rc = libmsa.msa_block_mask(ctypes.byref(sh.c()), good, ctypes.c_void_p((1 << 20) + 2), None, None, None)
+    assert rc == 1 and b"aligned" in libmsa.msa_last_error()
+    big = api.Shape(B=1, Nq=1, Nk=700000 * 128, Hq=8, Hkv=2, d=64, d_idx=64, topk=4, q_offset=700000 * 128 - 1)
+    rc = libmsa.msa_block_mask(ctypes.byref(big.c()), good, good, None, None, None)
+    assert rc == 2 and b"655,328" in libmsa.msa_last_error()
+
+
 def test_bwd_rejects_non_training_layout(libmsa):
     from block_sparse_gqa_causal_gb300 import api
     sh = api.Shape(B=1, Nq=3, Nk=256, Hq=8, Hkv=2, d=64, d_idx=64, topk=4, q_offset=253)
