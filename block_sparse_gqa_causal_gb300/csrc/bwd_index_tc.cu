@@ -15,15 +15,17 @@
 //   dK_idx += dsig^T q_idx                           (M = 128 keys, N = 128 features)
 // dq_idx leaves as bf16 partial rows per (query, group, slot), summed by the
 // combine kernel; dK_idx (shared by all groups) is added to an fp32 buffer
-// once per CTA.  coef = kl_coef / (B * Nq * Hkv), the mean over (query,
-// group) rows of the per-row KL.  The kKL instantiation also gives the loss
+// once per CTA.  coef = scale_idx * kl_coef / (B * Nq * Hkv): the mean over
+// (query, group) rows of the per-row KL, times the factor scale_idx that
+// both gradients take from s = scale_idx q_idx . k_idx.  The kKL instantiation also gives the loss
 // term sum_j Pt_j s_j log2(e) of each (query, group, selected block), one
 // partial per lane quarter of keys (a transposing warp sum); with the
 // teacher's sum of Pt log2 Pt and lse_idx it makes the KL of each row.
 //
-// Roles: warp 0 gathers q_idx rows (cp.async) and row data, warp 1 owns TMEM
-// and issues the MMAs, warps 2..9 are the epilogue (TMEM lanes 32*(w%4)..,
-// query columns half (w-2)/4).  s^T and dsig^T are double-buffered.
+// Roles: warps 0 and 18 gather q_idx rows (cp.async) and row data for
+// alternate chunks, warp 1 owns TMEM and issues the MMAs, warps 2..17 are
+// the epilogue (TMEM lanes 32*(w%4).., query columns 32*((w-2)/4) .. +31).
+// s^T and dsig^T are double-buffered.
 #include <cuda_fp16.h>
 
 #include <type_traits>
@@ -37,7 +39,9 @@ namespace {
 constexpr int DI = 128;
 constexpr int kKeys = 128;
 constexpr int kQ = 128;                        // queries per chunk
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;
+constexpr int kCols = 128 / (kEpiWarps / 4);    // query columns per epilogue warp
+constexpr int kHalves = kCols / 32;
 constexpr int kProd2 = 2 + kEpiWarps;          // second producer warp: the two take alternate chunks
 constexpr int kThreads = 32 * (3 + kEpiWarps);
 constexpr int SUB = 128 * 128;                 // [128 rows][64 bf16] swizzled sub-tile
@@ -57,7 +61,7 @@ struct Meta {
 };
 constexpr int META_BYTES = (int)((sizeof(Meta) + 127) & ~size_t(127));
 constexpr int OFF_STAGE = OFF_META + kStages * META_BYTES;   // per epilogue warp: dq_idx [64 rows][32 features] bf16
-constexpr int STAGE_BYTES = 64 * 64;
+constexpr int STAGE_BYTES = kCols * 64;
 constexpr int OFF_BAR = OFF_STAGE + kEpiWarps * STAGE_BYTES;
 constexpr int ALLOC = OFF_BAR + 256 + 1024;
 
@@ -267,33 +271,34 @@ bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, cons
         const long long j = j0 + kr;
         const bool key_ok = j < p.Nk;
         const float si2 = p.scale_idx * kLog2e;
-        const int cb = hf * 64;                     // first query column of this warp
-        long long rp_prev[2] = {-1, -1};            // partial rows of columns cb + lane, cb + 32 + lane
+        const int cb = hf * kCols;                  // first query column of this warp
+        long long rp_prev[kHalves];                 // partial rows of columns cb + 32 t + lane
+#pragma unroll
+        for (int t = 0; t < kHalves; ++t) rp_prev[t] = -1;
         bool ok = true;
         auto drain = [&](int m) -> bool {
             if (!wwait(dq_full, (uint32_t)m & 1u, st, 131, abort_flag)) return false;
             tc::fence_after_sync();
-            uint32_t v0[32], v1[32];
-            tc::tmem_ld32_nowait(tmem + lane_base + TM_DQI + cb, v0);
-            tc::tmem_ld32_nowait(tmem + lane_base + TM_DQI + cb + 32, v1);
-            tc::tmem_wait32(v0);
-            tc::tmem_wait32(v1);
+            uint32_t v[kHalves][32];
+#pragma unroll
+            for (int t = 0; t < kHalves; ++t) tc::tmem_ld32_nowait(tmem + lane_base + TM_DQI + cb + 32 * t, v[t]);
+#pragma unroll
+            for (int t = 0; t < kHalves; ++t) tc::tmem_wait32(v[t]);
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(dq_free);
-            // transpose the warp's [32 features][64 queries] block through shared
+            // transpose the warp's [32 features][kCols queries] block through shared
             // memory, then write 64 contiguous bytes per row with 16-byte stores
             uint8_t *stage = sm + OFF_STAGE + (warp - 2) * STAGE_BYTES;
 #pragma unroll
-            for (int cc = 0; cc < 32; ++cc) {
-                *reinterpret_cast<bf16 *>(stage + cc * 64 + lane * 2) =
-                    __float2bfloat16_rn(p.scale_idx * __uint_as_float(v0[cc]));
-                *reinterpret_cast<bf16 *>(stage + (32 + cc) * 64 + lane * 2) =
-                    __float2bfloat16_rn(p.scale_idx * __uint_as_float(v1[cc]));
-            }
+            for (int t = 0; t < kHalves; ++t)
+#pragma unroll
+                for (int cc = 0; cc < 32; ++cc)
+                    *reinterpret_cast<bf16 *>(stage + (32 * t + cc) * 64 + lane * 2) =
+                        __float2bfloat16_rn(__uint_as_float(v[t][cc]));
             __syncwarp();
 #pragma unroll
-            for (int it = 0; it < 8; ++it) {
+            for (int it = 0; it < kCols / 8; ++it) {
                 const int row = it * 8 + (lane >> 2), q4 = lane & 3;
                 const long long rix = __shfl_sync(0xffffffffu, rp_prev[it >> 2], row & 31);
                 const uint4 x = *reinterpret_cast<const uint4 *>(stage + row * 64 + q4 * 16);
@@ -307,41 +312,44 @@ bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, cons
             const Meta *meta = reinterpret_cast<const Meta *>(sm + OFF_META + s * META_BYTES);
             if (!wwait(&full[s], (uint32_t)(n / kStages) & 1u, st, 132, abort_flag)) { ok = false; break; }
             const int nq = meta->nq;
-            // teacher values of this key for the warp's 64 queries
-            // the teacher of this key for entries 128n + cb .. + 63: eight 8-entry
+            // the teacher of this key for entries 128n + cb .. + kCols-1: 8-entry
             // groups, 16 bytes each (padding entries beyond nq are masked below)
-            uint4 tv[8];
+            uint4 tv[kCols / 8];
             {
                 const __half *src = pt + ((long long)pt_off[bucket] + (long long)n * 128 + cb) * kKeys + kr * 8;
 #pragma unroll
-                for (int x = 0; x < 8; ++x) tv[x] = __ldg(reinterpret_cast<const uint4 *>(src + (long long)x * 8 * kKeys));
+                for (int x = 0; x < kCols / 8; ++x)
+                    tv[x] = __ldg(reinterpret_cast<const uint4 *>(src + (long long)x * 8 * kKeys));
             }
             if (!wwait(&s_full[sb], (uint32_t)(n >> 1) & 1u, st, 133, abort_flag)) { ok = false; break; }
             tc::fence_after_sync();
-            uint32_t s0[32], s1[32];
-            tc::tmem_ld32_nowait(tmem + lane_base + TM_S + sb * kQ + cb, s0);
-            tc::tmem_ld32_nowait(tmem + lane_base + TM_S + sb * kQ + cb + 32, s1);
-            long long rp_cur[2], kl_cur[2];
+            uint32_t sv_[kHalves][32];
 #pragma unroll
-            for (int t = 0; t < 2; ++t) {
+            for (int t = 0; t < kHalves; ++t) tc::tmem_ld32_nowait(tmem + lane_base + TM_S + sb * kQ + cb + 32 * t, sv_[t]);
+            long long rp_cur[kHalves], kl_cur[kHalves];
+#pragma unroll
+            for (int t = 0; t < kHalves; ++t) {
                 const int u = cb + 32 * t + lane;
                 rp_cur[t] = u < nq ? (((long long)b * p.Nq + meta->qi[u]) * p.Hkv + r) * p.topk + meta->slot[u] : -1;
                 kl_cur[t] = u < nq ? (((long long)b * p.Hkv + r) * p.Nq + meta->qi[u]) * p.topk + meta->slot[u] : -1;
             }
-            tc::tmem_wait32(s0);
-            tc::tmem_wait32(s1);
+#pragma unroll
+            for (int t = 0; t < kHalves; ++t) tc::tmem_wait32(sv_[t]);
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&s_free[sb]);
-            uint32_t sg[32];
-            // no per-element mask where every query of the warp's 64 sees the whole block
-            const int pmin = __reduce_min_sync(0xffffffffu, min(meta->pos[cb + lane], meta->pos[cb + 32 + lane]));
+            uint32_t sg[kCols / 2];
+            // no per-element mask where every query of the warp's columns sees the whole block
+            int pmin = meta->pos[cb + lane];
+#pragma unroll
+            for (int t = 1; t < kHalves; ++t) pmin = min(pmin, meta->pos[cb + 32 * t + lane]);
+            pmin = __reduce_min_sync(0xffffffffu, pmin);
             const bool all_vis = (long long)pmin >= j0 + kKeys - 1 && j0 + kKeys <= p.Nk;
             const int ji = (int)min(j, (long long)INT_MAX);
             auto dsig_tile = [&](auto all_tag) {
                 constexpr bool kAll = decltype(all_tag)::value;
 #pragma unroll
-                for (int t = 0; t < 2; ++t) {
+                for (int t = 0; t < kHalves; ++t) {
                     [[maybe_unused]] float lv[6];   // streaming warp sum of Pt s log2(e) (KL partial)
 #pragma unroll
                     for (int cc = 32 * t; cc < 32 * t + 32; cc += 4) {
@@ -359,7 +367,7 @@ bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, cons
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const int col = cc + e;
-                            const float sv = __uint_as_float(col < 32 ? s0[col] : s1[col - 32]);
+                            const float sv = __uint_as_float(sv_[col >> 5][col & 31]);
                             const __half2 h2 = *reinterpret_cast<const __half2 *>(
                                 reinterpret_cast<const uint32_t *>(&tv[col >> 3]) + ((col & 7) >> 1));
                             const float ptv = (col & 1) ? __high2float(h2) : __low2float(h2);
@@ -387,17 +395,18 @@ bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, cons
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&empty[s]);   // the stage's row data is no longer read
             if (n >= 1 && !wwait(g_free, (uint32_t)(n - 1) & 1u, st, 134, abort_flag)) { ok = false; break; }
-            uint8_t *dst = sm + OFF_SIG + hf * SUB;                   // query half hf = sub-tile hf
+            uint8_t *dst = sm + OFF_SIG + (cb >> 6) * SUB;           // 64-query sub-tile of column cb
+            const int ch0 = (cb & 63) >> 3;                           // its first 16-byte chunk
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch)
-                *reinterpret_cast<uint4 *>(dst + swz(kr, ch)) =
+            for (int ch = 0; ch < kCols / 8; ++ch)
+                *reinterpret_cast<uint4 *>(dst + swz(kr, ch0 + ch)) =
                     make_uint4(sg[ch * 4], sg[ch * 4 + 1], sg[ch * 4 + 2], sg[ch * 4 + 3]);
             tc::fence_proxy_async();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(g_full);
             if (n >= 1 && !drain(n - 1)) { ok = false; break; }
-            rp_prev[0] = rp_cur[0];
-            rp_prev[1] = rp_cur[1];
+#pragma unroll
+            for (int t = 0; t < kHalves; ++t) rp_prev[t] = rp_cur[t];
         }
         if (ok) ok = drain(nch - 1);
         if (ok) {
@@ -406,9 +415,9 @@ bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, cons
             tc::fence_after_sync();
         }
         if (ok) {
-            // dK_idx of this key, features cb .. cb+63 (the column half doubles as the feature half)
+            // dK_idx of this key, features cb .. cb+kCols-1 (the warp's column range doubles as its feature range)
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
+            for (int h2 = 0; h2 < kHalves; ++h2) {
                 uint32_t a[32];
                 tc::tmem_ld32_nowait(tmem + lane_base + TM_DKI + cb + h2 * 32, a);
                 tc::tmem_wait32(a);
@@ -416,8 +425,8 @@ bwd_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, cons
                     float *dst = dki_acc + ((long long)b * p.Nk + j) * DI + cb + h2 * 32;
 #pragma unroll
                     for (int x = 0; x < 32; x += 4)
-                        tc::red_add_v4(dst + x, p.scale_idx * __uint_as_float(a[x]), p.scale_idx * __uint_as_float(a[x + 1]),
-                                       p.scale_idx * __uint_as_float(a[x + 2]), p.scale_idx * __uint_as_float(a[x + 3]));
+                        tc::red_add_v4(dst + x, __uint_as_float(a[x]), __uint_as_float(a[x + 1]),
+                                       __uint_as_float(a[x + 2]), __uint_as_float(a[x + 3]));
                 }
             }
         }
@@ -444,7 +453,7 @@ cudaError_t launch_bwd_index_tc(const Problem &p, const bf16 *q_idx, const bf16 
     const unsigned long long si[2] = {DI * 2ull, (unsigned long long)p.kv_rows * DI * 2ull};
     const unsigned bi[3] = {64, (unsigned)kKeys, 1};
     if ((e = make_tmap_bf16(&tki, k_idx, 3, di, si, bi)) != cudaSuccess) return e;
-    const float coef = kl_coef / ((float)p.B * (float)p.Nq * (float)p.Hkv);
+    const float coef = p.scale_idx * kl_coef / ((float)p.B * (float)p.Nq * (float)p.Hkv);
     {
         TimedLaunch timed_("bwd_index_tc_kernel", s);
         kern<<<dim3(p.Hkv, p.nb, p.B), kThreads, ALLOC, s>>>(tki, p, q_idx, lse_idx, coef, w.bucket_off,
