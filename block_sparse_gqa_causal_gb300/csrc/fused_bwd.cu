@@ -100,59 +100,69 @@ __global__ void __launch_bounds__(256) bwd_rowdot_kernel(Problem p, const bf16 *
 // Teacher term of the KL loss (section 3.2, the L_KL equation): for every
 // (query, group, selected block), sum over the block's keys of Pt log2 Pt,
 // read back from the teacher the main-branch backward left per (bucket
-// entry, key) in groups of 8 entries ([group][key][8 entries], fp16).  One
-// CTA per bucket, four groups per step (two 16-byte loads in flight per
-// thread): thread k of a half reads key k's 8 entries of a group, each warp
-// sums its 32 keys per entry with a transposing warp sum, and the four warps
-// of a half add up in shared memory.  Writes kla[((b, r, query), slot)].
+// entry, key) in groups of 8 entries ([group][key][8 entries], fp16, each
+// bucket's entries padded to whole groups).  The grid runs over the flat
+// array of groups, 32 groups (64 KB) per CTA with all of a thread's loads in
+// flight, so the largest buckets (the early blocks most queries select) are
+// spread over many CTAs.  Thread k of a half reads key k's 8 entries of
+// every other group; each warp sums its 32 keys per entry with a transposing
+// warp sum, the four warps of a half add up in shared memory, and each
+// entry's bucket is found by binary search in pt_off.  Writes
+// kla[((b, r, query), slot)].
+constexpr int kEntGroups = 32;   // 8-entry groups per CTA
+
 __global__ void __launch_bounds__(256) bwd_teacher_entropy_kernel(Problem p, const int32_t *__restrict__ bucket_off,
                                                                   const int32_t *__restrict__ bucket_q,
                                                                   const __half *__restrict__ pt,
-                                                                  const int32_t *__restrict__ pt_off,
+                                                                  const int32_t *__restrict__ pt_off, int nbk,
                                                                   float *__restrict__ kla)
 {
-    const int r = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
-    const long long bucket = ((long long)b * p.Hkv + r) * p.nb + c;
-    const int qbeg = bucket_off[bucket], n = bucket_off[bucket + 1] - qbeg;
-    if (n <= 0) return;
-    const long long base = pt_off[bucket];
-    __shared__ float part[2][2][8][8];               // [step parity][sub-step][warp][entry]
+    const long long n_groups = pt_off[nbk] / 8;
+    const long long g0 = (long long)blockIdx.x * kEntGroups;
+    if (g0 >= n_groups) return;
+    __shared__ float part[kEntGroups / 2][8][8];     // [group pair][warp][entry]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int half = threadIdx.x >> 7, key = threadIdx.x & 127;
-    for (int g0 = 0, it = 0; g0 < n; g0 += 32, ++it) {
-        uint4 raw[2];
+    uint4 raw[kEntGroups / 2];
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int g = g0 + 16 * j + 8 * half;    // this thread's group of 8 entries
-            raw[j] = g < n ? __ldg(reinterpret_cast<const uint4 *>(pt + (base + g) * 128 + key * 8))
-                           : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            float v[8];
-            const __half2 *h = reinterpret_cast<const __half2 *>(&raw[j]);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 f = __half22float2(h[e]);
-                v[2 * e] = f.x > 0.f ? f.x * __log2f(f.x) : 0.f;
-                v[2 * e + 1] = f.y > 0.f ? f.y * __log2f(f.y) : 0.f;
-            }
-            float tot[1];
-            lane_colsum(v, lane, tot);               // lane l: entry l % 8 of the warp's 32 keys
-            if (lane < 8) part[it & 1][j][warp][lane] = tot[0];
-        }
-        __syncthreads();                             // the other parity buffer keeps the next step race-free
-        if (threadIdx.x < 32) {
-            const int j = threadIdx.x >> 4, hh = (threadIdx.x >> 3) & 1, e = threadIdx.x & 7;
-            const int t = g0 + 16 * j + 8 * hh + e;
-            if (t < n) {
-                const float a = (part[it & 1][j][4 * hh][e] + part[it & 1][j][4 * hh + 1][e]) +
-                                (part[it & 1][j][4 * hh + 2][e] + part[it & 1][j][4 * hh + 3][e]);
-                const int ent = bucket_q[qbeg + t];
-                kla[(((long long)b * p.Hkv + r) * p.Nq + entry_row(ent)) * p.topk + entry_slot(ent)] = a;
-            }
-        }
+    for (int j = 0; j < kEntGroups / 2; ++j) {
+        const long long g = g0 + 2 * j + half;       // this thread's groups: every other one
+        raw[j] = g < n_groups ? __ldg(reinterpret_cast<const uint4 *>(pt + g * 8 * 128 + key * 8))
+                              : make_uint4(0u, 0u, 0u, 0u);
     }
+#pragma unroll
+    for (int j = 0; j < kEntGroups / 2; ++j) {
+        float v[8];
+        const __half2 *h = reinterpret_cast<const __half2 *>(&raw[j]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __half22float2(h[e]);
+            v[2 * e] = f.x > 0.f ? f.x * __log2f(f.x) : 0.f;
+            v[2 * e + 1] = f.y > 0.f ? f.y * __log2f(f.y) : 0.f;
+        }
+        float tot[1];
+        lane_colsum(v, lane, tot);                   // lane l: entry l % 8 of the warp's 32 keys
+        if (lane < 8) part[j][warp][lane] = tot[0];
+    }
+    __syncthreads();
+    // one entry per thread: group gl = 2 j + half of the CTA, entry e
+    const int gl = threadIdx.x >> 3, e = threadIdx.x & 7;
+    const long long g = g0 + gl;
+    if (g >= n_groups) return;
+    const int j = gl >> 1, hh = gl & 1;
+    const float a = (part[j][4 * hh][e] + part[j][4 * hh + 1][e]) + (part[j][4 * hh + 2][e] + part[j][4 * hh + 3][e]);
+    const long long flat = g * 8 + e;
+    int lo = 0, hi = nbk;                            // the last bucket starting at or before `flat`
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (pt_off[mid] <= flat) lo = mid;
+        else hi = mid;
+    }
+    const int t = (int)(flat - pt_off[lo]);
+    if (t >= bucket_off[lo + 1] - bucket_off[lo]) return;   // padding entry of the bucket's last group
+    const int ent = bucket_q[bucket_off[lo] + t];
+    const long long br = lo / p.nb;                  // b * Hkv + r
+    kla[(br * p.Nq + entry_row(ent)) * p.topk + entry_slot(ent)] = a;
 }
 
 // pt_off[x] = sum over buckets y < x of cnt[y] rounded up to 8 (x = 0..n),
@@ -687,8 +697,11 @@ cudaError_t launch_fused_bwd(const Problem &p, const bf16 *q, const bf16 *k, con
         if (w.kla) {
             {
                 TimedLaunch timed_("bwd_teacher_entropy_kernel", s);
-                bwd_teacher_entropy_kernel<<<dim3(p.Hkv, p.nb, p.B), 256, 0, s>>>(p, w.bucket_off, w.bucket_q, w.pt,
-                                                                                 w.pt_off, w.kla);
+                // an upper bound of the padded entries: every (row, slot) once, plus < 8 per bucket
+                const int nbk = (int)((long long)p.B * p.Hkv * p.nb);
+                const long long max_groups = ((long long)p.B * p.Nq * p.Hkv * p.topk + 8LL * nbk) / 8;
+                bwd_teacher_entropy_kernel<<<(unsigned)((max_groups + kEntGroups - 1) / kEntGroups), 256, 0, s>>>(
+                    p, w.bucket_off, w.bucket_q, w.pt, w.pt_off, nbk, w.kla);
             }
             note_launch();
             if ((e = launch_bwd_kl_combine(p, sel, lse_idx, w.kla, w.klb, w.kl_rows, s)) != cudaSuccess) return e;
