@@ -65,18 +65,31 @@ sparse_attn_fwd_kernel(Problem p, const bf16 *__restrict__ q, const bf16 *__rest
     const long long pos = (long long)p.q_offset + i;
     const int32_t *srow = sel + (((long long)b * p.Hkv + r) * p.Nq + i) * p.topk;
 
-    if (tid == 0) {
-        int n = 0;
-        for (int m = 0; m < p.topk; ++m) {
-            const int c = srow[m];
-            if (c < 0) continue;
-            if ((long long)c * 128 > pos) { report(st, kDevCheck, 31, c); continue; }
-            const long long start = (long long)c * 128;
-            const long long end = min(min(start + 128, pos + 1), (long long)p.Nk);
-            for (long long s0 = start; s0 < end && n < kMaxChunks; s0 += kChunk)
-                chunks[n++] = make_int2((int)s0, (int)min((long long)kChunk, end - s0));
+    if (warp == 0) {
+        // the row's chunk list, in selection order: lane m takes selected block m
+        // (topk <= 32), its chunks go after those of the lanes below it
+        const int c = lane < p.topk ? srow[lane] : -1;
+        long long start = 0, end = 0;
+        if (c >= 0) {
+            if ((long long)c * 128 > pos) report(st, kDevCheck, 31, c);
+            else {
+                start = (long long)c * 128;
+                end = min(min(start + 128, pos + 1), (long long)p.Nk);
+            }
         }
-        n_chunks = n;
+        const int nck = end > start ? (int)((end - start + kChunk - 1) / kChunk) : 0;
+        int off = nck;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int o2 = __shfl_up_sync(0xffffffffu, off, d);
+            if (lane >= d) off += o2;
+        }
+        off -= nck;
+        for (int x = 0; x < nck; ++x) {
+            const long long s0 = start + (long long)x * kChunk;
+            chunks[off + x] = make_int2((int)s0, (int)min((long long)kChunk, end - s0));
+        }
+        if (lane == 31) n_chunks = off + nck;
     }
     // Q rows of the group's heads (rows >= G are zero)
     const bf16 *qrow = q + (((long long)b * p.Nq + i) * p.Hq + (long long)r * G) * D;
@@ -243,6 +256,18 @@ __global__ void __launch_bounds__(256) sparse_attn_merge_kernel(Problem p, int n
     const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= (long long)p.B * p.Nq * p.Hq) return;
+    constexpr int PER = D / 32;
+    // the first eight shares' rows are requested together with the (max, sum) pairs
+    float x[8][PER];
+    auto load8 = [&](int s0) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const float *src = part_o + (row * nsplit + min(s0 + u, nsplit - 1)) * D;
+#pragma unroll
+            for (int e = 0; e < PER; ++e) x[u][e] = __ldg(src + lane + 32 * e);
+        }
+    };
+    load8(0);
     const float2 ml = lane < nsplit ? part_ml[row * nsplit + lane] : make_float2(-INFINITY, 0.f);
     float M = ml.x;
 #pragma unroll
@@ -251,19 +276,12 @@ __global__ void __launch_bounds__(256) sparse_attn_merge_kernel(Problem p, int n
     float L = f * ml.y;
 #pragma unroll
     for (int o2 = 16; o2 > 0; o2 >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o2);
-    constexpr int PER = D / 32;
     float acc[PER];
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] = 0.f;
     // eight shares' rows in flight at a time
     for (int s0 = 0; s0 < nsplit; s0 += 8) {
-        float x[8][PER];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const float *src = part_o + (row * nsplit + min(s0 + u, nsplit - 1)) * D;
-#pragma unroll
-            for (int e = 0; e < PER; ++e) x[u][e] = __ldg(src + lane + 32 * e);
-        }
+        if (s0 > 0) load8(s0);
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const float w = s0 + u < nsplit ? __shfl_sync(0xffffffffu, f, (s0 + u) & 31) : 0.f;
