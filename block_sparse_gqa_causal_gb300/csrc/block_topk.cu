@@ -184,7 +184,10 @@ block_topk_split_kernel(Problem p, const float *__restrict__ bs, int32_t *__rest
 // Decode with the fused selection: the score kernel's CTA for slice y of a
 // row's blocks left that row's 16 best keys of the slice, in descending
 // order, at cand[(row * slices + y) * 16 ..] (0 = no block).  The row's k-1
-// best blocks are among them (each slice keeps at least k-1).  One CTA per
+// best blocks are among them (each slice keeps at least k-1).  Only slices
+// starting before the row's local block c0 are read: a slice whose blocks
+// lie past every row of its tile was skipped by the score kernel and holds
+// nothing of this call (its memory is stale).  One CTA per
 // row: warp w takes the slice pairs w, w + 8, ... (all its loads issued
 // before any merge); the two descending lists of a pair, the second
 // reversed, form a bitonic sequence, sorted by one bitonic merge and merged
@@ -192,7 +195,8 @@ block_topk_split_kernel(Problem p, const float *__restrict__ bs, int32_t *__rest
 constexpr int kMergeBatch = 4;   // slice pairs per warp per batch of loads
 
 __global__ void __launch_bounds__(kWarps * 32)
-block_topk_merge_kernel(Problem p, const unsigned long long *__restrict__ cand, int slices, int32_t *__restrict__ sel)
+block_topk_merge_kernel(Problem p, const unsigned long long *__restrict__ cand, int slices, int span,
+                        int32_t *__restrict__ sel)
 {
     __shared__ unsigned long long lists[kWarps][32];
     const int lane = threadIdx.x & 31;
@@ -210,14 +214,15 @@ block_topk_merge_kernel(Problem p, const unsigned long long *__restrict__ cand, 
         return;
     }
     const unsigned long long *src = cand + row * slices * 16;
-    const int pairs = (slices + 1) / 2;
+    const int ys = min(slices, (c0 + span - 1) / span);   // slices holding blocks before c0
+    const int pairs = (ys + 1) / 2;
     unsigned long long best = 0ull;
     for (int t0 = wi; t0 < pairs; t0 += kWarps * kMergeBatch) {
         unsigned long long ck[kMergeBatch];
 #pragma unroll
         for (int t = 0; t < kMergeBatch; ++t) {
             const int y = 2 * (t0 + t * kWarps) + (lane >> 4);
-            ck[t] = y < slices ? __ldg(src + (long long)y * 16 + (lane & 15)) : 0ull;
+            ck[t] = y < ys ? __ldg(src + (long long)y * 16 + (lane & 15)) : 0ull;
         }
 #pragma unroll
         for (int t = 0; t < kMergeBatch; ++t) {
@@ -240,13 +245,13 @@ block_topk_merge_kernel(Problem p, const unsigned long long *__restrict__ cand, 
 
 }  // namespace
 
-cudaError_t launch_block_topk_merge(const Problem &p, const unsigned long long *cand, int slices, int32_t *sel,
-                                    cudaStream_t s)
+cudaError_t launch_block_topk_merge(const Problem &p, const unsigned long long *cand, int slices, int span,
+                                    int32_t *sel, cudaStream_t s)
 {
     const long long rows = (long long)p.B * p.Nq * p.Hkv;
     {
         TimedLaunch timed_("block_topk_merge_kernel", s);
-        block_topk_merge_kernel<<<(unsigned)rows, kWarps * 32, 0, s>>>(p, cand, slices, sel);
+        block_topk_merge_kernel<<<(unsigned)rows, kWarps * 32, 0, s>>>(p, cand, slices, span, sel);
     }
     note_launch();
     return cudaGetLastError();

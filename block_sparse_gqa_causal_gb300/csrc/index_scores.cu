@@ -447,7 +447,7 @@ cudaError_t launch_index_select(const Problem &p, const bf16 *q_idx, const bf16 
         cudaError_t e = p.d_idx == 128 ? launch_t<128>(p, q_idx, k_idx, nullptr, nullptr, cand, st, s)
                                        : launch_t<64>(p, q_idx, k_idx, nullptr, nullptr, cand, st, s);
         if (e != cudaSuccess) return e;
-        return launch_block_topk_merge(p, cand, splits, sel, s);
+        return launch_block_topk_merge(p, cand, splits, span, sel, s);
     }
     float *bs = bs_out ? bs_out : bs_scratch;
     cudaError_t e = launch_index_scores(p, q_idx, k_idx, bs, st, s);

@@ -57,9 +57,10 @@ size_t block_mask_smem_bytes(const Problem &p);
 cudaError_t launch_block_mask(const Problem &p, const int32_t *sel, uint32_t *mask, int32_t *counts, int32_t *active,
                               cudaStream_t s);
 // Merge of per-slice candidate lists (16 descending block keys per (row,
-// slice)) into the selection: the second half of the fused decode selection.
-cudaError_t launch_block_topk_merge(const Problem &p, const unsigned long long *cand, int slices, int32_t *sel,
-                                    cudaStream_t s);
+// slice), slices of `span` blocks) into the selection: the second half of
+// the fused decode selection.
+cudaError_t launch_block_topk_merge(const Problem &p, const unsigned long long *cand, int slices, int span,
+                                    int32_t *sel, cudaStream_t s);
 // Index scores + selection: fused into the score kernel when every CTA sees
 // all blocks of its rows and topk <= 16 (scores stored only if bs_out is set),
 // else scores to bs_out (or bs_scratch) and the separate top-k kernel.

@@ -156,3 +156,26 @@ def test_decode_1m_split_fused_selection_matches_scores_path():
     s = sel_f.cpu().numpy().reshape(B * Hkv, k)
     assert np.array_equal(s, sel_s.cpu().numpy().reshape(B * Hkv, k))
     assert np.all(s[:, -1] == pos // 128) and np.all(np.diff(s, axis=1) > 0) and np.all(s >= 0)
+
+
+@pytest.mark.parametrize("B,Nq,Nk,q_offset,Hkv,k", [(1, 3000, 3000, 0, 8, 16), (2, 1, 200000, 199999, 4, 16),
+                                                     (1, 40, 70000, 69960, 2, 8)])
+def test_split_selection_ignores_stale_workspace(B, Nq, Nk, q_offset, Hkv, k):
+    """Rows split across CTAs with the scores not asked for (per-slice
+    candidates, then the merge), run in a workspace filled with garbage first:
+    the selection must equal the scores path's.  Early row tiles of a prefill
+    skip the slices past all their blocks, which then hold stale memory."""
+    import torch
+    from block_sparse_gqa_causal_gb300 import api
+    g = torch.Generator(device="cuda").manual_seed(Nq + Nk)
+    sh = api.Shape(B=B, Nq=Nq, Nk=Nk, Hq=Hkv, Hkv=Hkv, d=128, d_idx=128, topk=k, q_offset=q_offset)
+    qi = torch.randn(B, Nq, Hkv, 128, device="cuda", generator=g).bfloat16()
+    ki = torch.randn(B, Nk, 128, device="cuda", generator=g).bfloat16()
+    want, _ = api.index_select(sh, qi, ki, return_scores=True)
+    for fill in (0xFF, 0x7F, 0x3C):
+        ws = api.new_workspace(sh, api.OP_INDEX_SELECT)
+        ws.fill_(fill)
+        ws[:256] = 0                                   # the status word starts clear
+        got = api.index_select(sh, qi, ki, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(got, want), fill
