@@ -159,12 +159,14 @@ def test_decode_1m_split_fused_selection_matches_scores_path():
 
 
 @pytest.mark.parametrize("B,Nq,Nk,q_offset,Hkv,k", [(1, 3000, 3000, 0, 8, 16), (2, 1, 200000, 199999, 4, 16),
-                                                     (1, 40, 70000, 69960, 2, 8)])
+                                                     (1, 40, 70000, 69960, 2, 8), (1, 256, 202802, 202546, 2, 16)])
 def test_split_selection_ignores_stale_workspace(B, Nq, Nk, q_offset, Hkv, k):
     """Rows split across CTAs with the scores not asked for (per-slice
     candidates, then the merge), run in a workspace filled with garbage first:
-    the selection must equal the scores path's.  Early row tiles of a prefill
-    skip the slices past all their blocks, which then hold stale memory."""
+    the selection must equal the scores path's.  A row tile skips the slices
+    past all its blocks, which then hold stale memory: in the last case the
+    final slice (24 blocks wide) holds only block 1584, which the first tile's
+    rows (local blocks 1582, 1583) never see."""
     import torch
     from block_sparse_gqa_causal_gb300 import api
     g = torch.Generator(device="cuda").manual_seed(Nq + Nk)
