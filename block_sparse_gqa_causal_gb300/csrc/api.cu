@@ -603,6 +603,9 @@ msa_status msa_train_step(const msa_shape *shape, const void *q, const void *k, 
     fw.bucket_scratch = kw.bucket_scratch = w.bucket_scratch;
     fw.bucket_q = kw.bucket_q = w.bucket_q;
     fw.index_ready = kw.index_ready = w.index_ready = true;
+    fw.d_o = static_cast<const bf16 *>(d_o);           // the forward combine leaves D for the backward
+    fw.D = w.D;
+    w.D_ready = true;
     const bf16 *bq = static_cast<const bf16 *>(q), *bk = static_cast<const bf16 *>(k), *bv = static_cast<const bf16 *>(v);
     const bf16 *bqi = static_cast<const bf16 *>(q_idx), *bki = static_cast<const bf16 *>(k_idx);
     cudaError_t e = launch_index_select(p, bqi, bki, nullptr, bs_scratch, sel_idx, ds, s);

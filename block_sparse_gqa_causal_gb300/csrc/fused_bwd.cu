@@ -675,12 +675,14 @@ cudaError_t launch_fused_bwd(const Problem &p, const bf16 *q, const bf16 *k, con
     if ((e = cudaMemsetAsync(w.dki_acc, 0, n_dki * 4, s)) != cudaSuccess) return e;
 
     const long long rows = (long long)p.B * p.Nq * p.Hq;
-    {
-        TimedLaunch timed_("bwd_rowdot_kernel", s);
-        if (p.d == 128) bwd_rowdot_kernel<128><<<(unsigned)((rows + 63) / 64), 256, 0, s>>>(p, o, d_o, w.D);
-        else bwd_rowdot_kernel<64><<<(unsigned)((rows + 63) / 64), 256, 0, s>>>(p, o, d_o, w.D);
+    if (!w.D_ready) {
+        {
+            TimedLaunch timed_("bwd_rowdot_kernel", s);
+            if (p.d == 128) bwd_rowdot_kernel<128><<<(unsigned)((rows + 63) / 64), 256, 0, s>>>(p, o, d_o, w.D);
+            else bwd_rowdot_kernel<64><<<(unsigned)((rows + 63) / 64), 256, 0, s>>>(p, o, d_o, w.D);
+        }
+        note_launch();
     }
-    note_launch();
     if (!w.index_ready &&
         (e = launch_inverse_index(p, sel, w.bucket_cnt, w.bucket_off, w.bucket_scratch, w.bucket_q, st, s)) != cudaSuccess)
         return e;

@@ -80,6 +80,10 @@ struct FwdWork {
     float2 *stats;       // [B, Nq, Hq, topk] (row max in log2 units, row sum)
     int32_t *bucket_cnt, *bucket_off, *bucket_scratch, *bucket_q;
     bool index_ready = false;   // the inverse index of sel is already in bucket_* (built once per step)
+    // training step: with dO at hand the combine also leaves the backward's
+    // D[b, h, i] = sum_e dO * O (O as written, bf16) -- one pass over O fewer
+    const bf16 *d_o = nullptr;
+    float *D = nullptr;
 };
 cudaError_t launch_sparse_fwd_keymajor(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *v,
                                        const int32_t *sel, bf16 *o, float *lse, const FwdWork &w, DeviceStatus *st,
@@ -136,6 +140,7 @@ struct BwdWork {
     int32_t *bucket_scratch; // inverse_index_scratch_ints(p)
     int32_t *bucket_q;   // [B*Hkv*Nq*topk]  query rows per (b, r, block)
     bool index_ready;    // bucket_* already hold the inverse index of sel
+    bool D_ready;        // D already holds rowsum(dO * O) (the training step's forward combine)
 };
 cudaError_t launch_fused_bwd(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *v,
                              const bf16 *o, const bf16 *d_o, const float *lse, const bf16 *q_idx,

@@ -462,10 +462,13 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
 // contiguous; every lane loads 16 bytes of several slots at once (D/8 lanes
 // per slot, all loads in flight while the slot weights are reduced), and
 // lanes holding the same features of different slots add up with shuffles.
+// With d_o given (the training step) it also writes the backward's
+// Drow[b, h, i] = sum_e dO * O over the row, O taken as written (bf16).
 template <int D>
 __global__ void __launch_bounds__(256)
 sparse_fwd_combine_kernel(Problem p, const int32_t *__restrict__ sel, const bf16 *__restrict__ part,
-                          const float2 *__restrict__ stats, bf16 *__restrict__ o, float *__restrict__ lse)
+                          const float2 *__restrict__ stats, bf16 *__restrict__ o, float *__restrict__ lse,
+                          const bf16 *__restrict__ d_o, float *__restrict__ Drow)
 {
     constexpr int LPS = D / 8;                  // lanes per slot row
     constexpr int SPI = 32 / LPS;               // slots per load instruction
@@ -492,6 +495,8 @@ sparse_fwd_combine_kernel(Problem p, const int32_t *__restrict__ sel, const bf16
     // never written), so a row costs one memory round trip
     uint4 u[GI];
     load_group(u, 0);
+    const uint4 dov = d_o && lane < LPS ? __ldg(reinterpret_cast<const uint4 *>(d_o + row * D) + lane)
+                                        : make_uint4(0u, 0u, 0u, 0u);
     const float2 mz_raw = lane < p.topk ? __ldg(stats + row * p.topk + lane) : make_float2(-INFINITY, 0.f);
     // slot validity (same rule as the inverse index)
     const int cl = lane < p.topk ? __ldg(srow + lane) : -1;
@@ -525,11 +530,23 @@ sparse_fwd_combine_kernel(Problem p, const int32_t *__restrict__ sel, const bf16
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
     const float inv = 1.f / Z;
-    if (lane < LPS)
-        reinterpret_cast<uint4 *>(o + row * D)[lane] =
-            make_uint4(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv),
-                       pack_bf16(acc[4] * inv, acc[5] * inv), pack_bf16(acc[6] * inv, acc[7] * inv));
+    const uint4 ov = make_uint4(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv),
+                                pack_bf16(acc[4] * inv, acc[5] * inv), pack_bf16(acc[6] * inv, acc[7] * inv));
+    if (lane < LPS) reinterpret_cast<uint4 *>(o + row * D)[lane] = ov;
     if (lane == 0) lse[((long long)b * p.Hq + h) * p.Nq + i] = (M + log2f(Z)) * kLn2;
+    if (d_o) {
+        const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, gw[4] = {dov.x, dov.y, dov.z, dov.w};
+        float dd = 0.f;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+            const float2 x = unpack_bf16(ow[q4]), y = unpack_bf16(gw[q4]);
+            dd += x.x * y.x + x.y * y.y;
+        }
+        if (lane >= LPS) dd = 0.f;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, off);
+        if (lane == 0) Drow[((long long)b * p.Hq + h) * p.Nq + i] = dd;
+    }
 }
 
 template <int D, int G>
@@ -593,12 +610,14 @@ cudaError_t launch_sparse_fwd_keymajor(const Problem &p, const bf16 *q, const bf
     if (p.d == 128)
         {
             TimedLaunch timed_("sparse_fwd_combine_kernel", s);
-            sparse_fwd_combine_kernel<128><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p, sel, w.part, w.stats, o, lse);
+            sparse_fwd_combine_kernel<128><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p, sel, w.part, w.stats, o, lse,
+                                                                                     w.d_o, w.D);
         }
     else
         {
             TimedLaunch timed_("sparse_fwd_combine_kernel", s);
-            sparse_fwd_combine_kernel<64><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p, sel, w.part, w.stats, o, lse);
+            sparse_fwd_combine_kernel<64><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p, sel, w.part, w.stats, o, lse,
+                                                                                    w.d_o, w.D);
         }
     note_launch();
     return cudaGetLastError();
