@@ -23,7 +23,7 @@ OP_INDEX_SELECT, OP_SPARSE_ATTN_FWD, OP_KL_FWD, OP_FUSED_BWD, OP_FUSED_BWD_KL, O
 STATUS = {0: "MSA_OK", 1: "MSA_ERR_INVALID_ARGUMENT", 2: "MSA_ERR_UNSUPPORTED", 3: "MSA_ERR_WORKSPACE",
           4: "MSA_ERR_CUDA", 5: "MSA_ERR_TIMEOUT", 6: "MSA_ERR_DEVICE"}
 EXPORTS = ("msa_workspace_size", "msa_index_select", "msa_sparse_attn_fwd", "msa_kl_fwd", "msa_fused_bwd",
-           "msa_fused_bwd_kl", "msa_train_step", "msa_block_mask",
+           "msa_fused_bwd_kl", "msa_train_step", "msa_train_step_staged", "msa_block_mask",
            "msa_last_error", "msa_check_device_status", "msa_version", "msa_launch_count")
 
 
@@ -95,10 +95,12 @@ def lib() -> ctypes.CDLL:
             L.msa_fused_bwd.argtypes = [S, P, P, P, P, P, P, P, P, P, P, f, P, P, P, P, P, P, sz, P]
             L.msa_fused_bwd_kl.argtypes = [S, P, P, P, P, P, P, P, P, P, P, f, P, P, P, P, P, P, P, P, sz, P]
             L.msa_train_step.argtypes = [S, P, P, P, P, P, P, f, P, P, P, P, P, P, P, P, P, P, P, P, sz, P]
+            L.msa_train_step_staged.argtypes = [S, P, P, P, P, P, P, f, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P,
+                                                sz, P]
             L.msa_check_device_status.argtypes = [P, P]
             L.msa_block_mask.argtypes = [S, P, P, P, P, P]
             for fn in ("msa_index_select", "msa_sparse_attn_fwd", "msa_kl_fwd", "msa_fused_bwd", "msa_fused_bwd_kl",
-                       "msa_train_step", "msa_check_device_status", "msa_block_mask"):
+                       "msa_train_step", "msa_train_step_staged", "msa_check_device_status", "msa_block_mask"):
                 getattr(L, fn).restype = ctypes.c_int
             L.msa_last_error.restype = ctypes.c_char_p
             L.msa_version.restype = ctypes.c_char_p
@@ -250,10 +252,13 @@ def fused_bwd(shape: Shape, q, k, v, o, d_o, lse, q_idx, k_idx, sel_idx, lse_idx
 
 
 def train_step(shape: Shape, q, k, v, q_idx, k_idx, d_o, kl_coef: float = 1.0, *, out=None, workspace=None,
-               stream=None):
+               stream=None, input_ready=None):
     """msa_train_step: selection, forward, lse_idx, fused backward with the KL loss in one call.
     Returns a dict with sel, o, lse, lse_idx, kl_rows, kl_loss, dq, dk, dv, dq_idx, dk_idx
-    (pass `out`, a dict of preallocated tensors with those keys, to reuse buffers)."""
+    (pass `out`, a dict of preallocated tensors with those keys, to reuse buffers).
+    input_ready: three torch.cuda.Events (or None each), recorded after the writes
+    of (q_idx, k_idx), (q, k, v) and d_o: msa_train_step_staged, whose stream waits
+    on each just before the first phase reading those inputs."""
     s = shape
     for t, n, shp in ((q, "q", (s.B, s.Nq, s.Hq, s.d)), (d_o, "d_o", (s.B, s.Nq, s.Hq, s.d)),
                       (k, "k", (s.B, s.Nk, s.Hkv, s.d)), (v, "v", (s.B, s.Nk, s.Hkv, s.d)),
@@ -269,11 +274,15 @@ def train_step(shape: Shape, q, k, v, q_idx, k_idx, d_o, kl_coef: float = 1.0, *
                "dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v),
                "dq_idx": torch.empty_like(q_idx), "dk_idx": torch.empty_like(k_idx)}
     ws = _ws(workspace, s, OP_TRAIN_STEP, dev)
-    _check(lib().msa_train_step(ctypes.byref(s.c()), _ptr(q), _ptr(k), _ptr(v), _ptr(q_idx), _ptr(k_idx), _ptr(d_o),
-                                ctypes.c_float(kl_coef), _ptr(out["sel"]), _ptr(out["o"]), _ptr(out["lse"]),
-                                _ptr(out["lse_idx"]), _ptr(out.get("kl_rows")), _ptr(out["kl_loss"]), _ptr(out["dq"]),
-                                _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dq_idx"]), _ptr(out["dk_idx"]), _ptr(ws),
-                                ws.numel(), _stream(stream)))
+    args = [ctypes.byref(s.c()), _ptr(q), _ptr(k), _ptr(v), _ptr(q_idx), _ptr(k_idx), _ptr(d_o),
+            ctypes.c_float(kl_coef), _ptr(out["sel"]), _ptr(out["o"]), _ptr(out["lse"]), _ptr(out["lse_idx"]),
+            _ptr(out.get("kl_rows")), _ptr(out["kl_loss"]), _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]),
+            _ptr(out["dq_idx"]), _ptr(out["dk_idx"])]
+    if input_ready is None:
+        _check(lib().msa_train_step(*args, _ptr(ws), ws.numel(), _stream(stream)))
+    else:
+        evs = [None if ev is None else ctypes.c_void_p(ev.cuda_event) for ev in input_ready]
+        _check(lib().msa_train_step_staged(*args, *evs, _ptr(ws), ws.numel(), _stream(stream)))
     return out
 
 

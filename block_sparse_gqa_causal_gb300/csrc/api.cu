@@ -534,10 +534,17 @@ msa_status msa_fused_bwd_kl(const msa_shape *shape, const void *q, const void *k
                           dk_idx, true, kl_rows, kl_loss, workspace, workspace_bytes, stream);
 }
 
-msa_status msa_train_step(const msa_shape *shape, const void *q, const void *k, const void *v, const void *q_idx,
-                          const void *k_idx, const void *d_o, float kl_coef, int32_t *sel_idx, void *o, float *lse,
-                          float *lse_idx, float *kl_rows, float *kl_loss, void *dq, void *dk, void *dv, void *dq_idx,
-                          void *dk_idx, void *workspace, size_t workspace_bytes, void *stream)
+}  // extern "C"
+
+namespace {
+// The training step; ev_idx / ev_qkv / ev_do (nullable) are events the stream
+// waits on just before the first work that reads q_idx and k_idx / q, k and v
+// / d_o, so inputs still being copied in can overlap the earlier phases.
+msa_status train_step_impl(const msa_shape *shape, const void *q, const void *k, const void *v, const void *q_idx,
+                           const void *k_idx, const void *d_o, float kl_coef, int32_t *sel_idx, void *o, float *lse,
+                           float *lse_idx, float *kl_rows, float *kl_loss, void *dq, void *dk, void *dv, void *dq_idx,
+                           void *dk_idx, cudaEvent_t ev_idx, cudaEvent_t ev_qkv, cudaEvent_t ev_do, void *workspace,
+                           size_t workspace_bytes, void *stream)
 {
     Problem p;
     msa_status st = make_problem(shape, p);
@@ -562,15 +569,20 @@ msa_status msa_train_step(const msa_shape *shape, const void *q, const void *k, 
     st = check_ws(workspace, workspace_bytes, kStatusBytes + train_bytes(p));
     if (st != MSA_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    auto wait = [&](cudaEvent_t ev) { return ev ? cudaStreamWaitEvent(s, ev, 0) : cudaSuccess; };
+    cudaError_t e;
     if (!train_shared_index(p)) {
         // the four phases in turn, each carving the same workspace
+        if ((e = wait(ev_idx)) != cudaSuccess) return cuda_fail(e, "train_step: waiting for q_idx, k_idx");
         if ((st = msa_index_select(shape, q_idx, k_idx, sel_idx, nullptr, workspace, workspace_bytes, stream)) != MSA_OK)
             return st;
+        if ((e = wait(ev_qkv)) != cudaSuccess) return cuda_fail(e, "train_step: waiting for q, k, v");
         if ((st = msa_sparse_attn_fwd(shape, q, k, v, sel_idx, o, lse, workspace, workspace_bytes, stream)) != MSA_OK)
             return st;
         if ((st = msa_kl_fwd(shape, q, k, q_idx, k_idx, sel_idx, lse, kl_coef, lse_idx, nullptr, nullptr, workspace,
                              workspace_bytes, stream)) != MSA_OK)
             return st;
+        if ((e = wait(ev_do)) != cudaSuccess) return cuda_fail(e, "train_step: waiting for d_o");
         return msa_fused_bwd_kl(shape, q, k, v, o, d_o, lse, q_idx, k_idx, sel_idx, lse_idx, kl_coef, dq, dk, dv, dq_idx,
                                 dk_idx, kl_rows, kl_loss, workspace, workspace_bytes, stream);
     }
@@ -605,13 +617,16 @@ msa_status msa_train_step(const msa_shape *shape, const void *q, const void *k, 
     fw.index_ready = kw.index_ready = w.index_ready = true;
     fw.d_o = static_cast<const bf16 *>(d_o);           // the forward combine leaves D for the backward
     fw.D = w.D;
+    fw.d_o_ready = ev_do;
     w.D_ready = true;
     const bf16 *bq = static_cast<const bf16 *>(q), *bk = static_cast<const bf16 *>(k), *bv = static_cast<const bf16 *>(v);
     const bf16 *bqi = static_cast<const bf16 *>(q_idx), *bki = static_cast<const bf16 *>(k_idx);
-    cudaError_t e = launch_index_select(p, bqi, bki, nullptr, bs_scratch, sel_idx, ds, s);
+    if ((e = wait(ev_idx)) != cudaSuccess) return cuda_fail(e, "train_step: waiting for q_idx, k_idx");
+    e = launch_index_select(p, bqi, bki, nullptr, bs_scratch, sel_idx, ds, s);
     if (e != cudaSuccess) return cuda_fail(e, "train_step: selection");
     if ((e = launch_inverse_index(p, sel_idx, w.bucket_cnt, w.bucket_off, w.bucket_scratch, w.bucket_q, ds, s)) != cudaSuccess)
         return cuda_fail(e, "train_step: inverse index");
+    if ((e = wait(ev_qkv)) != cudaSuccess) return cuda_fail(e, "train_step: waiting for q, k, v");
     if ((e = launch_sparse_fwd_keymajor(p, bq, bk, bv, sel_idx, static_cast<bf16 *>(o), lse, fw, ds, s)) != cudaSuccess)
         return cuda_fail(e, "train_step: forward");
     if ((e = launch_kl_keymajor(p, bq, bk, bqi, bki, sel_idx, lse, lse_idx, nullptr, kw, ds, s)) != cudaSuccess)
@@ -623,6 +638,30 @@ msa_status msa_train_step(const msa_shape *shape, const void *q, const void *k, 
         return cuda_fail(e, "train_step: backward");
     if ((e = launch_kl_reduce(p, rows_kl, kl_coef, kl_loss, s)) != cudaSuccess) return cuda_fail(e, "train_step: loss");
     return MSA_OK;
+}
+}  // namespace
+
+extern "C" {
+
+msa_status msa_train_step(const msa_shape *shape, const void *q, const void *k, const void *v, const void *q_idx,
+                          const void *k_idx, const void *d_o, float kl_coef, int32_t *sel_idx, void *o, float *lse,
+                          float *lse_idx, float *kl_rows, float *kl_loss, void *dq, void *dk, void *dv, void *dq_idx,
+                          void *dk_idx, void *workspace, size_t workspace_bytes, void *stream)
+{
+    return train_step_impl(shape, q, k, v, q_idx, k_idx, d_o, kl_coef, sel_idx, o, lse, lse_idx, kl_rows, kl_loss, dq,
+                           dk, dv, dq_idx, dk_idx, nullptr, nullptr, nullptr, workspace, workspace_bytes, stream);
+}
+
+msa_status msa_train_step_staged(const msa_shape *shape, const void *q, const void *k, const void *v,
+                                 const void *q_idx, const void *k_idx, const void *d_o, float kl_coef, int32_t *sel_idx,
+                                 void *o, float *lse, float *lse_idx, float *kl_rows, float *kl_loss, void *dq,
+                                 void *dk, void *dv, void *dq_idx, void *dk_idx, void *idx_ready, void *qkv_ready,
+                                 void *do_ready, void *workspace, size_t workspace_bytes, void *stream)
+{
+    return train_step_impl(shape, q, k, v, q_idx, k_idx, d_o, kl_coef, sel_idx, o, lse, lse_idx, kl_rows, kl_loss, dq,
+                           dk, dv, dq_idx, dk_idx, static_cast<cudaEvent_t>(idx_ready),
+                           static_cast<cudaEvent_t>(qkv_ready), static_cast<cudaEvent_t>(do_ready), workspace,
+                           workspace_bytes, stream);
 }
 
 msa_status msa_check_device_status(void *workspace, void *stream)

@@ -84,6 +84,7 @@ struct FwdWork {
     // D[b, h, i] = sum_e dO * O (O as written, bf16) -- one pass over O fewer
     const bf16 *d_o = nullptr;
     float *D = nullptr;
+    cudaEvent_t d_o_ready = nullptr;   // the combine waits on it before reading d_o (nullable)
 };
 cudaError_t launch_sparse_fwd_keymajor(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *v,
                                        const int32_t *sel, bf16 *o, float *lse, const FwdWork &w, DeviceStatus *st,

@@ -607,6 +607,7 @@ cudaError_t launch_sparse_fwd_keymajor(const Problem &p, const bf16 *q, const bf
     e = p.d == 128 ? launch_d<128>(p, q, k, v, sel, w, st, s) : launch_d<64>(p, q, k, v, sel, w, st, s);
     if (e != cudaSuccess) return e;
     const long long rows = (long long)p.B * p.Nq * p.Hq;
+    if (w.d_o && w.d_o_ready && (e = cudaStreamWaitEvent(s, w.d_o_ready, 0)) != cudaSuccess) return e;
     if (p.d == 128)
         {
             TimedLaunch timed_("sparse_fwd_combine_kernel", s);

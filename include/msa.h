@@ -190,6 +190,24 @@ msa_status msa_train_step(const msa_shape *shape, const void *q, const void *k, 
                           void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * msa_train_step with its inputs still arriving: idx_ready, qkv_ready and
+ * do_ready are CUDA events (cudaEvent_t, each may be NULL) recorded after the
+ * writes of q_idx and k_idx, of q, k and v, and of d_o (for instance the
+ * host-to-device copies of this step's inputs on another stream).  The call
+ * makes its stream wait on each just before the first work that reads those
+ * tensors -- the selection, the forward, and the forward's combine (which
+ * reads d_o on the key-major path) or the backward -- so a copy of the later
+ * inputs overlaps the earlier phases.  Results are those of msa_train_step.
+ * The events must stay valid until the stream has passed those points.
+ */
+msa_status msa_train_step_staged(const msa_shape *shape, const void *q, const void *k, const void *v,
+                                 const void *q_idx, const void *k_idx, const void *d_o, float kl_coef,
+                                 int32_t *sel_idx, void *o, float *lse, float *lse_idx, float *kl_rows,
+                                 float *kl_loss, void *dq, void *dk, void *dv, void *dq_idx, void *dk_idx,
+                                 void *idx_ready, void *qkv_ready, void *do_ready,
+                                 void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Index selection without any allocation, for callers that cannot allocate
  * device memory (a serving process whose memory pool is frozen after
  * warm-up, or a plugin given only raw device pointers).  There is no

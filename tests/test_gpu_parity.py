@@ -291,3 +291,35 @@ def test_results_do_not_depend_on_workspace_contents(case):
         torch.cuda.synchronize()
         for n, g, ref in zip(("dq", "dk", "dv", "dq_idx", "dk_idx"), grads, res["grads"]):
             assert_close(bf16_to_np(g), ref, n + " (fused_bwd, dirty workspace)", rel_l2=1e-3, bf16_out=True)
+
+
+@pytest.mark.parametrize("case", [c for c in TRAIN_CASES if c[0] in ("g8_d128_b2_ragged", "g4_d64_ragged")],
+                         ids=lambda c: c[0])
+def test_train_step_staged_matches_train_step(case):
+    """msa_train_step_staged with its inputs copied in from pinned host memory
+    on another stream (events after q_idx/k_idx, q/k/v and d_o) gives what
+    msa_train_step gives on resident inputs."""
+    import torch
+    from block_sparse_gqa_causal_gb300 import api
+    x, osh, res = run_case(case)
+    name, B, Nq, Nk, qo, Hq, Hkv, d, di, k = case
+    sh = api.Shape(B=B, Nq=Nq, Nk=Nk, Hq=Hq, Hkv=Hkv, d=d, d_idx=di, topk=k, q_offset=qo)
+    host = {n: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory() for n, a in x.items()}
+    dev = {n: torch.empty(t.shape, dtype=t.dtype, device="cuda") for n, t in host.items()}
+    side = torch.cuda.Stream()
+    evs = [torch.cuda.Event() for _ in range(3)]
+    with torch.cuda.stream(side):
+        for gi, grp in enumerate((("q_idx", "k_idx"), ("q", "k", "v"), ("d_o",))):
+            for n in grp:
+                dev[n].copy_(host[n], non_blocking=True)
+            evs[gi].record(side)
+    ts = api.train_step(sh, dev["q"], dev["k"], dev["v"], dev["q_idx"], dev["k_idx"], dev["d_o"], 0.75,
+                        input_ready=tuple(evs))
+    torch.cuda.synchronize()
+    want = res["train_step"]
+    for n in ("sel", "o", "lse", "lse_idx"):
+        got = bf16_to_np(ts[n]) if ts[n].dtype == torch.bfloat16 else ts[n].cpu().numpy()
+        assert np.array_equal(got, want[n]), n
+    assert_close(ts["kl_rows"].cpu().numpy(), want["kl_rows"], "kl_rows (staged)", max_abs=1e-5, rel_l2=1e-6)
+    for n in ("dq", "dk", "dv", "dq_idx", "dk_idx"):
+        assert_close(bf16_to_np(ts[n]), want[n], n + " (staged)", rel_l2=1e-3, bf16_out=True)
