@@ -574,6 +574,50 @@ def run_decode(args, w, world, rank, local):
     launches = api.launch_count() - l0
     clk = clocks.stop()
     ms = max_over_ranks(a.elapsed_time(b), world, dev)
+
+    # ---- end to end: every step's new-token inputs (q, q_idx, and the k, v, k_idx
+    # rows appended to the caches) come from pinned host memory in one copy, and
+    # the attention output goes back to pinned host memory
+    e2e = None
+    if not args.no_e2e:
+        parts = [("q", (w.B, 1, w.Hq, w.d)), ("q_idx", (w.B, 1, w.Hkv, w.d_idx)), ("k", (w.B, w.Hkv, w.d)),
+                 ("v", (w.B, w.Hkv, w.d)), ("k_idx", (w.B, w.d_idx))]
+        sizes = [int(np.prod(shp)) for _, shp in parts]
+        offs = np.concatenate([[0], np.cumsum(sizes)])
+        total = int(offs[-1])
+        host = torch.empty((steps, total), dtype=torch.bfloat16).pin_memory()
+        for s in range(steps):
+            src = [q_s[s], qi_s[s], new_k[:, s], new_v[:, s], new_ki[:, s]]
+            host[s].copy_(torch.cat([t.reshape(-1).cpu() for t in src]))
+        staging = torch.empty(total, dtype=torch.bfloat16, device=dev)
+        view = {n: staging[offs[x]:offs[x + 1]].view(shp) for x, (n, shp) in enumerate(parts)}
+        o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+
+        def e2e_step(s):
+            pos = decode_position(w, s)
+            staging.copy_(host[s], non_blocking=True)
+            k[:, pos].copy_(view["k"])
+            v[:, pos].copy_(view["v"])
+            ki[:, pos].copy_(view["k_idx"])
+            api.index_select(shapes[s], view["q_idx"], ki, sel_idx=sel, workspace=ws_sel)
+            api.sparse_attn_fwd(shapes[s], view["q"], k, v, sel, o=o, lse=lse, workspace=ws_fwd)
+            o_host.copy_(o, non_blocking=True)
+
+        for s in range(min(args.warmup, steps)):
+            e2e_step(s)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        a2, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a2.record(stream)
+        for s in range(steps):
+            e2e_step(s)
+        b2.record(stream)
+        torch.cuda.synchronize(dev)
+        ms2 = max_over_ranks(a2.elapsed_time(b2), world, dev)
+        e2e = {"value": round(world * w.B * steps / (ms2 * 1e-3), 1), "unit": "tokens/s",
+               "ms_per_step": round(ms2 / steps, 4), "h2d_bytes_per_step": total * 2,
+               "d2h_bytes_per_step": o.numel() * o.element_size(),
+               "overlap": "none: each step's copy in, selection, attention and copy out in stream order"}
     flops, byts = decode_flops_bytes(w, [decode_position(w, s) for s in range(steps)])
     peaks = load_peaks()
     gbs = byts / (ms * 1e-3) / 1e9
@@ -590,7 +634,7 @@ def run_decode(args, w, world, rank, local):
             "roofline": {"kernel": "decode step (index scan dominant)", "bound": "hbm", "achieved": round(gbs, 1),
                          "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
                          "peak_source": peaks["source"] + " copy bandwidth", "traffic": None},
-            "gpu_launches": int(launches), "clocks": clk, "impl": "ours"}), flush=True)
+            "e2e": e2e, "gpu_launches": int(launches), "clocks": clk, "impl": "ours"}), flush=True)
 
 
 def run_reference(args, w, world, rank):
