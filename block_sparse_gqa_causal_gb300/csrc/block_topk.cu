@@ -8,7 +8,8 @@
 // lane, coalesced loads all in flight).  Per segment, a conservative cutoff
 // (section 4.2 of the same page: the k-th largest of a subset of at least k
 // elements never exceeds the global k-th largest) is the (k-1)-th largest of
-// the 32 lane maxima; only scores at or above it, and above the current
+// the 32 lane maxima (for k > 17: of each lane's two largest scores); only
+// scores at or above it, and above the current
 // (k-1)-th best, survive.  Survivors become 64-bit keys
 //   (order-preserving bits of the fp32 score) << 32 | (0xFFFFFFFF - c),
 // so one unsigned compare ranks by score then by lower index; they are
@@ -35,6 +36,17 @@ __device__ __forceinline__ float sort_desc_f(float v, int lane)
             const bool lower = (lane & stride) == 0;
             v = (lower == desc) ? fmaxf(v, o) : fminf(v, o);
         }
+    }
+    return v;
+}
+
+// a bitonic sequence of floats across the lanes -> descending order
+__device__ __forceinline__ float merge_desc_f(float v, int lane)
+{
+#pragma unroll
+    for (int stride = 16; stride > 0; stride >>= 1) {
+        const float o = __shfl_xor_sync(0xffffffffu, v, stride);
+        v = ((lane & stride) == 0) ? fmaxf(v, o) : fminf(v, o);
     }
     return v;
 }
@@ -74,10 +86,24 @@ __device__ __forceinline__ void warp_topk(const float *__restrict__ src, int c0,
             const int c = base + j * 32 + lane;
             v[j] = c < c0 ? __ldg(src + c) : -INFINITY;
         }
-        float lmax = v[0];
+        // the lane's two largest scores (of 16 distinct positions)
+        float lmax = v[0], l2 = -INFINITY;
 #pragma unroll
-        for (int j = 1; j < kR; ++j) lmax = fmaxf(lmax, v[j]);
-        const float tau = __shfl_sync(0xffffffffu, sort_desc_f(lmax, lane), K1 - 1);
+        for (int j = 1; j < kR; ++j) {
+            l2 = fmaxf(l2, fminf(lmax, v[j]));
+            lmax = fmaxf(lmax, v[j]);
+        }
+        float tau;
+        if (K1 <= 16) {
+            tau = __shfl_sync(0xffffffffu, sort_desc_f(lmax, lane), K1 - 1);
+        } else {
+            // larger k: the (k-1)-th largest of the 64 values formed by each lane's two
+            // largest (still a subset of the segment, so still a valid cutoff, but far
+            // tighter than the (k-1)-th of the 32 lane maxima when k-1 nears 32)
+            const float a = sort_desc_f(lmax, lane), c = sort_desc_f(l2, lane);
+            const float top = merge_desc_f(fmaxf(a, __shfl_sync(0xffffffffu, c, 31 - lane)), lane);
+            tau = __shfl_sync(0xffffffffu, top, K1 - 1);
+        }
         const unsigned long long kth = shfl64(best, K1 - 1);
         const float t_run = kth ? key_value(kth) : -INFINITY;
         // survivors: >= the segment cutoff and strictly above the running

@@ -323,3 +323,34 @@ def test_train_step_staged_matches_train_step(case):
     assert_close(ts["kl_rows"].cpu().numpy(), want["kl_rows"], "kl_rows (staged)", max_abs=1e-5, rel_l2=1e-6)
     for n in ("dq", "dk", "dv", "dq_idx", "dk_idx"):
         assert_close(bf16_to_np(ts[n]), want[n], n + " (staged)", rel_l2=1e-3, bf16_out=True)
+
+
+@pytest.mark.parametrize("k", [17, 24, 32])
+def test_index_select_large_k_parity(k):
+    """k above 16 takes the selection over stored block scores (`block_topk`:
+    segments of 512 scores, a cutoff from the lane maxima, survivors sorted
+    and merged): the same selection as the oracle's full sort.  Prefill rows
+    and a decode-like row with a long cache, where a CTA takes the row."""
+    import torch
+    from block_sparse_gqa_causal_gb300 import api
+    from block_sparse_gqa_causal_gb300.inputs import f32_to_bf16_bits
+    rng = np.random.default_rng(k)
+    bf = lambda shape: f32_to_bf16_bits(rng.standard_normal(shape).astype(np.float32))
+    for B, Nq, Nk, qo, Hkv in ((1, 4000, 4000, 0, 2), (2, 1, 300000, 299999, 2)):
+        qi, ki = bf((B, Nq, Hkv, 64)), bf((B, Nk, 64))
+        sh = api.Shape(B=B, Nq=Nq, Nk=Nk, Hq=Hkv, Hkv=Hkv, d=64, d_idx=64, topk=k, q_offset=qo)
+        sel = api.index_select(sh, to_torch(qi), to_torch(ki))
+        torch.cuda.synchronize()
+        osh = oracle.Shape(B=B, Nq=Nq, Nk=Nk, Hq=Hkv, Hkv=Hkv, d=64, d_idx=64, topk=k, q_offset=qo)
+        n = B * Nq
+        rows = np.arange(n) if n <= 64 else np.unique(np.concatenate(
+            [np.arange(0, n, 97), [n - 1, 2047, 2048, 2177], rng.choice(n, 40, replace=False)]))
+        bs_o = oracle.block_scores(osh, qi, ki, rows)
+        sel_o = oracle.select(osh, bs_o, rows)
+        sel_np = sel.cpu().numpy()
+        sel_g = np.stack([sel_np[row // Nq, :, row % Nq, :] for row in rows])
+        exact, tol = check_selection(k, 128, qo, Nq, rows, sel_g, sel_o, bs_o)
+        # near-ties (validated row by row above) grow with k: neighbouring order
+        # statistics of ~30 block scores are ~0.03 apart, so a few percent of
+        # rows fall within the 1e-3 gap
+        assert tol <= 0.1 * (exact + tol) + 2
