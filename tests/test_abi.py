@@ -103,6 +103,27 @@ def test_bwd_rejects_non_training_layout(libmsa):
     assert rc == 2
 
 
+def test_train_step_staged_rejects_bad_arguments_before_any_launch(libmsa):
+    """The staged training step validates like msa_train_step: a non-training
+    layout, a NULL input and a short workspace are refused on the host (the
+    event pointers are never touched on these paths)."""
+    from block_sparse_gqa_causal_gb300 import api
+    g = ctypes.c_void_p(1 << 20)
+    ev = ctypes.c_void_p(1 << 12)
+    f = ctypes.c_float(1.0)
+    chunked = api.Shape(B=1, Nq=3, Nk=256, Hq=8, Hkv=2, d=64, d_idx=64, topk=4, q_offset=253)
+    rc = libmsa.msa_train_step_staged(ctypes.byref(chunked.c()), g, g, g, g, g, g, f, g, g, g, g, None, g, g, g, g, g,
+                                      g, ev, ev, ev, g, 1 << 30, None)
+    assert rc == 2 and b"train_step" in libmsa.msa_last_error()
+    sh = api.Shape(B=1, Nq=256, Nk=256, Hq=8, Hkv=2, d=64, d_idx=64, topk=4)
+    rc = libmsa.msa_train_step_staged(ctypes.byref(sh.c()), None, g, g, g, g, g, f, g, g, g, g, None, g, g, g, g, g,
+                                      g, ev, ev, ev, g, 1 << 30, None)
+    assert rc == 1 and b"q is NULL" in libmsa.msa_last_error()
+    rc = libmsa.msa_train_step_staged(ctypes.byref(sh.c()), g, g, g, g, g, g, f, g, g, g, g, None, g, g, g, g, g,
+                                      g, None, None, None, g, 256, None)
+    assert rc == 3
+
+
 def test_product_path_has_no_oracle_or_fallback():
     """The library binding never imports the oracle and has no CPU path."""
     pkg = os.path.join(ROOT, "block_sparse_gqa_causal_gb300")
