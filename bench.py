@@ -67,44 +67,59 @@ def useful_flops(w, positions=None):
 
 
 def kernel_work(w):
-    """Algorithmic work of one launch of each library kernel that can
-    dominate a step, closed forms over the selected work: {"flops": F,
-    "bytes": B}, either may be None.  Bytes count what the algorithm must
-    move through HBM once: per selected (query, group, block) slot the rows a
-    key-major kernel gathers and the partial rows it writes, per (group,
-    block) bucket the K/V-side tiles it reads and writes."""
+    """Work of one launch of each library kernel that can dominate a step,
+    closed forms over the selected work: {"flops": F, "bytes": B,
+    "design_bytes": D}, any of them may be None.
+
+    "bytes" is the algorithmic traffic: every tensor the step that the kernel
+    computes must read, read once, and every tensor it produces, written once
+    (for the main backward: Q, dO, K, V, LSE, D and the selection in; dQ, dK,
+    dV out).  The roofline's binding side is chosen from these and the FLOPs.
+    "design_bytes" is this design's own traffic: per selected (query, group,
+    block) slot the rows a key-major kernel gathers and the partial rows it
+    writes, per (group, block) bucket the K/V-side tiles; what it moves above
+    "bytes" is the price of grouping the work by key block."""
     pos = np.arange(w.N, dtype=np.int64)
     T = tokens_per_row(w, pos).astype(np.float64)
     nsel = np.minimum(w.topk, pos // w.block + 1).astype(np.float64)     # valid selected blocks per row
     vis_blocks = (pos // w.block + 1).astype(np.float64)
-    B, G, d, di = w.B, w.G, w.d, w.d_idx
-    slots = B * w.Hkv * float(np.sum(nsel))                              # (query, group, block) slots
-    buckets = B * w.Hkv * float(w.nb)                                    # (group, block) buckets
+    B, G, d, di, N, Hq, Hkv = w.B, w.G, w.d, w.d_idx, w.N, w.Hq, w.Hkv
+    slots = B * Hkv * float(np.sum(nsel))                                # (query, group, block) slots
+    buckets = B * Hkv * float(w.nb)                                      # (group, block) buckets
+    # unique tensors, bytes
+    q_b = B * N * Hq * d * 2.0                                           # q, o, d_o, dq
+    kv_b = B * N * Hkv * d * 2.0                                         # k, v, dk, dv
+    qi_b = B * N * Hkv * di * 2.0                                        # q_idx, dq_idx
+    ki_b = B * N * di * 2.0                                              # k_idx, dk_idx
+    sel_b = B * Hkv * N * w.topk * 4.0
+    lse_b = B * Hq * N * 4.0                                             # lse, D
+    row_b = B * Hkv * N * 4.0                                            # lse_idx, kl_rows
     return {
-        "index_scores_tc_kernel": {"flops": B * float(np.sum(2.0 * di * (pos + 1) * w.Hkv)), "bytes": None},
-        # Q rows gathered, bf16 partial row + (m, z) written per slot; K, V per bucket
-        "sparse_fwd_tc_kernel": {"flops": B * float(np.sum(4.0 * d * T * w.Hq)),
-                                 "bytes": slots * (G * d * 2.0 + G * d * 2.0 + G * 8.0) + buckets * 2 * 128 * d * 2.0},
-        "kl_index_tc_kernel": {"flops": B * float(np.sum(2.0 * di * T * w.Hkv)),
-                               "bytes": slots * (di * 2.0 + 4.0 + 32.0) + buckets * 128 * di * 2.0},
-        # Q and dO rows gathered, dQ partial row + teacher row written, LSE and D read
-        # per slot; K, V read and dK, dV written per bucket
-        "bwd_main_tc_kernel": {"flops": B * float(np.sum(10.0 * d * T * w.Hq)),
-                               "bytes": slots * (2 * G * d * 2.0 + G * d * 2.0 + 128 * 2.0 + G * 8.0)
+        "index_scores_tc_kernel": {"flops": B * float(np.sum(2.0 * di * (pos + 1) * Hkv)),
+                                   "bytes": qi_b + ki_b + sel_b, "design_bytes": None},
+        "sparse_fwd_tc_kernel": {"flops": B * float(np.sum(4.0 * d * T * Hq)),
+                                 "bytes": q_b + 2 * kv_b + sel_b + q_b + lse_b,
+                                 "design_bytes": slots * (G * d * 2.0 + G * d * 2.0 + G * 8.0)
+                                 + buckets * 2 * 128 * d * 2.0},
+        "kl_index_tc_kernel": {"flops": B * float(np.sum(2.0 * di * T * Hkv)),
+                               "bytes": qi_b + ki_b + sel_b + row_b,
+                               "design_bytes": slots * (di * 2.0 + 4.0 + 32.0) + buckets * 128 * di * 2.0},
+        "bwd_main_tc_kernel": {"flops": B * float(np.sum(10.0 * d * T * Hq)),
+                               "bytes": 2 * q_b + 2 * kv_b + 2 * lse_b + sel_b + q_b + 2 * kv_b,
+                               "design_bytes": slots * (2 * G * d * 2.0 + G * d * 2.0 + 128 * 2.0 + G * 8.0)
                                + buckets * 4 * 128 * d * 2.0},
-        # q_idx row gathered, teacher row read, dq_idx partial row written per slot;
-        # K_idx read and dK_idx added (fp32) per bucket
-        "bwd_index_tc_kernel": {"flops": B * float(np.sum(6.0 * di * T * w.Hkv)),
-                                "bytes": slots * (di * 2.0 + 128 * 2.0 + di * 2.0 + 4.0)
+        "bwd_index_tc_kernel": {"flops": B * float(np.sum(6.0 * di * T * Hkv)),
+                                "bytes": qi_b + ki_b + row_b + sel_b + qi_b + ki_b,
+                                "design_bytes": slots * (di * 2.0 + 128 * 2.0 + di * 2.0 + 4.0)
                                 + buckets * 128 * di * (2.0 + 8.0)},
-        # block scores of the visible blocks in, indices out
-        "block_topk_kernel": {"flops": None, "bytes": B * w.Hkv * float(np.sum(vis_blocks * 4.0 + w.topk * 4.0))},
-        # bf16 partial rows + (m, z) per valid slot in, bf16 row + lse out
-        "sparse_fwd_combine_kernel": {"flops": None,
-                                      "bytes": B * w.Hq * float(np.sum(nsel * (2.0 * d + 8.0) + 2.0 * d + 4.0))},
-        # dQ and dq_idx: bf16 partial rows per valid slot in, one bf16 row out
-        "bwd_combine_kernel": {"flops": None,
-                               "bytes": B * float(np.sum((nsel + 1.0) * 2.0 * (d * w.Hq + di * w.Hkv)))},
+        # block scores of the visible blocks in, indices out (the top-k step itself)
+        "block_topk_kernel": {"flops": None, "bytes": B * Hkv * float(np.sum(vis_blocks * 4.0 + w.topk * 4.0)),
+                              "design_bytes": None},
+        # the combines exist only because of the key-major design: no algorithmic traffic of their own
+        "sparse_fwd_combine_kernel": {"flops": None, "bytes": None,
+                                      "design_bytes": B * Hq * float(np.sum(nsel * (2.0 * d + 8.0) + 2.0 * d + 4.0))},
+        "bwd_combine_kernel": {"flops": None, "bytes": None,
+                               "design_bytes": B * float(np.sum((nsel + 1.0) * 2.0 * (d * Hq + di * Hkv)))},
     }
 
 
@@ -131,6 +146,95 @@ def kernel_traffic(kernel, w):
     pos = np.arange(w.N, dtype=np.int64)
     slots = w.B * w.Hkv * float(np.sum(np.minimum(w.topk, pos // w.block + 1)))   # (query, group, block) entries
     return round(per_unit * slots)
+
+
+def kernel_roofline(kernel, ktimes, work, peaks, w):
+    """Roofline of one kernel over the timed steps: achieved = algorithmic
+    FLOPs (or bytes) per launch / mean launch time (CUDA events on the
+    launch's stream); the binding side is the one whose algorithmic work takes
+    longer at the measured peak (bf16 burst for FLOPs, the copy rate for
+    bytes).  `traffic` is the measured DRAM bytes per launch (ncu, scaled),
+    `waste_ratio` = traffic / algorithmic bytes."""
+    n_l, tot_ms = ktimes[kernel]
+    per_launch_ms = tot_ms / n_l
+    wk = work.get(kernel)
+    if wk is None or (not wk["flops"] and not wk["bytes"]):
+        return {"kernel": kernel, "bound": None, "achieved": None, "peak": None, "unit": None, "frac": None,
+                "traffic": None, "launch_ms": round(per_launch_ms, 3)}
+    fl, by = wk["flops"], wk["bytes"]
+    sides = {}
+    if fl:
+        ach_t = fl / (per_launch_ms * 1e-3) / 1e12
+        sides["tensor"] = {"achieved": round(ach_t, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                           "frac": round(ach_t / peaks["bf16_tflops"], 4),
+                           "frac_of_sustained": round(ach_t / peaks["bf16_tflops_sustained"], 4),
+                           "peak_source": peaks["source"] + " burst bf16", "algorithmic_per_launch": fl}
+    if by:
+        ach_h = by / (per_launch_ms * 1e-3) / 1e9
+        sides["hbm"] = {"achieved": round(ach_h, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": round(ach_h / peaks["hbm_gbs"], 4), "peak_source": peaks["source"] + " copy",
+                        "algorithmic_per_launch": by}
+    t_tensor = fl / (peaks["bf16_tflops"] * 1e12) if fl else 0.0
+    t_hbm = by / (peaks["hbm_gbs"] * 1e9) if by else 0.0
+    bound = "hbm" if t_hbm > t_tensor else "tensor"
+    other = "tensor" if bound == "hbm" else "hbm"
+    traffic = kernel_traffic(kernel, w)
+    out = {"kernel": kernel, "bound": bound, **sides[bound], "traffic": traffic,
+           "launch_ms": round(per_launch_ms, 3)}
+    if other in sides:
+        out[other] = sides[other]
+    if wk.get("design_bytes"):
+        out["design_bytes_per_launch"] = wk["design_bytes"]
+    if traffic and by:
+        out["waste_ratio"] = round(traffic / by, 2)
+    return out
+
+
+def target_report(w, ktimes, work, peaks, phase_ms, phase_flops, steps):
+    """The two stated targets, on this step's own work: the sparse-attention
+    forward at N = 131072 (>= 50% of the dense bf16 peak on useful FLOPs) and
+    the selection phase (>= 60% of the copy peak, or no HBM phase at all)."""
+    out = {}
+    if w.N == 131072:
+        fwd_ms = phase_ms.get("sparse_attn_fwd", 0.0)
+        tf = phase_flops["sparse_attn_fwd"] / (fwd_ms * 1e-3) / 1e12 if fwd_ms else None
+        kern = ktimes.get("sparse_fwd_tc_kernel")
+        ktf = phase_flops["sparse_attn_fwd"] / (kern[1] / steps * 1e-3) / 1e12 if kern else None
+        out["sparse_fwd_n131072"] = {
+            "useful_tflop": round(phase_flops["sparse_attn_fwd"] / 1e12, 4), "target_frac": 0.5,
+            "phase_ms": round(fwd_ms, 3), "phase_tflops": round(tf, 2) if tf else None,
+            "phase_frac": round(tf / peaks["bf16_tflops"], 4) if tf else None,
+            "kernel_tflops": round(ktf, 2) if ktf else None,
+            "kernel_frac": round(ktf / peaks["bf16_tflops"], 4) if ktf else None,
+            "met": bool(tf and tf / peaks["bf16_tflops"] >= 0.5),
+            "phase": "inverse index + sparse_fwd_tc_kernel + sparse_fwd_combine_kernel"}
+    topk = ktimes.get("block_topk_kernel")
+    if topk:
+        by = work["block_topk_kernel"]["bytes"]
+        gbs = by / (topk[1] / topk[0] * 1e-3) / 1e9
+        out["selection"] = {"form": "stored block scores + block_topk_kernel", "gbs": round(gbs, 1),
+                            "frac": round(gbs / peaks["hbm_gbs"], 4), "target_frac": 0.6,
+                            "met": gbs / peaks["hbm_gbs"] >= 0.6}
+    else:
+        out["selection"] = {"form": "fused into index_scores_tc_kernel's epilogue: the block scores never reach HBM, "
+                                    "so the selection has no memory-bound phase to time", "gbs": None, "frac": None,
+                            "target_frac": 0.6, "met": True}
+    return out
+
+
+def oracle_flops(w, positions):
+    """FLOPs the oracle sample actually performs, counted with the useful-work
+    closed forms: index scores, forward, the KL's index scores, and the
+    query-side backward of each sampled row (main: S, dP and dQ, 6 d T per
+    head; index: s and dq_idx, 4 d_idx T per group) -- the key-side gradients
+    (dK, dV, dK_idx) are not run on the sample and not counted."""
+    pos = np.asarray(positions, dtype=np.int64)
+    T = tokens_per_row(w, pos).astype(np.float64)
+    f = useful_flops(w.scaled(B=1), positions=pos)
+    total = f["index"] + f["fwd"]
+    if w.train:
+        total += f["kl"] + float(np.sum(6.0 * w.d * T * w.Hq + 4.0 * w.d_idx * T * w.Hkv))
+    return total
 
 
 def selection_stats(w, x, sh, sel):
@@ -247,8 +351,7 @@ def oracle_sample(w, x, n_rows: int, seed: int = 0):
         sel_full[0, :, rows, :] = sel_rows
         oracle.bwd_rows(osh, x["q"], x["k"], x["v"], x["d_o"], x["q_idx"], x["k_idx"], sel_full, 1.0, rows)
     dt = time.perf_counter() - t0
-    fl = useful_flops(w.scaled(B=1), positions=rows)
-    return dt, sum(fl.values()), oracle.num_threads(), len(rows)
+    return dt, oracle_flops(w, rows), oracle.num_threads(), len(rows)
 
 
 def calibrated_rows(w, x, target_s: float) -> tuple[int, float]:
@@ -267,6 +370,8 @@ def main():
     ap.add_argument("--workload", default="train_n128k")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true",
+                    help="skip the decode workload (1M-token caches) that the default run adds as the 'decode' key")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
 
@@ -430,6 +535,8 @@ def main():
         e2e = {"value": round(world * step_flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                "ms_per_step": round(e2e_ms, 3), "tokens_per_s": round(world * w.B * w.N / (e2e_ms * 1e-3), 1),
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": 4,
+               "d2h": "the loss scalar only: O and the five gradients stay on the device, where the next layer "
+                      "and the optimizer read them",
                "overlap": "each step's inputs uploaded on a second stream while the previous step computes, in the "
                           "order the step reads them; the step waits on each input group where it first reads it"}
 
@@ -439,36 +546,8 @@ def main():
     phase_flops = {"index_select": fl["index"], "sparse_attn_fwd": fl["fwd"], "kl_fwd": fl["kl"], "fused_bwd": fl["bwd"]}
     work = kernel_work(w)
     dom = max(ktimes, key=lambda k: ktimes[k][1])
-    n_l, tot_ms = ktimes[dom]
-    per_launch_ms = tot_ms / n_l
-    wk = work.get(dom)
-    if wk is None:
-        roofline = {"kernel": dom, "bound": None, "achieved": None, "peak": None, "unit": None, "frac": None,
-                    "traffic": None, "launch_ms": round(per_launch_ms, 3)}
-    else:
-        # the binding roofline: algorithmic bytes at the copy peak against FLOPs at
-        # the bf16 peak, whichever takes longer; the other side rides along
-        fl, by = wk["flops"], wk["bytes"]
-        t_tensor = fl / (peaks["bf16_tflops"] * 1e12) if fl else 0.0
-        t_hbm = by / (peaks["hbm_gbs"] * 1e9) if by else 0.0
-        sides = {}
-        if fl:
-            ach_t = fl / (per_launch_ms * 1e-3) / 1e12
-            sides["tensor"] = {"achieved": round(ach_t, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                               "frac": round(ach_t / peaks["bf16_tflops"], 4),
-                               "frac_of_sustained": round(ach_t / peaks["bf16_tflops_sustained"], 4),
-                               "peak_source": peaks["source"] + " burst bf16", "algorithmic_per_launch": fl}
-        if by:
-            ach_h = by / (per_launch_ms * 1e-3) / 1e9
-            sides["hbm"] = {"achieved": round(ach_h, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                            "frac": round(ach_h / peaks["hbm_gbs"], 4), "peak_source": peaks["source"] + " copy",
-                            "algorithmic_per_launch": by}
-        bound = "hbm" if t_hbm > t_tensor else "tensor"
-        other = "tensor" if bound == "hbm" else "hbm"
-        roofline = {"kernel": dom, "bound": bound, **sides[bound], "traffic": kernel_traffic(dom, w),
-                    "launch_ms": round(per_launch_ms, 3)}
-        if other in sides:
-            roofline[other] = sides[other]
+    roofline = kernel_roofline(dom, ktimes, work, peaks, w)
+    targets = target_report(w, ktimes, work, peaks, phase_ms, phase_flops, args.steps)
     kernels_ms = {k: round(v[1] / args.steps, 3) for k, v in sorted(ktimes.items(), key=lambda kv: -kv[1][1])}
     sel_stats = selection_stats(w, x, sh, sel) if rank == 0 else None
 
@@ -478,7 +557,12 @@ def main():
         dt, cfl, thr, n = oracle_sample(w, x, n_rows)
         cpu = {"value": round(cfl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
                "sample": f"{n} query rows of {w.name} (index scores, selection, forward, KL, query-side backward "
-                         f"of each), {dt:.1f} s; FLOPs counted with the same closed form"}
+                         f"of each), {dt:.1f} s; credited with the closed-form FLOPs of the work it ran (the "
+                         f"backward's query side only: 6 d T per head + 4 d_idx T per group)"}
+
+    decode = None
+    if not args.no_decode and w.name == "train_n128k":
+        decode = decode_line(args, BY_NAME["decode_1m_b4"], world, rank, dev)
 
     if rank == 0:
         line = {
@@ -495,8 +579,10 @@ def main():
             "useful_tflop_per_step": round(step_flops / 1e12, 4),
             "kernels_ms_per_step": kernels_ms,
             "selection": sel_stats,
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
+            "roofline": roofline, "targets": targets, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": int(launches),
             "clocks": clk, "impl": "ours",
+            "decode": decode,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -519,17 +605,49 @@ def decode_flops_bytes(w, positions):
 
 
 def run_decode(args, w, world, rank, local):
-    """Decode workload: every step appends the new token of each sequence to
-    the caches, then selects blocks and attends for the one new query."""
+    """Decode workload on its own: one JSON line."""
     import torch
-    from block_sparse_gqa_causal_gb300 import api
-    from block_sparse_gqa_causal_gb300.inputs import decode_position, make_inputs
     if world > 1:
         import torch.distributed as dist
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
+    line = decode_line(args, w, world, rank, dev)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def oracle_decode_sample(w, x, steps):
+    """The CPU oracle's decode step (block scores over the whole cache,
+    selection, attention) for every sequence at the listed steps; returns
+    (seconds, tokens, threads)."""
+    import oracle
+    from block_sparse_gqa_causal_gb300.inputs import decode_position
+    t0 = time.perf_counter()
+    for s in steps:
+        pos = decode_position(w, s)
+        osh = oracle.Shape(B=w.B, Nq=1, Nk=pos + 1, Hq=w.Hq, Hkv=w.Hkv, d=w.d, d_idx=w.d_idx, topk=w.topk,
+                           q_offset=pos, kv_rows=w.N)
+        rows = np.arange(w.B)
+        q = np.ascontiguousarray(x["q"][:, s:s + 1])
+        qi = np.ascontiguousarray(x["q_idx"][:, s:s + 1])
+        bs = oracle.block_scores(osh, qi, x["k_idx"], rows)
+        sel = oracle.select(osh, bs, rows)
+        oracle.sparse_fwd(osh, q, x["k"], x["v"], sel, rows)
+    return time.perf_counter() - t0, w.B * len(steps), oracle.num_threads()
+
+
+def decode_line(args, w, world, rank, dev):
+    """Decode workload: every step appends the new token of each sequence to
+    the caches, then selects blocks and attends for the one new query.
+    Returns the JSON record (rank 0) of the timed steps."""
+    import torch
+    from block_sparse_gqa_causal_gb300 import api
+    from block_sparse_gqa_causal_gb300.inputs import decode_position, make_inputs
     x = make_inputs(w)
     tt = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
     q, qi = tt(x["q"]).to(dev), tt(x["q_idx"]).to(dev)
@@ -621,20 +739,28 @@ def run_decode(args, w, world, rank, local):
     flops, byts = decode_flops_bytes(w, [decode_position(w, s) for s in range(steps)])
     peaks = load_peaks()
     gbs = byts / (ms * 1e-3) / 1e9
-    if rank == 0:
-        print(json.dumps({
-            "metric": "MSA decode tokens/s at 1M context on 1 GB300", "value": round(world * w.B * steps / (ms * 1e-3), 1),
-            "unit": "tokens/s", "n_gpus": world, "steps": steps, "warmup": args.warmup,
-            "ms_per_step": round(ms / steps, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "cache": w.N, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
-                       "d_idx": w.d_idx, "topk": w.topk, "seed": w.seed,
-                       "l2": "no flush: each step streams the 1 GB K_idx cache"},
-            "useful_tflops": round(world * flops / (ms * 1e-3) / 1e12, 3),
-            "roofline": {"kernel": "decode step (index scan dominant)", "bound": "hbm", "achieved": round(gbs, 1),
-                         "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
-                         "peak_source": peaks["source"] + " copy bandwidth", "traffic": None},
-            "e2e": e2e, "gpu_launches": int(launches), "clocks": clk, "impl": "ours"}), flush=True)
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        dt, toks, thr = oracle_decode_sample(w, x, (0, steps - 1))
+        cpu = {"value": round(toks / dt, 3), "unit": "tokens/s", "cores": thr, "kind": "oracle",
+               "sample": f"decode steps 0 and {steps - 1} of {w.name} for all {w.B} sequences (block scores over "
+                         f"the whole cache, selection, attention), {dt:.1f} s"}
+    del k, v, ki, new_k, new_v, new_ki
+    torch.cuda.empty_cache()
+    return {
+        "metric": "MSA decode tokens/s at 1M context on 1 GB300", "value": round(world * w.B * steps / (ms * 1e-3), 1),
+        "unit": "tokens/s", "n_gpus": world, "steps": steps, "warmup": args.warmup,
+        "ms_per_step": round(ms / steps, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "cache": w.N, "Hq": w.Hq, "Hkv": w.Hkv, "d": w.d,
+                   "d_idx": w.d_idx, "topk": w.topk, "seed": w.seed,
+                   "l2": "no flush: each step streams the 1 GB K_idx cache"},
+        "useful_tflops": round(world * flops / (ms * 1e-3) / 1e12, 3),
+        "roofline": {"kernel": "decode step (index scan dominant)", "bound": "hbm", "achieved": round(gbs, 1),
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                     "peak_source": peaks["source"] + " copy bandwidth", "traffic": None,
+                     "algorithmic": "K_idx scan (pos+1 rows), block scores written and read, selected K and V"},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches), "clocks": clk, "impl": "ours"}
 
 
 def run_reference(args, w, world, rank):
@@ -663,8 +789,10 @@ def run_reference(args, w, world, rank):
                        "d_idx": w.d_idx, "block": w.block, "topk": w.topk, "seed": w.seed},
             "impl": "reference",
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
-                             "sample": f"{n_rows} query rows per step (whole hot path of each row; ms_per_step "
-                                       f"extrapolated to all rows by the closed-form FLOP count)"},
+                             "sample": f"{n_rows} query rows per step (index scores, selection, forward, KL and the "
+                                       f"query-side backward of each row, credited with the closed-form FLOPs of "
+                                       f"that work; ms_per_step extrapolated to the whole step's useful FLOPs at "
+                                       f"that rate)"},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

@@ -414,14 +414,18 @@ bool index_select_split(const Problem &p)
 
 size_t index_select_scratch_floats(const Problem &p)
 {
+    // what the path launch_index_select takes (no scores asked for) reads and
+    // writes: nothing when the selection is fused into the score kernel, the
+    // per-slice candidate keys when rows are split across CTAs, else the
+    // block scores between the score kernel and the top-k kernel
+    if (index_select_fused(p)) return 0;
     const size_t rows = (size_t)p.B * p.Nq * p.Hkv;
-    size_t n = rows * (size_t)p.nb;                              // block scores
     if (index_select_split(p)) {
         int tiles, splits, span;
         plan_grid(p, tiles, splits, span);
-        n = std::max(n, rows * (size_t)splits * 16 * 2);   // 16 8-byte keys per (row, slice)
+        return rows * (size_t)splits * 16 * 2;             // 16 8-byte keys per (row, slice)
     }
-    return n;
+    return rows * (size_t)p.nb;                            // block scores
 }
 
 bool index_select_fused(const Problem &p)

@@ -71,8 +71,9 @@ bool index_select_fused(const Problem &p);
 // true when launch_index_select, with no scores wanted, selects in the
 // split form (rows split across CTAs; per-slice candidates, then a merge)
 bool index_select_split(const Problem &p);
-// fp32 words of bs_scratch launch_index_select may use when bs_out is null:
-// the block scores, or the per-slice candidate keys of the split form
+// fp32 words of bs_scratch launch_index_select uses when bs_out is null, for
+// the path it takes: none in the fused form, the per-slice candidate keys in
+// the split form, else the block scores
 size_t index_select_scratch_floats(const Problem &p);
 // Key-major main branch forward (many queries per selected block).
 struct FwdWork {

@@ -13,10 +13,12 @@
 //
 // Limits and sharing:
 //   * the array holds a 256-byte status word plus kScratchScoreBytes of
-//     selection scratch: the block scores (B * Nq * Hkv * nb * 4 bytes) or,
-//     when a row's blocks are split across CTAs, 128 bytes of candidate keys
-//     per (row, slice), whichever is larger, must fit; larger shapes are
-//     rejected with MSA_ERR_WORKSPACE before any launch;
+//     selection scratch; what the selection path taken for the shape needs
+//     must fit: nothing when the top-k runs inside the score kernel (topk <=
+//     16, every CTA sees all blocks of its rows: prefill), 128 bytes of
+//     candidate keys per (row, slice) when a row's blocks are split across
+//     CTAs (decode), else the block scores (B * Nq * Hkv * nb * 4 bytes);
+//     larger needs are rejected with MSA_ERR_WORKSPACE before any launch;
 //   * every device that loads the library holds the array until the process
 //     exits;
 //   * all calls share the one array: calls whose work overlaps on the GPU
@@ -24,7 +26,9 @@
 //     the array keeps the last call's contents;
 //   * on each device, the first call looks up the array's device address
 //     (cudaGetSymbolAddress, with that device current) and caches it; make
-//     that first call before any stream capture.
+//     that first call before any stream capture.  A cudaDeviceReset destroys
+//     the context that address belongs to: after one, the cached address is
+//     stale and the entry point must not be called again in that process.
 #include <stdio.h>
 
 #include <mutex>
@@ -41,7 +45,7 @@ using namespace msa;
 
 namespace {
 
-constexpr size_t kScratchScoreBytes = 64ull << 20;     // 64 MiB of fp32 block scores
+constexpr size_t kScratchScoreBytes = 64ull << 20;     // 64 MiB of selection scratch
 constexpr size_t kScratchBytes = kStatusBytes + kScratchScoreBytes;
 constexpr int kMaxDevices = 64;
 
@@ -82,8 +86,8 @@ extern "C" msa_status msa_index_select_noalloc(const msa_shape *shape, const voi
     if (need > kScratchScoreBytes) {
         char msg[256];
         snprintf(msg, sizeof msg,
-                 "msa_index_select_noalloc: the selection scratch needs %zu bytes, the static array holds %zu "
-                 "(B*Nq*Hkv*ceil(Nk/block)*4 must be <= 64 MiB)", need, kScratchScoreBytes);
+                 "msa_index_select_noalloc: this shape's selection path needs %zu bytes of scratch, the static "
+                 "array holds %zu (64 MiB)", need, kScratchScoreBytes);
         return set_error(MSA_ERR_WORKSPACE, msg);
     }
     if (!q_idx || !k_idx || !sel_idx) return set_error(MSA_ERR_INVALID_ARGUMENT, "q_idx, k_idx and sel_idx must be non-NULL");
@@ -93,7 +97,8 @@ extern "C" msa_status msa_index_select_noalloc(const msa_shape *shape, const voi
     cudaError_t e = scratch_on_current_device(&scratch);
     if (e != cudaSuccess) return set_error(MSA_ERR_CUDA, cudaGetErrorString(e));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // the status word must start at zero; the block scores are fully rewritten
+    // the status word must start at zero; the scratch a path reads is scratch it
+    // wrote in the same call
     e = cudaMemsetAsync(scratch, 0, kStatusBytes, s);
     if (e != cudaSuccess) return set_error(MSA_ERR_CUDA, cudaGetErrorString(e));
     DeviceStatus *ds = static_cast<DeviceStatus *>(scratch);

@@ -217,16 +217,20 @@ msa_status msa_train_step_staged(const msa_shape *shape, const void *q, const vo
  * split row) is a static device array inside the library instead of a
  * caller workspace.  The caller still passes q_idx, k_idx and sel_idx
  * (layouts as above); block scores are not returned.
- *   - Limit: the scratch msa_workspace_size(MSA_OP_INDEX_SELECT) counts
- *     beyond its 256-byte status word -- B * Nq * Hkv * ceil(Nk/block) * 4
- *     bytes, or 128 bytes per (row, slice) when rows are split across CTAs,
- *     whichever is larger -- must be <= 64 MiB, else MSA_ERR_WORKSPACE before
- *     any launch.  Every device that loads the library holds that array
- *     (plus 256 bytes) until the process exits.
+ *   - Limit: the scratch the shape's selection path needs, which is
+ *     msa_workspace_size(shape, MSA_OP_INDEX_SELECT) - 256, must be <= 64 MiB,
+ *     else MSA_ERR_WORKSPACE before any launch.  That is none for prefill
+ *     shapes with topk <= 16 (the top-k runs inside the score kernel), 128
+ *     bytes per (row, slice) when a row's blocks are split across CTAs
+ *     (decode), and B * Nq * Hkv * ceil(Nk/block) * 4 bytes of block scores
+ *     otherwise (topk > 16).  Every device that loads the library holds that
+ *     array (64 MiB plus 256 bytes) until the process exits.
  *   - All calls share the array and it keeps the last call's contents;
  *     calls that overlap on the GPU race with each other.
  *   - The first call on each device looks up the array's address with that
- *     device current; make it before any stream capture.
+ *     device current and keeps it; make it before any stream capture.  After
+ *     a cudaDeviceReset the kept address is stale: do not call this entry
+ *     point again in that process.
  *   - Device-side status is kept inside the array, cleared at every call,
  *     and not reported by this entry point.
  */

@@ -26,3 +26,19 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Raw errors of every tolerance comparison made in this run (passing ones
+    included): test, tensor, max-abs, max-abs beyond the bf16 rounding
+    allowance of entries >= 8, relative L2."""
+    try:
+        from msa_testutil import RECORD
+    except Exception:  # pragma: no cover
+        return
+    if not RECORD:
+        return
+    tr = terminalreporter
+    tr.section("parity errors (raw)")
+    for test, name, ma, ma_arith, rl in RECORD:
+        tr.write_line(f"{test} | {name} | max-abs {ma:.3e} | beyond-rounding {ma_arith:.3e} | rel-L2 {rl:.3e}")

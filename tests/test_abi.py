@@ -39,8 +39,11 @@ def test_version_and_workspace_sizes(libmsa):
     from block_sparse_gqa_causal_gb300 import api
     assert "sm_103a" in api.version()
     sh = api.Shape(B=1, Nq=131072, Nk=131072, Hq=64, Hkv=8, d=128, d_idx=128, topk=16)
-    # block scores: B*Nq*Hkv*nb fp32 + status word
-    assert api.workspace_size(sh, api.OP_INDEX_SELECT) >= 131072 * 8 * 1024 * 4 + 256
+    # topk <= 16 in prefill: the top-k runs inside the score kernel, so only the status word
+    assert api.workspace_size(sh, api.OP_INDEX_SELECT) == 256
+    # topk > 16: block scores B*Nq*Hkv*nb fp32 + status word
+    sh24 = api.Shape(B=1, Nq=131072, Nk=131072, Hq=64, Hkv=8, d=128, d_idx=128, topk=24)
+    assert api.workspace_size(sh24, api.OP_INDEX_SELECT) == 131072 * 8 * 1024 * 4 + 256
     # key-major forward: bf16 partial outputs per (query, head, selected block) + their (max, sum)
     assert api.workspace_size(sh, api.OP_SPARSE_ATTN_FWD) >= 131072 * 64 * 16 * (128 * 2 + 8)
     dec = api.Shape(B=4, Nq=1, Nk=1 << 20, Hq=64, Hkv=8, d=128, d_idx=128, topk=16, q_offset=(1 << 20) - 1)

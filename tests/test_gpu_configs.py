@@ -1,0 +1,293 @@
+"""GPU parity at the five stated workloads' own shapes and seeds, through the
+C-ABI, against the CPU oracle (the fifth, decode at a 1M-token cache, and
+the 128K training step of the benchmark have their full-size checks here and
+in test_gpu_fullsize.py).
+
+  tiny_fwd_kl_n1k  B=1, N=1024, Hq=8, Hkv=2, d=d_idx=64, k=4, seed 0:
+                   every output element by element (selection, O, LSE,
+                   lse_idx, KL rows and loss, dq, dk, dv, dq_idx, dk_idx),
+                   through the phase calls and through msa_train_step.
+  fwd_n8k_b2       B=2, N=8192, Hq=32, Hkv=8, d=d_idx=128, k=16, needles,
+                   seed 1: block scores, selection, O and LSE of every row.
+  train_n32k       B=1, N=32768, Hq=32, Hkv=8, k=16, seed 2, one
+                   msa_train_step: sampled rows (selection, O, LSE, lse_idx,
+                   KL, dq, dq_idx) and key blocks (dk, dv, dk_idx) recomputed by
+                   the oracle, properties of every row.
+  decode_1m_b4     B=4, 1,048,576-token caches, Hq=64, Hkv=8, k=16, needles,
+                   seed 4: decode steps 0, 127, 128 (the first query of the
+                   last block) and 255 on the real caches -- block scores,
+                   selection (the split form without stored scores and the
+                   stored-scores form), O and LSE.
+
+Tolerances are those of the method's statement: max-abs 2e-2 and relative
+L2 1e-2 for bf16 outputs, KL and gradients; block scores within 2e-3;
+selections bit-exact where the oracle's cutoff gap exceeds 1e-3.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from msa_testutil import assert_close, bf16_to_np, check_selection, to_torch
+
+pytestmark = pytest.mark.gpu
+
+KL_COEF = 1.0
+
+
+def _osh(w, **kw):
+    return oracle.Shape(B=w.B, Nq=kw.get("Nq", w.N), Nk=kw.get("Nk", w.N), Hq=w.Hq, Hkv=w.Hkv, d=w.d,
+                        d_idx=w.d_idx, topk=w.topk, q_offset=kw.get("q_offset", 0), kv_rows=kw.get("kv_rows", 0))
+
+
+def _ash(w, **kw):
+    from block_sparse_gqa_causal_gb300 import api
+    return api.Shape(B=w.B, Nq=kw.get("Nq", w.N), Nk=kw.get("Nk", w.N), Hq=w.Hq, Hkv=w.Hkv, d=w.d,
+                     d_idx=w.d_idx, topk=w.topk, q_offset=kw.get("q_offset", 0), kv_rows=kw.get("kv_rows", 0))
+
+
+def _rows_of(sel_full, osh):
+    """[B, Hkv, Nq, k] -> [B*Nq, Hkv, k] in row order."""
+    return np.ascontiguousarray(np.asarray(sel_full).transpose(0, 2, 1, 3).reshape(osh.B * osh.Nq, osh.Hkv, osh.topk))
+
+
+def _valid_everywhere(sel_full, w, q_offset=0):
+    """Every row: ascending distinct ids ending with the local block, only
+    visible blocks, min(k, c0+1) of them."""
+    s = np.asarray(sel_full)
+    nq = s.shape[2]
+    c0 = ((q_offset + np.arange(nq)) // w.block)[None, None, :]
+    valid = s >= 0
+    assert np.all(s.max(axis=-1) == c0)
+    assert np.all(np.where(valid[..., 1:] & valid[..., :-1], np.diff(s, axis=-1) > 0, True))
+    assert np.all(np.where(valid, s <= c0[..., None], True))
+    assert np.all(valid.sum(axis=-1) == np.minimum(w.topk, c0 + 1))
+
+
+# ------------------------------------------------------------------ tiny (seed 0)
+@pytest.fixture(scope="module")
+def tiny():
+    import torch
+    from block_sparse_gqa_causal_gb300 import api
+    from block_sparse_gqa_causal_gb300.inputs import make_inputs
+    from block_sparse_gqa_causal_gb300.workloads import TINY
+    w = TINY
+    x = make_inputs(w, with_grad=True)
+    t = {n: to_torch(x[n]) for n in ("q", "k", "v", "q_idx", "k_idx", "d_o")}
+    sh = _ash(w)
+    sel, bs = api.index_select(sh, t["q_idx"], t["k_idx"], return_scores=True)
+    o, lse = api.sparse_attn_fwd(sh, t["q"], t["k"], t["v"], sel)
+    kl_loss, lse_idx, kl_rows = api.kl_fwd(sh, t["q"], t["k"], t["q_idx"], t["k_idx"], sel, lse, KL_COEF)
+    grads = api.fused_bwd(sh, t["q"], t["k"], t["v"], o, t["d_o"], lse, t["q_idx"], t["k_idx"], sel, lse_idx, KL_COEF)
+    ts = api.train_step(sh, t["q"], t["k"], t["v"], t["q_idx"], t["k_idx"], t["d_o"], KL_COEF)
+    torch.cuda.synchronize()
+    res = {"sel": sel.cpu().numpy(), "bs": bs.cpu().numpy(), "o": bf16_to_np(o), "lse": lse.cpu().numpy(),
+           "lse_idx": lse_idx.cpu().numpy(), "kl_rows": kl_rows.cpu().numpy(), "kl_loss": float(kl_loss.item()),
+           "grads": dict(zip(("dq", "dk", "dv", "dq_idx", "dk_idx"), (bf16_to_np(g) for g in grads))),
+           "ts": {n: (bf16_to_np(v) if v.dtype == torch.bfloat16 else v.cpu().numpy()) for n, v in ts.items()}}
+    osh = _osh(w)
+    rows = np.arange(w.B * w.N)
+    bs_o = oracle.block_scores(osh, x["q_idx"], x["k_idx"], rows)
+    return w, x, osh, res, rows, bs_o
+
+
+def test_tiny_selection_and_scores(tiny):
+    w, x, osh, res, rows, bs_o = tiny
+    bs_g = res["bs"].reshape(w.B * w.N, w.Hkv, w.nb)
+    vis = np.isfinite(bs_o)
+    assert_close(bs_g[vis], bs_o[vis], "tiny block scores", max_abs=2e-3, rel_l2=1e-4)
+    sel_o = oracle.select(osh, bs_o, rows)
+    for sel in (res["sel"], res["ts"]["sel"]):
+        exact, tol = check_selection(w.topk, 128, 0, w.N, rows, _rows_of(sel, osh), sel_o, bs_o)
+        assert tol <= 0.01 * (exact + tol) + 2
+    _valid_everywhere(res["sel"], w)
+
+
+@pytest.mark.parametrize("via", ["phases", "train_step"])
+def test_tiny_forward_and_kl(tiny, via):
+    w, x, osh, res, rows, bs_o = tiny
+    r = res if via == "phases" else res["ts"]
+    sel_rows = _rows_of(r["sel"], osh)
+    o_ref, lse_ref = oracle.sparse_fwd(osh, x["q"], x["k"], x["v"], sel_rows, rows)
+    assert_close(r["o"].reshape(o_ref.shape), o_ref, f"tiny o ({via})", bf16_out=True)
+    assert_close(r["lse"].transpose(0, 2, 1).reshape(lse_ref.shape), lse_ref, f"tiny lse ({via})", max_abs=1e-3,
+                 rel_l2=1e-5)
+    lse_idx_ref, kl_ref = oracle.kl(osh, x["q"], x["k"], x["q_idx"], x["k_idx"], sel_rows, rows)
+    to_rows = lambda a: np.asarray(a).transpose(0, 2, 1).reshape(w.B * w.N, w.Hkv)
+    assert_close(to_rows(r["lse_idx"]), lse_idx_ref, f"tiny lse_idx ({via})", max_abs=1e-3, rel_l2=1e-5)
+    assert_close(to_rows(r["kl_rows"]), kl_ref, f"tiny kl_rows ({via})")
+    want = oracle.kl_loss(osh, kl_ref, KL_COEF)
+    got = float(r["kl_loss"])
+    assert abs(got - want) <= 2e-2 and abs(got - want) <= 1e-2 * abs(want) + 1e-6, (got, want)
+
+
+@pytest.mark.parametrize("via", ["phases", "train_step"])
+def test_tiny_gradients(tiny, via):
+    w, x, osh, res, rows, bs_o = tiny
+    sel = res["sel"] if via == "phases" else res["ts"]["sel"]
+    g = res["grads"] if via == "phases" else res["ts"]
+    args = (osh, x["q"], x["k"], x["v"], x["d_o"], x["q_idx"], x["k_idx"], sel, KL_COEF)
+    dq, dqi = oracle.bwd_rows(*args)
+    dk, dv, dki = oracle.bwd_keys(*args)
+    assert_close(g["dq"].reshape(dq.shape), dq, f"tiny dq ({via})", bf16_out=True)
+    assert_close(g["dq_idx"].reshape(dqi.shape), dqi, f"tiny dq_idx ({via})", bf16_out=True)
+    assert_close(g["dk"], dk[:, :w.N], f"tiny dk ({via})", bf16_out=True)
+    assert_close(g["dv"], dv[:, :w.N], f"tiny dv ({via})", bf16_out=True)
+    assert_close(g["dk_idx"], dki[:, :w.N], f"tiny dk_idx ({via})", bf16_out=True)
+
+
+# ------------------------------------------------------------------ 8K forward, B=2, needles (seed 1)
+@pytest.fixture(scope="module")
+def fwd8k():
+    import torch
+    from block_sparse_gqa_causal_gb300 import api
+    from block_sparse_gqa_causal_gb300.inputs import make_inputs
+    from block_sparse_gqa_causal_gb300.workloads import FWD_8K
+    w = FWD_8K
+    x = make_inputs(w)
+    t = {n: to_torch(x[n]) for n in ("q", "k", "v", "q_idx", "k_idx")}
+    sh = _ash(w)
+    sel_f = api.index_select(sh, t["q_idx"], t["k_idx"])                       # fused: scores never stored
+    sel, bs = api.index_select(sh, t["q_idx"], t["k_idx"], return_scores=True)
+    o, lse = api.sparse_attn_fwd(sh, t["q"], t["k"], t["v"], sel_f)
+    torch.cuda.synchronize()
+    res = {"sel_f": sel_f.cpu().numpy(), "sel": sel.cpu().numpy(), "bs": bs.cpu().numpy(), "o": bf16_to_np(o),
+           "lse": lse.cpu().numpy()}
+    return w, x, _osh(w), res
+
+
+def test_fwd8k_selection_every_row(fwd8k):
+    w, x, osh, res = fwd8k
+    assert np.array_equal(res["sel_f"], res["sel"])
+    rows = np.arange(w.B * w.N)
+    bs_o = oracle.block_scores(osh, x["q_idx"], x["k_idx"], rows)
+    bs_g = res["bs"].reshape(w.B * w.N, w.Hkv, w.nb)
+    vis = np.isfinite(bs_o)
+    assert_close(bs_g[vis], bs_o[vis], "8K block scores", max_abs=2e-3, rel_l2=1e-4)
+    sel_o = oracle.select(osh, bs_o, rows)
+    exact, tol = check_selection(w.topk, 128, 0, w.N, rows, _rows_of(res["sel_f"], osh), sel_o, bs_o)
+    assert tol <= 0.01 * (exact + tol) + 2
+    _valid_everywhere(res["sel_f"], w)
+
+
+def test_fwd8k_output_every_row(fwd8k):
+    w, x, osh, res = fwd8k
+    rows = np.arange(w.B * w.N)
+    o_ref, lse_ref = oracle.sparse_fwd(osh, x["q"], x["k"], x["v"], _rows_of(res["sel_f"], osh), rows)
+    assert_close(res["o"].reshape(o_ref.shape), o_ref, "8K o", bf16_out=True)
+    assert_close(res["lse"].transpose(0, 2, 1).reshape(lse_ref.shape), lse_ref, "8K lse", max_abs=1e-3, rel_l2=1e-5)
+
+
+# ------------------------------------------------------------------ 32K training step (seed 2)
+@pytest.fixture(scope="module")
+def train32k():
+    import torch
+    from block_sparse_gqa_causal_gb300 import api
+    from block_sparse_gqa_causal_gb300.inputs import make_inputs
+    from block_sparse_gqa_causal_gb300.workloads import TRAIN_32K
+    w = TRAIN_32K
+    x = make_inputs(w, with_grad=True)
+    t = {n: to_torch(x[n]) for n in ("q", "k", "v", "q_idx", "k_idx", "d_o")}
+    out = api.train_step(_ash(w), t["q"], t["k"], t["v"], t["q_idx"], t["k_idx"], t["d_o"], KL_COEF)
+    torch.cuda.synchronize()
+    res = {n: (bf16_to_np(v) if v.dtype == torch.bfloat16 else v.cpu().numpy()) for n, v in out.items()}
+    rng = np.random.default_rng(32)
+    fixed = [0, 1, 127, 128, 2047, 2048, 2049, 16383, 16384, w.N - 129, w.N - 1]
+    rows = np.unique(np.concatenate([fixed, rng.choice(w.N, size=21, replace=False)]))
+    return w, x, _osh(w), res, rows
+
+
+def test_train32k_selection_and_forward_sampled(train32k):
+    w, x, osh, res, rows = train32k
+    _valid_everywhere(res["sel"], w)
+    bs_o = oracle.block_scores(osh, x["q_idx"], x["k_idx"], rows)
+    sel_o = oracle.select(osh, bs_o, rows)
+    sel_g = oracle.sel_rows_from_full(osh, res["sel"], rows)
+    exact, tol = check_selection(w.topk, 128, 0, w.N, rows, sel_g, sel_o, bs_o)
+    assert exact >= len(rows) * w.Hkv // 2
+    o_ref, lse_ref = oracle.sparse_fwd(osh, x["q"], x["k"], x["v"], sel_g, rows)
+    assert_close(res["o"].reshape(w.N, w.Hq, w.d)[rows], o_ref, "32K o (sampled rows)", bf16_out=True)
+    assert_close(res["lse"][0][:, rows].T, lse_ref, "32K lse (sampled rows)", max_abs=1e-3, rel_l2=1e-5)
+    assert np.all(np.isfinite(res["o"])) and np.all(np.isfinite(res["lse"]))
+
+
+def test_train32k_kl_sampled_and_loss(train32k):
+    w, x, osh, res, rows = train32k
+    sel_g = oracle.sel_rows_from_full(osh, res["sel"], rows)
+    lse_idx_ref, kl_ref = oracle.kl(osh, x["q"], x["k"], x["q_idx"], x["k_idx"], sel_g, rows)
+    assert_close(res["lse_idx"][0][:, rows].T, lse_idx_ref, "32K lse_idx (sampled rows)", max_abs=1e-3, rel_l2=1e-5)
+    assert_close(res["kl_rows"][0][:, rows].T, kl_ref, "32K kl_rows (sampled rows)")
+    kl_all = res["kl_rows"].astype(np.float64)
+    assert np.all(np.isfinite(kl_all)) and np.all(kl_all > -1e-3)
+    want = KL_COEF * kl_all.sum() / (w.B * w.N * w.Hkv)
+    assert abs(float(res["kl_loss"]) - want) <= 1e-4 * abs(want) + 1e-7
+
+
+def test_train32k_gradients_sampled(train32k):
+    w, x, osh, res, rows = train32k
+    for n in ("dq", "dk", "dv", "dq_idx", "dk_idx"):
+        assert np.all(np.isfinite(res[n])), n
+    args = (osh, x["q"], x["k"], x["v"], x["d_o"], x["q_idx"], x["k_idx"], res["sel"], KL_COEF)
+    dq, dqi = oracle.bwd_rows(*args, rows=rows)
+    assert_close(res["dq"].reshape(w.N, w.Hq, w.d)[rows], dq, "32K dq (sampled rows)", bf16_out=True)
+    assert_close(res["dq_idx"].reshape(w.N, w.Hkv, w.d_idx)[rows], dqi, "32K dq_idx (sampled rows)", bf16_out=True)
+    kblocks = np.array([3, 100, w.nb - 1])
+    dk, dv, dki = oracle.bwd_keys(*args, kblocks=kblocks)
+    keys = (kblocks[:, None] * 128 + np.arange(128)[None, :]).reshape(-1)
+    assert_close(res["dk"][:, keys], dk, "32K dk (sampled blocks)", bf16_out=True)
+    assert_close(res["dv"][:, keys], dv, "32K dv (sampled blocks)", bf16_out=True)
+    assert_close(res["dk_idx"][:, keys], dki, "32K dk_idx (sampled blocks)", bf16_out=True)
+
+
+# ------------------------------------------------------------------ decode at 1M context (seed 4)
+DECODE_STEPS = (0, 127, 128, 255)
+
+
+@pytest.fixture(scope="module")
+def decode1m():
+    import torch
+    from block_sparse_gqa_causal_gb300.inputs import make_inputs
+    from block_sparse_gqa_causal_gb300.workloads import DECODE_1M
+    w = DECODE_1M
+    x = make_inputs(w)
+    t = {n: to_torch(x[n]) for n in ("k", "v", "k_idx")}
+    torch.cuda.synchronize()
+    return w, x, t
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("step", DECODE_STEPS)
+def test_decode1m_step_parity(decode1m, step):
+    """The caches hold the prefilled 1,048,320 tokens and the new tokens of
+    the steps (the token of step s sits at position 1,048,320 + s); step s
+    queries at that position with Nk = position + 1.  Steps 127 and 128 are
+    the last query of block 8190 and the first of block 8191."""
+    import torch
+    from block_sparse_gqa_causal_gb300 import api
+    from block_sparse_gqa_causal_gb300.inputs import decode_position
+    w, x, t = decode1m
+    pos = decode_position(w, step)
+    q = np.ascontiguousarray(x["q"][:, step:step + 1])
+    qi = np.ascontiguousarray(x["q_idx"][:, step:step + 1])
+    kw = dict(Nq=1, Nk=pos + 1, q_offset=pos, kv_rows=w.N)
+    sh = _ash(w, **kw)
+    tq, tqi = to_torch(q), to_torch(qi)
+    sel = api.index_select(sh, tqi, t["k_idx"])                               # split form: no scores stored
+    sel_s, bs = api.index_select(sh, tqi, t["k_idx"], return_scores=True)
+    o, lse = api.sparse_attn_fwd(sh, tq, t["k"], t["v"], sel)
+    torch.cuda.synchronize()
+    assert np.array_equal(sel.cpu().numpy(), sel_s.cpu().numpy())
+    osh = _osh(w, **kw)
+    rows = np.arange(w.B)
+    bs_o = oracle.block_scores(osh, qi, x["k_idx"], rows)
+    bs_g = bs.cpu().numpy().reshape(w.B, w.Hkv, -1)
+    vis = np.isfinite(bs_o)
+    assert_close(bs_g[vis], bs_o[vis], f"decode 1M step {step} block scores", max_abs=2e-3, rel_l2=1e-4)
+    sel_o = oracle.select(osh, bs_o, rows)
+    sel_g = sel.cpu().numpy()[:, :, 0, :]
+    exact, tol = check_selection(w.topk, 128, pos, 1, rows, sel_g, sel_o, bs_o)
+    assert exact >= w.B * w.Hkv // 2
+    assert np.all(sel_g[:, :, -1] == pos // 128)
+    o_ref, lse_ref = oracle.sparse_fwd(osh, q, x["k"], x["v"], sel_g, rows)
+    assert_close(bf16_to_np(o).reshape(o_ref.shape), o_ref, f"decode 1M step {step} o", bf16_out=True)
+    assert_close(lse.cpu().numpy().reshape(w.B, w.Hq), lse_ref, f"decode 1M step {step} lse", max_abs=1e-3,
+                 rel_l2=1e-5)

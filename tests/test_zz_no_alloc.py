@@ -26,17 +26,30 @@ def _noalloc_fn():
     return fn
 
 
-def test_noalloc_select_matches_workspace_entry_point_on_two_calls():
+CASES = [
+    # prefill, topk <= 16: the top-k runs in the score kernel, no scratch used
+    ("fused_small", dict(B=2, Nq=1000, Nk=1000, Hq=8, Hkv=2, d=64, d_idx=64, topk=4)),
+    ("fused_g8", dict(B=1, Nq=3000, Nk=3000, Hq=32, Hkv=8, d=128, d_idx=128, topk=16)),
+    # a 32K prefill: its fused selection needs no scratch, so the 64 MiB limit does not apply
+    ("fused_32k", dict(B=1, Nq=32768, Nk=32768, Hq=32, Hkv=8, d=128, d_idx=128, topk=16)),
+    # decode: a row's blocks split across CTAs, per-slice candidates in the array, then a merge
+    ("split_decode", dict(B=2, Nq=1, Nk=200000, Hq=4, Hkv=4, d=128, d_idx=128, topk=16, q_offset=199999)),
+    # topk > 16: block scores in the array, then the separate top-k kernel (warp per row)
+    ("scores_k24", dict(B=1, Nq=2000, Nk=2000, Hq=2, Hkv=2, d=64, d_idx=64, topk=24)),
+    # topk > 16 with a long decode row (a CTA per row in the top-k kernel)
+    ("scores_k24_decode", dict(B=2, Nq=1, Nk=300000, Hq=2, Hkv=2, d=64, d_idx=64, topk=24, q_offset=299999)),
+]
+
+
+@pytest.mark.parametrize("name,kw", CASES, ids=[c[0] for c in CASES])
+def test_noalloc_select_matches_workspace_entry_point_on_two_calls(name, kw):
     import torch
     from block_sparse_gqa_causal_gb300 import api
     fn = _noalloc_fn()
     stream = torch.cuda.current_stream()
-    cases = [
-        (api.Shape(B=2, Nq=1000, Nk=1000, Hq=8, Hkv=2, d=64, d_idx=64, topk=4), 1),
-        (api.Shape(B=1, Nq=3000, Nk=3000, Hq=32, Hkv=8, d=128, d_idx=128, topk=16), 2),
-    ]
-    for sh, seed in cases:
-        g = torch.Generator(device="cuda").manual_seed(seed)
+    sh = api.Shape(**kw)
+    for call in range(2):
+        g = torch.Generator(device="cuda").manual_seed(1000 * call + sh.Nk + sh.topk)
         qi = torch.randn(sh.B, sh.Nq, sh.Hkv, sh.d_idx, device="cuda", generator=g).bfloat16()
         ki = torch.randn(sh.B, sh.Nk, sh.d_idx, device="cuda", generator=g).bfloat16()
         want = api.index_select(sh, qi, ki)
@@ -44,14 +57,14 @@ def test_noalloc_select_matches_workspace_entry_point_on_two_calls():
         rc = fn(ctypes.byref(sh.c()), qi.data_ptr(), ki.data_ptr(), got.data_ptr(), stream.cuda_stream)
         assert rc == 0, api.lib().msa_last_error()
         torch.cuda.synchronize()
-        assert torch.equal(got, want)
+        assert torch.equal(got, want), (name, call)
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
     from block_sparse_gqa_causal_gb300 import api
     fn = _noalloc_fn()
-    # 32768 x 8 groups x 256 blocks x 4 bytes = 256 MiB of block scores > 64 MiB
-    sh = api.Shape(B=1, Nq=32768, Nk=32768, Hq=32, Hkv=8, d=128, d_idx=128, topk=16)
+    # topk > 16 keeps the block scores: 32768 x 8 groups x 256 blocks x 4 bytes = 256 MiB > 64 MiB
+    sh = api.Shape(B=1, Nq=32768, Nk=32768, Hq=32, Hkv=8, d=128, d_idx=128, topk=24)
     rc = fn(ctypes.byref(sh.c()), None, None, None, None)
     assert rc == 3
     assert b"64 MiB" in api.lib().msa_last_error()
