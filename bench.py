@@ -48,10 +48,12 @@ def tokens_per_row(w, pos):
 
 def useful_flops(w, positions=None):
     """Closed-form useful FLOPs per phase for one pass (all batch entries).
-    The KL's teacher needs the main-branch probabilities, which the backward
-    recomputes anyway (its S = QK^T, counted under "bwd"); the training step
-    takes the teacher's sums from there, so "kl" counts only the index
-    scores over the selected tokens (lse_idx)."""
+    The KL's teacher needs the main-branch probabilities, whose logits the
+    backward recomputes anyway (its S = QK^T, counted under "bwd"), so "kl"
+    counts only the index scores over the selected tokens (lse_idx); the
+    design's second recomputation of the logits for the teacher (next to the
+    index scores, so that no distribution is stored) is not useful work and
+    is not counted."""
     pos = np.arange(w.N, dtype=np.float64) if positions is None else np.asarray(positions, dtype=np.float64)
     T = tokens_per_row(w, pos.astype(np.int64)).astype(np.float64)
     B = w.B
@@ -106,12 +108,18 @@ def kernel_work(w):
                                "design_bytes": slots * (di * 2.0 + 4.0 + 32.0) + buckets * 128 * di * 2.0},
         "bwd_main_tc_kernel": {"flops": B * float(np.sum(10.0 * d * T * Hq)),
                                "bytes": 2 * q_b + 2 * kv_b + 2 * lse_b + sel_b + q_b + 2 * kv_b,
-                               "design_bytes": slots * (2 * G * d * 2.0 + G * d * 2.0 + 128 * 2.0 + G * 8.0)
+                               "design_bytes": slots * (2 * G * d * 2.0 + G * d * 2.0 + G * 8.0)
                                + buckets * 4 * 128 * d * 2.0},
-        "bwd_index_tc_kernel": {"flops": B * float(np.sum(6.0 * di * T * Hkv)),
-                                "bytes": qi_b + ki_b + row_b + sel_b + qi_b + ki_b,
-                                "design_bytes": slots * (di * 2.0 + 128 * 2.0 + di * 2.0 + 4.0)
-                                + buckets * 128 * di * (2.0 + 8.0)},
+        # index-branch backward with the teacher rebuilt on chip: the step reads q_idx,
+        # k_idx, lse_idx, the selection and what the teacher needs (Q, K, lse) and
+        # writes dq_idx, dk_idx; the design gathers Q and q_idx rows, lse and lse_idx
+        # per slot and writes a dq_idx partial row and the loss terms per slot, and
+        # per bucket reads K, K_idx and writes the group's fp32 dK_idx share
+        "index_teacher_bwd_tc_kernel": {"flops": B * float(np.sum(6.0 * di * T * Hkv)),
+                                        "bytes": qi_b + ki_b + row_b + sel_b + q_b + kv_b + lse_b + qi_b + ki_b,
+                                        "design_bytes": slots * (G * d * 2.0 + di * 2.0 + G * 4.0 + 4.0 + di * 2.0
+                                                                 + 16.0)
+                                        + buckets * 128 * (d + di) * 2.0 + buckets * 128 * di * 4.0},
         # block scores of the visible blocks in, indices out (the top-k step itself)
         "block_topk_kernel": {"flops": None, "bytes": B * Hkv * float(np.sum(vis_blocks * 4.0 + w.topk * 4.0)),
                               "design_bytes": None},
@@ -465,7 +473,8 @@ def main():
                 "sparse_attn_fwd_kernel": "sparse_attn_fwd", "sparse_attn_merge_kernel": "sparse_attn_fwd",
                 "index_count_kernel": "sparse_attn_fwd", "index_cta_scan_kernel": "sparse_attn_fwd",
                 "index_bucket_scan_kernel": "sparse_attn_fwd", "index_fill_kernel": "sparse_attn_fwd",
-                "kl_index_tc_kernel": "kl_fwd", "kl_combine_kernel": "kl_fwd"}
+                "kl_index_tc_kernel": "kl_fwd", "kl_combine_kernel": "kl_fwd",
+                "index_teacher_kl_tc_kernel": "kl_fwd"}
     phase_names = ["index_select", "sparse_attn_fwd"] + (["kl_fwd", "fused_bwd"] if w.train else [])
     phase_ms = {n: 0.0 for n in phase_names}
     for kname, (_, tot) in ktimes.items():

@@ -135,36 +135,42 @@ size_t fwd_bytes(const Problem &p)
     return align256(rows * p.d * 2) + align256(rows * 8) + index_bytes(p);
 }
 size_t klrows_bytes(const Problem &p) { return align256((size_t)p.B * p.Hkv * p.Nq * sizeof(float)); }
+// KL teacher terms: four floats per (query, group, slot)
+size_t klt_bytes(const Problem &p) { return align256((size_t)p.B * p.Hkv * p.Nq * p.topk * 16); }
 
-size_t kl_bytes(const Problem &p)
+// The KL forward with its teacher runs key-major (the teacher rebuilt on the
+// tensor cores next to the index scores) when d = d_idx = 128; the lse_idx-only
+// form runs key-major at any head dims; the rest streams query by query.
+bool kl_teacher_keymajor(const Problem &p) { return fwd_keymajor(p) && p.d == 128 && p.d_idx == 128; }
+size_t kl_bytes(const Problem &p, bool lse_only)
 {
-    if (!fwd_keymajor(p)) return 0;
-    return align256(kl_part_count(p) * 16) + align256((size_t)p.B * p.Hkv * p.Nq * p.topk * 128 * 2) + index_bytes(p);
+    if (!fwd_keymajor(p) || (!lse_only && !kl_teacher_keymajor(p))) return 0;
+    return align256(kl_part_count(p) * sizeof(float2)) + (lse_only ? 0 : klt_bytes(p)) + index_bytes(p);
 }
 
-// backward: D, dK_idx accumulators, the inverse index, and either the
-// per-slot partials + teacher (tcgen05 path) or fp32 dQ / dq_idx accumulators
+// backward: D, dK_idx accumulators (tcgen05 path: one fp32 share per group),
+// the inverse index, and either the per-slot partials (tcgen05 path) or fp32
+// dQ / dq_idx accumulators
 size_t bwd_bytes(const Problem &p)
 {
-    size_t n = align256((size_t)p.B * p.Hq * p.Nq * 4) + align256((size_t)p.B * p.Nk * p.d_idx * 4) + index_bytes(p);
+    const size_t dki = (size_t)p.B * p.Nk * p.d_idx * 4 * (bwd_tc(p) ? (size_t)p.Hkv : 1);
+    size_t n = align256((size_t)p.B * p.Hq * p.Nq * 4) + align256(dki) + index_bytes(p);
     const size_t slots = (size_t)p.B * p.Nq * p.topk;
     if (bwd_tc(p))
-        n += align256(slots * p.Hq * p.d * 2) + align256(slots * p.Hkv * p.d_idx * 2) +
-             align256((slots * p.Hkv + (size_t)8 * p.B * p.Hkv * p.nb) * 128 * 2) +
-             align256(((size_t)p.B * p.Hkv * p.nb + 1) * 4);
+        n += align256(slots * p.Hq * p.d * 2) + align256(slots * p.Hkv * p.d_idx * 2);
     else
         n += align256((size_t)p.B * p.Nq * p.Hq * p.d * 4) + align256((size_t)p.B * p.Nq * p.Hkv * p.d_idx * 4);
     return n;
 }
 
 // KL of the fused backward: rows (when the caller gives none) and either the
-// per-slot partials of the tensor-core backward or the KL forward's own
+// per-slot teacher terms of the tensor-core backward or the KL forward's own
 // scratch (with an lse_idx it recomputes)
 size_t bwdkl_bytes(const Problem &p)
 {
     const size_t rows = (size_t)p.B * p.Hkv * p.Nq;
-    if (bwd_tc(p)) return klrows_bytes(p) + align256(rows * p.topk * 4) + align256(rows * p.topk * 16);
-    return klrows_bytes(p) + kl_bytes(p) + align256(rows * 4);
+    if (bwd_tc(p)) return klrows_bytes(p) + klt_bytes(p);
+    return klrows_bytes(p) + kl_bytes(p, false) + align256(rows * 4);
 }
 
 // one training step: the shared inverse index, scores scratch (unfused
@@ -177,12 +183,12 @@ size_t train_bytes(const Problem &p)
     if (!train_shared_index(p)) {
         size_t n = bs_bytes(p);
         n = std::max(n, fwd_bytes(p));
-        n = std::max(n, klrows_bytes(p) + kl_bytes(p));
+        n = std::max(n, klrows_bytes(p) + kl_bytes(p, true));
         return std::max(n, bwd_bytes(p) + bwdkl_bytes(p));
     }
     const size_t rows = (size_t)p.B * p.Nq * p.Hq * p.topk;
-    return index_bytes(p) + (index_select_fused(p) ? 0 : bs_bytes(p)) + align256(rows * p.d * 2) + align256(rows * 8) +
-           align256(kl_part_count(p) * 16) + bwd_bytes(p) - index_bytes(p) + bwdkl_bytes(p);
+    return index_bytes(p) + bs_bytes(p) + align256(rows * p.d * 2) + align256(rows * 8) +
+           align256(kl_part_count(p) * sizeof(float2)) + bwd_bytes(p) - index_bytes(p) + bwdkl_bytes(p);
 }
 
 #define REQUIRE_PTR(ptr, name)                                                                         \
@@ -292,7 +298,7 @@ size_t msa_workspace_size(const msa_shape *shape, int op)
     switch (op) {
     case MSA_OP_INDEX_SELECT: return kStatusBytes + bs_bytes(p);
     case MSA_OP_SPARSE_ATTN_FWD: return kStatusBytes + fwd_bytes(p);
-    case MSA_OP_KL_FWD: return kStatusBytes + klrows_bytes(p) + kl_bytes(p);
+    case MSA_OP_KL_FWD: return kStatusBytes + klrows_bytes(p) + std::max(kl_bytes(p, false), kl_bytes(p, true));
     case MSA_OP_FUSED_BWD: return kStatusBytes + bwd_bytes(p);
     case MSA_OP_FUSED_BWD_KL: return kStatusBytes + bwd_bytes(p) + bwdkl_bytes(p);
     case MSA_OP_TRAIN_STEP: return kStatusBytes + train_bytes(p);
@@ -373,11 +379,10 @@ cudaError_t kl_forward(const Problem &p, const void *q, const void *k, const voi
                        float *scratch_rows, float *kl_loss, Carve &cv, DeviceStatus *ds, cudaStream_t s)
 {
     cudaError_t e;
-    if (fwd_keymajor(p)) {
+    if (rows ? kl_teacher_keymajor(p) : fwd_keymajor(p)) {
         KlWork w;
-        w.part = cv.take<float4>(kl_part_count(p));
-        __half *pt = cv.take<__half>((size_t)p.B * p.Hkv * p.Nq * p.topk * 128);
-        w.pt = rows ? pt : nullptr;
+        w.part = cv.take<float2>(kl_part_count(p));
+        w.klt = rows ? cv.take<float>((size_t)p.B * p.Hkv * p.Nq * p.topk * 4) : nullptr;
         carve_index(cv, p, w);
         e = launch_kl_keymajor(p, static_cast<const bf16 *>(q), static_cast<const bf16 *>(k),
                                static_cast<const bf16 *>(q_idx), static_cast<const bf16 *>(k_idx), sel_idx, lse,
@@ -427,7 +432,7 @@ msa_status msa_kl_fwd(const msa_shape *shape, const void *q, const void *k, cons
     if (!lse_only && !kl_loss)
         return fail(MSA_ERR_INVALID_ARGUMENT, "kl_loss is NULL (pass kl_rows and kl_loss both NULL for lse_idx only)");
     if (!isfinite(kl_coef)) return fail(MSA_ERR_INVALID_ARGUMENT, "kl_coef must be finite");
-    st = check_ws(workspace, workspace_bytes, kStatusBytes + (kl_rows ? 0 : klrows_bytes(p)) + kl_bytes(p));
+    st = check_ws(workspace, workspace_bytes, kStatusBytes + (kl_rows ? 0 : klrows_bytes(p)) + kl_bytes(p, lse_only));
     if (st != MSA_OK) return st;
     Carve cv{static_cast<char *>(workspace)};
     float *scratch = kl_rows ? nullptr : cv.take<float>((size_t)p.B * p.Hkv * p.Nq);
@@ -474,14 +479,12 @@ msa_status fused_bwd_impl(const msa_shape *shape, const void *q, const void *k, 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     BwdWork w{};
     w.D = cv.take<float>((size_t)p.B * p.Hq * p.Nq);
-    w.dki_acc = cv.take<float>((size_t)p.B * p.Nk * p.d_idx);
+    w.dki_acc = cv.take<float>((size_t)p.B * p.Nk * p.d_idx * (bwd_tc(p) ? (size_t)p.Hkv : 1));
     carve_index(cv, p, w);
     const size_t slots = (size_t)p.B * p.Nq * p.topk;
     if (bwd_tc(p)) {
         w.dq_part = cv.take<bf16>(slots * p.Hq * p.d);
         w.dqi_part = cv.take<bf16>(slots * p.Hkv * p.d_idx);
-        w.pt = cv.take<__half>((slots * p.Hkv + (size_t)8 * p.B * p.Hkv * p.nb) * 128);
-        w.pt_off = cv.take<int32_t>((size_t)p.B * p.Hkv * p.nb + 1);
     } else {
         w.dq_acc = cv.take<float>((size_t)p.B * p.Nq * p.Hq * p.d);
         w.dqi_acc = cv.take<float>((size_t)p.B * p.Nq * p.Hkv * p.d_idx);
@@ -491,8 +494,7 @@ msa_status fused_bwd_impl(const msa_shape *shape, const void *q, const void *k, 
     if (with_kl) {
         rows = kl_rows ? kl_rows : cv.take<float>((size_t)p.B * p.Hkv * p.Nq);
         if (bwd_tc(p)) {
-            w.kla = cv.take<float>(slots * p.Hkv);
-            w.klb = cv.take<float>(slots * p.Hkv * 4);
+            w.klt = cv.take<float>(slots * p.Hkv * 4);
             w.kl_rows = rows;
         } else {
             // no tensor-core backward: the KL forward's passes give the rows
@@ -596,18 +598,15 @@ msa_status train_step_impl(const msa_shape *shape, const void *q, const void *k,
     fw.part = cv.take<bf16>(rows * p.d);
     fw.stats = cv.take<float2>(rows);
     KlWork kw;
-    kw.part = cv.take<float4>(kl_part_count(p));
-    kw.pt = nullptr;                                   // lse_idx only: the loss comes from the backward
+    kw.part = cv.take<float2>(kl_part_count(p));
+    kw.klt = nullptr;                                  // lse_idx only: the loss comes from the backward
     w.D = cv.take<float>((size_t)p.B * p.Hq * p.Nq);
-    w.dki_acc = cv.take<float>((size_t)p.B * p.Nk * p.d_idx);
+    w.dki_acc = cv.take<float>((size_t)p.B * p.Hkv * p.Nk * p.d_idx);
     const size_t slots = (size_t)p.B * p.Nq * p.topk;
     w.dq_part = cv.take<bf16>(slots * p.Hq * p.d);
     w.dqi_part = cv.take<bf16>(slots * p.Hkv * p.d_idx);
-    w.pt = cv.take<__half>((slots * p.Hkv + (size_t)8 * p.B * p.Hkv * p.nb) * 128);
-    w.pt_off = cv.take<int32_t>((size_t)p.B * p.Hkv * p.nb + 1);
     float *rows_kl = kl_rows ? kl_rows : cv.take<float>((size_t)p.B * p.Hkv * p.Nq);
-    w.kla = cv.take<float>(slots * p.Hkv);
-    w.klb = cv.take<float>(slots * p.Hkv * 4);
+    w.klt = cv.take<float>(slots * p.Hkv * 4);
     w.kl_rows = rows_kl;
     // one inverse index of the selection serves the forward, the KL pass and the backward
     fw.bucket_cnt = kw.bucket_cnt = w.bucket_cnt;

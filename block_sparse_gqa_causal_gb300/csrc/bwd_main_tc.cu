@@ -14,10 +14,9 @@
 // dV and dK stay in TMEM for the whole bucket and are written once (one
 // owner, no atomics).  A chunk's dQ leaves as one bf16 partial row per
 // (query, head, slot); a combine kernel sums a row's slots (the split-KV
-// pattern of the forward).  The KL teacher (the mean over the group's heads
-// of P) falls out of the same tile: the heads of one query are consecutive
-// columns of a thread's row, so it is a register sum, written as fp16 per
-// (bucket entry, key) for the index-branch backward (and the KL loss terms).
+// pattern of the forward).  The KL's teacher and the index branch's backward
+// are computed elsewhere (index_teacher_tc.cu) from their own logit tiles, so
+// no probability distribution leaves this kernel.
 //
 // Roles: warps 0 and 11 load (TMA; alternate chunks), warp 1 owns TMEM and
 // issues the score MMAs, warp 10 the gradient MMAs, warps 2..9 are the
@@ -122,8 +121,7 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                    const bf16 *__restrict__ q, const bf16 *__restrict__ d_o, const float *__restrict__ lse,
                    const float *__restrict__ Dg, const int32_t *__restrict__ bucket_off,
                    const int32_t *__restrict__ bucket_q, bf16 *__restrict__ dk, bf16 *__restrict__ dv,
-                   bf16 *__restrict__ dq_part, __half *__restrict__ pt_out, const int32_t *__restrict__ pt_off,
-                   DeviceStatus *st)
+                   bf16 *__restrict__ dq_part, DeviceStatus *st)
 {
     constexpr int QC = kRows / G;                 // queries per chunk
     constexpr int EPL = (QC + 31) / 32;           // bucket entries per producer lane
@@ -407,10 +405,8 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         const long long j = j0 + kr;
         const bool key_ok = j < p.Nk;
         const float sl2 = p.scale * kLog2e;
-        const float invG = 1.f / (float)G;
         constexpr int NQH = 32 / G;                // query slots among this warp's 32 columns
         const int cb = hf * 32;                    // first column (row of the chunk) of this warp
-        const long long pt_base = pt_off[bucket];  // this bucket's first teacher row
         bool ok = true;
         for (int n = 0; ok && n < nch; ++n) {
             const int s = n % kStages, db = n % kDsBuf;
@@ -426,7 +422,7 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             int pos[NQH];
 #pragma unroll
             for (int u = 0; u < NQH; ++u) pos[u] = meta->pos[cb / G + u];
-            const int nq = meta->nq, e0 = meta->e0;
+            const int nq = meta->nq;
             long long ridx_cur;
             {
                 const int rho = cb + lane, qq = rho / G, g = rho % G;
@@ -436,16 +432,14 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             }
             tc::tmem_wait32(sv);
             tc::tmem_wait32(dp);
-            // P^T, dS^T of this key against the warp's 32 rows; teacher sums.  The
-            // mask is needed only where some row of the warp does not see the whole
-            // block (a bucket's local-block queries, its padded tail, the last block)
+            // P^T, dS^T of this key against the warp's 32 rows.  The mask is
+            // needed only where some row of the warp does not see the whole block
+            // (a bucket's local-block queries, its padded tail, the last block)
             uint32_t pk[16], dk2[16];
-            float ptq[NQH];
             int lim[NQH];                              // last visible key offset per query (-1: none)
             int minpos = pos[0];
 #pragma unroll
             for (int u = 0; u < NQH; ++u) {
-                ptq[u] = 0.f;
                 minpos = min(minpos, pos[u]);
                 lim[u] = (int)max(-1LL, min(min((long long)pos[u], (long long)p.Nk - 1) - j0, (long long)kKeys - 1));
             }
@@ -465,7 +459,6 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                         else pr[e] = kr <= lim[u] ? x : 0.f;
                         // dS carries the softmax scale, so dQ and dK need no rescaling
                         ds[e] = pr[e] * fmaf(__uint_as_float(dp[col]), p.scale, -(e ? dd.y : dd.x));
-                        ptq[u] += pr[e];
                     }
                     pk[cc / 2] = pack_bf16(pr[0], pr[1]);
                     dk2[cc / 2] = pack_bf16(ds[0], ds[1]);
@@ -475,30 +468,6 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             else softmax_grad(std::false_type{});
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&empty[s]);   // done with the stage's row data
-            {
-                // this key's teacher for the warp's NQH queries (consecutive entries,
-                // 4-aligned): 8 bytes into one 8-entry group, or 16 bytes per group
-                const int t = e0 - qbeg + cb / G;
-                __half *dst = pt_out + (pt_base + (t & ~7)) * kKeys + kr * 8 + (t & 7);
-                uint32_t hv[NQH / 2];
-#pragma unroll
-                for (int u = 0; u < NQH; u += 2) {
-                    const __half2 h2 = __floats2half2_rn(cb / G + u < nq ? ptq[u] * invG : 0.f,
-                                                         cb / G + u + 1 < nq ? ptq[u + 1] * invG : 0.f);
-                    hv[u / 2] = *reinterpret_cast<const uint32_t *>(&h2);
-                }
-                // only groups holding a valid entry: the rest may lie past this
-                // bucket's region (its count is rounded up to 8 entries only)
-                if constexpr (NQH == 4) {
-                    if (cb / G < nq) *reinterpret_cast<uint2 *>(dst) = make_uint2(hv[0], hv[1]);
-                } else {
-#pragma unroll
-                    for (int x = 0; x < NQH / 8; ++x)
-                        if (cb / G + 8 * x < nq)
-                            *reinterpret_cast<uint4 *>(dst + (long long)x * 8 * kKeys) =
-                                make_uint4(hv[4 * x], hv[4 * x + 1], hv[4 * x + 2], hv[4 * x + 3]);
-                }
-            }
             // P^T and dS^T over this warp's own S^T columns (read above) for the dV / dK MMAs
             tc::tmem_st16(ts, pk);
             tc::tmem_st16(ts + 16, dk2);
@@ -605,7 +574,7 @@ cudaError_t launch_g(const Problem &p, const bf16 *q, const bf16 *k, const bf16 
     {
         TimedLaunch timed_("bwd_main_tc_kernel", s);
         bwd_main_tc_kernel<G><<<dim3(p.Hkv, p.nb, p.B), kThreads, ALLOC, s>>>(
-            tq, tdo, tk, tv, p, q, d_o, lse, w.D, w.bucket_off, w.bucket_q, dk, dv, w.dq_part, w.pt, w.pt_off, st);
+            tq, tdo, tk, tv, p, q, d_o, lse, w.D, w.bucket_off, w.bucket_q, dk, dv, w.dq_part, st);
     }
     note_launch();
     return cudaGetLastError();

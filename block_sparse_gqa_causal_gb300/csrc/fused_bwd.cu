@@ -97,100 +97,6 @@ __global__ void __launch_bounds__(256) bwd_rowdot_kernel(Problem p, const bf16 *
     }
 }
 
-// Teacher term of the KL loss (section 3.2, the L_KL equation): for every
-// (query, group, selected block), sum over the block's keys of Pt log2 Pt,
-// read back from the teacher the main-branch backward left per (bucket
-// entry, key) in groups of 8 entries ([group][key][8 entries], fp16, each
-// bucket's entries padded to whole groups).  The grid runs over the flat
-// array of groups, 32 groups (64 KB) per CTA with all of a thread's loads in
-// flight, so the largest buckets (the early blocks most queries select) are
-// spread over many CTAs.  Thread k of a half reads key k's 8 entries of
-// every other group; each warp sums its 32 keys per entry with a transposing
-// warp sum, the four warps of a half add up in shared memory, and each
-// entry's bucket is found by binary search in pt_off.  Writes
-// kla[((b, r, query), slot)].
-constexpr int kEntGroups = 32;   // 8-entry groups per CTA
-
-__global__ void __launch_bounds__(256) bwd_teacher_entropy_kernel(Problem p, const int32_t *__restrict__ bucket_off,
-                                                                  const int32_t *__restrict__ bucket_q,
-                                                                  const __half *__restrict__ pt,
-                                                                  const int32_t *__restrict__ pt_off, int nbk,
-                                                                  float *__restrict__ kla)
-{
-    const long long n_groups = pt_off[nbk] / 8;
-    const long long g0 = (long long)blockIdx.x * kEntGroups;
-    if (g0 >= n_groups) return;
-    __shared__ float part[kEntGroups / 2][8][8];     // [group pair][warp][entry]
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int half = threadIdx.x >> 7, key = threadIdx.x & 127;
-    uint4 raw[kEntGroups / 2];
-#pragma unroll
-    for (int j = 0; j < kEntGroups / 2; ++j) {
-        const long long g = g0 + 2 * j + half;       // this thread's groups: every other one
-        raw[j] = g < n_groups ? __ldg(reinterpret_cast<const uint4 *>(pt + g * 8 * 128 + key * 8))
-                              : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int j = 0; j < kEntGroups / 2; ++j) {
-        float v[8];
-        const __half2 *h = reinterpret_cast<const __half2 *>(&raw[j]);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float2 f = __half22float2(h[e]);
-            v[2 * e] = f.x > 0.f ? f.x * __log2f(f.x) : 0.f;
-            v[2 * e + 1] = f.y > 0.f ? f.y * __log2f(f.y) : 0.f;
-        }
-        float tot[1];
-        lane_colsum(v, lane, tot);                   // lane l: entry l % 8 of the warp's 32 keys
-        if (lane < 8) part[j][warp][lane] = tot[0];
-    }
-    __syncthreads();
-    // one entry per thread: group gl = 2 j + half of the CTA, entry e
-    const int gl = threadIdx.x >> 3, e = threadIdx.x & 7;
-    const long long g = g0 + gl;
-    if (g >= n_groups) return;
-    const int j = gl >> 1, hh = gl & 1;
-    const float a = (part[j][4 * hh][e] + part[j][4 * hh + 1][e]) + (part[j][4 * hh + 2][e] + part[j][4 * hh + 3][e]);
-    const long long flat = g * 8 + e;
-    int lo = 0, hi = nbk;                            // the last bucket starting at or before `flat`
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (pt_off[mid] <= flat) lo = mid;
-        else hi = mid;
-    }
-    const int t = (int)(flat - pt_off[lo]);
-    if (t >= bucket_off[lo + 1] - bucket_off[lo]) return;   // padding entry of the bucket's last group
-    const int ent = bucket_q[bucket_off[lo] + t];
-    const long long br = lo / p.nb;                  // b * Hkv + r
-    kla[(br * p.Nq + entry_row(ent)) * p.topk + entry_slot(ent)] = a;
-}
-
-// pt_off[x] = sum over buckets y < x of cnt[y] rounded up to 8 (x = 0..n),
-// single CTA of 1024 threads
-__global__ void __launch_bounds__(1024) bwd_pad_scan_kernel(const int32_t *__restrict__ cnt,
-                                                            int32_t *__restrict__ off, int n)
-{
-    __shared__ int part[1024];
-    const int per = (n + 1023) / 1024;
-    const int lo = threadIdx.x * per, hi = min(n, lo + per);
-    int s = 0;
-    for (int x = lo; x < hi; ++x) s += (cnt[x] + 7) & ~7;
-    part[threadIdx.x] = s;
-    __syncthreads();
-    for (int d = 1; d < 1024; d <<= 1) {
-        const int v = threadIdx.x >= (unsigned)d ? part[threadIdx.x - d] : 0;
-        __syncthreads();
-        part[threadIdx.x] += v;
-        __syncthreads();
-    }
-    int run = threadIdx.x ? part[threadIdx.x - 1] : 0;
-    for (int x = lo; x < hi; ++x) {
-        off[x] = run;
-        run += (cnt[x] + 7) & ~7;
-    }
-    if (threadIdx.x == 1023) off[n] = part[1023];
-}
-
 __global__ void f32_to_bf16_kernel(const float *__restrict__ src, bf16 *__restrict__ dst, long long n)
 {
     for (long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x; x < n / 2; x += (long long)gridDim.x * blockDim.x) {
@@ -671,8 +577,8 @@ cudaError_t launch_fused_bwd(const Problem &p, const bf16 *q, const bf16 *k, con
     if (!tc) {
         if ((e = cudaMemsetAsync(w.dq_acc, 0, n_dq * 4, s)) != cudaSuccess) return e;
         if ((e = cudaMemsetAsync(w.dqi_acc, 0, n_dqi * 4, s)) != cudaSuccess) return e;
+        if ((e = cudaMemsetAsync(w.dki_acc, 0, n_dki * 4, s)) != cudaSuccess) return e;
     }
-    if ((e = cudaMemsetAsync(w.dki_acc, 0, n_dki * 4, s)) != cudaSuccess) return e;
 
     const long long rows = (long long)p.B * p.Nq * p.Hq;
     if (!w.D_ready) {
@@ -688,26 +594,14 @@ cudaError_t launch_fused_bwd(const Problem &p, const bf16 *q, const bf16 *k, con
         return e;
 
     if (tc) {
-        {
-            TimedLaunch timed_("bwd_pad_scan_kernel", s);
-            bwd_pad_scan_kernel<<<1, 1024, 0, s>>>(w.bucket_cnt, w.pt_off, (int)((long long)p.B * p.Hkv * p.nb));
-        }
-        note_launch();
-        // main branch first: it leaves the teacher per (bucket entry, key) for the index branch
+        // main branch: dK, dV and the dQ partial rows
         if ((e = launch_bwd_main_tc(p, q, k, v, d_o, lse, w, dk, dv, st, s)) != cudaSuccess) return e;
-        if ((e = launch_bwd_index_tc(p, q_idx, k_idx, lse_idx, kl_coef, w, st, s)) != cudaSuccess) return e;
-        if (w.kla) {
-            {
-                TimedLaunch timed_("bwd_teacher_entropy_kernel", s);
-                // an upper bound of the padded entries: every (row, slot) once, plus < 8 per bucket
-                const int nbk = (int)((long long)p.B * p.Hkv * p.nb);
-                const long long max_groups = ((long long)p.B * p.Nq * p.Hkv * p.topk + 8LL * nbk) / 8;
-                bwd_teacher_entropy_kernel<<<(unsigned)((max_groups + kEntGroups - 1) / kEntGroups), 256, 0, s>>>(
-                    p, w.bucket_off, w.bucket_q, w.pt, w.pt_off, nbk, w.kla);
-            }
-            note_launch();
-            if ((e = launch_bwd_kl_combine(p, sel, lse_idx, w.kla, w.klb, w.kl_rows, s)) != cudaSuccess) return e;
-        }
+        // index branch: the teacher rebuilt from its own logit tiles next to the index
+        // scores; dq_idx partial rows, each group's dK_idx share and the KL loss terms
+        if ((e = launch_index_teacher_tc(p, q, k, q_idx, k_idx, lse, lse_idx, kl_coef, w.bucket_off, w.bucket_q, w.klt,
+                                         w.dqi_part, w.dki_acc, st, s)) != cudaSuccess)
+            return e;
+        if (w.klt && (e = launch_kl_rows_combine(p, sel, lse_idx, w.klt, w.kl_rows, s)) != cudaSuccess) return e;
         {
             TimedLaunch timed_("bwd_combine_kernel", s);
             bwd_combine_kernel<128><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p, sel, w.dq_part, dq, p.Hq, p.G);
@@ -719,6 +613,8 @@ cudaError_t launch_fused_bwd(const Problem &p, const bf16 *q, const bf16 *k, con
             bwd_combine_kernel<128><<<(unsigned)((rows_i + 7) / 8), 256, 0, s>>>(p, sel, w.dqi_part, dq_idx, p.Hkv, 1);
         }
         note_launch();
+        if ((e = launch_dki_group_sum(p, w.dki_acc, dk_idx, s)) != cudaSuccess) return e;
+        return cudaGetLastError();
     } else {
         if (p.d == 128) e = launch_main<128, 64>(p, q, k, v, d_o, lse, q_idx, k_idx, lse_idx, kl_coef, w, dk, dv, s);
         else if (p.d_idx == 128) e = launch_main<64, 128>(p, q, k, v, d_o, lse, q_idx, k_idx, lse_idx, kl_coef, w, dk, dv, s);

@@ -5,7 +5,10 @@
 // query rows [t*kRowsPerCta, (t+1)*kRowsPerCta) and histograms their selected
 // blocks in shared memory; a scan kernel turns the per-CTA histograms into
 // each CTA's write offset inside each bucket (and the bucket offsets), and
-// the fill kernel replays the same rows with shared-memory cursors.  Entries
+// the fill kernel replays the same rows with shared-memory cursors, in row
+// order: every bucket lists its queries in ascending row order, the same on
+// every run, so the key-major kernels accumulate dK, dV and dK_idx in a fixed
+// order and the gradients are reproducible bit for bit.  Entries
 // that are not a valid selection for their row (a block after the query's
 // own, or beyond the keys) are reported through the status word and skipped.
 // Each list entry packs the query row with the slot of the block in that
@@ -89,6 +92,11 @@ __global__ void __launch_bounds__(1024) index_bucket_scan_kernel(const int32_t *
     if (threadIdx.x == 1023) off[n] = part[1023];
 }
 
+// The CTA's (row, slot) entries are taken in rounds of kThreads consecutive
+// entries.  Within a warp the lanes holding the same block are ranked by
+// lane (__match_any_sync), and the warps of a round claim their cursor
+// ranges one after another, so entries land in entry order -- row order,
+// since a row selects a block at most once.
 __global__ void __launch_bounds__(kThreads) index_fill_kernel(Problem p, const int32_t *__restrict__ sel, int nct,
                                                               const int32_t *__restrict__ cta_base,
                                                               const int32_t *__restrict__ off,
@@ -96,17 +104,37 @@ __global__ void __launch_bounds__(kThreads) index_fill_kernel(Problem p, const i
 {
     extern __shared__ int32_t cursor[];
     const int t = blockIdx.x, br = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int32_t *cb = cta_base + ((long long)br * nct + t) * p.nb;
     const int32_t *ob = off + (long long)br * p.nb;
     for (int c = threadIdx.x; c < p.nb; c += kThreads) cursor[c] = ob[c] + cb[c];
     __syncthreads();
     const int i0 = t * kRowsPerCta, i1 = min(p.Nq, i0 + kRowsPerCta);
     const int32_t *base = sel + (long long)br * p.Nq * p.topk;
-    for (long long x = (long long)i0 * p.topk + threadIdx.x; x < (long long)i1 * p.topk; x += kThreads) {
-        const int c = base[x];
-        const int i = (int)(x / p.topk);
-        if (!valid_sel(p, c, i)) continue;
-        list[atomicAdd(&cursor[c], 1)] = pack_entry(i, (int)(x % p.topk));
+    const long long x1 = (long long)i1 * p.topk;
+    for (long long xb = (long long)i0 * p.topk; xb < x1; xb += kThreads) {
+        const long long x = xb + threadIdx.x;
+        int c = -1, i = 0;
+        if (x < x1) {
+            c = base[x];
+            i = (int)(x / p.topk);
+            if (!valid_sel(p, c, i)) c = -1;
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, c);
+        const int leader = __ffs(peers) - 1;
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        for (int w = 0; w < kThreads / 32; ++w) {
+            if (warp == w) {
+                int start = 0;
+                if (c >= 0 && lane == leader) {
+                    start = cursor[c];
+                    cursor[c] = start + __popc(peers);
+                }
+                start = __shfl_sync(0xffffffffu, start, leader);
+                if (c >= 0) list[start + rank] = pack_entry(i, (int)(x % p.topk));
+            }
+            __syncthreads();
+        }
     }
 }
 

@@ -103,40 +103,51 @@ cudaError_t launch_kl_fwd(const Problem &p, const bf16 *q, const bf16 *k, const 
                           float *kl_rows, DeviceStatus *st, cudaStream_t s);
 // Key-major KL forward (many queries per selected block).
 struct KlWork {
-    float4 *part;        // [B, Hkv, Nq, topk, kl_part_count / (B*Hkv*Nq*topk)] partial sums
-    __half *pt;          // [B*Hkv*Nq*topk entries, 128] teacher per (bucket entry, key); nullptr: lse_idx only
+    float2 *part;        // [B, Hkv, Nq, topk, 2] (max s log2 e, sum 2^(s log2 e - max)) per key half
+    float *klt;          // [B*Hkv*Nq*topk, 4] sums of Pt (log2 Pt - s log2 e) per lane quarter of the
+                         // block's keys (teacher terms, d = d_idx = 128); nullptr: lse_idx only
     int32_t *bucket_cnt, *bucket_off, *bucket_scratch, *bucket_q;
     bool index_ready = false;
 };
-// float4 partials the key-major KL writes (several per (query, group, slot))
+// float2 partials the key-major KL's index pass writes (two per (query, group, slot))
 size_t kl_part_count(const Problem &p);
+// lse_idx (index pass + combine) and, with w.klt and kl_rows set, the KL rows
+// from the teacher terms of launch_index_teacher_tc (d = d_idx = 128 only)
 cudaError_t launch_kl_keymajor(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *q_idx, const bf16 *k_idx,
                                const int32_t *sel, const float *lse, float *lse_idx, float *kl_rows, const KlWork &w,
                                DeviceStatus *st, cudaStream_t s);
 cudaError_t launch_kl_reduce(const Problem &p, const float *kl_rows, float kl_coef, float *kl_loss,
                              cudaStream_t s);
-// KL rows from the fused backward's partials (BwdWork::kla / klb) and lse_idx
-cudaError_t launch_bwd_kl_combine(const Problem &p, const int32_t *sel, const float *lse_idx, const float *kla,
-                                  const float *klb, float *kl_rows, cudaStream_t s);
+// The KL's teacher terms and (dqi_part set) the index-branch backward,
+// key-major on the tcgen05 tensor cores (d = d_idx = 128), the teacher
+// recomputed from its own logit tiles: per (query, group, slot) klt (4 floats,
+// nullable) and, for the backward, dq_idx partial rows in dqi_part and each
+// group's fp32 dK_idx share in dki_g [B, Hkv, Nk, d_idx].
+cudaError_t launch_index_teacher_tc(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *q_idx,
+                                    const bf16 *k_idx, const float *lse, const float *lse_idx, float kl_coef,
+                                    const int32_t *bucket_off, const int32_t *bucket_q, float *klt, bf16 *dqi_part,
+                                    float *dki_g, DeviceStatus *st, cudaStream_t s);
+// KL rows = ln 2 * (sum of a row's klt over its valid slots) + lse_idx
+cudaError_t launch_kl_rows_combine(const Problem &p, const int32_t *sel, const float *lse_idx, const float *klt,
+                                   float *kl_rows, cudaStream_t s);
+// dk_idx = bf16 of the sum over groups, in order, of dki_g
+cudaError_t launch_dki_group_sum(const Problem &p, const float *dki_g, bf16 *dk_idx, cudaStream_t s);
 
 // Backward pieces.  Workspace carve-up is done by the caller (api.cu).
 struct BwdWork {
     float *D;            // [B, Hq, Nq]    rowsum(dO * O)
     float *dq_acc;       // [B, Nq, Hq, d]  fp32 accumulators (mma.sync path)
     float *dqi_acc;      // [B, Nq, Hkv, d_idx]              (mma.sync path)
-    float *dki_acc;      // [B, Nk, d_idx]
+    // dK_idx: [B, Nk, d_idx] fp32 accumulators (mma.sync path) or each group's
+    // share [B, Hkv, Nk, d_idx], summed over the groups in order (tcgen05 path)
+    float *dki_acc;
     bf16 *dq_part;       // [B, Nq, Hq, topk, d]      dQ per selected block (tcgen05 path)
     bf16 *dqi_part;      // [B, Nq, Hkv, topk, d_idx] dq_idx per selected block (tcgen05 path)
-    // teacher per (bucket entry, key), key-major within groups of 8 entries of a
-    // bucket: entry t of bucket x at [(pt_off[x] + (t & ~7)) * 128 + key * 8 + (t & 7)]
-    // (tcgen05 path); pt_off[x] = sum over earlier buckets of their counts rounded up to 8
-    __half *pt;
-    int32_t *pt_off;     // [B*Hkv*nb + 1]
-    // KL loss terms per ((b, r, query), slot) (tcgen05 path; nullptr when the
-    // loss is not asked for): kla = sum Pt log2 Pt over the block's keys (one
-    // float), klb = sum Pt s log2(e) per lane quarter of the keys (four floats)
-    float *kla, *klb;
-    float *kl_rows;      // [B, Hkv, Nq] KL rows assembled from kla / klb (when kla is set)
+    // KL loss terms per ((b, r, query), slot), four floats (tcgen05 path; nullptr
+    // when the loss is not asked for): sums of Pt (log2 Pt - s log2 e) per lane
+    // quarter of the block's keys
+    float *klt;
+    float *kl_rows;      // [B, Hkv, Nq] KL rows assembled from klt (when klt is set)
     int32_t *bucket_cnt; // [B*Hkv*nb]
     int32_t *bucket_off; // [B*Hkv*nb + 1]
     int32_t *bucket_scratch; // inverse_index_scratch_ints(p)
@@ -163,12 +174,9 @@ cudaError_t launch_inverse_index(const Problem &p, const int32_t *sel, int32_t *
 
 // The backward runs on the tcgen05 kernels when d = d_idx = 128.
 inline bool bwd_tc(const Problem &p) { return p.d == 128 && p.d_idx == 128; }
-// tcgen05 main-branch backward (d = 128): dK, dV, dQ partials, teacher per entry.
+// tcgen05 main-branch backward (d = 128): dK, dV and the dQ partials.
 cudaError_t launch_bwd_main_tc(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *v, const bf16 *d_o,
                                const float *lse, const BwdWork &w, bf16 *dk, bf16 *dv, DeviceStatus *st,
                                cudaStream_t s);
-// tcgen05 index-branch backward (d_idx = 128): dq_idx partials, dK_idx into w.dki_acc.
-cudaError_t launch_bwd_index_tc(const Problem &p, const bf16 *q_idx, const bf16 *k_idx, const float *lse_idx,
-                                float kl_coef, const BwdWork &w, DeviceStatus *st, cudaStream_t s);
 
 }  // namespace msa

@@ -91,6 +91,16 @@ MSA_DEV void prefetch_tmap(const CUtensorMap *map)
 {
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
+// Bring a 4-D tile into L2 (no shared-memory destination, no completion to
+// wait for): a later tile load of the same box then hits L2.
+MSA_DEV void tma_prefetch_4d(const CUtensorMap *map, int x, int y, int z, int w)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];\n" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z), "r"(w)
+                 : "memory");
+}
+MSA_DEV void prefetch_l2(const void *gmem) { asm volatile("prefetch.global.L2 [%0];\n" ::"l"(gmem)); }
 
 // ------------------------------------------------------------------ TMEM
 // Allocation is warp-wide; the allocated column base is written to smem.

@@ -30,8 +30,9 @@ def pytest_collection_modifyitems(config, items):
 
 def pytest_terminal_summary(terminalreporter, exitstatus, config):
     """Raw errors of every tolerance comparison made in this run (passing ones
-    included): test, tensor, max-abs, max-abs beyond the bf16 rounding
-    allowance of entries >= 8, relative L2."""
+    included): test, tensor, raw max-abs, max-abs beyond the output's bf16
+    rounding, relative L2, and the exact value and the result at the worst
+    entry."""
     try:
         from msa_testutil import RECORD
     except Exception:  # pragma: no cover
@@ -40,5 +41,6 @@ def pytest_terminal_summary(terminalreporter, exitstatus, config):
         return
     tr = terminalreporter
     tr.section("parity errors (raw)")
-    for test, name, ma, ma_arith, rl in RECORD:
-        tr.write_line(f"{test} | {name} | max-abs {ma:.3e} | beyond-rounding {ma_arith:.3e} | rel-L2 {rl:.3e}")
+    for test, name, ma, ma_arith, rl, w_at, g_at in RECORD:
+        tr.write_line(f"{test} | {name} | max-abs {ma:.3e} | beyond-rounding {ma_arith:.3e} | rel-L2 {rl:.3e} | "
+                      f"worst entry exact {w_at:.6g} got {g_at:.6g}")

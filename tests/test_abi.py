@@ -136,3 +136,22 @@ def test_product_path_has_no_oracle_or_fallback():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "msa_oracle" not in text, f
+
+
+def test_backward_workspace_holds_no_distribution(libmsa):
+    """The fused backward's workspace (d = d_idx = 128, the tensor-core path)
+    is D, one fp32 dK_idx share per group, the inverse index and the per-slot
+    dQ / dq_idx partial rows -- nothing per (slot, key): the teacher is rebuilt
+    on chip and never stored.  With the KL loss, four floats per slot more."""
+    from block_sparse_gqa_causal_gb300 import api
+    B, N, Hq, Hkv, d, k = 1, 131072, 64, 8, 128, 16
+    sh = api.Shape(B=B, Nq=N, Nk=N, Hq=Hq, Hkv=Hkv, d=d, d_idx=d, topk=k)
+    a = lambda x: (x + 255) // 256 * 256
+    nb = N // 128
+    nct = (N + 511) // 512
+    index = 2 * a((B * Hkv * nb + 1) * 4) + a(2 * B * Hkv * nct * nb * 4) + a(B * Hkv * N * k * 4)
+    slots = B * N * k
+    want = (256 + a(B * Hq * N * 4) + a(B * Hkv * N * d * 4) + index + a(slots * Hq * d * 2)
+            + a(slots * Hkv * d * 2))
+    assert api.workspace_size(sh, api.OP_FUSED_BWD) == want
+    assert api.workspace_size(sh, api.OP_FUSED_BWD_KL) == want + a(B * Hkv * N * 4) + a(slots * Hkv * 16)

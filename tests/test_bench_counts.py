@@ -67,7 +67,7 @@ def test_kernel_work_design_slot_counts():
     buckets = w.B * w.Hkv * w.nb
     G, d = w.G, w.d
     assert work["bwd_main_tc_kernel"]["design_bytes"] == pytest.approx(
-        slots * (2 * G * d * 2 + G * d * 2 + 256 + 8 * G) + buckets * 4 * 128 * d * 2, rel=1e-12)
+        slots * (2 * G * d * 2 + G * d * 2 + 8 * G) + buckets * 4 * 128 * d * 2, rel=1e-12)
     assert work["sparse_fwd_tc_kernel"]["design_bytes"] / 1e9 == pytest.approx(69.82, abs=0.01)
 
 

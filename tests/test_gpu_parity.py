@@ -354,3 +354,31 @@ def test_index_select_large_k_parity(k):
         # statistics of ~30 block scores are ~0.03 apart, so a few percent of
         # rows fall within the 1e-3 gap
         assert tol <= 0.1 * (exact + tol) + 2
+
+
+TC_TRAIN_CASES = [c for c in TRAIN_CASES if c[7] == 128 and c[8] == 128]
+
+
+@pytest.mark.parametrize("case", TC_TRAIN_CASES, ids=[c[0] for c in TC_TRAIN_CASES])
+def test_tensor_core_backward_is_reproducible_bit_for_bit(case):
+    """With d = d_idx = 128 the backward has no atomics: the inverse index
+    lists each block's queries in row order, dK and dV accumulate in TMEM in
+    that order, dK_idx is summed over the groups in a fixed order and the dQ /
+    dq_idx partial rows are combined in slot order.  Two training steps give
+    the same bits, and msa_fused_bwd_kl gives msa_fused_bwd's gradients."""
+    import torch
+    from block_sparse_gqa_causal_gb300 import api
+    x, osh, res = run_case(case)
+    name, B, Nq, Nk, qo, Hq, Hkv, d, di, k = case
+    sh = api.Shape(B=B, Nq=Nq, Nk=Nk, Hq=Hq, Hkv=Hkv, d=d, d_idx=di, topk=k, q_offset=qo)
+    t = {n: to_torch(a) for n, a in x.items()}
+    a = api.train_step(sh, t["q"], t["k"], t["v"], t["q_idx"], t["k_idx"], t["d_o"], 0.75)
+    b = api.train_step(sh, t["q"], t["k"], t["v"], t["q_idx"], t["k_idx"], t["d_o"], 0.75)
+    torch.cuda.synchronize()
+    for n in a:
+        assert torch.equal(a[n], b[n]), n
+    assert np.array_equal(res["lse_idx"], res["lse_idx_only"])
+    for g, ref, n in zip(res["grads_kl"], res["grads"], ("dq", "dk", "dv", "dq_idx", "dk_idx")):
+        assert np.array_equal(g, ref), n
+    for n, ref in zip(("dq", "dk", "dv", "dq_idx", "dk_idx"), res["grads"]):
+        assert np.array_equal(bf16_to_np(a[n]), ref), n + " (train_step vs fused_bwd)"
