@@ -9,6 +9,10 @@ with the CUDA library.
 Two builds of the same source: liboracle_bf16.so takes bf16 bit patterns
 (uint16), liboracle_f64.so takes float64 inputs (finite-difference checks).
 
+Also: the index projections of the detached hidden states (section 3.2's
+detachment equation) with their weight gradient, and the dense indexer
+warm-up loss (section 3.1) with its gradient in the index inputs.
+
 Parity pins (tests/test_oracle.py): brute-force block max-pool and a full
 sort for selection; the block-mask word of section 4.3's worked example
 (tests/golden/) and set unions for the mask and its traversal; dense causal GQA attention when every visible block is
@@ -94,8 +98,13 @@ def _lib(kind: str):
             lib.orc_bwd_keys.argtypes = [S, P, P, P, P, P, P, P, d, i, P, P, P, P]
             lib.orc_block_mask.argtypes = [S, P, P]
             lib.orc_mask_walk.argtypes = [P, i, P]
+            lib.orc_index_proj.argtypes = [i, i, i, i, P, P, P, P, P]
+            lib.orc_index_proj_bwd.argtypes = [i, i, i, i, P, P, P, P, P]
+            lib.orc_warmup_kl.argtypes = [S, P, P, P, P, i, P, P, P]
+            lib.orc_warmup_grad.argtypes = [S, P, P, P, P, d, P, P]
             for f in ("orc_block_scores", "orc_select", "orc_sparse_fwd", "orc_kl", "orc_bwd_rows", "orc_bwd_keys",
-                      "orc_block_mask", "orc_mask_walk", "orc_num_threads"):
+                      "orc_block_mask", "orc_mask_walk", "orc_num_threads", "orc_index_proj", "orc_index_proj_bwd",
+                      "orc_warmup_kl", "orc_warmup_grad"):
                 getattr(lib, f).restype = ctypes.c_int
             _loaded[kind] = lib
         return _loaded[kind]
@@ -250,3 +259,54 @@ def bwd_keys(shape: Shape, q, k, v, d_o, q_idx, k_idx, sel_full, kl_coef: float 
     if rc != 0:
         raise MemoryError("oracle could not allocate its partial buffers")
     return dk, dv, dki
+
+
+def index_proj(X, Wq, Wk, Hkv: int, d_idx: int):
+    """q_idx [T, Hkv*d_idx] and k_idx [T, d_idx] (float64) of X [T, Dm]."""
+    X, Wq, Wk = (_c(a, a.dtype) for a in (X, Wq, Wk))
+    kind = _kind(X, Wq, Wk)
+    T, Dm = X.shape
+    qi = np.empty((T, Hkv * d_idx), dtype=np.float64)
+    ki = np.empty((T, d_idx), dtype=np.float64)
+    _lib(kind).orc_index_proj(T, Dm, Hkv, d_idx, _in(X), _in(Wq), _in(Wk), _in(qi), _in(ki))
+    return qi, ki
+
+
+def index_proj_bwd(X, dq_idx, dk_idx, Hkv: int, d_idx: int):
+    """dWq [Dm, Hkv*d_idx] and dWk [Dm, d_idx] (float64); no gradient into X."""
+    X = _c(X, X.dtype)
+    dq_idx = _c(np.asarray(dq_idx).reshape(X.shape[0], Hkv * d_idx), X.dtype)
+    dk_idx = _c(np.asarray(dk_idx).reshape(X.shape[0], d_idx), X.dtype)
+    kind = _kind(X, dq_idx, dk_idx)
+    T, Dm = X.shape
+    dWq = np.empty((Dm, Hkv * d_idx), dtype=np.float64)
+    dWk = np.empty((Dm, d_idx), dtype=np.float64)
+    _lib(kind).orc_index_proj_bwd(T, Dm, Hkv, d_idx, _in(X), _in(dq_idx), _in(dk_idx), _in(dWq), _in(dWk))
+    return dWq, dWk
+
+
+def warmup_kl(shape: Shape, q, k, q_idx, k_idx, rows=None):
+    """Dense warm-up KL per (row, group) over the whole visible prefix, and
+    the index log-sum-exp, float64 [n_rows, Hkv]."""
+    rows = _rows(shape, rows)
+    q, k, q_idx, k_idx = (_c(a, a.dtype) for a in (q, k, q_idx, k_idx))
+    kind = _kind(q, k, q_idx, k_idx)
+    lse_idx = np.empty((len(rows), shape.Hkv), dtype=np.float64)
+    kl_rows = np.empty((len(rows), shape.Hkv), dtype=np.float64)
+    sh = shape.c()
+    _lib(kind).orc_warmup_kl(ctypes.byref(sh), _in(q), _in(k), _in(q_idx), _in(k_idx), len(rows), _in(rows),
+                             _in(lse_idx), _in(kl_rows))
+    return lse_idx, kl_rows
+
+
+def warmup_grad(shape: Shape, q, k, q_idx, k_idx, kl_coef: float = 1.0):
+    """Gradient of the dense warm-up loss kl_coef/(B Nq Hkv) * sum of rows in
+    the index inputs: dq_idx [B, Nq, Hkv, d_idx], dk_idx [B, Nk, d_idx]."""
+    q, k, q_idx, k_idx = (_c(a, a.dtype) for a in (q, k, q_idx, k_idx))
+    kind = _kind(q, k, q_idx, k_idx)
+    dqi = np.empty((shape.B, shape.Nq, shape.Hkv, shape.d_idx), dtype=np.float64)
+    dki = np.empty((shape.B, shape.Nk, shape.d_idx), dtype=np.float64)
+    sh = shape.c()
+    _lib(kind).orc_warmup_grad(ctypes.byref(sh), _in(q), _in(k), _in(q_idx), _in(k_idx), float(kl_coef), _in(dqi),
+                               _in(dki))
+    return dqi, dki

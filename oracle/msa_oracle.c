@@ -13,6 +13,10 @@
  * values, so that selection ties and near-ties are decided the same way a
  * fp32 implementation decides them.
  *
+ * Also here: the index projections of the detached hidden states and their
+ * weight gradient (the detachment equation of section 3.2), and the dense
+ * indexer warm-up loss of section 3.1 with its gradient.
+ *
  * No blocking, fusion or reordering beyond the definition: every function
  * walks queries, heads and tokens in the obvious order.  Parallelism is an
  * OpenMP loop over independent (row, group) or (batch, group, chunk) items.
@@ -547,6 +551,165 @@ int orc_mask_walk(const uint32_t *words, int n_words, int32_t *out)
         for (int rank = 0; rank < count; ++rank) out[n++] = 32 * w + nth_set_bit(words[w], rank);
     }
     return n;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Index projections (section 3.2, the detachment equation): the index
+ * queries and keys are linear maps of the detached hidden states X,
+ *   q_idx[t, r, e] = sum_m X[t, m] Wq[m, r*d_idx + e]
+ *   k_idx[t, e]    = sum_m X[t, m] Wk[m, e]
+ * X [T, Dm] (T = B*N tokens), Wq [Dm, Hkv*d_idx], Wk [Dm, d_idx]; outputs
+ * fp64, q_idx [T, Hkv*d_idx], k_idx [T, d_idx].                            */
+int orc_index_proj(int T, int Dm, int Hkv, int d_idx, const orc_in *X, const orc_in *Wq, const orc_in *Wk,
+                   double *q_idx, double *k_idx)
+{
+    const int nq = Hkv * d_idx;
+    #pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t) {
+        for (int c = 0; c < nq; ++c) {
+            double acc = 0.0;
+            for (int m = 0; m < Dm; ++m) acc += bfv(X[(long long)t * Dm + m]) * bfv(Wq[(long long)m * nq + c]);
+            q_idx[(long long)t * nq + c] = acc;
+        }
+        for (int e = 0; e < d_idx; ++e) {
+            double acc = 0.0;
+            for (int m = 0; m < Dm; ++m) acc += bfv(X[(long long)t * Dm + m]) * bfv(Wk[(long long)m * d_idx + e]);
+            k_idx[(long long)t * d_idx + e] = acc;
+        }
+    }
+    return 0;
+}
+
+/* Gradient of the projections in their weights.  X is detached (stopgrad),
+ * so nothing flows into it; the weights collect
+ *   dWq[m, c] = sum_t X[t, m] dq_idx[t, c],   dWk[m, e] = sum_t X[t, m] dk_idx[t, e].
+ * dq_idx [T, Hkv*d_idx], dk_idx [T, d_idx] (inputs); dWq [Dm, Hkv*d_idx],
+ * dWk [Dm, d_idx] fp64.                                                     */
+int orc_index_proj_bwd(int T, int Dm, int Hkv, int d_idx, const orc_in *X, const orc_in *dq_idx,
+                       const orc_in *dk_idx, double *dWq, double *dWk)
+{
+    const int nq = Hkv * d_idx;
+    #pragma omp parallel for schedule(static)
+    for (int m = 0; m < Dm; ++m) {
+        for (int c = 0; c < nq; ++c) {
+            double acc = 0.0;
+            for (int t = 0; t < T; ++t) acc += bfv(X[(long long)t * Dm + m]) * bfv(dq_idx[(long long)t * nq + c]);
+            dWq[(long long)m * nq + c] = acc;
+        }
+        for (int e = 0; e < d_idx; ++e) {
+            double acc = 0.0;
+            for (int t = 0; t < T; ++t) acc += bfv(X[(long long)t * Dm + m]) * bfv(dk_idx[(long long)t * d_idx + e]);
+            dWk[(long long)m * d_idx + e] = acc;
+        }
+    }
+    return 0;
+}
+
+/* Dense indexer warm-up (section 3.1, the warm-up loss, in MSA's per-group
+ * form of section 3.2): for query i and group r over EVERY causally visible
+ * key j <= pos (no blocks, no selection),
+ *   teacher  p_j = (1/G) sum over the group's heads h of softmax_j(scale q_h . k_j)
+ *   student  s_j = softmax_j(scale_idx q_idx . k_idx_j)
+ *   kl = sum_j p_j (log p_j - log s_j),  lse_idx = log sum_j exp(scale_idx q_idx . k_idx_j).
+ * Requires q_offset == 0 and Nq == Nk (a training sequence).              */
+int orc_warmup_kl(const orc_shape *s, const orc_in *q, const orc_in *k, const orc_in *q_idx, const orc_in *k_idx,
+                  int n_rows, const long long *rows, double *out_lse_idx, double *out_kl)
+{
+    const int G = s->Hq / s->Hkv;
+    const long long KR = kvrows(s);
+    #pragma omp parallel
+    {
+        double *lg = (double *)malloc(sizeof(double) * (size_t)s->Nk);
+        double *p = (double *)malloc(sizeof(double) * (size_t)s->Nk);
+        double *pt = (double *)malloc(sizeof(double) * (size_t)s->Nk);
+        double *ps = (double *)malloc(sizeof(double) * (size_t)s->Nk);
+        #pragma omp for schedule(dynamic, 1)
+        for (long long t = 0; t < (long long)n_rows * s->Hkv; ++t) {
+            const long long row = rows[t / s->Hkv];
+            const int r = (int)(t % s->Hkv);
+            const int b = (int)(row / s->Nq), i = (int)(row % s->Nq);
+            const int n = i + 1;                         /* keys 0 .. i */
+            for (int j = 0; j < n; ++j) pt[j] = 0.0;
+            for (int g = 0; g < G; ++g) {
+                const orc_in *qh = q + (((long long)b * s->Nq + i) * s->Hq + r * G + g) * s->d;
+                for (int j = 0; j < n; ++j)
+                    lg[j] = s->scale * dot_bf(qh, k + (((long long)b * KR + j) * s->Hkv + r) * s->d, s->d);
+                softmax_lse(lg, n, p);
+                for (int j = 0; j < n; ++j) pt[j] += p[j] / G;
+            }
+            const orc_in *qi = q_idx + (((long long)b * s->Nq + i) * s->Hkv + r) * s->d_idx;
+            for (int j = 0; j < n; ++j)
+                lg[j] = s->scale_idx * dot_bf(qi, k_idx + ((long long)b * KR + j) * s->d_idx, s->d_idx);
+            out_lse_idx[t] = softmax_lse(lg, n, ps);
+            double kl = 0.0;
+            for (int j = 0; j < n; ++j)
+                if (pt[j] > 0.0) kl += pt[j] * (log(pt[j]) - log(ps[j]));
+            out_kl[t] = kl;
+        }
+        free(lg); free(p); free(pt); free(ps);
+    }
+    return 0;
+}
+
+/* Gradient of L_warm = kl_coef / (B Nq Hkv) * sum of the rows' kl in the
+ * index inputs (the teacher is detached): with dsig_j = coef (s_j - p_j),
+ *   dq_idx[b, i, r, :] = scale_idx sum_j dsig_j k_idx[b, j, :]
+ *   dk_idx[b, j, :]   += scale_idx dsig_j q_idx[b, i, r, :]
+ * dq_idx [B, Nq, Hkv, d_idx], dk_idx [B, Nk, d_idx] fp64 (overwritten).
+ * Rows are taken one (b, group) at a time so the dk_idx sums are formed in
+ * a fixed order per thread and added under a lock.                         */
+int orc_warmup_grad(const orc_shape *s, const orc_in *q, const orc_in *k, const orc_in *q_idx,
+                    const orc_in *k_idx, double kl_coef, double *dq_idx, double *dk_idx)
+{
+    const int G = s->Hq / s->Hkv;
+    const long long KR = kvrows(s);
+    const double coef = kl_coef / ((double)s->B * s->Nq * s->Hkv);
+    memset(dk_idx, 0, sizeof(double) * (size_t)s->B * s->Nk * s->d_idx);
+    #pragma omp parallel
+    {
+        double *lg = (double *)malloc(sizeof(double) * (size_t)s->Nk);
+        double *p = (double *)malloc(sizeof(double) * (size_t)s->Nk);
+        double *pt = (double *)malloc(sizeof(double) * (size_t)s->Nk);
+        double *ps = (double *)malloc(sizeof(double) * (size_t)s->Nk);
+        double *dki = (double *)malloc(sizeof(double) * (size_t)s->Nk * s->d_idx);
+        #pragma omp for schedule(dynamic, 1)
+        for (int br = 0; br < s->B * s->Hkv; ++br) {
+            const int b = br / s->Hkv, r = br % s->Hkv;
+            memset(dki, 0, sizeof(double) * (size_t)s->Nk * s->d_idx);
+            for (int i = 0; i < s->Nq; ++i) {
+                const int n = i + 1;
+                for (int j = 0; j < n; ++j) pt[j] = 0.0;
+                for (int g = 0; g < G; ++g) {
+                    const orc_in *qh = q + (((long long)b * s->Nq + i) * s->Hq + r * G + g) * s->d;
+                    for (int j = 0; j < n; ++j)
+                        lg[j] = s->scale * dot_bf(qh, k + (((long long)b * KR + j) * s->Hkv + r) * s->d, s->d);
+                    softmax_lse(lg, n, p);
+                    for (int j = 0; j < n; ++j) pt[j] += p[j] / G;
+                }
+                const orc_in *qi = q_idx + (((long long)b * s->Nq + i) * s->Hkv + r) * s->d_idx;
+                for (int j = 0; j < n; ++j)
+                    lg[j] = s->scale_idx * dot_bf(qi, k_idx + ((long long)b * KR + j) * s->d_idx, s->d_idx);
+                softmax_lse(lg, n, ps);
+                double *dq = dq_idx + (((long long)b * s->Nq + i) * s->Hkv + r) * s->d_idx;
+                for (int e = 0; e < s->d_idx; ++e) dq[e] = 0.0;
+                for (int j = 0; j < n; ++j) {
+                    const double dsig = coef * (ps[j] - pt[j]);
+                    const orc_in *kj = k_idx + ((long long)b * KR + j) * s->d_idx;
+                    for (int e = 0; e < s->d_idx; ++e) {
+                        dq[e] += s->scale_idx * dsig * bfv(kj[e]);
+                        dki[(long long)j * s->d_idx + e] += s->scale_idx * dsig * bfv(qi[e]);
+                    }
+                }
+            }
+            #pragma omp critical
+            {
+                double *out = dk_idx + (long long)b * s->Nk * s->d_idx;
+                for (long long x = 0; x < (long long)s->Nk * s->d_idx; ++x) out[x] += dki[x];
+            }
+        }
+        free(lg); free(p); free(pt); free(ps); free(dki);
+    }
+    return 0;
 }
 
 int orc_num_threads(void)
