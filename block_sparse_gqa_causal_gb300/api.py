@@ -20,10 +20,12 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmsa.so")
 
 OP_INDEX_SELECT, OP_SPARSE_ATTN_FWD, OP_KL_FWD, OP_FUSED_BWD, OP_FUSED_BWD_KL, OP_TRAIN_STEP = 0, 1, 2, 3, 4, 5
+OP_WARMUP_KL = 6
 STATUS = {0: "MSA_OK", 1: "MSA_ERR_INVALID_ARGUMENT", 2: "MSA_ERR_UNSUPPORTED", 3: "MSA_ERR_WORKSPACE",
           4: "MSA_ERR_CUDA", 5: "MSA_ERR_TIMEOUT", 6: "MSA_ERR_DEVICE"}
 EXPORTS = ("msa_workspace_size", "msa_index_select", "msa_sparse_attn_fwd", "msa_kl_fwd", "msa_fused_bwd",
-           "msa_fused_bwd_kl", "msa_train_step", "msa_train_step_staged", "msa_block_mask",
+           "msa_fused_bwd_kl", "msa_train_step", "msa_train_step_staged", "msa_block_mask", "msa_warmup_kl",
+           "msa_index_proj_workspace_size", "msa_index_proj_fwd", "msa_index_proj_bwd",
            "msa_last_error", "msa_check_device_status", "msa_version", "msa_launch_count")
 
 
@@ -31,6 +33,23 @@ class MsaError(RuntimeError):
     def __init__(self, code: int, msg: str):
         super().__init__(f"{STATUS.get(code, code)}: {msg}")
         self.code = code
+
+
+class _CProjShape(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("T", "Dm", "Hkv", "d_idx")]
+
+
+@dataclass
+class ProjShape:
+    """msa_proj_shape: T tokens of Dm features projected to Hkv index queries
+    and one index key of d_idx features each."""
+    T: int
+    Dm: int
+    Hkv: int
+    d_idx: int
+
+    def c(self) -> _CProjShape:
+        return _CProjShape(self.T, self.Dm, self.Hkv, self.d_idx)
 
 
 class _CShape(ctypes.Structure):
@@ -99,8 +118,15 @@ def lib() -> ctypes.CDLL:
                                                 sz, P]
             L.msa_check_device_status.argtypes = [P, P]
             L.msa_block_mask.argtypes = [S, P, P, P, P, P]
+            L.msa_warmup_kl.argtypes = [S, P, P, P, P, P, f, P, P, P, P, P, P, P, sz, P]
+            PS = ctypes.POINTER(_CProjShape)
+            L.msa_index_proj_workspace_size.argtypes = [PS]
+            L.msa_index_proj_workspace_size.restype = sz
+            L.msa_index_proj_fwd.argtypes = [PS, P, P, P, P, P, P, sz, P]
+            L.msa_index_proj_bwd.argtypes = [PS, P, P, P, P, P, P, sz, P]
             for fn in ("msa_index_select", "msa_sparse_attn_fwd", "msa_kl_fwd", "msa_fused_bwd", "msa_fused_bwd_kl",
-                       "msa_train_step", "msa_train_step_staged", "msa_check_device_status", "msa_block_mask"):
+                       "msa_train_step", "msa_train_step_staged", "msa_check_device_status", "msa_block_mask",
+                       "msa_warmup_kl", "msa_index_proj_fwd", "msa_index_proj_bwd"):
                 getattr(L, fn).restype = ctypes.c_int
             L.msa_last_error.restype = ctypes.c_char_p
             L.msa_version.restype = ctypes.c_char_p
@@ -340,3 +366,65 @@ def version() -> str:
 
 def default_scale(d: int) -> float:
     return 1.0 / math.sqrt(d)
+
+
+def warmup_kl(shape: Shape, q, k, v, q_idx, k_idx, kl_coef: float = 1.0, *, out=None, workspace=None, stream=None):
+    """msa_warmup_kl: the dense indexer warm-up loss and its gradient in the
+    index inputs.  Returns a dict with lse [B,Hq,Nq], lse_idx, kl_rows
+    [B,Hkv,Nq], kl_loss (scalar), dq_idx, dk_idx (bf16)."""
+    s = shape
+    for t, n, shp in ((q, "q", (s.B, s.Nq, s.Hq, s.d)), (k, "k", (s.B, s.Nk, s.Hkv, s.d)),
+                      (v, "v", (s.B, s.Nk, s.Hkv, s.d)), (q_idx, "q_idx", (s.B, s.Nq, s.Hkv, s.d_idx)),
+                      (k_idx, "k_idx", (s.B, s.Nk, s.d_idx))):
+        _need(t, n, shp, torch.bfloat16)
+    dev = q.device
+    if out is None:
+        f32 = dict(dtype=torch.float32, device=dev)
+        out = {"lse": torch.empty((s.B, s.Hq, s.Nq), **f32), "lse_idx": torch.empty((s.B, s.Hkv, s.Nq), **f32),
+               "kl_rows": torch.empty((s.B, s.Hkv, s.Nq), **f32), "kl_loss": torch.empty((), **f32),
+               "dq_idx": torch.empty_like(q_idx), "dk_idx": torch.empty_like(k_idx)}
+    ws = _ws(workspace, s, OP_WARMUP_KL, dev)
+    _check(lib().msa_warmup_kl(ctypes.byref(s.c()), _ptr(q), _ptr(k), _ptr(v), _ptr(q_idx), _ptr(k_idx),
+                               ctypes.c_float(kl_coef), _ptr(out["lse"]), _ptr(out["lse_idx"]), _ptr(out["kl_rows"]),
+                               _ptr(out["kl_loss"]), _ptr(out["dq_idx"]), _ptr(out["dk_idx"]), _ptr(ws), ws.numel(),
+                               _stream(stream)))
+    return out
+
+
+def proj_workspace(shape: ProjShape, device=None) -> torch.Tensor:
+    n = lib().msa_index_proj_workspace_size(ctypes.byref(shape.c()))
+    if n == 0:
+        _check(1)
+    ws = torch.empty(int(n), dtype=torch.uint8, device=device or "cuda")
+    ws[:256].zero_()
+    return ws
+
+
+def index_proj_fwd(shape: ProjShape, x, wq_idx, wk_idx, *, q_idx=None, k_idx=None, workspace=None, stream=None):
+    """msa_index_proj_fwd: q_idx [T, Hkv, d_idx], k_idx [T, d_idx] (bf16) of x [T, Dm]."""
+    s = shape
+    _need(x, "x", (s.T, s.Dm), torch.bfloat16)
+    _need(wq_idx, "wq_idx", (s.Dm, s.Hkv * s.d_idx), torch.bfloat16)
+    _need(wk_idx, "wk_idx", (s.Dm, s.d_idx), torch.bfloat16)
+    dev = x.device
+    q_idx = torch.empty((s.T, s.Hkv, s.d_idx), dtype=torch.bfloat16, device=dev) if q_idx is None else q_idx
+    k_idx = torch.empty((s.T, s.d_idx), dtype=torch.bfloat16, device=dev) if k_idx is None else k_idx
+    ws = proj_workspace(s, dev) if workspace is None else workspace
+    _check(lib().msa_index_proj_fwd(ctypes.byref(s.c()), _ptr(x), _ptr(wq_idx), _ptr(wk_idx), _ptr(q_idx),
+                                    _ptr(k_idx), _ptr(ws), ws.numel(), _stream(stream)))
+    return q_idx, k_idx
+
+
+def index_proj_bwd(shape: ProjShape, x, dq_idx, dk_idx, *, dwq=None, dwk=None, workspace=None, stream=None):
+    """msa_index_proj_bwd: dwq [Dm, Hkv*d_idx], dwk [Dm, d_idx] (fp32); x gets no gradient."""
+    s = shape
+    _need(x, "x", (s.T, s.Dm), torch.bfloat16)
+    _need(dq_idx, "dq_idx", (s.T, s.Hkv, s.d_idx), torch.bfloat16)
+    _need(dk_idx, "dk_idx", (s.T, s.d_idx), torch.bfloat16)
+    dev = x.device
+    dwq = torch.empty((s.Dm, s.Hkv * s.d_idx), dtype=torch.float32, device=dev) if dwq is None else dwq
+    dwk = torch.empty((s.Dm, s.d_idx), dtype=torch.float32, device=dev) if dwk is None else dwk
+    ws = proj_workspace(s, dev) if workspace is None else workspace
+    _check(lib().msa_index_proj_bwd(ctypes.byref(s.c()), _ptr(x), _ptr(dq_idx), _ptr(dk_idx), _ptr(dwq), _ptr(dwk),
+                                    _ptr(ws), ws.numel(), _stream(stream)))
+    return dwq, dwk

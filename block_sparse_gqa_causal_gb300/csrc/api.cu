@@ -191,6 +191,32 @@ size_t train_bytes(const Problem &p)
            align256(kl_part_count(p) * sizeof(float2)) + bwd_bytes(p) - index_bytes(p) + bwdkl_bytes(p);
 }
 
+// The dense indexer warm-up runs the block-sparse kernels on the selection of
+// every visible block: topk = nb (at most 32 blocks: 4,096 tokens), the
+// tensor-core teacher and backward (d = d_idx = 128), a training sequence.
+bool warmup_shape_ok(const Problem &p)
+{
+    return p.q_offset == 0 && p.Nq == p.Nk && p.kv_rows == p.Nk && p.d == 128 && p.d_idx == 128 && p.nb <= 32;
+}
+Problem warmup_problem(const Problem &p)
+{
+    Problem w = p;
+    w.topk = p.nb;
+    return w;
+}
+size_t warmup_bytes(const Problem &p0)
+{
+    const Problem p = warmup_problem(p0);
+    const size_t slots = (size_t)p.B * p.Nq * p.topk;               // per (b, query), all groups below
+    const size_t rows = slots * p.Hq;
+    return align256(slots * p.Hkv * 4) + index_bytes(p)              // selection, inverse index
+           + align256((size_t)p.B * p.Nq * p.Hq * p.d * 2)           // the forward's output (not returned)
+           + align256(rows * p.d * 2) + align256(rows * 8)          // forward partials
+           + align256(kl_part_count(p) * sizeof(float2)) + klt_bytes(p) + klrows_bytes(p)
+           + align256(slots * p.Hkv * p.d_idx * 2)                   // dq_idx partial rows
+           + align256((size_t)p.B * p.Hkv * p.Nk * p.d_idx * 4);     // dK_idx shares per group
+}
+
 #define REQUIRE_PTR(ptr, name)                                                                         \
     do {                                                                                               \
         if (!(ptr)) return fail(MSA_ERR_INVALID_ARGUMENT, "%s is NULL", name);                         \
@@ -302,6 +328,10 @@ size_t msa_workspace_size(const msa_shape *shape, int op)
     case MSA_OP_FUSED_BWD: return kStatusBytes + bwd_bytes(p);
     case MSA_OP_FUSED_BWD_KL: return kStatusBytes + bwd_bytes(p) + bwdkl_bytes(p);
     case MSA_OP_TRAIN_STEP: return kStatusBytes + train_bytes(p);
+    case MSA_OP_WARMUP_KL: {
+        if (!warmup_shape_ok(p)) return 0;
+        return kStatusBytes + warmup_bytes(p);
+    }
     default: fail(MSA_ERR_INVALID_ARGUMENT, "unknown op %d", op); return 0;
     }
 }
@@ -661,6 +691,150 @@ msa_status msa_train_step_staged(const msa_shape *shape, const void *q, const vo
                            dk, dv, dq_idx, dk_idx, static_cast<cudaEvent_t>(idx_ready),
                            static_cast<cudaEvent_t>(qkv_ready), static_cast<cudaEvent_t>(do_ready), workspace,
                            workspace_bytes, stream);
+}
+
+msa_status msa_warmup_kl(const msa_shape *shape, const void *q, const void *k, const void *v, const void *q_idx,
+                         const void *k_idx, float kl_coef, float *lse, float *lse_idx, float *kl_rows, float *kl_loss,
+                         void *dq_idx, void *dk_idx, void *workspace, size_t workspace_bytes, void *stream)
+{
+    Problem p0;
+    msa_status st = make_problem(shape, p0);
+    if (st != MSA_OK) return st;
+    if (!warmup_shape_ok(p0))
+        return fail(MSA_ERR_UNSUPPORTED, "warmup_kl needs q_offset == 0, Nq == Nk == kv_rows, d = d_idx = 128 and at "
+                    "most 32 blocks (Nk <= 4096); got Nk=%d d=%d d_idx=%d", p0.Nk, p0.d, p0.d_idx);
+    REQUIRE_PTR(q, "q");
+    REQUIRE_PTR(k, "k");
+    REQUIRE_PTR(v, "v");
+    REQUIRE_PTR(q_idx, "q_idx");
+    REQUIRE_PTR(k_idx, "k_idx");
+    REQUIRE_PTR(dq_idx, "dq_idx");
+    REQUIRE_PTR(dk_idx, "dk_idx");
+    if (!lse || !lse_idx || !kl_loss) return fail(MSA_ERR_INVALID_ARGUMENT, "lse, lse_idx and kl_loss must be non-NULL");
+    if (!isfinite(kl_coef)) return fail(MSA_ERR_INVALID_ARGUMENT, "kl_coef must be finite");
+    st = check_ws(workspace, workspace_bytes, kStatusBytes + warmup_bytes(p0));
+    if (st != MSA_OK) return st;
+    const Problem p = warmup_problem(p0);
+    DeviceStatus *ds = static_cast<DeviceStatus *>(workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    Carve cv{static_cast<char *>(workspace)};
+    const size_t slots = (size_t)p.B * p.Nq * p.topk, rows = slots * p.Hq;
+    int32_t *sel = cv.take<int32_t>(slots * p.Hkv);
+    FwdWork fw;
+    carve_index(cv, p, fw);
+    bf16 *o = cv.take<bf16>((size_t)p.B * p.Nq * p.Hq * p.d);
+    fw.part = cv.take<bf16>(rows * p.d);
+    fw.stats = cv.take<float2>(rows);
+    fw.index_ready = true;
+    KlWork kw;
+    kw.part = cv.take<float2>(kl_part_count(p));
+    kw.klt = nullptr;
+    kw.bucket_cnt = fw.bucket_cnt;
+    kw.bucket_off = fw.bucket_off;
+    kw.bucket_scratch = fw.bucket_scratch;
+    kw.bucket_q = fw.bucket_q;
+    kw.index_ready = true;
+    float *klt = cv.take<float>(slots * p.Hkv * 4);
+    float *rows_kl = cv.take<float>((size_t)p.B * p.Hkv * p.Nq);
+    if (kl_rows) rows_kl = kl_rows;
+    bf16 *dqi_part = cv.take<bf16>(slots * p.Hkv * p.d_idx);
+    float *dki_g = cv.take<float>((size_t)p.B * p.Hkv * p.Nk * p.d_idx);
+    const bf16 *bq = static_cast<const bf16 *>(q), *bk = static_cast<const bf16 *>(k);
+    const bf16 *bqi = static_cast<const bf16 *>(q_idx), *bki = static_cast<const bf16 *>(k_idx);
+    cudaError_t e;
+    // every visible block selected: the dense teacher and student over the whole prefix
+    if ((e = launch_dense_selection(p, sel, s)) != cudaSuccess) return cuda_fail(e, "warmup_kl: selection");
+    if ((e = launch_inverse_index(p, sel, fw.bucket_cnt, fw.bucket_off, fw.bucket_scratch, fw.bucket_q, ds, s)) !=
+        cudaSuccess)
+        return cuda_fail(e, "warmup_kl: inverse index");
+    // the dense main attention: its lse normalises each head's teacher probabilities
+    if ((e = launch_sparse_fwd_keymajor(p, bq, bk, static_cast<const bf16 *>(v), sel, o, lse, fw, ds, s)) != cudaSuccess)
+        return cuda_fail(e, "warmup_kl: main attention");
+    if ((e = launch_kl_keymajor(p, bq, bk, bqi, bki, sel, lse, lse_idx, nullptr, kw, ds, s)) != cudaSuccess)
+        return cuda_fail(e, "warmup_kl: lse_idx");
+    if ((e = launch_index_teacher_tc(p, bq, bk, bqi, bki, lse, lse_idx, kl_coef, fw.bucket_off, fw.bucket_q, klt,
+                                     dqi_part, dki_g, ds, s)) != cudaSuccess)
+        return cuda_fail(e, "warmup_kl: teacher and index gradients");
+    if ((e = launch_kl_rows_combine(p, sel, lse_idx, klt, rows_kl, s)) != cudaSuccess) return cuda_fail(e, "warmup_kl: rows");
+    if ((e = launch_kl_reduce(p, rows_kl, kl_coef, kl_loss, s)) != cudaSuccess) return cuda_fail(e, "warmup_kl: loss");
+    if ((e = launch_bwd_combine(p, sel, dqi_part, static_cast<bf16 *>(dq_idx), p.Hkv, 1, s)) != cudaSuccess)
+        return cuda_fail(e, "warmup_kl: dq_idx");
+    if ((e = launch_dki_group_sum(p, dki_g, static_cast<bf16 *>(dk_idx), s)) != cudaSuccess)
+        return cuda_fail(e, "warmup_kl: dk_idx");
+    return MSA_OK;
+}
+
+}  // extern "C"
+
+namespace {
+msa_status make_proj(const msa_proj_shape *s, ProjProblem &pp)
+{
+    if (!s) return fail(MSA_ERR_INVALID_ARGUMENT, "shape is NULL");
+    if (s->T < 1 || s->Dm < 1 || s->Hkv < 1 || s->d_idx < 1)
+        return fail(MSA_ERR_INVALID_ARGUMENT, "projection shape has a non-positive size (T=%d Dm=%d Hkv=%d d_idx=%d)",
+                    s->T, s->Dm, s->Hkv, s->d_idx);
+    if (s->d_idx != 64 && s->d_idx != 128) return fail(MSA_ERR_UNSUPPORTED, "d_idx must be 64 or 128 (got %d)", s->d_idx);
+    if (s->Dm % 8 != 0) return fail(MSA_ERR_UNSUPPORTED, "Dm must be a multiple of 8 (got %d)", s->Dm);
+    if ((long long)s->T * s->Hkv * s->d_idx >= (1LL << 31) || (long long)s->T * s->Dm >= (1LL << 40))
+        return fail(MSA_ERR_UNSUPPORTED, "projection too large");
+    pp.T = s->T;
+    pp.Dm = s->Dm;
+    pp.Hkv = s->Hkv;
+    pp.d_idx = s->d_idx;
+    pp.num_sms = sm_count();
+    return MSA_OK;
+}
+}  // namespace
+
+extern "C" {
+
+size_t msa_index_proj_workspace_size(const msa_proj_shape *shape)
+{
+    ProjProblem pp;
+    if (make_proj(shape, pp) != MSA_OK) return 0;
+    return kStatusBytes + align256(index_proj_partial_floats(pp) * sizeof(float));
+}
+
+msa_status msa_index_proj_fwd(const msa_proj_shape *shape, const void *x, const void *wq_idx, const void *wk_idx,
+                              void *q_idx, void *k_idx, void *workspace, size_t workspace_bytes, void *stream)
+{
+    ProjProblem pp;
+    msa_status st = make_proj(shape, pp);
+    if (st != MSA_OK) return st;
+    REQUIRE_PTR(x, "x");
+    REQUIRE_PTR(wq_idx, "wq_idx");
+    REQUIRE_PTR(wk_idx, "wk_idx");
+    REQUIRE_PTR(q_idx, "q_idx");
+    REQUIRE_PTR(k_idx, "k_idx");
+    st = check_ws(workspace, workspace_bytes, kStatusBytes);
+    if (st != MSA_OK) return st;
+    cudaError_t e = launch_index_proj_fwd(pp, static_cast<const bf16 *>(x), static_cast<const bf16 *>(wq_idx),
+                                          static_cast<const bf16 *>(wk_idx), static_cast<bf16 *>(q_idx),
+                                          static_cast<bf16 *>(k_idx), static_cast<DeviceStatus *>(workspace),
+                                          static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "index_proj_fwd launch");
+    return MSA_OK;
+}
+
+msa_status msa_index_proj_bwd(const msa_proj_shape *shape, const void *x, const void *dq_idx, const void *dk_idx,
+                              float *dwq_idx, float *dwk_idx, void *workspace, size_t workspace_bytes, void *stream)
+{
+    ProjProblem pp;
+    msa_status st = make_proj(shape, pp);
+    if (st != MSA_OK) return st;
+    REQUIRE_PTR(x, "x");
+    REQUIRE_PTR(dq_idx, "dq_idx");
+    REQUIRE_PTR(dk_idx, "dk_idx");
+    REQUIRE_PTR(dwq_idx, "dwq_idx");
+    REQUIRE_PTR(dwk_idx, "dwk_idx");
+    st = check_ws(workspace, workspace_bytes, kStatusBytes + align256(index_proj_partial_floats(pp) * sizeof(float)));
+    if (st != MSA_OK) return st;
+    float *partial = reinterpret_cast<float *>(static_cast<char *>(workspace) + kStatusBytes);
+    cudaError_t e = launch_index_proj_dw(pp, static_cast<const bf16 *>(x), static_cast<const bf16 *>(dq_idx),
+                                         static_cast<const bf16 *>(dk_idx), dwq_idx, dwk_idx, partial,
+                                         static_cast<DeviceStatus *>(workspace), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "index_proj_bwd launch");
+    return MSA_OK;
 }
 
 msa_status msa_check_device_status(void *workspace, void *stream)

@@ -564,6 +564,18 @@ cudaError_t launch_main(const Problem &p, const bf16 *q, const bf16 *k, const bf
 
 }  // namespace
 
+cudaError_t launch_bwd_combine(const Problem &p, const int32_t *sel, const bf16 *part, bf16 *out, int H, int Gh,
+                               cudaStream_t s)
+{
+    const long long rows = (long long)p.B * p.Nq * H;
+    {
+        TimedLaunch timed_("bwd_combine_kernel", s);
+        bwd_combine_kernel<128><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p, sel, part, out, H, Gh);
+    }
+    note_launch();
+    return cudaGetLastError();
+}
+
 cudaError_t launch_fused_bwd(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *v, const bf16 *o,
                              const bf16 *d_o, const float *lse, const bf16 *q_idx, const bf16 *k_idx,
                              const int32_t *sel, const float *lse_idx, float kl_coef, bf16 *dq, bf16 *dk, bf16 *dv,

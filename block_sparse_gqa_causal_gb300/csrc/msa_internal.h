@@ -179,4 +179,24 @@ cudaError_t launch_bwd_main_tc(const Problem &p, const bf16 *q, const bf16 *k, c
                                const float *lse, const BwdWork &w, bf16 *dk, bf16 *dv, DeviceStatus *st,
                                cudaStream_t s);
 
+// Index projections of the detached hidden states (X [T, Dm], W_q^idx
+// [Dm, Hkv*d_idx], W_k^idx [Dm, d_idx]) and their weight gradient.
+struct ProjProblem {
+    int T, Dm, Hkv, d_idx, num_sms;
+};
+// token-range splits of the weight gradient, and the fp32 partial floats it needs
+int index_proj_splits(const ProjProblem &pp);
+size_t index_proj_partial_floats(const ProjProblem &pp);
+cudaError_t launch_index_proj_fwd(const ProjProblem &pp, const bf16 *x, const bf16 *wq, const bf16 *wk, bf16 *q_idx,
+                                  bf16 *k_idx, DeviceStatus *st, cudaStream_t s);
+cudaError_t launch_index_proj_dw(const ProjProblem &pp, const bf16 *x, const bf16 *dq_idx, const bf16 *dk_idx,
+                                 float *dwq, float *dwk, float *partial, DeviceStatus *st, cudaStream_t s);
+// Sum of a row's per-slot bf16 partial rows (128 features) over its valid
+// slots: H rows per (b, query), head h in group h / Gh.
+cudaError_t launch_bwd_combine(const Problem &p, const int32_t *sel, const bf16 *part, bf16 *out, int H, int Gh,
+                               cudaStream_t s);
+// The selection that keeps every visible block (topk = nb): sel[b, r, i, t] =
+// t for t <= c0(i), else -1 -- the dense warm-up's token set.
+cudaError_t launch_dense_selection(const Problem &p, int32_t *sel, cudaStream_t s);
+
 }  // namespace msa

@@ -84,7 +84,8 @@ enum {
     MSA_OP_KL_FWD = 2,
     MSA_OP_FUSED_BWD = 3,
     MSA_OP_FUSED_BWD_KL = 4,
-    MSA_OP_TRAIN_STEP = 5
+    MSA_OP_TRAIN_STEP = 5,
+    MSA_OP_WARMUP_KL = 6
 };
 
 /* Bytes of workspace `op` needs for `shape` (0 on an invalid shape). */
@@ -206,6 +207,54 @@ msa_status msa_train_step_staged(const msa_shape *shape, const void *q, const vo
                                  float *kl_loss, void *dq, void *dk, void *dv, void *dq_idx, void *dk_idx,
                                  void *idx_ready, void *qkv_ready, void *do_ready,
                                  void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Dense indexer warm-up (section 3.1, the warm-up loss L^I_warm, in MSA's
+ * per-group form of section 3.2: "after a dense warm-up, MSA computes the KL
+ * over tokens in the selected blocks").  Full attention is kept: for each
+ * query i and group r over EVERY visible key j <= i,
+ *   teacher  Pt_j = (1/G) sum_{h in r} softmax_j(l_{h,j})   (detached)
+ *   student  Ps_j = softmax_j(s_j),  s_j = scale_idx <q_idx, k_idx_j>
+ *   kl_rows[b,r,i] = KL(Pt || Ps),   *kl_loss = kl_coef / (B Nq Hkv) * sum of kl_rows
+ * and the loss's gradient in the index inputs, dL/ds_j = coef (Ps_j - Pt_j),
+ * chained into dq_idx [B, Nq, Hkv, d_idx] and dk_idx [B, Nk, d_idx] (bf16,
+ * fully written); q, k, v get none (the teacher is detached).  Also returns
+ * the dense main attention's lse [B, Hq, Nq] (the teacher's normaliser) and
+ * lse_idx; kl_rows may be NULL.  It is MSA's own block-sparse path run on
+ * the selection of every visible block, so shape->topk is ignored (any valid
+ * value): training layout (q_offset == 0, Nq == Nk, kv_rows == Nk), d = d_idx
+ * = 128 and at most 32 blocks (Nk <= 4096), else MSA_ERR_UNSUPPORTED.
+ * Workspace: msa_workspace_size(shape, MSA_OP_WARMUP_KL).  Deterministic.
+ */
+msa_status msa_warmup_kl(const msa_shape *shape, const void *q, const void *k, const void *v, const void *q_idx,
+                         const void *k_idx, float kl_coef, float *lse, float *lse_idx, float *kl_rows, float *kl_loss,
+                         void *dq_idx, void *dk_idx, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Index projections (section 3.2, the detachment equation): the index
+ * queries and keys are linear maps of the DETACHED hidden states,
+ *   q_idx = stopgrad(X) W_q^idx,   k_idx = stopgrad(X) W_k^idx.
+ * x [T, Dm] (T = B * N tokens), wq_idx [Dm, Hkv * d_idx] (group r's index
+ * query in columns r*d_idx ..), wk_idx [Dm, d_idx], all bf16 row-major;
+ * q_idx [T, Hkv, d_idx] and k_idx [T, d_idx] bf16 (the layouts the index
+ * branch takes).  msa_index_proj_bwd gives the KL's gradient in the weights,
+ *   dwq_idx = X^T dq_idx   [Dm, Hkv * d_idx],   dwk_idx = X^T dk_idx   [Dm, d_idx]
+ * (fp32, fully written), and nothing for X: the loss does not reach the
+ * backbone through the indexer.  Tensor-core GEMMs; the weight gradient
+ * splits the token sum over several CTAs and adds the parts in a fixed
+ * order (deterministic).  Supported: d_idx in {64, 128}, Dm a multiple of 8,
+ * Hkv >= 1, T * Hkv * d_idx < 2^31.  Pointers 16-byte aligned.  The
+ * workspace (msa_index_proj_workspace_size bytes, 256-byte aligned, first
+ * 256 bytes zero as for the other calls) serves both calls.
+ */
+typedef struct {
+    int T, Dm, Hkv, d_idx;
+} msa_proj_shape;
+size_t msa_index_proj_workspace_size(const msa_proj_shape *shape);
+msa_status msa_index_proj_fwd(const msa_proj_shape *shape, const void *x, const void *wq_idx, const void *wk_idx,
+                              void *q_idx, void *k_idx, void *workspace, size_t workspace_bytes, void *stream);
+msa_status msa_index_proj_bwd(const msa_proj_shape *shape, const void *x, const void *dq_idx, const void *dk_idx,
+                              float *dwq_idx, float *dwk_idx, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Index selection without any allocation, for callers that cannot allocate

@@ -155,3 +155,34 @@ def test_backward_workspace_holds_no_distribution(libmsa):
             + a(slots * Hkv * d * 2))
     assert api.workspace_size(sh, api.OP_FUSED_BWD) == want
     assert api.workspace_size(sh, api.OP_FUSED_BWD_KL) == want + a(B * Hkv * N * 4) + a(slots * Hkv * 16)
+
+
+def test_warmup_and_projection_calls_validate_on_the_host(libmsa):
+    """The dense warm-up needs a training sequence of at most 32 blocks with
+    d = d_idx = 128; the projections need d_idx in {64, 128} and Dm a multiple
+    of 8; bad pointers and short workspaces are refused before any launch."""
+    from block_sparse_gqa_causal_gb300 import api
+    g = ctypes.c_void_p(1 << 20)
+    f = ctypes.c_float(1.0)
+    for kw in (dict(Nq=8192, Nk=8192), dict(d=64), dict(Nq=3, Nk=256, q_offset=253)):
+        base = dict(B=1, Nq=1024, Nk=1024, Hq=8, Hkv=2, d=128, d_idx=128, topk=1)
+        base.update(kw)
+        sh = api.Shape(**base)
+        assert api.lib().msa_workspace_size(ctypes.byref(sh.c()), api.OP_WARMUP_KL) == 0
+        rc = libmsa.msa_warmup_kl(ctypes.byref(sh.c()), g, g, g, g, g, f, g, g, g, g, g, g, g, 1 << 40, None)
+        assert rc == 2, (kw, libmsa.msa_last_error())
+    sh = api.Shape(B=1, Nq=1024, Nk=1024, Hq=8, Hkv=2, d=128, d_idx=128, topk=1)
+    assert api.workspace_size(sh, api.OP_WARMUP_KL) > 0
+    rc = libmsa.msa_warmup_kl(ctypes.byref(sh.c()), None, g, g, g, g, f, g, g, g, g, g, g, g, 1 << 40, None)
+    assert rc == 1 and b"q is NULL" in libmsa.msa_last_error()
+    rc = libmsa.msa_warmup_kl(ctypes.byref(sh.c()), g, g, g, g, g, f, g, g, g, g, g, g, g, 256, None)
+    assert rc == 3
+    for T, Dm, Hkv, di, code in ((100, 256, 2, 96, 2), (100, 250, 2, 128, 2), (0, 256, 2, 128, 1)):
+        ps = api.ProjShape(T=T, Dm=Dm, Hkv=Hkv, d_idx=di)
+        rc = libmsa.msa_index_proj_fwd(ctypes.byref(ps.c()), g, g, g, g, g, g, 1 << 20, None)
+        assert rc == code, (T, Dm, di, libmsa.msa_last_error())
+    ps = api.ProjShape(T=20000, Dm=256, Hkv=2, d_idx=128)
+    need = libmsa.msa_index_proj_workspace_size(ctypes.byref(ps.c()))
+    assert need >= 256 + 256 * 384 * 4                  # at least one fp32 partial of [Dm][Hkv*d_idx + d_idx]
+    rc = libmsa.msa_index_proj_bwd(ctypes.byref(ps.c()), g, g, g, g, g, g, 256, None)
+    assert rc == 3
