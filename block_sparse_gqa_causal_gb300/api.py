@@ -124,9 +124,10 @@ def lib() -> ctypes.CDLL:
             L.msa_index_proj_workspace_size.restype = sz
             L.msa_index_proj_fwd.argtypes = [PS, P, P, P, P, P, P, sz, P]
             L.msa_index_proj_bwd.argtypes = [PS, P, P, P, P, P, P, sz, P]
+            L.msa_selftest_wait_timeout.argtypes = [P, ctypes.c_uint, P]
             for fn in ("msa_index_select", "msa_sparse_attn_fwd", "msa_kl_fwd", "msa_fused_bwd", "msa_fused_bwd_kl",
                        "msa_train_step", "msa_train_step_staged", "msa_check_device_status", "msa_block_mask",
-                       "msa_warmup_kl", "msa_index_proj_fwd", "msa_index_proj_bwd"):
+                       "msa_warmup_kl", "msa_index_proj_fwd", "msa_index_proj_bwd", "msa_selftest_wait_timeout"):
                 getattr(L, fn).restype = ctypes.c_int
             L.msa_last_error.restype = ctypes.c_char_p
             L.msa_version.restype = ctypes.c_char_p
@@ -428,3 +429,9 @@ def index_proj_bwd(shape: ProjShape, x, dq_idx, dk_idx, *, dwq=None, dwk=None, w
     _check(lib().msa_index_proj_bwd(ctypes.byref(s.c()), _ptr(x), _ptr(dq_idx), _ptr(dk_idx), _ptr(dwq), _ptr(dwk),
                                     _ptr(ws), ws.numel(), _stream(stream)))
     return dwq, dwk
+
+
+def selftest_wait_timeout(workspace, spin_limit: int = 4096, stream=None) -> None:
+    """msa_selftest_wait_timeout: one thread's bounded wait on a barrier that
+    nothing arrives on runs out and is recorded in the workspace's status word."""
+    _check(lib().msa_selftest_wait_timeout(_ptr(workspace), int(spin_limit), _stream(stream)))

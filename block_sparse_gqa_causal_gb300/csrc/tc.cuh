@@ -59,9 +59,10 @@ MSA_DEV bool mbar_test(uint64_t *bar, uint32_t parity)
 // the status word and returns false.  Callers then skip their remaining
 // work so the kernel ends instead of hanging.
 constexpr uint32_t kSpinLimit = 1u << 26;
-MSA_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, DeviceStatus *st, int site, volatile int *abort_flag)
+MSA_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, DeviceStatus *st, int site, volatile int *abort_flag,
+                       uint32_t limit = kSpinLimit)
 {
-    for (uint32_t it = 0; it < kSpinLimit; ++it) {
+    for (uint32_t it = 0; it < limit; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 1023u) == 1023u && abort_flag && *abort_flag) return false;
     }

@@ -314,7 +314,19 @@ const char *msa_last_error(void);
  * returns MSA_OK, MSA_ERR_TIMEOUT or MSA_ERR_DEVICE, and clears the word. */
 msa_status msa_check_device_status(void *workspace, void *stream);
 
-/* Library version string. */
+/* Self-test of the bounded device-side wait, with no counterpart in the
+ * method.  Every kernel of the library waits on its pipeline barriers with a
+ * poll limit; when a wait runs out it records code 5 in the workspace's
+ * status word and the kernel returns instead of hanging, so the context stays
+ * usable and msa_check_device_status() reports MSA_ERR_TIMEOUT.  This call
+ * launches one thread that waits, with spin_limit polls (1 .. 2^24), on a
+ * barrier in its own shared memory that nothing arrives on -- no copies or
+ * tensor-core work in flight -- and then writes 1 to the int at byte 128 of
+ * the workspace (2 if the wait had completed).  workspace: 256 bytes,
+ * 256-byte aligned, status word zero.  Asynchronous on stream. */
+msa_status msa_selftest_wait_timeout(void *workspace, unsigned int spin_limit, void *stream);
+
+/* Library version string. *//* Library version string. */
 const char *msa_version(void);
 
 /* Number of kernels this process has launched through the library so far
