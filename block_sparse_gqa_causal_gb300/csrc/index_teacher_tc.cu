@@ -524,49 +524,54 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
             // no per-element mask where every valid query of the chunk sees the whole
             // block (padding columns carry lse = +inf and zero rows: they add nothing)
             const bool all_vis = (long long)mt->pmin >= j0 + kKeys - 1 && j0 + kKeys <= p.Nk;
-            // ---- teacher of this key for the warp's 16 queries, from the G sub-chunks,
-            // taken two at a time (one wait round, two TMEM loads)
-            constexpr int kSP = G >= 2 ? 2 : 1;
+            // ---- teacher of this key for the warp's 16 queries, from the G sub-chunks.
+            // The warp's 16 columns of a sub-chunk are read as two 8-column pieces in
+            // a two-deep pipeline: piece i+1's TMEM load is in flight while piece i is
+            // summed (a wait covers every load issued before it, so one at a time).
+            constexpr int kPieces = 2 * G;
             float pt[kWC];
 #pragma unroll
             for (int k = 0; k < kWC; ++k) pt[k] = 0.f;
             auto teacher = [&](auto all_tag) {
                 constexpr bool kAll = decltype(all_tag)::value;
-#pragma unroll
-                for (int m0 = 0; m0 < G; m0 += kSP) {
-                    uint32_t sv[kSP][kWC];
-#pragma unroll
-                    for (int h = 0; h < kSP; ++h) {
-                        const int u = n * G + m0 + h;
-                        if (ok) ok = wwait(&s_full[u % kSSlots], (uint32_t)(u / kSSlots) & 1u, st, 152, abort_flag);
+                uint32_t buf[2][8];
+                auto issue = [&](int i) -> bool {       // piece i: sub-chunk i/2, columns c0 + 8*(i%2)
+                    const int u = n * G + i / 2;
+                    if ((i & 1) == 0) {
+                        if (!wwait(&s_full[u % kSSlots], (uint32_t)(u / kSSlots) & 1u, st, 152, abort_flag)) return false;
+                        tc::fence_after_sync();
                     }
-                    if (!ok) return;
-                    tc::fence_after_sync();
+                    tc::tmem_ld8_nowait(tmem + lane_base + TM_S + (u % kSSlots) * 64 + c0 + 8 * (i & 1), buf[i & 1]);
+                    return true;
+                };
+                if (!(ok = issue(0))) return;
+                tc::tmem_wait8(buf[0]);
 #pragma unroll
-                    for (int h = 0; h < kSP; ++h)
-                        tc::tmem_ld16_nowait(tmem + lane_base + TM_S + ((n * G + m0 + h) % kSSlots) * 64 + c0, sv[h]);
+                for (int i = 0; i < kPieces; ++i) {
+                    if (i + 1 < kPieces) {
+                        if (!(ok = issue(i + 1))) return;
+                    }
+                    if (i & 1) {
+                        // both pieces of sub-chunk i/2 are in registers: its slot is free
+                        tc::fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(&s_free[(n * G + i / 2) % kSSlots]);
+                    }
+                    const int m = i / 2;
+                    const float4 *l2 = reinterpret_cast<const float4 *>(mt->lse2 + (c0 + m * QW) * G + 8 * (i & 1));
 #pragma unroll
-                    for (int h = 0; h < kSP; ++h) tc::tmem_wait16(sv[h]);
-                    tc::fence_before_sync();
-                    __syncwarp();
-                    if (lane < kSP) tc::mbar_arrive(&s_free[(n * G + m0 + lane) % kSSlots]);
+                    for (int r4 = 0; r4 < 2; ++r4) {
+                        const float4 l = l2[r4];
+                        const float lv4[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
-                    for (int h = 0; h < kSP; ++h) {
-                        const int m = m0 + h;
-                        const float4 *l2 = reinterpret_cast<const float4 *>(mt->lse2 + (c0 + m * QW) * G);
-#pragma unroll
-                        for (int r4 = 0; r4 < kWC / 4; ++r4) {
-                            const float4 l = l2[r4];
-                            const float lv4[4] = {l.x, l.y, l.z, l.w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int rho = 4 * r4 + e, k = m * QW + rho / G;
-                                const float x = tc::ex2(__uint_as_float(sv[h][rho]) * sl2 - lv4[e]);
-                                if constexpr (kAll) pt[k] += x;
-                                else pt[k] += (key_ok && ji <= mt->pos[c0 + k]) ? x : 0.f;
-                            }
+                        for (int e = 0; e < 4; ++e) {
+                            const int rho = 8 * (i & 1) + 4 * r4 + e, k = m * QW + rho / G;
+                            const float x = tc::ex2(__uint_as_float(buf[i & 1][4 * r4 + e]) * sl2 - lv4[e]);
+                            if constexpr (kAll) pt[k] += x;
+                            else pt[k] += (key_ok && ji <= mt->pos[c0 + k]) ? x : 0.f;
                         }
                     }
+                    if (i + 1 < kPieces) tc::tmem_wait8(buf[(i + 1) & 1]);
                 }
             };
             if (all_vis) teacher(std::true_type{});

@@ -295,6 +295,22 @@ MSA_DEV void tmem_wait32(uint32_t *r)
                  :
                  : "memory");
 }
+MSA_DEV void tmem_ld8_nowait(uint32_t taddr, uint32_t *r)
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr)
+                 : "memory");
+}
+// Waits for every tcgen05.ld of this thread issued so far; r (8 registers)
+// is tied so nothing that reads it moves above the wait.
+MSA_DEV void tmem_wait8(uint32_t *r)
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])
+                 :
+                 : "memory");
+}
 MSA_DEV void tmem_wait16(uint32_t *r)
 {
     asm volatile("tcgen05.wait::ld.sync.aligned;\n"
