@@ -329,7 +329,11 @@ size_t msa_workspace_size(const msa_shape *shape, int op)
     case MSA_OP_FUSED_BWD_KL: return kStatusBytes + bwd_bytes(p) + bwdkl_bytes(p);
     case MSA_OP_TRAIN_STEP: return kStatusBytes + train_bytes(p);
     case MSA_OP_WARMUP_KL: {
-        if (!warmup_shape_ok(p)) return 0;
+        if (!warmup_shape_ok(p)) {
+            fail(MSA_ERR_UNSUPPORTED, "warmup_kl needs q_offset == 0, Nq == Nk == kv_rows, d = d_idx = 128 and at "
+                 "most 32 blocks (Nk <= 4096); got Nk=%d d=%d d_idx=%d", p.Nk, p.d, p.d_idx);
+            return 0;
+        }
         return kStatusBytes + warmup_bytes(p);
     }
     default: fail(MSA_ERR_INVALID_ARGUMENT, "unknown op %d", op); return 0;

@@ -147,7 +147,9 @@ msa_status msa_kl_fwd(const msa_shape *shape, const void *q, const void *k, cons
  * branch gets none from d_o (section 3.2 on the two detachments).  Uses the
  * forward's o and lse and the KL forward's lse_idx.  Requires q_offset == 0
  * and Nq == Nk (training layout).  dk, dv, dk_idx are fully written (zero
- * for keys no query selected).
+ * for keys no query selected).  With d = d_idx = 128 (the tensor-core
+ * path) every sum is taken in a fixed order: the same inputs give the same
+ * bits on every call.
  */
 msa_status msa_fused_bwd(const msa_shape *shape, const void *q, const void *k, const void *v,
                          const void *o, const void *d_o, const float *lse, const void *q_idx,

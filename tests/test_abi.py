@@ -169,6 +169,7 @@ def test_warmup_and_projection_calls_validate_on_the_host(libmsa):
         base.update(kw)
         sh = api.Shape(**base)
         assert api.lib().msa_workspace_size(ctypes.byref(sh.c()), api.OP_WARMUP_KL) == 0
+        assert b"at most 32 blocks" in libmsa.msa_last_error()
         rc = libmsa.msa_warmup_kl(ctypes.byref(sh.c()), g, g, g, g, g, f, g, g, g, g, g, g, g, 1 << 40, None)
         assert rc == 2, (kw, libmsa.msa_last_error())
     sh = api.Shape(B=1, Nq=1024, Nk=1024, Hq=8, Hkv=2, d=128, d_idx=128, topk=1)
