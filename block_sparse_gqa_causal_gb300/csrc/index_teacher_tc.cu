@@ -12,8 +12,8 @@
 // Every term is a sum over the selected blocks, so one CTA per 128-key block
 // of one (b, group) -- the queries that selected it come from the inverse
 // index -- evaluates them in chunks of 64 queries, keys as the MMA's M:
-//   S^T = K Q^T        (M = 128 keys, N = 64 (query, head) rows: G such
-//                       sub-chunks per chunk, 64/G queries x G heads each)
+//   S^T = K Q^T        (M = 128 keys, N = 128 (query, head) rows per
+//                       sub-chunk, 128/G queries x G heads; 64 for G = 1)
 //   s^T = K_idx q_idx^T (M = 128 keys, N = 64 queries)
 // With keys on the TMEM lanes a query's G head rows are adjacent columns of
 // one thread, so the teacher is a register sum, and it meets the index score
@@ -38,9 +38,10 @@
 //
 // Roles: warp 0 loads K and K_idx (TMA) and the Q sub-chunk tiles (one TMA
 // box per query when G = 8, cp.async otherwise); warp 1 owns TMEM and issues
-// the MMAs; warps 2..17 are the epilogue (TMEM lanes 32*(w%4).., column
-// quarter (w-2)/4: 16 of a tile's 64 columns); warp 18 gathers the chunk's
-// q_idx rows and row data.
+// the S^T MMAs; warps 2..17 are the epilogue (TMEM lanes 32*(w%4).., column
+// quarter (w-2)/4: a quarter of each S^T sub-chunk and 16 of the 64 s^T
+// columns); warp 18 gathers the chunk's q_idx rows and row data; warp 19
+// issues the index-score and gradient MMAs.
 #include <limits.h>
 
 #include <type_traits>
@@ -57,18 +58,37 @@ constexpr int kQ = 64;                     // queries per chunk (s^T columns)
 constexpr int kEpiWarps = 16;              // 4 per TMEM lane quarter
 constexpr int kWC = 16;                    // s^T / S^T columns per epilogue warp
 constexpr int kProdI = 2 + kEpiWarps;      // q_idx rows and row data
-constexpr int kThreads = 32 * (3 + kEpiWarps);
+constexpr int kIssI = 3 + kEpiWarps;       // issues the index-score and gradient MMAs
+constexpr int kThreads = 32 * (4 + kEpiWarps);
 constexpr int SUBK = kKeys * 128;          // [128 rows][64 bf16] swizzled sub-tile
-constexpr int TILE_Q = 64 * D * 2;         // 64 (query, head) rows in 8-row groups of 2048 bytes
 constexpr int SUBI = kQ * 128;             // [64 rows][64 bf16] swizzled sub-tile
 constexpr int TILE_I = 2 * SUBI;           // a chunk's q_idx rows, two feature halves
-constexpr int kQSt = 6;                    // Q sub-chunk stages (a sub-chunk lasts ~0.3 us)
+constexpr int kQBytes = 96 * 1024;         // the Q sub-chunk ring
 constexpr int kISt = 2;                    // q_idx + row-data stages
-constexpr int kSSlots = 4;                 // S^T slots in TMEM
 constexpr int OFF_K = 0;
 constexpr int OFF_KI = OFF_K + 2 * SUBK;
 constexpr int OFF_Q = OFF_KI + 2 * SUBK;
-constexpr int OFF_I = OFF_Q + kQSt * TILE_Q;
+constexpr int OFF_I = OFF_Q + kQBytes;
+
+// A chunk's 64 queries x G heads of S^T are formed in sub-chunks of NS
+// (query, head) columns, NS = 128 where G >= 2 (one MMA of N = 128 runs at
+// the full tensor rate and halves the instructions the issuing thread waits
+// through), 64 for G = 1.  Epilogue warp column quarter cq reads W = NS/4
+// columns of each sub-chunk: QW = W/G queries, all heads of each.
+template <int G>
+struct Cfg {
+    static constexpr int NS = G == 1 ? 64 : 128;
+    static constexpr int NSUB = kQ * G / NS;        // sub-chunks per chunk
+    static constexpr int QS = NS / G;               // queries per sub-chunk
+    static constexpr int TILE_Q = NS * D * 2;       // NS (query, head) rows in 8-row groups of 2048 bytes
+    static constexpr int QST = kQBytes / TILE_Q;    // Q stages
+    static constexpr int SSLOTS = 256 / NS;         // S^T slots in TMEM (256 columns)
+    static constexpr int W = NS / 4;                // columns of a sub-chunk per epilogue warp
+    static constexpr int PPS = W / 8;               // 8-column pieces per sub-chunk
+    static constexpr int QW = W / G;                // queries of a sub-chunk per epilogue warp
+    static_assert(QST * TILE_Q == kQBytes && QST >= 3, "Q ring");
+    static_assert(NSUB * QW == 16, "each epilogue warp holds 16 queries of a chunk");
+};
 constexpr int OFF_SG = OFF_I + kISt * TILE_I;        // dsig^T [128 keys][64 queries]
 constexpr int OFF_META = OFF_SG + SUBK;
 
@@ -91,13 +111,15 @@ constexpr int alloc_bytes() { return off_bar<G>() + 512 + 1024; }
 static_assert(alloc_bytes<8>() <= 227 * 1024, "shared memory");
 
 // mbarriers (Q, row-data, S^T and s^T rings, the dsig pair, dq_idx^T,
-// kv_full, done) and the TMEM address + abort flag, in 512 bytes
-constexpr int kBars = 2 * kQSt + 2 * kISt + 2 * kSSlots + 2 * 2 + 2 + 2 + 2;
-static_assert(kBars * 8 + 8 <= 512, "barrier region");
+// kv_full, one done per issuing thread) and the TMEM address + abort flag,
+// in 512 bytes
+template <int G>
+constexpr int n_bars() { return 2 * Cfg<G>::QST + 2 * kISt + 2 * Cfg<G>::SSLOTS + 2 * 2 + 2 + 2 + 3; }
+static_assert(n_bars<1>() * 8 + 8 <= 512 && n_bars<8>() * 8 + 8 <= 512, "barrier region");
 
-// TMEM: dK_idx; kSSlots 64-column slots for S^T; two 64-column slots for s^T,
+// TMEM: dK_idx; 256 columns of S^T slots; two 64-column slots for s^T,
 // where the chunk's dq_idx^T lands once the epilogue has read s^T
-constexpr uint32_t TM_DKI = 0, TM_S = 128, TM_SI = TM_S + 64 * kSSlots;
+constexpr uint32_t TM_DKI = 0, TM_S = 128, TM_SI = TM_S + 256;
 static_assert(TM_SI + 128 <= 512, "TMEM columns");
 
 __device__ __forceinline__ int swz(int row, int ch) { return row * 128 + ((ch ^ (row & 7)) << 4); }
@@ -107,15 +129,14 @@ __device__ __forceinline__ int roff(int rho, int half, int ch)
     return (rho >> 3) * 2048 + half * 1024 + (rho & 7) * 128 + (((ch ^ rho) & 7) << 4);
 }
 
-// s^T column c holds chunk query m (64/G) + cq (16/G) + t, for c = 16 cq +
-// m (16/G) + t: the query whose teacher the warps of column quarter cq sum
-// from sub-chunk m
+// s^T column c holds chunk query m QS + cq QW + t, for c = 16 cq + m QW + t:
+// the query whose teacher the warps of column quarter cq sum from sub-chunk m
 template <int G>
 __device__ __forceinline__ int col_query(int c)
 {
-    constexpr int QW = kWC / G;
+    constexpr int QW = Cfg<G>::QW;
     const int cq = c / kWC, k = c % kWC;
-    return (k / QW) * (64 / G) + cq * QW + k % QW;
+    return (k / QW) * Cfg<G>::QS + cq * QW + k % QW;
 }
 
 // Streaming transposing sum over the warp of 16 columns pushed in order
@@ -168,7 +189,8 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
                         const int32_t *__restrict__ bucket_q, float *__restrict__ klt, bf16 *__restrict__ dqi_part,
                         float *__restrict__ dki_g, DeviceStatus *st)
 {
-    constexpr int QS = 64 / G;                 // queries per sub-chunk
+    using C = Cfg<G>;
+    constexpr int QS = C::QS, NSUB = C::NSUB, QST = C::QST, SSLOTS = C::SSLOTS;
     using MetaT = Meta<G>;
     const int r = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
     const long long bucket = ((long long)b * p.Hkv + r) * p.nb + c;
@@ -190,16 +212,16 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
     // stays a shared-memory access (no generic addressing)
     uint8_t *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + off_bar<G>());
-    uint64_t *q_full = bars, *q_empty = q_full + kQSt, *i_full = q_empty + kQSt, *i_empty = i_full + kISt;
-    uint64_t *s_full = i_empty + kISt, *s_free = s_full + kSSlots, *si_full = s_free + kSSlots;
+    uint64_t *q_full = bars, *q_empty = q_full + QST, *i_full = q_empty + QST, *i_empty = i_full + kISt;
+    uint64_t *s_full = i_empty + kISt, *s_free = s_full + SSLOTS, *si_full = s_free + SSLOTS;
     uint64_t *si_free = si_full + 2, *g_full = si_free + 2, *g_free = g_full + 1, *dq_full = g_free + 1;
-    uint64_t *kv_full = dq_full + 2, *done = kv_full + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+    uint64_t *kv_full = dq_full + 2, *done = kv_full + 1;      // done[0]: S issuer, done[1]: index issuer
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int a = 0; a < kQSt; ++a) {
+        for (int a = 0; a < QST; ++a) {
             // G == 8: lane 0's expect_tx arrival; otherwise 32 cp.async + 32 lane arrivals
             tc::mbar_init(&q_full[a], G == 8 ? 1 : 64);
             tc::mbar_init(&q_empty[a], 1);
@@ -208,7 +230,7 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
             tc::mbar_init(&i_full[a], 64);                 // 32 cp.async + 32 row-data arrivals
             tc::mbar_init(&i_empty[a], 1 + kEpiWarps);     // last MMA reading q_idx + row data read
         }
-        for (int a = 0; a < kSSlots; ++a) {
+        for (int a = 0; a < SSLOTS; ++a) {
             tc::mbar_init(&s_full[a], 1);
             tc::mbar_init(&s_free[a], kEpiWarps);
         }
@@ -222,7 +244,8 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
         tc::mbar_init(g_full, kEpiWarps);                   // dsig tile written
         tc::mbar_init(g_free, 1);                           // its gradient MMAs done
         tc::mbar_init(kv_full, 1);
-        tc::mbar_init(done, 1);
+        tc::mbar_init(&done[0], 1);
+        tc::mbar_init(&done[1], 1);
         *abort_flag = 0;
         tc::fence_mbar_init();
     }
@@ -281,27 +304,28 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
             load_ent(ent2, n + 2);
             prefetch_rows(ent1);
             bool ok = true;
-            for (int m = 0; m < G; ++m) {
-                const int u = n * G + m, s = u % kQSt;
-                if (!tc::mbar_wait(&q_empty[s], ((uint32_t)(u / kQSt) & 1u) ^ 1u, st, 141, abort_flag)) {
+            for (int m = 0; m < NSUB; ++m) {
+                const int u = n * NSUB + m, s = u % QST;
+                if (!tc::mbar_wait(&q_empty[s], ((uint32_t)(u / QST) & 1u) ^ 1u, st, 141, abort_flag)) {
                     ok = false;
                     break;
                 }
-                uint8_t *sq = sm + OFF_Q + s * TILE_Q;
+                uint8_t *sq = sm + OFF_Q + s * C::TILE_Q;
                 if constexpr (G == 8) {
                     // one box {64 features, 8 heads, 2 halves} per query fills a 2048-byte
                     // row group; padding queries read rows past the end (zero fill)
-                    const int e = ent_of(ent, m * QS + (lane & 7));
-                    if (lane == 0) tc::mbar_arrive_expect_tx(&q_full[s], TILE_Q);
+                    static_assert(QS <= 32 && (QS & (QS - 1)) == 0, "one lane per query");
+                    const int e = ent_of(ent, m * QS + (lane & (QS - 1)));
+                    if (lane == 0) tc::mbar_arrive_expect_tx(&q_full[s], C::TILE_Q);
                     __syncwarp();
                     if (lane < QS) {
                         const int z = e >= 0 ? b * p.Nq + entry_row(e) : p.B * p.Nq;
                         tc::tma_load_4d(sq + lane * 2048, &tmap_q, &q_full[s], 0, r * G, 0, z);
                     }
                 } else {
-                    // 64 rows x 16 chunks: lane covers chunk lane%16 of rows 2*it + lane/16
+                    // NS rows x 16 chunks: lane covers chunk lane%16 of rows 2*it + lane/16
 #pragma unroll 4
-                    for (int it = 0; it < 32; ++it) {
+                    for (int it = 0; it < C::NS / 2; ++it) {
                         const int rho = it * 2 + (lane >> 4), ch = lane & 15;
                         const int g = rho % G;
                         const int e = ent_of(ent, m * QS + rho / G);
@@ -395,26 +419,20 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
         cp_async_wait<0>();
     } else if (warp == 1) {
         if (lane == 0) {
-            // ------------------------------------------------ MMA issuer
-            constexpr uint32_t I_S = tc::idesc_bf16(128, 64);
-            constexpr uint32_t I_DQ = tc::idesc_bf16(128, 64) | tc::kAMajorMN | tc::kBMajorMN;
-            constexpr uint32_t I_DKI = tc::idesc_bf16(128, D) | tc::kBMajorMN;
+            // ------------------------------------------------ MMA issuer: S^T sub-chunks
+            constexpr uint32_t I_S = tc::idesc_bf16(128, C::NS);
             const uint64_t dK = tc::sdesc_k128(smem_u32(sm + OFF_K));
-            const uint32_t aKI = smem_u32(sm + OFF_KI);
-            const uint64_t dKI = tc::sdesc_k128(aKI), dKIT = tc::sdesc_sw128(aKI, SUBK, 1024);
-            const uint32_t sg = smem_u32(sm + OFF_SG);
-            const uint64_t dSGT = tc::sdesc_sw128(sg, SUBK, 1024), dSG = tc::sdesc_k128(sg);
             // S^T of sub-chunk u: A = K (K-major), B = the Q rows (K-major, 8-row groups 2048 bytes apart)
             auto issue_S = [&](int u) -> bool {
-                const int s = u % kQSt, slot = u % kSSlots;
-                if (!tc::mbar_wait(&q_full[s], (uint32_t)(u / kQSt) & 1u, st, 143, abort_flag)) return false;
-                if (u >= kSSlots &&
-                    !tc::mbar_wait(&s_free[slot], (uint32_t)(u / kSSlots - 1) & 1u, st, 144, abort_flag))
+                const int s = u % QST, slot = u % SSLOTS;
+                if (!tc::mbar_wait(&q_full[s], (uint32_t)(u / QST) & 1u, st, 143, abort_flag)) return false;
+                if (u >= SSLOTS &&
+                    !tc::mbar_wait(&s_free[slot], (uint32_t)(u / SSLOTS - 1) & 1u, st, 144, abort_flag))
                     return false;
                 tc::fence_proxy_async();
                 tc::fence_after_sync();
-                const uint64_t dQ = tc::sdesc_sw128(smem_u32(sm + OFF_Q + s * TILE_Q), 16, 2048);
-                const uint32_t ts = tmem + TM_S + slot * 64;
+                const uint64_t dQ = tc::sdesc_sw128(smem_u32(sm + OFF_Q + s * C::TILE_Q), 16, 2048);
+                const uint32_t ts = tmem + TM_S + slot * C::NS;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t h = ks >> 2, ko = (ks & 3) * 32;
@@ -424,6 +442,24 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
                 tc::mma_commit(&q_empty[s]);
                 return true;
             };
+            bool ok = tc::mbar_wait(kv_full, 0, st, 149, abort_flag);
+            for (int u = 0; ok && u < nch * NSUB; ++u) ok = issue_S(u);
+            tc::mma_commit(&done[0]);
+            tc::mbar_wait(&done[0], 0, nullptr, 0, nullptr);
+        }
+    } else if (warp == kIssI) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer: index scores and gradients.
+            // A thread of its own on another scheduler than the S^T issuer: every
+            // wait and issue of a single thread queues behind the epilogue's
+            // exponentials, so two issuers keep the tensor pipe fed.
+            constexpr uint32_t I_SI = tc::idesc_bf16(128, 64);
+            constexpr uint32_t I_DQ = tc::idesc_bf16(128, 64) | tc::kAMajorMN | tc::kBMajorMN;
+            constexpr uint32_t I_DKI = tc::idesc_bf16(128, D) | tc::kBMajorMN;
+            const uint32_t aKI = smem_u32(sm + OFF_KI);
+            const uint64_t dKI = tc::sdesc_k128(aKI), dKIT = tc::sdesc_sw128(aKI, SUBK, 1024);
+            const uint32_t sg = smem_u32(sm + OFF_SG);
+            const uint64_t dSGT = tc::sdesc_sw128(sg, SUBK, 1024), dSG = tc::sdesc_k128(sg);
             // s^T of chunk n: A = K_idx (K-major), B = the chunk's q_idx rows (K-major)
             auto issue_SI = [&](int n) -> bool {
                 const int s = n % kISt;
@@ -437,7 +473,7 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t h = ks >> 2, ko = (ks & 3) * 32;
                     tc::mma_bf16(tmem + TM_SI + (n & 1) * 64, tc::desc_adv(dKI, h * SUBK + ko),
-                                 tc::desc_adv(dI, h * SUBI + ko), I_S, ks > 0);
+                                 tc::desc_adv(dI, h * SUBI + ko), I_SI, ks > 0);
                 }
                 tc::mma_commit(&si_full[n & 1]);
                 if constexpr (!kGrad) tc::mma_commit(&i_empty[s]);
@@ -468,8 +504,7 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
             // tensor pipe works on them while the epilogue forms chunk n's dsig
             bool ok = tc::mbar_wait(kv_full, 0, st, 149, abort_flag);
             for (int n = 0; ok && n < nch; ++n) {
-                for (int m = 0; ok && m < G; ++m) ok = issue_S(n * G + m);
-                if (ok) ok = issue_SI(n);
+                ok = issue_SI(n);
                 if constexpr (kGrad) {
                     if (ok && n >= 1) ok = issue_G(n - 1);
                 }
@@ -477,14 +512,15 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
             if constexpr (kGrad) {
                 if (ok) ok = issue_G(nch - 1);
             }
-            tc::mma_commit(done);
-            tc::mbar_wait(done, 0, nullptr, 0, nullptr);
+            tc::mma_commit(&done[1]);
+            tc::mbar_wait(&done[1], 0, nullptr, 0, nullptr);
         }
     } else {
         // ------------------------------------------------ epilogue
-        constexpr int QW = kWC / G;                // queries of a sub-chunk in one column quarter
+        constexpr int QW = C::QW, PPS = C::PPS;    // queries, 8-column pieces of a sub-chunk per warp
         const int qd = warp & 3, cq = (warp - 2) >> 2;
-        const int c0 = cq * kWC;                   // the warp's first column
+        const int c0 = cq * kWC;                   // the warp's first s^T column
+        const int cw = cq * C::W;                  // the warp's first column of an S^T sub-chunk
         const int kr = qd * 32 + lane;             // key (score phases) or feature (dq_idx^T drain)
         const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
         const long long j = j0 + kr;
@@ -524,24 +560,25 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
             // no per-element mask where every valid query of the chunk sees the whole
             // block (padding columns carry lse = +inf and zero rows: they add nothing)
             const bool all_vis = (long long)mt->pmin >= j0 + kKeys - 1 && j0 + kKeys <= p.Nk;
-            // ---- teacher of this key for the warp's 16 queries, from the G sub-chunks.
-            // The warp's 16 columns of a sub-chunk are read as two 8-column pieces in
-            // a two-deep pipeline: piece i+1's TMEM load is in flight while piece i is
+            // ---- teacher of this key for the warp's 16 queries, from the NSUB sub-chunks.
+            // The warp's W columns of a sub-chunk are read as 8-column pieces in a
+            // two-deep pipeline: piece i+1's TMEM load is in flight while piece i is
             // summed (a wait covers every load issued before it, so one at a time).
-            constexpr int kPieces = 2 * G;
+            constexpr int kPieces = NSUB * PPS;
             float pt[kWC];
 #pragma unroll
             for (int k = 0; k < kWC; ++k) pt[k] = 0.f;
             auto teacher = [&](auto all_tag) {
                 constexpr bool kAll = decltype(all_tag)::value;
                 uint32_t buf[2][8];
-                auto issue = [&](int i) -> bool {       // piece i: sub-chunk i/2, columns c0 + 8*(i%2)
-                    const int u = n * G + i / 2;
-                    if ((i & 1) == 0) {
-                        if (!wwait(&s_full[u % kSSlots], (uint32_t)(u / kSSlots) & 1u, st, 152, abort_flag)) return false;
+                auto issue = [&](int i) -> bool {       // piece i: sub-chunk i/PPS, columns cw + 8*(i%PPS)
+                    const int u = n * NSUB + i / PPS;
+                    if (i % PPS == 0) {
+                        if (!wwait(&s_full[u % SSLOTS], (uint32_t)(u / SSLOTS) & 1u, st, 152, abort_flag)) return false;
                         tc::fence_after_sync();
                     }
-                    tc::tmem_ld8_nowait(tmem + lane_base + TM_S + (u % kSSlots) * 64 + c0 + 8 * (i & 1), buf[i & 1]);
+                    tc::tmem_ld8_nowait(tmem + lane_base + TM_S + (u % SSLOTS) * C::NS + cw + 8 * (i % PPS),
+                                        buf[i & 1]);
                     return true;
                 };
                 if (!(ok = issue(0))) return;
@@ -551,21 +588,21 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
                     if (i + 1 < kPieces) {
                         if (!(ok = issue(i + 1))) return;
                     }
-                    if (i & 1) {
-                        // both pieces of sub-chunk i/2 are in registers: its slot is free
+                    if (i % PPS == PPS - 1) {
+                        // every piece of sub-chunk i/PPS is in registers: its slot is free
                         tc::fence_before_sync();
                         __syncwarp();
-                        if (lane == 0) tc::mbar_arrive(&s_free[(n * G + i / 2) % kSSlots]);
+                        if (lane == 0) tc::mbar_arrive(&s_free[(n * NSUB + i / PPS) % SSLOTS]);
                     }
-                    const int m = i / 2;
-                    const float4 *l2 = reinterpret_cast<const float4 *>(mt->lse2 + (c0 + m * QW) * G + 8 * (i & 1));
+                    const int m = i / PPS, part = i % PPS;
+                    const float4 *l2 = reinterpret_cast<const float4 *>(mt->lse2 + (c0 + m * QW) * G + 8 * part);
 #pragma unroll
                     for (int r4 = 0; r4 < 2; ++r4) {
                         const float4 l = l2[r4];
                         const float lv4[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const int rho = 8 * (i & 1) + 4 * r4 + e, k = m * QW + rho / G;
+                            const int rho = 8 * part + 4 * r4 + e, k = m * QW + rho / G;
                             const float x = tc::ex2(__uint_as_float(buf[i & 1][4 * r4 + e]) * sl2 - lv4[e]);
                             if constexpr (kAll) pt[k] += x;
                             else pt[k] += (key_ok && ji <= mt->pos[c0 + k]) ? x : 0.f;
