@@ -5,9 +5,9 @@
 // indexer is fitted to the main attention with full attention kept: the
 // teacher is the main branch's probabilities over the whole visible prefix
 // and the student the index scores' softmax over the same prefix.  Section
-// 3.2: "after a dense warm-up, MSA computes the KL over tokens in the
-// selected blocks" -- with every visible block selected the two are the same
-// loss, so the warm-up runs MSA's own block-sparse kernels on this selection.
+// 3.2 then restricts MSA's KL to the tokens of the selected blocks; with
+// every visible block selected the two are the same loss, so the warm-up
+// runs MSA's own block-sparse kernels on this selection.
 #include "msa_internal.h"
 
 namespace msa {

@@ -212,8 +212,8 @@ msa_status msa_train_step_staged(const msa_shape *shape, const void *q, const vo
 
 /*
  * Dense indexer warm-up (section 3.1, the warm-up loss L^I_warm, in MSA's
- * per-group form of section 3.2: "after a dense warm-up, MSA computes the KL
- * over tokens in the selected blocks").  Full attention is kept: for each
+ * per-group form of section 3.2, which follows the warm-up with the same KL
+ * restricted to the selected blocks).  Full attention is kept: for each
  * query i and group r over EVERY visible key j <= i,
  *   teacher  Pt_j = (1/G) sum_{h in r} softmax_j(l_{h,j})   (detached)
  *   student  Ps_j = softmax_j(s_j),  s_j = scale_idx <q_idx, k_idx_j>

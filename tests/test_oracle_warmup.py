@@ -2,8 +2,8 @@
 
 "Sparse Attention · Part II": section 3.2's detachment equation
 (Q_idx = stopgrad(X) W_q^idx, K_idx = stopgrad(X) W_k^idx) and section
-3.1's dense warm-up loss, in MSA's per-group form ("after a dense warm-up,
-MSA computes the KL over tokens in the selected blocks").  Each pin checks
+3.1's dense warm-up loss, in MSA's per-group form (section 3.2 follows the
+warm-up with the same KL restricted to the selected blocks).  Each pin checks
 the oracle against something other than itself: one-hot inputs, the
 adjoint identity of a linear map, the block-sparse KL with every visible
 block selected (a different formulation: blocks, selection and token sets),
