@@ -585,14 +585,16 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
                 tc::tmem_wait8(buf[0]);
 #pragma unroll
                 for (int i = 0; i < kPieces; ++i) {
-                    if (i + 1 < kPieces) {
-                        if (!(ok = issue(i + 1))) return;
-                    }
-                    if (i % PPS == PPS - 1) {
-                        // every piece of sub-chunk i/PPS is in registers: its slot is free
+                    // At a sub-chunk's last piece the slot is released first (every
+                    // piece is in registers) and the next sub-chunk is waited for only
+                    // after this piece's sums, so neither wait holds up the other slot.
+                    const bool last = i % PPS == PPS - 1;
+                    if (last) {
                         tc::fence_before_sync();
                         __syncwarp();
                         if (lane == 0) tc::mbar_arrive(&s_free[(n * NSUB + i / PPS) % SSLOTS]);
+                    } else if (i + 1 < kPieces) {
+                        if (!(ok = issue(i + 1))) return;
                     }
                     const int m = i / PPS, part = i % PPS;
                     const float4 *l2 = reinterpret_cast<const float4 *>(mt->lse2 + (c0 + m * QW) * G + 8 * part);
@@ -607,6 +609,9 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
                             if constexpr (kAll) pt[k] += x;
                             else pt[k] += (key_ok && ji <= mt->pos[c0 + k]) ? x : 0.f;
                         }
+                    }
+                    if (last && i + 1 < kPieces) {
+                        if (!(ok = issue(i + 1))) return;
                     }
                     if (i + 1 < kPieces) tc::tmem_wait8(buf[(i + 1) & 1]);
                 }
