@@ -125,8 +125,10 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
 {
     constexpr int QC = kRows / G;                 // queries per chunk
     constexpr int EPL = (QC + 31) / 32;           // bucket entries per producer lane
-    // x = group, y = key block: the heavy early blocks of every group start first
-    const int r = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
+    // the (group, block) bucket of this CTA (visiting order: bucket_of)
+    int r, c;
+    bucket_of((int)blockIdx.x, p.Hkv, p.nb, p.num_sms, r, c);
+    const int b = blockIdx.y;
     const long long bucket = ((long long)b * p.Hkv + r) * p.nb + c;
     const int qbeg = bucket_off[bucket], qend = bucket_off[bucket + 1];
     const int nch = (qend - qbeg + QC - 1) / QC;
@@ -573,7 +575,7 @@ cudaError_t launch_g(const Problem &p, const bf16 *q, const bf16 *k, const bf16 
     }
     {
         TimedLaunch timed_("bwd_main_tc_kernel", s);
-        bwd_main_tc_kernel<G><<<dim3(p.Hkv, p.nb, p.B), kThreads, ALLOC, s>>>(
+        bwd_main_tc_kernel<G><<<dim3(p.Hkv * p.nb, p.B), kThreads, ALLOC, s>>>(
             tq, tdo, tk, tv, p, q, d_o, lse, w.D, w.bucket_off, w.bucket_q, dk, dv, w.dq_part, st);
     }
     note_launch();

@@ -192,7 +192,10 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
     using C = Cfg<G>;
     constexpr int QS = C::QS, NSUB = C::NSUB, QST = C::QST, SSLOTS = C::SSLOTS;
     using MetaT = Meta<G>;
-    const int r = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
+    // the (group, block) bucket of this CTA (visiting order: bucket_of)
+    int r, c;
+    bucket_of((int)blockIdx.x, p.Hkv, p.nb, p.num_sms, r, c);
+    const int b = blockIdx.y;
     const long long bucket = ((long long)b * p.Hkv + r) * p.nb + c;
     const int qbeg = bucket_off[bucket], qend = bucket_off[bucket + 1];
     const long long j0 = (long long)c * kKeys;
@@ -805,7 +808,7 @@ cudaError_t launch_g(const Problem &p, const bf16 *q, const bf16 *k, const bf16 
     }
     {
         TimedLaunch timed_(kGrad ? "index_teacher_bwd_tc_kernel" : "index_teacher_kl_tc_kernel", s);
-        index_teacher_tc_kernel<G, kGrad><<<dim3(p.Hkv, p.nb, p.B), kThreads, ALLOC, s>>>(
+        index_teacher_tc_kernel<G, kGrad><<<dim3(p.Hkv * p.nb, p.B), kThreads, ALLOC, s>>>(
             tq, tk, tki, p, q, q_idx, lse, lse_idx, coef, bucket_off, bucket_q, klt, dqi_part, dki_g, st);
     }
     note_launch();

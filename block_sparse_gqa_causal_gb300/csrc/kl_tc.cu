@@ -86,7 +86,10 @@ kl_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, const
 {
     using L = IndexLayout<DI>;
     using Meta = typename L::Meta;
-    const int r = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
+    // the (group, block) bucket of this CTA (visiting order: bucket_of)
+    int r, c;
+    bucket_of((int)blockIdx.x, p.Hkv, p.nb, p.num_sms, r, c);
+    const int b = blockIdx.y;
     const long long bucket = ((long long)b * p.Hkv + r) * p.nb + c;
     const int qbeg = bucket_off[bucket], qend = bucket_off[bucket + 1];
     if (qend <= qbeg) return;
@@ -289,7 +292,7 @@ cudaError_t launch_index(const Problem &p, const bf16 *q_idx, const bf16 *k_idx,
     if ((e = make_tmap_bf16(&tki, k_idx, 3, di, si, bi)) != cudaSuccess) return e;
     {
         TimedLaunch timed_("kl_index_tc_kernel", s);
-        kl_index_tc_kernel<DI><<<dim3(p.Hkv, p.nb, p.B), kThreads, L::ALLOC, s>>>(tki, p, q_idx, w.bucket_off,
+        kl_index_tc_kernel<DI><<<dim3(p.Hkv * p.nb, p.B), kThreads, L::ALLOC, s>>>(tki, p, q_idx, w.bucket_off,
                                                                                   w.bucket_q, w.part, st);
     }
     note_launch();

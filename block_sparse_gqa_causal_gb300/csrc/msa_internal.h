@@ -172,6 +172,26 @@ __host__ __device__ __forceinline__ int entry_slot(int32_t e) { return (int)((ui
 cudaError_t launch_inverse_index(const Problem &p, const int32_t *sel, int32_t *cnt, int32_t *off, int32_t *scratch,
                                  int32_t *list, DeviceStatus *st, cudaStream_t s);
 
+// Order in which the key-major kernels visit the (group, key block) buckets
+// of a batch: CTA x of a grid of Hkv * nb, early (larger) blocks first.
+// When a group's blocks span several waves of the GPU (long sequences), the
+// buckets go group by group, so the CTAs resident at one time share a
+// group's query rows in L2 (each query's rows are gathered by every block it
+// selected; at 131,072 tokens this saves 2 ms of a training step).  With
+// fewer blocks the groups are interleaved instead (block c of every group,
+// then c + 1): there the longest CTAs must start together or they make a
+// tail, which costs more than L2 reuse gains (measured at 8,192 and 32,768).
+__host__ __device__ __forceinline__ void bucket_of(int x, int Hkv, int nb, int num_sms, int &r, int &c)
+{
+    if (nb >= 4 * num_sms) {
+        r = x / nb;
+        c = x % nb;
+    } else {
+        r = x % Hkv;
+        c = x / Hkv;
+    }
+}
+
 // The backward runs on the tcgen05 kernels when d = d_idx = 128.
 inline bool bwd_tc(const Problem &p) { return p.d == 128 && p.d_idx == 128; }
 // tcgen05 main-branch backward (d = 128): dK, dV and the dQ partials.

@@ -118,8 +118,10 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
 {
     using L = FwdLayout<D>;
     constexpr int QPC = kRows / G;                          // queries per chunk
-    // x = group, y = key block: the heavy early blocks of every group start first
-    const int r = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
+    // the (group, block) bucket of this CTA (visiting order: bucket_of)
+    int r, c;
+    bucket_of((int)blockIdx.x, p.Hkv, p.nb, p.num_sms, r, c);
+    const int b = blockIdx.y;
     const long long bucket = ((long long)b * p.Hkv + r) * p.nb + c;
     const int qbeg = bucket_off[bucket], qend = bucket_off[bucket + 1];
     if (qend <= qbeg) return;                               // nobody selected this block
@@ -576,7 +578,7 @@ cudaError_t launch_dg(const Problem &p, const bf16 *q, const bf16 *k, const bf16
     }
     {
         TimedLaunch timed_("sparse_fwd_tc_kernel", s);
-        sparse_fwd_tc_kernel<D, G><<<dim3(p.Hkv, p.nb, p.B), kThreads, L::ALLOC, s>>>(
+        sparse_fwd_tc_kernel<D, G><<<dim3(p.Hkv * p.nb, p.B), kThreads, L::ALLOC, s>>>(
             tq, tk, tv, p, q, w.bucket_off, w.bucket_q, w.part, w.stats, st);
     }
     note_launch();
