@@ -421,37 +421,41 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
         }
         cp_async_wait<0>();
     } else if (warp == 1) {
-        if (lane == 0) {
+        {
             // ------------------------------------------------ MMA issuer: S^T sub-chunks
+            // (the whole warp runs the loop; one elected lane issues)
             constexpr uint32_t I_S = tc::idesc_bf16(128, C::NS);
             const uint64_t dK = tc::sdesc_k128(smem_u32(sm + OFF_K));
             // S^T of sub-chunk u: A = K (K-major), B = the Q rows (K-major, 8-row groups 2048 bytes apart)
             auto issue_S = [&](int u) -> bool {
                 const int s = u % QST, slot = u % SSLOTS;
-                if (!tc::mbar_wait(&q_full[s], (uint32_t)(u / QST) & 1u, st, 143, abort_flag)) return false;
-                if (u >= SSLOTS &&
-                    !tc::mbar_wait(&s_free[slot], (uint32_t)(u / SSLOTS - 1) & 1u, st, 144, abort_flag))
+                if (!wwait(&q_full[s], (uint32_t)(u / QST) & 1u, st, 143, abort_flag)) return false;
+                if (u >= SSLOTS && !wwait(&s_free[slot], (uint32_t)(u / SSLOTS - 1) & 1u, st, 144, abort_flag))
                     return false;
                 tc::fence_proxy_async();
                 tc::fence_after_sync();
                 const uint64_t dQ = tc::sdesc_sw128(smem_u32(sm + OFF_Q + s * C::TILE_Q), 16, 2048);
                 const uint32_t ts = tmem + TM_S + slot * C::NS;
+                if (tc::elect_one()) {
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t h = ks >> 2, ko = (ks & 3) * 32;
-                    tc::mma_bf16(ts, tc::desc_adv(dK, h * SUBK + ko), tc::desc_adv(dQ, h * 1024 + ko), I_S, ks > 0);
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint32_t h = ks >> 2, ko = (ks & 3) * 32;
+                        tc::mma_bf16(ts, tc::desc_adv(dK, h * SUBK + ko), tc::desc_adv(dQ, h * 1024 + ko), I_S, ks > 0);
+                    }
+                    tc::mma_commit(&s_full[slot]);
+                    tc::mma_commit(&q_empty[s]);
                 }
-                tc::mma_commit(&s_full[slot]);
-                tc::mma_commit(&q_empty[s]);
+                __syncwarp();
                 return true;
             };
-            bool ok = tc::mbar_wait(kv_full, 0, st, 149, abort_flag);
+            bool ok = wwait(kv_full, 0, st, 149, abort_flag);
             for (int u = 0; ok && u < nch * NSUB; ++u) ok = issue_S(u);
-            tc::mma_commit(&done[0]);
+            if (tc::elect_one()) tc::mma_commit(&done[0]);
+            __syncwarp();
             tc::mbar_wait(&done[0], 0, nullptr, 0, nullptr);
         }
     } else if (warp == kIssI) {
-        if (lane == 0) {
+        {
             // ------------------------------------------------ MMA issuer: index scores and gradients.
             // A thread of its own on another scheduler than the S^T issuer: every
             // wait and issue of a single thread queues behind the epilogue's
@@ -466,46 +470,52 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
             // s^T of chunk n: A = K_idx (K-major), B = the chunk's q_idx rows (K-major)
             auto issue_SI = [&](int n) -> bool {
                 const int s = n % kISt;
-                if (!tc::mbar_wait(&i_full[s], (uint32_t)(n / kISt) & 1u, st, 145, abort_flag)) return false;
-                if (n >= 2 && !tc::mbar_wait(&si_free[n & 1], (uint32_t)((n >> 1) - 1) & 1u, st, 146, abort_flag))
+                if (!wwait(&i_full[s], (uint32_t)(n / kISt) & 1u, st, 145, abort_flag)) return false;
+                if (n >= 2 && !wwait(&si_free[n & 1], (uint32_t)((n >> 1) - 1) & 1u, st, 146, abort_flag))
                     return false;
                 tc::fence_proxy_async();
                 tc::fence_after_sync();
                 const uint64_t dI = tc::sdesc_k128(smem_u32(sm + OFF_I + s * TILE_I));
+                if (tc::elect_one()) {
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t h = ks >> 2, ko = (ks & 3) * 32;
-                    tc::mma_bf16(tmem + TM_SI + (n & 1) * 64, tc::desc_adv(dKI, h * SUBK + ko),
-                                 tc::desc_adv(dI, h * SUBI + ko), I_SI, ks > 0);
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint32_t h = ks >> 2, ko = (ks & 3) * 32;
+                        tc::mma_bf16(tmem + TM_SI + (n & 1) * 64, tc::desc_adv(dKI, h * SUBK + ko),
+                                     tc::desc_adv(dI, h * SUBI + ko), I_SI, ks > 0);
+                    }
+                    tc::mma_commit(&si_full[n & 1]);
+                    if constexpr (!kGrad) tc::mma_commit(&i_empty[s]);
                 }
-                tc::mma_commit(&si_full[n & 1]);
-                if constexpr (!kGrad) tc::mma_commit(&i_empty[s]);
+                __syncwarp();
                 return true;
             };
             // gradients of chunk n from the dsig tile; dq_idx^T goes over chunk n's s^T
             // (the epilogue has read it before writing dsig)
             auto issue_G = [&](int n) -> bool {
-                if (!tc::mbar_wait(g_full, (uint32_t)n & 1u, st, 147, abort_flag)) return false;
+                if (!wwait(g_full, (uint32_t)n & 1u, st, 147, abort_flag)) return false;
                 tc::fence_after_sync();
                 const uint64_t dIm = tc::sdesc_sw128(smem_u32(sm + OFF_I + (n % kISt) * TILE_I), SUBI, 1024);
-                // dq_idx^T = K_idx^T dsig^T: both operands MN-major; K = 128 keys
+                if (tc::elect_one()) {
+                    // dq_idx^T = K_idx^T dsig^T: both operands MN-major; K = 128 keys
 #pragma unroll
-                for (int ks = 0; ks < kKeys / 16; ++ks)
-                    tc::mma_bf16(tmem + TM_SI + (n & 1) * 64, tc::desc_adv(dKIT, ks * 2048),
-                                 tc::desc_adv(dSGT, ks * 2048), I_DQ, ks > 0);
-                tc::mma_commit(&dq_full[n & 1]);
-                // dK_idx += dsig q_idx: A K-major over queries, B = q_idx MN-major; K = 64 queries
+                    for (int ks = 0; ks < kKeys / 16; ++ks)
+                        tc::mma_bf16(tmem + TM_SI + (n & 1) * 64, tc::desc_adv(dKIT, ks * 2048),
+                                     tc::desc_adv(dSGT, ks * 2048), I_DQ, ks > 0);
+                    tc::mma_commit(&dq_full[n & 1]);
+                    // dK_idx += dsig q_idx: A K-major over queries, B = q_idx MN-major; K = 64 queries
 #pragma unroll
-                for (int ks = 0; ks < kQ / 16; ++ks)
-                    tc::mma_bf16(tmem + TM_DKI, tc::desc_adv(dSG, ks * 32), tc::desc_adv(dIm, ks * 2048), I_DKI,
-                                 n > 0 || ks > 0);
-                tc::mma_commit(&i_empty[n % kISt]);
-                tc::mma_commit(g_free);
+                    for (int ks = 0; ks < kQ / 16; ++ks)
+                        tc::mma_bf16(tmem + TM_DKI, tc::desc_adv(dSG, ks * 32), tc::desc_adv(dIm, ks * 2048), I_DKI,
+                                     n > 0 || ks > 0);
+                    tc::mma_commit(&i_empty[n % kISt]);
+                    tc::mma_commit(g_free);
+                }
+                __syncwarp();
                 return true;
             };
             // the scores of chunk n+1 are issued before the gradients of chunk n, so the
             // tensor pipe works on them while the epilogue forms chunk n's dsig
-            bool ok = tc::mbar_wait(kv_full, 0, st, 149, abort_flag);
+            bool ok = wwait(kv_full, 0, st, 149, abort_flag);
             for (int n = 0; ok && n < nch; ++n) {
                 ok = issue_SI(n);
                 if constexpr (kGrad) {
@@ -515,7 +525,8 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
             if constexpr (kGrad) {
                 if (ok) ok = issue_G(nch - 1);
             }
-            tc::mma_commit(&done[1]);
+            if (tc::elect_one()) tc::mma_commit(&done[1]);
+            __syncwarp();
             tc::mbar_wait(&done[1], 0, nullptr, 0, nullptr);
         }
     } else {

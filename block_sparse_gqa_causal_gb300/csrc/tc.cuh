@@ -167,6 +167,17 @@ MSA_DEV void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate));
 }
 
+// One lane of a converged warp (the lowest active one) gets true: the lane
+// that issues a warp's tensor-core instructions, so that the code around
+// them (waits, descriptors) runs warp-uniform.
+MSA_DEV bool elect_one()
+{
+    uint32_t pred = 0;
+    asm volatile("{\n .reg .pred p;\n .reg .b32 r;\n elect.sync r|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n"
+                 : "=r"(pred));
+    return pred != 0;
+}
+
 // Arrive on `bar` once every tcgen05.mma issued so far by this thread is done.
 MSA_DEV void mma_commit(uint64_t *bar)
 {
