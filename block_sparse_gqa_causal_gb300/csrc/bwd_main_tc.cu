@@ -290,8 +290,9 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         }
         cp_async_wait<0>();
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ------------------------------------------------ MMA issuer
+        {
+            // ------------------------------------------------ MMA issuer (the whole warp
+            // runs the loop; one lane chosen by elect.sync issues)
             constexpr uint32_t I_S = tc::idesc_bf16(128, kRows);
             const uint64_t dK = tc::sdesc_k128(smem_u32(sm + OFF_K)), dV = tc::sdesc_k128(smem_u32(sm + OFF_V));
             auto issue_scores = [&](int n) {
@@ -299,38 +300,42 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 const uint32_t sq = smem_u32(sm + OFF_STG + (n % kStages) * STG_BYTES);
                 const uint64_t dQ = tc::sdesc_sw128(sq, 16, 2048), dDO = tc::sdesc_sw128(sq + TILE_R, 16, 2048);
                 const uint32_t ts = tmem + TM_SLOT + (n & 1) * 128;
+                if (tc::elect_one()) {
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t h = ks >> 2, ko = (ks & 3) * 32;
-                    tc::mma_bf16(ts, tc::desc_adv(dK, h * SUBK + ko), tc::desc_adv(dQ, h * 1024 + ko), I_S, ks > 0);
-                    tc::mma_bf16(ts + TM_DP_OFF, tc::desc_adv(dV, h * SUBK + ko), tc::desc_adv(dDO, h * 1024 + ko), I_S,
-                                 ks > 0);
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint32_t h = ks >> 2, ko = (ks & 3) * 32;
+                        tc::mma_bf16(ts, tc::desc_adv(dK, h * SUBK + ko), tc::desc_adv(dQ, h * 1024 + ko), I_S, ks > 0);
+                        tc::mma_bf16(ts + TM_DP_OFF, tc::desc_adv(dV, h * SUBK + ko), tc::desc_adv(dDO, h * 1024 + ko),
+                                     I_S, ks > 0);
+                    }
+                    tc::mma_commit(&s_full[n & 1]);
                 }
-                tc::mma_commit(&s_full[n & 1]);
+                __syncwarp();
             };
             // Scores here, gradients on warp kGradWarp: the two streams touch
             // disjoint TMEM and shared memory, are ordered only through the
             // mbarriers, and issuing them from two threads overlaps their issue.
-            bool ok = tc::mbar_wait(kv_full, 0, st, 102, abort_flag);
+            bool ok = wwait(kv_full, 0, st, 102, abort_flag);
             if (ok) tc::fence_proxy_async();
             for (int ns = 0; ok && ns < nch; ++ns) {
-                if (!tc::mbar_wait(&full[ns % kStages], (uint32_t)(ns / kStages) & 1u, st, 103, abort_flag)) break;
+                if (!wwait(&full[ns % kStages], (uint32_t)(ns / kStages) & 1u, st, 103, abort_flag)) break;
                 // the slot's previous chunk (ns-2) has had its dQ^T drained
-                if (ns >= 2 &&
-                    !tc::mbar_wait(&slot_free[ns & 1], (uint32_t)((ns >> 1) - 1) & 1u, st, 104, abort_flag))
+                if (ns >= 2 && !wwait(&slot_free[ns & 1], (uint32_t)((ns >> 1) - 1) & 1u, st, 104, abort_flag))
                     break;
                 tc::fence_proxy_async();
                 tc::fence_after_sync();
                 issue_scores(ns);
             }
-            // every MMA this thread issued has completed once `done` fires (it also
+            // every MMA this warp issued has completed once `done` fires (it also
             // waits for the gradient issuer's commit)
-            tc::mma_commit(done);
+            if (tc::elect_one()) tc::mma_commit(done);
+            __syncwarp();
             tc::mbar_wait(done, 0, nullptr, 0, nullptr);
         }
     } else if (warp == kGradWarp) {
-        if (lane == 0) {
-            // ------------------------------------------------ MMA issuer: gradients
+        {
+            // ------------------------------------------------ MMA issuer: gradients (warp-uniform,
+            // one elected lane issues)
             constexpr uint32_t I_DKV = tc::idesc_bf16(128, 128) | tc::kBMajorMN;
             constexpr uint32_t I_DQ = tc::idesc_bf16(128, kRows) | tc::kAMajorMN | tc::kBMajorMN;
             const uint64_t dKT = tc::sdesc_sw128(smem_u32(sm + OFF_K), SUBK, 1024);
@@ -344,31 +349,35 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 // of the K dimension: warp half ks/2, 8 packed columns per step), B =
                 // dO / Q read MN-major (feature halves 1024 bytes apart, 8-row groups
                 // 2048 apart); K = 64 rows
-#pragma unroll
-                for (int ks = 0; ks < kRows / 16; ++ks) {
-                    const bool acc = n > 0 || ks > 0;
-                    const uint32_t col = (ks >> 1) * 32 + (ks & 1) * 8;
-                    tc::mma_bf16_ts(tmem + TM_DV, ts + col, tc::desc_adv(dDOm, ks * 4096), I_DKV, acc);
-                    tc::mma_bf16_ts(tmem + TM_DK, ts + col + 16, tc::desc_adv(dQm, ks * 4096), I_DKV, acc);
-                }
-                tc::mma_commit(&empty[n % kStages]);
                 // dQ^T = K^T dS^T over the slot's S^T half (in order after the MMAs
-                // above have read it): A = K read MN-major (64-feature atoms SUBK
+                // below have read it): A = K read MN-major (64-feature atoms SUBK
                 // apart), B = dS^T [keys][rows] MN-major; K = 128 keys
                 const uint64_t dDST = tc::desc_adv(dDST0, db * SUBK);
+                if (tc::elect_one()) {
 #pragma unroll
-                for (int ks = 0; ks < kKeys / 16; ++ks)
-                    tc::mma_bf16(ts, tc::desc_adv(dKT, ks * 2048), tc::desc_adv(dDST, ks * 2048), I_DQ, ks > 0);
-                tc::mma_commit(&dq_full[n & 1]);
-                tc::mma_commit(&ds_free[db]);
+                    for (int ks = 0; ks < kRows / 16; ++ks) {
+                        const bool acc = n > 0 || ks > 0;
+                        const uint32_t col = (ks >> 1) * 32 + (ks & 1) * 8;
+                        tc::mma_bf16_ts(tmem + TM_DV, ts + col, tc::desc_adv(dDOm, ks * 4096), I_DKV, acc);
+                        tc::mma_bf16_ts(tmem + TM_DK, ts + col + 16, tc::desc_adv(dQm, ks * 4096), I_DKV, acc);
+                    }
+                    tc::mma_commit(&empty[n % kStages]);
+#pragma unroll
+                    for (int ks = 0; ks < kKeys / 16; ++ks)
+                        tc::mma_bf16(ts, tc::desc_adv(dKT, ks * 2048), tc::desc_adv(dDST, ks * 2048), I_DQ, ks > 0);
+                    tc::mma_commit(&dq_full[n & 1]);
+                    tc::mma_commit(&ds_free[db]);
+                }
+                __syncwarp();
             };
-            bool ok = tc::mbar_wait(kv_full, 0, st, 105, abort_flag);
+            bool ok = wwait(kv_full, 0, st, 105, abort_flag);
             for (int ng = 0; ok && ng < nch; ++ng) {
-                if (!tc::mbar_wait(&p_full[ng % kDsBuf], (uint32_t)(ng / kDsBuf) & 1u, st, 106, abort_flag)) break;
+                if (!wwait(&p_full[ng % kDsBuf], (uint32_t)(ng / kDsBuf) & 1u, st, 106, abort_flag)) break;
                 tc::fence_after_sync();
                 issue_grads(ng);
             }
-            tc::mma_commit(done);
+            if (tc::elect_one()) tc::mma_commit(done);
+            __syncwarp();
         }
     } else if (warp >= 4 + kEpiWarps) {
         // ------------------------------------------------ dQ^T drain: features 32*qd.. of all 64 rows
