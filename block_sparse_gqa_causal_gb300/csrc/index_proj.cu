@@ -104,13 +104,14 @@ index_proj_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ------------------------------------------------ MMA issuer
+        {
+            // ------------------------------------------------ MMA issuer (warp-uniform; one
+            // elect.sync lane issues)
             constexpr uint32_t I = tc::idesc_bf16(BM, BN) | tc::kBMajorMN | (kGradW ? tc::kAMajorMN : 0u);
             bool ok = true;
             for (int kb = kb0; ok && kb < kb1; ++kb) {
                 const int it = kb - kb0, s = it % kSt;
-                if (!tc::mbar_wait(&full[s], (uint32_t)(it / kSt) & 1u, st, 162, abort_flag)) {
+                if (!tc::mbar_wait_warp(&full[s], (uint32_t)(it / kSt) & 1u, st, 162, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -118,13 +119,17 @@ index_proj_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
                 const uint32_t sa = smem_u32(sm + s * STAGE), sb = sa + SUB;
                 const uint64_t dA = kGradW ? tc::sdesc_sw128(sa, SUB / 2, 1024) : tc::sdesc_k128(sa);
                 const uint64_t dB = tc::sdesc_sw128(sb, SUB / 2, 1024);
+                if (tc::elect_one()) {
 #pragma unroll
-                for (int ks = 0; ks < BK / 16; ++ks)
-                    tc::mma_bf16(tmem, tc::desc_adv(dA, kGradW ? ks * 2048 : ks * 32), tc::desc_adv(dB, ks * 2048), I,
-                                 it > 0 || ks > 0);
-                tc::mma_commit(&empty[s]);
+                    for (int ks = 0; ks < BK / 16; ++ks)
+                        tc::mma_bf16(tmem, tc::desc_adv(dA, kGradW ? ks * 2048 : ks * 32), tc::desc_adv(dB, ks * 2048),
+                                     I, it > 0 || ks > 0);
+                    tc::mma_commit(&empty[s]);
+                }
+                __syncwarp();
             }
-            tc::mma_commit(acc_full);
+            if (tc::elect_one()) tc::mma_commit(acc_full);
+            __syncwarp();
         }
     } else {
         // ------------------------------------------------ epilogue: row m0 + 32*(warp%4) + lane

@@ -144,9 +144,9 @@ index_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ---------------- MMA issuer
-            bool ok = tc::mbar_wait(q_full, 0, st, 12, abort_flag);
+        {
+            // ---------------- MMA issuer (warp-uniform; one elect.sync lane issues)
+            bool ok = tc::mbar_wait_warp(q_full, 0, st, 12, abort_flag);
             const uint64_t dq = tc::sdesc_k128(smem_u32(sQ));
             int issued = 0;
             for (int n = 0; ok && n < nblk; ++n) {
@@ -154,20 +154,24 @@ index_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_
                 const uint32_t ph = (uint32_t)(n / kStages) & 1u;
                 const int a = n & 1;
                 const uint32_t aph = (uint32_t)(n >> 1) & 1u;
-                if (!tc::mbar_wait(&acc_empty[a], aph ^ 1u, st, 13, abort_flag)) break;
-                if (!tc::mbar_wait(&full[s], ph, st, 14, abort_flag)) break;
+                if (!tc::mbar_wait_warp(&acc_empty[a], aph ^ 1u, st, 13, abort_flag)) break;
+                if (!tc::mbar_wait_warp(&full[s], ph, st, 14, abort_flag)) break;
                 tc::fence_after_sync();
                 const uint64_t dk = tc::sdesc_k128(smem_u32(sK + s * S::K_BYTES));
-                for (int m = 0; m < mt; ++m) {
-                    const uint32_t d = tmem + (uint32_t)((a * 2 + m) * 128);
+                if (tc::elect_one()) {
+                    for (int m = 0; m < mt; ++m) {
+                        const uint32_t d = tmem + (uint32_t)((a * 2 + m) * 128);
 #pragma unroll
-                    for (int ks = 0; ks < DI / 16; ++ks) {
-                        const uint32_t off = (ks >> 2) * kSub + (ks & 3) * 32;
-                        tc::mma_bf16(d, tc::desc_adv(dq, m * S::KB * kSub + off), tc::desc_adv(dk, off), kIdesc, ks > 0);
+                        for (int ks = 0; ks < DI / 16; ++ks) {
+                            const uint32_t off = (ks >> 2) * kSub + (ks & 3) * 32;
+                            tc::mma_bf16(d, tc::desc_adv(dq, m * S::KB * kSub + off), tc::desc_adv(dk, off), kIdesc,
+                                         ks > 0);
+                        }
                     }
+                    tc::mma_commit(&empty[s]);
+                    tc::mma_commit(&acc_full[a]);
                 }
-                tc::mma_commit(&empty[s]);
-                tc::mma_commit(&acc_full[a]);
+                __syncwarp();
                 issued = n + 1;
             }
             if (*abort_flag && issued > 0) {

@@ -177,26 +177,31 @@ kl_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, const
         }
         cp_async_wait<0>();
     } else if (warp == 1) {
-        if (lane == 0) {
+        {
             // ------------------------------------------------ MMA issuer: s = q_idx K_idx^T
+            // (warp-uniform; one elect.sync lane issues)
             constexpr uint32_t I_S = tc::idesc_bf16(128, kKeys);
             const uint64_t dKI = tc::sdesc_k128(smem_u32(sm + L::OFF_KI));
-            bool ok = tc::mbar_wait(kv_full, 0, st, 86, abort_flag);
+            bool ok = wwait(kv_full, 0, st, 86, abort_flag);
             for (int n = 0; ok && n < nch; ++n) {
-                if (!tc::mbar_wait(&full[n % kStages], (uint32_t)(n / kStages) & 1u, st, 87, abort_flag)) break;
-                if (n >= 2 && !tc::mbar_wait(&s_free[n & 1], ((uint32_t)(n >> 1) & 1u) ^ 1u, st, 88, abort_flag)) break;
+                if (!wwait(&full[n % kStages], (uint32_t)(n / kStages) & 1u, st, 87, abort_flag)) break;
+                if (n >= 2 && !wwait(&s_free[n & 1], ((uint32_t)(n >> 1) & 1u) ^ 1u, st, 88, abort_flag)) break;
                 tc::fence_proxy_async();
                 tc::fence_after_sync();
                 const uint64_t dQ = tc::sdesc_k128(smem_u32(sm + L::OFF_Q + (n % kStages) * (L::H * SUB)));
+                if (tc::elect_one()) {
 #pragma unroll
-                for (int ks = 0; ks < DI / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * SUB + (ks & 3) * 32;
-                    tc::mma_bf16(tmem + (n & 1) * kKeys, tc::desc_adv(dQ, off), tc::desc_adv(dKI, off), I_S, ks > 0);
+                    for (int ks = 0; ks < DI / 16; ++ks) {
+                        const uint32_t off = (ks >> 2) * SUB + (ks & 3) * 32;
+                        tc::mma_bf16(tmem + (n & 1) * kKeys, tc::desc_adv(dQ, off), tc::desc_adv(dKI, off), I_S, ks > 0);
+                    }
+                    tc::mma_commit(&s_full[n & 1]);
+                    tc::mma_commit(&empty[n % kStages]);
                 }
-                tc::mma_commit(&s_full[n & 1]);
-                tc::mma_commit(&empty[n % kStages]);
+                __syncwarp();
             }
-            tc::mma_commit(done);
+            if (tc::elect_one()) tc::mma_commit(done);
+            __syncwarp();
             tc::mbar_wait(done, 0, nullptr, 0, nullptr);
         }
     } else if (warp < kProd2) {

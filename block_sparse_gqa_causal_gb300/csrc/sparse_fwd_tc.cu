@@ -228,38 +228,45 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         }
         cp_async_wait<0>();
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ------------------------------------------------ MMA issuer
+        {
+            // ------------------------------------------------ MMA issuer (the whole warp runs
+            // the loop; one lane chosen by elect.sync issues)
             constexpr uint32_t I_S = tc::idesc_bf16(128, kKeys);
             constexpr uint32_t I_O = tc::idesc_bf16(128, D) | tc::kBMajorMN;
             const uint64_t dK = tc::sdesc_k128(smem_u32(sm + L::OFF_K));
             const uint64_t dV = tc::sdesc_sw128(smem_u32(sm + L::OFF_V), SUB, 1024);
             const uint64_t dQ0 = tc::sdesc_sw128(smem_u32(sm + L::OFF_Q), 16, L::KB * 1024);
-            bool ok = tc::mbar_wait(kv_full, 0, st, 62, abort_flag);
+            bool ok = wwait(kv_full, 0, st, 62, abort_flag);
             if (ok) tc::fence_proxy_async();
             auto issue_s = [&](int n) {
                 const int a = n & 1;
                 const uint64_t dQ = tc::desc_adv(dQ0, a * (L::KB * SUB));
+                if (tc::elect_one()) {
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t h = ks >> 2, ko = (ks & 3) * 32;
-                    // A = Q rows (K-major, 8-row groups KB KB apart), B = K
-                    tc::mma_bf16(tmem + L::TM_S + a * 128, tc::desc_adv(dQ, h * 1024 + ko), tc::desc_adv(dK, h * SUB + ko),
-                                 I_S, ks > 0);
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint32_t h = ks >> 2, ko = (ks & 3) * 32;
+                        // A = Q rows (K-major, 8-row groups KB KB apart), B = K
+                        tc::mma_bf16(tmem + L::TM_S + a * 128, tc::desc_adv(dQ, h * 1024 + ko),
+                                     tc::desc_adv(dK, h * SUB + ko), I_S, ks > 0);
+                    }
+                    tc::mma_commit(&s_full[a]);
+                    tc::mma_commit(&q_empty[a]);
                 }
-                tc::mma_commit(&s_full[a]);
-                tc::mma_commit(&q_empty[a]);
+                __syncwarp();
             };
             auto issue_o = [&](int m) {
                 const int a = m & 1;
+                if (tc::elect_one()) {
 #pragma unroll
-                for (int ks = 0; ks < kKeys / 16; ++ks) {
-                    // A = P [rows][keys] from TMEM (16 keys = 8 packed columns per
-                    // step); B = V [keys][d] read MN-major (atoms of 64 d, 8-key groups)
-                    tc::mma_bf16_ts(tmem + L::TM_O + a * D, tmem + L::TM_S + a * 128 + ks * 8, tc::desc_adv(dV, ks * 2048),
-                                    I_O, ks > 0);
+                    for (int ks = 0; ks < kKeys / 16; ++ks) {
+                        // A = P [rows][keys] from TMEM (16 keys = 8 packed columns per
+                        // step); B = V [keys][d] read MN-major (atoms of 64 d, 8-key groups)
+                        tc::mma_bf16_ts(tmem + L::TM_O + a * D, tmem + L::TM_S + a * 128 + ks * 8,
+                                        tc::desc_adv(dV, ks * 2048), I_O, ks > 0);
+                    }
+                    tc::mma_commit(&o_full[a]);
                 }
-                tc::mma_commit(&o_full[a]);
+                __syncwarp();
             };
             // The two epilogue warpgroups run chunks n and n+1 at once, so S of
             // one chunk and O of another are issued in whichever order their
@@ -268,17 +275,20 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             uint32_t idle = 0;
             while (ok && no < nch) {
                 bool did = false;
-                // S(ns) overwrites the TMEM buffer holding P(ns-2): only after O(ns-2) is issued
-                if (ns < nch && (ns < 2 || no >= ns - 1) && tc::mbar_test(&q_full[ns & 1], (uint32_t)(ns >> 1) & 1u) &&
-                    (ns < 2 || tc::mbar_test(&s_free[ns & 1], ((uint32_t)(ns >> 1) & 1u) ^ 1u))) {
+                // S(ns) overwrites the TMEM buffer holding P(ns-2): only after O(ns-2) is issued.
+                // Each decision is lane 0's, so the warp never splits.
+                bool go_s = ns < nch && (ns < 2 || no >= ns - 1) && tc::mbar_test(&q_full[ns & 1], (uint32_t)(ns >> 1) & 1u) &&
+                            (ns < 2 || tc::mbar_test(&s_free[ns & 1], ((uint32_t)(ns >> 1) & 1u) ^ 1u));
+                if (__shfl_sync(0xffffffffu, go_s, 0)) {
                     tc::fence_proxy_async();
                     tc::fence_after_sync();
                     issue_s(ns);
                     ++ns;
                     did = true;
                 }
-                if (no < ns && tc::mbar_test(&p_full[no & 1], (uint32_t)(no >> 1) & 1u) &&
-                    (no < 2 || tc::mbar_test(&o_free[no & 1], ((uint32_t)(no >> 1) & 1u) ^ 1u))) {
+                bool go_o = no < ns && tc::mbar_test(&p_full[no & 1], (uint32_t)(no >> 1) & 1u) &&
+                            (no < 2 || tc::mbar_test(&o_free[no & 1], ((uint32_t)(no >> 1) & 1u) ^ 1u));
+                if (__shfl_sync(0xffffffffu, go_o, 0)) {
                     tc::fence_after_sync();
                     issue_o(no);
                     ++no;
@@ -287,15 +297,18 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                 if (did) {
                     idle = 0;
                 } else if (++idle >= tc::kSpinLimit) {
-                    report(st, kDevTimeout, 63, ns * 65536 + no);
-                    *abort_flag = 1;
+                    if (lane == 0) {
+                        report(st, kDevTimeout, 63, ns * 65536 + no);
+                        *abort_flag = 1;
+                    }
                     ok = false;
-                } else if ((idle & 1023u) == 1023u && *abort_flag) {
+                } else if ((idle & 1023u) == 1023u && __shfl_sync(0xffffffffu, *abort_flag, 0)) {
                     ok = false;
                 }
             }
             // every MMA issued above has completed once `done` fires
-            tc::mma_commit(done);
+            if (tc::elect_one()) tc::mma_commit(done);
+            __syncwarp();
             tc::mbar_wait(done, 0, nullptr, 0, nullptr);
         }
     } else if (warp < kProd2) {

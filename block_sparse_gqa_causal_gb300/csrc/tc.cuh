@@ -71,6 +71,14 @@ MSA_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, DeviceStatus *st, int sit
     return false;
 }
 
+// The bounded wait run by every lane of a warp, with the same outcome on all
+// of them (warp-uniform code such as an elected MMA issuer follows).
+MSA_DEV bool mbar_wait_warp(uint64_t *bar, uint32_t parity, DeviceStatus *st, int site, volatile int *abort_flag)
+{
+    const bool r = mbar_wait(bar, parity, st, site, abort_flag);
+    return __all_sync(0xffffffffu, r);
+}
+
 // ------------------------------------------------------------------ TMA
 MSA_DEV void tma_load_3d(void *smem_dst, const CUtensorMap *map, uint64_t *bar, int x, int y, int z)
 {
