@@ -226,6 +226,15 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             const int nq = min(QC, qend - q0);
             load_entries(ent2, bucket_q, q0 + 4 * QC, min(QC, qend - q0 - 4 * QC), lane);
             if (m + 2 < nch) load_rows(vl_next, vd_next, ent1, min(QC, qend - q0 - 2 * QC));
+            if constexpr (G == 8) {
+                // the Q and dO rows of this producer's next chunk (m + 2) into L2 while
+                // this one waits for its stage, so its gathers do not wait on HBM
+                if (lane < min(QC, qend - q0 - 2 * QC)) {
+                    const int z2 = b * p.Nq + entry_row(ent1[0]);
+                    tc::tma_prefetch_4d(&tmap_q, 0, r * G, 0, z2);
+                    tc::tma_prefetch_4d(&tmap_do, 0, r * G, 0, z2);
+                }
+            }
             if (!tc::mbar_wait(&empty[s], ((uint32_t)(m / kStages) & 1u) ^ 1u, st, 101, abort_flag)) break;
             Meta *meta = reinterpret_cast<Meta *>(sm + OFF_META + s * META_BYTES);
 #pragma unroll

@@ -206,6 +206,10 @@ sparse_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                     tc::tma_load_4d(sq + lane * (L::KB * 1024), &tmap_q, &q_full[a], 0, r * G, 0, z);
                 }
                 tc::mbar_arrive(&q_full[a]);
+                // the rows of this producer's next chunk (m + 2) into L2 now, so its
+                // gathers do not wait on HBM
+                if (m + 2 < nch && lane < min(QPC, qend - q0 - 2 * QPC))
+                    tc::tma_prefetch_4d(&tmap_q, 0, r * G, 0, b * p.Nq + entry_row(ent_next[0]));
             } else {
                 // Q rows: lanes cover whole 16-byte chunks of consecutive rows; the
                 // query index comes from the metadata just written (shared memory)
