@@ -117,23 +117,29 @@ index_scores_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        if (lane == 0) {
-            // ---------------- TMA producer
-            tc::prefetch_tmap(&tmap_q);
-            tc::prefetch_tmap(&tmap_k);
-            tc::mbar_arrive_expect_tx(q_full, mt * S::KB * kSub);
-            for (int m = 0; m < mt; ++m)
-                for (int kb = 0; kb < S::KB; ++kb)
-                    tc::tma_load_3d(sQ + (m * S::KB + kb) * kSub, &tmap_q, q_full, kb * 64, row0 + m * 128, b);
+        {
+            // ---------------- TMA producer (warp-uniform; one elect.sync lane issues)
+            if (tc::elect_one()) {
+                tc::prefetch_tmap(&tmap_q);
+                tc::prefetch_tmap(&tmap_k);
+                tc::mbar_arrive_expect_tx(q_full, mt * S::KB * kSub);
+                for (int m = 0; m < mt; ++m)
+                    for (int kb = 0; kb < S::KB; ++kb)
+                        tc::tma_load_3d(sQ + (m * S::KB + kb) * kSub, &tmap_q, q_full, kb * 64, row0 + m * 128, b);
+            }
+            __syncwarp();
             int issued = 0;
             for (int n = 0; n < nblk; ++n) {
                 const int s = n % kStages;
                 const uint32_t ph = (uint32_t)(n / kStages) & 1u;
-                if (!tc::mbar_wait(&empty[s], ph ^ 1u, st, 11, abort_flag)) break;
-                tc::mbar_arrive_expect_tx(&full[s], S::KB * kSub);
-                for (int kb = 0; kb < S::KB; ++kb)
-                    tc::tma_load_3d(sK + s * S::K_BYTES + kb * kSub, &tmap_k, &full[s], kb * 64,
-                                    (c_begin + n) * 128, b);
+                if (!tc::mbar_wait_warp(&empty[s], ph ^ 1u, st, 11, abort_flag)) break;
+                if (tc::elect_one()) {
+                    tc::mbar_arrive_expect_tx(&full[s], S::KB * kSub);
+                    for (int kb = 0; kb < S::KB; ++kb)
+                        tc::tma_load_3d(sK + s * S::K_BYTES + kb * kSub, &tmap_k, &full[s], kb * 64,
+                                        (c_begin + n) * 128, b);
+                }
+                __syncwarp();
                 issued = n + 1;
             }
             if (*abort_flag) {
