@@ -138,40 +138,29 @@ size_t klrows_bytes(const Problem &p) { return align256((size_t)p.B * p.Hkv * p.
 // KL teacher terms: four floats per (query, group, slot)
 size_t klt_bytes(const Problem &p) { return align256((size_t)p.B * p.Hkv * p.Nq * p.topk * 16); }
 
-// The KL forward with its teacher runs key-major (the teacher rebuilt on the
-// tensor cores next to the index scores) when d = d_idx = 128; the lse_idx-only
-// form runs key-major at any head dims; the rest streams query by query.
-bool kl_teacher_keymajor(const Problem &p) { return fwd_keymajor(p) && p.d == 128 && p.d_idx == 128; }
+// The KL forward runs key-major (the teacher rebuilt on the tensor cores next
+// to the index scores) where the forward does; the rest (decode shapes)
+// streams query by query.
+bool kl_teacher_keymajor(const Problem &p) { return fwd_keymajor(p) && bwd_tc(p); }
 size_t kl_bytes(const Problem &p, bool lse_only)
 {
     if (!fwd_keymajor(p) || (!lse_only && !kl_teacher_keymajor(p))) return 0;
     return align256(kl_part_count(p) * sizeof(float2)) + (lse_only ? 0 : klt_bytes(p)) + index_bytes(p);
 }
 
-// backward: D, dK_idx accumulators (tcgen05 path: one fp32 share per group),
-// the inverse index, and either the per-slot partials (tcgen05 path) or fp32
-// dQ / dq_idx accumulators
+// backward: D, each group's fp32 dK_idx share, the inverse index and the
+// per-slot dQ / dq_idx partial rows
 size_t bwd_bytes(const Problem &p)
 {
-    const size_t dki = (size_t)p.B * p.Nk * p.d_idx * 4 * (bwd_tc(p) ? (size_t)p.Hkv : 1);
-    size_t n = align256((size_t)p.B * p.Hq * p.Nq * 4) + align256(dki) + index_bytes(p);
+    const size_t dki = (size_t)p.B * p.Nk * p.d_idx * 4 * (size_t)p.Hkv;
     const size_t slots = (size_t)p.B * p.Nq * p.topk;
-    if (bwd_tc(p))
-        n += align256(slots * p.Hq * p.d * 2) + align256(slots * p.Hkv * p.d_idx * 2);
-    else
-        n += align256((size_t)p.B * p.Nq * p.Hq * p.d * 4) + align256((size_t)p.B * p.Nq * p.Hkv * p.d_idx * 4);
-    return n;
+    return align256((size_t)p.B * p.Hq * p.Nq * 4) + align256(dki) + index_bytes(p) +
+           align256(slots * p.Hq * p.d * 2) + align256(slots * p.Hkv * p.d_idx * 2);
 }
 
-// KL of the fused backward: rows (when the caller gives none) and either the
-// per-slot teacher terms of the tensor-core backward or the KL forward's own
-// scratch (with an lse_idx it recomputes)
-size_t bwdkl_bytes(const Problem &p)
-{
-    const size_t rows = (size_t)p.B * p.Hkv * p.Nq;
-    if (bwd_tc(p)) return klrows_bytes(p) + klt_bytes(p);
-    return klrows_bytes(p) + kl_bytes(p, false) + align256(rows * 4);
-}
+// KL of the fused backward: rows (when the caller gives none) and the per-slot
+// teacher terms
+size_t bwdkl_bytes(const Problem &p) { return klrows_bytes(p) + klt_bytes(p); }
 
 // one training step: the shared inverse index, scores scratch (unfused
 // selection only), forward partials, the KL index pass's partials, the
@@ -193,10 +182,10 @@ size_t train_bytes(const Problem &p)
 
 // The dense indexer warm-up runs the block-sparse kernels on the selection of
 // every visible block: topk = nb (at most 32 blocks: 4,096 tokens), the
-// tensor-core teacher and backward (d = d_idx = 128), a training sequence.
+// tensor-core teacher and backward, a training sequence.
 bool warmup_shape_ok(const Problem &p)
 {
-    return p.q_offset == 0 && p.Nq == p.Nk && p.kv_rows == p.Nk && p.d == 128 && p.d_idx == 128 && p.nb <= 32;
+    return p.q_offset == 0 && p.Nq == p.Nk && p.kv_rows == p.Nk && bwd_tc(p) && p.nb <= 32;
 }
 Problem warmup_problem(const Problem &p)
 {
@@ -330,7 +319,7 @@ size_t msa_workspace_size(const msa_shape *shape, int op)
     case MSA_OP_TRAIN_STEP: return kStatusBytes + train_bytes(p);
     case MSA_OP_WARMUP_KL: {
         if (!warmup_shape_ok(p)) {
-            fail(MSA_ERR_UNSUPPORTED, "warmup_kl needs q_offset == 0, Nq == Nk == kv_rows, d = d_idx = 128 and at "
+            fail(MSA_ERR_UNSUPPORTED, "warmup_kl needs q_offset == 0, Nq == Nk == kv_rows and at "
                  "most 32 blocks (Nk <= 4096); got Nk=%d d=%d d_idx=%d", p.Nk, p.d, p.d_idx);
             return 0;
         }
@@ -513,29 +502,17 @@ msa_status fused_bwd_impl(const msa_shape *shape, const void *q, const void *k, 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     BwdWork w{};
     w.D = cv.take<float>((size_t)p.B * p.Hq * p.Nq);
-    w.dki_acc = cv.take<float>((size_t)p.B * p.Nk * p.d_idx * (bwd_tc(p) ? (size_t)p.Hkv : 1));
+    w.dki_acc = cv.take<float>((size_t)p.B * p.Nk * p.d_idx * (size_t)p.Hkv);
     carve_index(cv, p, w);
     const size_t slots = (size_t)p.B * p.Nq * p.topk;
-    if (bwd_tc(p)) {
-        w.dq_part = cv.take<bf16>(slots * p.Hq * p.d);
-        w.dqi_part = cv.take<bf16>(slots * p.Hkv * p.d_idx);
-    } else {
-        w.dq_acc = cv.take<float>((size_t)p.B * p.Nq * p.Hq * p.d);
-        w.dqi_acc = cv.take<float>((size_t)p.B * p.Nq * p.Hkv * p.d_idx);
-    }
+    w.dq_part = cv.take<bf16>(slots * p.Hq * p.d);
+    w.dqi_part = cv.take<bf16>(slots * p.Hkv * p.d_idx);
     float *rows = nullptr;
     cudaError_t e;
     if (with_kl) {
         rows = kl_rows ? kl_rows : cv.take<float>((size_t)p.B * p.Hkv * p.Nq);
-        if (bwd_tc(p)) {
-            w.klt = cv.take<float>(slots * p.Hkv * 4);
-            w.kl_rows = rows;
-        } else {
-            // no tensor-core backward: the KL forward's passes give the rows
-            float *lse_scratch = cv.take<float>((size_t)p.B * p.Hkv * p.Nq);
-            e = kl_forward(p, q, k, q_idx, k_idx, sel_idx, lse, kl_coef, lse_scratch, rows, rows, nullptr, cv, ds, s);
-            if (e != cudaSuccess) return cuda_fail(e, "fused_bwd_kl: KL passes");
-        }
+        w.klt = cv.take<float>(slots * p.Hkv * 4);
+        w.kl_rows = rows;
     }
     e = launch_fused_bwd(p, static_cast<const bf16 *>(q), static_cast<const bf16 *>(k), static_cast<const bf16 *>(v),
                          static_cast<const bf16 *>(o), static_cast<const bf16 *>(d_o), lse,
@@ -705,7 +682,7 @@ msa_status msa_warmup_kl(const msa_shape *shape, const void *q, const void *k, c
     msa_status st = make_problem(shape, p0);
     if (st != MSA_OK) return st;
     if (!warmup_shape_ok(p0))
-        return fail(MSA_ERR_UNSUPPORTED, "warmup_kl needs q_offset == 0, Nq == Nk == kv_rows, d = d_idx = 128 and at "
+        return fail(MSA_ERR_UNSUPPORTED, "warmup_kl needs q_offset == 0, Nq == Nk == kv_rows and at "
                     "most 32 blocks (Nk <= 4096); got Nk=%d d=%d d_idx=%d", p0.Nk, p0.d, p0.d_idx);
     REQUIRE_PTR(q, "q");
     REQUIRE_PTR(k, "k");
@@ -761,7 +738,7 @@ msa_status msa_warmup_kl(const msa_shape *shape, const void *q, const void *k, c
         return cuda_fail(e, "warmup_kl: teacher and index gradients");
     if ((e = launch_kl_rows_combine(p, sel, lse_idx, klt, rows_kl, s)) != cudaSuccess) return cuda_fail(e, "warmup_kl: rows");
     if ((e = launch_kl_reduce(p, rows_kl, kl_coef, kl_loss, s)) != cudaSuccess) return cuda_fail(e, "warmup_kl: loss");
-    if ((e = launch_bwd_combine(p, sel, dqi_part, static_cast<bf16 *>(dq_idx), p.Hkv, 1, s)) != cudaSuccess)
+    if ((e = launch_bwd_combine(p, sel, dqi_part, static_cast<bf16 *>(dq_idx), p.Hkv, 1, p.d_idx, s)) != cudaSuccess)
         return cuda_fail(e, "warmup_kl: dq_idx");
     if ((e = launch_dki_group_sum(p, dki_g, static_cast<bf16 *>(dk_idx), s)) != cudaSuccess)
         return cuda_fail(e, "warmup_kl: dk_idx");

@@ -1,5 +1,7 @@
-// bwd_main_tc.cu -- main-branch backward of MSA on the tcgen05 tensor cores
-// (d = 128), key-major.
+// bwd_main_tc.cu -- main-branch backward of MSA on the tcgen05 tensor cores,
+// key-major.  The tiles hold 128 features; at d = 64 the upper 64 are zeros
+// (TMA fills the boxes past the tensor's width, gathers zero-fill them), which
+// add nothing to any product, and are never written back.
 //
 // "Sparse Attention · Part II", section 3.2: the main branch's gradients come
 // from dO alone (the selection is not differentiated).  One CTA owns one
@@ -276,9 +278,9 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
                 for (int it = 0; it < kRows / 2; ++it) {
                     const int rho = it * 2 + (lane >> 4), ch = lane & 15;
                     const int qq = rho / G, g = rho % G;
-                    const bool ok = qq < nq;
+                    const bool ok = qq < nq && ch * 8 < p.d;
                     const long long off =
-                        (((long long)b * p.Nq + meta->qi[qq]) * p.Hq + (long long)r * G + g) * D + ch * 8;
+                        (((long long)b * p.Nq + meta->qi[qq]) * p.Hq + (long long)r * G + g) * p.d + (ok ? ch * 8 : 0);
                     const int o = roff(rho, ch >> 3, ch & 7);
                     cp_async16_zfill(sq + o, q + off, ok);
                     cp_async16_zfill(sdo + o, d_o + off, ok);
@@ -393,6 +395,7 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         const int qd = warp & 3;
         const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
         bf16 *col = dq_part + qd * 32 + lane;
+        const bool feat_ok = qd * 32 + lane < p.d;   // features past d are the zero padding
         for (int m = 0; m < nch; ++m) {
             const int pb = m & 1, x = m % kRx;
             if (!wwait(&rx_full[x], (uint32_t)(m / kRx) & 1u, st, 117, abort_flag)) break;
@@ -411,8 +414,8 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
 #pragma unroll
             for (int cc = 0; cc < 32; ++cc) {
                 const long long r0 = rx[cc], r1 = rx[32 + cc];
-                if (r0 >= 0) col[r0 * D] = __float2bfloat16_rn(__uint_as_float(v0[cc]));
-                if (r1 >= 0) col[r1 * D] = __float2bfloat16_rn(__uint_as_float(v1[cc]));
+                if (feat_ok && r0 >= 0) col[r0 * p.d] = __float2bfloat16_rn(__uint_as_float(v0[cc]));
+                if (feat_ok && r1 >= 0) col[r1 * p.d] = __float2bfloat16_rn(__uint_as_float(v1[cc]));
             }
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&rx_free[x]);
@@ -525,9 +528,9 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             ok = wwait(&ds_free[m % kDsBuf], (uint32_t)(m / kDsBuf) & 1u, st, 115, abort_flag);
             tc::fence_after_sync();
         }
-        if (ok) {
-            bf16 *pk_ = dk + (((long long)b * p.kv_rows + j) * p.Hkv + r) * D + hf * 64;
-            bf16 *pv_ = dv + (((long long)b * p.kv_rows + j) * p.Hkv + r) * D + hf * 64;
+        if (ok && hf * 64 < p.d) {
+            bf16 *pk_ = dk + (((long long)b * p.kv_rows + j) * p.Hkv + r) * p.d + hf * 64;
+            bf16 *pv_ = dv + (((long long)b * p.kv_rows + j) * p.Hkv + r) * p.d + hf * 64;
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
                 uint32_t a[32], g2[32];
@@ -576,17 +579,19 @@ cudaError_t launch_g(const Problem &p, const bf16 *q, const bf16 *k, const bf16 
     CUtensorMap tq, tdo, tk, tv;
     {
         // Q / dO as {d within a half, head, half, query row}: one box {64, G, 2, 1}
-        // is a query's G head rows in both feature halves
-        const unsigned long long dq4[4] = {64, (unsigned long long)p.Hq, 2, (unsigned long long)p.B * p.Nq};
-        const unsigned long long sq4[3] = {D * 2ull, 128ull, (unsigned long long)p.Hq * D * 2ull};
+        // is a query's G head rows in both feature halves (at d = 64 the second
+        // half lies past the tensor and reads as zeros)
+        const unsigned long long dq4[4] = {64, (unsigned long long)p.Hq, (unsigned long long)p.d / 64,
+                                           (unsigned long long)p.B * p.Nq};
+        const unsigned long long sq4[3] = {p.d * 2ull, 128ull, (unsigned long long)p.Hq * p.d * 2ull};
         const unsigned bq4[4] = {64, (unsigned)G, 2, 1};
         if ((e = make_tmap_bf16(&tq, q, 4, dq4, sq4, bq4)) != cudaSuccess) return e;
         if ((e = make_tmap_bf16(&tdo, d_o, 4, dq4, sq4, bq4)) != cudaSuccess) return e;
-        // K/V as [B][Nk][Hkv][D] (rows past Nk are out of bounds)
-        const unsigned long long dk4[4] = {(unsigned long long)D, (unsigned long long)p.Hkv, (unsigned long long)p.Nk,
+        // K/V as [B][Nk][Hkv][d] (rows past Nk, and features past d, are out of bounds)
+        const unsigned long long dk4[4] = {(unsigned long long)p.d, (unsigned long long)p.Hkv, (unsigned long long)p.Nk,
                                            (unsigned long long)p.B};
-        const unsigned long long sk[3] = {D * 2ull, (unsigned long long)p.Hkv * D * 2ull,
-                                          (unsigned long long)p.kv_rows * p.Hkv * D * 2ull};
+        const unsigned long long sk[3] = {p.d * 2ull, (unsigned long long)p.Hkv * p.d * 2ull,
+                                          (unsigned long long)p.kv_rows * p.Hkv * p.d * 2ull};
         const unsigned bk[4] = {64, 1, (unsigned)kKeys, 1};
         if ((e = make_tmap_bf16(&tk, k, 4, dk4, sk, bk)) != cudaSuccess) return e;
         if ((e = make_tmap_bf16(&tv, v, 4, dk4, sk, bk)) != cudaSuccess) return e;

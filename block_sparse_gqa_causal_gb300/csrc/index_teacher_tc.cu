@@ -1,7 +1,9 @@
 // index_teacher_tc.cu -- the KL alignment loss's teacher terms and the index
-// branch's backward of MSA, key-major on the tcgen05 tensor cores (d = d_idx
-// = 128), with the teacher recomputed on chip: neither probability
-// distribution is written to memory.
+// branch's backward of MSA, key-major on the tcgen05 tensor cores, with the
+// teacher recomputed on chip: neither probability distribution is written to
+// memory.  The tiles hold 128 features; at d or d_idx = 64 the upper 64 are
+// zeros (TMA fills boxes past the tensor's width, gathers zero-fill them),
+// which add nothing to any product, and are never written back.
 //
 // "Sparse Attention · Part II", section 3.2: for query i and group r over the
 // selected token set T, the teacher is Pt_j = (1/G) sum_h exp(l_{h,j} - lse_h)
@@ -52,7 +54,7 @@
 namespace msa {
 namespace {
 
-constexpr int D = 128;                     // d = d_idx
+constexpr int D = 128;                     // tile features (d, d_idx of 64 are zero-padded)
 constexpr int kKeys = 128;
 constexpr int kQ = 64;                     // queries per chunk (s^T columns)
 constexpr int kEpiWarps = 16;              // 4 per TMEM lane quarter
@@ -202,8 +204,8 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
     if (qend <= qbeg) {
         if constexpr (kGrad) {
             // no query selected this block: the group's dK_idx share is zero
-            float4 *dst = reinterpret_cast<float4 *>(dki_g + (((long long)b * p.Hkv + r) * p.Nk + j0) * D);
-            const int n4 = (int)(min((long long)kKeys, (long long)p.Nk - j0) * (D / 4));
+            float4 *dst = reinterpret_cast<float4 *>(dki_g + (((long long)b * p.Hkv + r) * p.Nk + j0) * p.d_idx);
+            const int n4 = (int)(min((long long)kKeys, (long long)p.Nk - j0) * (p.d_idx / 4));
             for (int x = threadIdx.x; x < n4; x += kThreads) dst[x] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         return;
@@ -294,9 +296,8 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
                 if constexpr (G == 8) {
                     tc::tma_prefetch_4d(&tmap_q, 0, r * G, 0, (int)row);
                 } else {
-                    const char *base = reinterpret_cast<const char *>(q + (row * p.Hq + (long long)r * G) * D);
-#pragma unroll
-                    for (int x = 0; x < 2 * G; ++x) tc::prefetch_l2(base + x * 128);
+                    const char *base = reinterpret_cast<const char *>(q + (row * p.Hq + (long long)r * G) * p.d);
+                    for (int x = 0; x < G * p.d / 64; ++x) tc::prefetch_l2(base + x * 128);
                 }
             }
         };
@@ -333,8 +334,10 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
                         const int g = rho % G;
                         const int e = ent_of(ent, m * QS + rho / G);
                         const int i = e >= 0 ? entry_row(e) : 0;
-                        const long long off = (((long long)b * p.Nq + i) * p.Hq + (long long)r * G + g) * D + ch * 8;
-                        cp_async16_zfill(sq + roff(rho, ch >> 3, ch & 7), q + off, e >= 0);
+                        const bool ok = e >= 0 && ch * 8 < p.d;
+                        const long long off =
+                            (((long long)b * p.Nq + i) * p.Hq + (long long)r * G + g) * p.d + (ok ? ch * 8 : 0);
+                        cp_async16_zfill(sq + roff(rho, ch >> 3, ch & 7), q + off, ok);
                     }
                     cp_async_arrive_noinc(&q_full[s]);
                     tc::mbar_arrive(&q_full[s]);
@@ -406,10 +409,12 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
                 mt->lsei2[col] = cur.li[t];
 #pragma unroll
                 for (int g = 0; g < G; ++g) mt->lse2[col * G + g] = cur.l2[t][g];
-                const bf16 *src = q_idx + (((long long)b * p.Nq + i) * p.Hkv + r) * D;
+                const bf16 *src = q_idx + (((long long)b * p.Nq + i) * p.Hkv + r) * p.d_idx;
 #pragma unroll
-                for (int ch = 0; ch < D / 8; ++ch)
-                    cp_async16_zfill(si + (ch >> 3) * SUBI + swz(col, ch & 7), src + ch * 8, ok);
+                for (int ch = 0; ch < D / 8; ++ch) {
+                    const bool okc = ok && ch * 8 < p.d_idx;
+                    cp_async16_zfill(si + (ch >> 3) * SUBI + swz(col, ch & 7), src + (okc ? ch * 8 : 0), okc);
+                }
             }
             pm = __reduce_min_sync(0xffffffffu, pm);
             if (lane == 0) mt->pmin = pm;
@@ -557,10 +562,11 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&si_free[m & 1]);
             bf16 *col = dqi_part + qd * 32 + lane;
+            const bool feat_ok = qd * 32 + lane < p.d_idx;     // features past d_idx are padding
 #pragma unroll
             for (int cc = 0; cc < kWC; ++cc) {
                 const int rix = __shfl_sync(0xffffffffu, rp_prev, cc);
-                if (rix >= 0) col[(long long)rix * D] = __float2bfloat16_rn(__uint_as_float(v[cc]));
+                if (feat_ok && rix >= 0) col[(long long)rix * p.d_idx] = __float2bfloat16_rn(__uint_as_float(v[cc]));
             }
             return true;
         };
@@ -726,8 +732,8 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
                 uint32_t a[32];
                 tc::tmem_ld32_nowait(tmem + lane_base + TM_DKI + cq * 32, a);
                 tc::tmem_wait32(a);
-                if (key_ok) {
-                    float *dst = dki_g + (((long long)b * p.Hkv + r) * p.Nk + j) * D + cq * 32;
+                if (key_ok && cq * 32 < p.d_idx) {
+                    float *dst = dki_g + (((long long)b * p.Hkv + r) * p.Nk + j) * p.d_idx + cq * 32;
 #pragma unroll
                     for (int x = 0; x < 32; x += 4)
                         *reinterpret_cast<float4 *>(dst + x) =
@@ -750,8 +756,8 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
 __global__ void __launch_bounds__(256) dki_group_sum_kernel(Problem p, const float4 *__restrict__ dki_g,
                                                             bf16 *__restrict__ dk_idx)
 {
-    const long long n4 = (long long)p.B * p.Nk * (D / 4);
-    const long long per_b = (long long)p.Nk * (D / 4);
+    const long long n4 = (long long)p.B * p.Nk * (p.d_idx / 4);
+    const long long per_b = (long long)p.Nk * (p.d_idx / 4);
     for (long long x = (long long)blockIdx.x * blockDim.x + threadIdx.x; x < n4; x += (long long)gridDim.x * blockDim.x) {
         const long long bb = x / per_b, rest = x % per_b;
         float4 a = __ldg(dki_g + (bb * p.Hkv) * per_b + rest);
@@ -799,21 +805,24 @@ cudaError_t launch_g(const Problem &p, const bf16 *q, const bf16 *k, const bf16 
     CUtensorMap tq, tk, tki;
     {
         // Q as {d within a half, head, half, query row}: one box {64, G, 2, 1} is a
-        // query's G head rows in both feature halves
-        const unsigned long long dq4[4] = {64, (unsigned long long)p.Hq, 2, (unsigned long long)p.B * p.Nq};
-        const unsigned long long sq4[3] = {D * 2ull, 128ull, (unsigned long long)p.Hq * D * 2ull};
+        // query's G head rows in both feature halves (at d = 64 the second half
+        // lies past the tensor and reads as zeros)
+        const unsigned long long dq4[4] = {64, (unsigned long long)p.Hq, (unsigned long long)p.d / 64,
+                                           (unsigned long long)p.B * p.Nq};
+        const unsigned long long sq4[3] = {p.d * 2ull, 128ull, (unsigned long long)p.Hq * p.d * 2ull};
         const unsigned bq4[4] = {64, (unsigned)G, 2, 1};
         if ((e = make_tmap_bf16(&tq, q, 4, dq4, sq4, bq4)) != cudaSuccess) return e;
-        // K as [B][Nk][Hkv][D] (rows past Nk read as zeros)
-        const unsigned long long dk4[4] = {(unsigned long long)D, (unsigned long long)p.Hkv, (unsigned long long)p.Nk,
+        // K as [B][Nk][Hkv][d] (rows past Nk, features past d read as zeros)
+        const unsigned long long dk4[4] = {(unsigned long long)p.d, (unsigned long long)p.Hkv, (unsigned long long)p.Nk,
                                            (unsigned long long)p.B};
-        const unsigned long long sk[3] = {D * 2ull, (unsigned long long)p.Hkv * D * 2ull,
-                                          (unsigned long long)p.kv_rows * p.Hkv * D * 2ull};
+        const unsigned long long sk[3] = {p.d * 2ull, (unsigned long long)p.Hkv * p.d * 2ull,
+                                          (unsigned long long)p.kv_rows * p.Hkv * p.d * 2ull};
         const unsigned bk[4] = {64, 1, (unsigned)kKeys, 1};
         if ((e = make_tmap_bf16(&tk, k, 4, dk4, sk, bk)) != cudaSuccess) return e;
-        // K_idx as [B][Nk][D]
-        const unsigned long long di[3] = {(unsigned long long)D, (unsigned long long)p.Nk, (unsigned long long)p.B};
-        const unsigned long long si[2] = {D * 2ull, (unsigned long long)p.kv_rows * D * 2ull};
+        // K_idx as [B][Nk][d_idx]
+        const unsigned long long di[3] = {(unsigned long long)p.d_idx, (unsigned long long)p.Nk,
+                                          (unsigned long long)p.B};
+        const unsigned long long si[2] = {p.d_idx * 2ull, (unsigned long long)p.kv_rows * p.d_idx * 2ull};
         const unsigned bi[3] = {64, (unsigned)kKeys, 1};
         if ((e = make_tmap_bf16(&tki, k_idx, 3, di, si, bi)) != cudaSuccess) return e;
     }
@@ -847,7 +856,7 @@ cudaError_t launch_index_teacher_tc(const Problem &p, const bf16 *q, const bf16 
                                     const int32_t *bucket_off, const int32_t *bucket_q, float *klt, bf16 *dqi_part,
                                     float *dki_g, DeviceStatus *st, cudaStream_t s)
 {
-    if (p.d != D || p.d_idx != D) return cudaErrorInvalidValue;
+    if ((p.d != 64 && p.d != D) || (p.d_idx != 64 && p.d_idx != D)) return cudaErrorInvalidValue;
     const float coef = p.scale_idx * kl_coef / ((float)p.B * (float)p.Nq * (float)p.Hkv);
     if (dqi_part)
         return launch_grad<true>(p, q, k, q_idx, k_idx, lse, lse_idx, coef, bucket_off, bucket_q, klt, dqi_part, dki_g,

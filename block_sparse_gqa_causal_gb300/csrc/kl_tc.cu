@@ -312,7 +312,7 @@ cudaError_t launch_kl_keymajor(const Problem &p, const bf16 *q, const bf16 *k, c
                                const int32_t *sel, const float *lse, float *lse_idx, float *kl_rows, const KlWork &w,
                                DeviceStatus *st, cudaStream_t s)
 {
-    if (kl_rows && (!w.klt || p.d != 128 || p.d_idx != 128)) return cudaErrorInvalidValue;
+    if (kl_rows && (!w.klt || !bwd_tc(p))) return cudaErrorInvalidValue;
     cudaError_t e = w.index_ready ? cudaSuccess
                                   : launch_inverse_index(p, sel, w.bucket_cnt, w.bucket_off, w.bucket_scratch, w.bucket_q, st, s);
     if (e != cudaSuccess) return e;

@@ -105,21 +105,21 @@ cudaError_t launch_kl_fwd(const Problem &p, const bf16 *q, const bf16 *k, const 
 struct KlWork {
     float2 *part;        // [B, Hkv, Nq, topk, 2] (max s log2 e, sum 2^(s log2 e - max)) per key half
     float *klt;          // [B*Hkv*Nq*topk, 4] sums of Pt (log2 Pt - s log2 e) per lane quarter of the
-                         // block's keys (teacher terms, d = d_idx = 128); nullptr: lse_idx only
+                         // block's keys (teacher terms); nullptr: lse_idx only
     int32_t *bucket_cnt, *bucket_off, *bucket_scratch, *bucket_q;
     bool index_ready = false;
 };
 // float2 partials the key-major KL's index pass writes (two per (query, group, slot))
 size_t kl_part_count(const Problem &p);
 // lse_idx (index pass + combine) and, with w.klt and kl_rows set, the KL rows
-// from the teacher terms of launch_index_teacher_tc (d = d_idx = 128 only)
+// from the teacher terms of launch_index_teacher_tc
 cudaError_t launch_kl_keymajor(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *q_idx, const bf16 *k_idx,
                                const int32_t *sel, const float *lse, float *lse_idx, float *kl_rows, const KlWork &w,
                                DeviceStatus *st, cudaStream_t s);
 cudaError_t launch_kl_reduce(const Problem &p, const float *kl_rows, float kl_coef, float *kl_loss,
                              cudaStream_t s);
 // The KL's teacher terms and (dqi_part set) the index-branch backward,
-// key-major on the tcgen05 tensor cores (d = d_idx = 128), the teacher
+// key-major on the tcgen05 tensor cores (d, d_idx of 64 zero-padded to 128), the teacher
 // recomputed from its own logit tiles: per (query, group, slot) klt (4 floats,
 // nullable) and, for the backward, dq_idx partial rows in dqi_part and each
 // group's fp32 dK_idx share in dki_g [B, Hkv, Nk, d_idx].
@@ -136,16 +136,13 @@ cudaError_t launch_dki_group_sum(const Problem &p, const float *dki_g, bf16 *dk_
 // Backward pieces.  Workspace carve-up is done by the caller (api.cu).
 struct BwdWork {
     float *D;            // [B, Hq, Nq]    rowsum(dO * O)
-    float *dq_acc;       // [B, Nq, Hq, d]  fp32 accumulators (mma.sync path)
-    float *dqi_acc;      // [B, Nq, Hkv, d_idx]              (mma.sync path)
-    // dK_idx: [B, Nk, d_idx] fp32 accumulators (mma.sync path) or each group's
-    // share [B, Hkv, Nk, d_idx], summed over the groups in order (tcgen05 path)
+    // dK_idx: each group's share [B, Hkv, Nk, d_idx], summed over the groups in order
     float *dki_acc;
-    bf16 *dq_part;       // [B, Nq, Hq, topk, d]      dQ per selected block (tcgen05 path)
-    bf16 *dqi_part;      // [B, Nq, Hkv, topk, d_idx] dq_idx per selected block (tcgen05 path)
-    // KL loss terms per ((b, r, query), slot), four floats (tcgen05 path; nullptr
-    // when the loss is not asked for): sums of Pt (log2 Pt - s log2 e) per lane
-    // quarter of the block's keys
+    bf16 *dq_part;       // [B, Nq, Hq, topk, d]      dQ per selected block
+    bf16 *dqi_part;      // [B, Nq, Hkv, topk, d_idx] dq_idx per selected block
+    // KL loss terms per ((b, r, query), slot), four floats (nullptr when the loss
+    // is not asked for): sums of Pt (log2 Pt - s log2 e) per lane quarter of
+    // the block's keys
     float *klt;
     float *kl_rows;      // [B, Hkv, Nq] KL rows assembled from klt (when klt is set)
     int32_t *bucket_cnt; // [B*Hkv*nb]
@@ -192,9 +189,10 @@ __host__ __device__ __forceinline__ void bucket_of(int x, int Hkv, int nb, int n
     }
 }
 
-// The backward runs on the tcgen05 kernels when d = d_idx = 128.
-inline bool bwd_tc(const Problem &p) { return p.d == 128 && p.d_idx == 128; }
-// tcgen05 main-branch backward (d = 128): dK, dV and the dQ partials.
+// The backward runs on the tcgen05 kernels for d and d_idx of 64 or 128 (the
+// tiles hold 128 features; 64 are zero-padded), i.e. for every valid shape.
+inline bool bwd_tc(const Problem &p) { return (p.d == 64 || p.d == 128) && (p.d_idx == 64 || p.d_idx == 128); }
+// tcgen05 main-branch backward: dK, dV and the dQ partials.
 cudaError_t launch_bwd_main_tc(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *v, const bf16 *d_o,
                                const float *lse, const BwdWork &w, bf16 *dk, bf16 *dv, DeviceStatus *st,
                                cudaStream_t s);
@@ -211,9 +209,9 @@ cudaError_t launch_index_proj_fwd(const ProjProblem &pp, const bf16 *x, const bf
                                   bf16 *k_idx, DeviceStatus *st, cudaStream_t s);
 cudaError_t launch_index_proj_dw(const ProjProblem &pp, const bf16 *x, const bf16 *dq_idx, const bf16 *dk_idx,
                                  float *dwq, float *dwk, float *partial, DeviceStatus *st, cudaStream_t s);
-// Sum of a row's per-slot bf16 partial rows (128 features) over its valid
-// slots: H rows per (b, query), head h in group h / Gh.
-cudaError_t launch_bwd_combine(const Problem &p, const int32_t *sel, const bf16 *part, bf16 *out, int H, int Gh,
+// Sum of a row's per-slot bf16 partial rows (width 64 or 128 features) over
+// its valid slots: H rows per (b, query), head h in group h / Gh.
+cudaError_t launch_bwd_combine(const Problem &p, const int32_t *sel, const bf16 *part, bf16 *out, int H, int Gh, int width,
                                cudaStream_t s);
 // The selection that keeps every visible block (topk = nb): sel[b, r, i, t] =
 // t for t <= c0(i), else -1 -- the dense warm-up's token set.

@@ -147,9 +147,8 @@ msa_status msa_kl_fwd(const msa_shape *shape, const void *q, const void *k, cons
  * branch gets none from d_o (section 3.2 on the two detachments).  Uses the
  * forward's o and lse and the KL forward's lse_idx.  Requires q_offset == 0
  * and Nq == Nk (training layout).  dk, dv, dk_idx are fully written (zero
- * for keys no query selected).  With d = d_idx = 128 (the tensor-core
- * path) every sum is taken in a fixed order: the same inputs give the same
- * bits on every call.
+ * for keys no query selected).  Every sum is taken in a fixed order: the
+ * same inputs give the same bits on every call.
  */
 msa_status msa_fused_bwd(const msa_shape *shape, const void *q, const void *k, const void *v,
                          const void *o, const void *d_o, const float *lse, const void *q_idx,
@@ -165,8 +164,6 @@ msa_status msa_fused_bwd(const msa_shape *shape, const void *q, const void *k, c
  * kl_loss NULL) and gets the loss here without a separate teacher pass.
  * kl_loss (device scalar) must be non-NULL; kl_rows may be NULL (then it
  * lives in the workspace).  Workspace: msa_workspace_size(MSA_OP_FUSED_BWD_KL).
- * Where the tensor-core backward does not apply (d or d_idx of 64) the loss
- * is computed by the KL forward's own passes inside this call.
  */
 msa_status msa_fused_bwd_kl(const msa_shape *shape, const void *q, const void *k, const void *v,
                             const void *o, const void *d_o, const float *lse, const void *q_idx,
@@ -180,10 +177,10 @@ msa_status msa_fused_bwd_kl(const msa_shape *shape, const void *q, const void *k
  * msa_sparse_attn_fwd, msa_kl_fwd in its lse_idx-only form and
  * msa_fused_bwd_kl, with their definitions, layouts and outputs (sel_idx,
  * o, lse, lse_idx, kl_rows (may be NULL), *kl_loss, and the five gradients
- * from d_o).  On the key-major tensor-core path (prefill with >= 8 queries
- * per selected block on average, d = d_idx = 128) the per-block query lists
- * of the selection are built once for all phases; elsewhere the phases run
- * one after another.  Training layout only (q_offset == 0, Nq == Nk,
+ * from d_o).  On the key-major path (>= 8 queries per selected block on
+ * average, which every training shape with Nq == Nk meets) the per-block
+ * query lists of the selection are built once for all phases; elsewhere the
+ * phases run one after another.  Training layout only (q_offset == 0, Nq == Nk,
  * kv_rows == Nk).  Workspace: msa_workspace_size(MSA_OP_TRAIN_STEP).
  */
 msa_status msa_train_step(const msa_shape *shape, const void *q, const void *k, const void *v,
@@ -224,8 +221,8 @@ msa_status msa_train_step_staged(const msa_shape *shape, const void *q, const vo
  * the dense main attention's lse [B, Hq, Nq] (the teacher's normaliser) and
  * lse_idx; kl_rows may be NULL.  It is MSA's own block-sparse path run on
  * the selection of every visible block, so shape->topk is ignored (any valid
- * value): training layout (q_offset == 0, Nq == Nk, kv_rows == Nk), d = d_idx
- * = 128 and at most 32 blocks (Nk <= 4096), else MSA_ERR_UNSUPPORTED.
+ * value): training layout (q_offset == 0, Nq == Nk, kv_rows == Nk) and at
+ * most 32 blocks (Nk <= 4096), else MSA_ERR_UNSUPPORTED.
  * Workspace: msa_workspace_size(shape, MSA_OP_WARMUP_KL).  Deterministic.
  */
 msa_status msa_warmup_kl(const msa_shape *shape, const void *q, const void *k, const void *v, const void *q_idx,

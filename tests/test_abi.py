@@ -138,33 +138,35 @@ def test_product_path_has_no_oracle_or_fallback():
                 assert "msa_oracle" not in text, f
 
 
-def test_backward_workspace_holds_no_distribution(libmsa):
-    """The fused backward's workspace (d = d_idx = 128, the tensor-core path)
-    is D, one fp32 dK_idx share per group, the inverse index and the per-slot
-    dQ / dq_idx partial rows -- nothing per (slot, key): the teacher is rebuilt
-    on chip and never stored.  With the KL loss, four floats per slot more."""
+@pytest.mark.parametrize("d,di", [(128, 128), (64, 64), (128, 64)])
+def test_backward_workspace_holds_no_distribution(libmsa, d, di):
+    """The fused backward's workspace (the tensor-core path, at every head
+    dim) is D, one fp32 dK_idx share per group, the inverse index and the
+    per-slot dQ / dq_idx partial rows -- nothing per (slot, key): the teacher
+    is rebuilt on chip and never stored.  With the KL loss, four floats per
+    slot more."""
     from block_sparse_gqa_causal_gb300 import api
-    B, N, Hq, Hkv, d, k = 1, 131072, 64, 8, 128, 16
-    sh = api.Shape(B=B, Nq=N, Nk=N, Hq=Hq, Hkv=Hkv, d=d, d_idx=d, topk=k)
+    B, N, Hq, Hkv, k = 1, 131072, 64, 8, 16
+    sh = api.Shape(B=B, Nq=N, Nk=N, Hq=Hq, Hkv=Hkv, d=d, d_idx=di, topk=k)
     a = lambda x: (x + 255) // 256 * 256
     nb = N // 128
     nct = (N + 511) // 512
     index = 2 * a((B * Hkv * nb + 1) * 4) + a(2 * B * Hkv * nct * nb * 4) + a(B * Hkv * N * k * 4)
     slots = B * N * k
-    want = (256 + a(B * Hq * N * 4) + a(B * Hkv * N * d * 4) + index + a(slots * Hq * d * 2)
-            + a(slots * Hkv * d * 2))
+    want = (256 + a(B * Hq * N * 4) + a(B * Hkv * N * di * 4) + index + a(slots * Hq * d * 2)
+            + a(slots * Hkv * di * 2))
     assert api.workspace_size(sh, api.OP_FUSED_BWD) == want
     assert api.workspace_size(sh, api.OP_FUSED_BWD_KL) == want + a(B * Hkv * N * 4) + a(slots * Hkv * 16)
 
 
 def test_warmup_and_projection_calls_validate_on_the_host(libmsa):
-    """The dense warm-up needs a training sequence of at most 32 blocks with
-    d = d_idx = 128; the projections need d_idx in {64, 128} and Dm a multiple
-    of 8; bad pointers and short workspaces are refused before any launch."""
+    """The dense warm-up needs a training sequence of at most 32 blocks; the
+    projections need d_idx in {64, 128} and Dm a multiple of 8; bad pointers
+    and short workspaces are refused before any launch."""
     from block_sparse_gqa_causal_gb300 import api
     g = ctypes.c_void_p(1 << 20)
     f = ctypes.c_float(1.0)
-    for kw in (dict(Nq=8192, Nk=8192), dict(d=64), dict(Nq=3, Nk=256, q_offset=253)):
+    for kw in (dict(Nq=8192, Nk=8192), dict(Nq=3, Nk=256, q_offset=253)):
         base = dict(B=1, Nq=1024, Nk=1024, Hq=8, Hkv=2, d=128, d_idx=128, topk=1)
         base.update(kw)
         sh = api.Shape(**base)

@@ -61,17 +61,18 @@ def test_index_projection_weight_gradient(T, Dm, Hkv, di):
     assert_close(dwk.cpu().numpy().astype(np.float64) / scale, wk_o / scale, "dW_k = X^T dk_idx")
 
 
-WARM = [  # name, B, N, Hq, Hkv
-    ("n2048_g8", 1, 2048, 16, 2),
-    ("b2_n1000_g4_ragged", 2, 1000, 8, 2),
-    ("n4096_32_blocks", 1, 4096, 8, 1),
+WARM = [  # name, B, N, Hq, Hkv, d, d_idx
+    ("n2048_g8", 1, 2048, 16, 2, 128, 128),
+    ("b2_n1000_g4_ragged", 2, 1000, 8, 2, 128, 128),
+    ("n4096_32_blocks", 1, 4096, 8, 1, 128, 128),
+    ("n1500_g8_d64", 1, 1500, 16, 2, 64, 64),
 ]
 
 
-def _warm_inputs(name, B, N, Hq, Hkv, seed):
+def _warm_inputs(name, B, N, Hq, Hkv, d=128, di=128, seed=0):
     rng = np.random.default_rng(seed)
-    x = {"q": _bf(rng, (B, N, Hq, 128)), "k": _bf(rng, (B, N, Hkv, 128)), "v": _bf(rng, (B, N, Hkv, 128)),
-         "q_idx": _bf(rng, (B, N, Hkv, 128)), "k_idx": _bf(rng, (B, N, 128))}
+    x = {"q": _bf(rng, (B, N, Hq, d)), "k": _bf(rng, (B, N, Hkv, d)), "v": _bf(rng, (B, N, Hkv, d)),
+         "q_idx": _bf(rng, (B, N, Hkv, di)), "k_idx": _bf(rng, (B, N, di))}
     return x
 
 
@@ -79,10 +80,10 @@ def _warm_inputs(name, B, N, Hq, Hkv, seed):
 def test_warmup_kl_and_gradients(case):
     import torch
     from block_sparse_gqa_causal_gb300 import api
-    name, B, N, Hq, Hkv = case
+    name, B, N, Hq, Hkv, d, di = case
     x = _warm_inputs(*case, seed=N + Hq)
     coef = float(B * N * Hkv)                           # gradients of order one
-    sh = api.Shape(B=B, Nq=N, Nk=N, Hq=Hq, Hkv=Hkv, d=128, d_idx=128, topk=1)
+    sh = api.Shape(B=B, Nq=N, Nk=N, Hq=Hq, Hkv=Hkv, d=d, d_idx=di, topk=1)
     t = {n: to_torch(a) for n, a in x.items()}
     out = api.warmup_kl(sh, t["q"], t["k"], t["v"], t["q_idx"], t["k_idx"], coef)
     again = api.warmup_kl(sh, t["q"], t["k"], t["v"], t["q_idx"], t["k_idx"], coef)
@@ -90,7 +91,7 @@ def test_warmup_kl_and_gradients(case):
     for n in out:
         assert torch.equal(out[n], again[n]), n          # deterministic
     nb = (N + 127) // 128
-    osh = oracle.Shape(B=B, Nq=N, Nk=N, Hq=Hq, Hkv=Hkv, d=128, d_idx=128, topk=nb)
+    osh = oracle.Shape(B=B, Nq=N, Nk=N, Hq=Hq, Hkv=Hkv, d=d, d_idx=di, topk=nb)
     lse_idx_o, kl_o = oracle.warmup_kl(osh, x["q"], x["k"], x["q_idx"], x["k_idx"])
     to_rows = lambda a: a.cpu().numpy().transpose(0, 2, 1).reshape(B * N, Hkv)
     assert_close(to_rows(out["lse_idx"]), lse_idx_o, "warm-up lse_idx", max_abs=1e-3, rel_l2=1e-5)
