@@ -395,7 +395,18 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         const int qd = warp & 3;
         const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
         bf16 *col = dq_part + qd * 32 + lane;
-        const bool feat_ok = qd * 32 + lane < p.d;   // features past d are the zero padding
+        // one row per step: the warp's 32 lanes write 64 contiguous bytes of it;
+        // partial rows are DW = d features apart, features past d are padding
+        auto store_rows = [&](auto dw_tag, const long long *rx, const uint32_t (&v0)[32], const uint32_t (&v1)[32]) {
+            constexpr int DW = decltype(dw_tag)::value;
+            const bool feat_ok = qd * 32 + lane < DW;
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc) {
+                const long long r0 = rx[cc], r1 = rx[32 + cc];
+                if (feat_ok && r0 >= 0) col[r0 * DW] = __float2bfloat16_rn(__uint_as_float(v0[cc]));
+                if (feat_ok && r1 >= 0) col[r1 * DW] = __float2bfloat16_rn(__uint_as_float(v1[cc]));
+            }
+        };
         for (int m = 0; m < nch; ++m) {
             const int pb = m & 1, x = m % kRx;
             if (!wwait(&rx_full[x], (uint32_t)(m / kRx) & 1u, st, 117, abort_flag)) break;
@@ -409,14 +420,9 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&slot_free[pb]);
-            // one row per step: the warp's 32 lanes write 64 contiguous bytes of it
             const long long *rx = ridx_ring + x * kRows;
-#pragma unroll
-            for (int cc = 0; cc < 32; ++cc) {
-                const long long r0 = rx[cc], r1 = rx[32 + cc];
-                if (feat_ok && r0 >= 0) col[r0 * p.d] = __float2bfloat16_rn(__uint_as_float(v0[cc]));
-                if (feat_ok && r1 >= 0) col[r1 * p.d] = __float2bfloat16_rn(__uint_as_float(v1[cc]));
-            }
+            if (p.d == 128) store_rows(std::integral_constant<int, 128>{}, rx, v0, v1);
+            else store_rows(std::integral_constant<int, 64>{}, rx, v0, v1);
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&rx_free[x]);
         }

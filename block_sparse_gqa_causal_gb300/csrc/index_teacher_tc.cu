@@ -562,12 +562,18 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&si_free[m & 1]);
             bf16 *col = dqi_part + qd * 32 + lane;
-            const bool feat_ok = qd * 32 + lane < p.d_idx;     // features past d_idx are padding
+            // partial rows are DW = d_idx features apart; features past d_idx are padding
+            auto store_rows = [&](auto dw_tag) {
+                constexpr int DW = decltype(dw_tag)::value;
+                const bool feat_ok = qd * 32 + lane < DW;
 #pragma unroll
-            for (int cc = 0; cc < kWC; ++cc) {
-                const int rix = __shfl_sync(0xffffffffu, rp_prev, cc);
-                if (feat_ok && rix >= 0) col[(long long)rix * p.d_idx] = __float2bfloat16_rn(__uint_as_float(v[cc]));
-            }
+                for (int cc = 0; cc < kWC; ++cc) {
+                    const int rix = __shfl_sync(0xffffffffu, rp_prev, cc);
+                    if (feat_ok && rix >= 0) col[(long long)rix * DW] = __float2bfloat16_rn(__uint_as_float(v[cc]));
+                }
+            };
+            if (p.d_idx == 128) store_rows(std::integral_constant<int, 128>{});
+            else store_rows(std::integral_constant<int, 64>{});
             return true;
         };
         for (int n = 0; ok && n < nch; ++n) {
