@@ -275,8 +275,12 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
             }
         }
         // a chunk's 64 bucket entries, lane l holding queries l and l + 32 (-1:
-        // padding), loaded two chunks ahead; the next chunk's Q rows are
-        // prefetched into L2 while this chunk's sub-chunks are staged
+        // padding), loaded two chunks ahead.  The next chunk's Q rows are not
+        // prefetched into L2: at G = 8 one TMA-unit prefetch per query cost this
+        // warp as much issue time as the loads themselves and made it late at
+        // every chunk boundary (9.25 -> 8.38 ms without it at 128K); at G = 4 the
+        // per-line prefetches cost 3% of the kernel.  The three stages cover the
+        // loads' latency.
         auto load_ent = [&](int (&e)[2], int n) {
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
@@ -288,25 +292,11 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
             const int x0 = __shfl_sync(0xffffffffu, e[0], qq & 31), x1 = __shfl_sync(0xffffffffu, e[1], qq & 31);
             return qq < 32 ? x0 : x1;
         };
-        auto prefetch_rows = [&](const int (&e)[2]) {
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                if (e[t] < 0) continue;
-                const long long row = (long long)b * p.Nq + entry_row(e[t]);
-                if constexpr (G == 8) {
-                    tc::tma_prefetch_4d(&tmap_q, 0, r * G, 0, (int)row);
-                } else {
-                    const char *base = reinterpret_cast<const char *>(q + (row * p.Hq + (long long)r * G) * p.d);
-                    for (int x = 0; x < G * p.d / 64; ++x) tc::prefetch_l2(base + x * 128);
-                }
-            }
-        };
         int ent[2], ent1[2], ent2[2];
         load_ent(ent, 0);
         load_ent(ent1, 1);
         for (int n = 0; n < nch; ++n) {
             load_ent(ent2, n + 2);
-            prefetch_rows(ent1);
             bool ok = true;
             for (int m = 0; m < NSUB; ++m) {
                 const int u = n * NSUB + m, s = u % QST;
@@ -664,8 +654,8 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
             float lv[5];                               // streaming warp sums of the loss terms
             [[maybe_unused]] uint32_t sg[kWC / 2];
             auto index_terms = [&](auto all_tag) {
-                constexpr bool kAll = decltype(all_tag)::value;
-                float li[kWC];
+                [[maybe_unused]] constexpr bool kAll = decltype(all_tag)::value;
+                [[maybe_unused]] float li[kWC];
                 if constexpr (kGrad) {
 #pragma unroll
                     for (int r4 = 0; r4 < kWC / 4; ++r4) {
@@ -678,7 +668,7 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
                 }
 #pragma unroll
                 for (int k = 0; k < kWC; k += 2) {
-                    float gv[2];
+                    [[maybe_unused]] float gv[2];
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         // explicit roundings: the same bits whether or not the loss terms
