@@ -15,6 +15,12 @@
 // so one unsigned compare ranks by score then by lower index; they are
 // sorted 32 at a time and merged into the running top-(k-1), which is kept
 // sorted across the lanes.
+//
+// Rows of at most 1,024 earlier blocks (every prefill row up to 128K tokens)
+// take a shorter road, warp_topk_regs: the row is held in registers, the
+// (k-1)-th largest score T is found among the few scores that pass the same
+// cutoff, and the chosen blocks are written in index order by ballots, with
+// no 64-bit keys and no running list.
 #include "msa_internal.h"
 
 namespace msa {
@@ -135,6 +141,101 @@ __device__ __forceinline__ void warp_topk(const float *__restrict__ src, int c0,
     }
 }
 
+// One warp's top-(k-1) of a row whose c0 earlier blocks fit in J registers
+// per lane (c0 <= 32 J), written with the local block into out:
+//   1. tau = the (k-1)-th largest of each lane's largest score (of its two
+//      largest for k > 17): a subset of the row, so tau <= T, the row's
+//      (k-1)-th largest score, and at least k-1 scores reach it (the
+//      lanes' second-largest scores alone would give a looser cutoff: about
+//      1.75 (k-1) survivors against 1.5 (k-1), too often over 64);
+//   2. the scores >= tau, at most 64, are collected in block order by
+//      ballots (survivor t of the row goes to lane t % 32, slot t / 32);
+//      T, their (k-1)-th largest, is found by taking out the largest (or,
+//      when T lies nearer the bottom, the smallest) values one at a time,
+//      all copies of a value at once, with warp max / min reductions on
+//      order-preserving keys;
+//   3. every survivor > T is chosen, and of those equal to T the first in
+//      block order, up to k-1 in all (ties to the lower index); a ballot
+//      gives each its output slot, so the list comes out ascending, the
+//      local block last.
+// Returns false with nothing written when more than 64 scores pass the
+// cutoff or the cutoff is not finite (-inf or NaN scores); warp_topk then
+// takes the row.  sbuf: 64 floats and 64 ints of this warp's scratch.
+template <int J>
+__device__ __forceinline__ bool warp_topk_regs(const float *__restrict__ src, int c0, int K1, float *sbuf,
+                                               int32_t *out, int lane)
+{
+    float v[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const int c = j * 32 + lane;
+        v[j] = c < c0 ? __ldg(src + c) : -INFINITY;
+    }
+    float m1 = -INFINITY, m2 = -INFINITY;          // the lane's two largest
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        m2 = fmaxf(m2, fminf(m1, v[j]));
+        m1 = fmaxf(m1, v[j]);
+    }
+    float tau;
+    if (K1 <= 16) {
+        tau = __shfl_sync(0xffffffffu, sort_desc_f(m1, lane), K1 - 1);
+    } else {
+        const float a = sort_desc_f(m1, lane), b = sort_desc_f(m2, lane);
+        tau = __shfl_sync(0xffffffffu, merge_desc_f(fmaxf(a, __shfl_sync(0xffffffffu, b, 31 - lane)), lane), K1 - 1);
+    }
+    if (!(tau > -INFINITY)) return false;
+    int *sidx = reinterpret_cast<int *>(sbuf + 64);
+    const unsigned lt = (1u << lane) - 1u;
+    int m = 0;                                     // survivors so far (warp-uniform)
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        if (j * 32 >= c0) break;
+        const bool sv = v[j] >= tau;
+        const unsigned bal = __ballot_sync(0xffffffffu, sv);
+        const int at = m + __popc(bal & lt);
+        if (sv && at < 64) {
+            sbuf[at] = v[j];
+            sidx[at] = j * 32 + lane;
+        }
+        m += __popc(bal);
+    }
+    if (m > 64) return false;
+    __syncwarp();
+    const float a0 = lane < m ? sbuf[lane] : -INFINITY, b0 = lane + 32 < m ? sbuf[lane + 32] : -INFINITY;
+    const int ia = sidx[lane], ib = sidx[lane + 32];
+    __syncwarp();
+    // survivors a0 (block order 0..31) then b0 (32..63) as keys; padding 0,
+    // below every score's key
+    const uint32_t ka = lane < m ? float_key(a0) : 0u, kb = lane + 32 < m ? float_key(b0) : 0u;
+    const bool top = K1 <= m - K1 + 1;            // T is the K1-th from the top or the (m-K1+1)-th from the bottom
+    int rank = top ? K1 : m - K1 + 1;
+    const uint32_t gone = top ? 0u : 0xFFFFFFFFu;  // taken-out values and padding
+    uint32_t xa = lane < m ? ka : gone, xb = lane + 32 < m ? kb : gone, tk;
+    for (;;) {
+        const uint32_t e = top ? __reduce_max_sync(0xffffffffu, max(xa, xb))
+                               : __reduce_min_sync(0xffffffffu, min(xa, xb));
+        const int copies = __popc(__ballot_sync(0xffffffffu, xa == e)) + __popc(__ballot_sync(0xffffffffu, xb == e));
+        if (rank <= copies) {
+            tk = e;
+            break;
+        }
+        rank -= copies;
+        if (xa == e) xa = gone;
+        if (xb == e) xb = gone;
+    }
+    const unsigned ga = __ballot_sync(0xffffffffu, ka > tk), gb = __ballot_sync(0xffffffffu, kb > tk);
+    const unsigned ea = __ballot_sync(0xffffffffu, ka == tk), eb = __ballot_sync(0xffffffffu, kb == tk);
+    const int need_eq = K1 - __popc(ga) - __popc(gb);          // 1 .. number equal to T
+    const bool sa = ((ga >> lane) & 1u) || (((ea >> lane) & 1u) && __popc(ea & lt) < need_eq);
+    const bool sb = ((gb >> lane) & 1u) || (((eb >> lane) & 1u) && __popc(ea) + __popc(eb & lt) < need_eq);
+    const unsigned ba = __ballot_sync(0xffffffffu, sa), bb = __ballot_sync(0xffffffffu, sb);
+    if (sa) out[__popc(ba & lt)] = ia;
+    if (sb) out[__popc(ba) + __popc(bb & lt)] = ib;
+    if (lane == 0) out[K1] = c0;
+    return true;
+}
+
 // the k-1 chosen blocks plus the local block, ascending, into out
 __device__ __forceinline__ void write_selection(int32_t *out, unsigned long long best, int K1, int c0, int k, int lane)
 {
@@ -165,8 +266,17 @@ block_topk_kernel(Problem p, const float *__restrict__ bs, int32_t *__restrict__
         return;
     }
     const int K1 = k - 1;            // slots the indexer chooses, 0..31
+    const float *src = bs + row * p.nb;
+    if (K1 > 0 && c0 <= 1024) {
+        float *sbuf = reinterpret_cast<float *>(cand_buf[wi]);
+        const bool done = c0 <= 256   ? warp_topk_regs<8>(src, c0, K1, sbuf, out, lane)
+                          : c0 <= 512 ? warp_topk_regs<16>(src, c0, K1, sbuf, out, lane)
+                                      : warp_topk_regs<32>(src, c0, K1, sbuf, out, lane);
+        if (done) return;
+        __syncwarp();
+    }
     unsigned long long best = 0ull;  // lane m: m-th best key so far (0 = empty)
-    warp_topk(bs + row * p.nb, c0, K1, 0, kSeg, cand_buf[wi], best, lane);
+    warp_topk(src, c0, K1, 0, kSeg, cand_buf[wi], best, lane);
     write_selection(out, best, K1, c0, k, lane);
 }
 

@@ -175,9 +175,11 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 // Order-preserving map of a finite fp32 to uint32 (larger float -> larger key).
+// -0 is first turned into +0, so two equal scores always get equal keys and
+// their order falls to the block index.
 MSA_DEV uint32_t float_key(float f)
 {
-    uint32_t u = __float_as_uint(f);
+    uint32_t u = __float_as_uint(__fadd_rn(f, 0.0f));
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 

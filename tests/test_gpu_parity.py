@@ -14,7 +14,7 @@ import numpy as np
 import pytest
 
 import oracle
-from msa_testutil import assert_close, bf16_to_np, check_selection, errors, to_torch
+from msa_testutil import SEL_GAP, assert_close, bf16_to_np, check_selection, errors, to_torch
 
 pytestmark = pytest.mark.gpu
 
@@ -329,10 +329,11 @@ def test_train_step_staged_matches_train_step(case):
 
 @pytest.mark.parametrize("k", [17, 24, 32])
 def test_index_select_large_k_parity(k):
-    """k above 16 takes the selection over stored block scores (`block_topk`:
-    segments of 512 scores, a cutoff from the lane maxima, survivors sorted
-    and merged): the same selection as the oracle's full sort.  Prefill rows
-    and a decode-like row with a long cache, where a CTA takes the row."""
+    """k above 16 takes the selection over stored block scores (`block_topk`):
+    the same selection as the oracle's full sort.  Prefill rows of up to 31
+    earlier blocks (held in registers) and a decode-like row with a long
+    cache (segments of 512 scores, survivors sorted and merged; a CTA takes
+    the row)."""
     import torch
     from block_sparse_gqa_causal_gb300 import api
     from block_sparse_gqa_causal_gb300.inputs import f32_to_bf16_bits
@@ -356,6 +357,53 @@ def test_index_select_large_k_parity(k):
         # statistics of ~30 block scores are ~0.03 apart, so a few percent of
         # rows fall within the 1e-3 gap
         assert tol <= 0.1 * (exact + tol) + 2
+
+
+@pytest.mark.parametrize("k", [17, 24, 32])
+def test_index_select_stored_scores_rows_up_to_1024_blocks(k):
+    """k above 16 over a 131,072-token prefill (1,024 blocks): rows of every
+    length the stored-scores selection holds in registers (up to 256, 512
+    and 1,024 earlier blocks) against the oracle's full sort.  Then K_idx
+    built from five key blocks repeated in turn, so that every earlier block
+    of a row scores one of five exact values: the choice among the many equal
+    scores is decided by the lower block index alone and must match the
+    oracle's exactly wherever the five values are more than 1e-3 apart."""
+    import torch
+    from block_sparse_gqa_causal_gb300 import api
+    from block_sparse_gqa_causal_gb300.inputs import f32_to_bf16_bits
+    rng = np.random.default_rng(100 + k)
+    bf = lambda shape: f32_to_bf16_bits(rng.standard_normal(shape).astype(np.float32))
+    N, Hkv, di = 131072, 1, 64
+    qi = bf((1, N, Hkv, di))
+    rows = np.unique(np.concatenate([rng.choice(N, 90, replace=False), np.arange(0, N, 4099),
+                                     [128 * k - 1, 128 * k, 256 * 128 - 1, 256 * 128, 257 * 128,
+                                      512 * 128 - 1, 512 * 128, 513 * 128, N - 1]]))
+    osh = oracle.Shape(B=1, Nq=N, Nk=N, Hq=Hkv, Hkv=Hkv, d=di, d_idx=di, topk=k)
+    sh = api.Shape(B=1, Nq=N, Nk=N, Hq=Hkv, Hkv=Hkv, d=di, d_idx=di, topk=k)
+    pat = bf((5, 128, di))
+    for form, ki in (("random", bf((1, N, di))),
+                     ("five repeated key blocks", np.ascontiguousarray(pat[np.arange(N // 128) % 5].reshape(1, N, di)))):
+        sel = api.index_select(sh, to_torch(qi), to_torch(ki))
+        torch.cuda.synchronize()
+        bs_o = oracle.block_scores(osh, qi, ki, rows)
+        sel_o = oracle.select(osh, bs_o, rows)
+        sel_np = sel.cpu().numpy()
+        sel_g = np.stack([sel_np[0, :, row, :] for row in rows])
+        if form == "random":
+            exact, tol = check_selection(k, 128, 0, N, rows, sel_g, sel_o, bs_o)
+            assert tol <= 0.1 * (exact + tol) + 2
+            continue
+        decided = 0
+        for t, row in enumerate(rows):
+            c0 = int(row) // 128
+            vals = np.unique(bs_o[t, 0, :c0])
+            if c0 >= 5:
+                assert len(vals) <= 5, (row, vals)
+            if len(vals) > 1 and np.min(np.diff(vals)) <= SEL_GAP:
+                continue
+            assert np.array_equal(sel_g[t, 0], sel_o[t, 0]), (row, sel_g[t, 0].tolist(), sel_o[t, 0].tolist())
+            decided += 1
+        assert decided >= 0.8 * len(rows), (decided, len(rows))
 
 
 @pytest.mark.parametrize("case", TRAIN_CASES, ids=[c[0] for c in TRAIN_CASES])
