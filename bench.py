@@ -667,6 +667,9 @@ def decode_line(args, w, world, rank, dev):
     new_k, new_v, new_ki = k[:, L0:].clone(), v[:, L0:].clone(), ki[:, L0:].clone()
     q_s = [q[:, s:s + 1].contiguous() for s in range(steps)]
     qi_s = [qi[:, s:s + 1].contiguous() for s in range(steps)]
+    k_s = [new_k[:, s:s + 1].contiguous() for s in range(steps)]
+    v_s = [new_v[:, s:s + 1].contiguous() for s in range(steps)]
+    ki_s = [new_ki[:, s:s + 1].contiguous() for s in range(steps)]
     sel = torch.empty((w.B, w.Hkv, 1, w.topk), dtype=torch.int32, device=dev)
     o = torch.empty((w.B, 1, w.Hq, w.d), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.B, w.Hq, 1), dtype=torch.float32, device=dev)
@@ -677,10 +680,8 @@ def decode_line(args, w, world, rank, dev):
     stream = torch.cuda.current_stream(dev)
 
     def step(s):
-        pos = decode_position(w, s)
-        k[:, pos].copy_(new_k[:, s], non_blocking=True)
-        v[:, pos].copy_(new_v[:, s], non_blocking=True)
-        ki[:, pos].copy_(new_ki[:, s], non_blocking=True)
+        # the new token's K, V and K_idx rows join the caches (one library launch)
+        api.kv_append(shapes[s], k_s[s], v_s[s], ki_s[s], k, v, ki)
         api.index_select(shapes[s], qi_s[s], ki, sel_idx=sel, workspace=ws_sel)
         api.sparse_attn_fwd(shapes[s], q_s[s], k, v, sel, o=o, lse=lse, workspace=ws_fwd)
 
@@ -707,25 +708,22 @@ def decode_line(args, w, world, rank, dev):
     # the attention output goes back to pinned host memory
     e2e = None
     if not args.no_e2e:
-        parts = [("q", (w.B, 1, w.Hq, w.d)), ("q_idx", (w.B, 1, w.Hkv, w.d_idx)), ("k", (w.B, w.Hkv, w.d)),
-                 ("v", (w.B, w.Hkv, w.d)), ("k_idx", (w.B, w.d_idx))]
+        parts = [("q", (w.B, 1, w.Hq, w.d)), ("q_idx", (w.B, 1, w.Hkv, w.d_idx)), ("k", (w.B, 1, w.Hkv, w.d)),
+                 ("v", (w.B, 1, w.Hkv, w.d)), ("k_idx", (w.B, 1, w.d_idx))]
         sizes = [int(np.prod(shp)) for _, shp in parts]
         offs = np.concatenate([[0], np.cumsum(sizes)])
         total = int(offs[-1])
         host = torch.empty((steps, total), dtype=torch.bfloat16).pin_memory()
         for s in range(steps):
-            src = [q_s[s], qi_s[s], new_k[:, s], new_v[:, s], new_ki[:, s]]
+            src = [q_s[s], qi_s[s], k_s[s], v_s[s], ki_s[s]]
             host[s].copy_(torch.cat([t.reshape(-1).cpu() for t in src]))
         staging = torch.empty(total, dtype=torch.bfloat16, device=dev)
         view = {n: staging[offs[x]:offs[x + 1]].view(shp) for x, (n, shp) in enumerate(parts)}
         o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
 
         def e2e_step(s):
-            pos = decode_position(w, s)
             staging.copy_(host[s], non_blocking=True)
-            k[:, pos].copy_(view["k"])
-            v[:, pos].copy_(view["v"])
-            ki[:, pos].copy_(view["k_idx"])
+            api.kv_append(shapes[s], view["k"], view["v"], view["k_idx"], k, v, ki)
             api.index_select(shapes[s], view["q_idx"], ki, sel_idx=sel, workspace=ws_sel)
             api.sparse_attn_fwd(shapes[s], view["q"], k, v, sel, o=o, lse=lse, workspace=ws_fwd)
             o_host.copy_(o, non_blocking=True)

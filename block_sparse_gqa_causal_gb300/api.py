@@ -25,7 +25,7 @@ STATUS = {0: "MSA_OK", 1: "MSA_ERR_INVALID_ARGUMENT", 2: "MSA_ERR_UNSUPPORTED", 
           4: "MSA_ERR_CUDA", 5: "MSA_ERR_TIMEOUT", 6: "MSA_ERR_DEVICE"}
 EXPORTS = ("msa_workspace_size", "msa_index_select", "msa_sparse_attn_fwd", "msa_kl_fwd", "msa_fused_bwd",
            "msa_fused_bwd_kl", "msa_train_step", "msa_train_step_staged", "msa_block_mask", "msa_warmup_kl",
-           "msa_index_proj_workspace_size", "msa_index_proj_fwd", "msa_index_proj_bwd",
+           "msa_index_proj_workspace_size", "msa_index_proj_fwd", "msa_index_proj_bwd", "msa_kv_append",
            "msa_last_error", "msa_check_device_status", "msa_version", "msa_launch_count")
 
 
@@ -118,6 +118,7 @@ def lib() -> ctypes.CDLL:
                                                 sz, P]
             L.msa_check_device_status.argtypes = [P, P]
             L.msa_block_mask.argtypes = [S, P, P, P, P, P]
+            L.msa_kv_append.argtypes = [S, P, P, P, P, P, P, P]
             L.msa_warmup_kl.argtypes = [S, P, P, P, P, P, f, P, P, P, P, P, P, P, sz, P]
             PS = ctypes.POINTER(_CProjShape)
             L.msa_index_proj_workspace_size.argtypes = [PS]
@@ -127,7 +128,8 @@ def lib() -> ctypes.CDLL:
             L.msa_selftest_wait_timeout.argtypes = [P, ctypes.c_uint, P]
             for fn in ("msa_index_select", "msa_sparse_attn_fwd", "msa_kl_fwd", "msa_fused_bwd", "msa_fused_bwd_kl",
                        "msa_train_step", "msa_train_step_staged", "msa_check_device_status", "msa_block_mask",
-                       "msa_warmup_kl", "msa_index_proj_fwd", "msa_index_proj_bwd", "msa_selftest_wait_timeout"):
+                       "msa_warmup_kl", "msa_index_proj_fwd", "msa_index_proj_bwd", "msa_selftest_wait_timeout",
+                       "msa_kv_append"):
                 getattr(L, fn).restype = ctypes.c_int
             L.msa_last_error.restype = ctypes.c_char_p
             L.msa_version.restype = ctypes.c_char_p
@@ -329,6 +331,21 @@ def block_mask(shape: Shape, sel_idx, *, counts=False, blocks=False, stream=None
                                 _stream(stream)))
     out = (mask,) + ((cnt,) if counts else ()) + ((blk,) if blocks else ())
     return out[0] if len(out) == 1 else out
+
+
+def kv_append(shape: Shape, k_new, v_new, k_idx_new, k, v, k_idx, *, stream=None) -> None:
+    """msa_kv_append: the Nq new tokens' K, V [B, Nq, Hkv, d] and K_idx
+    [B, Nq, d_idx] rows into the caches k, v [B, kv_rows, Hkv, d] and k_idx
+    [B, kv_rows, d_idx] at rows q_offset .. q_offset+Nq-1 (a pair given as
+    None, None is skipped)."""
+    s = shape
+    for new, cache, row in ((k_new, k, (s.Hkv, s.d)), (v_new, v, (s.Hkv, s.d)), (k_idx_new, k_idx, (s.d_idx,))):
+        if new is not None:
+            _need(new, "new rows", (s.B, s.Nq) + row, torch.bfloat16)
+        if cache is not None:
+            _need(cache, "cache", (s.B, s.rows_kv) + row, torch.bfloat16)
+    _check(lib().msa_kv_append(ctypes.byref(s.c()), _ptr(k_new), _ptr(v_new), _ptr(k_idx_new), _ptr(k), _ptr(v),
+                               _ptr(k_idx), _stream(stream)))
 
 
 def check_device_status(workspace, stream=None) -> None:

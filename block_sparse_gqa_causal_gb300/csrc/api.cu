@@ -439,6 +439,26 @@ msa_status msa_block_mask(const msa_shape *shape, const int32_t *sel_idx, uint32
     return MSA_OK;
 }
 
+msa_status msa_kv_append(const msa_shape *shape, const void *k_new, const void *v_new, const void *k_idx_new,
+                         void *k, void *v, void *k_idx, void *stream)
+{
+    Problem p;
+    msa_status st = make_problem(shape, p);   // q_offset + Nq <= Nk <= kv_rows
+    if (st != MSA_OK) return st;
+    if (!k_new != !k || !v_new != !v || !k_idx_new != !k_idx)
+        return fail(MSA_ERR_INVALID_ARGUMENT, "kv_append: give both or neither of each (new rows, cache) pair");
+    if (!k && !v && !k_idx) return fail(MSA_ERR_INVALID_ARGUMENT, "kv_append: nothing to append");
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_idx_new) || !aligned16(k) || !aligned16(v) ||
+        !aligned16(k_idx))
+        return fail(MSA_ERR_INVALID_ARGUMENT, "kv_append: pointers must be 16-byte aligned");
+    cudaError_t e = launch_kv_append(p, static_cast<const bf16 *>(k_new), static_cast<const bf16 *>(v_new),
+                                     static_cast<const bf16 *>(k_idx_new), static_cast<bf16 *>(k),
+                                     static_cast<bf16 *>(v), static_cast<bf16 *>(k_idx),
+                                     static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
+    return MSA_OK;
+}
+
 msa_status msa_kl_fwd(const msa_shape *shape, const void *q, const void *k, const void *q_idx, const void *k_idx,
                       const int32_t *sel_idx, const float *lse, float kl_coef, float *lse_idx, float *kl_rows,
                       float *kl_loss, void *workspace, size_t workspace_bytes, void *stream)

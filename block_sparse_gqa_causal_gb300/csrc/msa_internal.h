@@ -51,6 +51,9 @@ cudaError_t launch_index_scores(const Problem &p, const bf16 *q_idx, const bf16 
 // Top-k block selection from block scores.  sel: [B, Hkv, Nq, topk].
 cudaError_t launch_block_topk(const Problem &p, const float *bs, int32_t *sel, DeviceStatus *st,
                               cudaStream_t s);
+// kv_append.cu: the new tokens' K, V and K_idx rows into the caches
+cudaError_t launch_kv_append(const Problem &p, const bf16 *k_new, const bf16 *v_new, const bf16 *ki_new, bf16 *k,
+                             bf16 *v, bf16 *ki, cudaStream_t s);
 // Block mask of a selection (uint32 words per 128-query tile, one bit per
 // key block), optionally each tile's active-block count and ascending list.
 size_t block_mask_smem_bytes(const Problem &p);

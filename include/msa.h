@@ -306,6 +306,25 @@ msa_status msa_index_select_noalloc(const msa_shape *shape, const void *q_idx, c
 msa_status msa_block_mask(const msa_shape *shape, const int32_t *sel_idx, uint32_t *mask, int32_t *tile_counts,
                           int32_t *tile_blocks, void *stream);
 
+/* KV-cache append of a decode (or chunked prefill) step.  "Sparse
+ * Attention · Part II", section 3.2: every token carries its own K and V
+ * rows per KV head and one index key k_idx shared by the groups; section 4.1:
+ * in decode the new token's rows join the cache that its own query then
+ * scans.  Writes the Nq new tokens at positions q_offset .. q_offset+Nq-1
+ * of the caches, in one launch:
+ *   k_new, v_new   [B, Nq, Hkv, d] bf16     -> k, v   [B, kv_rows, Hkv, d]
+ *   k_idx_new      [B, Nq, d_idx] bf16      -> k_idx  [B, kv_rows, d_idx]
+ * Shape fields used: B, Nq, Hkv, d, d_idx, q_offset, kv_rows (the other
+ * fields must form a valid shape, as for msa_index_select).  Each pair
+ * (k_new, k), (v_new, v), (k_idx_new, k_idx) is copied when both are
+ * non-NULL and skipped when both are NULL; at least one pair is given.
+ * Caller-owned device memory, 16-byte aligned; sources and destinations
+ * must not overlap.  q_offset + Nq > kv_rows, a half-given pair, or a
+ * misaligned pointer -> MSA_ERR_INVALID_ARGUMENT before any launch.  No
+ * workspace; asynchronous on stream. */
+msa_status msa_kv_append(const msa_shape *shape, const void *k_new, const void *v_new, const void *k_idx_new,
+                         void *k, void *v, void *k_idx, void *stream);
+
 /* Message of the last failed call on this host thread ("" if none). */
 const char *msa_last_error(void);
 

@@ -97,6 +97,27 @@ def test_block_mask_rejects_bad_arguments_before_any_launch(libmsa):
     assert rc == 2 and b"655,328" in libmsa.msa_last_error()
 
 
+def test_kv_append_rejects_bad_arguments_before_any_launch(libmsa):
+    from block_sparse_gqa_causal_gb300 import api
+    sh = api.Shape(B=2, Nq=1, Nk=501, Hq=8, Hkv=2, d=64, d_idx=128, topk=4, q_offset=500, kv_rows=1000)
+    good = ctypes.c_void_p(1 << 20)
+    # a half-given pair
+    rc = libmsa.msa_kv_append(ctypes.byref(sh.c()), good, None, None, None, None, None, None)
+    assert rc == 1 and b"both or neither" in libmsa.msa_last_error()
+    rc = libmsa.msa_kv_append(ctypes.byref(sh.c()), None, None, None, None, None, None, None)
+    assert rc == 1 and b"nothing to append" in libmsa.msa_last_error()
+    bad = ctypes.c_void_p((1 << 20) + 8)
+    rc = libmsa.msa_kv_append(ctypes.byref(sh.c()), good, good, good, good, good, bad, None)
+    assert rc == 1 and b"aligned" in libmsa.msa_last_error()
+    # the new rows must lie inside the cache: q_offset + Nq <= Nk <= kv_rows
+    over = api.Shape(B=2, Nq=2, Nk=501, Hq=8, Hkv=2, d=64, d_idx=128, topk=4, q_offset=500, kv_rows=1000)
+    rc = libmsa.msa_kv_append(ctypes.byref(over.c()), good, good, good, good, good, good, None)
+    assert rc == 1 and b"exceeds Nk" in libmsa.msa_last_error()
+    small = api.Shape(B=2, Nq=1, Nk=501, Hq=8, Hkv=2, d=64, d_idx=128, topk=4, q_offset=500, kv_rows=400)
+    rc = libmsa.msa_kv_append(ctypes.byref(small.c()), good, good, good, good, good, good, None)
+    assert rc == 1 and b"kv_rows" in libmsa.msa_last_error()
+
+
 def test_bwd_rejects_non_training_layout(libmsa):
     from block_sparse_gqa_causal_gb300 import api
     sh = api.Shape(B=1, Nq=3, Nk=256, Hq=8, Hkv=2, d=64, d_idx=64, topk=4, q_offset=253)

@@ -181,3 +181,28 @@ def test_split_selection_ignores_stale_workspace(B, Nq, Nk, q_offset, Hkv, k):
         got = api.index_select(sh, qi, ki, workspace=ws)
         torch.cuda.synchronize()
         assert torch.equal(got, want), fill
+
+
+def test_kv_append_writes_exactly_the_new_rows():
+    """msa_kv_append: the new tokens' K, V and K_idx rows land at cache rows
+    q_offset .. q_offset+Nq-1 of every batch entry, bit for bit; every other
+    row is untouched; a pair given as None is skipped."""
+    import torch
+    from block_sparse_gqa_causal_gb300 import api
+    rng = np.random.default_rng(11)
+    B, cap, Hkv, d, di = 3, 1000, 2, 64, 128
+    mk = lambda shape: torch.from_numpy(rng.standard_normal(shape).astype(np.float32)).to(torch.bfloat16).cuda()
+    for Nq, qo, skip_v in ((1, 999, False), (5, 300, False), (2, 0, True)):
+        k, v, ki = mk((B, cap, Hkv, d)), mk((B, cap, Hkv, d)), mk((B, cap, di))
+        k0, v0, ki0 = k.clone(), v.clone(), ki.clone()
+        kn, vn, kin = mk((B, Nq, Hkv, d)), mk((B, Nq, Hkv, d)), mk((B, Nq, di))
+        sh = api.Shape(B=B, Nq=Nq, Nk=qo + Nq, Hq=4 * Hkv, Hkv=Hkv, d=d, d_idx=di, topk=4, q_offset=qo, kv_rows=cap)
+        api.kv_append(sh, kn, None if skip_v else vn, kin, k, None if skip_v else v, ki)
+        torch.cuda.synchronize()
+        want_k, want_v, want_ki = k0.clone(), v0.clone(), ki0.clone()
+        want_k[:, qo:qo + Nq] = kn
+        if not skip_v:
+            want_v[:, qo:qo + Nq] = vn
+        want_ki[:, qo:qo + Nq] = kin
+        for got, want in ((k, want_k), (v, want_v), (ki, want_ki)):
+            assert torch.equal(got.view(torch.int16), want.view(torch.int16))
