@@ -162,11 +162,24 @@ size_t bwd_bytes(const Problem &p)
 // teacher terms
 size_t bwdkl_bytes(const Problem &p) { return klrows_bytes(p) + klt_bytes(p); }
 
-// one training step: the shared inverse index, scores scratch (unfused
-// selection only), forward partials, the KL index pass's partials, the
-// backward with its KL terms; shapes outside the shared-index path run the
-// four phases one after another in the same workspace, so the largest suffices
+// one training step: the shared inverse index and D (the forward's combine
+// leaves it for the backward) for the whole step, then one region that each
+// phase's own buffers overlay in turn -- the selection's score scratch
+// (unfused selection only), the forward's partial rows, the KL index pass's
+// partials, the backward's dK_idx shares, partial rows and KL terms: each
+// phase's partials are combined before the next phase writes (stream
+// order).  Shapes outside the shared-index path run the four phases one
+// after another in the same workspace, so the largest suffices.
 bool train_shared_index(const Problem &p) { return fwd_keymajor(p) && bwd_tc(p); }
+size_t train_phase_bytes(const Problem &p)
+{
+    const size_t rows = (size_t)p.B * p.Nq * p.Hq * p.topk, slots = (size_t)p.B * p.Nq * p.topk;
+    const size_t fwd = align256(rows * p.d * 2) + align256(rows * 8);
+    const size_t kl = align256(kl_part_count(p) * sizeof(float2));
+    const size_t bwd = align256((size_t)p.B * p.Hkv * p.Nk * p.d_idx * 4) + align256(slots * p.Hq * p.d * 2) +
+                       align256(slots * p.Hkv * p.d_idx * 2) + bwdkl_bytes(p);
+    return std::max(std::max(bs_bytes(p), fwd), std::max(kl, bwd));
+}
 size_t train_bytes(const Problem &p)
 {
     if (!train_shared_index(p)) {
@@ -175,9 +188,7 @@ size_t train_bytes(const Problem &p)
         n = std::max(n, klrows_bytes(p) + kl_bytes(p, true));
         return std::max(n, bwd_bytes(p) + bwdkl_bytes(p));
     }
-    const size_t rows = (size_t)p.B * p.Nq * p.Hq * p.topk;
-    return index_bytes(p) + bs_bytes(p) + align256(rows * p.d * 2) + align256(rows * 8) +
-           align256(kl_part_count(p) * sizeof(float2)) + bwd_bytes(p) - index_bytes(p) + bwdkl_bytes(p);
+    return index_bytes(p) + align256((size_t)p.B * p.Hq * p.Nq * 4) + train_phase_bytes(p);
 }
 
 // The dense indexer warm-up runs the block-sparse kernels on the selection of
@@ -623,15 +634,20 @@ msa_status train_step_impl(const msa_shape *shape, const void *q, const void *k,
     Carve cv{static_cast<char *>(workspace)};
     BwdWork w{};
     carve_index(cv, p, w);
+    w.D = cv.take<float>((size_t)p.B * p.Hq * p.Nq);
+    // the phases' own buffers overlay one region (see train_bytes)
+    const size_t region = cv.off;
     float *bs_scratch = index_select_fused(p) ? nullptr : cv.take<float>(index_select_scratch_floats(p));
+    cv.off = region;
     const size_t rows = (size_t)p.B * p.Nq * p.Hq * p.topk;
     FwdWork fw;
     fw.part = cv.take<bf16>(rows * p.d);
     fw.stats = cv.take<float2>(rows);
+    cv.off = region;
     KlWork kw;
     kw.part = cv.take<float2>(kl_part_count(p));
     kw.klt = nullptr;                                  // lse_idx only: the loss comes from the backward
-    w.D = cv.take<float>((size_t)p.B * p.Hq * p.Nq);
+    cv.off = region;
     w.dki_acc = cv.take<float>((size_t)p.B * p.Hkv * p.Nk * p.d_idx);
     const size_t slots = (size_t)p.B * p.Nq * p.topk;
     w.dq_part = cv.take<bf16>(slots * p.Hq * p.d);

@@ -180,6 +180,29 @@ def test_backward_workspace_holds_no_distribution(libmsa, d, di):
     assert api.workspace_size(sh, api.OP_FUSED_BWD_KL) == want + a(B * Hkv * N * 4) + a(slots * Hkv * 16)
 
 
+def test_training_step_phases_share_one_workspace_region(libmsa):
+    """msa_train_step keeps the inverse index and D for the whole step and
+    overlays the phases' own buffers in one region -- the forward's partial
+    rows, the KL index pass's partials, the backward's dK_idx shares, partial
+    rows and KL terms -- since each phase's partials are combined before the
+    next phase writes: at 128K the region is the larger of the forward's and
+    the backward's buffers, not their sum."""
+    from block_sparse_gqa_causal_gb300 import api
+    B, N, Hq, Hkv, d, di, k = 1, 131072, 64, 8, 128, 128, 16
+    sh = api.Shape(B=B, Nq=N, Nk=N, Hq=Hq, Hkv=Hkv, d=d, d_idx=di, topk=k)
+    a = lambda x: (x + 255) // 256 * 256
+    nb = N // 128
+    nct = (N + 511) // 512
+    index = 2 * a((B * Hkv * nb + 1) * 4) + a(2 * B * Hkv * nct * nb * 4) + a(B * Hkv * N * k * 4)
+    rows, slots = B * N * Hq * k, B * N * k
+    fwd = a(rows * d * 2) + a(rows * 8)
+    bwd = a(B * Hkv * N * di * 4) + a(slots * Hq * d * 2) + a(slots * Hkv * di * 2) + a(B * Hkv * N * 4) \
+        + a(slots * Hkv * 16)
+    want = 256 + index + a(B * Hq * N * 4) + max(fwd, bwd)
+    assert api.workspace_size(sh, api.OP_TRAIN_STEP) == want
+    assert want < 40e9      # the forward's 35.4 GB of partial rows and the backward's 39.5 GB are never live together
+
+
 def test_warmup_and_projection_calls_validate_on_the_host(libmsa):
     """The dense warm-up needs a training sequence of at most 32 blocks; the
     projections need d_idx in {64, 128} and Dm a multiple of 8; bad pointers
