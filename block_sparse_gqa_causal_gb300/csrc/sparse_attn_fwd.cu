@@ -306,8 +306,10 @@ int sparse_attn_splits(const Problem &p)
 {
     const long long ctas = (long long)p.Nq * p.Hkv * p.B;
     if (ctas >= p.num_sms) return 1;
-    // at most 32 shares (the merge holds one per lane) and at most one per 64-token chunk
-    return (int)std::min<long long>(std::min<long long>(32, 2LL * p.topk), (2LL * p.num_sms + ctas - 1) / ctas);
+    // about one CTA per SM (more shares only lengthen the merge: at 1M-token decode the
+    // kernel takes the same time with 5 to 32 shares), at most 32 shares (the merge
+    // holds one per lane) and at most one per 64-token chunk
+    return (int)std::min<long long>(std::min<long long>(32, 2LL * p.topk), ((long long)p.num_sms + ctas - 1) / ctas);
 }
 
 cudaError_t launch_sparse_attn_fwd(const Problem &p, const bf16 *q, const bf16 *k, const bf16 *v,
