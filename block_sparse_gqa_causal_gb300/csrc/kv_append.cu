@@ -2,8 +2,9 @@
 //
 // "Sparse Attention · Part II", section 3.2: each token brings its K and V
 // rows (one per KV head) and one index key k_idx shared by the groups;
-// section 4.1: in decode the new token's rows join the cache its own query
-// then scans.  The Nq new tokens of every batch entry go to cache rows
+// section 4.1 notes that in decoding, reading the KV cache dominates.  A
+// decode step first adds the new token's rows to that cache, since its own
+// query attends to them.  The Nq new tokens of every batch entry go to cache rows
 // q_offset .. q_offset+Nq-1.  All three tensors move in one launch, 16 bytes
 // per thread: a token's K row group (Hkv*d bf16), its V row group and its
 // K_idx row are contiguous in both the source and the cache.

@@ -308,9 +308,10 @@ msa_status msa_block_mask(const msa_shape *shape, const int32_t *sel_idx, uint32
 
 /* KV-cache append of a decode (or chunked prefill) step.  "Sparse
  * Attention · Part II", section 3.2: every token carries its own K and V
- * rows per KV head and one index key k_idx shared by the groups; section 4.1:
- * in decode the new token's rows join the cache that its own query then
- * scans.  Writes the Nq new tokens at positions q_offset .. q_offset+Nq-1
+ * rows per KV head and one index key k_idx shared by the groups; section 4.1
+ * notes that in decoding, reading the KV cache dominates.  A decode step
+ * first adds the new token's rows to that cache, since its own query attends
+ * to them.  Writes the Nq new tokens at positions q_offset .. q_offset+Nq-1
  * of the caches, in one launch:
  *   k_new, v_new   [B, Nq, Hkv, d] bf16     -> k, v   [B, kv_rows, Hkv, d]
  *   k_idx_new      [B, Nq, d_idx] bf16      -> k_idx  [B, kv_rows, d_idx]
