@@ -394,17 +394,26 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         // ------------------------------------------------ dQ^T drain: features 32*qd.. of all 64 rows
         const int qd = warp & 3;
         const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
-        bf16 *col = dq_part + qd * 32 + lane;
-        // one row per step: the warp's 32 lanes write 64 contiguous bytes of it;
-        // partial rows are DW = d features apart, features past d are padding
-        auto store_rows = [&](auto dw_tag, const long long *rx, const uint32_t (&v0)[32], const uint32_t (&v1)[32]) {
+        // lanes 2m, 2m+1 trade values so that each lane holds features (2m, 2m+1)
+        // of one row of a row pair: lane 2m row 2t, lane 2m+1 row 2t+1; one
+        // 4-byte store per lane writes two rows' 64 contiguous bytes each
+        const int fpair = qd * 32 + (lane & ~1);          // this lane's first feature
+        const int odd = lane & 1;
+        auto store_rows = [&](auto dw_tag, const long long *rx, const uint32_t (&v)[32], int r0) {
             constexpr int DW = decltype(dw_tag)::value;
-            const bool feat_ok = qd * 32 + lane < DW;
+            const bool feat_ok = fpair < DW;
 #pragma unroll
-            for (int cc = 0; cc < 32; ++cc) {
-                const long long r0 = rx[cc], r1 = rx[32 + cc];
-                if (feat_ok && r0 >= 0) col[r0 * DW] = __float2bfloat16_rn(__uint_as_float(v0[cc]));
-                if (feat_ok && r1 >= 0) col[r1 * DW] = __float2bfloat16_rn(__uint_as_float(v1[cc]));
+            for (int t = 0; t < 16; ++t) {
+                // rows r0 + 2t (even lanes) and r0 + 2t + 1 (odd lanes)
+                // even lane: keeps row 2t of its feature, gives row 2t+1; odd lane: keeps
+                // row 2t+1, gives row 2t
+                const float ev = __uint_as_float(v[2 * t]), od = __uint_as_float(v[2 * t + 1]);
+                const float mine = odd ? od : ev, give = odd ? ev : od;
+                const float other = __shfl_xor_sync(0xffffffffu, give, 1);
+                const float lo = odd ? other : mine, hi = odd ? mine : other;
+                const long long row = rx[r0 + 2 * t + odd];
+                if (feat_ok && row >= 0)
+                    *reinterpret_cast<uint32_t *>(dq_part + row * DW + fpair) = pack_bf16(lo, hi);
             }
         };
         for (int m = 0; m < nch; ++m) {
@@ -421,8 +430,13 @@ bwd_main_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&slot_free[pb]);
             const long long *rx = ridx_ring + x * kRows;
-            if (p.d == 128) store_rows(std::integral_constant<int, 128>{}, rx, v0, v1);
-            else store_rows(std::integral_constant<int, 64>{}, rx, v0, v1);
+            if (p.d == 128) {
+                store_rows(std::integral_constant<int, 128>{}, rx, v0, 0);
+                store_rows(std::integral_constant<int, 128>{}, rx, v1, 32);
+            } else {
+                store_rows(std::integral_constant<int, 64>{}, rx, v0, 0);
+                store_rows(std::integral_constant<int, 64>{}, rx, v1, 32);
+            }
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&rx_free[x]);
         }
