@@ -551,15 +551,23 @@ index_teacher_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&si_free[m & 1]);
-            bf16 *col = dqi_part + qd * 32 + lane;
-            // partial rows are DW = d_idx features apart; features past d_idx are padding
+            // partial rows are DW = d_idx features apart; features past d_idx are
+            // padding.  Lanes 2m, 2m+1 trade values so that each lane holds
+            // features (2m, 2m+1) of one column of a column pair (lane 2m column
+            // 2t, lane 2m+1 column 2t+1): one 4-byte store per lane
+            const int fpair = qd * 32 + (lane & ~1), odd = lane & 1;
             auto store_rows = [&](auto dw_tag) {
                 constexpr int DW = decltype(dw_tag)::value;
-                const bool feat_ok = qd * 32 + lane < DW;
+                const bool feat_ok = fpair < DW;
 #pragma unroll
-                for (int cc = 0; cc < kWC; ++cc) {
-                    const int rix = __shfl_sync(0xffffffffu, rp_prev, cc);
-                    if (feat_ok && rix >= 0) col[(long long)rix * DW] = __float2bfloat16_rn(__uint_as_float(v[cc]));
+                for (int t = 0; t < kWC / 2; ++t) {
+                    const float ev = __uint_as_float(v[2 * t]), od = __uint_as_float(v[2 * t + 1]);
+                    const float mine = odd ? od : ev, give = odd ? ev : od;
+                    const float other = __shfl_xor_sync(0xffffffffu, give, 1);
+                    const int rix = __shfl_sync(0xffffffffu, rp_prev, 2 * t + odd);
+                    if (feat_ok && rix >= 0)
+                        *reinterpret_cast<uint32_t *>(dqi_part + (long long)rix * DW + fpair) =
+                            pack_bf16(odd ? other : mine, odd ? mine : other);
                 }
             };
             if (p.d_idx == 128) store_rows(std::integral_constant<int, 128>{});
