@@ -257,6 +257,7 @@ kl_index_tc_kernel(const __grid_constant__ CUtensorMap tmap_ki, Problem p, const
 
 // Folds a (query, group) row's partials over its valid slots in a fixed
 // order: lse_idx = (M + log2 Z) ln 2.
+template <int MAXK>   // an upper bound of topk: the row's partials stay in registers
 __global__ void kl_combine_kernel(Problem p, const int32_t *__restrict__ sel, const float2 *__restrict__ part,
                                   float *__restrict__ lse_idx)
 {
@@ -265,19 +266,30 @@ __global__ void kl_combine_kernel(Problem p, const int32_t *__restrict__ sel, co
     const int i = (int)(row % p.Nq);
     const long long pos = (long long)p.q_offset + i;
     const int32_t *srow = sel + row * p.topk;
+    // the row's partials, both key halves of a slot in one 16-byte load, read once
+    static_assert(kParts == 2, "one float4 per slot");
+    const float4 *prow = reinterpret_cast<const float4 *>(part + row * p.topk * kParts);
+    float4 v[MAXK];
+    bool ok[MAXK];
     float M = -INFINITY;
-    for (int t = 0; t < p.topk; ++t) {
-        const int cc = srow[t];
-        if (cc < 0 || cc >= p.nb || (long long)cc * 128 > pos) continue;
-        for (int w = 0; w < kParts; ++w) M = fmaxf(M, part[(row * p.topk + t) * kParts + w].x);
+#pragma unroll
+    for (int t = 0; t < MAXK; ++t) {
+        ok[t] = false;
+        if (t < p.topk) {
+            const int cc = srow[t];
+            ok[t] = cc >= 0 && cc < p.nb && (long long)cc * 128 <= pos;
+            if (ok[t]) {
+                v[t] = __ldg(prow + t);
+                M = fmaxf(fmaxf(M, v[t].x), v[t].z);
+            }
+        }
     }
     float Z = 0.f;
-    for (int t = 0; t < p.topk; ++t) {
-        const int cc = srow[t];
-        if (cc < 0 || cc >= p.nb || (long long)cc * 128 > pos) continue;
-        for (int w = 0; w < kParts; ++w) {
-            const float2 v = part[(row * p.topk + t) * kParts + w];
-            if (v.y > 0.f) Z += v.y * exp2f(v.x - M);
+#pragma unroll
+    for (int t = 0; t < MAXK; ++t) {
+        if (ok[t]) {
+            if (v[t].y > 0.f) Z += v[t].y * exp2f(v[t].x - M);
+            if (v[t].w > 0.f) Z += v[t].w * exp2f(v[t].z - M);
         }
     }
     lse_idx[row] = (M + log2f(Z)) * kLn2;
@@ -321,7 +333,8 @@ cudaError_t launch_kl_keymajor(const Problem &p, const bf16 *q, const bf16 *k, c
     const long long rows = (long long)p.B * p.Hkv * p.Nq;
     {
         TimedLaunch timed_("kl_combine_kernel", s);
-        kl_combine_kernel<<<(unsigned)((rows + 255) / 256), 256, 0, s>>>(p, sel, w.part, lse_idx);
+        if (p.topk <= 16) kl_combine_kernel<16><<<(unsigned)((rows + 255) / 256), 256, 0, s>>>(p, sel, w.part, lse_idx);
+        else kl_combine_kernel<32><<<(unsigned)((rows + 255) / 256), 256, 0, s>>>(p, sel, w.part, lse_idx);
     }
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess || !kl_rows) return e;
