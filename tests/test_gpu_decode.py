@@ -206,3 +206,43 @@ def test_kv_append_writes_exactly_the_new_rows():
         want_ki[:, qo:qo + Nq] = kin
         for got, want in ((k, want_k), (v, want_v), (ki, want_ki)):
             assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+
+
+def test_decode_steps_through_the_cache_append():
+    """A decode loop as a caller runs it, at a head layout no other decode case
+    uses (G = 4, d = d_idx = 64, batch 2): each step appends the new token's K,
+    V and K_idx rows to caches that end at the previous token
+    (msa_kv_append), selects and attends for its query, and is checked against
+    the oracle on caches holding every token so far -- steps that stay inside
+    a block and one that opens a new block."""
+    import torch
+    from block_sparse_gqa_causal_gb300 import api
+    from block_sparse_gqa_causal_gb300.inputs import f32_to_bf16_bits
+    rng = np.random.default_rng(23)
+    bf = lambda shape: f32_to_bf16_bits(rng.standard_normal(shape).astype(np.float32))
+    B, Hq, Hkv, d, di, k, cap = 2, 8, 2, 64, 64, 8, 8192
+    pos0 = 6013                                       # steps at 6013 .. 6017 cross into block 47 at 6016
+    kx, vx, kix = bf((B, cap, Hkv, d)), bf((B, cap, Hkv, d)), bf((B, cap, di))
+    kc, vc, kic = to_torch(kx.copy()), to_torch(vx.copy()), to_torch(kix.copy())
+    kc[:, pos0:].zero_()
+    vc[:, pos0:].zero_()
+    kic[:, pos0:].zero_()
+    for s in range(5):
+        pos = pos0 + s
+        q, qi = bf((B, 1, Hq, d)), bf((B, 1, Hkv, di))
+        sh = api.Shape(B=B, Nq=1, Nk=pos + 1, Hq=Hq, Hkv=Hkv, d=d, d_idx=di, topk=k, q_offset=pos, kv_rows=cap)
+        api.kv_append(sh, to_torch(np.ascontiguousarray(kx[:, pos:pos + 1])), to_torch(np.ascontiguousarray(vx[:, pos:pos + 1])),
+                      to_torch(np.ascontiguousarray(kix[:, pos:pos + 1])), kc, vc, kic)
+        sel = api.index_select(sh, to_torch(qi), kic)
+        o, lse = api.sparse_attn_fwd(sh, to_torch(q), kc, vc, sel)
+        torch.cuda.synchronize()
+        osh = oracle.Shape(B=B, Nq=1, Nk=pos + 1, Hq=Hq, Hkv=Hkv, d=d, d_idx=di, topk=k, q_offset=pos, kv_rows=cap)
+        rows = np.arange(B)
+        bs_o = oracle.block_scores(osh, qi, kix, rows)
+        sel_o = oracle.select(osh, bs_o, rows)
+        sel_g = sel.cpu().numpy()[:, :, 0, :]
+        check_selection(k, 128, pos, 1, rows, sel_g, sel_o, bs_o)
+        assert np.all(sel_g[:, :, -1] == pos // 128), "the local block is last and always selected"
+        o_ref, lse_ref = oracle.sparse_fwd(osh, q, kx, vx, sel_g, rows)
+        assert_close(bf16_to_np(o).reshape(o_ref.shape), o_ref, f"o (step {s})", bf16_out=True)
+        assert_close(lse.cpu().numpy().reshape(lse_ref.shape), lse_ref, f"lse (step {s})", max_abs=1e-3, rel_l2=1e-5)
